@@ -1,0 +1,116 @@
+/*
+ * txl.h -- C ABI of libtxl: Transformer-XL segment-level relative multi-head
+ * attention and the per-layer memory rollover on one GB300 GPU (sm_103a).
+ *
+ * Every pointer argument named "device" is a CUDA device pointer owned by the
+ * caller; the library never frees caller memory and keeps no pointer to it
+ * after the call returns.  Calls are asynchronous on the given stream (a
+ * cudaStream_t passed as void*, NULL = the legacy default stream): the library
+ * never synchronises the device inside a compute call.  Argument errors are
+ * detected on the host before any launch and nothing is launched then.
+ *
+ * Notation (Transformer-XL, Section 3.2 and Appendix B): B batch, H heads,
+ * D head dimension, L segment length, M memory length, T = M + L the extended
+ * context [memory (M rows, oldest first); current segment (L rows)].
+ * Row-major layouts, D innermost:
+ *     q, out : [L][B][H][D]      k, v : [T][B][H][D]
+ *     r      : [T][H][D]  -- row t holds W_kR R_{T-1-t} (the reversed table Q
+ *                            of Appendix B); shared by every sequence
+ *     u_bias, v_bias : [H][D] float32 (the global biases u and v of
+ *                            Section 3.3, one vector per head)
+ */
+#ifndef TXL_H_
+#define TXL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TXL_OK = 0,
+    TXL_ERR_INVALID = 1,     /* bad argument: NULL, negative size, misaligned, overlap */
+    TXL_ERR_UNSUPPORTED = 2, /* valid but not built: d_head > 128, unknown dtype */
+    TXL_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (also: no GPU) */
+    TXL_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up (see txl_check) */
+} txl_status;
+
+typedef enum {
+    TXL_F32 = 0,             /* float32 in, float32 accumulate, float32 out */
+    TXL_BF16 = 1             /* bfloat16 in, float32 accumulate, bfloat16 out */
+} txl_dtype;
+
+/*
+ * txl_rel_attn_fwd -- one layer of relative attention (Transformer-XL,
+ * Section 3.3, the computing procedure; Appendix B, the linear-cost route).
+ *
+ * For every b < batch, h < heads and query position i < seg_len:
+ *     s_ij = ((q_i + u).k_j + (q_i + v).r[T-1-(M+i-j)]) / sqrt(d_head)
+ *                                          for key j = 0 .. M+i (causal)
+ *     out_i = sum_j softmax_j(s_ij) v_j
+ * where j indexes the extended context [memory; segment] and M+i-j is the
+ * relative distance of the pair.
+ *
+ * q, k, v, r, out : device, dtype elements, layouts above; base addresses
+ *                   16-byte aligned; out must not overlap any input.
+ * u_bias, v_bias  : device, float32 [heads][d_head], 4-byte aligned.
+ * batch, heads, seg_len >= 0 (0 => nothing to do, TXL_OK, pointers unused);
+ * mem_len >= 0; 1 <= d_head <= 128.
+ * stream          : cudaStream_t as void*.
+ * Returns TXL_OK once the work is enqueued.  TXL_ERR_INVALID /
+ * TXL_ERR_UNSUPPORTED before any launch; TXL_ERR_CUDA if a launch fails.
+ * Long memories (few query tiles, many keys) split the keys across CTAs; the
+ * partial results then live in a library-owned device scratch buffer that is
+ * allocated on first need, grown when needed and released by txl_shutdown().
+ * Calls that need the scratch must not run concurrently on different streams.
+ */
+txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
+                            const float *u_bias, const float *v_bias,
+                            int batch, int mem_len, int seg_len, int heads, int d_head,
+                            txl_dtype dtype, void *out, void *stream);
+
+/*
+ * txl_mem_update -- the per-layer memory rollover (Transformer-XL,
+ * Section 3.2: a cache of the last M hidden states, possibly spanning several
+ * segments, reused as extended context by the next segment).
+ *
+ * ext_ctx  : device, [M+L][batch][d_model] = [memory; current hidden states].
+ * mem_next : device, at least [M][batch][d_model]; rows 0..M-1 receive the
+ *            newest M rows of ext_ctx (rows L..M+L-1), oldest first -- i.e.
+ *            the memory part of the next segment's extended context.  Must not
+ *            overlap ext_ctx (use two buffers and swap them per segment).
+ * Bit-exact copy of dtype elements.  mem_len == 0 or batch == 0 or
+ * d_model == 0 => nothing to do.  Same error behaviour as above.
+ */
+txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int mem_len,
+                          int seg_len, int d_model, txl_dtype dtype, void *stream);
+
+/*
+ * txl_check -- synchronise `stream`, then report and clear the library's
+ * device error word: TXL_ERR_TIMEOUT if an in-kernel bounded wait gave up
+ * since the last check, TXL_ERR_CUDA if the stream reports an error, else
+ * TXL_OK.
+ */
+txl_status txl_check(void *stream);
+
+/* Static description of a status code; never NULL. */
+const char *txl_status_string(txl_status s);
+
+/* Number of the most recent CUDA error seen by the library on this thread
+ * (0 if none); pairs with TXL_ERR_CUDA. */
+int txl_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int txl_version(void);
+
+/* Free the library-owned scratch of the current device.  Safe to call more
+ * than once; later calls re-allocate on demand. */
+void txl_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TXL_H_ */

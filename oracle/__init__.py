@@ -1,0 +1,153 @@
+"""Plain CPU reference (the oracle) for Transformer-XL relative attention.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only code that may import this package.
+The product library (``transformer_xl_relative_rel_gb300``) never imports it,
+and this package imports nothing from the product.
+
+Contents
+  * ``txl_oracle.c`` -- the float64 triple loop over (i, j, d) with direct
+    ``r_{i-j}`` indexing (Transformer-XL, Section 3.3 procedure and Appendix B
+    table order), built here with gcc into ``liboracle.so``.
+  * ``mem_update`` -- the memory rollover of Section 3.2 written as its plain
+    definition in numpy: the new memory is the newest M rows of
+    [old memory; current hidden states].
+
+All functions take numpy arrays in the T-major layouts of the library:
+``q, out: [L, B, H, D]``, ``k, v: [T, B, H, D]`` with ``T = M + L``,
+``r: [T, H, D]`` (row t is ``W_kR R_{T-1-t}``), ``u, w: [H, D]``.
+Any float dtype is accepted and converted exactly to float64.
+
+Status: parity pinned (tests/test_oracle_pins.py); no function here is
+unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "txl_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib: Optional[ctypes.CDLL] = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``txl_oracle.c`` into ``liboracle.so`` (gcc, OpenMP, -O2).
+
+    Plain portable C: no architecture flags, so the same source builds on the
+    x86 development host and on the Arm GPU host.
+    """
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.txl_oracle_rel_attn.argtypes = [
+            _dp, _dp, _dp, _dp, _dp, _dp,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            _dp, _dp, ctypes.c_int]
+        lib.txl_oracle_rel_attn.restype = None
+        lib.txl_oracle_rel_attn_rows.argtypes = [
+            _dp, _dp, _dp, _dp, _dp, _dp,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.POINTER(ctypes.c_int64), ctypes.c_long, _dp, ctypes.c_int]
+        lib.txl_oracle_rel_attn_rows.restype = None
+        lib.txl_oracle_max_threads.argtypes = []
+        lib.txl_oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    """Threads the OpenMP runtime would give the oracle on this host."""
+    return int(_load().txl_oracle_max_threads())
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _shapes(q, k, v, r, u, w, mem_len):
+    L, B, H, D = q.shape
+    T = mem_len + L
+    if k.shape != (T, B, H, D) or v.shape != (T, B, H, D):
+        raise ValueError(f"k/v must be [{T},{B},{H},{D}], got {k.shape}, {v.shape}")
+    if r.shape != (T, H, D):
+        raise ValueError(f"r must be [{T},{H},{D}], got {r.shape}")
+    if u.shape != (H, D) or w.shape != (H, D):
+        raise ValueError(f"u/v biases must be [{H},{D}]")
+    return B, H, D, L, T
+
+
+def rel_attn(q, k, v, r, u, w, mem_len: int, return_prob: bool = False,
+             nthreads: int = 0):
+    """Relative attention of one layer over [memory; segment], float64.
+
+    Returns ``out`` of shape [L, B, H, D] and, when ``return_prob``, the
+    attention weights ``P`` of shape [B, H, L, M+L] (exact zeros where masked).
+    """
+    q, k, v, r, u, w = (_f64(x) for x in (q, k, v, r, u, w))
+    B, H, D, L, T = _shapes(q, k, v, r, u, w, mem_len)
+    out = np.zeros((L, B, H, D), dtype=np.float64)
+    prob = np.zeros((B, H, L, T), dtype=np.float64) if return_prob else None
+    _load().txl_oracle_rel_attn(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u), _ptr(w),
+        B, H, D, L, mem_len, _ptr(out),
+        _ptr(prob) if prob is not None else ctypes.cast(None, _dp), int(nthreads))
+    return (out, prob) if return_prob else out
+
+
+def rel_attn_rows(q, k, v, r, u, w, mem_len: int, rows, nthreads: int = 0):
+    """The same computation for selected query rows only.
+
+    ``rows`` is an int array of shape [n, 3] holding (b, h, i) triples; the
+    result is [n, D] float64.
+    """
+    q, k, v, r, u, w = (_f64(x) for x in (q, k, v, r, u, w))
+    B, H, D, L, T = _shapes(q, k, v, r, u, w, mem_len)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    if rows.size and ((rows < 0).any() or (rows[:, 0] >= B).any()
+                      or (rows[:, 1] >= H).any() or (rows[:, 2] >= L).any()):
+        raise ValueError("row index out of range")
+    out = np.zeros((rows.shape[0], D), dtype=np.float64)
+    _load().txl_oracle_rel_attn_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u), _ptr(w),
+        B, H, D, L, mem_len,
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.shape[0],
+        _ptr(out), int(nthreads))
+    return out
+
+
+def mem_update(ext_ctx, mem_len: int) -> np.ndarray:
+    """New memory after one segment (Section 3.2: a cache of length M).
+
+    ``ext_ctx`` is the layer's extended context [M+L, ...] = [old memory;
+    current hidden states].  The new memory is its newest ``mem_len`` rows,
+    oldest first.  Works on any dtype, bit for bit.
+    """
+    ext = np.asarray(ext_ctx)
+    if mem_len == 0:
+        return ext[:0].copy()
+    return ext[ext.shape[0] - mem_len:].copy()

@@ -1,0 +1,381 @@
+"""Pins for the oracle: checks against what the method and the mathematics fix.
+
+Nothing here re-types the oracle's loop.  Each pin reaches the same numbers by
+another route the pages give, or by a special case that reduces to a library
+routine or to a closed form:
+
+* the four-term expansion of Transformer-XL Section 3.3 from hidden states and
+  weights, with the naive per-pair projection W_kR R_{i-j};
+* the Appendix B route: B~ = q Q^T followed by a per-row left shift, and the
+  same shift read as a flat array with row pitch T-1;
+* an absolute-position route (sinusoids at absolute positions combined by the
+  angle-difference identities), which pins the sign of i-j and the table order;
+* the segment-recurrence identity (Section 3.2): the memory path equals the
+  last L rows of the same attention over the whole concatenated context;
+* reductions to torch's scaled-dot-product attention and to a plain softmax.
+
+A final test plants mistakes in copies of the oracle's C source and checks that
+these pins catch every one of them.
+"""
+import os
+import shutil
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_xl_relative_rel_gb300 import inputs
+
+TOL = 1e-12
+
+
+def _rand(shape, g):
+    return g.standard_normal(shape)
+
+
+def _problem(B, H, D, L, M, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    T = M + L
+    return dict(q=_rand((L, B, H, D), g), k=_rand((T, B, H, D), g), v=_rand((T, B, H, D), g),
+                r=_rand((T, H, D), g), u=_rand((H, D), g), w=_rand((H, D), g)), g
+
+
+def _softmax_rows(s):
+    s = s - s.max(axis=-1, keepdims=True)
+    e = np.exp(s)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _attend(scores, mask, v):
+    """scores, mask: [L, T]; v: [T, D] -> [L, D] (masked entries excluded)."""
+    s = np.where(mask, scores, -np.inf)
+    return _softmax_rows(s) @ v
+
+
+def _visible(L, M):
+    i = np.arange(L)[:, None]
+    j = np.arange(M + L)[None, :]
+    return j <= M + i
+
+
+# ---------------------------------------------------------------------------
+# 1. Four-term expansion from hidden states (Section 3.3), naive per-pair route
+# ---------------------------------------------------------------------------
+def _four_term_bruteforce(h_ext, Wq, Wk, Wv, Wr, R, u, w, B, H, D, L, M):
+    """Scores from the four named terms with W_kR R_{i-j} projected per pair.
+
+    h_ext: [T, B, d_model] extended context [memory; segment]; R: [T, d_model]
+    relative encodings indexed by the distance i-j (row p = distance p).
+    """
+    T = M + L
+    out = np.zeros((L, B, H, D))
+    for b in range(B):
+        for hd in range(H):
+            sl = slice(hd * D, (hd + 1) * D)
+            for i in range(L):
+                xi = h_ext[M + i, b]                    # the query token's state
+                qi = xi @ Wq[:, sl]
+                scores = np.full(T, -np.inf)
+                for j in range(T):
+                    if j > M + i:
+                        continue                        # future position
+                    kj = h_ext[j, b] @ Wk[:, sl]        # W_kE E_xj
+                    rij = R[M + i - j] @ Wr[:, sl]      # W_kR R_{i-j}, per pair
+                    a = qi @ kj                         # (a) content addressing
+                    bb = qi @ rij                       # (b) content-dependent position bias
+                    c = u[hd] @ kj                      # (c) global content bias
+                    d = w[hd] @ rij                     # (d) global position bias
+                    scores[j] = (a + bb + c + d) / np.sqrt(D)
+                p = _softmax_rows(scores[None, :])[0]
+                vals = h_ext[:, b] @ Wv[:, sl]
+                out[i, b, hd] = p @ vals
+    return out
+
+
+@pytest.mark.parametrize("B,H,D,L,M", [(2, 2, 4, 5, 3), (1, 3, 2, 4, 0), (1, 1, 3, 1, 6),
+                                       (2, 1, 5, 6, 6)])
+def test_four_term_bruteforce(oracle_lib, B, H, D, L, M):
+    g = np.random.Generator(np.random.PCG64(100 + L + M))
+    T, dm = M + L, H * D
+    h_ext = _rand((T, B, dm), g)
+    Wq, Wk, Wv, Wr = (_rand((dm, dm), g) * 0.5 for _ in range(4))
+    R = _rand((T, dm), g)            # any table works; rows indexed by distance
+    u, w = _rand((H, D), g), _rand((H, D), g)
+    ref = _four_term_bruteforce(h_ext, Wq, Wk, Wv, Wr, R, u, w, B, H, D, L, M)
+
+    # the library's inputs: projected q, k, v and the reversed table of Appendix B
+    q = (h_ext[M:] @ Wq).reshape(L, B, H, D)
+    k = (h_ext @ Wk).reshape(T, B, H, D)
+    v = (h_ext @ Wv).reshape(T, B, H, D)
+    Q = np.stack([R[T - 1 - t] @ Wr for t in range(T)]).reshape(T, H, D)   # Q_t = W_kR R_{T-1-t}
+    got = oracle.rel_attn(q, k, v, Q, u, w, mem_len=M)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=TOL * max(1.0, np.abs(ref).max()))
+
+
+# ---------------------------------------------------------------------------
+# 2. Appendix B: B~ = (q+v) Q^T, then row i left-shifted by L-1-i
+# ---------------------------------------------------------------------------
+def _appendix_b(q, k, v, r, u, w, M, strided):
+    L, B, H, D = q.shape
+    T = M + L
+    out = np.zeros_like(q)
+    vis = _visible(L, M)
+    for b in range(B):
+        for hd in range(H):
+            qu = q[:, b, hd] + u[hd]
+            qv = q[:, b, hd] + w[hd]
+            ac = qu @ k[:, b, hd].T                      # terms (a)+(c), [L, T]
+            bt = qv @ r[:, hd].T                         # B~ = qv Q^T, [L, T]
+            if strided:
+                # the left shift as a read of the flat B~ with row pitch T-1
+                flat = bt.reshape(-1)
+                bd = np.zeros((L, T))
+                for i in range(L):
+                    for j in range(M + i + 1):
+                        bd[i, j] = flat[(L - 1) + i * (T - 1) + j]
+            else:
+                bd = np.zeros((L, T))
+                for i in range(L):
+                    s = L - 1 - i                        # row i shifts left by L-1-i
+                    bd[i, : T - s] = bt[i, s:]
+            out[:, b, hd] = _attend((ac + bd) / np.sqrt(D), vis, v[:, b, hd])
+    return out
+
+
+@pytest.mark.parametrize("strided", [False, True])
+@pytest.mark.parametrize("B,H,D,L,M", [(2, 2, 8, 7, 5), (1, 2, 3, 9, 0), (1, 1, 4, 3, 11)])
+def test_appendix_b_left_shift(oracle_lib, strided, B, H, D, L, M):
+    p, _ = _problem(B, H, D, L, M, seed=7 + L)
+    ref = _appendix_b(**p, M=M, strided=strided)
+    got = oracle.rel_attn(**p, mem_len=M)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=TOL * 10)
+
+
+def test_left_shift_equals_strided_read():
+    """The two readings of the shift agree entry by entry on the visible part."""
+    g = np.random.Generator(np.random.PCG64(3))
+    L, M = 6, 4
+    T = L + M
+    bt = g.standard_normal((L, T))
+    flat = bt.reshape(-1)
+    for i in range(L):
+        for j in range(M + i + 1):
+            assert bt[i, j + L - 1 - i] == flat[(L - 1) + i * (T - 1) + j]
+
+
+# ---------------------------------------------------------------------------
+# 3. Masked softmax: rows sum to one, future keys get exactly zero weight
+# ---------------------------------------------------------------------------
+def test_softmax_rows_and_mask(oracle_lib):
+    p, _ = _problem(2, 3, 8, 10, 6, seed=11)
+    out, prob = oracle.rel_attn(**p, mem_len=6, return_prob=True)
+    L, T = 10, 16
+    vis = _visible(L, 6)
+    np.testing.assert_allclose(prob.sum(-1), 1.0, rtol=0, atol=TOL)
+    assert (prob[..., ~vis] == 0.0).all()                    # exact zeros when masked
+    assert (prob[:, :, vis] > 0).all()
+    # out is the probability-weighted sum of the values
+    v = p["v"]
+    recon = np.einsum("bhlt,tbhd->lbhd", prob, v)
+    np.testing.assert_allclose(out, recon, rtol=0, atol=TOL)
+
+
+# ---------------------------------------------------------------------------
+# 4. Only the distance matters: an absolute-position route
+# ---------------------------------------------------------------------------
+def _abs_route(q, k, v, u, w, Wr, M, c, dm):
+    """BD from sinusoids at absolute positions pos_q = c+M+i, pos_k = c+j,
+    combined with sin(a-b) = sin a cos b - cos a sin b and
+    cos(a-b) = cos a cos b + sin a sin b."""
+    L, B, H, D = q.shape
+    T = M + L
+    freq = np.power(10000.0, -np.arange(0, dm, 2) / dm)
+    out = np.zeros_like(q)
+    vis = _visible(L, M)
+    for b in range(B):
+        for hd in range(H):
+            sl = slice(hd * D, (hd + 1) * D)
+            sc = np.zeros((L, T))
+            for i in range(L):
+                a = (c + M + i) * freq
+                for j in range(T):
+                    bb = (c + j) * freq
+                    enc = np.zeros(dm)
+                    enc[0::2] = np.sin(a) * np.cos(bb) - np.cos(a) * np.sin(bb)
+                    enc[1::2] = np.cos(a) * np.cos(bb) + np.sin(a) * np.sin(bb)
+                    rr = enc @ Wr[:, sl]
+                    sc[i, j] = ((q[i, b, hd] + u[hd]) @ k[j, b, hd]
+                                + (q[i, b, hd] + w[hd]) @ rr)
+            out[:, b, hd] = _attend(sc / np.sqrt(D), vis, v[:, b, hd])
+    return out
+
+
+@pytest.mark.parametrize("c", [0, 7, 1000])
+def test_shift_invariance_absolute_positions(oracle_lib, c):
+    B, H, D, L, M = 1, 2, 4, 5, 4
+    T, dm = M + L, H * D
+    p, g = _problem(B, H, D, L, M, seed=21)
+    Wr = g.standard_normal((dm, dm)) * 0.5
+    # the relative table in float64: row t holds W_kR R_{T-1-t}
+    r = (inputs.sinusoid(T, dm) @ Wr)[::-1].reshape(T, H, D)
+    got = oracle.rel_attn(p["q"], p["k"], p["v"], r, p["u"], p["w"], mem_len=M)
+    ref = _abs_route(p["q"], p["k"], p["v"], p["u"], p["w"], Wr, M, c, dm)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# 5. Segment recurrence: memory path == last L rows over the whole context
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L,M", [(4, 6), (8, 8), (5, 1)])
+def test_recurrence_equivalence(oracle_lib, L, M):
+    B, H, D = 2, 2, 6
+    p, g = _problem(B, H, D, L, M, seed=31 + M)
+    T = M + L
+    q_mem = g.standard_normal((M, B, H, D))
+    q_full = np.concatenate([q_mem, p["q"]], 0)       # queries for all T positions
+    full = oracle.rel_attn(q_full, p["k"], p["v"], p["r"], p["u"], p["w"], mem_len=0)
+    mem_path = oracle.rel_attn(**p, mem_len=M)
+    assert full.shape[0] == T
+    np.testing.assert_allclose(mem_path, full[M:], rtol=0, atol=TOL)
+
+
+# ---------------------------------------------------------------------------
+# 6. Special cases: library softmax attention, constant position term, L = 1
+# ---------------------------------------------------------------------------
+def _sdpa(qq, k, v, L, M):
+    """torch scaled-dot-product attention, float64, explicit boolean mask."""
+    qt = torch.from_numpy(np.ascontiguousarray(qq.transpose(1, 2, 0, 3)))      # B,H,L,D
+    kt = torch.from_numpy(np.ascontiguousarray(k.transpose(1, 2, 0, 3)))       # B,H,T,D
+    vt = torch.from_numpy(np.ascontiguousarray(v.transpose(1, 2, 0, 3)))
+    mask = torch.from_numpy(_visible(L, M))
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask)
+    return o.numpy().transpose(2, 0, 1, 3)
+
+
+def test_no_position_term_is_textbook_attention(oracle_lib):
+    B, H, D, L, M = 2, 3, 8, 9, 7
+    p, _ = _problem(B, H, D, L, M, seed=41)
+    p["r"][:] = 0.0
+    p["u"][:] = 0.0
+    p["w"][:] = 0.0
+    got = oracle.rel_attn(**p, mem_len=M)
+    np.testing.assert_allclose(got, _sdpa(p["q"], p["k"], p["v"], L, M), rtol=0, atol=TOL)
+
+
+def test_constant_position_term_cancels(oracle_lib):
+    B, H, D, L, M = 1, 2, 8, 6, 5
+    p, g = _problem(B, H, D, L, M, seed=43)
+    p["r"][:] = g.standard_normal((1, H, D))        # every distance encodes the same
+    got = oracle.rel_attn(**p, mem_len=M)
+    ref = _sdpa(p["q"] + p["u"][None, None], p["k"], p["v"], L, M)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=TOL)
+
+
+def test_single_query_sees_all_keys(oracle_lib):
+    B, H, D, L, M = 2, 2, 5, 1, 9
+    p, _ = _problem(B, H, D, L, M, seed=47)
+    got = oracle.rel_attn(**p, mem_len=M)
+    T = M + L
+    for b in range(B):
+        for hd in range(H):
+            s = np.array([((p["q"][0, b, hd] + p["u"][hd]) @ p["k"][j, b, hd]
+                           + (p["q"][0, b, hd] + p["w"][hd]) @ p["r"][T - 1 - (M - j), hd])
+                          for j in range(T)]) / np.sqrt(D)
+            ref = _softmax_rows(s[None])[0] @ p["v"][:, b, hd]
+            np.testing.assert_allclose(got[0, b, hd], ref, rtol=0, atol=TOL)
+
+
+def test_rows_variant_matches_full(oracle_lib):
+    B, H, D, L, M = 3, 2, 6, 7, 5
+    p, _ = _problem(B, H, D, L, M, seed=53)
+    full = oracle.rel_attn(**p, mem_len=M)
+    rows = np.array([[0, 0, 0], [2, 1, 6], [1, 0, 3], [2, 1, 0]])
+    got = oracle.rel_attn_rows(**p, mem_len=M, rows=rows)
+    for x, (b, h, i) in enumerate(rows):
+        assert np.array_equal(got[x], full[i, b, h])
+
+
+# ---------------------------------------------------------------------------
+# 7. Memory rollover (Section 3.2): newest M rows of [memory; segment]
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L,M", [(4, 4), (6, 2), (2, 7), (5, 0)])
+def test_mem_update_closed_forms(L, M):
+    g = np.random.Generator(np.random.PCG64(61))
+    mem = g.standard_normal((M, 3, 4)).astype(np.float32)
+    h = g.standard_normal((L, 3, 4)).astype(np.float32)
+    new = oracle.mem_update(np.concatenate([mem, h], 0), M)
+    assert new.shape == (M, 3, 4)
+    if M <= L:
+        assert np.array_equal(new, h[L - M:])             # only current states survive
+    else:
+        assert np.array_equal(new[: M - L], mem[L:])      # the newest old memory first
+        assert np.array_equal(new[M - L:], h)
+    # two rollovers: memory spans the last two segments when M = 2L
+    if M == 2 * L and M > 0:
+        h2 = g.standard_normal((L, 3, 4)).astype(np.float32)
+        new2 = oracle.mem_update(np.concatenate([new, h2], 0), M)
+        assert np.array_equal(new2, np.concatenate([h, h2], 0))
+
+
+# ---------------------------------------------------------------------------
+# 8. The pins catch planted mistakes (mutants of the oracle's C source)
+# ---------------------------------------------------------------------------
+MUTANTS = {
+    "table_not_reversed": ("(T - 1 - off) * H", "(off) * H"),
+    # a reversed distance that still stays inside the table
+    "distance_reversed": ("const long off = M + i - j;", "const long off = j - i + L - 1;"),
+    "self_masked": ("const long last = M + i;", "const long last = M + i - 1;"),
+    "dropped_u_term": ("(qi[d] + uh[d]) * kj[d]", "(qi[d]) * kj[d]"),
+    "dropped_d_term": ("(qi[d] + wh[d]) * rr[d]", "(qi[d]) * rr[d]"),
+    "no_scale": ("s[j] = a * scale;", "s[j] = a;"),
+    "key_index_transposed": ("k + ((j * B + b) * H + h) * D", "k + ((b * B + j) * H + h) * D"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "txl_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert old in src, f"mutation anchor for {name} no longer in the oracle source"
+    mdir = tmp_path / name
+    mdir.mkdir()
+    shutil.copy(os.path.join(os.path.dirname(oracle.__file__), "__init__.py"), mdir / "__init__.py")
+    (mdir / "txl_oracle.c").write_text(src.replace(old, new))
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(f"oracle_mutant_{name}", mdir / "__init__.py")
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build(force=True)          # a mutant that does not compile is a test error
+    return mod
+
+
+def _pins_pass(mod):
+    """Run a compact set of the pins above against an oracle module."""
+    B, H, D, L, M = 1, 2, 4, 5, 3
+    g = np.random.Generator(np.random.PCG64(5))
+    T, dm = M + L, H * D
+    h_ext = _rand((T, B, dm), g)
+    Wq, Wk, Wv, Wr = (_rand((dm, dm), g) * 0.5 for _ in range(4))
+    R = _rand((T, dm), g)
+    u, w = _rand((H, D), g), _rand((H, D), g)
+    ref = _four_term_bruteforce(h_ext, Wq, Wk, Wv, Wr, R, u, w, B, H, D, L, M)
+    q = (h_ext[M:] @ Wq).reshape(L, B, H, D)
+    k = (h_ext @ Wk).reshape(T, B, H, D)
+    v = (h_ext @ Wv).reshape(T, B, H, D)
+    Q = np.stack([R[T - 1 - t] @ Wr for t in range(T)]).reshape(T, H, D)
+    if not np.allclose(mod.rel_attn(q, k, v, Q, u, w, mem_len=M), ref, rtol=0, atol=1e-10):
+        return False
+    p, _ = _problem(2, 2, 4, 5, 3, seed=9)
+    if not np.allclose(mod.rel_attn(**p, mem_len=3),
+                       _appendix_b(**p, M=3, strided=False), rtol=0, atol=1e-10):
+        return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc missing")
+    assert _pins_pass(oracle), "pins must pass on the real oracle"
+    mod = _build_mutant(tmp_path, name)
+    assert not _pins_pass(mod), f"planted mistake {name!r} went unnoticed"

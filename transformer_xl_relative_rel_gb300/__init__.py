@@ -1,0 +1,12 @@
+"""GB300-native Transformer-XL segment-level relative attention.
+
+The compute lives in ``libtxl.so`` (hand-written sm_103a CUDA behind the C-ABI
+declared in ``include/txl.h``); ``abi`` is the thin ctypes binding with the same
+entry-point names.  Importing this package does not load the library; the first
+call does, and raises ``TxlError`` if it was not built.
+"""
+from .abi import (TxlError, TXL_F32, TXL_BF16, rel_attn_fwd, mem_update,  # noqa: F401
+                  check, load_library, library_path, status_string)
+
+__all__ = ["TxlError", "TXL_F32", "TXL_BF16", "rel_attn_fwd", "mem_update", "check",
+           "load_library", "library_path", "status_string"]

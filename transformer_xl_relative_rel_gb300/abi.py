@@ -1,0 +1,172 @@
+"""ctypes binding of libtxl (the C ABI in include/txl.h).
+
+Argument marshalling only: the functions take torch tensors that already live
+on the GPU, check their shapes, dtypes and layouts, and pass raw device
+pointers and sizes to the library.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU path.  If ``libtxl.so`` is missing the
+first call raises ``TxlError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+TXL_F32 = 0
+TXL_BF16 = 1
+
+_STATUS = {0: "TXL_OK", 1: "TXL_ERR_INVALID", 2: "TXL_ERR_UNSUPPORTED", 3: "TXL_ERR_CUDA",
+           4: "TXL_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libtxl.so"
+_lib: Optional[ctypes.CDLL] = None
+
+#: every symbol include/txl.h declares (checked by the host-side tests)
+EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
+           "txl_last_cuda_error", "txl_version", "txl_shutdown")
+
+
+class TxlError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libtxl.so from the package directory (built by ``_build.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise TxlError(3, f"{path} not built (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.txl_rel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.txl_rel_attn_fwd.restype = i
+    lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.txl_mem_update.restype = i
+    lib.txl_check.argtypes = [vp]
+    lib.txl_check.restype = i
+    lib.txl_status_string.argtypes = [i]
+    lib.txl_status_string.restype = ctypes.c_char_p
+    lib.txl_last_cuda_error.argtypes = []
+    lib.txl_last_cuda_error.restype = i
+    lib.txl_version.argtypes = []
+    lib.txl_version.restype = i
+    lib.txl_shutdown.argtypes = []
+    lib.txl_shutdown.restype = None
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().txl_status_string(int(status)).decode()
+
+
+def _raise(st: int, what: str):
+    if st != 0:
+        lib = load_library()
+        msg = f"{what} ({lib.txl_status_string(st).decode()}"
+        if st == 3:
+            msg += f", cuda error {lib.txl_last_cuda_error()}"
+        raise TxlError(st, msg + ")")
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return TXL_F32
+    if t.dtype == torch.bfloat16:
+        return TXL_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t) -> Optional[int]:
+    return t.data_ptr() if t is not None and t.numel() > 0 else None
+
+
+def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None):
+    """Relative attention of one layer (Transformer-XL Section 3.3).
+
+    q: [L, B, H, D]; k, v: [M+L, B, H, D]; r: [M+L, H, D] (reversed table);
+    u_bias, v_bias: [H, D] float32; all CUDA, contiguous, same dtype
+    (float32 or bfloat16) except the biases.  Returns ``out`` [L, B, H, D].
+    """
+    import torch
+    L, B, H, D = q.shape
+    T = mem_len + L
+    code = _dtype_code(q)
+    for name, t, shp in (("k", k, (T, B, H, D)), ("v", v, (T, B, H, D)), ("r", r, (T, H, D))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be {list(shp)}, got {list(t.shape)}")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} dtype {t.dtype} != q dtype {q.dtype}")
+    for name, t in (("u_bias", u_bias), ("v_bias", v_bias)):
+        if tuple(t.shape) != (H, D) or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32 [{H}, {D}]")
+    for t in (q, k, v, r, u_bias, v_bias):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != (L, B, H, D) or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    st = load_library().txl_rel_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+        B, mem_len, L, H, D, code, _ptr(out), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd")
+    return out
+
+
+def rel_attn_fwd_raw(q_ptr, k_ptr, v_ptr, r_ptr, u_ptr, w_ptr, batch, mem_len, seg_len,
+                     heads, d_head, dtype_code, out_ptr, stream_ptr) -> int:
+    """The C entry point with raw integers (for host-side argument tests)."""
+    return load_library().txl_rel_attn_fwd(q_ptr, k_ptr, v_ptr, r_ptr, u_ptr, w_ptr, batch,
+                                           mem_len, seg_len, heads, d_head, dtype_code,
+                                           out_ptr, stream_ptr)
+
+
+def mem_update(mem_next, ext_ctx, mem_len: int, stream=None):
+    """Memory rollover (Section 3.2): mem_next[:M] = newest M rows of ext_ctx.
+
+    ext_ctx: [M+L, B, d_model]; mem_next: [>= M, B, d_model]; same dtype.
+    """
+    T, B, dm = ext_ctx.shape
+    L = T - mem_len
+    if L < 0:
+        raise ValueError("mem_len larger than the extended context")
+    if mem_next.dim() != 3 or mem_next.shape[0] < mem_len or tuple(mem_next.shape[1:]) != (B, dm):
+        raise ValueError(f"mem_next must be [>= {mem_len}, {B}, {dm}]")
+    if mem_next.dtype != ext_ctx.dtype:
+        raise TypeError("mem_next and ext_ctx dtypes differ")
+    for t in (mem_next, ext_ctx):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    st = load_library().txl_mem_update(_ptr(mem_next), _ptr(ext_ctx), B, mem_len, L, dm,
+                                       _dtype_code(ext_ctx), _stream_ptr(stream))
+    _raise(st, "txl_mem_update")
+    return mem_next
+
+
+def mem_update_raw(dst_ptr, src_ptr, batch, mem_len, seg_len, d_model, dtype_code,
+                   stream_ptr) -> int:
+    return load_library().txl_mem_update(dst_ptr, src_ptr, batch, mem_len, seg_len, d_model,
+                                         dtype_code, stream_ptr)
+
+
+def check(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel reported an error."""
+    _raise(load_library().txl_check(_stream_ptr(stream)), "txl_check")
