@@ -32,7 +32,7 @@ extern "C" {
 typedef enum {
     TXL_OK = 0,
     TXL_ERR_INVALID = 1,     /* bad argument: NULL, negative size, misaligned, overlap */
-    TXL_ERR_UNSUPPORTED = 2, /* valid but not built: d_head > 128, unknown dtype */
+    TXL_ERR_UNSUPPORTED = 2, /* valid but not built: d_head too large, unknown dtype */
     TXL_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (also: no GPU) */
     TXL_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up (see txl_check) */
 } txl_status;
@@ -57,7 +57,8 @@ typedef enum {
  *                   16-byte aligned; out must not overlap any input.
  * u_bias, v_bias  : device, float32 [heads][d_head], 4-byte aligned.
  * batch, heads, seg_len >= 0 (0 => nothing to do, TXL_OK, pointers unused);
- * mem_len >= 0; 1 <= d_head <= 128.
+ * mem_len >= 0; 1 <= d_head <= 128 for TXL_F32, 1 <= d_head <= 64 for
+ * TXL_BF16 (larger: TXL_ERR_UNSUPPORTED).
  * stream          : cudaStream_t as void*.
  * Returns TXL_OK once the work is enqueued.  TXL_ERR_INVALID /
  * TXL_ERR_UNSUPPORTED before any launch; TXL_ERR_CUDA if a launch fails.

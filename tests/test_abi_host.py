@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol include/txl.h declares, and rejects bad arguments before launching
+anything.  No compute call is made here (these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_xl_relative_rel_gb300 as txl
+from transformer_xl_relative_rel_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, CUDA, TIMEOUT = 0, 1, 2, 3, 4
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from transformer_xl_relative_rel_gb300 import _build
+    _build.build()
+    return abi.load_library()
+
+
+def test_header_declares_exactly_the_exports(lib):
+    hdr = open(os.path.join(ROOT, "include", "txl.h")).read()
+    declared = set(re.findall(r"\b(txl_[a-z_0-9]+)\s*\(", hdr))
+    assert declared == set(abi.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in (OK, INVALID, UNSUPPORTED, CUDA, TIMEOUT):
+        assert txl.status_string(st)
+    assert txl.status_string(99) == "unknown status"
+    assert lib.txl_version() >= 100
+
+
+def _attn(**kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, r=FAKE * 4, u=FAKE * 5, w=FAKE * 6, B=2, M=8, L=8, H=2,
+             D=16, dt=1, out=FAKE * 7, stream=None)
+    a.update(kw)
+    return abi.rel_attn_fwd_raw(a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["B"], a["M"],
+                                a["L"], a["H"], a["D"], a["dt"], a["out"], a["stream"])
+
+
+def test_attn_rejects_bad_arguments(lib):
+    assert _attn(dt=7) == UNSUPPORTED
+    assert _attn(B=-1) == INVALID
+    assert _attn(M=-1) == INVALID
+    assert _attn(L=-3) == INVALID
+    assert _attn(D=0) == INVALID
+    assert _attn(D=129, dt=0) == UNSUPPORTED
+    assert _attn(D=65, dt=1) == UNSUPPORTED
+    assert _attn(q=None) == INVALID
+    assert _attn(u=None) == INVALID
+    assert _attn(out=None) == INVALID
+    assert _attn(q=FAKE + 2) == INVALID            # misaligned
+    assert _attn(u=FAKE + 2) == INVALID
+    assert _attn(out=FAKE) == INVALID              # out overlaps q
+    assert _attn(out=FAKE * 2 + 64) == INVALID     # out overlaps k
+
+
+def test_attn_empty_is_a_no_op(lib):
+    # nothing to compute: OK without touching any pointer (NULLs allowed)
+    assert _attn(B=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None) == OK
+    assert _attn(L=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None) == OK
+    assert _attn(H=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None) == OK
+
+
+def test_mem_update_rejects_bad_arguments(lib):
+    f = abi.mem_update_raw
+    assert f(FAKE, FAKE * 4, 2, 4, 4, 8, 9, None) == UNSUPPORTED
+    assert f(FAKE, FAKE * 4, -1, 4, 4, 8, 1, None) == INVALID
+    assert f(None, FAKE * 4, 2, 4, 4, 8, 1, None) == INVALID
+    assert f(FAKE + 1, FAKE * 4, 2, 4, 4, 8, 1, None) == INVALID     # misaligned
+    assert f(FAKE * 4 + 16, FAKE * 4, 2, 4, 4, 8, 1, None) == INVALID  # overlapping buffers
+    assert f(None, None, 2, 0, 4, 8, 1, None) == OK                   # M = 0: nothing to copy
+    assert f(None, None, 0, 4, 4, 8, 1, None) == OK
+
+
+def test_no_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.txl_check(None) == CUDA
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(abi, "_lib", None)
+    monkeypatch.setattr(abi, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(txl.TxlError):
+        abi.load_library()

@@ -1,0 +1,112 @@
+"""Parity of the CUDA relative attention against the oracle (float64).
+
+Element by element on small seeded problems that span several tiles and a
+ragged tail; on sampled rows at the full workload sizes, in the same launch
+configuration the benchmark uses.  Tolerances: max |err| <= 1e-4 on the fp32
+path, <= 2e-2 on the bf16 path with unit-variance inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests.helpers import (TOL_BF16, TOL_F32, device_layer, gather_rows, oracle_full,
+                           oracle_rows, run_library, unit_shape)
+from transformer_xl_relative_rel_gb300 import inputs
+from transformer_xl_relative_rel_gb300.workloads import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from transformer_xl_relative_rel_gb300 import _build, abi
+    _build.build()
+    abi.load_library()
+
+
+def _check_full(B, H, D, L, M, dtype, seed, tol):
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), seed)
+    dev, host = device_layer(p, dtype)
+    out = run_library(dev, M)
+    torch.cuda.synchronize()
+    ref = oracle_full(host, M)
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref).max()
+    assert np.isfinite(got).all()
+    assert err <= tol, f"max abs err {err:.3e} > {tol} for B{B} H{H} D{D} L{L} M{M} {dtype}"
+    return err
+
+
+# ------------------------------------------------------------------ fp32 path
+@pytest.mark.parametrize("B,H,D,L,M", [
+    (1, 2, 16, 16, 16),        # the tiny workload
+    (2, 3, 24, 70, 45),        # several query blocks and key tiles, ragged tails
+    (1, 2, 41, 37, 0),         # no memory
+    (1, 1, 8, 1, 50),          # a single query sees all memory
+    (1, 1, 128, 40, 30),       # widest head
+    (1, 1, 1, 5, 3),           # d_head = 1
+    (3, 1, 64, 33, 97),
+])
+def test_f32_parity(B, H, D, L, M):
+    _check_full(B, H, D, L, M, torch.float32, seed=1000 + L + M, tol=TOL_F32)
+
+
+def test_f32_tiny_workload_exact_inputs():
+    w = WORKLOADS["tiny_f32"]
+    s = w.shape
+    p = inputs.unit_layer(s, w.seed)
+    dev, host = device_layer(p, torch.float32)
+    out = run_library(dev, s.mem_len)
+    ref = oracle_full(host, s.mem_len)
+    assert np.abs(out.double().cpu().numpy() - ref).max() <= TOL_F32
+
+
+# ------------------------------------------------------------------ bf16 path
+@pytest.mark.parametrize("B,H,D,L,M", [
+    (1, 2, 64, 16, 16),
+    (2, 2, 64, 200, 150),      # two query tiles (ragged), several key tiles
+    (1, 3, 64, 300, 0),        # no memory: pure causal
+    (1, 1, 64, 1, 300),        # one query over long memory
+    (2, 2, 41, 150, 150),      # d_head 41: padded to 48, loaded without TMA
+    (1, 2, 48, 130, 70),
+    (1, 2, 40, 129, 127),      # d_head % 16 == 8: zero padding slice with TMA
+    (1, 2, 32, 257, 31),
+    (1, 2, 16, 64, 64),
+    (1, 1, 24, 100, 20),
+    (1, 2, 64, 128, 1600),     # long memory: keys split across CTAs + combine
+    (2, 1, 41, 128, 900),      # split path without TMA
+])
+def test_bf16_parity(B, H, D, L, M):
+    _check_full(B, H, D, L, M, torch.bfloat16, seed=2000 + L + M + D, tol=TOL_BF16)
+
+
+def test_bf16_repeatable():
+    """Same inputs, same bits: no races between the CTA's roles."""
+    p = inputs.unit_layer(unit_shape(2, 2, 64, 200, 150), 7)
+    dev, _ = device_layer(p, torch.bfloat16)
+    a = run_library(dev, 150).clone()
+    for _ in range(3):
+        b = run_library(dev, 150)
+        assert torch.equal(a, b)
+
+
+# -------------------------------------------- full workload sizes, sampled rows
+FULL = ["base_lm", "large_lm", "long_mem_b1", "long_mem_b16", "char_train", "char_eval"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_bf16_full_size_unit_variance(name):
+    w = WORKLOADS[name]
+    s = w.shape
+    p = inputs.unit_layer(s, w.seed)
+    dev, host = device_layer(p, torch.bfloat16)
+    out = run_library(dev, s.mem_len)
+    torch.cuda.synchronize()
+    rows = inputs.sample_rows(s, w.seed, n_random=256, all_heads_of_b0=(s.heads * s.seg_len <= 4096))
+    ref = oracle_rows(host, s.mem_len, rows)
+    got = gather_rows(out, rows)
+    err = np.abs(got - ref).max()
+    assert err <= TOL_BF16, f"{name}: max abs err {err:.3e}"
+    assert torch.isfinite(out.float()).all()

@@ -1,0 +1,205 @@
+// api.cu -- the C ABI of include/txl.h: argument checks, dispatch, scratch.
+//
+// Every argument error is found here, on the host, before anything is
+// launched.  There is no CPU path: without a GPU the calls report
+// TXL_ERR_CUDA.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "txl.h"
+
+namespace txl {
+
+static thread_local int g_last_cuda_error = 0;
+
+static txl_status cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    cudaGetLastError();   // clear the sticky-free error state of this thread
+    return TXL_ERR_CUDA;
+}
+
+int device_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Library-owned scratch for split-key partial results, one buffer per device.
+namespace {
+struct Scratch {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_scratch_mu;
+Scratch g_scratch[64];
+
+txl_status get_scratch(size_t bytes, cudaStream_t stream, void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return TXL_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    Scratch &s = g_scratch[dev];
+    if (s.bytes < bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return cuda_fail(e);
+        // growing the buffer allocates; a call made once outside capture first
+        // sizes it, after which captured calls reuse it.
+        if (cs != cudaStreamCaptureStatusNone) return TXL_ERR_UNSUPPORTED;
+        if (s.ptr) {
+            e = cudaDeviceSynchronize();   // earlier launches may still read it
+            if (e != cudaSuccess) return cuda_fail(e);
+            cudaFree(s.ptr);
+            s.ptr = nullptr;
+            s.bytes = 0;
+        }
+        size_t want = bytes + bytes / 4;
+        e = cudaMalloc(&s.ptr, want);
+        if (e != cudaSuccess) {
+            s.ptr = nullptr;
+            return cuda_fail(e);
+        }
+        s.bytes = want;
+    }
+    *out = s.ptr;
+    return TXL_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+bool aligned(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
+
+}  // namespace
+}  // namespace txl
+
+using namespace txl;
+
+extern "C" {
+
+txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
+                            const float *u_bias, const float *v_bias,
+                            int batch, int mem_len, int seg_len, int heads, int d_head,
+                            txl_dtype dtype, void *out, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
+    if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
+    if (d_head > 128) return TXL_ERR_UNSUPPORTED;
+    if (dtype == TXL_BF16 && d_head > 64) return TXL_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !r || !u_bias || !v_bias || !out) return TXL_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(r, 16) ||
+        !aligned(out, 16) || !aligned(u_bias, 4) || !aligned(v_bias, 4))
+        return TXL_ERR_INVALID;
+    // sizes: every index is 64-bit in the kernels; keep byte counts in range
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    const size_t T = (size_t)mem_len + (size_t)seg_len;
+    if (T > (size_t)INT32_MAX) return TXL_ERR_UNSUPPORTED;
+    const size_t row = (size_t)batch * (size_t)heads * (size_t)d_head;
+    const size_t nq = (size_t)seg_len * row * esz, nk = T * row * esz;
+    const size_t nr = T * (size_t)heads * (size_t)d_head * esz;
+    const size_t nb = (size_t)heads * (size_t)d_head * 4;
+    if ((size_t)batch * (size_t)heads > (size_t)INT32_MAX || nk / esz / T != row)
+        return TXL_ERR_UNSUPPORTED;
+    if (overlaps(out, nq, q, nq) || overlaps(out, nq, k, nk) || overlaps(out, nq, v, nk) ||
+        overlaps(out, nq, r, nr) || overlaps(out, nq, u_bias, nb) || overlaps(out, nq, v_bias, nb))
+        return TXL_ERR_INVALID;
+    if ((seg_len + 31) / 32 > 65535) return TXL_ERR_UNSUPPORTED;
+
+    AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len};
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    if (dtype == TXL_F32) {
+        e = launch_attn_f32(a, s);
+    } else {
+        const int splits = bf16_num_splits(a, device_sm_count());
+        void *scratch = nullptr;
+        if (splits > 1) {
+            txl_status st = get_scratch(bf16_scratch_bytes(a, splits), s, &scratch);
+            if (st != TXL_OK) return st;
+        }
+        e = launch_attn_bf16(a, splits, scratch, s);
+    }
+    return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+}
+
+txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int mem_len,
+                          int seg_len, int d_model, txl_dtype dtype, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (batch < 0 || mem_len < 0 || seg_len < 0 || d_model < 0) return TXL_ERR_INVALID;
+    if (batch == 0 || mem_len == 0 || d_model == 0) return TXL_OK;
+    if (!mem_next || !ext_ctx) return TXL_ERR_INVALID;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (!aligned(mem_next, esz) || !aligned(ext_ctx, esz)) return TXL_ERR_INVALID;
+    const size_t row = (size_t)batch * (size_t)d_model * esz;
+    const size_t T = (size_t)mem_len + (size_t)seg_len;
+    if (row / esz / (size_t)batch != (size_t)d_model) return TXL_ERR_UNSUPPORTED;
+    const size_t nbytes = (size_t)mem_len * row;
+    if (overlaps(mem_next, nbytes, ext_ctx, T * row)) return TXL_ERR_INVALID;
+    const void *src = (const unsigned char *)ext_ctx + (size_t)seg_len * row;
+    cudaError_t e = launch_rollover(mem_next, src, nbytes, (int)esz, (cudaStream_t)stream);
+    return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+}
+
+txl_status txl_check(void *stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int word = 0;
+    e = read_and_clear_device_error(&word, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word ? TXL_ERR_TIMEOUT : TXL_OK;
+}
+
+const char *txl_status_string(txl_status st)
+{
+    switch (st) {
+    case TXL_OK: return "ok";
+    case TXL_ERR_INVALID: return "invalid argument";
+    case TXL_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TXL_ERR_CUDA: return "CUDA error";
+    case TXL_ERR_TIMEOUT: return "in-kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+int txl_last_cuda_error(void) { return g_last_cuda_error; }
+
+int txl_version(void) { return 100; }
+
+void txl_shutdown(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    Scratch &s = g_scratch[dev];
+    if (s.ptr) {
+        cudaDeviceSynchronize();
+        cudaFree(s.ptr);
+    }
+    s.ptr = nullptr;
+    s.bytes = 0;
+}
+
+}  // extern "C"

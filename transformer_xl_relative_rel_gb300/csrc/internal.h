@@ -1,0 +1,35 @@
+// internal.h -- launchers shared between the library's translation units.
+// Not part of the public ABI (that is include/txl.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace txl {
+
+struct AttnArgs {
+    const void *q, *k, *v, *r;
+    const float *u, *w;           // u and v biases, [H][D] float32
+    void *out;
+    int B, H, D, L, M;
+};
+
+// fp32 SIMT path (attn_f32.cu)
+cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s);
+
+// bf16 tcgen05 path (attn_bf16.cu).  `scratch` is device memory of at least
+// bf16_scratch_bytes(a, splits) bytes (ignored when splits == 1).
+int bf16_num_splits(const AttnArgs &a, int num_sms);
+size_t bf16_scratch_bytes(const AttnArgs &a, int splits);
+cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaStream_t s);
+// reads and clears the device error word written by bounded waits (syncs on s)
+cudaError_t read_and_clear_device_error(unsigned int *word, cudaStream_t s);
+
+// memory rollover (rollover.cu): bit copy of `bytes` bytes
+cudaError_t launch_rollover(void *dst, const void *src, size_t bytes, int elem_size,
+                            cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace txl
