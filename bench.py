@@ -1,0 +1,495 @@
+"""Benchmark: Transformer-XL relative attention + memory rollover on GB300.
+
+One step = one pass of the hot path over one batch of the workload: every
+segment of the workload's chain, and in each segment every layer's relative
+attention call (txl_rel_attn_fwd) followed by its memory rollover
+(txl_mem_update).  Inputs are seeded and synthetic, resident in HBM before the
+timed region; the per-step working set is far larger than L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the float64 CPU oracle
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+(weak scaling: independent sequences, no data-path collective); timing is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from transformer_xl_relative_rel_gb300 import inputs  # noqa: E402
+from transformer_xl_relative_rel_gb300.workloads import DEFAULT_BENCH, WORKLOADS, Workload  # noqa: E402
+
+METRIC = "rel-attn query-tokens/s and TFLOP/s (% of BF16 tensor peak), 1 GB300"
+UNIT = "query-tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rel_attn_bf16_char_train.md")
+KERNEL_SRC = os.path.join(ROOT, "transformer_xl_relative_rel_gb300", "csrc", "attn_bf16.cu")
+
+
+# --------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_rate(units_per_rank: float, local_seconds: float, world: int) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    t = max_over_ranks(local_seconds, world)
+    return units_per_rank * world / t
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source and this workload."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]{16})", text)
+    m_wl = re.search(r"workload:\s*(\S+)", text)
+    m_b = re.search(r"dram bytes per launch \(read\+write\):\s*([0-9.eE+]+)", text)
+    if not (m_src and m_wl and m_b):
+        return None
+    if m_src.group(1) != kernel_hash() or m_wl.group(1) != workload:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except OSError:
+            pass
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ workload
+class Chain:
+    """Device buffers of one replica of a workload: per layer q, k, v, r,
+    u, v-bias, the attention output and two extended-context buffers
+    [M+L, B, d_model] that trade places every segment."""
+
+    def __init__(self, w: Workload, device):
+        s = w.shape
+        self.w = w
+        self.dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        B, H, D, L, M, T, dm = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len, s.klen, s.d_model
+        g = torch.Generator(device=device).manual_seed(w.seed)
+        self.layers = []
+        sin = torch.from_numpy(inputs.sinusoid(T, dm)).float().to(device)
+        for n in range(w.layers):
+            if w.init == "unit":
+                q = torch.randn(L, B, H, D, generator=g, device=device)
+                k = torch.randn(T, B, H, D, generator=g, device=device)
+                v = torch.randn(T, B, H, D, generator=g, device=device)
+                wr = torch.randn(dm, dm, generator=g, device=device) * math.sqrt(2.0 / dm)
+                u = torch.randn(H, D, generator=g, device=device)
+                wb = torch.randn(H, D, generator=g, device=device)
+                ext = torch.randn(T, B, dm, generator=g, device=device)
+            else:   # hidden states N(0,1), projection weights N(0, 0.02^2)
+                ext = torch.randn(T, B, dm, generator=g, device=device)
+                wq, wk, wv, wr = (torch.randn(dm, dm, generator=g, device=device) * 0.02 for _ in range(4))
+                q = (ext[M:] @ wq).view(L, B, H, D)
+                k = (ext @ wk).view(T, B, H, D)
+                v = (ext @ wv).view(T, B, H, D)
+                u = torch.randn(H, D, generator=g, device=device) * 0.02
+                wb = torch.randn(H, D, generator=g, device=device) * 0.02
+            r = (sin @ wr).flip(0).reshape(T, H, D)
+            self.layers.append(dict(
+                q=q.to(self.dtype).contiguous(), k=k.to(self.dtype).contiguous(),
+                v=v.to(self.dtype).contiguous(), r=r.to(self.dtype).contiguous(),
+                u=u.float().contiguous(), w=wb.float().contiguous(),
+                out=torch.empty(L, B, H, D, dtype=self.dtype, device=device),
+                ext=[ext.to(self.dtype).contiguous(), torch.empty(T, B, dm, dtype=self.dtype, device=device)]))
+        torch.cuda.synchronize()
+
+    def step(self, txl, attn_events=None):
+        M = self.w.shape.mem_len
+        launches = 0
+        for _seg in range(self.w.segments):
+            for lay in self.layers:
+                if attn_events is not None:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                                 mem_len=M, out=lay["out"])
+                if attn_events is not None:
+                    e1.record()
+                    attn_events.append((e0, e1))
+                txl.mem_update(lay["ext"][1], lay["ext"][0], mem_len=M)
+                lay["ext"].reverse()
+                launches += 1 + self.attn_extra_launches + 1
+        return launches
+
+    @property
+    def working_set_bytes(self) -> int:
+        tot = 0
+        for lay in self.layers:
+            for key in ("q", "k", "v", "r", "out"):
+                tot += lay[key].numel() * lay[key].element_size()
+            tot += sum(x.numel() * x.element_size() for x in lay["ext"])
+        return tot
+
+    attn_extra_launches = 0
+
+
+def splits_for(w: Workload) -> int:
+    """Mirror of the library's split choice (for the launch count only)."""
+    s = w.shape
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    nqt = (s.seg_len + 127) // 128
+    ctas = s.batch * s.heads * nqt
+    ntile = (s.klen + 127) // 128
+    best, best_s = 1e30, 1
+    for sp in range(1, min(16, ntile) + 1):
+        waves = (ctas * sp + sms - 1) // sms
+        per = (ntile + sp - 1) // sp
+        cost = waves * per + (1.0 if sp > 1 else 0.0)
+        if cost < best - 1e-9:
+            best, best_s = cost, sp
+    return best_s
+
+
+# ------------------------------------------------------------- e2e measurement
+def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
+    """The same step through the public API with the inputs in pinned host
+    memory: every step copies each layer's q, k, v, r, biases and extended
+    context host->device, runs the calls, and reads the last layer's output
+    back.  Timed with CUDA events around the whole step."""
+    host = []
+    for lay in chain.layers:
+        host.append({key: lay[key].cpu().pin_memory() for key in ("q", "k", "v", "r", "u", "w")}
+                    | {"ext": lay["ext"][0].cpu().pin_memory()})
+    out_host = torch.empty_like(chain.layers[-1]["out"], device="cpu").pin_memory()
+    M = w.shape.mem_len
+    h2d = sum(t.numel() * t.element_size() for hl in host for t in hl.values()) * w.segments
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for _seg in range(w.segments):
+            for lay, hl in zip(chain.layers, host):
+                for key in ("q", "k", "v", "r", "u", "w"):
+                    lay[key].copy_(hl[key], non_blocking=True)
+                lay["ext"][0].copy_(hl["ext"], non_blocking=True)
+                txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                                 mem_len=M, out=lay["out"])
+                txl.mem_update(lay["ext"][1], lay["ext"][0], mem_len=M)
+        out_host.copy_(chain.layers[-1]["out"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = e0.elapsed_time(e1) / 1e3
+    tokens = w.shape.batch * w.shape.seg_len * w.segments * steps
+    return {"value": aggregate_rate(tokens, sec, world), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ------------------------------------------------------------ oracle (CPU) leg
+_ORACLE_INPUTS = {}
+
+
+def oracle_rate(w: Workload, budget_s: float, layer=None):
+    """The float64 oracle, as it stands, on a bounded sample of one layer call
+    of the workload: random (b, h, i) rows.  Returns query-tokens/s in the
+    benchmark's unit (a query token = one position through every head of
+    every layer), the rows done and the threads used."""
+    import oracle
+    s = w.shape
+    key = (w.name, id(layer))
+    host = _ORACLE_INPUTS.get(key)
+    if host is None:
+        if layer is None:
+            p = inputs.unit_layer(s, w.seed)
+            host = {k: v.astype(np.float64) for k, v in p.items()}
+        else:
+            host = {k: layer[k].double().cpu().numpy() for k in ("q", "k", "v", "r", "u", "w")}
+        _ORACLE_INPUTS.clear()
+        _ORACLE_INPUTS[key] = host
+    g = np.random.Generator(np.random.PCG64(w.seed + 1))
+    threads = oracle.max_threads()
+    n = max(threads, 16)
+    done, spent = 0, 0.0
+    while spent < budget_s:
+        rows = np.stack([g.integers(0, s.batch, n), g.integers(0, s.heads, n),
+                         g.integers(0, s.seg_len, n)], 1)
+        t0 = time.perf_counter()
+        oracle.rel_attn_rows(host["q"], host["k"], host["v"], host["r"], host["u"], host["w"],
+                             mem_len=s.mem_len, rows=rows)
+        dt = time.perf_counter() - t0
+        done += n
+        spent += dt
+        if dt < budget_s / 8:
+            n *= 2
+    rows_per_s = done / spent
+    return rows_per_s / (s.heads * w.layers), done, threads, spent
+
+
+def config_of(w: Workload, world: int, working_set: int = 0):
+    s = w.shape
+    c = {"workload": w.name, "batch": s.batch, "heads": s.heads, "d_head": s.d_head,
+         "seg_len": s.seg_len, "mem_len": s.mem_len, "layers": w.layers, "segments": w.segments,
+         "parallelism": f"replicas x{world} (batch-independent, no collective)"}
+    if working_set:
+        c["l2"] = f"per-step working set {working_set / 1e9:.2f} GB > 129 MB L2 (inputs larger than L2, no flush)"
+    return c
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(w, per_step / 4)
+    rates, spent = [], 0.0
+    rows = 0
+    threads = 1
+    for _ in range(args.steps):
+        r, n, threads, t = oracle_rate(w, per_step)
+        rates.append(r)
+        rows += n
+        spent += t
+    value = rows / spent / (w.shape.heads * w.layers)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} random (b,h,i) rows of one layer call, unit-variance "
+                                       f"inputs; rate scaled to whole query tokens (x{w.shape.heads} heads "
+                                       f"x{w.layers} layers)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_BENCH, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="txl", choices=["txl", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--segments", type=int, default=0, help="override the workload's segment count")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import transformer_xl_relative_rel_gb300 as txl
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    init_dist(world)
+    try:
+        txl.load_library()
+    except txl.TxlError:
+        from transformer_xl_relative_rel_gb300 import _build
+        _build.build()
+        txl.load_library()
+
+    w = WORKLOADS[args.workload]
+    if args.layers or args.segments:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.layers or w.layers, segments=args.segments or w.segments)
+    s = w.shape
+    chain = Chain(w, torch.device("cuda", local))
+    splits = splits_for(w) if w.dtype == "bf16" else 1
+    chain.attn_extra_launches = 1 if splits > 1 else 0
+    for _ in range(args.warmup):
+        chain.step(txl)
+    txl.check()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    attn_events = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    launches = 0
+    for _ in range(args.steps):
+        launches += chain.step(txl, attn_events)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    txl.check()
+    local_s = e0.elapsed_time(e1) / 1e3
+    tokens_per_step = s.batch * s.seg_len * w.segments
+    value = aggregate_rate(tokens_per_step * args.steps, local_s, world)
+    step_s = max_over_ranks(local_s, world) / args.steps
+    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
+
+    flops_call = w.flops_per_call()
+    calls_per_step = w.layers * w.segments
+    tflops_step = flops_call * calls_per_step / step_s / 1e12
+    peaks, peak_kind = load_peaks()
+    ai = flops_call / w.bytes_per_call()
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai >= ridge:
+        achieved = flops_call / attn_avg_s / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    else:
+        achieved = w.bytes_per_call() / attn_avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof["traffic"] = profiled_traffic(w.name)
+    roof["kernel"] = "rel_attn_bf16_kernel" if w.dtype == "bf16" else "rel_attn_f32_kernel"
+    roof["launch_avg_us"] = attn_avg_s * 1e6
+    roof["peak_source"] = f"{peak_kind} ({'MEASURED_PEAKS.json burst' if peak_kind == 'measured' else 'fallback'})"
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, world, chain.working_set_bytes),
+            "tflops": tflops_step, "pct_bf16_peak": tflops_step / peaks["bf16_tflops"] * 100.0,
+            "roofline": roof, "clocks": clk, "gpu_launches": launches}
+
+    e2e_steps = args.e2e_steps or max(2, min(args.steps, 5))
+    line["e2e"] = measure_e2e(w, chain, txl, e2e_steps, world)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, threads, spent = oracle_rate(w, 12.0, layer=chain.layers[0])
+        line["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{rows} random (b,h,i) rows of layer 0's inputs ({spent:.1f} s of CPU); rate scaled "
+                      f"to whole query tokens (x{s.heads} heads x{w.layers} layers)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
