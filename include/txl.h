@@ -89,6 +89,38 @@ txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int me
                           int seg_len, int d_model, txl_dtype dtype, void *stream);
 
 /*
+ * txl_rel_attn_fwd_noalloc -- txl_rel_attn_fwd for callers that may not
+ * allocate device memory.  (No counterpart in the paper: this is a deployment
+ * variant of the same computation.)
+ *
+ * Some callers cannot call cudaMalloc: code inside a framework that owns all
+ * device memory through its own pool or a fixed arena, hosts that forbid
+ * allocation once initialised, or processes whose device memory is already
+ * fully reserved.  txl_rel_attn_fwd may allocate its split-key scratch on
+ * first use; this entry point allocates nothing.  Its scratch is one fixed
+ * array of TXL_NOALLOC_SCRATCH_BYTES inside the library's device code, held
+ * on every GPU that loads that code until the process exits.
+ *
+ * Same arguments, layouts, results and error rules as txl_rel_attn_fwd, plus:
+ *   - a call whose key split needs more than TXL_NOALLOC_SCRATCH_BYTES
+ *     (splits * batch * heads * seg_len * (ceil16(d_head) + 1) * 4 + 256
+ *     bytes) returns TXL_ERR_UNSUPPORTED before touching the GPU;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture;
+ *   - every call shares the one array, and each call writes every part of it
+ *     that it reads back, so nothing carries over between calls; but calls
+ *     whose kernels overlap on the GPU (different streams, or concurrent
+ *     host threads) race on it and must be serialised by the caller.
+ */
+#define TXL_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+txl_status txl_rel_attn_fwd_noalloc(const void *q, const void *k, const void *v, const void *r,
+                                    const float *u_bias, const float *v_bias,
+                                    int batch, int mem_len, int seg_len, int heads, int d_head,
+                                    txl_dtype dtype, void *out, void *stream);
+
+/*
  * txl_check -- synchronise `stream`, then report and clear the library's
  * device error word: TXL_ERR_TIMEOUT if an in-kernel bounded wait gave up
  * since the last check, TXL_ERR_CUDA if the stream reports an error, else

@@ -1,0 +1,77 @@
+"""txl_rel_attn_fwd_noalloc, the entry point for callers that cannot allocate
+device memory (framework-owned pools, hosts that forbid allocation after
+start-up).  It must give what txl_rel_attn_fwd gives, on consecutive calls,
+while taking its split-key scratch from the library's fixed array.
+
+Collected last on purpose (file name), so a run that stops at the first
+failure has already run every other test; it also passes on its own.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from tests.helpers import TOL_BF16, device_layer, unit_shape
+from transformer_xl_relative_rel_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+UNSUPPORTED = 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from transformer_xl_relative_rel_gb300 import _build, abi
+    _build.build()
+    return abi.load_library()
+
+
+def _call_noalloc(lib, dev, out, mem_len):
+    L, B, H, D = dev["q"].shape
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.txl_rel_attn_fwd_noalloc(
+        dev["q"].data_ptr(), dev["k"].data_ptr(), dev["v"].data_ptr(), dev["r"].data_ptr(),
+        dev["u"].data_ptr(), dev["w"].data_ptr(), B, mem_len, L, H, D, 1, out.data_ptr(), stream)
+
+
+def _call_default(lib, dev, out, mem_len):
+    L, B, H, D = dev["q"].shape
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.txl_rel_attn_fwd(
+        dev["q"].data_ptr(), dev["k"].data_ptr(), dev["v"].data_ptr(), dev["r"].data_ptr(),
+        dev["u"].data_ptr(), dev["w"].data_ptr(), B, mem_len, L, H, D, 1, out.data_ptr(), stream)
+
+
+@pytest.mark.parametrize("B,H,D,L,M", [(1, 4, 64, 128, 1600),    # key split + combine
+                                       (2, 2, 41, 130, 900)])    # split, no-TMA loads
+def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
+    for call in range(2):                       # the second call reuses the array
+        p = inputs.unit_layer(unit_shape(B, H, D, L, M), 300 + call)
+        dev, _ = device_layer(p, torch.bfloat16)
+        ref = torch.empty_like(dev["q"])
+        got = torch.full_like(dev["q"], float("nan"))
+        assert _call_default(lib, dev, ref, M) == 0
+        assert _call_noalloc(lib, dev, got, M) == 0
+        torch.cuda.synchronize()
+        err = (got.float() - ref.float()).abs().max().item()
+        assert np.isfinite(err) and err <= TOL_BF16, f"call {call}: max abs diff {err}"
+
+
+def test_noalloc_refuses_scratch_beyond_its_maximum(lib):
+    # B44 H8 D64 L128 M3800 splits its keys three ways: ~35 MB of partials,
+    # more than the fixed 32 MiB.  Real buffers, so nothing could go wrong on
+    # the device even if the refusal failed.
+    B, H, D, L, M = 44, 8, 64, 128, 3800
+    T = L + M
+    dev = {"q": torch.zeros(L, B, H, D, dtype=torch.bfloat16, device="cuda"),
+           "k": torch.zeros(T, B, H, D, dtype=torch.bfloat16, device="cuda"),
+           "v": torch.zeros(T, B, H, D, dtype=torch.bfloat16, device="cuda"),
+           "r": torch.zeros(T, H, D, dtype=torch.bfloat16, device="cuda"),
+           "u": torch.zeros(H, D, device="cuda"), "w": torch.zeros(H, D, device="cuda")}
+    out = torch.zeros(L, B, H, D, dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(lib, dev, out, M) == UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (out == 0).all()          # refused before anything ran

@@ -24,7 +24,7 @@ _lib: Optional[ctypes.CDLL] = None
 
 #: every symbol include/txl.h declares (checked by the host-side tests)
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
-           "txl_last_cuda_error", "txl_version", "txl_shutdown")
+           "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc")
 
 
 class TxlError(RuntimeError):
@@ -49,6 +49,8 @@ def load_library() -> ctypes.CDLL:
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.txl_rel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd.restype = i
+    lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.txl_rel_attn_fwd_noalloc.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_mem_update.restype = i
     lib.txl_check.argtypes = [vp]
@@ -128,6 +130,19 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
         B, mem_len, L, H, D, code, _ptr(out), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd")
+    return out
+
+
+def rel_attn_fwd_noalloc(q, k, v, r, u_bias, v_bias, mem_len: int, out, stream=None):
+    """The same call through txl_rel_attn_fwd_noalloc, for callers that may not
+    allocate device memory: ``out`` must be given, and the library allocates
+    nothing (its split-key scratch is a fixed array in the library)."""
+    L, B, H, D = q.shape
+    code = _dtype_code(q)
+    st = load_library().txl_rel_attn_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+        B, mem_len, L, H, D, code, _ptr(out), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_noalloc")
     return out
 
 

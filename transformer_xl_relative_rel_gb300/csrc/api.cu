@@ -23,6 +23,13 @@ static txl_status cuda_fail(cudaError_t e)
     return TXL_ERR_CUDA;
 }
 
+cudaError_t note_cuda_error(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    cudaGetLastError();
+    return e;
+}
+
 int device_sm_count()
 {
     static int cached[64] = {0};

@@ -32,4 +32,8 @@ cudaError_t launch_rollover(void *dst, const void *src, size_t bytes, int elem_s
 
 int device_sm_count();
 
+// records `e` as the thread's last CUDA error (reported by txl_last_cuda_error)
+// and clears the runtime's error state; returns e
+cudaError_t note_cuda_error(cudaError_t e);
+
 }  // namespace txl
