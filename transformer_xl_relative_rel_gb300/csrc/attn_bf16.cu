@@ -5,29 +5,32 @@
 //     out_i = softmax_j(s_ij) v_j,
 // with Q the reversed projected table of Appendix B (row t = W_kR R_{T-1-t}).
 //
-// How (one CTA = 128 query rows of one (b, h), or one key-range split of them):
-//   * q+u and q+v are formed once per CTA in fp32 and rounded to bf16 into two
-//     shared-memory operand tiles (Section 3.3: u and v replace the per-query
-//     position term of the absolute formulation).
-//   * K, V and the table band are staged by TMA (one 4-D box each) in the
-//     canonical no-swizzle K-major layout [d/8][rows][8].
-//   * Content term: S = (q+u) K^T, one 128x128 tcgen05 MMA chain into TMEM.
-//   * Position term, Appendix B: B~ = (q+v) Q_band^T over the 256 table rows
-//     that the tile's pairs touch; the left shift of row i by L-1-i is pure
-//     index arithmetic: row ii of the tile reads B~ column 127-ii+jj.  TMEM
-//     loads are warp-uniform in the column, so each warp loads the 64-column
-//     window its 32 rows need and every thread aligns its own row with a
-//     5-stage register barrel shift by 31-lane.  The shifted matrix is never
-//     materialised in memory.
-//   * Mask j <= M+i, scale and online softmax in the log2 domain, one query
-//     row per thread (row reductions stay inside the thread), P rounded to
-//     bf16 into shared memory, O += P V as a tcgen05 MMA accumulating in TMEM,
-//     O rescaled in TMEM when the running max grows.
-//   * Epilogue: O / l to bf16 in global memory, or, when the keys are split
-//     across CTAs (long memories), normalised partials plus their log-sum-exp
-//     for the combine kernel below.
-// Every mbarrier wait is bounded; on expiry the kernel records an error word
-// (read by txl_check) and winds down.
+// One CTA owns 128 query rows of one (b, h) -- or one key-range split of them
+// -- and walks its keys in tiles of 64.  Six warps with fixed roles:
+//   warp 0    producer: TMA loads of K, V and one 64-row chunk of the table
+//             per tile into a four-stage shared-memory ring (threads' loads
+//             when D is not a multiple of 8: rows are then not 16-byte
+//             aligned and TMA cannot address them);
+//   warp 1    MMA issuer (one thread): per tile, S = (q+u) K^T into one of
+//             three TMEM S buffers and the next band chunk B~ = (q+v) Q_chunk^T
+//             into a 4-slot TMEM ring; then O += P V for the previous tile.
+//             q+u, q+v, K, the table and V come from shared memory, P is a
+//             TMEM A operand;
+//   warps 2-5 softmax, one query row per thread (TMEM lane = row): each tile
+//             reads S and the band window its warp needs, aligns the band to
+//             the row (Appendix B's left shift of row i by L-1-i, done as a
+//             register barrel shift by 31-lane), adds, masks j <= M+i, and
+//             runs the online softmax in the log2 domain.  P (bf16) goes back
+//             into the S buffer's TMEM columns for the P.V MMA.
+// Appendix B's table product is formed once per 64-row chunk: tile n uses
+// chunks n, n+1, n+2 of the band, and computes chunk n+2 itself, so the
+// position term costs the same tensor work as the content term.  The MMAs of
+// the next tiles run while the softmax of tile n runs (three S buffers).
+// The running max used for the exponentials is raised only when a row's max
+// grows by more than 8 (log2 units); O in TMEM is rescaled only then.
+// The scale log2(e)/sqrt(D) is folded into q+u and q+v before rounding.
+// Every mbarrier wait is bounded; on expiry the CTA records an error word
+// (read by txl_check) and every role winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,16 +48,19 @@ __device__ unsigned int g_err_word;
 namespace {
 using namespace sm100;
 
-constexpr int BM = 128;          // query rows per CTA (TMEM lanes)
-constexpr int BN = 128;          // keys per tile
-constexpr int RWIN = 256;        // table rows of a tile's band (BM+BN-1, rounded up)
-constexpr int NT = 128;          // threads per CTA
-constexpr uint32_t TM_S = 0;     // TMEM columns: S (fp32, then the scaled logits)
-constexpr uint32_t TM_B = 128;   //               B~ band (256 columns)
-constexpr uint32_t TM_O = 384;   //               O accumulator (DP <= 64 columns)
+constexpr int BM = 128;           // query rows per CTA (TMEM lanes)
+constexpr int BN = 64;            // keys per tile; also table rows per band chunk
+constexpr int NCHUNK = 4;         // TMEM band-chunk ring
+constexpr int NSTAGE = 4;         // shared-memory ring of (K, V, table chunk) tiles
+constexpr int NT = 192;           // 6 warps
+constexpr int NSBUF = 3;          // S buffers (P aliases the first 32 columns of each)
+constexpr uint32_t TM_S = 0;      // 3 x 64 columns
+constexpr uint32_t TM_BAND = 192; // band ring, 4 x 64 columns
+constexpr uint32_t TM_O = 448;    // O accumulator, DP <= 64 columns
 constexpr uint32_t TM_COLS = 512;
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait, then give up
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;          // raise the exponent base only past 2^8
 
 struct Params {
     const __nv_bfloat16 *q, *k, *v, *r;
@@ -69,21 +75,22 @@ struct Params {
 
 template <int DP>
 struct Smem {
-    static constexpr uint32_t Q_BYTES = BM * DP * 2;
-    static constexpr uint32_t K_BYTES = BN * DP * 2;
-    static constexpr uint32_t R_BYTES = RWIN * DP * 2;
-    static constexpr uint32_t P_BYTES = BM * BN * 2;
-    static constexpr uint32_t QU = 0;
-    static constexpr uint32_t QV = QU + Q_BYTES;
-    static constexpr uint32_t KS = QV + Q_BYTES;
-    static constexpr uint32_t VS = KS + K_BYTES;
-    static constexpr uint32_t RS = VS + K_BYTES;
-    static constexpr uint32_t PS = RS + R_BYTES;
-    static constexpr uint32_t BARS = PS + P_BYTES;       // 6 mbarriers
-    static constexpr uint32_t TMEM_HOLDER = BARS + 64;
+    static constexpr uint32_t TILE = BN * DP * 2;          // one K, V or table chunk
+    static constexpr uint32_t STAGE = 3 * TILE;             // K, V, chunk
+    static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
+    static constexpr uint32_t PRE = NSTAGE * STAGE;         // table chunks 0 and 1
+    static constexpr uint32_t QU = PRE + 2 * TILE;          // q+u, q+v: [d/8][128][8] bf16
+    static constexpr uint32_t QV = QU + BM * DP * 2;
+    static constexpr uint32_t BARS = QV + BM * DP * 2;
+    // barrier slots (8 bytes each): stage full / empty, S full, P full,
+    // P.V done, O done
+    static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE,
+                         B_S = 2 + 2 * NSTAGE, B_P = B_S + NSBUF, B_PV = B_P + NSBUF,
+                         B_O = B_PV + NSBUF;
+    static constexpr uint32_t MISC = BARS + 24 * 8;         // tmem holder, abort flag
+    static constexpr uint32_t USED = MISC + 16;
     // at least 120 KB so that only one CTA fits on an SM: each CTA takes all
     // 512 TMEM columns
-    static constexpr uint32_t USED = TMEM_HOLDER + 16;
     static constexpr uint32_t TOTAL = USED > 120 * 1024 ? USED : 120 * 1024;
 };
 
@@ -100,32 +107,88 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction, two lanes of work)
+__device__ __forceinline__ uint64_t f2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_err_word, code); }
 
-// Cooperative (all 128 threads) load of `nrows` rows of D bf16 elements into
-// the [d/8][nrows][8] layout, rows outside [0, limit) and columns >= D zero.
-// Used when D is not a multiple of 8 (rows are then not 16-byte aligned and
-// TMA cannot address them).
-template <int DP>
-__device__ __forceinline__ void load_rows_generic(unsigned char *dst, int nrows,
-                                                  const __nv_bfloat16 *src, long row0_elems,
-                                                  long row_stride, int first_row, int limit, int D)
+// A bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int rr = warp; rr < nrows; rr += NT / 32) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > WAIT_NS) {
+            *abort = 1;
+            record_error(1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Warp-cooperative load of `nrows` rows of D bf16 elements into the
+// [d/8][nrows][8] layout, for D not a multiple of 8 (rows are then not
+// 16-byte aligned and TMA cannot address them).  Each row is read as aligned
+// 32-bit words, one per lane (coalesced); a row that starts in the middle of a
+// word is realigned with a funnel shift from the next lane's word.  Rows
+// outside [0, limit) are written as zeros; element D (the first padding
+// element, when D is odd) is written as zero; later padding was zeroed once.
+__device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, const __nv_bfloat16 *src,
+                                               long row0_elems, long row_stride, int first_row,
+                                               int limit, int D, int lane)
+{
+    const int npairs = (D + 1) >> 1;     // element pairs covering D (<= 32 for D <= 64)
+#pragma unroll 4
+    for (int rr = 0; rr < nrows; ++rr) {
         const int row = first_row + rr;
         const bool ok = row >= 0 && row < limit;
-        const __nv_bfloat16 *p = src + row0_elems + (long)row * row_stride;
-#pragma unroll
-        for (int d0 = 0; d0 < DP; d0 += 32) {
-            const int d = d0 + lane;
-            if (d < DP) {
-                __nv_bfloat16 x = __float2bfloat16(0.f);
-                if (ok && d < D) x = p[d];
-                *reinterpret_cast<__nv_bfloat16 *>(dst + (d >> 3) * (nrows * 16) + rr * 16 +
-                                                   (d & 7) * 2) = x;
-            }
-        }
+        const long e0 = row0_elems + (long)row * row_stride;        // first element of the row
+        const uint32_t *wbase = reinterpret_cast<const uint32_t *>(src + (e0 & ~1L));
+        const int odd = (int)(e0 & 1);
+        // lane l holds word l (elements 2l-odd .. 2l+1-odd of the row); only the
+        // words that overlap the row are read
+        uint32_t w = 0;
+        if (ok && lane <= ((odd + D - 1) >> 1)) w = wbase[lane];
+        const uint32_t wn = __shfl_down_sync(0xffffffffu, w, 1);
+        uint32_t pair = odd ? __byte_perm(w, wn, 0x5432) : w;      // elements 2l, 2l+1
+        if (2 * lane + 1 == D) pair &= 0xFFFFu;                      // zero the padding element
+        if (lane < npairs)
+            *reinterpret_cast<uint32_t *>(dst + (lane >> 2) * (nrows * 16) + rr * 16 + (lane & 3) * 4) = pair;
     }
 }
 
@@ -152,36 +215,48 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int ntile = (kend + BN - 1) / BN;
     const int t0 = (int)(((long)split * ntile) / p.splits);
     const int t1 = (int)(((long)(split + 1) * ntile) / p.splits);
-    const int ii = tid;                                    // this thread's row = TMEM lane
-    const int i = i0 + ii;
-    const bool row_valid = ii < rows_here;
+    const int N = t1 - t0;                                 // tiles of this CTA
     const long qkv_row = (long)p.B * p.H * p.D;            // elements between positions
     const long head_off = ((long)b * p.H + h) * p.D;
+    const int kb0 = p.L - BM - i0 + t0 * BN;              // first table row of chunk 0
 
-    if (t0 >= t1) {   // an empty key split for this tile: neutral partials
-        if (row_valid) {
-            const long prow = ((long)split * p.B * p.H + bh) * p.L + i;
+    if (N <= 0) {   // an empty key split for this tile: neutral partials
+        if (tid < rows_here) {
+            const long prow = ((long)split * p.B * p.H + bh) * p.L + i0 + tid;
             p.part_lse[prow] = -INFINITY;
             for (int d = 0; d < DP; ++d) p.part_o[prow * DP + d] = 0.f;
         }
         return;
     }
 
-    unsigned char *qu_s = smem + S::QU, *qv_s = smem + S::QV, *k_s = smem + S::KS;
-    unsigned char *v_s = smem + S::VS, *r_s = smem + S::RS, *p_s = smem + S::PS;
-    const uint32_t bar_kr = smem_u32(smem + S::BARS), bar_v = bar_kr + 8, bar_mma = bar_kr + 16;
-    const uint32_t bar_pv = bar_kr + 24;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::TMEM_HOLDER);
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + S::BARS + 8u * (uint32_t)i; };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::MISC + 8);
+    // every lane of a warp waits; the warp continues only if all of them saw
+    // the barrier (keeps the warp converged for its collective instructions)
+    auto wwait = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar(i), parity, abort)) != 0;
+    };
 
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(bar_kr, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_pv, 1);
+        *abort = 0;
+        mbar_init(bar(S::B_Q), 128);
+        mbar_init(bar(S::B_PRE), kTma ? 1 : 32);
+        for (int x = 0; x < NSTAGE; ++x) {
+            mbar_init(bar(S::B_FULL + x), kTma ? 1 : 32);
+            mbar_init(bar(S::B_EMPTY + x), 1);
+        }
+        for (int x = 0; x < NSBUF; ++x) {
+            mbar_init(bar(S::B_S + x), 1);
+            mbar_init(bar(S::B_P + x), 128);
+            mbar_init(bar(S::B_PV + x), 1);
+        }
+        mbar_init(bar(S::B_O), 1);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -189,56 +264,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             prefetch_tmap(&tm_r);
         }
     }
-    // padding slice (D rounded up to 16 for the MMA K dimension) must be zero:
-    // TMA never writes it, and 0 * (stale NaN) would poison the sums
-    if (kTma && (p.D & 15)) {
-        const int s0 = p.D >> 3;   // first padding slice
-        for (int x = tid; x < BN * 4; x += NT) {
-            reinterpret_cast<uint32_t *>(k_s + s0 * BN * 16)[x] = 0u;
-            reinterpret_cast<uint32_t *>(v_s + s0 * BN * 16)[x] = 0u;
-        }
-        for (int x = tid; x < RWIN * 4; x += NT)
-            reinterpret_cast<uint32_t *>(r_s + s0 * RWIN * 16)[x] = 0u;
-    }
-
-    // ---- q+u and q+v for this thread's row, rounded once to bf16
-    {
-        float qrow[DP];
-#pragma unroll
-        for (int d = 0; d < DP; ++d) qrow[d] = 0.f;
-        if (row_valid) {
-            const __nv_bfloat16 *qp = p.q + (long)i * qkv_row + head_off;
-            if ((p.D & 7) == 0) {
-#pragma unroll
-                for (int d8 = 0; d8 < DP / 8; ++d8) {
-                    if (d8 * 8 < p.D) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(qp + d8 * 8);
-                        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-                        for (int z = 0; z < 8; ++z) qrow[d8 * 8 + z] = __bfloat162float(e[z]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int d = 0; d < DP; ++d)
-                    if (d < p.D) qrow[d] = __bfloat162float(qp[d]);
-            }
-        }
-        const float *up = p.u + h * p.D, *wp = p.w + h * p.D;
-#pragma unroll
-        for (int d8 = 0; d8 < DP / 8; ++d8) {
-            uint32_t a[4], c[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const int d = d8 * 8 + 2 * z;
-                const bool in0 = row_valid && d < p.D, in1 = row_valid && d + 1 < p.D;
-                const float u0 = in0 ? up[d] : 0.f, u1 = in1 ? up[d + 1] : 0.f;
-                const float w0 = in0 ? wp[d] : 0.f, w1 = in1 ? wp[d + 1] : 0.f;
-                a[z] = pack_bf16(qrow[d] + u0, qrow[d + 1] + u1);
-                c[z] = pack_bf16(qrow[d] + w0, qrow[d + 1] + w1);
-            }
-            *reinterpret_cast<uint4 *>(qu_s + d8 * (BM * 16) + ii * 16) = make_uint4(a[0], a[1], a[2], a[3]);
-            *reinterpret_cast<uint4 *>(qv_s + d8 * (BM * 16) + ii * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+    // the padding slice of D (rounded up to 16 for the MMA K dimension) must be
+    // zero in every K / V / table buffer: loads never write it
+    if ((p.D & 15) != 0) {
+        for (int tile = 0; tile < 3 * NSTAGE + 2; ++tile) {
+            unsigned char *base = smem + S::ST0 + tile * S::TILE;   // stages, then the two pre chunks
+            for (int sl = p.D >> 3; sl < DP / 8; ++sl)
+                for (int x = tid; x < BN * 4; x += NT) reinterpret_cast<uint32_t *>(base + sl * BN * 16)[x] = 0u;
         }
     }
     fence_proxy_async_smem();
@@ -246,231 +278,314 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's lanes
 
-    const uint32_t kr_bytes = (uint32_t)(BN + RWIN) * (uint32_t)(p.D / 8) * 16u;
-    const uint32_t v_bytes = (uint32_t)BN * (uint32_t)(p.D / 8) * 16u;
-    const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-    const uint32_t idesc_b = idesc_bf16(BM, RWIN, 0, 0);
-    const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
-    const uint32_t a_qu = smem_u32(qu_s), a_qv = smem_u32(qv_s), a_k = smem_u32(k_s);
-    const uint32_t a_v = smem_u32(v_s), a_r = smem_u32(r_s), a_p = smem_u32(p_s);
-
-    if (kTma && tid == 0) {
-        const int j0 = t0 * BN, kb = p.L - BM - i0 + j0;
-        mbar_arrive_expect_tx(bar_kr, kr_bytes);
-        tma_load_4d(a_k, &tm_k, bar_kr, 0, j0, 0, bh);
-        tma_load_4d(a_r, &tm_r, bar_kr, 0, kb, 0, h);
-    }
-
-    uint32_t ph_kr = 0, ph_v = 0, ph_mma = 0, ph_pv = 0;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool fail = false;
-
-    for (int t = t0; t < t1; ++t) {
-        const int j0 = t * BN;
-        const int kb = p.L - BM - i0 + j0;     // first table row of the band
-        if (!kTma) {
-            if (t > t0) {                       // previous P.V done: V and P free
-                fail |= !mbar_wait(bar_pv, ph_pv, WAIT_NS);
-                ph_pv ^= 1;
+    if (warp == 0) {
+        // =============================================================== producer
+        const uint32_t tile_bytes = (uint32_t)BN * (uint32_t)(p.D / 8) * 16u;
+        // table chunks 0 and 1 for the first tile
+        if (kTma) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(S::B_PRE), 2 * tile_bytes);
+                tma_load_4d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, 0, h);
+                tma_load_4d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, 0, h);
             }
-            load_rows_generic<DP>(k_s, BN, p.k, head_off, qkv_row, j0, p.T, p.D);
-            load_rows_generic<DP>(v_s, BN, p.v, head_off, qkv_row, j0, p.T, p.D);
-            load_rows_generic<DP>(r_s, RWIN, p.r, (long)h * p.D, (long)p.H * p.D, kb, p.T, p.D);
+        } else {
+            warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
+            warp_load_rows(smem + S::PRE + S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0 + BN,
+                           p.T, p.D, lane);
             fence_proxy_async_smem();
-            tc_fence_before();
-            if (__syncthreads_or(fail)) break;
-            tc_fence_after();
+            mbar_arrive(bar(S::B_PRE));
         }
-        // ---- content and position MMAs (one thread issues)
-        if (tid == 0) {
-            bool ok = true;
+        for (int n = 0; n < N; ++n) {
+            const int st = n % NSTAGE;
+            // the stage is free once the P.V of tile n-NSTAGE (its last reader) is done
+            if (n >= NSTAGE && !wwait(S::B_EMPTY + st, ((n / NSTAGE) - 1) & 1)) break;
+            const int j0 = (t0 + n) * BN;
+            const int crow = kb0 + (n + 2) * BN;     // table chunk n+2
+            const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
             if (kTma) {
-                ok = mbar_wait(bar_kr, ph_kr, WAIT_NS);
-                ph_kr ^= 1;
-            }
-            tc_fence_after();
-            if (ok) {
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks) {
-                    mma_bf16_ss(tmem + TM_S, smem_desc(a_qu + ks * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(a_k + ks * 2 * BN * 16, BN * 16, 128), idesc_s, ks > 0);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_FULL + st), 3 * tile_bytes);
+                    tma_load_4d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, 0, bh);
+                    tma_load_4d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, 0, bh);
+                    tma_load_4d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, 0, h);
                 }
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks) {
-                    mma_bf16_ss(tmem + TM_B, smem_desc(a_qv + ks * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(a_r + ks * 2 * RWIN * 16, RWIN * 16, 128), idesc_b, ks > 0);
-                }
-                mma_commit(bar_mma);
             } else {
-                fail = true;
+                unsigned char *d = smem + S::ST0 + st * S::STAGE;
+                warp_load_rows(d, BN, p.k, head_off, qkv_row, j0, p.T, p.D, lane);
+                warp_load_rows(d + S::TILE, BN, p.v, head_off, qkv_row, j0, p.T, p.D, lane);
+                warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, crow, p.T, p.D, lane);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(S::B_FULL + st));
             }
         }
-        __syncwarp();
-        if (__syncthreads_or(fail)) break;
-        fail |= !mbar_wait(bar_mma, ph_mma, WAIT_NS);
-        ph_mma ^= 1;
+    } else if (warp == 1) {
+        // =============================================================== MMA issuer
+        const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
+        const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
+        bool ok = wwait(S::B_Q, 0) && wwait(S::B_PRE, 0);
         tc_fence_after();
-        if (kTma && tid == 0 && !fail) {
-            // the commit above also covers the previous P.V, so V is free
-            mbar_arrive_expect_tx(bar_v, v_bytes);
-            tma_load_4d(a_v, &tm_v, bar_v, 0, j0, 0, bh);
-            if (t + 1 < t1) {   // K and the band are consumed: prefetch the next tile
-                mbar_arrive_expect_tx(bar_kr, kr_bytes);
-                tma_load_4d(a_k, &tm_k, bar_kr, 0, j0 + BN, 0, bh);
-                tma_load_4d(a_r, &tm_r, bar_kr, 0, kb + BN, 0, h);
+        const uint32_t a_qu = sbase + S::QU, a_qv = sbase + S::QV;
+        if (ok && lane == 0) {
+            for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
+                const uint32_t bsm = sbase + S::PRE + c * S::TILE;
+#pragma unroll
+                for (int ks = 0; ks < DP / 16; ++ks)
+                    mma_bf16_ss(tmem + TM_BAND + 64 * c, smem_desc(a_qv + ks * 2 * BM * 16, BM * 16, 128),
+                                smem_desc(bsm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
             }
         }
         __syncwarp();
-        if (__syncthreads_or(fail)) break;
-
-        // ---- pass 1: align the position term, add, mask, scale; keep in TMEM
-        const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);   // visible iff jj <= lim
-        const int shift = 31 - lane;
-        float tmax = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float s[32], a[64];
-            const int base = 96 - 32 * warp + 32 * c;   // window of this warp's rows
-            tmem_ld32(tlane + TM_S + 32 * c, s);
-            tmem_ld32(tlane + TM_B + base, *reinterpret_cast<float(*)[32]>(&a[0]));
-            tmem_ld32(tlane + TM_B + base + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
-#pragma unroll
-            for (int x = 0; x < 48; ++x) a[x] = (shift & 16) ? a[x + 16] : a[x];
-#pragma unroll
-            for (int x = 0; x < 40; ++x) a[x] = (shift & 8) ? a[x + 8] : a[x];
-#pragma unroll
-            for (int x = 0; x < 36; ++x) a[x] = (shift & 4) ? a[x + 4] : a[x];
-#pragma unroll
-            for (int x = 0; x < 34; ++x) a[x] = (shift & 2) ? a[x + 2] : a[x];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) a[x] = (shift & 1) ? a[x + 1] : a[x];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                float val = (s[x] + a[x]) * p.sl2;
-                val = (32 * c + x <= lim) ? val : -INFINITY;
-                tmax = fmaxf(tmax, val);
-                s[x] = val;
-            }
-            tmem_st32(tlane + TM_S + 32 * c, s);
-        }
-        tmem_wait_st();
-
-        // ---- pass 2: probabilities to shared memory (bf16), running sums
-        const float m_new = fmaxf(m_run, tmax);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2(m_run - m_use);
-        float sum = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float x[32];
-            tmem_ld32(tlane + TM_S + 32 * c, x);
-            uint32_t pk[16];
-#pragma unroll
-            for (int y = 0; y < 16; ++y) {
-                const float p0 = ex2(x[2 * y] - m_use), p1 = ex2(x[2 * y + 1] - m_use);
-                sum += p0 + p1;
-                pk[y] = pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int z = 0; z < 4; ++z)
-                *reinterpret_cast<uint4 *>(p_s + (4 * c + z) * (BM * 16) + ii * 16) =
-                    make_uint4(pk[4 * z], pk[4 * z + 1], pk[4 * z + 2], pk[4 * z + 3]);
-        }
-        l_run = l_run * alpha + sum;
-        m_run = m_new;
-        // ---- rescale the accumulator when the running max moved
-        if (t > t0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-#pragma unroll
-            for (int c = 0; c < DP / 16; ++c) {
-                float o[16];
-                tmem_ld16(tlane + TM_O + 16 * c, o);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) o[x] *= alpha;
-                tmem_st16(tlane + TM_O + 16 * c, o);
-            }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(fail)) break;
-
-        // ---- O += P V
-        if (tid == 0) {
-            bool ok = true;
-            if (kTma) {
-                ok = mbar_wait(bar_v, ph_v, WAIT_NS);
-                ph_v ^= 1;
-            }
+        for (int n = 0; ok && n < N; ++n) {
+            const int sb = n % NSBUF;
+            const int st = n % NSTAGE;
+            // S buffer sb last held P of tile n-NSBUF: its P.V must be done
+            if (n >= NSBUF) ok = wwait(S::B_PV + sb, ((n / NSBUF) - 1) & 1);
+            ok = ok && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
             tc_fence_after();
-            if (ok) {
+            if (ok && lane == 0) {
+                const uint32_t ksm = sbase + S::ST0 + st * S::STAGE;
+                const uint32_t csm = ksm + 2 * S::TILE;
+                const uint32_t slot = (uint32_t)((n + 2) % NCHUNK);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_bf16_ss(tmem + TM_O, smem_desc(a_p + kk * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(a_v + kk * 16 * 16, 128, BN * 16), idesc_o,
-                                (t > t0 || kk > 0) ? 1u : 0u);
+                for (int ks = 0; ks < DP / 16; ++ks)
+                    mma_bf16_ss(tmem + TM_S + 64 * sb, smem_desc(a_qu + ks * 2 * BM * 16, BM * 16, 128),
+                                smem_desc(ksm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < DP / 16; ++ks)
+                    mma_bf16_ss(tmem + TM_BAND + 64 * slot, smem_desc(a_qv + ks * 2 * BM * 16, BM * 16, 128),
+                                smem_desc(csm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
+                mma_commit(bar(S::B_S + sb));
+            }
+            __syncwarp();
+            if (ok && n >= 1) {   // P.V of the previous tile
+                const int pb = (n - 1) % NSBUF;
+                ok = wwait(S::B_P + pb, ((n - 1) / NSBUF) & 1);
+                tc_fence_after();
+                if (ok && lane == 0) {
+                    const int pst = (n - 1) % NSTAGE;
+                    const uint32_t vsm = sbase + S::ST0 + pst * S::STAGE + S::TILE;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_S + 64 * pb + 8 * kk,
+                                    smem_desc(vsm + kk * 16 * 16, 128, BN * 16), idesc_o,
+                                    (n - 1 > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_PV + pb));
+                    mma_commit(bar(S::B_EMPTY + pst));
                 }
-                if (!kTma) mma_commit(bar_pv);
-            } else {
-                fail = true;
+                __syncwarp();
             }
         }
-        __syncwarp();
-    }
-
-    // ---- wait for the last P.V, then the epilogue
-    if (__syncthreads_or(fail)) {
-        record_error(1u);
+        if (ok) {   // P.V of the last tile, then release the epilogue
+            const int pb = (N - 1) % NSBUF;
+            ok = wwait(S::B_P + pb, ((N - 1) / NSBUF) & 1);
+            tc_fence_after();
+            if (ok && lane == 0) {
+                const int pst = (N - 1) % NSTAGE;
+                const uint32_t vsm = sbase + S::ST0 + pst * S::STAGE + S::TILE;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_S + 64 * pb + 8 * kk,
+                                smem_desc(vsm + kk * 16 * 16, 128, BN * 16), idesc_o,
+                                (N - 1 > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(S::B_PV + pb));
+                mma_commit(bar(S::B_O));
+            }
+            __syncwarp();
+        }
     } else {
-        if (tid == 0) mma_commit(bar_mma);
-        __syncwarp();
-        if (!mbar_wait(bar_mma, ph_mma, WAIT_NS)) {
-            record_error(2u);
-            fail = true;
-        }
-        tc_fence_after();
-    }
-    if (!__syncthreads_or(fail)) {
-        float o[DP];
+        // =============================================================== softmax
+        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+        const int ii = quarter * 32 + lane;        // this thread's query row
+        const int i = i0 + ii;
+        const bool row_valid = ii < rows_here;
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+
+        // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into TMEM
+        {
+            float qrow[DP];
 #pragma unroll
-        for (int c = 0; c < DP / 16; ++c) tmem_ld16(tlane + TM_O + 16 * c, *reinterpret_cast<float(*)[16]>(&o[16 * c]));
-        if (row_valid) {
-            if (p.splits == 1) {
-                const float inv = 1.f / l_run;
-                __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off;
+            for (int d = 0; d < DP; ++d) qrow[d] = 0.f;
+            if (row_valid) {
+                const __nv_bfloat16 *qp = p.q + (long)i * qkv_row + head_off;
                 if ((p.D & 7) == 0) {
 #pragma unroll
                     for (int d8 = 0; d8 < DP / 8; ++d8) {
                         if (d8 * 8 < p.D) {
-                            uint4 pk;
-                            pk.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
-                            pk.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
-                            pk.z = pack_bf16(o[d8 * 8 + 4] * inv, o[d8 * 8 + 5] * inv);
-                            pk.w = pack_bf16(o[d8 * 8 + 6] * inv, o[d8 * 8 + 7] * inv);
-                            *reinterpret_cast<uint4 *>(op + d8 * 8) = pk;
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(qp + d8 * 8);
+                            const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+                            for (int z = 0; z < 8; ++z) qrow[d8 * 8 + z] = __bfloat162float(e[z]);
                         }
                     }
                 } else {
 #pragma unroll
                     for (int d = 0; d < DP; ++d)
-                        if (d < p.D) op[d] = __float2bfloat16(o[d] * inv);
+                        if (d < p.D) qrow[d] = __bfloat162float(qp[d]);
                 }
-            } else {
-                const long prow = ((long)split * p.B * p.H + bh) * p.L + i;
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP);
+            }
+            const float *up = p.u + h * p.D, *wp = p.w + h * p.D;
+            // row ii of the [d/8][128][8] operand tiles: one 16-byte store per slice
 #pragma unroll
-                for (int d4 = 0; d4 < DP / 4; ++d4)
-                    po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
-                                         o[4 * d4 + 3] * inv);
-                p.part_lse[prow] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+            for (int d8 = 0; d8 < DP / 8; ++d8) {
+                uint32_t a4[4], c4[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const int d = d8 * 8 + 2 * z;
+                    const bool in0 = row_valid && d < p.D, in1 = row_valid && d + 1 < p.D;
+                    const float u0 = in0 ? up[d] : 0.f, u1 = in1 ? up[d + 1] : 0.f;
+                    const float w0 = in0 ? wp[d] : 0.f, w1 = in1 ? wp[d + 1] : 0.f;
+                    a4[z] = pack_bf16((qrow[d] + u0) * p.sl2, (qrow[d + 1] + u1) * p.sl2);
+                    c4[z] = pack_bf16((qrow[d] + w0) * p.sl2, (qrow[d + 1] + w1) * p.sl2);
+                }
+                *reinterpret_cast<uint4 *>(smem + S::QU + d8 * (BM * 16) + ii * 16) =
+                    make_uint4(a4[0], a4[1], a4[2], a4[3]);
+                *reinterpret_cast<uint4 *>(smem + S::QV + d8 * (BM * 16) + ii * 16) =
+                    make_uint4(c4[0], c4[1], c4[2], c4[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(S::B_Q));
+        }
+
+        float m_used = -INFINITY, l_run = 0.f;
+        const int shift = 31 - lane;
+        bool ok = true;
+        for (int n = 0; n < N; ++n) {
+            const int sb = n % NSBUF;
+            const int j0 = (t0 + n) * BN;
+            if (!wwait(S::B_S + sb, (n / NSBUF) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[64], a[96];
+            uint32_t bcol[3];
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc) {
+                const int rel = 96 - 32 * quarter + 32 * pc;           // column in chunks n..n+2
+                bcol[pc] = TM_BAND + 64 * (uint32_t)((n + (rel >> 6)) % NCHUNK) + (rel & 63);
+            }
+            tmem_ld_5x32(tl + TM_S + 64 * sb, tl + TM_S + 64 * sb + 32, tl + bcol[0], tl + bcol[1],
+                         tl + bcol[2], x, a);
+            // row ii reads band column 127-ii+jj: a warp-uniform start plus 31-lane
+#pragma unroll
+            for (int y = 0; y < 79; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
+#pragma unroll
+            for (int y = 0; y < 71; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
+#pragma unroll
+            for (int y = 0; y < 67; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
+#pragma unroll
+            for (int y = 0; y < 65; ++y) a[y] = (shift & 2) ? a[y + 2] : a[y];
+#pragma unroll
+            for (int y = 0; y < 64; ++y) a[y] = (shift & 1) ? a[y + 1] : a[y];
+#pragma unroll
+            for (int y = 0; y < 32; ++y) unf2(add2(f2(x[2 * y], x[2 * y + 1]), f2(a[2 * y], a[2 * y + 1])),
+                                              x[2 * y], x[2 * y + 1]);
+            // causal mask, only where the tile reaches past the diagonal of this warp
+            if (j0 + BN - 1 > p.M + i0 + 32 * quarter) {
+                const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
+#pragma unroll
+                for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
+            }
+            // row max as a tree of 3-input maxima (short dependency chains)
+            float m1[22];
+#pragma unroll
+            for (int y = 0; y < 21; ++y) m1[y] = max3(x[3 * y], x[3 * y + 1], x[3 * y + 2]);
+            m1[21] = x[63];
+            float m2[8];
+#pragma unroll
+            for (int y = 0; y < 7; ++y) m2[y] = max3(m1[3 * y], m1[3 * y + 1], m1[3 * y + 2]);
+            m2[7] = m1[21];
+            const float tmax = max3(max3(m2[0], m2[1], m2[2]), max3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+            float alpha = 1.f;
+            const bool raise = tmax > m_used + RESCALE_LOG2;
+            if (raise) {
+                alpha = ex2(m_used - tmax);        // 0 on the first raise (m_used = -inf)
+                m_used = tmax;
+            }
+            if (n > 0 && __any_sync(0xffffffffu, raise)) {
+                // O holds P.V of earlier tiles: wait until the last one landed
+                if (!wwait(S::B_PV + ((n - 1) % NSBUF), ((n - 1) / NSBUF) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < DP / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(tl + TM_O + 16 * c, o);
+#pragma unroll
+                    for (int y = 0; y < 16; ++y) o[y] *= alpha;
+                    tmem_st16(tl + TM_O + 16 * c, o);
+                }
+            }
+            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+            const uint64_t mu2 = f2(mu, mu);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // four packed partial sums
+            float pk[32];
+#pragma unroll
+            for (int y = 0; y < 32; ++y) {
+                float d0, d1;
+                unf2(sub2(f2(x[2 * y], x[2 * y + 1]), mu2), d0, d1);
+                const float p0 = ex2(d0), p1 = ex2(d1);
+                acc[y & 3] = add2(acc[y & 3], f2(p0, p1));
+                pk[y] = __uint_as_float(pack_bf16(p0, p1));
+            }
+            float s0, s1;
+            unf2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+            l_run = l_run * alpha + (s0 + s1);
+            tmem_st32(tl + TM_S + 64 * sb, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(S::B_P + sb));
+        }
+
+        // ---- epilogue
+        if (ok && wwait(S::B_O, 0)) {
+            tc_fence_after();
+            float o[DP];
+#pragma unroll
+            for (int c = 0; c < DP / 16; ++c)
+                tmem_ld16(tl + TM_O + 16 * c, *reinterpret_cast<float(*)[16]>(&o[16 * c]));
+            if (row_valid) {
+                if (p.splits == 1) {
+                    const float inv = 1.f / l_run;
+                    __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off;
+                    if ((p.D & 7) == 0) {
+#pragma unroll
+                        for (int d8 = 0; d8 < DP / 8; ++d8) {
+                            if (d8 * 8 < p.D) {
+                                uint4 pk4;
+                                pk4.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
+                                pk4.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
+                                pk4.z = pack_bf16(o[d8 * 8 + 4] * inv, o[d8 * 8 + 5] * inv);
+                                pk4.w = pack_bf16(o[d8 * 8 + 6] * inv, o[d8 * 8 + 7] * inv);
+                                *reinterpret_cast<uint4 *>(op + d8 * 8) = pk4;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int d = 0; d < DP; ++d)
+                            if (d < p.D) op[d] = __float2bfloat16(o[d] * inv);
+                    }
+                } else {
+                    const long prow = ((long)split * p.B * p.H + bh) * p.L + i;
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                    float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP);
+#pragma unroll
+                    for (int d4 = 0; d4 < DP / 4; ++d4)
+                        po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
+                                             o[4 * d4 + 3] * inv);
+                    // m_used is in log2 units of the scaled logits
+                    p.part_lse[prow] = l_run > 0.f ? m_used + log2f(l_run) : -INFINITY;
+                }
             }
         }
     }
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
     }
@@ -557,13 +672,14 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
     const long ctas = (long)a.B * a.H * nqt;
     const int ntile = (a.M + a.L + BN - 1) / BN;     // key tiles of the last query tile
     // choose the split count that minimises (waves x tiles per split), with a
-    // small charge for the combine pass; 1 when the grid already fills the GPU
+    // charge for the partials and the combine pass; 1 when the grid already
+    // fills the GPU
     double best = 1e30;
     int best_s = 1;
     for (int s = 1; s <= 16 && s <= ntile; ++s) {
         const long waves = (ctas * s + num_sms - 1) / num_sms;
         const int per = (ntile + s - 1) / s;
-        const double cost = (double)waves * per + (s > 1 ? 1.0 : 0.0);
+        const double cost = (double)waves * (per + 2) + (s > 1 ? 2.0 : 0.0);
         if (cost < best - 1e-9) {
             best = cost;
             best_s = s;
@@ -615,7 +731,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
         const long bhn = (long)a.B * a.H;
         const long rs = bhn * a.D;
         if (!make_map(&mk, a.k, p.T, rs, a.D, bhn, BN) || !make_map(&mv, a.v, p.T, rs, a.D, bhn, BN) ||
-            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.D, a.H, RWIN))
+            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.D, a.H, BN))
             return cudaErrorInvalidValue;
     }
     cudaError_t e;

@@ -148,6 +148,19 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.  A is M x K with
+// row m in TMEM lane m and two 16-bit elements per 32-bit column.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 async op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -176,6 +189,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
           "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+
+// Five 32-column loads (S: two; band window: three) issued back to back with
+// one wait at the end; all 160 registers are outputs of this one statement,
+// so nothing reads them before the wait.
+__device__ __forceinline__ void tmem_ld_5x32(uint32_t s0, uint32_t s1, uint32_t b0, uint32_t b1,
+                                             uint32_t b2, float (&x)[64], float (&a)[96])
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(x);
+    uint32_t *q = reinterpret_cast<uint32_t *>(a);
+#define TXL_R8(p, o) "=r"(p[o]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3]), "=r"(p[o + 4]), \
+                     "=r"(p[o + 5]), "=r"(p[o + 6]), "=r"(p[o + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%160];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%161];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%162];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%163];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%128,%129,%130,%131,%132,%133,%134,%135,%136,%137,%138,%139,%140,%141,%142,%143,"
+        "%144,%145,%146,%147,%148,%149,%150,%151,%152,%153,%154,%155,%156,%157,%158,%159}, [%164];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TXL_R8(r, 0), TXL_R8(r, 8), TXL_R8(r, 16), TXL_R8(r, 24), TXL_R8(r, 32), TXL_R8(r, 40),
+          TXL_R8(r, 48), TXL_R8(r, 56), TXL_R8(q, 0), TXL_R8(q, 8), TXL_R8(q, 16), TXL_R8(q, 24),
+          TXL_R8(q, 32), TXL_R8(q, 40), TXL_R8(q, 48), TXL_R8(q, 56), TXL_R8(q, 64), TXL_R8(q, 72),
+          TXL_R8(q, 80), TXL_R8(q, 88)
+        : "r"(s0), "r"(s1), "r"(b0), "r"(b1), "r"(b2)
+        : "memory");
+#undef TXL_R8
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
