@@ -8,20 +8,24 @@
 // One CTA owns 128 query rows of one (b, h) -- or one key-range split of them
 // -- and walks its keys in tiles of 64.  Six warps with fixed roles:
 //   warp 0    producer: TMA loads of K, V and one 64-row chunk of the table
-//             per tile into a four-stage shared-memory ring (threads' loads
-//             when D is not a multiple of 8: rows are then not 16-byte
-//             aligned and TMA cannot address them);
-//   warp 1    MMA issuer (one thread): per tile, S = (q+u) K^T into one of
+//             per tile into a seven-stage shared-memory ring, 128-byte rows
+//             with the 128-byte swizzle (threads' coalesced loads for head
+//             sizes other than 64);
+//   warp 1    S-MMA issuer (one thread): per tile, S = (q+u) K^T into one of
 //             three TMEM S buffers and the next band chunk B~ = (q+v) Q_chunk^T
-//             into a 4-slot TMEM ring; then O += P V for the previous tile.
-//             q+u, q+v, K, the table and V come from shared memory, P is a
-//             TMEM A operand;
+//             into a 4-slot TMEM ring, as far ahead as the buffers allow;
+//   warp 6    P.V issuer (one thread): O += P V as each tile's P arrives
+//             (two issuers, so neither kind of MMA waits on the other's
+//             barrier).  q+u, q+v, K, the table and V come from shared
+//             memory, P is a TMEM A operand;
 //   warps 2-5 softmax, one query row per thread (TMEM lane = row): each tile
-//             reads S and the band window its warp needs, aligns the band to
-//             the row (Appendix B's left shift of row i by L-1-i, done as a
-//             register barrel shift by 31-lane), adds, masks j <= M+i, and
-//             runs the online softmax in the log2 domain.  P (bf16) goes back
-//             into the S buffer's TMEM columns for the P.V MMA.
+//             is two independent 32-key halves; each half reads its S part
+//             and the band window it needs, aligns the band to the row
+//             (Appendix B's left shift of row i by L-1-i, done as a register
+//             barrel shift by 31-lane; three stages as selects on the ALU,
+//             two as exact arithmetic selects on the FMA pipe), adds, masks
+//             j <= M+i, and runs the online softmax in the log2 domain.  P
+//             (bf16) goes back into the S buffer's TMEM columns for P.V.
 // Appendix B's table product is formed once per 64-row chunk: tile n uses
 // chunks n, n+1, n+2 of the band, and computes chunk n+2 itself, so the
 // position term costs the same tensor work as the content term.  The MMAs of
@@ -51,8 +55,8 @@ using namespace sm100;
 constexpr int BM = 128;           // query rows per CTA (TMEM lanes)
 constexpr int BN = 64;            // keys per tile; also table rows per band chunk
 constexpr int NCHUNK = 4;         // TMEM band-chunk ring
-constexpr int NSTAGE = 4;         // shared-memory ring of (K, V, table chunk) tiles
-constexpr int NT = 192;           // 6 warps
+constexpr int NSTAGE = 7;         // shared-memory ring of (K, V, table chunk) tiles
+constexpr int NT = 224;           // 7 warps: producer, S-MMA issuer, 4 softmax, P.V issuer
 constexpr int NSBUF = 3;          // S buffers (P aliases the first 32 columns of each)
 constexpr uint32_t TM_S = 0;      // 3 x 64 columns
 constexpr uint32_t TM_BAND = 192; // band ring, 4 x 64 columns
@@ -73,25 +77,29 @@ struct Params {
     float sl2;          // log2(e) / sqrt(D)
 };
 
+// Every operand tile in shared memory uses 128-byte rows with the 128-byte
+// swizzle (element (row, k) at sw128_offset(row, k)); D <= 64 fits one row.
 template <int DP>
 struct Smem {
-    static constexpr uint32_t TILE = BN * DP * 2;          // one K, V or table chunk
+    static constexpr uint32_t TILE = BN * 128;             // one K, V or table chunk
     static constexpr uint32_t STAGE = 3 * TILE;             // K, V, chunk
     static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
     static constexpr uint32_t PRE = NSTAGE * STAGE;         // table chunks 0 and 1
-    static constexpr uint32_t QU = PRE + 2 * TILE;          // q+u, q+v: [d/8][128][8] bf16
-    static constexpr uint32_t QV = QU + BM * DP * 2;
-    static constexpr uint32_t BARS = QV + BM * DP * 2;
+    static constexpr uint32_t QU = PRE + 2 * TILE;          // q+u, q+v: 128 rows of 128 bytes
+    static constexpr uint32_t QV = QU + BM * 128;
+    static constexpr uint32_t XCH = QV + BM * 128;          // [2 parity][2 half][128] row maxima
+    static constexpr uint32_t XL = XCH + 2 * 2 * BM * 4;    // [2 half][128] row sums
+    static constexpr uint32_t BARS = XL + 2 * BM * 4;
     // barrier slots (8 bytes each): stage full / empty, S full, P full,
-    // P.V done, O done
+    // P.V done, O done, and one exchange barrier per TMEM lane quarter
     static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE,
                          B_S = 2 + 2 * NSTAGE, B_P = B_S + NSBUF, B_PV = B_P + NSBUF,
-                         B_O = B_PV + NSBUF;
-    static constexpr uint32_t MISC = BARS + 24 * 8;         // tmem holder, abort flag
+                         B_O = B_PV + NSBUF, B_X = B_O + 1;
+    static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
-    // at least 120 KB so that only one CTA fits on an SM: each CTA takes all
-    // 512 TMEM columns
-    static constexpr uint32_t TOTAL = USED > 120 * 1024 ? USED : 120 * 1024;
+    // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
+    // so that only one CTA fits on an SM: each CTA takes all 512 TMEM columns
+    static constexpr uint32_t TOTAL = USED + 1024 > 120 * 1024 ? USED + 1024 : 120 * 1024;
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -161,9 +169,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Warp-cooperative load of `nrows` rows of D bf16 elements into the
-// [d/8][nrows][8] layout, for D not a multiple of 8 (rows are then not
-// 16-byte aligned and TMA cannot address them).  Each row is read as aligned
+// Warp-cooperative load of `nrows` rows of D bf16 elements into the 128-byte
+// swizzled row layout, for head sizes TMA does not load (D != 64; D not a
+// multiple of 8 also leaves rows that are not 16-byte aligned).  Each row is read as aligned
 // 32-bit words, one per lane (coalesced); a row that starts in the middle of a
 // word is realigned with a funnel shift from the next lane's word.  Rows
 // outside [0, limit) are written as zeros; element D (the first padding
@@ -187,8 +195,7 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
         const uint32_t wn = __shfl_down_sync(0xffffffffu, w, 1);
         uint32_t pair = odd ? __byte_perm(w, wn, 0x5432) : w;      // elements 2l, 2l+1
         if (2 * lane + 1 == D) pair &= 0xFFFFu;                      // zero the padding element
-        if (lane < npairs)
-            *reinterpret_cast<uint32_t *>(dst + (lane >> 2) * (nrows * 16) + rr * 16 + (lane & 3) * 4) = pair;
+        if (lane < npairs) *reinterpret_cast<uint32_t *>(dst + sw128_offset(rr, 2 * lane)) = pair;
     }
 }
 
@@ -198,7 +205,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_r, const Params p)
 {
     using S = Smem<DP>;
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- which (b, h, query tile, key split) this CTA owns; late (heavier)
@@ -257,6 +266,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             mbar_init(bar(S::B_PV + x), 1);
         }
         mbar_init(bar(S::B_O), 1);
+        for (int x = 0; x < 4; ++x) mbar_init(bar(S::B_X + x), 64);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -264,14 +274,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             prefetch_tmap(&tm_r);
         }
     }
-    // the padding slice of D (rounded up to 16 for the MMA K dimension) must be
-    // zero in every K / V / table buffer: loads never write it
-    if ((p.D & 15) != 0) {
-        for (int tile = 0; tile < 3 * NSTAGE + 2; ++tile) {
-            unsigned char *base = smem + S::ST0 + tile * S::TILE;   // stages, then the two pre chunks
-            for (int sl = p.D >> 3; sl < DP / 8; ++sl)
-                for (int x = tid; x < BN * 4; x += NT) reinterpret_cast<uint32_t *>(base + sl * BN * 16)[x] = 0u;
-        }
+    // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
+    // every operand buffer, and loads never write it: clear everything once
+    if (p.D != DP) {
+        for (uint32_t x = tid; x < S::XCH / 16; x += NT)
+            reinterpret_cast<uint4 *>(smem)[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -281,13 +288,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
     if (warp == 0) {
         // =============================================================== producer
-        const uint32_t tile_bytes = (uint32_t)BN * (uint32_t)(p.D / 8) * 16u;
+        const uint32_t tile_bytes = (uint32_t)BN * 128u;     // TMA only for D = 64
         // table chunks 0 and 1 for the first tile
         if (kTma) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(S::B_PRE), 2 * tile_bytes);
-                tma_load_4d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, 0, h);
-                tma_load_4d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, 0, h);
+                tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, h);
+                tma_load_3d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, h);
             }
         } else {
             warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
@@ -306,9 +313,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             if (kTma) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar(S::B_FULL + st), 3 * tile_bytes);
-                    tma_load_4d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, 0, bh);
-                    tma_load_4d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, 0, bh);
-                    tma_load_4d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, 0, h);
+                    tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, bh);
+                    tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, bh);
+                    tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, h);
                 }
             } else {
                 unsigned char *d = smem + S::ST0 + st * S::STAGE;
@@ -319,79 +326,79 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 mbar_arrive(bar(S::B_FULL + st));
             }
         }
-    } else if (warp == 1) {
-        // =============================================================== MMA issuer
+    } else if (warp == 1 || warp == 6) {
+        // =============================================================== MMA issuers
         const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
         const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
         bool ok = wwait(S::B_Q, 0) && wwait(S::B_PRE, 0);
         tc_fence_after();
-        const uint32_t a_qu = sbase + S::QU, a_qv = sbase + S::QV;
-        if (ok && lane == 0) {
+        // descriptors built once; the 14-bit start-address field (address / 16)
+        // advances by 2 per 32-byte K step within a 128-byte swizzled row
+        const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
+        const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
+        const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
+        const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+        constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
+        if (ok && lane == 0 && warp == 1) {
             for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
-                const uint32_t bsm = sbase + S::PRE + c * S::TILE;
 #pragma unroll
                 for (int ks = 0; ks < DP / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_BAND + 64 * c, smem_desc(a_qv + ks * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(bsm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
+                    mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
+                                idesc_64, ks > 0);
             }
         }
         __syncwarp();
-        for (int n = 0; ok && n < N; ++n) {
+        // S and band MMAs of tile n (into S buffer n % NSBUF, band slot (n+2) % 4)
+        auto issue_s = [&](int n) -> bool {
             const int sb = n % NSBUF;
             const int st = n % NSTAGE;
-            // S buffer sb last held P of tile n-NSBUF: its P.V must be done
-            if (n >= NSBUF) ok = wwait(S::B_PV + sb, ((n / NSBUF) - 1) & 1);
-            ok = ok && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
+            // the S buffer last held P of tile n-NSBUF: its P.V must be done;
+            // band slot (n+2) % 4 was last read by the softmax of tile n-2:
+            // its P must be written
+            bool good = true;
+            if (n >= NSBUF) good = wwait(S::B_PV + sb, ((n / NSBUF) - 1) & 1);
+            if (n >= 2) good = good && wwait(S::B_P + (n - 2) % NSBUF, ((n - 2) / NSBUF) & 1);
+            good = good && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
             tc_fence_after();
-            if (ok && lane == 0) {
-                const uint32_t ksm = sbase + S::ST0 + st * S::STAGE;
-                const uint32_t csm = ksm + 2 * S::TILE;
-                const uint32_t slot = (uint32_t)((n + 2) % NCHUNK);
+            if (good && lane == 0) {
+                const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
+                const uint32_t ts = tmem + TM_S + 64 * sb;
+                const uint32_t tb = tmem + TM_BAND + 64 * (uint32_t)((n + 2) % NCHUNK);
 #pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_S + 64 * sb, smem_desc(a_qu + ks * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(ksm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
+                for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(ts, d_qu + 2 * ks, dk + 2 * ks, idesc_64, ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_BAND + 64 * slot, smem_desc(a_qv + ks * 2 * BM * 16, BM * 16, 128),
-                                smem_desc(csm + ks * 2 * BN * 16, BN * 16, 128), idesc_64, ks > 0);
+                for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_64, ks > 0);
                 mma_commit(bar(S::B_S + sb));
             }
             __syncwarp();
-            if (ok && n >= 1) {   // P.V of the previous tile
-                const int pb = (n - 1) % NSBUF;
-                ok = wwait(S::B_P + pb, ((n - 1) / NSBUF) & 1);
-                tc_fence_after();
-                if (ok && lane == 0) {
-                    const int pst = (n - 1) % NSTAGE;
-                    const uint32_t vsm = sbase + S::ST0 + pst * S::STAGE + S::TILE;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_S + 64 * pb + 8 * kk,
-                                    smem_desc(vsm + kk * 16 * 16, 128, BN * 16), idesc_o,
-                                    (n - 1 > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(S::B_PV + pb));
-                    mma_commit(bar(S::B_EMPTY + pst));
-                }
-                __syncwarp();
-            }
-        }
-        if (ok) {   // P.V of the last tile, then release the epilogue
-            const int pb = (N - 1) % NSBUF;
-            ok = wwait(S::B_P + pb, ((N - 1) / NSBUF) & 1);
+            return good;
+        };
+        // P.V of tile n, once its softmax has written P
+        auto issue_pv = [&](int n) -> bool {
+            const int pb = n % NSBUF;
+            const int pst = n % NSTAGE;
+            const bool good = wwait(S::B_P + pb, (n / NSBUF) & 1);
             tc_fence_after();
-            if (ok && lane == 0) {
-                const int pst = (N - 1) % NSTAGE;
-                const uint32_t vsm = sbase + S::ST0 + pst * S::STAGE + S::TILE;
+            if (good && lane == 0) {
+                const uint64_t dv = d_st0 + pst * STAGE16 + TILE16;
+                const uint32_t tp = tmem + TM_S + 64 * pb;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_S + 64 * pb + 8 * kk,
-                                smem_desc(vsm + kk * 16 * 16, 128, BN * 16), idesc_o,
-                                (N - 1 > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 swizzled rows = 2048 bytes
+                    mma_bf16_ts(tmem + TM_O, tp + 8 * kk, dv + 128 * kk, idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(S::B_PV + pb));
-                mma_commit(bar(S::B_O));
+                mma_commit(bar(S::B_EMPTY + pst));
+                if (n == N - 1) mma_commit(bar(S::B_O));
             }
             __syncwarp();
+            return good;
+        };
+        // this warp issues the S and band MMAs as far ahead as the S buffers
+        // allow; warp 6 issues the P.V MMAs as each P arrives, so neither
+        // kind of MMA waits behind the other's barrier
+        if (warp == 1) {
+            for (int n = 0; ok && n < N; ++n) ok = issue_s(n);
+        } else {
+            for (int n = 0; ok && n < N; ++n) ok = issue_pv(n);
         }
     } else {
         // =============================================================== softmax
@@ -401,7 +408,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const bool row_valid = ii < rows_here;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
 
-        // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into TMEM
+        // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into
+        // shared memory as the A operands of the content and band MMAs
         {
             float qrow[DP];
 #pragma unroll
@@ -425,7 +433,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
             }
             const float *up = p.u + h * p.D, *wp = p.w + h * p.D;
-            // row ii of the [d/8][128][8] operand tiles: one 16-byte store per slice
+            // row ii of the swizzled operand tiles: one 16-byte store per 8 elements
 #pragma unroll
             for (int d8 = 0; d8 < DP / 8; ++d8) {
                 uint32_t a4[4], c4[4];
@@ -438,9 +446,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     a4[z] = pack_bf16((qrow[d] + u0) * p.sl2, (qrow[d + 1] + u1) * p.sl2);
                     c4[z] = pack_bf16((qrow[d] + w0) * p.sl2, (qrow[d + 1] + w1) * p.sl2);
                 }
-                *reinterpret_cast<uint4 *>(smem + S::QU + d8 * (BM * 16) + ii * 16) =
+                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
-                *reinterpret_cast<uint4 *>(smem + S::QV + d8 * (BM * 16) + ii * 16) =
+                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ii, 8 * d8)) =
                     make_uint4(c4[0], c4[1], c4[2], c4[3]);
             }
             fence_proxy_async_smem();
@@ -449,6 +457,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
         float m_used = -INFINITY, l_run = 0.f;
         const int shift = 31 - lane;
+        // per-row select masks of the two low barrel stages, done on the FMA
+        // pipe as exact m*b + (1-m)*a (the band values are finite)
+        const float m2 = (shift & 2) ? 1.f : 0.f, n2 = 1.f - m2;
+        const float m1 = (shift & 1) ? 1.f : 0.f, n1 = 1.f - m1;
         bool ok = true;
         for (int n = 0; n < N; ++n) {
             const int sb = n % NSBUF;
@@ -458,82 +470,96 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 break;
             }
             tc_fence_after();
-            float x[64], a[96];
-            uint32_t bcol[3];
+            // mask needed only where this warp's rows meet the diagonal
+            const bool diag = j0 + BN - 1 > p.M + i0 + 32 * quarter;
+            const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
+            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+            float xs[64];            // scaled logits of the tile's 64 keys
+            float pk[32];            // bf16 pairs of P
+            float tmax = -INFINITY, psum = 0.f;
+            // two independent 32-key halves: the scheduler can run one half's
+            // shift (ALU) while the other's exponentials (MUFU) run; the
+            // exponentials use the current running max and are redone below
+            // in the rare case that the max has to be raised
 #pragma unroll
-            for (int pc = 0; pc < 3; ++pc) {
-                const int rel = 96 - 32 * quarter + 32 * pc;           // column in chunks n..n+2
-                bcol[pc] = TM_BAND + 64 * (uint32_t)((n + (rel >> 6)) % NCHUNK) + (rel & 63);
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[32], a[64];
+                {
+                    const int rel = 96 - 32 * quarter + 32 * hf;   // window start in chunks n..n+2
+                    const int rel1 = rel + 32;
+                    const uint32_t c0 = TM_BAND + 64 * (uint32_t)((n + (rel >> 6)) % NCHUNK) + (rel & 63);
+                    const uint32_t c1 = TM_BAND + 64 * (uint32_t)((n + (rel1 >> 6)) % NCHUNK) + (rel1 & 63);
+                    tmem_ld_3x32(tl + TM_S + 64 * sb + 32 * hf, tl + c0, tl + c1, x, a);
+                }
+                // row ii reads band column 127-ii+jj: a warp-uniform start plus 31-lane
+#pragma unroll
+                for (int y = 0; y < 47; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
+#pragma unroll
+                for (int y = 0; y < 39; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
+#pragma unroll
+                for (int y = 0; y < 35; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
+#pragma unroll
+                for (int y = 0; y < 33; ++y) a[y] = fmaf(m2, a[y + 2], n2 * a[y]);
+#pragma unroll
+                for (int y = 0; y < 32; ++y) a[y] = fmaf(m1, a[y + 1], n1 * a[y]);
+#pragma unroll
+                for (int y = 0; y < 32; ++y) x[y] += a[y];
+                if (diag) {
+#pragma unroll
+                    for (int y = 0; y < 32; ++y) x[y] = (32 * hf + y <= lim) ? x[y] : -INFINITY;
+                }
+                float q1[11];
+#pragma unroll
+                for (int y = 0; y < 10; ++y) q1[y] = max3(x[3 * y], x[3 * y + 1], x[3 * y + 2]);
+                q1[10] = fmaxf(x[30], x[31]);
+                const float hmax = max3(max3(q1[0], q1[1], q1[2]), max3(q1[3], q1[4], q1[5]),
+                                        max3(q1[6], q1[7], max3(q1[8], q1[9], q1[10])));
+                tmax = fmaxf(tmax, hmax);
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int y = 0; y < 16; ++y) {
+                    const float p0 = ex2(x[2 * y] - mu), p1 = ex2(x[2 * y + 1] - mu);
+                    sacc[y & 3] += p0 + p1;
+                    pk[16 * hf + y] = __uint_as_float(pack_bf16(p0, p1));
+                }
+                psum += (sacc[0] + sacc[1]) + (sacc[2] + sacc[3]);
+#pragma unroll
+                for (int y = 0; y < 32; ++y) xs[32 * hf + y] = x[y];
             }
-            tmem_ld_5x32(tl + TM_S + 64 * sb, tl + TM_S + 64 * sb + 32, tl + bcol[0], tl + bcol[1],
-                         tl + bcol[2], x, a);
-            // row ii reads band column 127-ii+jj: a warp-uniform start plus 31-lane
-#pragma unroll
-            for (int y = 0; y < 79; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
-#pragma unroll
-            for (int y = 0; y < 71; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
-#pragma unroll
-            for (int y = 0; y < 67; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
-#pragma unroll
-            for (int y = 0; y < 65; ++y) a[y] = (shift & 2) ? a[y + 2] : a[y];
-#pragma unroll
-            for (int y = 0; y < 64; ++y) a[y] = (shift & 1) ? a[y + 1] : a[y];
-#pragma unroll
-            for (int y = 0; y < 32; ++y) unf2(add2(f2(x[2 * y], x[2 * y + 1]), f2(a[2 * y], a[2 * y + 1])),
-                                              x[2 * y], x[2 * y + 1]);
-            // causal mask, only where the tile reaches past the diagonal of this warp
-            if (j0 + BN - 1 > p.M + i0 + 32 * quarter) {
-                const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
-#pragma unroll
-                for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
-            }
-            // row max as a tree of 3-input maxima (short dependency chains)
-            float m1[22];
-#pragma unroll
-            for (int y = 0; y < 21; ++y) m1[y] = max3(x[3 * y], x[3 * y + 1], x[3 * y + 2]);
-            m1[21] = x[63];
-            float m2[8];
-#pragma unroll
-            for (int y = 0; y < 7; ++y) m2[y] = max3(m1[3 * y], m1[3 * y + 1], m1[3 * y + 2]);
-            m2[7] = m1[21];
-            const float tmax = max3(max3(m2[0], m2[1], m2[2]), max3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
             float alpha = 1.f;
             const bool raise = tmax > m_used + RESCALE_LOG2;
-            if (raise) {
-                alpha = ex2(m_used - tmax);        // 0 on the first raise (m_used = -inf)
-                m_used = tmax;
-            }
-            if (n > 0 && __any_sync(0xffffffffu, raise)) {
-                // O holds P.V of earlier tiles: wait until the last one landed
-                if (!wwait(S::B_PV + ((n - 1) % NSBUF), ((n - 1) / NSBUF) & 1)) {
-                    ok = false;
-                    break;
+            if (__any_sync(0xffffffffu, raise)) {
+                // rare: the running max moves; redo this tile's exponentials
+                if (raise) {
+                    alpha = ex2(m_used - tmax);        // 0 on the first raise (m_used = -inf)
+                    m_used = tmax;
                 }
-                tc_fence_after();
+                const float mu2 = (m_used == -INFINITY) ? 0.f : m_used;
+                psum = 0.f;
 #pragma unroll
-                for (int c = 0; c < DP / 16; ++c) {
-                    float o[16];
-                    tmem_ld16(tl + TM_O + 16 * c, o);
+                for (int y = 0; y < 32; ++y) {
+                    const float p0 = ex2(xs[2 * y] - mu2), p1 = ex2(xs[2 * y + 1] - mu2);
+                    psum += p0 + p1;
+                    pk[y] = __uint_as_float(pack_bf16(p0, p1));
+                }
+                if (n > 0) {
+                    // O holds P.V of earlier tiles: wait until the last one landed
+                    if (!wwait(S::B_PV + ((n - 1) % NSBUF), ((n - 1) / NSBUF) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                    for (int y = 0; y < 16; ++y) o[y] *= alpha;
-                    tmem_st16(tl + TM_O + 16 * c, o);
+                    for (int c = 0; c < DP / 16; ++c) {
+                        float o[16];
+                        tmem_ld16(tl + TM_O + 16 * c, o);
+#pragma unroll
+                        for (int y = 0; y < 16; ++y) o[y] *= alpha;
+                        tmem_st16(tl + TM_O + 16 * c, o);
+                    }
                 }
             }
-            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-            const uint64_t mu2 = f2(mu, mu);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // four packed partial sums
-            float pk[32];
-#pragma unroll
-            for (int y = 0; y < 32; ++y) {
-                float d0, d1;
-                unf2(sub2(f2(x[2 * y], x[2 * y + 1]), mu2), d0, d1);
-                const float p0 = ex2(d0), p1 = ex2(d1);
-                acc[y & 3] = add2(acc[y & 3], f2(p0, p1));
-                pk[y] = __uint_as_float(pack_bf16(p0, p1));
-            }
-            float s0, s1;
-            unf2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-            l_run = l_run * alpha + (s0 + s1);
+            l_run = l_run * alpha + psum;
             tmem_st32(tl + TM_S + 64 * sb, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -631,20 +657,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-// 4-D view {8, rows, D/8, groups} of a bf16 tensor whose rows are `row_stride`
-// elements apart and whose groups (b*H+h or h) are D elements apart; the box
-// {8, box_rows, D/8, 1} lands in shared memory as [d/8][box_rows][8].
-bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, int D, long groups,
-              int box_rows)
+// 3-D view {64, rows, groups} of a bf16 tensor with D = 64 elements per row,
+// rows `row_stride` elements apart and groups (b*H+h or h) 64 elements apart;
+// the box {64, box_rows, 1} lands in shared memory as 128-byte rows with the
+// 128-byte swizzle (the layout the MMA descriptors expect).
+bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long groups, int box_rows)
 {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[4] = {8, (cuuint64_t)rows, (cuuint64_t)(D / 8), (cuuint64_t)groups};
-    cuuint64_t strides[3] = {(cuuint64_t)row_stride * 2, 16, (cuuint64_t)D * 2};
-    cuuint32_t box[4] = {8, (cuuint32_t)box_rows, (cuuint32_t)(D / 8), 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)groups};
+    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, 64 * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -726,12 +752,12 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
     memset(&mr, 0, sizeof(mr));
-    const bool tma = (a.D % 8) == 0;
+    const bool tma = a.D == 64;
     if (tma) {
         const long bhn = (long)a.B * a.H;
         const long rs = bhn * a.D;
-        if (!make_map(&mk, a.k, p.T, rs, a.D, bhn, BN) || !make_map(&mv, a.v, p.T, rs, a.D, bhn, BN) ||
-            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.D, a.H, BN))
+        if (!make_map(&mk, a.k, p.T, rs, bhn, BN) || !make_map(&mv, a.v, p.T, rs, bhn, BN) ||
+            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN))
             return cudaErrorInvalidValue;
     }
     cudaError_t e;

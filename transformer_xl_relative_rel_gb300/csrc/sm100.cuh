@@ -82,6 +82,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                            int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -122,6 +132,29 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     d |= (uint64_t)1 << 46;          // descriptor version for tcgen05
     // base offset 0, absolute-LBO mode off, swizzle mode 0 (none)
     return d;
+}
+
+// Shared-memory matrix descriptor for the 128-byte swizzled layout: rows of
+// 128 bytes, 8-row atoms of 1024 bytes (1024-byte aligned), the 16-byte chunk c
+// of row r stored at chunk position c ^ (r % 8).  sbo: distance between
+// 8-row atoms; lbo: distance between atoms along the other dimension (unused
+// when the operand is one atom wide there).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;          // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;          // swizzle mode: 128 bytes
+    return d;
+}
+
+// Byte offset of element (row, k) of a bf16 operand stored with 128-byte rows
+// and the 128-byte swizzle.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k)
+{
+    return row * 128u + ((((k * 2u) >> 4) ^ (row & 7u)) << 4) + ((k * 2u) & 15u);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulation.
@@ -225,6 +258,37 @@ __device__ __forceinline__ void tmem_ld_5x32(uint32_t s0, uint32_t s1, uint32_t 
         : "r"(s0), "r"(s1), "r"(b0), "r"(b1), "r"(b2)
         : "memory");
 #undef TXL_R8
+}
+
+// One 32-column load (S) and two 32-column loads (band window) with one wait.
+__device__ __forceinline__ void tmem_ld_3x32(uint32_t s0, uint32_t b0, uint32_t b1, float (&x)[32],
+                                             float (&a)[64])
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(x);
+    uint32_t *q = reinterpret_cast<uint32_t *>(a);
+#define TXL_R8(p, o) "=r"(p[o]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3]), "=r"(p[o + 4]), \
+                     "=r"(p[o + 5]), "=r"(p[o + 6]), "=r"(p[o + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%96];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%97];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TXL_R8(r, 0), TXL_R8(r, 8), TXL_R8(r, 16), TXL_R8(r, 24), TXL_R8(q, 0), TXL_R8(q, 8),
+          TXL_R8(q, 16), TXL_R8(q, 24), TXL_R8(q, 32), TXL_R8(q, 40), TXL_R8(q, 48), TXL_R8(q, 56)
+        : "r"(s0), "r"(b0), "r"(b1)
+        : "memory");
+#undef TXL_R8
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
