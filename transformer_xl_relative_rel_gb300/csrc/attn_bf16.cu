@@ -55,13 +55,14 @@ using namespace sm100;
 constexpr int BM = 128;           // query rows per CTA (TMEM lanes)
 constexpr int BN = 64;            // keys per tile; also table rows per band chunk
 constexpr int NCHUNK = 4;         // TMEM band-chunk ring
-constexpr int NSTAGE = 7;         // shared-memory ring of (K, V, table chunk) tiles
-constexpr int NT = 224;           // 7 warps: producer, S-MMA issuer, 4 softmax, P.V issuer
-constexpr int NSBUF = 3;          // S buffers (P aliases the first 32 columns of each)
-constexpr uint32_t TM_S = 0;      // 3 x 64 columns
-constexpr uint32_t TM_BAND = 192; // band ring, 4 x 64 columns
-constexpr uint32_t TM_O = 448;    // O accumulator, DP <= 64 columns
+constexpr int NSTAGE = 5;         // shared-memory ring of (K, V, table chunk) tiles
+constexpr int NT = 384;           // 12 warps, see the role list above
+constexpr uint32_t TM_S = 0;      // two S buffers (one per softmax set) of 64 columns
+constexpr uint32_t TM_BAND = 128; // band ring, 4 x 64 columns
+constexpr uint32_t TM_O = 384;    // two O accumulators (one per set), 64 columns each
 constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t REG_LOW = 96, REG_HIGH = 200;     // per-thread registers after the split
+static_assert(128 * REG_LOW + 256 * REG_HIGH <= 65536 / NT / 8 * 8 * NT, "register split exceeds the launch");
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait, then give up
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;          // raise the exponent base only past 2^8
@@ -87,14 +88,15 @@ struct Smem {
     static constexpr uint32_t PRE = NSTAGE * STAGE;         // table chunks 0 and 1
     static constexpr uint32_t QU = PRE + 2 * TILE;          // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
-    static constexpr uint32_t XCH = QV + BM * 128;          // [2 parity][2 half][128] row maxima
-    static constexpr uint32_t XL = XCH + 2 * 2 * BM * 4;    // [2 half][128] row sums
-    static constexpr uint32_t BARS = XL + 2 * BM * 4;
-    // barrier slots (8 bytes each): stage full / empty, S full, P full,
-    // P.V done, O done, and one exchange barrier per TMEM lane quarter
+    static constexpr uint32_t PB = QV + BM * 128;           // P (bf16) of each set: 128 rows x 128 bytes
+    static constexpr uint32_t XML = PB + 2 * BM * 128;      // epilogue: [128 rows] (m, l) of set 1
+    static constexpr uint32_t BARS = XML + BM * 8;
+    // barrier slots (8 bytes each): stage full / empty; per softmax set: S
+    // full, S free (read by the softmax), P full, P.V done, O done; epilogue
+    // exchange
     static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE,
-                         B_S = 2 + 2 * NSTAGE, B_P = B_S + NSBUF, B_PV = B_P + NSBUF,
-                         B_O = B_PV + NSBUF, B_X = B_O + 1;
+                         B_S = 2 + 2 * NSTAGE, B_SF = B_S + 2, B_P = B_SF + 2, B_PV = B_P + 2,
+                         B_O = B_PV + 2, B_X = B_O + 2;
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -181,21 +183,28 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
                                                int limit, int D, int lane)
 {
     const int npairs = (D + 1) >> 1;     // element pairs covering D (<= 32 for D <= 64)
-#pragma unroll 4
-    for (int rr = 0; rr < nrows; ++rr) {
-        const int row = first_row + rr;
-        const bool ok = row >= 0 && row < limit;
-        const long e0 = row0_elems + (long)row * row_stride;        // first element of the row
-        const uint32_t *wbase = reinterpret_cast<const uint32_t *>(src + (e0 & ~1L));
-        const int odd = (int)(e0 & 1);
-        // lane l holds word l (elements 2l-odd .. 2l+1-odd of the row); only the
-        // words that overlap the row are read
-        uint32_t w = 0;
-        if (ok && lane <= ((odd + D - 1) >> 1)) w = wbase[lane];
-        const uint32_t wn = __shfl_down_sync(0xffffffffu, w, 1);
-        uint32_t pair = odd ? __byte_perm(w, wn, 0x5432) : w;      // elements 2l, 2l+1
-        if (2 * lane + 1 == D) pair &= 0xFFFFu;                      // zero the padding element
-        if (lane < npairs) *reinterpret_cast<uint32_t *>(dst + sw128_offset(rr, 2 * lane)) = pair;
+    // 16 rows at a time: all their loads are issued before any is used
+    for (int r0 = 0; r0 < nrows; r0 += 16) {
+        uint32_t w[16];
+        int odd[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int row = first_row + r0 + k;
+            const bool ok = row >= 0 && row < limit;
+            const long e0 = row0_elems + (long)row * row_stride;    // first element of the row
+            odd[k] = (int)(e0 & 1);
+            // lane l reads word l of the row (elements 2l-odd .. 2l+1-odd);
+            // only the words that overlap the row are read
+            const uint32_t *wbase = reinterpret_cast<const uint32_t *>(src + (e0 & ~1L));
+            w[k] = (ok && lane <= ((odd[k] + D - 1) >> 1)) ? wbase[lane] : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t wn = __shfl_down_sync(0xffffffffu, w[k], 1);
+            uint32_t pair = odd[k] ? __byte_perm(w[k], wn, 0x5432) : w[k];   // elements 2l, 2l+1
+            if (2 * lane + 1 == D) pair &= 0xFFFFu;                            // padding element
+            if (lane < npairs) *reinterpret_cast<uint32_t *>(dst + sw128_offset(r0 + k, 2 * lane)) = pair;
+        }
     }
 }
 
@@ -224,7 +233,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int ntile = (kend + BN - 1) / BN;
     const int t0 = (int)(((long)split * ntile) / p.splits);
     const int t1 = (int)(((long)(split + 1) * ntile) / p.splits);
-    const int N = t1 - t0;                                 // tiles of this CTA
+    const int N = t1 - t0;                                 // key tiles of this CTA
     const long qkv_row = (long)p.B * p.H * p.D;            // elements between positions
     const long head_off = ((long)b * p.H + h) * p.D;
     const int kb0 = p.L - BM - i0 + t0 * BN;              // first table row of chunk 0
@@ -257,16 +266,17 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         mbar_init(bar(S::B_Q), 128);
         mbar_init(bar(S::B_PRE), kTma ? 1 : 32);
         for (int x = 0; x < NSTAGE; ++x) {
-            mbar_init(bar(S::B_FULL + x), kTma ? 1 : 32);
+            mbar_init(bar(S::B_FULL + x), kTma ? 1 : 64);
             mbar_init(bar(S::B_EMPTY + x), 1);
         }
-        for (int x = 0; x < NSBUF; ++x) {
+        for (int x = 0; x < 2; ++x) {
             mbar_init(bar(S::B_S + x), 1);
+            mbar_init(bar(S::B_SF + x), 128);
             mbar_init(bar(S::B_P + x), 128);
             mbar_init(bar(S::B_PV + x), 1);
+            mbar_init(bar(S::B_O + x), 1);
         }
-        mbar_init(bar(S::B_O), 1);
-        for (int x = 0; x < 4; ++x) mbar_init(bar(S::B_X + x), 64);
+        mbar_init(bar(S::B_X), 128);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -277,7 +287,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
     // every operand buffer, and loads never write it: clear everything once
     if (p.D != DP) {
-        for (uint32_t x = tid; x < S::XCH / 16; x += NT)
+        for (uint32_t x = tid; x < S::XML / 16; x += NT)
             reinterpret_cast<uint4 *>(smem)[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -286,131 +296,139 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // =============================================================== producer
-        const uint32_t tile_bytes = (uint32_t)BN * 128u;     // TMA only for D = 64
-        // table chunks 0 and 1 for the first tile
-        if (kTma) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(S::B_PRE), 2 * tile_bytes);
-                tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, h);
-                tma_load_3d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, h);
-            }
-        } else {
-            warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
-            warp_load_rows(smem + S::PRE + S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0 + BN,
-                           p.T, p.D, lane);
-            fence_proxy_async_smem();
-            mbar_arrive(bar(S::B_PRE));
-        }
-        for (int n = 0; n < N; ++n) {
-            const int st = n % NSTAGE;
-            // the stage is free once the P.V of tile n-NSTAGE (its last reader) is done
-            if (n >= NSTAGE && !wwait(S::B_EMPTY + st, ((n / NSTAGE) - 1) & 1)) break;
-            const int j0 = (t0 + n) * BN;
-            const int crow = kb0 + (n + 2) * BN;     // table chunk n+2
-            const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
+    // warpgroup 0 (producer, issuers) gives registers to the two softmax
+    // warpgroups: 128 x 96 + 256 x 200 <= 384 x 168 (the launch allocation)
+    if (warp < 4) {
+        setmaxnreg_dec<REG_LOW>();
+        if (warp == 0 || (warp == 3 && !kTma)) {
+            // =============================================================== producer
+            // (without TMA: warp 0 loads K and the table chunks, warp 3 loads V)
+            const uint32_t tile_bytes = (uint32_t)BN * 128u;     // TMA only for D = 64
+            // table chunks 0 and 1 for the first tile
             if (kTma) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(S::B_FULL + st), 3 * tile_bytes);
-                    tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, bh);
-                    tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, bh);
-                    tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, h);
+                    mbar_arrive_expect_tx(bar(S::B_PRE), 2 * tile_bytes);
+                    tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, h);
+                    tma_load_3d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, h);
                 }
-            } else {
-                unsigned char *d = smem + S::ST0 + st * S::STAGE;
-                warp_load_rows(d, BN, p.k, head_off, qkv_row, j0, p.T, p.D, lane);
-                warp_load_rows(d + S::TILE, BN, p.v, head_off, qkv_row, j0, p.T, p.D, lane);
-                warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, crow, p.T, p.D, lane);
+            } else if (warp == 0) {
+                warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
+                warp_load_rows(smem + S::PRE + S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0 + BN,
+                               p.T, p.D, lane);
                 fence_proxy_async_smem();
-                mbar_arrive(bar(S::B_FULL + st));
+                mbar_arrive(bar(S::B_PRE));
             }
-        }
-    } else if (warp == 1 || warp == 6) {
-        // =============================================================== MMA issuers
-        const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
-        const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
-        bool ok = wwait(S::B_Q, 0) && wwait(S::B_PRE, 0);
-        tc_fence_after();
-        // descriptors built once; the 14-bit start-address field (address / 16)
-        // advances by 2 per 32-byte K step within a 128-byte swizzled row
-        const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
-        const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
-        const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
-        const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-        constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
-        if (ok && lane == 0 && warp == 1) {
-            for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks)
-                    mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
-                                idesc_64, ks > 0);
+            for (int n = 0; n < N; ++n) {
+                const int st = n % NSTAGE;
+                // the stage is free once the P.V of tile n-NSTAGE (its last reader) is done
+                if (n >= NSTAGE && !wwait(S::B_EMPTY + st, ((n / NSTAGE) - 1) & 1)) break;
+                const int j0 = (t0 + n) * BN;
+                const int crow = kb0 + (n + 2) * BN;     // table chunk n+2
+                const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
+                if (kTma) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(S::B_FULL + st), 3 * tile_bytes);
+                        tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, bh);
+                        tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, bh);
+                        tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, h);
+                    }
+                } else {
+                    unsigned char *d = smem + S::ST0 + st * S::STAGE;
+                    if (warp == 0) {
+                        warp_load_rows(d, BN, p.k, head_off, qkv_row, j0, p.T, p.D, lane);
+                        warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, crow, p.T,
+                                       p.D, lane);
+                    } else {
+                        warp_load_rows(d + S::TILE, BN, p.v, head_off, qkv_row, j0, p.T, p.D, lane);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(S::B_FULL + st));
+                }
             }
-        }
-        __syncwarp();
-        // S and band MMAs of tile n (into S buffer n % NSBUF, band slot (n+2) % 4)
-        auto issue_s = [&](int n) -> bool {
-            const int sb = n % NSBUF;
-            const int st = n % NSTAGE;
-            // the S buffer last held P of tile n-NSBUF: its P.V must be done;
-            // band slot (n+2) % 4 was last read by the softmax of tile n-2:
-            // its P must be written
-            bool good = true;
-            if (n >= NSBUF) good = wwait(S::B_PV + sb, ((n / NSBUF) - 1) & 1);
-            if (n >= 2) good = good && wwait(S::B_P + (n - 2) % NSBUF, ((n - 2) / NSBUF) & 1);
-            good = good && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
+        } else if (warp == 1) {
+            // =============================================================== S / band MMAs
+            const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
+            bool ok = wwait(S::B_Q, 0) && wwait(S::B_PRE, 0);
             tc_fence_after();
-            if (good && lane == 0) {
-                const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
-                const uint32_t ts = tmem + TM_S + 64 * sb;
-                const uint32_t tb = tmem + TM_BAND + 64 * (uint32_t)((n + 2) % NCHUNK);
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(ts, d_qu + 2 * ks, dk + 2 * ks, idesc_64, ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_64, ks > 0);
-                mma_commit(bar(S::B_S + sb));
+            // descriptors built once; the 14-bit start-address field (address / 16)
+            // advances by 2 per 32-byte K step within a 128-byte swizzled row
+            const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
+            const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
+            const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
+            const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+            constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
+            if (ok && lane == 0) {
+                for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
+    #pragma unroll
+                    for (int ks = 0; ks < DP / 16; ++ks)
+                        mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
+                                    idesc_64, ks > 0);
+                }
             }
             __syncwarp();
-            return good;
-        };
-        // P.V of tile n, once its softmax has written P
-        auto issue_pv = [&](int n) -> bool {
-            const int pb = n % NSBUF;
-            const int pst = n % NSTAGE;
-            const bool good = wwait(S::B_P + pb, (n / NSBUF) & 1);
-            tc_fence_after();
-            if (good && lane == 0) {
-                const uint64_t dv = d_st0 + pst * STAGE16 + TILE16;
-                const uint32_t tp = tmem + TM_S + 64 * pb;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)   // 16 keys = 16 swizzled rows = 2048 bytes
-                    mma_bf16_ts(tmem + TM_O, tp + 8 * kk, dv + 128 * kk, idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(S::B_PV + pb));
-                mma_commit(bar(S::B_EMPTY + pst));
-                if (n == N - 1) mma_commit(bar(S::B_O));
+            for (int n = 0; ok && n < N; ++n) {
+                const int sb = n & 1, st = n % NSTAGE;
+                // S buffer sb was last read by the softmax of tile n-2, and band
+                // slot (n+2) % 4 by the softmaxes of tiles n-4..n-2: wait for
+                // tile n-2 here (tile n-3 was waited one iteration earlier)
+                if (n >= 2) ok = wwait(S::B_SF + sb, ((n - 2) >> 1) & 1);
+                ok = ok && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
+                tc_fence_after();
+                if (ok && lane == 0) {
+                    const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
+                    const uint32_t ts = tmem + TM_S + 64 * sb;
+                    const uint32_t tb = tmem + TM_BAND + 64 * (uint32_t)((n + 2) % NCHUNK);
+    #pragma unroll
+                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(ts, d_qu + 2 * ks, dk + 2 * ks, idesc_64, ks > 0);
+    #pragma unroll
+                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_64, ks > 0);
+                    mma_commit(bar(S::B_S + sb));
+                }
+                __syncwarp();
             }
-            __syncwarp();
-            return good;
-        };
-        // this warp issues the S and band MMAs as far ahead as the S buffers
-        // allow; warp 6 issues the P.V MMAs as each P arrives, so neither
-        // kind of MMA waits behind the other's barrier
-        if (warp == 1) {
-            for (int n = 0; ok && n < N; ++n) ok = issue_s(n);
-        } else {
-            for (int n = 0; ok && n < N; ++n) ok = issue_pv(n);
+        } else if (warp == 2) {
+            // =============================================================== P.V MMAs
+            const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
+            const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+            const uint64_t d_p0 = smem_desc_sw128(sbase + S::PB, 16, 1024);
+            constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4, PB16 = (BM * 128) >> 4;
+            bool ok = true;
+            for (int n = 0; ok && n < N; ++n) {
+                const int sb = n & 1, st = n % NSTAGE;
+                ok = wwait(S::B_P + sb, (n >> 1) & 1);
+                tc_fence_after();
+                if (ok && lane == 0) {
+                    const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
+                    const uint64_t dp = d_p0 + sb * PB16;                  // 16 keys = 32 bytes of P
+                    const uint32_t to = tmem + TM_O + 64 * sb;
+    #pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_bf16_ss(to, dp + 2 * kk, dv + 128 * kk, idesc_o, (n >= 2 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_PV + sb));
+                    mma_commit(bar(S::B_EMPTY + st));
+                    if (n + 2 >= N) mma_commit(bar(S::B_O + sb));   // last tile of this set
+                }
+                __syncwarp();
+            }
         }
     } else {
+        setmaxnreg_inc<REG_HIGH>();
         // =============================================================== softmax
+        // two sets of four warps; set k takes the key tiles n = k, k+2, k+4, ...
+        // with its own S buffer and O accumulator, so the two warps that share
+        // a scheduler work on different tiles and their ALU and MUFU phases
+        // overlap; the two partial results are merged once at the end
+        const int set = (warp - 4) >> 2;
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int ii = quarter * 32 + lane;        // this thread's query row
         const int i = i0 + ii;
         const bool row_valid = ii < rows_here;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t ts = tl + TM_S + 64 * set, tb0 = tl + TM_BAND, to = tl + TM_O + 64 * set;
 
-        // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into
-        // shared memory as the A operands of the content and band MMAs
-        {
+        if (set == 0) {
+            // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into
+            // shared memory as the A operands of the content and band MMAs
             float qrow[DP];
 #pragma unroll
             for (int d = 0; d < DP; ++d) qrow[d] = 0.f;
@@ -433,7 +451,6 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
             }
             const float *up = p.u + h * p.D, *wp = p.w + h * p.D;
-            // row ii of the swizzled operand tiles: one 16-byte store per 8 elements
 #pragma unroll
             for (int d8 = 0; d8 < DP / 8; ++d8) {
                 uint32_t a4[4], c4[4];
@@ -455,127 +472,163 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             mbar_arrive(bar(S::B_Q));
         }
 
-        float m_used = -INFINITY, l_run = 0.f;
         const int shift = 31 - lane;
-        // per-row select masks of the two low barrel stages, done on the FMA
-        // pipe as exact m*b + (1-m)*a (the band values are finite)
-        const float m2 = (shift & 2) ? 1.f : 0.f, n2 = 1.f - m2;
-        const float m1 = (shift & 1) ? 1.f : 0.f, n1 = 1.f - m1;
+        // the tile's S (64 columns) and the 96-column band window its rows
+        // need, in one batch of TMEM loads: the buffers are free right after
+        auto load_tile = [&](int n, float (&x)[64], float (&a)[96]) {
+            const int rel = 96 - 32 * quarter;            // window start in chunks n..n+2
+            uint32_t c[3];
+#pragma unroll
+            for (int z = 0; z < 3; ++z) {
+                const int rz = rel + 32 * z;
+                c[z] = 64 * (uint32_t)((n + (rz >> 6)) % NCHUNK) + (rz & 63);
+            }
+            tmem_ld_5x32(ts, ts + 32, tb0 + c[0], tb0 + c[1], tb0 + c[2], x, a);
+        };
+        // scaled logits of the 64 keys: S plus the band aligned to this row
+        // (Appendix B's left shift of row i by L-1-i: row ii reads band column
+        // 127-ii+jj, a warp-uniform window start plus 31-lane), masked
+        auto logits = [&](bool diag, int lim, float (&x)[64], float (&a)[96]) {
+#pragma unroll
+            for (int y = 0; y < 80; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
+#pragma unroll
+            for (int y = 0; y < 72; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
+#pragma unroll
+            for (int y = 0; y < 68; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
+#pragma unroll
+            for (int y = 0; y < 66; ++y) a[y] = (shift & 2) ? a[y + 2] : a[y];
+#pragma unroll
+            for (int y = 0; y < 64; ++y) a[y] = (shift & 1) ? a[y + 1] : a[y];
+#pragma unroll
+            for (int y = 0; y < 64; ++y) x[y] += a[y];
+            if (diag) {
+#pragma unroll
+                for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
+            }
+        };
+        auto rowmax32 = [&](const float *x) {
+            float q1[11];
+#pragma unroll
+            for (int y = 0; y < 10; ++y) q1[y] = max3(x[3 * y], x[3 * y + 1], x[3 * y + 2]);
+            q1[10] = fmaxf(x[30], x[31]);
+            return max3(max3(q1[0], q1[1], q1[2]), max3(q1[3], q1[4], q1[5]),
+                        max3(q1[6], q1[7], max3(q1[8], q1[9], q1[10])));
+        };
+        auto expo = [&](const float *x, float mu, float *pk) {
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int y = 0; y < 16; ++y) {
+                const float p0 = ex2(x[2 * y] - mu), p1 = ex2(x[2 * y + 1] - mu);
+                sacc[y & 3] += p0 + p1;
+                pk[y] = __uint_as_float(pack_bf16(p0, p1));
+            }
+            return (sacc[0] + sacc[1]) + (sacc[2] + sacc[3]);
+        };
+
+        float m_used = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int n = 0; n < N; ++n) {
-            const int sb = n % NSBUF;
+        for (int n = set; n < N; n += 2) {
             const int j0 = (t0 + n) * BN;
-            if (!wwait(S::B_S + sb, (n / NSBUF) & 1)) {
+            if (!wwait(S::B_S + set, (n >> 1) & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // mask needed only where this warp's rows meet the diagonal
+            // the mask matters only where this warp's rows meet the diagonal
             const bool diag = j0 + BN - 1 > p.M + i0 + 32 * quarter;
             const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
-            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-            float xs[64];            // scaled logits of the tile's 64 keys
-            float pk[32];            // bf16 pairs of P
-            float tmax = -INFINITY, psum = 0.f;
-            // two independent 32-key halves: the scheduler can run one half's
-            // shift (ALU) while the other's exponentials (MUFU) run; the
-            // exponentials use the current running max and are redone below
-            // in the rare case that the max has to be raised
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float x[32], a[64];
-                {
-                    const int rel = 96 - 32 * quarter + 32 * hf;   // window start in chunks n..n+2
-                    const int rel1 = rel + 32;
-                    const uint32_t c0 = TM_BAND + 64 * (uint32_t)((n + (rel >> 6)) % NCHUNK) + (rel & 63);
-                    const uint32_t c1 = TM_BAND + 64 * (uint32_t)((n + (rel1 >> 6)) % NCHUNK) + (rel1 & 63);
-                    tmem_ld_3x32(tl + TM_S + 64 * sb + 32 * hf, tl + c0, tl + c1, x, a);
-                }
-                // row ii reads band column 127-ii+jj: a warp-uniform start plus 31-lane
-#pragma unroll
-                for (int y = 0; y < 47; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
-#pragma unroll
-                for (int y = 0; y < 39; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
-#pragma unroll
-                for (int y = 0; y < 35; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
-#pragma unroll
-                for (int y = 0; y < 33; ++y) a[y] = fmaf(m2, a[y + 2], n2 * a[y]);
-#pragma unroll
-                for (int y = 0; y < 32; ++y) a[y] = fmaf(m1, a[y + 1], n1 * a[y]);
-#pragma unroll
-                for (int y = 0; y < 32; ++y) x[y] += a[y];
-                if (diag) {
-#pragma unroll
-                    for (int y = 0; y < 32; ++y) x[y] = (32 * hf + y <= lim) ? x[y] : -INFINITY;
-                }
-                float q1[11];
-#pragma unroll
-                for (int y = 0; y < 10; ++y) q1[y] = max3(x[3 * y], x[3 * y + 1], x[3 * y + 2]);
-                q1[10] = fmaxf(x[30], x[31]);
-                const float hmax = max3(max3(q1[0], q1[1], q1[2]), max3(q1[3], q1[4], q1[5]),
-                                        max3(q1[6], q1[7], max3(q1[8], q1[9], q1[10])));
-                tmax = fmaxf(tmax, hmax);
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int y = 0; y < 16; ++y) {
-                    const float p0 = ex2(x[2 * y] - mu), p1 = ex2(x[2 * y + 1] - mu);
-                    sacc[y & 3] += p0 + p1;
-                    pk[16 * hf + y] = __uint_as_float(pack_bf16(p0, p1));
-                }
-                psum += (sacc[0] + sacc[1]) + (sacc[2] + sacc[3]);
-#pragma unroll
-                for (int y = 0; y < 32; ++y) xs[32 * hf + y] = x[y];
-            }
+            float x[64], a[96];
+            load_tile(n, x, a);
+            // S and the band window are in registers: the S buffer and the band
+            // slot may be overwritten by the next MMAs from here on
+            tc_fence_before();
+            mbar_arrive(bar(S::B_SF + set));
+            logits(diag, lim, x, a);
+            const float *x0 = x, *x1 = x + 32;
+            const float tmax = fmaxf(rowmax32(x0), rowmax32(x1));
             float alpha = 1.f;
-            const bool raise = tmax > m_used + RESCALE_LOG2;
-            if (__any_sync(0xffffffffu, raise)) {
-                // rare: the running max moves; redo this tile's exponentials
-                if (raise) {
-                    alpha = ex2(m_used - tmax);        // 0 on the first raise (m_used = -inf)
-                    m_used = tmax;
+            const bool raise = tmax > m_used + RESCALE_LOG2;   // also the first finite max
+            if (raise) {
+                alpha = ex2(m_used - tmax);                     // 0 when m_used = -inf
+                m_used = tmax;
+            }
+            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+            float pk[32];
+            const float psum = expo(x0, mu, pk) + expo(x1, mu, pk + 16);
+            l_run = l_run * alpha + psum;
+            if (n >= 2) {
+                // the set's P buffer and O are free once the P.V of its previous tile is done
+                if (!wwait(S::B_PV + set, ((n - 2) >> 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                const float mu2 = (m_used == -INFINITY) ? 0.f : m_used;
-                psum = 0.f;
-#pragma unroll
-                for (int y = 0; y < 32; ++y) {
-                    const float p0 = ex2(xs[2 * y] - mu2), p1 = ex2(xs[2 * y + 1] - mu2);
-                    psum += p0 + p1;
-                    pk[y] = __uint_as_float(pack_bf16(p0, p1));
-                }
-                if (n > 0) {
-                    // O holds P.V of earlier tiles: wait until the last one landed
-                    if (!wwait(S::B_PV + ((n - 1) % NSBUF), ((n - 1) / NSBUF) & 1)) {
-                        ok = false;
-                        break;
-                    }
+                if (__any_sync(0xffffffffu, raise)) {
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < DP / 16; ++c) {
                         float o[16];
-                        tmem_ld16(tl + TM_O + 16 * c, o);
+                        tmem_ld16(to + 16 * c, o);
 #pragma unroll
                         for (int y = 0; y < 16; ++y) o[y] *= alpha;
-                        tmem_st16(tl + TM_O + 16 * c, o);
+                        tmem_st16(to + 16 * c, o);
                     }
+                    tmem_wait_st();
                 }
             }
-            l_run = l_run * alpha + psum;
-            tmem_st32(tl + TM_S + 64 * sb, pk);
-            tmem_wait_st();
+            unsigned char *pb = smem + S::PB + set * (BM * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(pb + sw128_offset(ii, 8 * c)) =
+                    make_uint4(__float_as_uint(pk[4 * c]), __float_as_uint(pk[4 * c + 1]),
+                               __float_as_uint(pk[4 * c + 2]), __float_as_uint(pk[4 * c + 3]));
+            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(S::B_P + sb));
+            mbar_arrive(bar(S::B_P + set));
         }
 
-        // ---- epilogue
-        if (ok && wwait(S::B_O, 0)) {
-            tc_fence_after();
-            float o[DP];
+        // ---- epilogue: merge the two sets' partial results of each row
+        const bool has = set < N;                  // set 1 has no tile when N == 1
+        if (ok && has) ok = wwait(S::B_O + set, 0);
+        float o[DP];
 #pragma unroll
-            for (int c = 0; c < DP / 16; ++c)
-                tmem_ld16(tl + TM_O + 16 * c, *reinterpret_cast<float(*)[16]>(&o[16 * c]));
+        for (int d = 0; d < DP; ++d) o[d] = 0.f;
+        if (ok && has) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < DP / 16; ++c) tmem_ld16(to + 16 * c, *reinterpret_cast<float(*)[16]>(&o[16 * c]));
+        }
+        // set 1 hands (m, l, O) to set 0 through the stage ring, once every
+        // P.V of both sets (the ring's last readers) has completed
+        float *xo = reinterpret_cast<float *>(smem + S::ST0);   // [128][64] O of set 1
+        float *xml = reinterpret_cast<float *>(smem + S::XML);  // [128][2] (m, l) of set 1
+        if (set == 1 && ok) ok = wwait(S::B_O + 0, 0);
+        if (set == 1) {
+#pragma unroll
+            for (int d4 = 0; d4 < DP / 4; ++d4)
+                reinterpret_cast<float4 *>(xo + ii * 64)[d4] =
+                    make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
+            xml[2 * ii] = has ? m_used : -INFINITY;
+            xml[2 * ii + 1] = has ? l_run : 0.f;
+            mbar_arrive(bar(S::B_X));
+        } else if (ok && wwait(S::B_X, 0)) {
+            const float m1 = xml[2 * ii], l1 = xml[2 * ii + 1];
+            const float mx = fmaxf(m_used, m1);
+            const float w0 = (m_used == -INFINITY) ? 0.f : ex2(m_used - mx);
+            const float w1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mx);
+            const float l = l_run * w0 + l1 * w1;
+#pragma unroll
+            for (int d4 = 0; d4 < DP / 4; ++d4) {
+                const float4 v1 = reinterpret_cast<const float4 *>(xo + ii * 64)[d4];
+                o[4 * d4] = o[4 * d4] * w0 + v1.x * w1;
+                o[4 * d4 + 1] = o[4 * d4 + 1] * w0 + v1.y * w1;
+                o[4 * d4 + 2] = o[4 * d4 + 2] * w0 + v1.z * w1;
+                o[4 * d4 + 3] = o[4 * d4 + 3] * w0 + v1.w * w1;
+            }
+            l_run = l;
+            m_used = mx;
             if (row_valid) {
                 if (p.splits == 1) {
-                    const float inv = 1.f / l_run;
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
                     __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off;
                     if ((p.D & 7) == 0) {
 #pragma unroll
