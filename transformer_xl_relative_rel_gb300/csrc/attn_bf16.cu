@@ -85,18 +85,18 @@ struct Smem {
     static constexpr uint32_t TILE = BN * 128;             // one K, V or table chunk
     static constexpr uint32_t STAGE = 3 * TILE;             // K, V, chunk
     static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
-    static constexpr uint32_t PRE = NSTAGE * STAGE;         // table chunks 0 and 1
-    static constexpr uint32_t QU = PRE + 2 * TILE;          // q+u, q+v: 128 rows of 128 bytes
+    static constexpr uint32_t QU = NSTAGE * STAGE;          // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
-    static constexpr uint32_t PB = QV + BM * 128;           // P (bf16) of each set: 128 rows x 128 bytes
-    static constexpr uint32_t XML = PB + 2 * BM * 128;      // epilogue: [128 rows] (m, l) of set 1
+    static constexpr uint32_t PB = QV + BM * 128;           // P (bf16): two buffers per set, 128 rows x 128 bytes
+    static constexpr uint32_t PRE = PB;                     // table chunks 0, 1 (read before any P is written)
+    static constexpr uint32_t XML = PB + 4 * BM * 128;      // epilogue: [128 rows] (m, l) of set 1
     static constexpr uint32_t BARS = XML + BM * 8;
     // barrier slots (8 bytes each): stage full / empty; per softmax set: S
-    // full, S free (read by the softmax), P full, P.V done, O done; epilogue
-    // exchange
+    // full, S free (read by the softmax), P full, O done; per P buffer: P.V
+    // done; epilogue exchange
     static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE,
                          B_S = 2 + 2 * NSTAGE, B_SF = B_S + 2, B_P = B_SF + 2, B_PV = B_P + 2,
-                         B_O = B_PV + 2, B_X = B_O + 2;
+                         B_O = B_PV + 4, B_X = B_O + 2;
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -115,6 +115,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// two fp32 -> packed fp16 pair (lo = a), round to nearest, saturated to +-65504
+__device__ __forceinline__ uint32_t pack_f16_sat(float a, float b)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// x0 += fp16 low half of h, x1 += fp16 high half (one fp32 rounding each)
+__device__ __forceinline__ void add_f16x2_to(float &x0, float &x1, uint32_t h)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "r"(h));
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c)
@@ -273,7 +292,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             mbar_init(bar(S::B_S + x), 1);
             mbar_init(bar(S::B_SF + x), 128);
             mbar_init(bar(S::B_P + x), 128);
-            mbar_init(bar(S::B_PV + x), 1);
+            mbar_init(bar(S::B_PV + 2 * x), 1);
+            mbar_init(bar(S::B_PV + 2 * x + 1), 1);
             mbar_init(bar(S::B_O + x), 1);
         }
         mbar_init(bar(S::B_X), 128);
@@ -399,12 +419,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 tc_fence_after();
                 if (ok && lane == 0) {
                     const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
-                    const uint64_t dp = d_p0 + sb * PB16;                  // 16 keys = 32 bytes of P
+                    const int pbuf = 2 * sb + ((n >> 1) & 1);              // P buffer of tile n
+                    const uint64_t dp = d_p0 + pbuf * PB16;                // 16 keys = 32 bytes of P
                     const uint32_t to = tmem + TM_O + 64 * sb;
     #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_bf16_ss(to, dp + 2 * kk, dv + 128 * kk, idesc_o, (n >= 2 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(S::B_PV + sb));
+                    mma_commit(bar(S::B_PV + pbuf));
                     mma_commit(bar(S::B_EMPTY + st));
                     if (n + 2 >= N) mma_commit(bar(S::B_O + sb));   // last tile of this set
                 }
@@ -487,20 +508,26 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         };
         // scaled logits of the 64 keys: S plus the band aligned to this row
         // (Appendix B's left shift of row i by L-1-i: row ii reads band column
-        // 127-ii+jj, a warp-uniform window start plus 31-lane), masked
+        // 127-ii+jj, a warp-uniform window start plus 31-lane), masked.  The
+        // shift runs on the band rounded to fp16 pairs (11-bit significand,
+        // saturated to the finite range): four select stages move whole
+        // registers (shift / 2), one byte permute moves half a register
+        // (shift & 1), then each fp16 is added to the fp32 content logit.
+        const uint32_t odd_sel = (shift & 1) ? 0x5432u : 0x3210u;
         auto logits = [&](bool diag, int lim, float (&x)[64], float (&a)[96]) {
+            uint32_t hb[48];
 #pragma unroll
-            for (int y = 0; y < 80; ++y) a[y] = (shift & 16) ? a[y + 16] : a[y];
+            for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
 #pragma unroll
-            for (int y = 0; y < 72; ++y) a[y] = (shift & 8) ? a[y + 8] : a[y];
+            for (int y = 0; y < 40; ++y) hb[y] = (shift & 16) ? hb[y + 8] : hb[y];
 #pragma unroll
-            for (int y = 0; y < 68; ++y) a[y] = (shift & 4) ? a[y + 4] : a[y];
+            for (int y = 0; y < 36; ++y) hb[y] = (shift & 8) ? hb[y + 4] : hb[y];
 #pragma unroll
-            for (int y = 0; y < 66; ++y) a[y] = (shift & 2) ? a[y + 2] : a[y];
+            for (int y = 0; y < 34; ++y) hb[y] = (shift & 4) ? hb[y + 2] : hb[y];
 #pragma unroll
-            for (int y = 0; y < 64; ++y) a[y] = (shift & 1) ? a[y + 1] : a[y];
+            for (int y = 0; y < 33; ++y) hb[y] = (shift & 2) ? hb[y + 1] : hb[y];
 #pragma unroll
-            for (int y = 0; y < 64; ++y) x[y] += a[y];
+            for (int y = 0; y < 32; ++y) add_f16x2_to(x[2 * y], x[2 * y + 1], __byte_perm(hb[y], hb[y + 1], odd_sel));
             if (diag) {
 #pragma unroll
                 for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
@@ -556,26 +583,31 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             float pk[32];
             const float psum = expo(x0, mu, pk) + expo(x1, mu, pk + 16);
             l_run = l_run * alpha + psum;
-            if (n >= 2) {
-                // the set's P buffer and O are free once the P.V of its previous tile is done
-                if (!wwait(S::B_PV + set, ((n - 2) >> 1) & 1)) {
+            // P buffer b of this set was last read by the P.V of tile n-4
+            const int b = (n >> 1) & 1;
+            if (n >= 4 && !wwait(S::B_PV + 2 * set + b, ((n >> 2) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (n >= 2 && __any_sync(0xffffffffu, raise)) {
+                // O holds the P.V of this set's earlier tiles: rescale it once the
+                // last of them (tile n-2, the other buffer) is done
+                if (!wwait(S::B_PV + 2 * set + (1 - b), ((n - 2) >> 2) & 1)) {
                     ok = false;
                     break;
                 }
-                if (__any_sync(0xffffffffu, raise)) {
-                    tc_fence_after();
+                tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < DP / 16; ++c) {
-                        float o[16];
-                        tmem_ld16(to + 16 * c, o);
+                for (int c = 0; c < DP / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(to + 16 * c, o);
 #pragma unroll
-                        for (int y = 0; y < 16; ++y) o[y] *= alpha;
-                        tmem_st16(to + 16 * c, o);
-                    }
-                    tmem_wait_st();
+                    for (int y = 0; y < 16; ++y) o[y] *= alpha;
+                    tmem_st16(to + 16 * c, o);
                 }
+                tmem_wait_st();
             }
-            unsigned char *pb = smem + S::PB + set * (BM * 128);
+            unsigned char *pb = smem + S::PB + (2 * set + b) * (BM * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4 *>(pb + sw128_offset(ii, 8 * c)) =
@@ -605,7 +637,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         if (set == 1) {
 #pragma unroll
             for (int d4 = 0; d4 < DP / 4; ++d4)
-                reinterpret_cast<float4 *>(xo + ii * 64)[d4] =
+                reinterpret_cast<float4 *>(xo + ii * 64)[d4 ^ (ii & 7)] =   // swizzled: no bank conflicts
                     make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
             xml[2 * ii] = has ? m_used : -INFINITY;
             xml[2 * ii + 1] = has ? l_run : 0.f;
@@ -618,7 +650,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const float l = l_run * w0 + l1 * w1;
 #pragma unroll
             for (int d4 = 0; d4 < DP / 4; ++d4) {
-                const float4 v1 = reinterpret_cast<const float4 *>(xo + ii * 64)[d4];
+                const float4 v1 = reinterpret_cast<const float4 *>(xo + ii * 64)[d4 ^ (ii & 7)];
                 o[4 * d4] = o[4 * d4] * w0 + v1.x * w1;
                 o[4 * d4 + 1] = o[4 * d4 + 1] * w0 + v1.y * w1;
                 o[4 * d4 + 2] = o[4 * d4 + 2] * w0 + v1.z * w1;
