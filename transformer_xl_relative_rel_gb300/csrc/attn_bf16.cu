@@ -367,70 +367,71 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
         } else if (warp == 1) {
             // =============================================================== S / band MMAs
-            const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
-            bool ok = wwait(S::B_Q, 0) && wwait(S::B_PRE, 0);
-            tc_fence_after();
-            // descriptors built once; the 14-bit start-address field (address / 16)
-            // advances by 2 per 32-byte K step within a 128-byte swizzled row
-            const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
-            const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
-            const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
-            const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-            constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
-            if (ok && lane == 0) {
-                for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
-    #pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks)
-                        mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
-                                    idesc_64, ks > 0);
-                }
-            }
-            __syncwarp();
-            for (int n = 0; ok && n < N; ++n) {
-                const int sb = n & 1, st = n % NSTAGE;
-                // S buffer sb was last read by the softmax of tile n-2, and band
-                // slot (n+2) % 4 by the softmaxes of tiles n-4..n-2: wait for
-                // tile n-2 here (tile n-3 was waited one iteration earlier)
-                if (n >= 2) ok = wwait(S::B_SF + sb, ((n - 2) >> 1) & 1);
-                ok = ok && wwait(S::B_FULL + st, (n / NSTAGE) & 1);
+            // one thread waits and issues (no warp-wide votes on this path: the
+            // issuing lane shares its scheduler with two softmax warps)
+            if (lane == 0) {
+                const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
+                bool ok = wait_or_abort(bar(S::B_Q), 0, abort) && wait_or_abort(bar(S::B_PRE), 0, abort);
                 tc_fence_after();
-                if (ok && lane == 0) {
+                // descriptors built once; the 14-bit start-address field (address / 16)
+                // advances by 2 per 32-byte K step within a 128-byte swizzled row
+                const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
+                const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
+                const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
+                const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
+                if (ok) {
+                    for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
+#pragma unroll
+                        for (int ks = 0; ks < DP / 16; ++ks)
+                            mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
+                                        idesc_64, ks > 0);
+                    }
+                }
+                for (int n = 0; ok && n < N; ++n) {
+                    const int sb = n & 1, st = n % NSTAGE;
+                    // S buffer sb was last read by the softmax of tile n-2, and band
+                    // slot (n+2) % 4 by the softmaxes of tiles n-4..n-2: wait for
+                    // tile n-2 here (tile n-3 was waited one iteration earlier)
+                    if (n >= 2) ok = wait_or_abort(bar(S::B_SF + sb), ((n - 2) >> 1) & 1, abort);
+                    ok = ok && wait_or_abort(bar(S::B_FULL + st), (n / NSTAGE) & 1, abort);
+                    if (!ok) break;
+                    tc_fence_after();
                     const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
                     const uint32_t ts = tmem + TM_S + 64 * sb;
                     const uint32_t tb = tmem + TM_BAND + 64 * (uint32_t)((n + 2) % NCHUNK);
-    #pragma unroll
+#pragma unroll
                     for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(ts, d_qu + 2 * ks, dk + 2 * ks, idesc_64, ks > 0);
-    #pragma unroll
+#pragma unroll
                     for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_64, ks > 0);
                     mma_commit(bar(S::B_S + sb));
                 }
-                __syncwarp();
             }
+            __syncwarp();
         } else if (warp == 2) {
             // =============================================================== P.V MMAs
-            const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
-            const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-            const uint64_t d_p0 = smem_desc_sw128(sbase + S::PB, 16, 1024);
-            constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4, PB16 = (BM * 128) >> 4;
-            bool ok = true;
-            for (int n = 0; ok && n < N; ++n) {
-                const int sb = n & 1, st = n % NSTAGE;
-                ok = wwait(S::B_P + sb, (n >> 1) & 1);
-                tc_fence_after();
-                if (ok && lane == 0) {
+            if (lane == 0) {
+                const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
+                const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+                const uint64_t d_p0 = smem_desc_sw128(sbase + S::PB, 16, 1024);
+                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4, PB16 = (BM * 128) >> 4;
+                for (int n = 0; n < N; ++n) {
+                    const int sb = n & 1, st = n % NSTAGE;
+                    if (!wait_or_abort(bar(S::B_P + sb), (n >> 1) & 1, abort)) break;
+                    tc_fence_after();
                     const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
                     const int pbuf = 2 * sb + ((n >> 1) & 1);              // P buffer of tile n
                     const uint64_t dp = d_p0 + pbuf * PB16;                // 16 keys = 32 bytes of P
                     const uint32_t to = tmem + TM_O + 64 * sb;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_bf16_ss(to, dp + 2 * kk, dv + 128 * kk, idesc_o, (n >= 2 || kk > 0) ? 1u : 0u);
                     mma_commit(bar(S::B_PV + pbuf));
                     mma_commit(bar(S::B_EMPTY + st));
                     if (n + 2 >= N) mma_commit(bar(S::B_O + sb));   // last tile of this set
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
     } else {
         setmaxnreg_inc<REG_HIGH>();
