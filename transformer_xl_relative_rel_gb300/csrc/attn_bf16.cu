@@ -6,35 +6,34 @@
 // with Q the reversed projected table of Appendix B (row t = W_kR R_{T-1-t}).
 //
 // One CTA owns 128 query rows of one (b, h) -- or one key-range split of them
-// -- and walks its keys in tiles of 64.  Six warps with fixed roles:
-//   warp 0    producer: TMA loads of K, V and one 64-row chunk of the table
-//             per tile into a seven-stage shared-memory ring, 128-byte rows
-//             with the 128-byte swizzle (threads' coalesced loads for head
-//             sizes other than 64);
-//   warp 1    S-MMA issuer (one thread): per tile, S = (q+u) K^T into one of
-//             three TMEM S buffers and the next band chunk B~ = (q+v) Q_chunk^T
-//             into a 4-slot TMEM ring, as far ahead as the buffers allow;
-//   warp 6    P.V issuer (one thread): O += P V as each tile's P arrives
-//             (two issuers, so neither kind of MMA waits on the other's
-//             barrier).  q+u, q+v, K, the table and V come from shared
-//             memory, P is a TMEM A operand;
-//   warps 2-5 softmax, one query row per thread (TMEM lane = row): each tile
-//             is two independent 32-key halves; each half reads its S part
-//             and the band window it needs, aligns the band to the row
-//             (Appendix B's left shift of row i by L-1-i, done as a register
-//             barrel shift by 31-lane; three stages as selects on the ALU,
-//             two as exact arithmetic selects on the FMA pipe), adds, masks
-//             j <= M+i, and runs the online softmax in the log2 domain.  P
-//             (bf16) goes back into the S buffer's TMEM columns for P.V.
-// Appendix B's table product is formed once per 64-row chunk: tile n uses
-// chunks n, n+1, n+2 of the band, and computes chunk n+2 itself, so the
-// position term costs the same tensor work as the content term.  The MMAs of
-// the next tiles run while the softmax of tile n runs (three S buffers).
-// The running max used for the exponentials is raised only when a row's max
-// grows by more than 8 (log2 units); O in TMEM is rescaled only then.
-// The scale log2(e)/sqrt(D) is folded into q+u and q+v before rounding.
-// Every mbarrier wait is bounded; on expiry the CTA records an error word
-// (read by txl_check) and every role winds down.
+// -- and walks its keys in tiles of 128.  Twelve warps with fixed roles:
+//   warp 0     producer: TMA loads of K, V and one 128-row chunk of the table
+//              per tile into a three-stage shared-memory ring (128-byte rows,
+//              128-byte swizzle); for head sizes other than 64, coalesced
+//              thread loads (warp 0: K and the table, warp 3: V);
+//   warp 1     one thread issues, per tile, S = (q+u) K^T (N = 128) into the
+//              TMEM S buffer and the next band chunk (q+v) Q_chunk^T (N = 128)
+//              into a two-slot TMEM ring;
+//   warp 2     one thread issues O += P V with P read from TMEM;
+//   warps 4-11 softmax: the two warps of a TMEM lane quadrant share its 32
+//              query rows (one row per thread), warps 4-7 take keys 0-63 of
+//              the tile and warps 8-11 keys 64-127.  Each thread loads its S
+//              columns and the 96-column band window its row needs in one
+//              batch (the S buffer is free for the next tile's MMAs right
+//              after), aligns the band to the row (Appendix B's left shift of
+//              row i by L-1-i, a register barrel shift by 31-lane on fp16
+//              pairs), adds, masks j <= M+i, trades its partial row max with
+//              the partner warp through shared memory, and writes P (bf16) to
+//              TMEM for the P.V MMA.
+// Appendix B's table product is formed once per 128-row chunk: tile n uses
+// chunks n and n+1 of the band and computes chunk n+1 itself, so the position
+// term costs the same tensor work as the content term.  The S and band MMAs of
+// tile n+1 run while the softmax of tile n runs.  The running max used for the
+// exponentials is raised only when a row's max grows by more than 8 (log2
+// units); O in TMEM is rescaled only then.  The scale log2(e)/sqrt(D) is
+// folded into q+u and q+v before rounding.  Every mbarrier wait is bounded; on
+// expiry the CTA records an error word (read by txl_check) and every role
+// winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,19 +52,20 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128;           // query rows per CTA (TMEM lanes)
-constexpr int BN = 64;            // keys per tile; also table rows per band chunk
-constexpr int NCHUNK = 4;         // TMEM band-chunk ring
-constexpr int NSTAGE = 5;         // shared-memory ring of (K, V, table chunk) tiles
+constexpr int BN = 128;           // keys per tile; also table rows per band chunk
+constexpr int HN = BN / 2;        // keys per softmax thread and tile
+constexpr int NSTAGE = 3;         // shared-memory ring of (K, V, table chunk) tiles
 constexpr int NT = 384;           // 12 warps, see the role list above
-constexpr uint32_t TM_S = 0;      // two S buffers (one per softmax set) of 64 columns
-constexpr uint32_t TM_BAND = 128; // band ring, 4 x 64 columns
-constexpr uint32_t TM_O = 384;    // two O accumulators (one per set), 64 columns each
+constexpr uint32_t TM_S = 0;      // S of the current tile, 128 columns
+constexpr uint32_t TM_BAND = 128; // band ring, 2 x 128 columns
+constexpr uint32_t TM_P = 384;    // P (bf16 pairs), 64 columns
+constexpr uint32_t TM_O = 448;    // O accumulator, up to 64 columns
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t REG_LOW = 96, REG_HIGH = 200;     // per-thread registers after the split
 static_assert(128 * REG_LOW + 256 * REG_HIGH <= 65536 / NT / 8 * 8 * NT, "register split exceeds the launch");
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait, then give up
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float RESCALE_LOG2 = 8.0f;          // raise the exponent base only past 2^8
+constexpr float SUM_LIMIT = 4096.0f;          // raise the exponent base once a row sum passes 2^12
 
 struct Params {
     const __nv_bfloat16 *q, *k, *v, *r;
@@ -82,21 +82,19 @@ struct Params {
 // swizzle (element (row, k) at sw128_offset(row, k)); D <= 64 fits one row.
 template <int DP>
 struct Smem {
-    static constexpr uint32_t TILE = BN * 128;             // one K, V or table chunk
+    static constexpr uint32_t TILE = BN * 128;             // one K, V or table chunk (128 rows)
     static constexpr uint32_t STAGE = 3 * TILE;             // K, V, chunk
     static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
     static constexpr uint32_t QU = NSTAGE * STAGE;          // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
-    static constexpr uint32_t PB = QV + BM * 128;           // P (bf16): two buffers per set, 128 rows x 128 bytes
-    static constexpr uint32_t PRE = PB;                     // table chunks 0, 1 (read before any P is written)
-    static constexpr uint32_t XML = PB + 4 * BM * 128;      // epilogue: [128 rows] (m, l) of set 1
-    static constexpr uint32_t BARS = XML + BM * 8;
-    // barrier slots (8 bytes each): stage full / empty; per softmax set: S
-    // full, S free (read by the softmax), P full, O done; per P buffer: P.V
-    // done; epilogue exchange
-    static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE,
-                         B_S = 2 + 2 * NSTAGE, B_SF = B_S + 2, B_P = B_SF + 2, B_PV = B_P + 2,
-                         B_O = B_PV + 4, B_X = B_O + 2;
+    static constexpr uint32_t PRE = QV + BM * 128;          // table chunk 0
+    static constexpr uint32_t XM = PRE + TILE;              // row-max exchange [2 phases][2 halves][128 rows]
+    static constexpr uint32_t BARS = XM + 2 * 2 * BM * 4;
+    // barrier slots (8 bytes each): q ready, chunk 0 ready, stage full /
+    // empty, S full, S free (read by the softmax), P full, P.V done, and one
+    // exchange barrier per TMEM lane quadrant
+    static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE, B_S = 2 + 2 * NSTAGE,
+                         B_SF = B_S + 1, B_P = B_SF + 1, B_PV = B_P + 1, B_X = B_PV + 1;
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -143,30 +141,6 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
-// packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction, two lanes of work)
-__device__ __forceinline__ uint64_t f2(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unf2(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
 __device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_err_word, code); }
 
 // A bounded wait that also gives up as soon as another role has given up.
@@ -175,7 +149,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > WAIT_NS) {
             *abort = 1;
@@ -255,7 +229,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int N = t1 - t0;                                 // key tiles of this CTA
     const long qkv_row = (long)p.B * p.H * p.D;            // elements between positions
     const long head_off = ((long)b * p.H + h) * p.D;
-    const int kb0 = p.L - BM - i0 + t0 * BN;              // first table row of chunk 0
+    // table row of (query i0+ii, key j0+jj) in tile n: kb0 + n*BN + 127 - ii + jj
+    const int kb0 = p.L - BM - i0 + t0 * BN;
 
     if (N <= 0) {   // an empty key split for this tile: neutral partials
         if (tid < rows_here) {
@@ -288,15 +263,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             mbar_init(bar(S::B_FULL + x), kTma ? 1 : 64);
             mbar_init(bar(S::B_EMPTY + x), 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(S::B_S + x), 1);
-            mbar_init(bar(S::B_SF + x), 128);
-            mbar_init(bar(S::B_P + x), 128);
-            mbar_init(bar(S::B_PV + 2 * x), 1);
-            mbar_init(bar(S::B_PV + 2 * x + 1), 1);
-            mbar_init(bar(S::B_O + x), 1);
-        }
-        mbar_init(bar(S::B_X), 128);
+        mbar_init(bar(S::B_S), 1);
+        mbar_init(bar(S::B_SF), 256);
+        mbar_init(bar(S::B_P), 256);
+        mbar_init(bar(S::B_PV), 1);
+        for (int x = 0; x < 4; ++x) mbar_init(bar(S::B_X + x), 64);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -307,7 +278,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
     // every operand buffer, and loads never write it: clear everything once
     if (p.D != DP) {
-        for (uint32_t x = tid; x < S::XML / 16; x += NT)
+        for (uint32_t x = tid; x < S::XM / 16; x += NT)
             reinterpret_cast<uint4 *>(smem)[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -322,19 +293,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         setmaxnreg_dec<REG_LOW>();
         if (warp == 0 || (warp == 3 && !kTma)) {
             // =============================================================== producer
-            // (without TMA: warp 0 loads K and the table chunks, warp 3 loads V)
-            const uint32_t tile_bytes = (uint32_t)BN * 128u;     // TMA only for D = 64
-            // table chunks 0 and 1 for the first tile
             if (kTma) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(S::B_PRE), 2 * tile_bytes);
+                    mbar_arrive_expect_tx(bar(S::B_PRE), S::TILE);
                     tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, h);
-                    tma_load_3d(sbase + S::PRE + S::TILE, &tm_r, bar(S::B_PRE), 0, kb0 + BN, h);
                 }
             } else if (warp == 0) {
                 warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
-                warp_load_rows(smem + S::PRE + S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0 + BN,
-                               p.T, p.D, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(S::B_PRE));
             }
@@ -343,11 +308,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 // the stage is free once the P.V of tile n-NSTAGE (its last reader) is done
                 if (n >= NSTAGE && !wwait(S::B_EMPTY + st, ((n / NSTAGE) - 1) & 1)) break;
                 const int j0 = (t0 + n) * BN;
-                const int crow = kb0 + (n + 2) * BN;     // table chunk n+2
+                const int crow = kb0 + (n + 1) * BN;     // table chunk n+1
                 const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
                 if (kTma) {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(bar(S::B_FULL + st), 3 * tile_bytes);
+                        mbar_arrive_expect_tx(bar(S::B_FULL + st), S::STAGE);
                         tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, bh);
                         tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, bh);
                         tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, h);
@@ -367,10 +332,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
         } else if (warp == 1) {
             // =============================================================== S / band MMAs
-            // one thread waits and issues (no warp-wide votes on this path: the
-            // issuing lane shares its scheduler with two softmax warps)
+            // one thread waits and issues (the issuing lane shares its
+            // scheduler with two softmax warps: no warp-wide votes here)
             if (lane == 0) {
-                const uint32_t idesc_64 = idesc_bf16(BM, BN, 0, 0);
+                const uint32_t idesc_n = idesc_bf16(BM, BN, 0, 0);
                 bool ok = wait_or_abort(bar(S::B_Q), 0, abort) && wait_or_abort(bar(S::B_PRE), 0, abort);
                 tc_fence_after();
                 // descriptors built once; the 14-bit start-address field (address / 16)
@@ -380,31 +345,27 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
                 constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
-                if (ok) {
-                    for (int c = 0; c < 2; ++c) {   // band chunks 0 and 1
+                if (ok) {   // band chunk 0
 #pragma unroll
-                        for (int ks = 0; ks < DP / 16; ++ks)
-                            mma_bf16_ss(tmem + TM_BAND + 64 * c, d_qv + 2 * ks, d_pre + c * TILE16 + 2 * ks,
-                                        idesc_64, ks > 0);
-                    }
+                    for (int ks = 0; ks < DP / 16; ++ks)
+                        mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, d_pre + 2 * ks, idesc_n, ks > 0);
                 }
                 for (int n = 0; ok && n < N; ++n) {
-                    const int sb = n & 1, st = n % NSTAGE;
-                    // S buffer sb was last read by the softmax of tile n-2, and band
-                    // slot (n+2) % 4 by the softmaxes of tiles n-4..n-2: wait for
-                    // tile n-2 here (tile n-3 was waited one iteration earlier)
-                    if (n >= 2) ok = wait_or_abort(bar(S::B_SF + sb), ((n - 2) >> 1) & 1, abort);
+                    const int st = n % NSTAGE;
+                    // the S buffer and band slot (n+1) % 2 were last read by the
+                    // softmax loads of tile n-1
+                    if (n >= 1) ok = wait_or_abort(bar(S::B_SF), (n - 1) & 1, abort);
                     ok = ok && wait_or_abort(bar(S::B_FULL + st), (n / NSTAGE) & 1, abort);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
-                    const uint32_t ts = tmem + TM_S + 64 * sb;
-                    const uint32_t tb = tmem + TM_BAND + 64 * (uint32_t)((n + 2) % NCHUNK);
+                    const uint32_t tb = tmem + TM_BAND + BN * (uint32_t)((n + 1) & 1);
 #pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(ts, d_qu + 2 * ks, dk + 2 * ks, idesc_64, ks > 0);
+                    for (int ks = 0; ks < DP / 16; ++ks)
+                        mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
 #pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_64, ks > 0);
-                    mma_commit(bar(S::B_S + sb));
+                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_n, ks > 0);
+                    mma_commit(bar(S::B_S));
                 }
             }
             __syncwarp();
@@ -413,22 +374,18 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             if (lane == 0) {
                 const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-                const uint64_t d_p0 = smem_desc_sw128(sbase + S::PB, 16, 1024);
-                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4, PB16 = (BM * 128) >> 4;
+                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
                 for (int n = 0; n < N; ++n) {
-                    const int sb = n & 1, st = n % NSTAGE;
-                    if (!wait_or_abort(bar(S::B_P + sb), (n >> 1) & 1, abort)) break;
+                    const int st = n % NSTAGE;
+                    if (!wait_or_abort(bar(S::B_P), n & 1, abort)) break;
                     tc_fence_after();
                     const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
-                    const int pbuf = 2 * sb + ((n >> 1) & 1);              // P buffer of tile n
-                    const uint64_t dp = d_p0 + pbuf * PB16;                // 16 keys = 32 bytes of P
-                    const uint32_t to = tmem + TM_O + 64 * sb;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_bf16_ss(to, dp + 2 * kk, dv + 128 * kk, idesc_o, (n >= 2 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(S::B_PV + pbuf));
+                    for (int kk = 0; kk < BN / 16; ++kk)   // P: 16 keys = 8 TMEM columns
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, dv + 128 * kk, idesc_o,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(S::B_PV));
                     mma_commit(bar(S::B_EMPTY + st));
-                    if (n + 2 >= N) mma_commit(bar(S::B_O + sb));   // last tile of this set
                 }
             }
             __syncwarp();
@@ -436,19 +393,24 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     } else {
         setmaxnreg_inc<REG_HIGH>();
         // =============================================================== softmax
-        // two sets of four warps; set k takes the key tiles n = k, k+2, k+4, ...
-        // with its own S buffer and O accumulator, so the two warps that share
-        // a scheduler work on different tiles and their ALU and MUFU phases
-        // overlap; the two partial results are merged once at the end
-        const int set = (warp - 4) >> 2;
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 4) >> 2;          // keys 64*half .. +63 of each tile
         const int ii = quarter * 32 + lane;        // this thread's query row
         const int i = i0 + ii;
         const bool row_valid = ii < rows_here;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t ts = tl + TM_S + 64 * set, tb0 = tl + TM_BAND, to = tl + TM_O + 64 * set;
+        float *xm = reinterpret_cast<float *>(smem + S::XM);
+        // trade a per-row value with the partner warp (same rows, other key
+        // half); exchange k uses buffer k & 1 and phase k of the quadrant's barrier
+        auto exchange = [&](int k, float v, float &other) {
+            xm[((k & 1) * 2 + half) * BM + ii] = v;
+            mbar_arrive(bar(S::B_X + quarter));
+            if (!wwait(S::B_X + quarter, k & 1)) return false;
+            other = xm[((k & 1) * 2 + (1 - half)) * BM + ii];
+            return true;
+        };
 
-        if (set == 0) {
+        if (half == 0) {
             // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into
             // shared memory as the A operands of the content and band MMAs
             float qrow[DP];
@@ -495,44 +457,45 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
 
         const int shift = 31 - lane;
-        // the tile's S (64 columns) and the 96-column band window its rows
-        // need, in one batch of TMEM loads: the buffers are free right after
+        // this thread's 64 S columns and the 96-column band window its row
+        // needs (band column 127-ii+jj of chunks n, n+1: a warp-uniform start
+        // plus 31-lane), in one batch of TMEM loads; the buffers are free for
+        // the next tile's MMAs right after
         auto load_tile = [&](int n, float (&x)[64], float (&a)[96]) {
-            const int rel = 96 - 32 * quarter;            // window start in chunks n..n+2
+            const int rel = 96 - 32 * quarter + HN * half;   // window start in chunks n, n+1
             uint32_t c[3];
 #pragma unroll
             for (int z = 0; z < 3; ++z) {
                 const int rz = rel + 32 * z;
-                c[z] = 64 * (uint32_t)((n + (rz >> 6)) % NCHUNK) + (rz & 63);
+                c[z] = TM_BAND + BN * (uint32_t)((n + (rz >> 7)) & 1) + (rz & (BN - 1));
             }
-            tmem_ld_5x32(ts, ts + 32, tb0 + c[0], tb0 + c[1], tb0 + c[2], x, a);
+            const uint32_t ts = tl + TM_S + HN * half;
+            tmem_ld_5x32(ts, ts + 32, tl + c[0], tl + c[1], tl + c[2], x, a);
         };
-        // scaled logits of the 64 keys: S plus the band aligned to this row
-        // (Appendix B's left shift of row i by L-1-i: row ii reads band column
-        // 127-ii+jj, a warp-uniform window start plus 31-lane), masked.  The
-        // shift runs on the band rounded to fp16 pairs (11-bit significand,
-        // saturated to the finite range): four select stages move whole
-        // registers (shift / 2), one byte permute moves half a register
-        // (shift & 1), then each fp16 is added to the fp32 content logit.
+        // the band of one 32-key block aligned to this row and added to its
+        // fp32 content logits.  The shift runs on the band rounded to fp16
+        // pairs (11-bit significand, saturated to the finite range): four
+        // select stages move whole registers (shift / 2) within the block's
+        // 32-register window, one byte permute moves half a register
+        // (shift & 1), then each fp16 is added to the fp32 logit.
         const uint32_t odd_sel = (shift & 1) ? 0x5432u : 0x3210u;
-        auto logits = [&](bool diag, int lim, float (&x)[64], float (&a)[96]) {
-            uint32_t hb[48];
+        auto band_block = [&](const uint32_t *w, float *xb) {
+            uint32_t g[24];
 #pragma unroll
-            for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
+            for (int y = 0; y < 24; ++y) g[y] = (shift & 16) ? w[y + 8] : w[y];
 #pragma unroll
-            for (int y = 0; y < 40; ++y) hb[y] = (shift & 16) ? hb[y + 8] : hb[y];
+            for (int y = 0; y < 20; ++y) g[y] = (shift & 8) ? g[y + 4] : g[y];
 #pragma unroll
-            for (int y = 0; y < 36; ++y) hb[y] = (shift & 8) ? hb[y + 4] : hb[y];
+            for (int y = 0; y < 18; ++y) g[y] = (shift & 4) ? g[y + 2] : g[y];
 #pragma unroll
-            for (int y = 0; y < 34; ++y) hb[y] = (shift & 4) ? hb[y + 2] : hb[y];
+            for (int y = 0; y < 17; ++y) g[y] = (shift & 2) ? g[y + 1] : g[y];
 #pragma unroll
-            for (int y = 0; y < 33; ++y) hb[y] = (shift & 2) ? hb[y + 1] : hb[y];
+            for (int k = 0; k < 16; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(g[k], g[k + 1], odd_sel));
+        };
+        // keys past the row's causal limit (j > M+i) get -inf
+        auto mask_block = [&](float *xb, int first, int lim) {
 #pragma unroll
-            for (int y = 0; y < 32; ++y) add_f16x2_to(x[2 * y], x[2 * y + 1], __byte_perm(hb[y], hb[y + 1], odd_sel));
-            if (diag) {
-#pragma unroll
-                for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
-            }
+            for (int y = 0; y < 32; ++y) xb[y] = (first + y <= lim) ? xb[y] : -INFINITY;
         };
         auto rowmax32 = [&](const float *x) {
             float q1[11];
@@ -553,120 +516,124 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             return (sacc[0] + sacc[1]) + (sacc[2] + sacc[3]);
         };
 
-        float m_used = -INFINITY, l_run = 0.f;
+        constexpr int DH = DP / 2;                 // O columns this warp rescales and stores
+        const uint32_t to = tl + TM_O + DH * half;
+        float m_used = -INFINITY, l_run = 0.f;     // l_run: this thread's key half only
+        int xk = 0;                                // exchanges done with the partner warp
         bool ok = true;
-        for (int n = set; n < N; n += 2) {
-            const int j0 = (t0 + n) * BN;
-            if (!wwait(S::B_S + set, (n >> 1) & 1)) {
+        for (int n = 0; n < N; ++n) {
+            const int j0 = (t0 + n) * BN + HN * half;     // first key of this thread's half
+            if (!wwait(S::B_S, n & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             // the mask matters only where this warp's rows meet the diagonal
-            const bool diag = j0 + BN - 1 > p.M + i0 + 32 * quarter;
+            const bool diag = j0 + HN - 1 > p.M + i0 + 32 * quarter;
             const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
             float x[64], a[96];
             load_tile(n, x, a);
-            // S and the band window are in registers: the S buffer and the band
-            // slot may be overwritten by the next MMAs from here on
             tc_fence_before();
-            mbar_arrive(bar(S::B_SF + set));
-            logits(diag, lim, x, a);
-            const float *x0 = x, *x1 = x + 32;
-            const float tmax = fmaxf(rowmax32(x0), rowmax32(x1));
-            float alpha = 1.f;
-            const bool raise = tmax > m_used + RESCALE_LOG2;   // also the first finite max
-            if (raise) {
-                alpha = ex2(m_used - tmax);                     // 0 when m_used = -inf
-                m_used = tmax;
-            }
-            const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-            float pk[32];
-            const float psum = expo(x0, mu, pk) + expo(x1, mu, pk + 16);
-            l_run = l_run * alpha + psum;
-            // P buffer b of this set was last read by the P.V of tile n-4
-            const int b = (n >> 1) & 1;
-            if (n >= 4 && !wwait(S::B_PV + 2 * set + b, ((n >> 2) - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            if (n >= 2 && __any_sync(0xffffffffu, raise)) {
-                // O holds the P.V of this set's earlier tiles: rescale it once the
-                // last of them (tile n-2, the other buffer) is done
-                if (!wwait(S::B_PV + 2 * set + (1 - b), ((n - 2) >> 2) & 1)) {
+            mbar_arrive(bar(S::B_SF));
+            uint32_t hb[48];
+#pragma unroll
+            for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
+            // rows without a finite reference max yet take the exact path; the
+            // others exponentiate against the running reference right away
+            // (block 0's exponentials and block 1's shift are independent
+            // work the scheduler can interleave) and check the row sum after
+            const bool exact = __any_sync(0xffffffffu, m_used == -INFINITY);
+            float pk[32], psum = 0.f, alpha = 1.f, other;
+            bool raise = false;
+            band_block(hb, x);
+            if (diag) mask_block(x, 0, lim);
+            if (!exact) {
+                psum = expo(x, m_used, pk);
+                band_block(hb + 16, x + 32);
+                if (diag) mask_block(x + 32, 32, lim);
+                psum += expo(x + 32, m_used, pk + 16);
+            } else {
+                band_block(hb + 16, x + 32);
+                if (diag) mask_block(x + 32, 32, lim);
+                float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                if (!exchange(xk++, lmax, other)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < DP / 16; ++c) {
-                    float o[16];
-                    tmem_ld16(to + 16 * c, o);
-#pragma unroll
-                    for (int y = 0; y < 16; ++y) o[y] *= alpha;
-                    tmem_st16(to + 16 * c, o);
+                const float m_new = fmaxf(m_used, fmaxf(lmax, other));
+                if (m_new > m_used) {
+                    alpha = ex2(m_used - m_new);       // 0 when m_used = -inf
+                    m_used = m_new;
+                    raise = true;
                 }
-                tmem_wait_st();
+                const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+                psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
             }
-            unsigned char *pb = smem + S::PB + (2 * set + b) * (BM * 128);
+            // the row's sum over all 128 keys against the reference; past
+            // SUM_LIMIT the reference is raised to the row's max (both warps of
+            // the pair see the same sum and take the same branch)
+            if (!exchange(xk++, psum, other)) {
+                ok = false;
+                break;
+            }
+            const float tot = psum + other;
+            const bool need = !(tot <= SUM_LIMIT);
+            if (__any_sync(0xffffffffu, need)) {
+                const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                if (!exchange(xk++, lmax, other)) {
+                    ok = false;
+                    break;
+                }
+                if (need) {
+                    const float m_new = fmaxf(m_used, fmaxf(lmax, other));
+                    alpha *= ex2(m_used - m_new);
+                    m_used = m_new;
+                    raise = true;
+                    psum = expo(x, m_used, pk) + expo(x + 32, m_used, pk + 16);
+                }
+            }
+            l_run = l_run * alpha + psum;
+            // P in TMEM and O are free once the P.V of tile n-1 is done
+            if (n >= 1 && !wwait(S::B_PV, (n - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (n >= 1 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(pb + sw128_offset(ii, 8 * c)) =
-                    make_uint4(__float_as_uint(pk[4 * c]), __float_as_uint(pk[4 * c + 1]),
-                               __float_as_uint(pk[4 * c + 2]), __float_as_uint(pk[4 * c + 3]));
-            fence_proxy_async_smem();
+                for (int c = 0; c < DH / 8; ++c) {
+                    float o[8];
+                    tmem_ld8(to + 8 * c, o);
+#pragma unroll
+                    for (int y = 0; y < 8; ++y) o[y] *= alpha;
+                    tmem_st8(to + 8 * c, o);
+                }
+            }
+            tmem_st32(tl + TM_P + 32 * half, *reinterpret_cast<float(*)[32]>(pk));
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(S::B_P + set));
+            mbar_arrive(bar(S::B_P));
         }
 
-        // ---- epilogue: merge the two sets' partial results of each row
-        const bool has = set < N;                  // set 1 has no tile when N == 1
-        if (ok && has) ok = wwait(S::B_O + set, 0);
-        float o[DP];
-#pragma unroll
-        for (int d = 0; d < DP; ++d) o[d] = 0.f;
-        if (ok && has) {
+        // ---- epilogue: O / l for this warp's half of the columns
+        float l_other = 0.f;
+        if (ok) ok = wwait(S::B_PV, (N - 1) & 1);
+        if (ok) ok = exchange(xk++, l_run, l_other);
+        if (ok) {
             tc_fence_after();
+            float o[DH];
 #pragma unroll
-            for (int c = 0; c < DP / 16; ++c) tmem_ld16(to + 16 * c, *reinterpret_cast<float(*)[16]>(&o[16 * c]));
-        }
-        // set 1 hands (m, l, O) to set 0 through the stage ring, once every
-        // P.V of both sets (the ring's last readers) has completed
-        float *xo = reinterpret_cast<float *>(smem + S::ST0);   // [128][64] O of set 1
-        float *xml = reinterpret_cast<float *>(smem + S::XML);  // [128][2] (m, l) of set 1
-        if (set == 1 && ok) ok = wwait(S::B_O + 0, 0);
-        if (set == 1) {
-#pragma unroll
-            for (int d4 = 0; d4 < DP / 4; ++d4)
-                reinterpret_cast<float4 *>(xo + ii * 64)[d4 ^ (ii & 7)] =   // swizzled: no bank conflicts
-                    make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
-            xml[2 * ii] = has ? m_used : -INFINITY;
-            xml[2 * ii + 1] = has ? l_run : 0.f;
-            mbar_arrive(bar(S::B_X));
-        } else if (ok && wwait(S::B_X, 0)) {
-            const float m1 = xml[2 * ii], l1 = xml[2 * ii + 1];
-            const float mx = fmaxf(m_used, m1);
-            const float w0 = (m_used == -INFINITY) ? 0.f : ex2(m_used - mx);
-            const float w1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mx);
-            const float l = l_run * w0 + l1 * w1;
-#pragma unroll
-            for (int d4 = 0; d4 < DP / 4; ++d4) {
-                const float4 v1 = reinterpret_cast<const float4 *>(xo + ii * 64)[d4 ^ (ii & 7)];
-                o[4 * d4] = o[4 * d4] * w0 + v1.x * w1;
-                o[4 * d4 + 1] = o[4 * d4 + 1] * w0 + v1.y * w1;
-                o[4 * d4 + 2] = o[4 * d4 + 2] * w0 + v1.z * w1;
-                o[4 * d4 + 3] = o[4 * d4 + 3] * w0 + v1.w * w1;
-            }
-            l_run = l;
-            m_used = mx;
+            for (int c = 0; c < DH / 8; ++c) tmem_ld8(to + 8 * c, o + 8 * c);
+            const float l = l_run + l_other;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int d0 = DH * half;
             if (row_valid) {
                 if (p.splits == 1) {
-                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                    __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off;
+                    __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off + d0;
                     if ((p.D & 7) == 0) {
 #pragma unroll
-                        for (int d8 = 0; d8 < DP / 8; ++d8) {
-                            if (d8 * 8 < p.D) {
+                        for (int d8 = 0; d8 < DH / 8; ++d8) {
+                            if (d0 + d8 * 8 < p.D) {
                                 uint4 pk4;
                                 pk4.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
                                 pk4.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
@@ -677,19 +644,18 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         }
                     } else {
 #pragma unroll
-                        for (int d = 0; d < DP; ++d)
-                            if (d < p.D) op[d] = __float2bfloat16(o[d] * inv);
+                        for (int d = 0; d < DH; ++d)
+                            if (d0 + d < p.D) op[d] = __float2bfloat16(o[d] * inv);
                     }
                 } else {
                     const long prow = ((long)split * p.B * p.H + bh) * p.L + i;
-                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                    float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP);
+                    float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP + d0);
 #pragma unroll
-                    for (int d4 = 0; d4 < DP / 4; ++d4)
+                    for (int d4 = 0; d4 < DH / 4; ++d4)
                         po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
                                              o[4 * d4 + 3] * inv);
                     // m_used is in log2 units of the scaled logits
-                    p.part_lse[prow] = l_run > 0.f ? m_used + log2f(l_run) : -INFINITY;
+                    if (half == 0) p.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 }
             }
         }
@@ -791,7 +757,7 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
     for (int s = 1; s <= 16 && s <= ntile; ++s) {
         const long waves = (ctas * s + num_sms - 1) / num_sms;
         const int per = (ntile + s - 1) / s;
-        const double cost = (double)waves * (per + 2) + (s > 1 ? 2.0 : 0.0);
+        const double cost = (double)waves * (per + 1) + (s > 1 ? 1.0 : 0.0);
         if (cost < best - 1e-9) {
             best = cost;
             best_s = s;
