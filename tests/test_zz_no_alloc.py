@@ -61,10 +61,11 @@ def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
 
 
 def test_noalloc_refuses_scratch_beyond_its_maximum(lib):
-    # B44 H8 D64 L128 M3800 splits its keys three ways: ~35 MB of partials,
-    # more than the fixed 32 MiB.  Real buffers, so nothing could go wrong on
-    # the device even if the refusal failed.
-    B, H, D, L, M = 44, 8, 64, 128, 3800
+    # B1 H8 D64 L4096 M16384 (eight heads, a long memory) splits its keys
+    # five ways: ~41 MiB of partials, more than the fixed 32 MiB.  Real
+    # buffers, so nothing could go wrong on the device even if the refusal
+    # failed.
+    B, H, D, L, M = 1, 8, 64, 4096, 16384
     T = L + M
     dev = {"q": torch.zeros(L, B, H, D, dtype=torch.bfloat16, device="cuda"),
            "k": torch.zeros(T, B, H, D, dtype=torch.bfloat16, device="cuda"),

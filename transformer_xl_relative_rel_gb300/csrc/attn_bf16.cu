@@ -75,6 +75,7 @@ struct Params {
     float *part_lse;    // [splits][B*H][L]
     int B, H, D, L, M, T;
     int nqt, splits;
+    int items;          // B*H*nqt*splits work items
     float sl2;          // log2(e) / sqrt(D)
 };
 
@@ -87,14 +88,18 @@ struct Smem {
     static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
     static constexpr uint32_t QU = NSTAGE * STAGE;          // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
-    static constexpr uint32_t PRE = QV + BM * 128;          // table chunk 0
-    static constexpr uint32_t XM = PRE + TILE;              // row-max exchange [2 phases][2 halves][128 rows]
+    static constexpr uint32_t PRE = QV + BM * 128;          // table chunk 0 of an item
+    static constexpr uint32_t QRAW = PRE + TILE;            // raw q rows of the next item
+    static constexpr uint32_t UW = QRAW + BM * 128;         // its head's u and v biases (fp32, 2 x 64)
+    static constexpr uint32_t XM = UW + 2 * 64 * 4;         // row exchange [2 phases][2 halves][128 rows]
     static constexpr uint32_t BARS = XM + 2 * 2 * BM * 4;
-    // barrier slots (8 bytes each): q ready, chunk 0 ready, stage full /
-    // empty, S full, S free (read by the softmax), P full, P.V done, and one
-    // exchange barrier per TMEM lane quadrant
-    static constexpr int B_Q = 0, B_PRE = 1, B_FULL = 2, B_EMPTY = 2 + NSTAGE, B_S = 2 + 2 * NSTAGE,
-                         B_SF = B_S + 1, B_P = B_SF + 1, B_PV = B_P + 1, B_X = B_PV + 1;
+    // barrier slots (8 bytes each): q+u/q+v ready, chunk 0 ready, chunk 0
+    // read, raw q ready, raw q read, stage full / empty, S full, S free
+    // (loaded by the softmax), P full, P.V done, and one exchange barrier per
+    // TMEM lane quadrant
+    static constexpr int B_Q = 0, B_PRE = 1, B_PREF = 2, B_QRAW = 3, B_QRF = 4, B_FULL = 5,
+                         B_EMPTY = 5 + NSTAGE, B_S = 5 + 2 * NSTAGE, B_SF = B_S + 1, B_P = B_SF + 1,
+                         B_PV = B_P + 1, B_X = B_PV + 1;
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -201,45 +206,69 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
     }
 }
 
+// One work item: 128 query rows of one (b, h) and one key-range split of
+// them.  Items are numbered heaviest first (query tiles from the last one
+// down); CTA c of G takes items c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the
+// sorted list, so that every CTA gets a similar total of key tiles).
+struct Item {
+    int bh, b, h, i0, rows_here, split, t0, N, kb0;
+    long head_off;
+};
+
+__device__ __forceinline__ Item make_item(const Params &p, int k)
+{
+    Item it;
+    const int per_qt = p.B * p.H * p.splits;
+    const int qt = p.nqt - 1 - k / per_qt;
+    const int rem = k % per_qt;
+    it.bh = rem / p.splits;
+    it.split = rem % p.splits;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    it.i0 = qt * BM;
+    it.rows_here = min(BM, p.L - it.i0);
+    const int kend = min(p.T, p.M + it.i0 + it.rows_here);   // keys these rows can see
+    const int ntile = (kend + BN - 1) / BN;
+    it.t0 = (int)(((long)it.split * ntile) / p.splits);
+    const int t1 = (int)(((long)(it.split + 1) * ntile) / p.splits);
+    it.N = t1 - it.t0;
+    // table row of (query i0+ii, key j0+jj) in tile n: kb0 + n*BN + 127 - ii + jj
+    it.kb0 = p.L - BM - it.i0 + it.t0 * BN;
+    it.head_off = ((long)it.b * p.H + it.h) * p.D;
+    return it;
+}
+
+// the j-th item of this CTA, or -1 past the end
+__device__ __forceinline__ int item_of(const Params &p, int j)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    const long k = (long)j * G + ((j & 1) ? (G - 1 - c) : c);
+    return k < p.items ? (int)k : -1;
+}
+
+// the first item at position >= j with at least one key tile (-1 if none)
+__device__ __forceinline__ int next_busy(const Params &p, int j, Item &it)
+{
+    for (;; ++j) {
+        const int k = item_of(p, j);
+        if (k < 0) return -1;
+        it = make_item(p, k);
+        if (it.N > 0) return j;
+    }
+}
+
 template <int DP, bool kTma>
 __global__ void __launch_bounds__(NT, 1)
 rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_r, const Params p)
+                     const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
+                     const Params p)
 {
     using S = Smem<DP>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- which (b, h, query tile, key split) this CTA owns; late (heavier)
-    // query tiles first so that the causal tail is not left for the last wave
-    const int per_bh = p.nqt * p.splits;
-    const int bh = blockIdx.x / per_bh;
-    const int rem = blockIdx.x % per_bh;
-    const int qt = p.nqt - 1 - rem / p.splits;
-    const int split = rem % p.splits;
-    const int b = bh / p.H, h = bh % p.H;
-    const int i0 = qt * BM;
-    const int rows_here = min(BM, p.L - i0);
-    const int kend = min(p.T, p.M + i0 + rows_here);      // keys this tile can see
-    const int ntile = (kend + BN - 1) / BN;
-    const int t0 = (int)(((long)split * ntile) / p.splits);
-    const int t1 = (int)(((long)(split + 1) * ntile) / p.splits);
-    const int N = t1 - t0;                                 // key tiles of this CTA
     const long qkv_row = (long)p.B * p.H * p.D;            // elements between positions
-    const long head_off = ((long)b * p.H + h) * p.D;
-    // table row of (query i0+ii, key j0+jj) in tile n: kb0 + n*BN + 127 - ii + jj
-    const int kb0 = p.L - BM - i0 + t0 * BN;
-
-    if (N <= 0) {   // an empty key split for this tile: neutral partials
-        if (tid < rows_here) {
-            const long prow = ((long)split * p.B * p.H + bh) * p.L + i0 + tid;
-            p.part_lse[prow] = -INFINITY;
-            for (int d = 0; d < DP; ++d) p.part_o[prow * DP + d] = 0.f;
-        }
-        return;
-    }
 
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + S::BARS + 8u * (uint32_t)i; };
@@ -259,6 +288,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         *abort = 0;
         mbar_init(bar(S::B_Q), 128);
         mbar_init(bar(S::B_PRE), kTma ? 1 : 32);
+        mbar_init(bar(S::B_PREF), 1);
+        mbar_init(bar(S::B_QRAW), kTma ? 1 : 32);
+        mbar_init(bar(S::B_QRF), 128);
         for (int x = 0; x < NSTAGE; ++x) {
             mbar_init(bar(S::B_FULL + x), kTma ? 1 : 64);
             mbar_init(bar(S::B_EMPTY + x), 1);
@@ -273,12 +305,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_r);
+            prefetch_tmap(&tm_q);
         }
     }
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
     // every operand buffer, and loads never write it: clear everything once
     if (p.D != DP) {
-        for (uint32_t x = tid; x < S::XM / 16; x += NT)
+        for (uint32_t x = tid; x < S::UW / 16; x += NT)
             reinterpret_cast<uint4 *>(smem)[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -293,42 +326,89 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         setmaxnreg_dec<REG_LOW>();
         if (warp == 0 || (warp == 3 && !kTma)) {
             // =============================================================== producer
-            if (kTma) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(S::B_PRE), S::TILE);
-                    tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, kb0, h);
-                }
-            } else if (warp == 0) {
-                warp_load_rows(smem + S::PRE, BN, p.r, (long)h * p.D, (long)p.H * p.D, kb0, p.T, p.D, lane);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(S::B_PRE));
-            }
-            for (int n = 0; n < N; ++n) {
-                const int st = n % NSTAGE;
-                // the stage is free once the P.V of tile n-NSTAGE (its last reader) is done
-                if (n >= NSTAGE && !wwait(S::B_EMPTY + st, ((n / NSTAGE) - 1) & 1)) break;
-                const int j0 = (t0 + n) * BN;
-                const int crow = kb0 + (n + 1) * BN;     // table chunk n+1
-                const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
+            // raw q rows (+ the head's u, v biases) of an item, for the
+            // softmax warps to turn into the MMA operands q+u, q+v
+            auto load_q = [&](const Item &it) {
                 if (kTma) {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(bar(S::B_FULL + st), S::STAGE);
-                        tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, bh);
-                        tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, bh);
-                        tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, h);
+                        mbar_arrive_expect_tx(bar(S::B_QRAW), S::TILE + 2 * 64 * 4);
+                        tma_load_3d(sbase + S::QRAW, &tm_q, bar(S::B_QRAW), 0, it.i0, it.bh);
+                        bulk_load(sbase + S::UW, p.u + it.h * p.D, 64 * 4, bar(S::B_QRAW));
+                        bulk_load(sbase + S::UW + 256, p.w + it.h * p.D, 64 * 4, bar(S::B_QRAW));
                     }
-                } else {
-                    unsigned char *d = smem + S::ST0 + st * S::STAGE;
-                    if (warp == 0) {
-                        warp_load_rows(d, BN, p.k, head_off, qkv_row, j0, p.T, p.D, lane);
-                        warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, crow, p.T,
-                                       p.D, lane);
-                    } else {
-                        warp_load_rows(d + S::TILE, BN, p.v, head_off, qkv_row, j0, p.T, p.D, lane);
+                } else if (warp == 0) {
+                    warp_load_rows(smem + S::QRAW, BM, p.q, it.head_off + (long)it.i0 * qkv_row, qkv_row, 0,
+                                   it.rows_here, p.D, lane);
+                    float *uw = reinterpret_cast<float *>(smem + S::UW);
+                    for (int d = lane; d < 64; d += 32) {
+                        uw[d] = d < p.D ? p.u[it.h * p.D + d] : 0.f;
+                        uw[64 + d] = d < p.D ? p.w[it.h * p.D + d] : 0.f;
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(bar(S::B_FULL + st));
+                    mbar_arrive(bar(S::B_QRAW));
                 }
+            };
+            Item it;
+            int j = next_busy(p, 0, it);
+            if (j >= 0) load_q(it);
+            int g = 0, ni = 0;                       // key tiles and items so far
+            bool ok = true;
+            while (ok && j >= 0) {
+                // table chunk 0 of the item, once the band MMA of the previous
+                // item's chunk 0 has read the buffer
+                if (ni >= 1 && !wwait(S::B_PREF, (ni - 1) & 1)) break;
+                if (kTma) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(S::B_PRE), S::TILE);
+                        tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, it.kb0, it.h);
+                    }
+                } else if (warp == 0) {
+                    warp_load_rows(smem + S::PRE, BN, p.r, (long)it.h * p.D, (long)p.H * p.D, it.kb0, p.T, p.D,
+                                   lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(S::B_PRE));
+                }
+                for (int n = 0; n < it.N; ++n, ++g) {
+                    const int st = g % NSTAGE;
+                    // the stage is free once the P.V of tile g-NSTAGE (its last reader) is done
+                    if (g >= NSTAGE && !wwait(S::B_EMPTY + st, ((g / NSTAGE) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int j0 = (it.t0 + n) * BN;
+                    const int crow = it.kb0 + (n + 1) * BN;     // table chunk n+1
+                    const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
+                    if (kTma) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(bar(S::B_FULL + st), S::STAGE);
+                            tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, it.bh);
+                            tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, it.bh);
+                            tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, it.h);
+                        }
+                    } else {
+                        unsigned char *d = smem + S::ST0 + st * S::STAGE;
+                        if (warp == 0) {
+                            warp_load_rows(d, BN, p.k, it.head_off, qkv_row, j0, p.T, p.D, lane);
+                            warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)it.h * p.D, (long)p.H * p.D, crow,
+                                           p.T, p.D, lane);
+                        } else {
+                            warp_load_rows(d + S::TILE, BN, p.v, it.head_off, qkv_row, j0, p.T, p.D, lane);
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(S::B_FULL + st));
+                    }
+                }
+                if (!ok) break;
+                // the next item's q rows, once this item's have been converted
+                Item nx;
+                const int jn = next_busy(p, j + 1, nx);
+                if (jn >= 0) {
+                    if (!wwait(S::B_QRF, ni & 1)) break;
+                    load_q(nx);
+                }
+                j = jn;
+                it = nx;
+                ++ni;
             }
         } else if (warp == 1) {
             // =============================================================== S / band MMAs
@@ -336,8 +416,6 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             // scheduler with two softmax warps: no warp-wide votes here)
             if (lane == 0) {
                 const uint32_t idesc_n = idesc_bf16(BM, BN, 0, 0);
-                bool ok = wait_or_abort(bar(S::B_Q), 0, abort) && wait_or_abort(bar(S::B_PRE), 0, abort);
-                tc_fence_after();
                 // descriptors built once; the 14-bit start-address field (address / 16)
                 // advances by 2 per 32-byte K step within a 128-byte swizzled row
                 const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
@@ -345,27 +423,40 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
                 constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
-                if (ok) {   // band chunk 0
-#pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks)
-                        mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, d_pre + 2 * ks, idesc_n, ks > 0);
-                }
-                for (int n = 0; ok && n < N; ++n) {
-                    const int st = n % NSTAGE;
-                    // the S buffer and band slot (n+1) % 2 were last read by the
-                    // softmax loads of tile n-1
-                    if (n >= 1) ok = wait_or_abort(bar(S::B_SF), (n - 1) & 1, abort);
-                    ok = ok && wait_or_abort(bar(S::B_FULL + st), (n / NSTAGE) & 1, abort);
+                Item it;
+                int g = 0, ni = 0;
+                bool ok = true;
+                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it), ++ni) {
+                    // q+u, q+v and table chunk 0 of the item; the S buffer and
+                    // band slot g % 2 were last read by the loads of tile g-1
+                    ok = wait_or_abort(bar(S::B_Q), ni & 1, abort) && wait_or_abort(bar(S::B_PRE), ni & 1, abort);
+                    if (ok && g >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
-                    const uint32_t tb = tmem + TM_BAND + BN * (uint32_t)((n + 1) & 1);
+                    // chunk c of this item lives in band slot (g0 + c) % 2
 #pragma unroll
                     for (int ks = 0; ks < DP / 16; ++ks)
-                        mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+                        mma_bf16_ss(tmem + TM_BAND + BN * (uint32_t)(g & 1), d_qv + 2 * ks, d_pre + 2 * ks, idesc_n,
+                                    ks > 0);
+                    mma_commit(bar(S::B_PREF));
+                    for (int n = 0; n < it.N; ++n, ++g) {
+                        const int st = g % NSTAGE;
+                        // the S buffer and band slot (g+1) % 2 were last read by
+                        // the softmax loads of tile g-1
+                        if (n >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
+                        ok = ok && wait_or_abort(bar(S::B_FULL + st), (g / NSTAGE) & 1, abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
+                        const uint32_t tb = tmem + TM_BAND + BN * (uint32_t)((g + 1) & 1);
 #pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks) mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_n, ks > 0);
-                    mma_commit(bar(S::B_S));
+                        for (int ks = 0; ks < DP / 16; ++ks)
+                            mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < DP / 16; ++ks)
+                            mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_n, ks > 0);
+                        mma_commit(bar(S::B_S));
+                    }
                 }
             }
             __syncwarp();
@@ -375,17 +466,25 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
                 constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
-                for (int n = 0; n < N; ++n) {
-                    const int st = n % NSTAGE;
-                    if (!wait_or_abort(bar(S::B_P), n & 1, abort)) break;
-                    tc_fence_after();
-                    const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
+                Item it;
+                int g = 0;
+                bool ok = true;
+                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it)) {
+                    for (int n = 0; n < it.N; ++n, ++g) {
+                        const int st = g % NSTAGE;
+                        if (!wait_or_abort(bar(S::B_P), g & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)   // P: 16 keys = 8 TMEM columns
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, dv + 128 * kk, idesc_o,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(S::B_PV));
-                    mma_commit(bar(S::B_EMPTY + st));
+                        for (int kk = 0; kk < BN / 16; ++kk)   // P: 16 keys = 8 TMEM columns
+                            mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, dv + 128 * kk, idesc_o,
+                                        (n > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar(S::B_PV));
+                        mma_commit(bar(S::B_EMPTY + st));
+                    }
                 }
             }
             __syncwarp();
@@ -396,56 +495,40 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;          // keys 64*half .. +63 of each tile
         const int ii = quarter * 32 + lane;        // this thread's query row
-        const int i = i0 + ii;
-        const bool row_valid = ii < rows_here;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         float *xm = reinterpret_cast<float *>(smem + S::XM);
+        int xk = 0;                                // exchanges done with the partner warp
         // trade a per-row value with the partner warp (same rows, other key
         // half); exchange k uses buffer k & 1 and phase k of the quadrant's barrier
-        auto exchange = [&](int k, float v, float &other) {
-            xm[((k & 1) * 2 + half) * BM + ii] = v;
+        auto exchange = [&](float v, float &other) {
+            xm[((xk & 1) * 2 + half) * BM + ii] = v;
             mbar_arrive(bar(S::B_X + quarter));
-            if (!wwait(S::B_X + quarter, k & 1)) return false;
-            other = xm[((k & 1) * 2 + (1 - half)) * BM + ii];
-            return true;
+            const bool ok = wwait(S::B_X + quarter, xk & 1);
+            other = xm[((xk & 1) * 2 + (1 - half)) * BM + ii];
+            ++xk;
+            return ok;
         };
-
-        if (half == 0) {
-            // q+u and q+v, scaled by log2(e)/sqrt(D), rounded once to bf16, into
-            // shared memory as the A operands of the content and band MMAs
-            float qrow[DP];
-#pragma unroll
-            for (int d = 0; d < DP; ++d) qrow[d] = 0.f;
-            if (row_valid) {
-                const __nv_bfloat16 *qp = p.q + (long)i * qkv_row + head_off;
-                if ((p.D & 7) == 0) {
-#pragma unroll
-                    for (int d8 = 0; d8 < DP / 8; ++d8) {
-                        if (d8 * 8 < p.D) {
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(qp + d8 * 8);
-                            const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-                            for (int z = 0; z < 8; ++z) qrow[d8 * 8 + z] = __bfloat162float(e[z]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int d = 0; d < DP; ++d)
-                        if (d < p.D) qrow[d] = __bfloat162float(qp[d]);
-                }
-            }
-            const float *up = p.u + h * p.D, *wp = p.w + h * p.D;
+        // q+u and q+v of an item's row ii, scaled by log2(e)/sqrt(D) and
+        // rounded once to bf16, from the raw rows into the MMA operand buffers
+        // (warps 4-7; item number ni)
+        auto convert_q = [&](const Item &it, int ni) {
+            if (!wwait(S::B_QRAW, ni & 1)) return false;
+            const float *uw = reinterpret_cast<const float *>(smem + S::UW);
+            const bool row_valid = ii < it.rows_here;
 #pragma unroll
             for (int d8 = 0; d8 < DP / 8; ++d8) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * d8));
+                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw);
                 uint32_t a4[4], c4[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
                     const int d = d8 * 8 + 2 * z;
-                    const bool in0 = row_valid && d < p.D, in1 = row_valid && d + 1 < p.D;
-                    const float u0 = in0 ? up[d] : 0.f, u1 = in1 ? up[d + 1] : 0.f;
-                    const float w0 = in0 ? wp[d] : 0.f, w1 = in1 ? wp[d + 1] : 0.f;
-                    a4[z] = pack_bf16((qrow[d] + u0) * p.sl2, (qrow[d + 1] + u1) * p.sl2);
-                    c4[z] = pack_bf16((qrow[d] + w0) * p.sl2, (qrow[d + 1] + w1) * p.sl2);
+                    const float q0 = row_valid ? __bfloat162float(e[2 * z]) : 0.f;
+                    const float q1 = row_valid ? __bfloat162float(e[2 * z + 1]) : 0.f;
+                    const float u0 = row_valid ? uw[d] : 0.f, u1 = row_valid ? uw[d + 1] : 0.f;
+                    const float w0 = row_valid ? uw[64 + d] : 0.f, w1 = row_valid ? uw[64 + d + 1] : 0.f;
+                    a4[z] = pack_bf16((q0 + u0) * p.sl2, (q1 + u1) * p.sl2);
+                    c4[z] = pack_bf16((q0 + w0) * p.sl2, (q1 + w1) * p.sl2);
                 }
                 *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
@@ -454,20 +537,23 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(S::B_Q));
-        }
+            mbar_arrive(bar(S::B_QRF));
+            return true;
+        };
 
         const int shift = 31 - lane;
         // this thread's 64 S columns and the 96-column band window its row
         // needs (band column 127-ii+jj of chunks n, n+1: a warp-uniform start
         // plus 31-lane), in one batch of TMEM loads; the buffers are free for
-        // the next tile's MMAs right after
-        auto load_tile = [&](int n, float (&x)[64], float (&a)[96]) {
+        // the next tile's MMAs right after.  Chunk c of the item is in band
+        // slot (g0 + c) % 2, so tile g reads slots g % 2 and (g+1) % 2.
+        auto load_tile = [&](int g, float (&x)[64], float (&a)[96]) {
             const int rel = 96 - 32 * quarter + HN * half;   // window start in chunks n, n+1
             uint32_t c[3];
 #pragma unroll
             for (int z = 0; z < 3; ++z) {
                 const int rz = rel + 32 * z;
-                c[z] = TM_BAND + BN * (uint32_t)((n + (rz >> 7)) & 1) + (rz & (BN - 1));
+                c[z] = TM_BAND + BN * (uint32_t)((g + (rz >> 7)) & 1) + (rz & (BN - 1));
             }
             const uint32_t ts = tl + TM_S + HN * half;
             tmem_ld_5x32(ts, ts + 32, tl + c[0], tl + c[1], tl + c[2], x, a);
@@ -518,115 +604,148 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
         constexpr int DH = DP / 2;                 // O columns this warp rescales and stores
         const uint32_t to = tl + TM_O + DH * half;
-        float m_used = -INFINITY, l_run = 0.f;     // l_run: this thread's key half only
-        int xk = 0;                                // exchanges done with the partner warp
         bool ok = true;
-        for (int n = 0; n < N; ++n) {
-            const int j0 = (t0 + n) * BN + HN * half;     // first key of this thread's half
-            if (!wwait(S::B_S, n & 1)) {
-                ok = false;
-                break;
+        Item it;
+        int j = next_busy(p, 0, it);
+        if (half == 0 && j >= 0) ok = convert_q(it, 0);
+        int g = 0, ni = 0;
+        // items without key tiles (empty key splits) only get neutral partials
+        auto neutral = [&](int jfrom, int jto) {
+            for (int q = jfrom; q < jto; ++q) {
+                const int k = item_of(p, q);
+                if (k < 0) break;
+                const Item e = make_item(p, k);
+                if (e.N <= 0 && half == 0 && ii < e.rows_here) {
+                    const long prow = ((long)e.split * p.B * p.H + e.bh) * p.L + e.i0 + ii;
+                    p.part_lse[prow] = -INFINITY;
+                    for (int d = 0; d < DP; ++d) p.part_o[prow * DP + d] = 0.f;
+                }
             }
-            tc_fence_after();
-            // the mask matters only where this warp's rows meet the diagonal
-            const bool diag = j0 + HN - 1 > p.M + i0 + 32 * quarter;
-            const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
-            float x[64], a[96];
-            load_tile(n, x, a);
-            tc_fence_before();
-            mbar_arrive(bar(S::B_SF));
-            uint32_t hb[48];
+        };
+        neutral(0, j >= 0 ? j : 1 << 30);
+        while (ok && j >= 0) {
+            const int i = it.i0 + ii;
+            const bool row_valid = ii < it.rows_here;
+            Item nx;
+            const int jn = next_busy(p, j + 1, nx);
+            float m_used = -INFINITY, l_run = 0.f;     // l_run: this thread's key half only
+            for (int n = 0; n < it.N; ++n, ++g) {
+                const int j0 = (it.t0 + n) * BN + HN * half;     // first key of this thread's half
+                if (!wwait(S::B_S, g & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // the item's last S MMAs have read q+u, q+v: the next item's
+                // operands go in now, so that its first MMAs overlap the rest
+                // of this item
+                if (n == it.N - 1 && half == 0 && jn >= 0 && !convert_q(nx, ni + 1)) {
+                    ok = false;
+                    break;
+                }
+                // the mask matters only where this warp's rows meet the diagonal
+                const bool diag = j0 + HN - 1 > p.M + it.i0 + 32 * quarter;
+                const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
+                float x[64], a[96];
+                load_tile(g, x, a);
+                tc_fence_before();
+                mbar_arrive(bar(S::B_SF));
+                uint32_t hb[48];
 #pragma unroll
-            for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
-            // rows without a finite reference max yet take the exact path; the
-            // others exponentiate against the running reference right away
-            // (block 0's exponentials and block 1's shift are independent
-            // work the scheduler can interleave) and check the row sum after
-            const bool exact = __any_sync(0xffffffffu, m_used == -INFINITY);
-            float pk[32], psum = 0.f, alpha = 1.f, other;
-            bool raise = false;
-            band_block(hb, x);
-            if (diag) mask_block(x, 0, lim);
-            if (!exact) {
-                psum = expo(x, m_used, pk);
-                band_block(hb + 16, x + 32);
-                if (diag) mask_block(x + 32, 32, lim);
-                psum += expo(x + 32, m_used, pk + 16);
-            } else {
-                band_block(hb + 16, x + 32);
-                if (diag) mask_block(x + 32, 32, lim);
-                float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                if (!exchange(xk++, lmax, other)) {
-                    ok = false;
-                    break;
-                }
-                const float m_new = fmaxf(m_used, fmaxf(lmax, other));
-                if (m_new > m_used) {
-                    alpha = ex2(m_used - m_new);       // 0 when m_used = -inf
-                    m_used = m_new;
-                    raise = true;
-                }
-                const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-                psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
-            }
-            // the row's sum over all 128 keys against the reference; past
-            // SUM_LIMIT the reference is raised to the row's max (both warps of
-            // the pair see the same sum and take the same branch)
-            if (!exchange(xk++, psum, other)) {
-                ok = false;
-                break;
-            }
-            const float tot = psum + other;
-            const bool need = !(tot <= SUM_LIMIT);
-            if (__any_sync(0xffffffffu, need)) {
-                const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                if (!exchange(xk++, lmax, other)) {
-                    ok = false;
-                    break;
-                }
-                if (need) {
+                for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
+                // rows without a finite reference max yet take the exact path;
+                // the others exponentiate against the running reference right
+                // away (block 0's exponentials and block 1's shift are
+                // independent work the scheduler can interleave) and check the
+                // row sum after
+                const bool exact = __any_sync(0xffffffffu, m_used == -INFINITY);
+                float pk[32], psum = 0.f, alpha = 1.f, other;
+                bool raise = false;
+                band_block(hb, x);
+                if (diag) mask_block(x, 0, lim);
+                if (!exact) {
+                    psum = expo(x, m_used, pk);
+                    band_block(hb + 16, x + 32);
+                    if (diag) mask_block(x + 32, 32, lim);
+                    psum += expo(x + 32, m_used, pk + 16);
+                } else {
+                    band_block(hb + 16, x + 32);
+                    if (diag) mask_block(x + 32, 32, lim);
+                    float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                    if (!exchange(lmax, other)) {
+                        ok = false;
+                        break;
+                    }
                     const float m_new = fmaxf(m_used, fmaxf(lmax, other));
-                    alpha *= ex2(m_used - m_new);
-                    m_used = m_new;
-                    raise = true;
-                    psum = expo(x, m_used, pk) + expo(x + 32, m_used, pk + 16);
+                    if (m_new > m_used) {
+                        alpha = ex2(m_used - m_new);       // 0 when m_used = -inf
+                        m_used = m_new;
+                        raise = true;
+                    }
+                    const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+                    psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
                 }
-            }
-            l_run = l_run * alpha + psum;
-            // P in TMEM and O are free once the P.V of tile n-1 is done
-            if (n >= 1 && !wwait(S::B_PV, (n - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (n >= 1 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll
-                for (int c = 0; c < DH / 8; ++c) {
-                    float o[8];
-                    tmem_ld8(to + 8 * c, o);
-#pragma unroll
-                    for (int y = 0; y < 8; ++y) o[y] *= alpha;
-                    tmem_st8(to + 8 * c, o);
+                // the row's sum over all 128 keys against the reference; past
+                // SUM_LIMIT the reference is raised to the row's max (both warps
+                // of the pair see the same sum and take the same branch)
+                if (!exchange(psum, other)) {
+                    ok = false;
+                    break;
                 }
+                const float tot = psum + other;
+                const bool need = !(tot <= SUM_LIMIT);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                    if (!exchange(lmax, other)) {
+                        ok = false;
+                        break;
+                    }
+                    if (need) {
+                        const float m_new = fmaxf(m_used, fmaxf(lmax, other));
+                        alpha *= ex2(m_used - m_new);
+                        m_used = m_new;
+                        raise = true;
+                        psum = expo(x, m_used, pk) + expo(x + 32, m_used, pk + 16);
+                    }
+                }
+                l_run = l_run * alpha + psum;
+                // P in TMEM and O are free once the P.V of tile g-1 is done (for
+                // the item's first tile the epilogue of the previous item waited)
+                if (n >= 1 && !wwait(S::B_PV, (g - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (n >= 1 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int c = 0; c < DH / 8; ++c) {
+                        float o[8];
+                        tmem_ld8(to + 8 * c, o);
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) o[y] *= alpha;
+                        tmem_st8(to + 8 * c, o);
+                    }
+                }
+                tmem_st32(tl + TM_P + 32 * half, *reinterpret_cast<float(*)[32]>(pk));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(S::B_P));
             }
-            tmem_st32(tl + TM_P + 32 * half, *reinterpret_cast<float(*)[32]>(pk));
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(S::B_P));
-        }
+            if (!ok) break;
 
-        // ---- epilogue: O / l for this warp's half of the columns
-        float l_other = 0.f;
-        if (ok) ok = wwait(S::B_PV, (N - 1) & 1);
-        if (ok) ok = exchange(xk++, l_run, l_other);
-        if (ok) {
+            // ---- epilogue: O / l for this warp's half of the columns
+            float l_other = 0.f;
+            ok = wwait(S::B_PV, (g - 1) & 1) && exchange(l_run, l_other);
+            if (!ok) break;
             tc_fence_after();
             float o[DH];
 #pragma unroll
             for (int c = 0; c < DH / 8; ++c) tmem_ld8(to + 8 * c, o + 8 * c);
+            tc_fence_before();
             const float l = l_run + l_other;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int d0 = DH * half;
+            const long head_off = it.head_off;
             if (row_valid) {
                 if (p.splits == 1) {
                     __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off + d0;
@@ -648,7 +767,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                             if (d0 + d < p.D) op[d] = __float2bfloat16(o[d] * inv);
                     }
                 } else {
-                    const long prow = ((long)split * p.B * p.H + bh) * p.L + i;
+                    const long prow = ((long)it.split * p.B * p.H + it.bh) * p.L + i;
                     float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP + d0);
 #pragma unroll
                     for (int d4 = 0; d4 < DH / 4; ++d4)
@@ -658,6 +777,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     if (half == 0) p.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
                 }
             }
+            neutral(j + 1, jn >= 0 ? jn : 1 << 30);
+            j = jn;
+            it = nx;
+            ++ni;
         }
     }
 
@@ -729,14 +852,15 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
 
 template <int DP, bool kTma>
 cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                     const CUtensorMap &mr, cudaStream_t s)
+                     const CUtensorMap &mr, const CUtensorMap &mq, cudaStream_t s)
 {
     const uint32_t smem = Smem<DP>::TOTAL;
     auto kern = rel_attn_bf16_kernel<DP, kTma>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long grid = (long)p.B * p.H * p.nqt * p.splits;
-    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, p);
+    // persistent: one CTA per SM, each walks its share of the work items
+    const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
+    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, p);
     return cudaGetLastError();
 }
 
@@ -746,18 +870,33 @@ int dpad(int D) { return (D + 15) / 16 * 16; }
 
 int bf16_num_splits(const AttnArgs &a, int num_sms)
 {
+    // cost model in units of one key tile (~1.2 us of one SM): the CTAs share
+    // the items' tiles (plus about half a tile of fill per item), the last
+    // item adds about half its length, and splitting pays for the fp32
+    // partials (written and read once, ~6 TB/s) and the combine launch
     const int nqt = (a.L + BM - 1) / BM;
-    const long ctas = (long)a.B * a.H * nqt;
-    const int ntile = (a.M + a.L + BN - 1) / BN;     // key tiles of the last query tile
-    // choose the split count that minimises (waves x tiles per split), with a
-    // charge for the partials and the combine pass; 1 when the grid already
-    // fills the GPU
+    const long bh = (long)a.B * a.H;
+    const long T = (long)a.M + a.L;
+    long tiles = 0;
+    int maxn = 1;
+    for (int qt = 0; qt < nqt; ++qt) {
+        const long kend = T < a.M + (long)(qt + 1) * BM ? T : a.M + (long)(qt + 1) * BM;
+        const int nt = (int)((kend + BN - 1) / BN);
+        tiles += nt;
+        maxn = nt > maxn ? nt : maxn;
+    }
+    tiles *= bh;
+    const double tile_us = 1.2;
     double best = 1e30;
     int best_s = 1;
-    for (int s = 1; s <= 16 && s <= ntile; ++s) {
-        const long waves = (ctas * s + num_sms - 1) / num_sms;
-        const int per = (ntile + s - 1) / s;
-        const double cost = (double)waves * (per + 1) + (s > 1 ? 1.0 : 0.0);
+    for (int s = 1; s <= 16 && s <= maxn; ++s) {
+        const long items = bh * nqt * s;
+        const long G = items < num_sms ? items : num_sms;
+        double cost = ((double)tiles + 0.5 * (double)items) / (double)G + 0.5 * (double)((maxn + s - 1) / s);
+        if (s > 1) {
+            const double bytes = 2.0 * s * (double)bh * a.L * (dpad(a.D) + 1) * 4.0;
+            cost += (bytes / 6.0e6 + 3.0) / tile_us;
+        }
         if (cost < best - 1e-9) {
             best = cost;
             best_s = s;
@@ -800,24 +939,28 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
         p.part_o = (float *)scratch;
         p.part_lse = (float *)((char *)scratch + rows * DP * 4);
     }
-    CUtensorMap mk, mv, mr;
+    p.items = (int)((long)a.B * a.H * p.nqt * splits);
+    CUtensorMap mk, mv, mr, mq;
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
     memset(&mr, 0, sizeof(mr));
-    const bool tma = a.D == 64;
+    memset(&mq, 0, sizeof(mq));
+    // TMA for D = 64 (128-byte rows); the biases then come by bulk copy,
+    // which wants them 16-byte aligned
+    const bool tma = a.D == 64 && ((uintptr_t)a.u & 15) == 0 && ((uintptr_t)a.w & 15) == 0;
     if (tma) {
         const long bhn = (long)a.B * a.H;
         const long rs = bhn * a.D;
         if (!make_map(&mk, a.k, p.T, rs, bhn, BN) || !make_map(&mv, a.v, p.T, rs, bhn, BN) ||
-            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN))
+            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM))
             return cudaErrorInvalidValue;
     }
     cudaError_t e;
     switch (DP) {
-    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, s) : launch_t<16, false>(p, mk, mv, mr, s); break;
-    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, s) : launch_t<32, false>(p, mk, mv, mr, s); break;
-    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, s) : launch_t<48, false>(p, mk, mv, mr, s); break;
-    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, s) : launch_t<64, false>(p, mk, mv, mr, s); break;
+    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, s) : launch_t<16, false>(p, mk, mv, mr, mq, s); break;
+    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, s) : launch_t<32, false>(p, mk, mv, mr, mq, s); break;
+    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, s) : launch_t<48, false>(p, mk, mv, mr, mq, s); break;
+    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, s) : launch_t<64, false>(p, mk, mv, mr, mq, s); break;
     }
     if (e != cudaSuccess || splits == 1) return e;
     rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
