@@ -229,8 +229,8 @@ __device__ __forceinline__ Item make_item(const Params &p, int k)
     it.rows_here = min(BM, p.L - it.i0);
     const int kend = min(p.T, p.M + it.i0 + it.rows_here);   // keys these rows can see
     const int ntile = (kend + BN - 1) / BN;
-    it.t0 = (int)(((long)it.split * ntile) / p.splits);
-    const int t1 = (int)(((long)(it.split + 1) * ntile) / p.splits);
+    it.t0 = it.split * ntile / p.splits;                      // 32-bit: ntile * splits is small
+    const int t1 = (it.split + 1) * ntile / p.splits;
     it.N = t1 - it.t0;
     // table row of (query i0+ii, key j0+jj) in tile n: kb0 + n*BN + 127 - ii + jj
     it.kb0 = p.L - BM - it.i0 + it.t0 * BN;
@@ -513,22 +513,32 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         // (warps 4-7; item number ni)
         auto convert_q = [&](const Item &it, int ni) {
             if (!wwait(S::B_QRAW, ni & 1)) return false;
-            const float *uw = reinterpret_cast<const float *>(smem + S::UW);
-            const bool row_valid = ii < it.rows_here;
+            const float4 *uw4 = reinterpret_cast<const float4 *>(smem + S::UW);
+            const float keep = ii < it.rows_here ? 1.f : 0.f;   // rows past L: zero operands
+            // every load first (the stores below could alias them as far as the
+            // compiler knows), then the arithmetic and the stores
+            uint4 raw[DP / 8];
+            float4 u4[DP / 4], w4[DP / 4];
+#pragma unroll
+            for (int d8 = 0; d8 < DP / 8; ++d8)
+                raw[d8] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * d8));
+#pragma unroll
+            for (int d4 = 0; d4 < DP / 4; ++d4) {
+                u4[d4] = uw4[d4];
+                w4[d4] = uw4[16 + d4];
+            }
+            const float sk = p.sl2 * keep;
 #pragma unroll
             for (int d8 = 0; d8 < DP / 8; ++d8) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * d8));
-                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw[d8]);
+                const float *uu = reinterpret_cast<const float *>(&u4[2 * d8]);
+                const float *ww = reinterpret_cast<const float *>(&w4[2 * d8]);
                 uint32_t a4[4], c4[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    const int d = d8 * 8 + 2 * z;
-                    const float q0 = row_valid ? __bfloat162float(e[2 * z]) : 0.f;
-                    const float q1 = row_valid ? __bfloat162float(e[2 * z + 1]) : 0.f;
-                    const float u0 = row_valid ? uw[d] : 0.f, u1 = row_valid ? uw[d + 1] : 0.f;
-                    const float w0 = row_valid ? uw[64 + d] : 0.f, w1 = row_valid ? uw[64 + d + 1] : 0.f;
-                    a4[z] = pack_bf16((q0 + u0) * p.sl2, (q1 + u1) * p.sl2);
-                    c4[z] = pack_bf16((q0 + w0) * p.sl2, (q1 + w1) * p.sl2);
+                    const float q0 = __bfloat162float(e[2 * z]), q1 = __bfloat162float(e[2 * z + 1]);
+                    a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
+                    c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
                 }
                 *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
@@ -604,11 +614,57 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
         constexpr int DH = DP / 2;                 // O columns this warp rescales and stores
         const uint32_t to = tl + TM_O + DH * half;
-        bool ok = true;
-        Item it;
-        int j = next_busy(p, 0, it);
-        if (half == 0 && j >= 0) ok = convert_q(it, 0);
-        int g = 0, ni = 0;
+        // an item's output: O / l for this warp's half of the columns (after
+        // the item's last P.V; l is the sum of both key halves)
+        struct Done {
+            long head_off;
+            int i0, rows_here, bh, split;
+            float m, l;
+        };
+        auto epilogue = [&](const Done &dn, int g_last) {
+            float l_other = 0.f;
+            if (!wwait(S::B_PV, g_last & 1) || !exchange(dn.l, l_other)) return false;
+            tc_fence_after();
+            float o[DH];
+#pragma unroll
+            for (int c = 0; c < DH / 8; ++c) tmem_ld8(to + 8 * c, o + 8 * c);
+            tc_fence_before();
+            const float l = dn.l + l_other;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int d0 = DH * half;
+            const int i = dn.i0 + ii;
+            if (ii >= dn.rows_here) return true;
+            if (p.splits == 1) {
+                __nv_bfloat16 *op = p.out + (long)i * qkv_row + dn.head_off + d0;
+                if ((p.D & 7) == 0) {
+#pragma unroll
+                    for (int d8 = 0; d8 < DH / 8; ++d8) {
+                        if (d0 + d8 * 8 < p.D) {
+                            uint4 pk4;
+                            pk4.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
+                            pk4.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
+                            pk4.z = pack_bf16(o[d8 * 8 + 4] * inv, o[d8 * 8 + 5] * inv);
+                            pk4.w = pack_bf16(o[d8 * 8 + 6] * inv, o[d8 * 8 + 7] * inv);
+                            *reinterpret_cast<uint4 *>(op + d8 * 8) = pk4;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int d = 0; d < DH; ++d)
+                        if (d0 + d < p.D) op[d] = __float2bfloat16(o[d] * inv);
+                }
+            } else {
+                const long prow = ((long)dn.split * p.B * p.H + dn.bh) * p.L + i;
+                float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP + d0);
+#pragma unroll
+                for (int d4 = 0; d4 < DH / 4; ++d4)
+                    po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
+                                         o[4 * d4 + 3] * inv);
+                // m is in log2 units of the scaled logits
+                if (half == 0) p.part_lse[prow] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
+            }
+            return true;
+        };
         // items without key tiles (empty key splits) only get neutral partials
         auto neutral = [&](int jfrom, int jto) {
             for (int q = jfrom; q < jto; ++q) {
@@ -622,6 +678,14 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
             }
         };
+
+        bool ok = true;
+        Item it;
+        int j = next_busy(p, 0, it);
+        if (half == 0 && j >= 0) ok = convert_q(it, 0);
+        int g = 0, ni = 0;
+        bool pending = false;                      // the previous item's output is still in O
+        Done prev;
         neutral(0, j >= 0 ? j : 1 << 30);
         while (ok && j >= 0) {
             const int i = it.i0 + ii;
@@ -709,9 +773,16 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     }
                 }
                 l_run = l_run * alpha + psum;
-                // P in TMEM and O are free once the P.V of tile g-1 is done (for
-                // the item's first tile the epilogue of the previous item waited)
-                if (n >= 1 && !wwait(S::B_PV, (g - 1) & 1)) {
+                if (n == 0) {
+                    // the previous item's output leaves O before this item's
+                    // first P.V overwrites it; its last P.V has long finished
+                    if (pending && !epilogue(prev, g - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    pending = false;
+                } else if (!wwait(S::B_PV, (g - 1) & 1)) {
+                    // P in TMEM and O are free once the P.V of tile g-1 is done
                     ok = false;
                     break;
                 }
@@ -732,56 +803,20 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 mbar_arrive(bar(S::B_P));
             }
             if (!ok) break;
-
-            // ---- epilogue: O / l for this warp's half of the columns
-            float l_other = 0.f;
-            ok = wwait(S::B_PV, (g - 1) & 1) && exchange(l_run, l_other);
-            if (!ok) break;
-            tc_fence_after();
-            float o[DH];
-#pragma unroll
-            for (int c = 0; c < DH / 8; ++c) tmem_ld8(to + 8 * c, o + 8 * c);
-            tc_fence_before();
-            const float l = l_run + l_other;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int d0 = DH * half;
-            const long head_off = it.head_off;
-            if (row_valid) {
-                if (p.splits == 1) {
-                    __nv_bfloat16 *op = p.out + (long)i * qkv_row + head_off + d0;
-                    if ((p.D & 7) == 0) {
-#pragma unroll
-                        for (int d8 = 0; d8 < DH / 8; ++d8) {
-                            if (d0 + d8 * 8 < p.D) {
-                                uint4 pk4;
-                                pk4.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
-                                pk4.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
-                                pk4.z = pack_bf16(o[d8 * 8 + 4] * inv, o[d8 * 8 + 5] * inv);
-                                pk4.w = pack_bf16(o[d8 * 8 + 6] * inv, o[d8 * 8 + 7] * inv);
-                                *reinterpret_cast<uint4 *>(op + d8 * 8) = pk4;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int d = 0; d < DH; ++d)
-                            if (d0 + d < p.D) op[d] = __float2bfloat16(o[d] * inv);
-                    }
-                } else {
-                    const long prow = ((long)it.split * p.B * p.H + it.bh) * p.L + i;
-                    float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP + d0);
-#pragma unroll
-                    for (int d4 = 0; d4 < DH / 4; ++d4)
-                        po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
-                                             o[4 * d4 + 3] * inv);
-                    // m_used is in log2 units of the scaled logits
-                    if (half == 0) p.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
-                }
-            }
+            prev.head_off = it.head_off;
+            prev.i0 = it.i0;
+            prev.rows_here = it.rows_here;
+            prev.bh = it.bh;
+            prev.split = it.split;
+            prev.m = m_used;
+            prev.l = l_run;
+            pending = true;
             neutral(j + 1, jn >= 0 ? jn : 1 << 30);
             j = jn;
             it = nx;
             ++ni;
         }
+        if (ok && pending) epilogue(prev, g - 1);
     }
 
     tc_fence_before();
