@@ -717,61 +717,44 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 uint32_t hb[48];
 #pragma unroll
                 for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
-                // rows without a finite reference max yet take the exact path;
-                // the others exponentiate against the running reference right
-                // away (block 0's exponentials and block 1's shift are
-                // independent work the scheduler can interleave) and check the
-                // row sum after
-                const bool exact = __any_sync(0xffffffffu, m_used == -INFINITY);
-                float pk[32], psum = 0.f, alpha = 1.f, other;
-                bool raise = false;
                 band_block(hb, x);
-                if (diag) mask_block(x, 0, lim);
-                if (!exact) {
-                    psum = expo(x, m_used, pk);
-                    band_block(hb + 16, x + 32);
-                    if (diag) mask_block(x + 32, 32, lim);
-                    psum += expo(x + 32, m_used, pk + 16);
-                } else {
-                    band_block(hb + 16, x + 32);
-                    if (diag) mask_block(x + 32, 32, lim);
-                    float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                    if (!exchange(lmax, other)) {
-                        ok = false;
-                        break;
-                    }
-                    const float m_new = fmaxf(m_used, fmaxf(lmax, other));
-                    if (m_new > m_used) {
-                        alpha = ex2(m_used - m_new);       // 0 when m_used = -inf
-                        m_used = m_new;
-                        raise = true;
+                band_block(hb + 16, x + 32);
+                if (diag) {
+                    mask_block(x, 0, lim);
+                    mask_block(x + 32, 32, lim);
+                }
+                // exponentials against the running reference max; rows without
+                // a finite reference yet take the row's max first.  The row's
+                // sum over all 128 keys is then checked (both warps of the pair
+                // see the same sum and take the same branch): past SUM_LIMIT the
+                // reference is raised to the row's max and the pass repeated.
+                float pk[32], psum, alpha = 1.f, other;
+                bool raise = false;
+                bool find_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+                for (int pass = 0;; ++pass) {
+                    if (find_max) {
+                        const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                        if (!exchange(lmax, other)) {
+                            ok = false;
+                            break;
+                        }
+                        const float m_new = fmaxf(m_used, fmaxf(lmax, other));
+                        if (m_new > m_used) {
+                            alpha *= ex2(m_used - m_new);      // 0 when m_used = -inf
+                            m_used = m_new;
+                            raise = true;
+                        }
                     }
                     const float mu = (m_used == -INFINITY) ? 0.f : m_used;
                     psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
-                }
-                // the row's sum over all 128 keys against the reference; past
-                // SUM_LIMIT the reference is raised to the row's max (both warps
-                // of the pair see the same sum and take the same branch)
-                if (!exchange(psum, other)) {
-                    ok = false;
-                    break;
-                }
-                const float tot = psum + other;
-                const bool need = !(tot <= SUM_LIMIT);
-                if (__any_sync(0xffffffffu, need)) {
-                    const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                    if (!exchange(lmax, other)) {
+                    if (!exchange(psum, other)) {
                         ok = false;
                         break;
                     }
-                    if (need) {
-                        const float m_new = fmaxf(m_used, fmaxf(lmax, other));
-                        alpha *= ex2(m_used - m_new);
-                        m_used = m_new;
-                        raise = true;
-                        psum = expo(x, m_used, pk) + expo(x + 32, m_used, pk + 16);
-                    }
+                    find_max = __any_sync(0xffffffffu, !(psum + other <= SUM_LIMIT));
+                    if (!find_max || pass > 0) break;
                 }
+                if (!ok) break;
                 l_run = l_run * alpha + psum;
                 if (n == 0) {
                     // the previous item's output leaves O before this item's
