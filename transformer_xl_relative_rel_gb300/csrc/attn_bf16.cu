@@ -146,6 +146,30 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
+// packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction, two elements)
+__device__ __forceinline__ uint64_t f2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_err_word, code); }
 
 // A bounded wait that also gives up as soon as another role has given up.
@@ -601,15 +625,23 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             return max3(max3(q1[0], q1[1], q1[2]), max3(q1[3], q1[4], q1[5]),
                         max3(q1[6], q1[7], max3(q1[8], q1[9], q1[10])));
         };
+        // 2^(x - mu) of 32 logits, packed to bf16 pairs; returns their sum.
+        // The subtraction and the sum run on element pairs (f32x2).
         auto expo = [&](const float *x, float mu, float *pk) {
-            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t mu2 = f2(mu, mu);
+            uint64_t acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
             for (int y = 0; y < 16; ++y) {
-                const float p0 = ex2(x[2 * y] - mu), p1 = ex2(x[2 * y + 1] - mu);
-                sacc[y & 3] += p0 + p1;
+                float e0, e1;
+                unf2(sub2(f2(x[2 * y], x[2 * y + 1]), mu2), e0, e1);
+                const float p0 = ex2(e0), p1 = ex2(e1);
+                acc[y & 1] = add2(acc[y & 1], f2(p0, p1));
                 pk[y] = __uint_as_float(pack_bf16(p0, p1));
             }
-            return (sacc[0] + sacc[1]) + (sacc[2] + sacc[3]);
+            float s0, s1, s2, s3;
+            unf2(acc[0], s0, s1);
+            unf2(acc[1], s2, s3);
+            return (s0 + s1) + (s2 + s3);
         };
 
         constexpr int DH = DP / 2;                 // O columns this warp rescales and stores
