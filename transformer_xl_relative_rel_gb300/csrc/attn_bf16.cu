@@ -592,25 +592,24 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const uint32_t ts = tl + TM_S + HN * half;
             tmem_ld_5x32(ts, ts + 32, tl + c[0], tl + c[1], tl + c[2], x, a);
         };
-        // the band of one 32-key block aligned to this row and added to its
-        // fp32 content logits.  The shift runs on the band rounded to fp16
-        // pairs (11-bit significand, saturated to the finite range): four
-        // select stages move whole registers (shift / 2) within the block's
-        // 32-register window, one byte permute moves half a register
-        // (shift & 1), then each fp16 is added to the fp32 logit.
+        // the band aligned to this row and added to its 64 fp32 content
+        // logits.  The shift runs on the band rounded to fp16 pairs (11-bit
+        // significand, saturated to the finite range): four select stages
+        // move whole registers (shift / 2) within a 48-register window, one
+        // byte permute moves half a register (shift & 1), then each fp16 is
+        // added to its fp32 logit.
         const uint32_t odd_sel = (shift & 1) ? 0x5432u : 0x3210u;
-        auto band_block = [&](const uint32_t *w, float *xb) {
-            uint32_t g[24];
+        auto band_all = [&](uint32_t *w, float *xb) {
 #pragma unroll
-            for (int y = 0; y < 24; ++y) g[y] = (shift & 16) ? w[y + 8] : w[y];
+            for (int y = 0; y < 40; ++y) w[y] = (shift & 16) ? w[y + 8] : w[y];
 #pragma unroll
-            for (int y = 0; y < 20; ++y) g[y] = (shift & 8) ? g[y + 4] : g[y];
+            for (int y = 0; y < 36; ++y) w[y] = (shift & 8) ? w[y + 4] : w[y];
 #pragma unroll
-            for (int y = 0; y < 18; ++y) g[y] = (shift & 4) ? g[y + 2] : g[y];
+            for (int y = 0; y < 34; ++y) w[y] = (shift & 4) ? w[y + 2] : w[y];
 #pragma unroll
-            for (int y = 0; y < 17; ++y) g[y] = (shift & 2) ? g[y + 1] : g[y];
+            for (int y = 0; y < 33; ++y) w[y] = (shift & 2) ? w[y + 1] : w[y];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(g[k], g[k + 1], odd_sel));
+            for (int k = 0; k < 32; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(w[k], w[k + 1], odd_sel));
         };
         // keys past the row's causal limit (j > M+i) get -inf
         auto mask_block = [&](float *xb, int first, int lim) {
@@ -749,8 +748,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 uint32_t hb[48];
 #pragma unroll
                 for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
-                band_block(hb, x);
-                band_block(hb + 16, x + 32);
+                band_all(hb, x);
                 if (diag) {
                     mask_block(x, 0, lim);
                     mask_block(x + 32, 32, lim);
