@@ -8,6 +8,7 @@ timed region; the per-step working set is far larger than L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the float64 CPU oracle
+    python bench.py --recompute-vs-reuse     # eval cost per token, window recompute vs memory reuse
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (weak scaling: independent sequences, no data-path collective); timing is the
@@ -384,6 +385,75 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------ main
+# ------------------------------------------------- recompute vs reuse (Table 9)
+TABLE9_PAPER = {3800: 1874, 2800: 1409, 1800: 773, 800: 363}   # Transformer-XL, Table 9 (whole model)
+
+
+def recompute_vs_reuse(args, local: int):
+    """Per-token evaluation cost of the attention, the two ways the paper
+    compares in its evaluation-speed section: the vanilla model re-runs a
+    whole window of W positions for every prediction (one call with L = W,
+    M = 0 gives B new tokens), Transformer-XL runs a 128-token segment against
+    a cached memory of W (one call with L = 128, M = W gives 128*B tokens).
+    Both through txl_rel_attn_fwd on the char-LM head shape (H 8, D 64).
+    One JSON line per attention length; the paper's ratio is for the whole
+    model on its own hardware (context, not a target)."""
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, D, seg = args.batch_t9, 8, 64, 128
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    dev = torch.device("cuda", local)
+
+    def layer(L, M):
+        T = L + M
+        def rnd(*shape):
+            return (0.45 * torch.randn(*shape, generator=gen, device=dev)).to(torch.bfloat16)
+        return dict(q=rnd(L, B, H, D), k=rnd(T, B, H, D), v=rnd(T, B, H, D), r=rnd(T, H, D),
+                    u=0.02 * torch.randn(H, D, generator=gen, device=dev),
+                    w=0.02 * torch.randn(H, D, generator=gen, device=dev),
+                    out=torch.empty(L, B, H, D, dtype=torch.bfloat16, device=dev), M=M)
+
+    def time_call(lay, reps):
+        call = lambda: txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                                        mem_len=lay["M"], out=lay["out"])
+        for _ in range(args.warmup):
+            call()
+        txl.check()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        txl.check()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    def flops(L, M):
+        return 6.0 * D * B * H * (L * M + L * (L + 1) / 2)
+
+    for W in sorted(TABLE9_PAPER):
+        reuse = layer(seg, W)
+        t_reuse = time_call(reuse, max(5, args.steps))
+        del reuse
+        recompute = layer(W, 0)
+        t_recompute = time_call(recompute, max(3, args.steps // 4))
+        del recompute
+        torch.cuda.empty_cache()
+        per_tok_reuse = t_reuse / (B * seg)
+        per_tok_recompute = t_recompute / B
+        print(json.dumps({
+            "metric": "eval attention time per token: recompute the window (vanilla) vs reuse the memory",
+            "attn_len": W, "batch": B, "heads": H, "d_head": D, "seg_len": seg, "dtype": "bf16",
+            "data": "synthetic",
+            "reuse_us_per_token": per_tok_reuse * 1e6, "recompute_us_per_token": per_tok_recompute * 1e6,
+            "slowdown": per_tok_recompute / per_tok_reuse,
+            "flop_ratio_per_token": (flops(W, 0) / B) / (flops(seg, W) / (B * seg)),
+            "reuse_call_us": t_reuse * 1e6, "recompute_call_us": t_recompute * 1e6,
+            "recompute_tflops": flops(W, 0) / t_recompute / 1e12, "reuse_tflops": flops(seg, W) / t_reuse / 1e12,
+            "paper_slowdown_whole_model": TABLE9_PAPER[W]}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,6 +465,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     ap.add_argument("--segments", type=int, default=0, help="override the workload's segment count")
+    ap.add_argument("--recompute-vs-reuse", action="store_true",
+                    help="per-token eval attention cost, sliding-window recompute vs memory reuse (Table 9)")
+    ap.add_argument("--batch-t9", type=int, default=22, help="batch for --recompute-vs-reuse")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
@@ -412,6 +485,9 @@ def main(argv=None):
         from transformer_xl_relative_rel_gb300 import _build
         _build.build()
         txl.load_library()
+
+    if args.recompute_vs_reuse:
+        return recompute_vs_reuse(args, local)
 
     w = WORKLOADS[args.workload]
     if args.layers or args.segments:

@@ -110,3 +110,21 @@ def test_bf16_full_size_unit_variance(name):
     err = np.abs(got - ref).max()
     assert err <= TOL_BF16, f"{name}: max abs err {err:.3e}"
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("B,H,L,M", [
+    (2, 2, 3800, 0),     # the sliding-window recompute of bench.py --recompute-vs-reuse
+    (2, 2, 128, 3800),   # its memory-reuse counterpart
+])
+def test_bf16_recompute_vs_reuse_shapes(B, H, L, M):
+    """The two call shapes the recompute-vs-reuse measurement times, on
+    unit-variance inputs, checked on sampled rows."""
+    s = inputs.LayerShape(batch=B, heads=H, d_head=64, seg_len=L, mem_len=M)
+    p = inputs.unit_layer(s, 900 + L)
+    dev, host = device_layer(p, torch.bfloat16)
+    out = run_library(dev, M)
+    torch.cuda.synchronize()
+    rows = inputs.sample_rows(s, 900 + L, n_random=128, all_heads_of_b0=False)
+    ref = oracle_rows(host, M, rows)
+    err = np.abs(gather_rows(out, rows) - ref).max()
+    assert err <= TOL_BF16, f"max abs err {err:.3e}"
