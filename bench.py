@@ -539,6 +539,8 @@ def main(argv=None):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
     roof["traffic"] = profiled_traffic(w.name)
+    if w.dtype == "bf16":
+        roof["issued_to_algorithmic_flops"] = w.issued_flops_per_call(splits) / flops_call
     roof["kernel"] = "rel_attn_bf16_kernel" if w.dtype == "bf16" else "rel_attn_f32_kernel"
     roof["launch_avg_us"] = attn_avg_s * 1e6
     roof["peak_source"] = f"{peak_kind} ({'MEASURED_PEAKS.json burst' if peak_kind == 'measured' else 'fallback'})"

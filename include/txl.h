@@ -55,7 +55,12 @@ typedef enum {
  *
  * q, k, v, r, out : device, dtype elements, layouts above; base addresses
  *                   16-byte aligned; out must not overlap any input.
- * u_bias, v_bias  : device, float32 [heads][d_head], 4-byte aligned.
+ * u_bias, v_bias  : device, float32 [heads][d_head], 4-byte aligned; either
+ *                   may be NULL, which drops its term: with both NULL the
+ *                   score is terms (a) + (b) only, the form of Shaw et al.
+ *                   the paper contrasts in Section 3.3 (r may then be any
+ *                   table, e.g. a learned R^ in place of W_kR R).  NULL needs
+ *                   heads*d_head <= 65536 (else TXL_ERR_UNSUPPORTED).
  * batch, heads, seg_len >= 0 (0 => nothing to do, TXL_OK, pointers unused);
  * mem_len >= 0; 1 <= d_head <= 128 for TXL_F32, 1 <= d_head <= 64 for
  * TXL_BF16 (larger: TXL_ERR_UNSUPPORTED).

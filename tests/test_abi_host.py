@@ -54,12 +54,21 @@ def test_attn_rejects_bad_arguments(lib):
     assert _attn(D=129, dt=0) == UNSUPPORTED
     assert _attn(D=65, dt=1) == UNSUPPORTED
     assert _attn(q=None) == INVALID
-    assert _attn(u=None) == INVALID
     assert _attn(out=None) == INVALID
     assert _attn(q=FAKE + 2) == INVALID            # misaligned
     assert _attn(u=FAKE + 2) == INVALID
     assert _attn(out=FAKE) == INVALID              # out overlaps q
     assert _attn(out=FAKE * 2 + 64) == INVALID     # out overlaps k
+
+
+def test_attn_accepts_absent_biases(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the call would launch on the fake pointers")
+    # a NULL bias drops its term (Shaw et al.'s form): the arguments pass and
+    # the call fails only at the device, which this machine does not have
+    assert _attn(u=None) == CUDA
+    assert _attn(u=None, w=None) == CUDA
 
 
 def test_attn_empty_is_a_no_op(lib):

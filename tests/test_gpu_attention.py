@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tests.helpers import (TOL_BF16, TOL_F32, device_layer, gather_rows, oracle_full,
                            oracle_rows, run_library, unit_shape)
 from transformer_xl_relative_rel_gb300 import inputs
@@ -128,3 +129,26 @@ def test_bf16_recompute_vs_reuse_shapes(B, H, L, M):
     ref = oracle_rows(host, M, rows)
     err = np.abs(gather_rows(out, rows) - ref).max()
     assert err <= TOL_BF16, f"max abs err {err:.3e}"
+
+
+# ------------------------------------ absent biases: the Shaw et al. form
+@pytest.mark.parametrize("dtype,tol,D", [(torch.float32, TOL_F32, 24), (torch.bfloat16, TOL_BF16, 64),
+                                         (torch.bfloat16, TOL_BF16, 41)])
+def test_absent_biases_are_the_shaw_form(dtype, tol, D):
+    """u_bias = v_bias = None: terms (a) + (b) only.  Same bits as explicit
+    zero biases, and the oracle with u = v = 0; one absent bias drops one term."""
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, L, M = 2, 2, 150, 140
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), 4100 + D)
+    dev, host = device_layer(p, dtype)
+    zero = torch.zeros_like(dev["u"])
+    got = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], None, None, mem_len=M).clone()
+    same = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], zero, zero, mem_len=M)
+    assert torch.equal(got, same)
+    z = np.zeros_like(host["u"])
+    ref = oracle.rel_attn(host["q"], host["k"], host["v"], host["r"], z, z, mem_len=M)
+    assert np.abs(got.double().cpu().numpy() - ref).max() <= tol
+    # only u absent: the global content bias (c) goes, (d) stays
+    got_u = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], None, dev["w"], mem_len=M).clone()
+    same_u = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], zero, dev["w"], mem_len=M)
+    assert torch.equal(got_u, same_u)

@@ -113,6 +113,45 @@ def test_four_term_bruteforce(oracle_lib, B, H, D, L, M):
     np.testing.assert_allclose(got, ref, rtol=0, atol=TOL * max(1.0, np.abs(ref).max()))
 
 
+def _shaw_bruteforce(h_ext, Wq, Wk, Wv, Rhat, B, H, D, L, M):
+    """Shaw et al.'s form as Section 3.3 describes it: terms (a) and (b) only,
+    with one free relative-position table Rhat [distance][H*D] in place of
+    W_kR R (no global biases)."""
+    T = M + L
+    out = np.zeros((L, B, H, D))
+    for b in range(B):
+        for hd in range(H):
+            sl = slice(hd * D, (hd + 1) * D)
+            for i in range(L):
+                qi = h_ext[M + i, b] @ Wq[:, sl]
+                scores = np.full(T, -np.inf)
+                for j in range(M + i + 1):
+                    kj = h_ext[j, b] @ Wk[:, sl]
+                    scores[j] = (qi @ kj + qi @ Rhat[M + i - j, sl]) / np.sqrt(D)
+                p = _softmax_rows(scores[None, :])[0]
+                out[i, b, hd] = p @ (h_ext[:, b] @ Wv[:, sl])
+    return out
+
+
+@pytest.mark.parametrize("B,H,D,L,M", [(2, 2, 4, 5, 3), (1, 2, 3, 6, 0)])
+def test_shaw_form_is_zero_bias_case(oracle_lib, B, H, D, L, M):
+    """Terms (a) + (b) with a free table == the oracle with u = v = 0 and the
+    table reversed as in Appendix B."""
+    g = np.random.Generator(np.random.PCG64(300 + L + M))
+    T, dm = M + L, H * D
+    h_ext = _rand((T, B, dm), g)
+    Wq, Wk, Wv = (_rand((dm, dm), g) * 0.5 for _ in range(3))
+    Rhat = _rand((T, dm), g)
+    ref = _shaw_bruteforce(h_ext, Wq, Wk, Wv, Rhat, B, H, D, L, M)
+    q = (h_ext[M:] @ Wq).reshape(L, B, H, D)
+    k = (h_ext @ Wk).reshape(T, B, H, D)
+    v = (h_ext @ Wv).reshape(T, B, H, D)
+    r = np.stack([Rhat[T - 1 - t] for t in range(T)]).reshape(T, H, D)
+    zero = np.zeros((H, D))
+    got = oracle.rel_attn(q, k, v, r, zero, zero, mem_len=M)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=TOL * max(1.0, np.abs(ref).max()))
+
+
 # ---------------------------------------------------------------------------
 # 2. Appendix B: B~ = (q+v) Q^T, then row i left-shifted by L-1-i
 # ---------------------------------------------------------------------------

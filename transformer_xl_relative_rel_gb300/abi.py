@@ -104,8 +104,10 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
     """Relative attention of one layer (Transformer-XL Section 3.3).
 
     q: [L, B, H, D]; k, v: [M+L, B, H, D]; r: [M+L, H, D] (reversed table);
-    u_bias, v_bias: [H, D] float32; all CUDA, contiguous, same dtype
-    (float32 or bfloat16) except the biases.  Returns ``out`` [L, B, H, D].
+    u_bias, v_bias: [H, D] float32, or None to drop that bias term (both
+    None: Shaw et al.'s form, terms (a) + (b) only); all CUDA, contiguous,
+    same dtype (float32 or bfloat16) except the biases.  Returns ``out``
+    [L, B, H, D].
     """
     import torch
     L, B, H, D = q.shape
@@ -117,10 +119,10 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         if t.dtype != q.dtype:
             raise TypeError(f"{name} dtype {t.dtype} != q dtype {q.dtype}")
     for name, t in (("u_bias", u_bias), ("v_bias", v_bias)):
-        if tuple(t.shape) != (H, D) or t.dtype != torch.float32:
-            raise ValueError(f"{name} must be float32 [{H}, {D}]")
+        if t is not None and (tuple(t.shape) != (H, D) or t.dtype != torch.float32):
+            raise ValueError(f"{name} must be float32 [{H}, {D}] or None")
     for t in (q, k, v, r, u_bias, v_bias):
-        if not t.is_cuda or not t.is_contiguous():
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("all tensors must be contiguous CUDA tensors")
     if out is None:
         out = torch.empty_like(q)

@@ -96,7 +96,31 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 bool aligned(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
+// zeros standing in for an absent bias (Shaw et al.'s form has no u, v terms)
+constexpr size_t kZeroBiasFloats = 1 << 16;
+static __device__ __align__(256) float g_zero_bias[kZeroBiasFloats];
+std::mutex g_zb_mu;
+void *g_zb_addr[64] = {nullptr};
+
 }  // namespace
+
+cudaError_t zero_bias(size_t count, const float **out)
+{
+    if (count > kZeroBiasFloats) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+    std::lock_guard<std::mutex> lock(g_zb_mu);
+    if (!g_zb_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_zero_bias);
+        if (e != cudaSuccess) return e;
+        g_zb_addr[dev] = p;
+    }
+    *out = (const float *)g_zb_addr[dev];
+    return cudaSuccess;
+}
 }  // namespace txl
 
 using namespace txl;
@@ -113,7 +137,7 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
     if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
     if (d_head > 128) return TXL_ERR_UNSUPPORTED;
     if (dtype == TXL_BF16 && d_head > 64) return TXL_ERR_UNSUPPORTED;
-    if (!q || !k || !v || !r || !u_bias || !v_bias || !out) return TXL_ERR_INVALID;
+    if (!q || !k || !v || !r || !out) return TXL_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(r, 16) ||
         !aligned(out, 16) || !aligned(u_bias, 4) || !aligned(v_bias, 4))
         return TXL_ERR_INVALID;
@@ -132,6 +156,15 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
         return TXL_ERR_INVALID;
     if ((seg_len + 31) / 32 > 65535) return TXL_ERR_UNSUPPORTED;
 
+    // an absent bias drops its term (terms (a) + (b) only: Shaw et al.'s form)
+    if (!u_bias || !v_bias) {
+        const float *z = nullptr;
+        const cudaError_t ze = zero_bias((size_t)heads * (size_t)d_head, &z);
+        if (ze == cudaErrorNotSupported) return TXL_ERR_UNSUPPORTED;
+        if (ze != cudaSuccess) return cuda_fail(ze);
+        if (!u_bias) u_bias = z;
+        if (!v_bias) v_bias = z;
+    }
     AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len};
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;

@@ -32,6 +32,12 @@ cudaError_t launch_rollover(void *dst, const void *src, size_t bytes, int elem_s
 
 int device_sm_count();
 
+// Device address of `count` zero floats on the current device (a fixed array
+// in the library), standing in for an absent u or v bias.  Returns
+// cudaErrorNotSupported when count exceeds the array, or the CUDA error of
+// the lookup.
+cudaError_t zero_bias(size_t count, const float **out);
+
 // records `e` as the thread's last CUDA error (reported by txl_last_cuda_error)
 // and clears the runtime's error state; returns e
 cudaError_t note_cuda_error(cudaError_t e);

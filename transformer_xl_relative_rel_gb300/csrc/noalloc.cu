@@ -80,7 +80,7 @@ extern "C" txl_status txl_rel_attn_fwd_noalloc(const void *q, const void *k, con
     if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
     if (d_head > 128) return TXL_ERR_UNSUPPORTED;
     if (dtype == TXL_BF16 && d_head > 64) return TXL_ERR_UNSUPPORTED;
-    if (!q || !k || !v || !r || !u_bias || !v_bias || !out) return TXL_ERR_INVALID;
+    if (!q || !k || !v || !r || !out) return TXL_ERR_INVALID;
     if (!na_aligned(q, 16) || !na_aligned(k, 16) || !na_aligned(v, 16) || !na_aligned(r, 16) ||
         !na_aligned(out, 16) || !na_aligned(u_bias, 4) || !na_aligned(v_bias, 4))
         return TXL_ERR_INVALID;
@@ -99,6 +99,19 @@ extern "C" txl_status txl_rel_attn_fwd_noalloc(const void *q, const void *k, con
         return TXL_ERR_INVALID;
     if ((seg_len + 31) / 32 > 65535) return TXL_ERR_UNSUPPORTED;
 
+    // an absent bias drops its term (Shaw et al.'s form); the zeros are a
+    // fixed array too, so nothing is allocated here either
+    if (!u_bias || !v_bias) {
+        const float *z = nullptr;
+        const cudaError_t ze = zero_bias((size_t)heads * (size_t)d_head, &z);
+        if (ze == cudaErrorNotSupported) return TXL_ERR_UNSUPPORTED;
+        if (ze != cudaSuccess) {
+            note_cuda_error(ze);
+            return TXL_ERR_CUDA;
+        }
+        if (!u_bias) u_bias = z;
+        if (!v_bias) v_bias = z;
+    }
     AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len};
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;

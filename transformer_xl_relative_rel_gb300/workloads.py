@@ -32,6 +32,23 @@ class Workload:
         pairs = s.seg_len * s.mem_len + s.seg_len * (s.seg_len + 1) // 2
         return 6.0 * s.d_head * s.batch * s.heads * pairs
 
+    def issued_flops_per_call(self, splits: int = 1) -> float:
+        """FLOPs the bf16 kernel issues to the tensor cores for one call: per
+        128-key tile of a 128-row query tile, the content tile, one 128-row
+        band chunk and the P.V tile (each 2*128*128*DP, DP = D padded to 16),
+        plus band chunk 0 once per work item.  Tiles past a query tile's
+        causal limit are not issued."""
+        s = self.shape
+        dp = (s.d_head + 15) // 16 * 16
+        per = 2.0 * 128 * 128 * dp
+        nqt = (s.seg_len + 127) // 128
+        total = 0.0
+        for qt in range(nqt):
+            kend = min(s.klen, s.mem_len + min(s.seg_len, (qt + 1) * 128))
+            ntile = (kend + 127) // 128
+            total += 3 * per * ntile + per * min(splits, ntile)
+        return total * s.batch * s.heads
+
     def bytes_per_call(self) -> float:
         """Minimum HBM bytes of one layer call: q and out once, k and v once,
         r once (element size of the workload's dtype; u, v biases are tiny)."""
