@@ -94,6 +94,43 @@ txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int me
                           int seg_len, int d_model, txl_dtype dtype, void *stream);
 
 /*
+ * txl_rel_attn_fwd_ring -- txl_rel_attn_fwd with k and v stored as a ring.
+ * The extended context [memory; segment] of Section 3.2 slides forward by L
+ * rows per segment; kept in a ring of M+L rows, a segment adds only its L new
+ * rows (txl_ring_append) instead of moving the M memory rows.  The paper has
+ * no counterpart to this storage order; the result is exactly that of
+ * txl_rel_attn_fwd on the unrolled context.
+ *
+ * k, v     : device, [M+L][batch][heads][d_head]; the context's key j (j = 0
+ *            is the oldest memory row, j = M+L-1 the segment's last row) is
+ *            stored at row (kv_start + j) mod (M+L).
+ * kv_start : 0 <= kv_start < M+L (0 gives txl_rel_attn_fwd's layout).
+ * Everything else as txl_rel_attn_fwd.  With bf16 and d_head = 64 the rows
+ * are read by TMA when kv_start and M+L are multiples of 8, by thread loads
+ * otherwise (same result, slower).
+ */
+txl_status txl_rel_attn_fwd_ring(const void *q, const void *k, const void *v, const void *r,
+                                 const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                 int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
+                                 void *out, void *stream);
+
+/*
+ * txl_ring_append -- write n_rows new rows into a ring of ring_len rows at
+ * rows (start + i) mod ring_len, i = 0 .. n_rows-1 (the oldest rows of the
+ * ring, for a ring kept as above: start = the current kv_start, after which
+ * the next kv_start is (start + n_rows) mod ring_len).  Serves both the
+ * cached hidden states of Section 3.2 and projected k / v rings.
+ *
+ * ring : device, [ring_len][row_elems] dtype elements.
+ * rows : device, [n_rows][row_elems]; must not overlap ring.
+ * 0 <= n_rows <= ring_len, 0 <= start < ring_len (unless nothing to do),
+ * row_elems >= 0; element-aligned pointers.  Bit-exact copy (one or two
+ * contiguous runs).  Same error behaviour as txl_mem_update.
+ */
+txl_status txl_ring_append(void *ring, const void *rows, int ring_len, int n_rows, int row_elems,
+                           int start, txl_dtype dtype, void *stream);
+
+/*
  * txl_rel_attn_fwd_noalloc -- txl_rel_attn_fwd for callers that may not
  * allocate device memory.  (No counterpart in the paper: this is a deployment
  * variant of the same computation.)

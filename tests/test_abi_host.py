@@ -101,3 +101,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(abi, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(txl.TxlError):
         abi.load_library()
+
+
+def test_ring_calls_reject_bad_arguments(lib):
+    f = lib.txl_rel_attn_fwd_ring
+    args = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 2, 8, 8, 2, 16]
+    assert f(*args, -1, 1, FAKE * 7, None) == INVALID      # kv_start < 0
+    assert f(*args, 16, 1, FAKE * 7, None) == INVALID      # kv_start >= M+L
+    g = lib.txl_ring_append
+    assert g(FAKE, FAKE * 4, 10, 11, 8, 0, 1, None) == INVALID   # more rows than the ring
+    assert g(FAKE, FAKE * 4, 10, 3, 8, 10, 1, None) == INVALID   # start outside the ring
+    assert g(FAKE, FAKE * 4, 10, 3, 8, -1, 1, None) == INVALID
+    assert g(FAKE, FAKE + 8, 10, 3, 8, 0, 1, None) == INVALID    # rows overlap the ring
+    assert g(None, FAKE * 4, 10, 3, 8, 0, 1, None) == INVALID
+    assert g(FAKE, FAKE * 4, 10, 3, 8, 0, 9, None) == UNSUPPORTED
+    assert g(None, None, 10, 0, 8, 0, 1, None) == OK              # nothing to copy

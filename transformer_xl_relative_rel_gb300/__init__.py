@@ -5,8 +5,8 @@ declared in ``include/txl.h``); ``abi`` is the thin ctypes binding with the same
 entry-point names.  Importing this package does not load the library; the first
 call does, and raises ``TxlError`` if it was not built.
 """
-from .abi import (TxlError, TXL_F32, TXL_BF16, rel_attn_fwd, mem_update,  # noqa: F401
-                  check, load_library, library_path, status_string)
+from .abi import (TxlError, TXL_F32, TXL_BF16, rel_attn_fwd, rel_attn_fwd_ring,  # noqa: F401
+                  mem_update, ring_append, check, load_library, library_path, status_string)
 
-__all__ = ["TxlError", "TXL_F32", "TXL_BF16", "rel_attn_fwd", "mem_update", "check",
-           "load_library", "library_path", "status_string"]
+__all__ = ["TxlError", "TXL_F32", "TXL_BF16", "rel_attn_fwd", "rel_attn_fwd_ring", "mem_update",
+           "ring_append", "check", "load_library", "library_path", "status_string"]

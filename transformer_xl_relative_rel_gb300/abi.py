@@ -24,7 +24,8 @@ _lib: Optional[ctypes.CDLL] = None
 
 #: every symbol include/txl.h declares (checked by the host-side tests)
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
-           "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc")
+           "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
+           "txl_rel_attn_fwd_ring", "txl_ring_append")
 
 
 class TxlError(RuntimeError):
@@ -51,6 +52,10 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd.restype = i
     lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd_noalloc.restype = i
+    lib.txl_rel_attn_fwd_ring.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
+    lib.txl_rel_attn_fwd_ring.restype = i
+    lib.txl_ring_append.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.txl_ring_append.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_mem_update.restype = i
     lib.txl_check.argtypes = [vp]
@@ -100,19 +105,10 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr() if t is not None and t.numel() > 0 else None
 
 
-def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None):
-    """Relative attention of one layer (Transformer-XL Section 3.3).
-
-    q: [L, B, H, D]; k, v: [M+L, B, H, D]; r: [M+L, H, D] (reversed table);
-    u_bias, v_bias: [H, D] float32, or None to drop that bias term (both
-    None: Shaw et al.'s form, terms (a) + (b) only); all CUDA, contiguous,
-    same dtype (float32 or bfloat16) except the biases.  Returns ``out``
-    [L, B, H, D].
-    """
+def _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out):
     import torch
     L, B, H, D = q.shape
     T = mem_len + L
-    code = _dtype_code(q)
     for name, t, shp in (("k", k, (T, B, H, D)), ("v", v, (T, B, H, D)), ("r", r, (T, H, D))):
         if tuple(t.shape) != shp:
             raise ValueError(f"{name} must be {list(shp)}, got {list(t.shape)}")
@@ -128,11 +124,54 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         out = torch.empty_like(q)
     elif tuple(out.shape) != (L, B, H, D) or out.dtype != q.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    return out
+
+
+def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None):
+    """Relative attention of one layer (Transformer-XL Section 3.3).
+
+    q: [L, B, H, D]; k, v: [M+L, B, H, D]; r: [M+L, H, D] (reversed table);
+    u_bias, v_bias: [H, D] float32, or None to drop that bias term (both
+    None: Shaw et al.'s form, terms (a) + (b) only); all CUDA, contiguous,
+    same dtype (float32 or bfloat16) except the biases.  Returns ``out``
+    [L, B, H, D].
+    """
+    L, B, H, D = q.shape
+    out = _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
     st = load_library().txl_rel_attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
-        B, mem_len, L, H, D, code, _ptr(out), _stream_ptr(stream))
+        B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd")
     return out
+
+
+def rel_attn_fwd_ring(q, k, v, r, u_bias, v_bias, mem_len: int, kv_start: int, out=None, stream=None):
+    """rel_attn_fwd with k, v stored as a ring of M+L rows: the context's key j
+    (0 = oldest memory row) is at row (kv_start + j) mod (M+L)."""
+    L, B, H, D = q.shape
+    out = _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
+    st = load_library().txl_rel_attn_fwd_ring(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+        B, mem_len, L, H, D, int(kv_start), _dtype_code(q), _ptr(out), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_ring")
+    return out
+
+
+def ring_append(ring, rows, start: int, stream=None):
+    """Write ``rows`` [n, ...] into ``ring`` [ring_len, ...] at rows
+    (start + i) mod ring_len; returns the next start, (start + n) mod ring_len."""
+    n = rows.shape[0]
+    ring_len = ring.shape[0]
+    if tuple(rows.shape[1:]) != tuple(ring.shape[1:]) or rows.dtype != ring.dtype:
+        raise ValueError("rows must match the ring's row shape and dtype")
+    for t in (ring, rows):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    row_elems = ring[0].numel() if ring_len else 0
+    st = load_library().txl_ring_append(_ptr(ring), _ptr(rows), ring_len, n, row_elems, int(start),
+                                        _dtype_code(ring), _stream_ptr(stream))
+    _raise(st, "txl_ring_append")
+    return (start + n) % ring_len if ring_len else 0
 
 
 def rel_attn_fwd_noalloc(q, k, v, r, u_bias, v_bias, mem_len: int, out, stream=None):

@@ -127,14 +127,15 @@ using namespace txl;
 
 extern "C" {
 
-txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
-                            const float *u_bias, const float *v_bias,
-                            int batch, int mem_len, int seg_len, int heads, int d_head,
-                            txl_dtype dtype, void *out, void *stream)
+static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
+                                  const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                  int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
+                                  void *out, void *stream)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
     if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
+    if (kv_start < 0 || (long)kv_start >= (long)mem_len + seg_len) return TXL_ERR_INVALID;
     if (d_head > 128) return TXL_ERR_UNSUPPORTED;
     if (dtype == TXL_BF16 && d_head > 64) return TXL_ERR_UNSUPPORTED;
     if (!q || !k || !v || !r || !out) return TXL_ERR_INVALID;
@@ -165,7 +166,7 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
         if (!u_bias) u_bias = z;
         if (!v_bias) v_bias = z;
     }
-    AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len};
+    AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len, kv_start};
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     if (dtype == TXL_F32) {
@@ -180,6 +181,24 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
         e = launch_attn_bf16(a, splits, scratch, s);
     }
     return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+}
+
+txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
+                            const float *u_bias, const float *v_bias,
+                            int batch, int mem_len, int seg_len, int heads, int d_head,
+                            txl_dtype dtype, void *out, void *stream)
+{
+    return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0,
+                           dtype, out, stream);
+}
+
+txl_status txl_rel_attn_fwd_ring(const void *q, const void *k, const void *v, const void *r,
+                                 const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                 int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
+                                 void *out, void *stream)
+{
+    return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head,
+                           kv_start, dtype, out, stream);
 }
 
 txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int mem_len,
@@ -198,6 +217,28 @@ txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int me
     if (overlaps(mem_next, nbytes, ext_ctx, T * row)) return TXL_ERR_INVALID;
     const void *src = (const unsigned char *)ext_ctx + (size_t)seg_len * row;
     cudaError_t e = launch_rollover(mem_next, src, nbytes, (int)esz, (cudaStream_t)stream);
+    return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+}
+
+txl_status txl_ring_append(void *ring, const void *rows, int ring_len, int n_rows, int row_elems,
+                           int start, txl_dtype dtype, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (ring_len < 0 || n_rows < 0 || row_elems < 0 || n_rows > ring_len) return TXL_ERR_INVALID;
+    if (n_rows == 0 || row_elems == 0) return TXL_OK;
+    if (start < 0 || start >= ring_len) return TXL_ERR_INVALID;
+    if (!ring || !rows) return TXL_ERR_INVALID;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (!aligned(ring, esz) || !aligned(rows, esz)) return TXL_ERR_INVALID;
+    const size_t row = (size_t)row_elems * esz;
+    if (overlaps(ring, (size_t)ring_len * row, rows, (size_t)n_rows * row)) return TXL_ERR_INVALID;
+    // rows [start, start + n) mod ring_len: one run up to the end, one from row 0
+    const size_t first = (size_t)(ring_len - start) < (size_t)n_rows ? (size_t)(ring_len - start) : (size_t)n_rows;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_rollover((unsigned char *)ring + (size_t)start * row, rows, first * row, (int)esz, s);
+    if (e == cudaSuccess && first < (size_t)n_rows)
+        e = launch_rollover(ring, (const unsigned char *)rows + first * row, ((size_t)n_rows - first) * row,
+                            (int)esz, s);
     return e == cudaSuccess ? TXL_OK : cuda_fail(e);
 }
 

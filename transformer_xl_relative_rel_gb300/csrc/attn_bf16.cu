@@ -76,6 +76,7 @@ struct Params {
     int B, H, D, L, M, T;
     int nqt, splits;
     int items;          // B*H*nqt*splits work items
+    int kv_start;       // K, V rows form a ring: key j at row (kv_start + j) mod T
     float sl2;          // log2(e) / sqrt(D)
 };
 
@@ -202,7 +203,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 // element, when D is odd) is written as zero; later padding was zeroed once.
 __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, const __nv_bfloat16 *src,
                                                long row0_elems, long row_stride, int first_row,
-                                               int limit, int D, int lane)
+                                               int limit, int D, int lane, int ring_start = 0)
 {
     const int npairs = (D + 1) >> 1;     // element pairs covering D (<= 32 for D <= 64)
     // 16 rows at a time: all their loads are issued before any is used
@@ -213,7 +214,9 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
         for (int k = 0; k < 16; ++k) {
             const int row = first_row + r0 + k;
             const bool ok = row >= 0 && row < limit;
-            const long e0 = row0_elems + (long)row * row_stride;    // first element of the row
+            // a ring of `limit` rows stores logical row j at (ring_start + j) mod limit
+            const int srow = row + ring_start < limit ? row + ring_start : row + ring_start - limit;
+            const long e0 = row0_elems + (long)srow * row_stride;   // first element of the row
             odd[k] = (int)(e0 & 1);
             // lane l reads word l of the row (elements 2l-odd .. 2l+1-odd);
             // only the words that overlap the row are read
@@ -285,6 +288,7 @@ template <int DP, bool kTma>
 __global__ void __launch_bounds__(NT, 1)
 rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8,
                      const Params p)
 {
     using S = Smem<DP>;
@@ -330,6 +334,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_r);
             prefetch_tmap(&tm_q);
+            if (p.kv_start) {
+                prefetch_tmap(&tm_k8);
+                prefetch_tmap(&tm_v8);
+            }
         }
     }
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
@@ -404,19 +412,38 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
                     if (kTma) {
                         if (lane == 0) {
+                            // K, V rows may sit in a ring (key j at row (kv_start + j) mod T)
+                            int s0 = p.kv_start + j0;
+                            if (s0 >= p.T) s0 -= p.T;
                             mbar_arrive_expect_tx(bar(S::B_FULL + st), S::STAGE);
-                            tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, it.bh);
-                            tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, it.bh);
+                            if (p.kv_start == 0 || s0 + BN <= p.T) {
+                                // one box; in the plain layout rows past the last key
+                                // are zero-filled
+                                tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, s0, it.bh);
+                                tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, s0, it.bh);
+                            } else {
+                                // the tile crosses the ring's end: sixteen 8-row boxes
+                                // (one swizzle atom each, 1 KB apart in the stage), each
+                                // from its own ring row; rows past the last key are
+                                // other ring rows (finite, masked)
+                                for (int m = 0; m < BN / 8; ++m) {
+                                    const int sr = (s0 + 8 * m) % p.T;   // T may be below 128
+                                    tma_load_3d(dst + 1024u * m, &tm_k8, bar(S::B_FULL + st), 0, sr, it.bh);
+                                    tma_load_3d(dst + S::TILE + 1024u * m, &tm_v8, bar(S::B_FULL + st), 0, sr,
+                                                it.bh);
+                                }
+                            }
                             tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, it.h);
                         }
                     } else {
                         unsigned char *d = smem + S::ST0 + st * S::STAGE;
                         if (warp == 0) {
-                            warp_load_rows(d, BN, p.k, it.head_off, qkv_row, j0, p.T, p.D, lane);
+                            warp_load_rows(d, BN, p.k, it.head_off, qkv_row, j0, p.T, p.D, lane, p.kv_start);
                             warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)it.h * p.D, (long)p.H * p.D, crow,
                                            p.T, p.D, lane);
                         } else {
-                            warp_load_rows(d + S::TILE, BN, p.v, it.head_off, qkv_row, j0, p.T, p.D, lane);
+                            warp_load_rows(d + S::TILE, BN, p.v, it.head_off, qkv_row, j0, p.T, p.D, lane,
+                                           p.kv_start);
                         }
                         fence_proxy_async_smem();
                         mbar_arrive(bar(S::B_FULL + st));
@@ -900,7 +927,8 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
 
 template <int DP, bool kTma>
 cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                     const CUtensorMap &mr, const CUtensorMap &mq, cudaStream_t s)
+                     const CUtensorMap &mr, const CUtensorMap &mq, const CUtensorMap &mk8,
+                     const CUtensorMap &mv8, cudaStream_t s)
 {
     const uint32_t smem = Smem<DP>::TOTAL;
     auto kern = rel_attn_bf16_kernel<DP, kTma>;
@@ -908,7 +936,7 @@ cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM, each walks its share of the work items
     const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
-    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, p);
+    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, mk8, mv8, p);
     return cudaGetLastError();
 }
 
@@ -988,27 +1016,34 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
         p.part_lse = (float *)((char *)scratch + rows * DP * 4);
     }
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
-    CUtensorMap mk, mv, mr, mq;
+    p.kv_start = a.kv_start;
+    CUtensorMap mk, mv, mr, mq, mk8, mv8;
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
     memset(&mr, 0, sizeof(mr));
     memset(&mq, 0, sizeof(mq));
+    memset(&mk8, 0, sizeof(mk8));
+    memset(&mv8, 0, sizeof(mv8));
     // TMA for D = 64 (128-byte rows); the biases then come by bulk copy,
-    // which wants them 16-byte aligned
-    const bool tma = a.D == 64 && ((uintptr_t)a.u & 15) == 0 && ((uintptr_t)a.w & 15) == 0;
+    // which wants them 16-byte aligned.  A K/V ring whose start or length is
+    // not a multiple of 8 rows is read by the thread loader (the 8-row boxes
+    // of a wrapping tile must not straddle the ring's end).
+    const bool ring_ok = a.kv_start == 0 || (a.kv_start % 8 == 0 && p.T % 8 == 0);
+    const bool tma = a.D == 64 && ((uintptr_t)a.u & 15) == 0 && ((uintptr_t)a.w & 15) == 0 && ring_ok;
     if (tma) {
         const long bhn = (long)a.B * a.H;
         const long rs = bhn * a.D;
         if (!make_map(&mk, a.k, p.T, rs, bhn, BN) || !make_map(&mv, a.v, p.T, rs, bhn, BN) ||
-            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM))
+            !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM) ||
+            !make_map(&mk8, a.k, p.T, rs, bhn, 8) || !make_map(&mv8, a.v, p.T, rs, bhn, 8))
             return cudaErrorInvalidValue;
     }
     cudaError_t e;
     switch (DP) {
-    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, s) : launch_t<16, false>(p, mk, mv, mr, mq, s); break;
-    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, s) : launch_t<32, false>(p, mk, mv, mr, mq, s); break;
-    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, s) : launch_t<48, false>(p, mk, mv, mr, mq, s); break;
-    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, s) : launch_t<64, false>(p, mk, mv, mr, mq, s); break;
+    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<16, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
+    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<32, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
+    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<48, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
+    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
     }
     if (e != cudaSuccess || splits == 1) return e;
     rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(NT)
 rel_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                     const float *__restrict__ v, const float *__restrict__ r,
                     const float *__restrict__ u, const float *__restrict__ w,
-                    float *__restrict__ out, int B, int H, int D, int L, int M)
+                    float *__restrict__ out, int B, int H, int D, int L, int M, int kv_start)
 {
     extern __shared__ float smem[];
     const int DP = D + 1;                 // odd pitch: rows land in distinct banks
@@ -81,8 +81,10 @@ rel_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
             const int j = j0 + c;
             float kk = 0.f, vv = 0.f;
             if (j < T) {
-                kk = k[(long)j * rowstride + hoff + d];
-                vv = v[(long)j * rowstride + hoff + d];
+                // K, V may form a ring: key j at row (kv_start + j) mod T
+                const int sj = j + kv_start < T ? j + kv_start : j + kv_start - T;
+                kk = k[(long)sj * rowstride + hoff + d];
+                vv = v[(long)sj * rowstride + hoff + d];
             }
             ks[c * DP + d] = kk;
             vs[c * DP + d] = vv;
@@ -166,7 +168,7 @@ cudaError_t launch(const AttnArgs &a, cudaStream_t s)
     dim3 grid(a.B * a.H, (a.L + BR - 1) / BR);
     rel_attn_f32_kernel<DMAX><<<grid, NT, smem, s>>>(
         (const float *)a.q, (const float *)a.k, (const float *)a.v, (const float *)a.r, a.u, a.w,
-        (float *)a.out, a.B, a.H, a.D, a.L, a.M);
+        (float *)a.out, a.B, a.H, a.D, a.L, a.M, a.kv_start);
     return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@ struct AttnArgs {
     const float *u, *w;           // u and v biases, [H][D] float32
     void *out;
     int B, H, D, L, M;
+    int kv_start = 0;             // K, V in a ring of M+L rows: key j at row (kv_start + j) mod (M+L)
 };
 
 // fp32 SIMT path (attn_f32.cu)
