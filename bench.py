@@ -182,10 +182,11 @@ class Chain:
     u, v-bias, the attention output and two extended-context buffers
     [M+L, B, d_model] that trade places every segment."""
 
-    def __init__(self, w: Workload, device, ring: bool = False):
+    def __init__(self, w: Workload, device, ring: bool = False, pad: int = 0):
         s = w.shape
         self.w = w
         self.ring = ring
+        self.pad = pad if pad and pad != s.d_head else 0
         self.dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         B, H, D, L, M, T, dm = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len, s.klen, s.d_model
         g = torch.Generator(device=device).manual_seed(w.seed)
@@ -209,11 +210,17 @@ class Chain:
                 u = torch.randn(H, D, generator=g, device=device) * 0.02
                 wb = torch.randn(H, D, generator=g, device=device) * 0.02
             r = (sin @ wr).flip(0).reshape(T, H, D)
+            if self.pad:
+                # head vectors stored with `pad` elements (zeros past D), the
+                # layout txl_project_heads / txl_rel_table write
+                def padh(x):
+                    return torch.nn.functional.pad(x, (0, self.pad - D))
+                q, k, v, r, u, wb = (padh(x) for x in (q, k, v, r, u, wb))
             self.layers.append(dict(
                 q=q.to(self.dtype).contiguous(), k=k.to(self.dtype).contiguous(),
                 v=v.to(self.dtype).contiguous(), r=r.to(self.dtype).contiguous(),
                 u=u.float().contiguous(), w=wb.float().contiguous(),
-                out=torch.empty(L, B, H, D, dtype=self.dtype, device=device), start=0,
+                out=torch.empty(L, B, H, self.pad or D, dtype=self.dtype, device=device), start=0,
                 ext=[ext.to(self.dtype).contiguous(), torch.empty(T, B, dm, dtype=self.dtype, device=device)]))
         torch.cuda.synchronize()
 
@@ -226,28 +233,41 @@ class Chain:
                 if attn_events is not None:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
-                if self.ring:
-                    txl.rel_attn_fwd_ring(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
-                                          mem_len=M, kv_start=lay["start"], out=lay["out"])
-                else:
-                    txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
-                                     mem_len=M, out=lay["out"])
+                self.attn(txl, lay)
                 if attn_events is not None:
                     e1.record()
                     attn_events.append((e0, e1))
-                if self.ring:
-                    # the context is a ring of T rows: the segment's L rows
-                    # replace the oldest L (the hidden states here; a k / v
-                    # ring takes its projected rows the same way)
-                    w0 = (lay["start"] + M) % T
-                    txl.ring_append(lay["ext"][0], lay["ext"][1][:L], w0)
-                    lay["start"] = (lay["start"] + L) % T
-                    launches += 1 + self.attn_extra_launches + (2 if w0 + L > T else 1)
-                else:
-                    txl.mem_update(lay["ext"][1], lay["ext"][0], mem_len=M)
-                    lay["ext"].reverse()
-                    launches += 1 + self.attn_extra_launches + 1
+                launches += 1 + self.attn_extra_launches + self.memory(txl, lay)
         return launches
+
+    def attn(self, txl, lay):
+        """The layer's attention call in this chain's storage mode."""
+        M = self.w.shape.mem_len
+        if self.ring:
+            txl.rel_attn_fwd_ring(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                                  mem_len=M, kv_start=lay["start"], out=lay["out"])
+        elif self.pad:
+            txl.rel_attn_fwd_padded(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                                    mem_len=M, d_head=self.w.shape.d_head, out=lay["out"])
+        else:
+            txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
+                             mem_len=M, out=lay["out"])
+
+    def memory(self, txl, lay) -> int:
+        """The layer's memory update; returns the kernels it launched."""
+        M, L = self.w.shape.mem_len, self.w.shape.seg_len
+        T = M + L
+        if self.ring:
+            # the context is a ring of T rows: the segment's L rows replace the
+            # oldest L (the hidden states here; a k / v ring takes its
+            # projected rows the same way)
+            w0 = (lay["start"] + M) % T
+            txl.ring_append(lay["ext"][0], lay["ext"][1][:L], w0)
+            lay["start"] = (lay["start"] + L) % T
+            return 2 if w0 + L > T else 1
+        txl.mem_update(lay["ext"][1], lay["ext"][0], mem_len=M)
+        lay["ext"].reverse()
+        return 1
 
     @property
     def working_set_bytes(self) -> int:
@@ -299,9 +319,8 @@ def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
                 for key in ("q", "k", "v", "r", "u", "w"):
                     lay[key].copy_(hl[key], non_blocking=True)
                 lay["ext"][0].copy_(hl["ext"], non_blocking=True)
-                txl.rel_attn_fwd(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"],
-                                 mem_len=M, out=lay["out"])
-                txl.mem_update(lay["ext"][1], lay["ext"][0], mem_len=M)
+                chain.attn(txl, lay)
+                chain.memory(txl, lay)
         out_host.copy_(chain.layers[-1]["out"], non_blocking=True)
 
     one()
@@ -317,8 +336,7 @@ def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
     sec = e0.elapsed_time(e1) / 1e3
     tokens = w.shape.batch * w.shape.seg_len * w.segments * steps
     return {"value": aggregate_rate(tokens, sec, world), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "path": "txl_rel_attn_fwd + txl_mem_update"}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
 # ------------------------------------------------------------ oracle (CPU) leg
@@ -361,13 +379,15 @@ def oracle_rate(w: Workload, budget_s: float, layer=None):
     return rows_per_s / (s.heads * w.layers), done, threads, spent
 
 
-def config_of(w: Workload, world: int, working_set: int = 0, ring: bool = False):
+def config_of(w: Workload, world: int, working_set: int = 0, ring: bool = False, pad: int = 0):
     s = w.shape
     c = {"workload": w.name, "batch": s.batch, "heads": s.heads, "d_head": s.d_head,
          "seg_len": s.seg_len, "mem_len": s.mem_len, "layers": w.layers, "segments": w.segments,
          "parallelism": f"replicas x{world} (batch-independent, no collective)"}
     if ring:
         c["memory"] = "ring (txl_rel_attn_fwd_ring + txl_ring_append of L rows)"
+    if pad and pad != s.d_head:
+        c["head_storage"] = f"padded to {pad} (txl_rel_attn_fwd_padded)"
     if working_set:
         c["l2"] = f"per-step working set {working_set / 1e9:.2f} GB > 129 MB L2 (inputs larger than L2, no flush)"
     return c
@@ -486,6 +506,8 @@ def main(argv=None):
     ap.add_argument("--recompute-vs-reuse", action="store_true",
                     help="per-token eval attention cost, sliding-window recompute vs memory reuse (Table 9)")
     ap.add_argument("--batch-t9", type=int, default=22, help="batch for --recompute-vs-reuse")
+    ap.add_argument("--pad", type=int, default=0,
+                    help="store head vectors padded to this many elements (txl_rel_attn_fwd_padded)")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
     args = ap.parse_args(argv)
@@ -514,7 +536,7 @@ def main(argv=None):
         import dataclasses
         w = dataclasses.replace(w, layers=args.layers or w.layers, segments=args.segments or w.segments)
     s = w.shape
-    chain = Chain(w, torch.device("cuda", local), ring=args.ring)
+    chain = Chain(w, torch.device("cuda", local), ring=args.ring, pad=args.pad)
     splits = splits_for(w) if w.dtype == "bf16" else 1
     chain.attn_extra_launches = 1 if splits > 1 else 0
     for _ in range(args.warmup):
@@ -568,7 +590,7 @@ def main(argv=None):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": config_of(w, world, chain.working_set_bytes, args.ring),
+            "config": config_of(w, world, chain.working_set_bytes, args.ring, args.pad),
             "tflops": tflops_step, "pct_bf16_peak": tflops_step / peaks["bf16_tflops"] * 100.0,
             "roofline": roof, "clocks": clk, "gpu_launches": launches}
 

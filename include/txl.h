@@ -70,7 +70,11 @@ typedef enum {
  * Long memories (few query tiles, many keys) split the keys across CTAs; the
  * partial results then live in a library-owned device scratch buffer that is
  * allocated on first need, grown when needed and released by txl_shutdown().
- * Calls that need the scratch must not run concurrently on different streams.
+ * bf16 heads with d_head != 64 also use it: q, k, v, r and the biases are
+ * copied into 64-wide zero-padded vectors there (rows the TMA unit can
+ * read), and the output's d_head columns are copied back.  Calls that need
+ * the scratch must not run concurrently on different streams, and the first
+ * such call of a size must not be made during stream capture.
  */
 txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
                             const float *u_bias, const float *v_bias,
@@ -113,6 +117,43 @@ txl_status txl_rel_attn_fwd_ring(const void *q, const void *k, const void *v, co
                                  const float *u_bias, const float *v_bias, int batch, int mem_len,
                                  int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
                                  void *out, void *stream);
+
+/*
+ * txl_rel_attn_fwd_padded -- txl_rel_attn_fwd on head vectors stored with
+ * d_pad >= d_head elements each (zeros past d_head), the layout
+ * txl_project_heads and txl_rel_table write.  q, k, v, r, out are
+ * [..][heads][d_pad]; u_bias, v_bias [heads][d_pad] (or NULL).  The result
+ * equals txl_rel_attn_fwd on the first d_head elements (scale 1/sqrt(d_head));
+ * out's padding columns come out zero.  With bf16 and d_pad = 64 the rows are
+ * read by TMA whatever d_head is (e.g. d_head 41 padded to 64).
+ */
+txl_status txl_rel_attn_fwd_padded(const void *q, const void *k, const void *v, const void *r,
+                                   const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                   int seg_len, int heads, int d_head, int d_pad, txl_dtype dtype,
+                                   void *out, void *stream);
+
+/*
+ * txl_project_heads -- the projections of Section 3.3 (W_q, W_kE, W_v) into
+ * the attention's layout: y[rows][heads][d_pad] = x[rows][d_in] .
+ * W[d_in][heads*d_head], padding columns d_head..d_pad-1 set to zero.  With
+ * x = a T-major [positions][batch][d_model] buffer (rows = positions*batch)
+ * the result is the T-major [positions][batch][heads][d_pad] layout.  A plain
+ * GEMM (cuBLAS, fp32 accumulation); x, w, out device, row-major, dtype
+ * elements, out must not overlap x or w.  d_pad >= d_head >= 1.
+ */
+txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, int d_in, int heads,
+                             int d_head, int d_pad, txl_dtype dtype, void *stream);
+
+/*
+ * txl_rel_table -- Appendix B's reversed projected table of one layer:
+ * out[t][h][d] = sum_c R[klen-1-t][c] * W_kR[c][h*d_head + d] for t < klen,
+ * R[p][2c] = sin(p * 10000^(-2c/d_model)), R[p][2c+1] = cos(the same angle)
+ * (the sinusoid of the relative distance p, evaluated in fp32 on the device;
+ * fp32 accumulation).  out [klen][heads][d_pad], padding zero; W_kR
+ * [d_model][heads*d_head].  Batch- and segment-independent: once per layer.
+ */
+txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int heads, int d_head, int d_pad,
+                         txl_dtype dtype, void *stream);
 
 /*
  * txl_ring_append -- write n_rows new rows into a ring of ring_len rows at

@@ -1,0 +1,96 @@
+"""Projections into the attention layout, the device-built relative table and
+attention on padded heads (CUDA, `-m gpu`).  References: float64 numpy on
+exactly the values the device read, the oracle for the attention."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.helpers import TOL_BF16, TOL_F32
+from transformer_xl_relative_rel_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _rel_err(got, ref):
+    return np.abs(got - ref).max() / max(1e-12, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("dtype,rtol", [(torch.float32, 1e-5), (torch.bfloat16, 1e-2)])
+@pytest.mark.parametrize("rows,d_in,heads,d_head,d_pad", [(300, 410, 10, 41, 64), (96, 64, 2, 32, 32),
+                                                          (7, 24, 3, 5, 8)])
+def test_project_heads(dtype, rtol, rows, d_in, heads, d_head, d_pad):
+    import transformer_xl_relative_rel_gb300 as txl
+    g = torch.Generator(device="cuda").manual_seed(rows + d_in)
+    x = torch.randn(rows, d_in, generator=g, device="cuda").to(dtype)
+    w = (0.05 * torch.randn(d_in, heads * d_head, generator=g, device="cuda")).to(dtype)
+    y = txl.project_heads(x, w, heads, d_head, d_pad)
+    ref = (x.double().cpu().numpy() @ w.double().cpu().numpy()).reshape(rows, heads, d_head)
+    got = y.double().cpu().numpy()
+    assert _rel_err(got[..., :d_head], ref) <= rtol
+    assert (got[..., d_head:] == 0).all()
+
+
+@pytest.mark.parametrize("dtype,rtol", [(torch.float32, 2e-4), (torch.bfloat16, 1e-2)])
+@pytest.mark.parametrize("klen,d_model,heads,d_head,d_pad", [(300, 410, 10, 41, 64), (1536, 512, 8, 64, 64),
+                                                             (33, 20, 2, 10, 16)])
+def test_rel_table(dtype, rtol, klen, d_model, heads, d_head, d_pad):
+    import transformer_xl_relative_rel_gb300 as txl
+    g = torch.Generator(device="cuda").manual_seed(klen + d_model)
+    w_r = (0.02 * torch.randn(d_model, heads * d_head, generator=g, device="cuda")).to(dtype)
+    r = txl.rel_table(w_r, klen, heads, d_head, d_pad)
+    R = inputs.sinusoid(klen, d_model)[::-1]            # row t: distance klen-1-t (Appendix B)
+    ref = (R @ w_r.double().cpu().numpy()).reshape(klen, heads, d_head)
+    got = r.double().cpu().numpy()
+    assert _rel_err(got[..., :d_head], ref) <= rtol
+    assert (got[..., d_head:] == 0).all()
+
+
+@pytest.mark.parametrize("dtype,tol,B,H,D,Dp,L,M", [
+    (torch.bfloat16, TOL_BF16, 2, 3, 41, 64, 150, 150),   # base-LM head size, TMA on the padded rows
+    (torch.bfloat16, TOL_BF16, 2, 2, 41, 48, 130, 70),    # padded to 48: thread loads
+    (torch.bfloat16, TOL_BF16, 1, 2, 20, 32, 64, 200),
+    (torch.float32, TOL_F32, 1, 2, 13, 16, 40, 24),
+])
+def test_padded_attention_matches_unpadded(dtype, tol, B, H, D, Dp, L, M):
+    import transformer_xl_relative_rel_gb300 as txl
+    p = inputs.unit_layer(inputs.LayerShape(B, H, D, L, M), 6000 + D + Dp)
+
+    def padded(a):
+        z = np.zeros(a.shape[:-1] + (Dp,), dtype=np.float32)
+        z[..., :D] = a
+        return torch.from_numpy(z)
+    dev = {n: padded(p[n]).to(dtype).cuda() for n in ("q", "k", "v", "r")}
+    for n in ("u", "w"):
+        dev[n] = padded(p[n]).float().cuda()
+    out = txl.rel_attn_fwd_padded(dev["q"], dev["k"], dev["v"], dev["r"], dev["u"], dev["w"], mem_len=M,
+                                  d_head=D)
+    host = {n: dev[n][..., :D].double().cpu().numpy() for n in ("q", "k", "v", "r", "u", "w")}
+    ref = oracle.rel_attn(host["q"], host["k"], host["v"], host["r"], host["u"], host["w"], mem_len=M)
+    got = out.double().cpu().numpy()
+    assert np.abs(got[..., :D] - ref).max() <= tol
+    assert (got[..., D:] == 0).all()
+
+
+def test_layer_from_hidden_states():
+    """Hidden states -> projections + table (d_head 41 padded to 64) -> padded
+    attention, against the oracle on the projected values."""
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, D, Dp, L, M = 2, 10, 41, 64, 150, 150
+    T, dm = M + L, H * D
+    g = torch.Generator(device="cuda").manual_seed(41)
+    h_ext = torch.randn(T, B, dm, generator=g, device="cuda").bfloat16()
+    wq, wk, wv, wr = ((0.05 * torch.randn(dm, dm, generator=g, device="cuda")).bfloat16() for _ in range(4))
+    u = 0.02 * torch.randn(H, Dp, generator=g, device="cuda")
+    w = 0.02 * torch.randn(H, Dp, generator=g, device="cuda")
+    u[:, D:] = 0
+    w[:, D:] = 0
+    q = txl.project_heads(h_ext[M:].contiguous(), wq, H, D, Dp)
+    k = txl.project_heads(h_ext, wk, H, D, Dp)
+    v = txl.project_heads(h_ext, wv, H, D, Dp)
+    r = txl.rel_table(wr, T, H, D, Dp)
+    out = txl.rel_attn_fwd_padded(q, k, v, r, u, w, mem_len=M, d_head=D)
+    host = {n: t[..., :D].double().cpu().numpy() for n, t in (("q", q), ("k", k), ("v", v), ("r", r),
+                                                               ("u", u), ("w", w))}
+    ref = oracle.rel_attn(host["q"], host["k"], host["v"], host["r"], host["u"], host["w"], mem_len=M)
+    assert np.abs(out[..., :D].double().cpu().numpy() - ref).max() <= TOL_BF16

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import TOL_BF16, device_layer, unit_shape
+from tests.helpers import TOL_BF16, device_layer, oracle_full, unit_shape
 from transformer_xl_relative_rel_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -50,7 +50,7 @@ def _call_default(lib, dev, out, mem_len):
 def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
     for call in range(2):                       # the second call reuses the array
         p = inputs.unit_layer(unit_shape(B, H, D, L, M), 300 + call)
-        dev, _ = device_layer(p, torch.bfloat16)
+        dev, host = device_layer(p, torch.bfloat16)
         ref = torch.empty_like(dev["q"])
         got = torch.full_like(dev["q"], float("nan"))
         assert _call_default(lib, dev, ref, M) == 0
@@ -58,6 +58,11 @@ def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
         torch.cuda.synchronize()
         err = (got.float() - ref.float()).abs().max().item()
         assert np.isfinite(err) and err <= TOL_BF16, f"call {call}: max abs diff {err}"
+        if D != 64:
+            # this entry reads odd head widths with thread loads (the default
+            # one repacks them): pin it to the oracle directly
+            want = oracle_full(host, M)
+            assert np.abs(got.double().cpu().numpy() - want).max() <= TOL_BF16
 
 
 def test_noalloc_refuses_scratch_beyond_its_maximum(lib):

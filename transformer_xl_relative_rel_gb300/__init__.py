@@ -6,7 +6,9 @@ entry-point names.  Importing this package does not load the library; the first
 call does, and raises ``TxlError`` if it was not built.
 """
 from .abi import (TxlError, TXL_F32, TXL_BF16, rel_attn_fwd, rel_attn_fwd_ring,  # noqa: F401
-                  mem_update, ring_append, check, load_library, library_path, status_string)
+                  rel_attn_fwd_padded, project_heads, rel_table, mem_update, ring_append, check,
+                  load_library, library_path, status_string)
 
 __all__ = ["TxlError", "TXL_F32", "TXL_BF16", "rel_attn_fwd", "rel_attn_fwd_ring", "mem_update",
-           "ring_append", "check", "load_library", "library_path", "status_string"]
+           "ring_append", "rel_attn_fwd_padded", "project_heads", "rel_table", "check", "load_library",
+           "library_path", "status_string"]

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libtxl.so")
-SOURCES = ["api.cu", "attn_f32.cu", "attn_bf16.cu", "rollover.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attn_f32.cu", "attn_bf16.cu", "rollover.cu", "noalloc.cu", "project.cu", "pack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -72,7 +72,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
+        # cuBLAS (the plain projection GEMM of project.cu) from the toolkit's
+        # library directory, found at run time through the rpath
+        libdir = os.path.join(os.path.dirname(os.path.dirname(cc)), "lib64")
+        cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + \
+            ["-lcublas", "-Xlinker", "-rpath=" + libdir]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

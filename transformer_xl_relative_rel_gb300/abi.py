@@ -25,7 +25,8 @@ _lib: Optional[ctypes.CDLL] = None
 #: every symbol include/txl.h declares (checked by the host-side tests)
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
-           "txl_rel_attn_fwd_ring", "txl_ring_append")
+           "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
+           "txl_rel_table")
 
 
 class TxlError(RuntimeError):
@@ -56,6 +57,12 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd_ring.restype = i
     lib.txl_ring_append.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_ring_append.restype = i
+    lib.txl_rel_attn_fwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
+    lib.txl_rel_attn_fwd_padded.restype = i
+    lib.txl_project_heads.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.txl_project_heads.restype = i
+    lib.txl_rel_table.argtypes = [vp, vp, i, i, i, i, i, i, vp]
+    lib.txl_rel_table.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_mem_update.restype = i
     lib.txl_check.argtypes = [vp]
@@ -154,6 +161,55 @@ def rel_attn_fwd_ring(q, k, v, r, u_bias, v_bias, mem_len: int, kv_start: int, o
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
         B, mem_len, L, H, D, int(kv_start), _dtype_code(q), _ptr(out), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd_ring")
+    return out
+
+
+def rel_attn_fwd_padded(q, k, v, r, u_bias, v_bias, mem_len: int, d_head: int, out=None, stream=None):
+    """rel_attn_fwd on head vectors padded to q.shape[-1] elements (zeros past
+    ``d_head``), as project_heads / rel_table write them."""
+    L, B, H, Dp = q.shape
+    out = _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
+    st = load_library().txl_rel_attn_fwd_padded(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+        B, mem_len, L, H, int(d_head), Dp, _dtype_code(q), _ptr(out), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_padded")
+    return out
+
+
+def project_heads(x, w, heads: int, d_head: int, d_pad: int, out=None, stream=None):
+    """y[..., heads, d_pad] = x[..., d_in] @ w[d_in, heads*d_head], padding zero.
+    x: [*lead, d_in]; returns [*lead, heads, d_pad]."""
+    import torch
+    lead = tuple(x.shape[:-1])
+    d_in = x.shape[-1]
+    rows = 1
+    for n in lead:
+        rows *= n
+    if tuple(w.shape) != (d_in, heads * d_head) or w.dtype != x.dtype:
+        raise ValueError(f"w must be [{d_in}, {heads * d_head}] of x's dtype")
+    for t in (x, w):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty(*lead, heads, d_pad, dtype=x.dtype, device=x.device)
+    st = load_library().txl_project_heads(_ptr(x), _ptr(w), _ptr(out), rows, d_in, heads, d_head, d_pad,
+                                          _dtype_code(x), _stream_ptr(stream))
+    _raise(st, "txl_project_heads")
+    return out
+
+
+def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: int, out=None, stream=None):
+    """Appendix B's reversed projected table [klen, heads, d_pad] from W_kR
+    [d_model, heads*d_head] and the sinusoid of the relative distance."""
+    import torch
+    d_model = w_r.shape[0]
+    if w_r.dim() != 2 or w_r.shape[1] != heads * d_head or not w_r.is_cuda or not w_r.is_contiguous():
+        raise ValueError(f"w_r must be a contiguous CUDA [d_model, {heads * d_head}] tensor")
+    if out is None:
+        out = torch.empty(klen, heads, d_pad, dtype=w_r.dtype, device=w_r.device)
+    st = load_library().txl_rel_table(_ptr(w_r), _ptr(out), klen, d_model, heads, d_head, d_pad,
+                                      _dtype_code(w_r), _stream_ptr(stream))
+    _raise(st, "txl_rel_table")
     return out
 
 

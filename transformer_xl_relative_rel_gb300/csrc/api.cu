@@ -130,7 +130,7 @@ extern "C" {
 static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
                                   const float *u_bias, const float *v_bias, int batch, int mem_len,
                                   int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
-                                  void *out, void *stream)
+                                  void *out, void *stream, int scale_d = 0)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
@@ -166,12 +166,12 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
         if (!u_bias) u_bias = z;
         if (!v_bias) v_bias = z;
     }
-    AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len, kv_start};
+    AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len, kv_start, scale_d};
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     if (dtype == TXL_F32) {
         e = launch_attn_f32(a, s);
-    } else {
+    } else if (a.D == 64) {
         const int splits = bf16_num_splits(a, device_sm_count());
         void *scratch = nullptr;
         if (splits > 1) {
@@ -179,6 +179,44 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
             if (st != TXL_OK) return st;
         }
         e = launch_attn_bf16(a, splits, scratch, s);
+    } else {
+        // head vectors of another width: 64-wide zero-padded copies in the
+        // scratch (rows TMA can read), the kernel on those, the output's first
+        // D columns copied back
+        constexpr int W = 64;
+        const long nq = (long)seg_len * batch * heads, nk = (long)(mem_len + seg_len) * batch * heads;
+        const long nr = (long)(mem_len + seg_len) * heads;
+        auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+        const size_t bq = up((size_t)nq * W * 2), bk = up((size_t)nk * W * 2), br = up((size_t)nr * W * 2),
+                     bb = up((size_t)heads * W * 4);
+        AttnArgs ap = a;
+        ap.D = W;
+        ap.scale_d = a.scale_d ? a.scale_d : a.D;
+        const int splits = bf16_num_splits(ap, device_sm_count());
+        const size_t bs = splits > 1 ? up(bf16_scratch_bytes(ap, splits)) : 0;
+        void *scratch = nullptr;
+        txl_status st = get_scratch(2 * bq + 2 * bk + br + 2 * bb + bs, s, &scratch);
+        if (st != TXL_OK) return st;
+        unsigned char *base = (unsigned char *)scratch;
+        void *qp = base, *op = base + bq, *kp = base + 2 * bq, *vp = base + 2 * bq + bk;
+        void *rp = base + 2 * bq + 2 * bk;
+        float *up_ = (float *)(base + 2 * bq + 2 * bk + br), *wp = (float *)(base + 2 * bq + 2 * bk + br + bb);
+        void *sp = bs ? base + 2 * bq + 2 * bk + br + 2 * bb : nullptr;
+        e = launch_pad_heads(qp, a.q, nq, a.D, W, 2, s);
+        if (e == cudaSuccess) e = launch_pad_heads(kp, a.k, nk, a.D, W, 2, s);
+        if (e == cudaSuccess) e = launch_pad_heads(vp, a.v, nk, a.D, W, 2, s);
+        if (e == cudaSuccess) e = launch_pad_heads(rp, a.r, nr, a.D, W, 2, s);
+        if (e == cudaSuccess) e = launch_pad_heads(up_, a.u, heads, a.D, W, 4, s);
+        if (e == cudaSuccess) e = launch_pad_heads(wp, a.w, heads, a.D, W, 4, s);
+        ap.q = qp;
+        ap.k = kp;
+        ap.v = vp;
+        ap.r = rp;
+        ap.u = up_;
+        ap.w = wp;
+        ap.out = op;
+        if (e == cudaSuccess) e = launch_attn_bf16(ap, splits, sp, s);
+        if (e == cudaSuccess) e = launch_unpad_heads(a.out, op, nq, a.D, W, 2, s);
     }
     return e == cudaSuccess ? TXL_OK : cuda_fail(e);
 }
@@ -190,6 +228,18 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
 {
     return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0,
                            dtype, out, stream);
+}
+
+txl_status txl_rel_attn_fwd_padded(const void *q, const void *k, const void *v, const void *r,
+                                   const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                   int seg_len, int heads, int d_head, int d_pad, txl_dtype dtype,
+                                   void *out, void *stream)
+{
+    // every head vector is stored with d_pad elements, zeros past d_head: the
+    // kernels run at width d_pad (the zeros add nothing) and scale by d_head
+    if (d_head < 1 || d_pad < d_head) return TXL_ERR_INVALID;
+    return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_pad, 0, dtype, out,
+                           stream, d_head);
 }
 
 txl_status txl_rel_attn_fwd_ring(const void *q, const void *k, const void *v, const void *r,
@@ -281,6 +331,7 @@ void txl_shutdown(void)
     }
     s.ptr = nullptr;
     s.bytes = 0;
+    blas_shutdown();
 }
 
 }  // extern "C"

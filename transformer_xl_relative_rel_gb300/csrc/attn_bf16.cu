@@ -1007,7 +1007,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.T = a.M + a.L;
     p.nqt = (a.L + BM - 1) / BM;
     p.splits = splits;
-    p.sl2 = LOG2E / sqrtf((float)a.D);
+    p.sl2 = LOG2E / sqrtf((float)(a.scale_d ? a.scale_d : a.D));
     p.part_o = nullptr;
     p.part_lse = nullptr;
     if (splits > 1) {

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(NT)
 rel_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                     const float *__restrict__ v, const float *__restrict__ r,
                     const float *__restrict__ u, const float *__restrict__ w,
-                    float *__restrict__ out, int B, int H, int D, int L, int M, int kv_start)
+                    float *__restrict__ out, int B, int H, int D, int L, int M, int kv_start, int scale_d)
 {
     extern __shared__ float smem[];
     const int DP = D + 1;                 // odd pitch: rows land in distinct banks
@@ -48,7 +48,7 @@ rel_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
     const long rowstride = (long)B * H * D;      // between positions in q/k/v/out
     const long hoff = ((long)b * H + h) * D;
     const int rows_here = min(BR, L - i0);
-    const float scale = 1.0f / sqrtf((float)D);
+    const float scale = 1.0f / sqrtf((float)scale_d);   // d_head (D may be a padded width)
 
     // stage q+u and q+v for the block (rows past L are zero)
     for (int x = tid; x < BR * D; x += NT) {
@@ -168,7 +168,7 @@ cudaError_t launch(const AttnArgs &a, cudaStream_t s)
     dim3 grid(a.B * a.H, (a.L + BR - 1) / BR);
     rel_attn_f32_kernel<DMAX><<<grid, NT, smem, s>>>(
         (const float *)a.q, (const float *)a.k, (const float *)a.v, (const float *)a.r, a.u, a.w,
-        (float *)a.out, a.B, a.H, a.D, a.L, a.M, a.kv_start);
+        (float *)a.out, a.B, a.H, a.D, a.L, a.M, a.kv_start, a.scale_d ? a.scale_d : a.D);
     return cudaGetLastError();
 }
 

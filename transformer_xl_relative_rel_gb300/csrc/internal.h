@@ -14,6 +14,7 @@ struct AttnArgs {
     void *out;
     int B, H, D, L, M;
     int kv_start = 0;             // K, V in a ring of M+L rows: key j at row (kv_start + j) mod (M+L)
+    int scale_d = 0;              // d_head for the 1/sqrt(d_head) scale when D is a padded width (0: D)
 };
 
 // fp32 SIMT path (attn_f32.cu)
@@ -31,6 +32,12 @@ cudaError_t read_and_clear_device_error(unsigned int *word, cudaStream_t s);
 cudaError_t launch_rollover(void *dst, const void *src, size_t bytes, int elem_size,
                             cudaStream_t s);
 
+// head vectors to / from a zero-padded width (pack.cu); elem_size 2 or 4
+cudaError_t launch_pad_heads(void *dst, const void *src, long nvec, int d, int dp, int elem_size,
+                             cudaStream_t s);
+cudaError_t launch_unpad_heads(void *dst, const void *src, long nvec, int d, int dp, int elem_size,
+                               cudaStream_t s);
+
 int device_sm_count();
 
 // Device address of `count` zero floats on the current device (a fixed array
@@ -38,6 +45,9 @@ int device_sm_count();
 // cudaErrorNotSupported when count exceeds the array, or the CUDA error of
 // the lookup.
 cudaError_t zero_bias(size_t count, const float **out);
+
+// releases the per-device cuBLAS handles of project.cu
+cudaError_t blas_shutdown();
 
 // records `e` as the thread's last CUDA error (reported by txl_last_cuda_error)
 // and clears the runtime's error state; returns e
