@@ -54,10 +54,11 @@ using namespace sm100;
 constexpr int BM = 128;           // query rows per CTA (TMEM lanes)
 constexpr int BN = 128;           // keys per tile; also table rows per band chunk
 constexpr int HN = BN / 2;        // keys per softmax thread and tile
-constexpr int NSTAGE = 3;         // shared-memory ring of (K, V, table chunk) tiles
+constexpr int NSTAGE = 3;         // shared-memory ring of K, V tiles
+constexpr int NCH = 4;            // shared-memory ring of 128-row table chunks
 constexpr int NT = 384;           // 12 warps, see the role list above
 constexpr uint32_t TM_S = 0;      // S of the current tile, 128 columns
-constexpr uint32_t TM_BAND = 128; // band ring, 2 x 128 columns
+constexpr uint32_t TM_BAND = 128; // the tile's band window: 256 table rows, 256 columns
 constexpr uint32_t TM_P = 384;    // P (bf16 pairs), 64 columns
 constexpr uint32_t TM_O = 448;    // O accumulator, up to 64 columns
 constexpr uint32_t TM_COLS = 512;
@@ -84,23 +85,22 @@ struct Params {
 // swizzle (element (row, k) at sw128_offset(row, k)); D <= 64 fits one row.
 template <int DP>
 struct Smem {
-    static constexpr uint32_t TILE = BN * 128;             // one K, V or table chunk (128 rows)
-    static constexpr uint32_t STAGE = 3 * TILE;             // K, V, chunk
-    static constexpr uint32_t ST0 = 0;                      // NSTAGE stages
-    static constexpr uint32_t QU = NSTAGE * STAGE;          // q+u, q+v: 128 rows of 128 bytes
+    static constexpr uint32_t TILE = BN * 128;             // 128 rows of 128 bytes: K, V or a table chunk
+    static constexpr uint32_t KV = 2 * TILE;                // K and V of one key tile
+    static constexpr uint32_t ST0 = 0;                      // NSTAGE K/V stages
+    static constexpr uint32_t CH0 = NSTAGE * KV;            // NCH table chunks (a ring)
+    static constexpr uint32_t QU = CH0 + NCH * TILE;        // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
-    static constexpr uint32_t PRE = QV + BM * 128;          // table chunk 0 of an item
-    static constexpr uint32_t QRAW = PRE + TILE;            // raw q rows of the next item
+    static constexpr uint32_t QRAW = QV + BM * 128;         // raw q rows of the next item
     static constexpr uint32_t UW = QRAW + BM * 128;         // its head's u and v biases (fp32, 2 x 64)
-    static constexpr uint32_t XM = UW + 2 * 64 * 4;         // row exchange [2 phases][2 halves][128 rows]
-    static constexpr uint32_t BARS = XM + 2 * 2 * BM * 4;
-    // barrier slots (8 bytes each): q+u/q+v ready, chunk 0 ready, chunk 0
-    // read, raw q ready, raw q read, stage full / empty, S full, S free
-    // (loaded by the softmax), P full, P.V done, and one exchange barrier per
-    // TMEM lane quadrant
-    static constexpr int B_Q = 0, B_PRE = 1, B_PREF = 2, B_QRAW = 3, B_QRF = 4, B_FULL = 5,
-                         B_EMPTY = 5 + NSTAGE, B_S = 5 + 2 * NSTAGE, B_SF = B_S + 1, B_P = B_SF + 1,
-                         B_PV = B_P + 1, B_X = B_PV + 1;
+    static constexpr uint32_t BARS = UW + 2 * 64 * 4;
+    // barrier slots (8 bytes each): q+u/q+v ready, raw q ready, raw q read;
+    // per K/V stage full / empty; per chunk slot full / empty; S full, S
+    // free (loaded by the softmax), P full, P.V done
+    static constexpr int B_Q = 0, B_QRAW = 1, B_QRF = 2, B_FULL = 3, B_EMPTY = 3 + NSTAGE,
+                         B_CHF = 3 + 2 * NSTAGE, B_CHE = B_CHF + NCH, B_S = B_CHE + NCH, B_SF = B_S + 1,
+                         B_P = B_SF + 1, B_PV = B_P + 1;
+    static_assert(B_PV < 32, "barrier slots");
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -315,19 +315,20 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     if (tid == 0) {
         *abort = 0;
         mbar_init(bar(S::B_Q), 128);
-        mbar_init(bar(S::B_PRE), kTma ? 1 : 32);
-        mbar_init(bar(S::B_PREF), 1);
         mbar_init(bar(S::B_QRAW), kTma ? 1 : 32);
         mbar_init(bar(S::B_QRF), 128);
         for (int x = 0; x < NSTAGE; ++x) {
             mbar_init(bar(S::B_FULL + x), kTma ? 1 : 64);
             mbar_init(bar(S::B_EMPTY + x), 1);
         }
+        for (int x = 0; x < NCH; ++x) {
+            mbar_init(bar(S::B_CHF + x), kTma ? 1 : 32);
+            mbar_init(bar(S::B_CHE + x), 1);
+        }
         mbar_init(bar(S::B_S), 1);
         mbar_init(bar(S::B_SF), 256);
         mbar_init(bar(S::B_P), 256);
         mbar_init(bar(S::B_PV), 1);
-        for (int x = 0; x < 4; ++x) mbar_init(bar(S::B_X + x), 64);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -380,26 +381,33 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     mbar_arrive(bar(S::B_QRAW));
                 }
             };
+            // table chunk number cg (global count) into ring slot cg % NCH,
+            // once the S MMAs of its previous occupant are done (warp 0)
+            auto load_chunk = [&](int cg, int row, int h) {
+                const int slot = cg % NCH;
+                if (cg >= NCH && !wwait(S::B_CHE + slot, ((cg / NCH) - 1) & 1)) return false;
+                if (kTma) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(S::B_CHF + slot), S::TILE);
+                        tma_load_3d(sbase + S::CH0 + slot * S::TILE, &tm_r, bar(S::B_CHF + slot), 0, row, h);
+                    }
+                } else {
+                    warp_load_rows(smem + S::CH0 + slot * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, row,
+                                   p.T, p.D, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(S::B_CHF + slot));
+                }
+                return true;
+            };
             Item it;
             int j = next_busy(p, 0, it);
             if (j >= 0) load_q(it);
-            int g = 0, ni = 0;                       // key tiles and items so far
+            int g = 0, cg = 0, ni = 0;               // key tiles, table chunks, items so far
             bool ok = true;
             while (ok && j >= 0) {
-                // table chunk 0 of the item, once the band MMA of the previous
-                // item's chunk 0 has read the buffer
-                if (ni >= 1 && !wwait(S::B_PREF, (ni - 1) & 1)) break;
-                if (kTma) {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(bar(S::B_PRE), S::TILE);
-                        tma_load_3d(sbase + S::PRE, &tm_r, bar(S::B_PRE), 0, it.kb0, it.h);
-                    }
-                } else if (warp == 0) {
-                    warp_load_rows(smem + S::PRE, BN, p.r, (long)it.h * p.D, (long)p.H * p.D, it.kb0, p.T, p.D,
-                                   lane);
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(S::B_PRE));
-                }
+                // chunk 0 of the item (its tile n reads chunks n and n+1)
+                if (warp == 0 && !load_chunk(cg, it.kb0, it.h)) break;
+                ++cg;
                 for (int n = 0; n < it.N; ++n, ++g) {
                     const int st = g % NSTAGE;
                     // the stage is free once the P.V of tile g-NSTAGE (its last reader) is done
@@ -408,14 +416,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         break;
                     }
                     const int j0 = (it.t0 + n) * BN;
-                    const int crow = it.kb0 + (n + 1) * BN;     // table chunk n+1
-                    const uint32_t dst = sbase + S::ST0 + st * S::STAGE;
+                    const uint32_t dst = sbase + S::ST0 + st * S::KV;
                     if (kTma) {
                         if (lane == 0) {
                             // K, V rows may sit in a ring (key j at row (kv_start + j) mod T)
                             int s0 = p.kv_start + j0;
                             if (s0 >= p.T) s0 -= p.T;
-                            mbar_arrive_expect_tx(bar(S::B_FULL + st), S::STAGE);
+                            mbar_arrive_expect_tx(bar(S::B_FULL + st), S::KV);
                             if (p.kv_start == 0 || s0 + BN <= p.T) {
                                 // one box; in the plain layout rows past the last key
                                 // are zero-filled
@@ -433,21 +440,23 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                                                 it.bh);
                                 }
                             }
-                            tma_load_3d(dst + 2 * S::TILE, &tm_r, bar(S::B_FULL + st), 0, crow, it.h);
                         }
                     } else {
-                        unsigned char *d = smem + S::ST0 + st * S::STAGE;
-                        if (warp == 0) {
+                        unsigned char *d = smem + S::ST0 + st * S::KV;
+                        if (warp == 0)
                             warp_load_rows(d, BN, p.k, it.head_off, qkv_row, j0, p.T, p.D, lane, p.kv_start);
-                            warp_load_rows(d + 2 * S::TILE, BN, p.r, (long)it.h * p.D, (long)p.H * p.D, crow,
-                                           p.T, p.D, lane);
-                        } else {
+                        else
                             warp_load_rows(d + S::TILE, BN, p.v, it.head_off, qkv_row, j0, p.T, p.D, lane,
                                            p.kv_start);
-                        }
                         fence_proxy_async_smem();
                         mbar_arrive(bar(S::B_FULL + st));
                     }
+                    // table chunk n+1
+                    if (warp == 0 && !load_chunk(cg, it.kb0 + (n + 1) * BN, it.h)) {
+                        ok = false;
+                        break;
+                    }
+                    ++cg;
                 }
                 if (!ok) break;
                 // the next item's q rows, once this item's have been converted
@@ -463,51 +472,49 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
         } else if (warp == 1) {
             // =============================================================== S / band MMAs
-            // one thread waits and issues (the issuing lane shares its
-            // scheduler with two softmax warps: no warp-wide votes here)
+            // per tile: S = (q+u) K^T (N = 128) and the tile's band window
+            // (q+v) [chunk n; chunk n+1]^T (two N = 128 MMAs per K step) into
+            // TMEM.  One thread waits and issues.
             if (lane == 0) {
                 const uint32_t idesc_n = idesc_bf16(BM, BN, 0, 0);
                 // descriptors built once; the 14-bit start-address field (address / 16)
                 // advances by 2 per 32-byte K step within a 128-byte swizzled row
                 const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
                 const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
-                const uint64_t d_pre = smem_desc_sw128(sbase + S::PRE, 16, 1024);
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
+                const uint64_t d_ch0 = smem_desc_sw128(sbase + S::CH0, 16, 1024);
+                constexpr uint64_t KV16 = S::KV >> 4, TILE16 = S::TILE >> 4;
                 Item it;
-                int g = 0, ni = 0;
+                int g = 0, cg = 0, ni = 0;
                 bool ok = true;
                 for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it), ++ni) {
-                    // q+u, q+v and table chunk 0 of the item; the S buffer and
-                    // band slot g % 2 were last read by the loads of tile g-1
-                    ok = wait_or_abort(bar(S::B_Q), ni & 1, abort) && wait_or_abort(bar(S::B_PRE), ni & 1, abort);
-                    if (ok && g >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // chunk c of this item lives in band slot (g0 + c) % 2
-#pragma unroll
-                    for (int ks = 0; ks < DP / 16; ++ks)
-                        mma_bf16_ss(tmem + TM_BAND + BN * (uint32_t)(g & 1), d_qv + 2 * ks, d_pre + 2 * ks, idesc_n,
-                                    ks > 0);
-                    mma_commit(bar(S::B_PREF));
+                    if (!wait_or_abort(bar(S::B_Q), ni & 1, abort)) break;     // q+u, q+v of the item
+                    const int c0 = cg;
                     for (int n = 0; n < it.N; ++n, ++g) {
                         const int st = g % NSTAGE;
-                        // the S buffer and band slot (g+1) % 2 were last read by
-                        // the softmax loads of tile g-1
-                        if (n >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
-                        ok = ok && wait_or_abort(bar(S::B_FULL + st), (g / NSTAGE) & 1, abort);
+                        const int ca = c0 + n, cb = ca + 1, sa = ca % NCH, sb = cb % NCH;
+                        // the S buffer and the band window were last read by the
+                        // softmax loads of tile g-1
+                        if (g >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
+                        ok = ok && wait_or_abort(bar(S::B_FULL + st), (g / NSTAGE) & 1, abort) &&
+                             wait_or_abort(bar(S::B_CHF + sa), (ca / NCH) & 1, abort) &&
+                             wait_or_abort(bar(S::B_CHF + sb), (cb / NCH) & 1, abort);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint64_t dk = d_st0 + st * STAGE16, dc = dk + 2 * TILE16;
-                        const uint32_t tb = tmem + TM_BAND + BN * (uint32_t)((g + 1) & 1);
+                        const uint64_t dk = d_st0 + st * KV16, da = d_ch0 + sa * TILE16, db = d_ch0 + sb * TILE16;
 #pragma unroll
                         for (int ks = 0; ks < DP / 16; ++ks)
                             mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
 #pragma unroll
-                        for (int ks = 0; ks < DP / 16; ++ks)
-                            mma_bf16_ss(tb, d_qv + 2 * ks, dc + 2 * ks, idesc_n, ks > 0);
+                        for (int ks = 0; ks < DP / 16; ++ks) {
+                            mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_n, ks > 0);
+                            mma_bf16_ss(tmem + TM_BAND + BN, d_qv + 2 * ks, db + 2 * ks, idesc_n, ks > 0);
+                        }
                         mma_commit(bar(S::B_S));
+                        mma_commit(bar(S::B_CHE + sa));                   // chunk n: read for the last time
+                        if (n == it.N - 1) mma_commit(bar(S::B_CHE + sb));   // the item's last chunk
                     }
+                    cg = c0 + it.N + 1;
                 }
             }
             __syncwarp();
@@ -516,7 +523,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             if (lane == 0) {
                 const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
-                constexpr uint64_t STAGE16 = S::STAGE >> 4, TILE16 = S::TILE >> 4;
+                constexpr uint64_t KV16 = S::KV >> 4, TILE16 = S::TILE >> 4;
                 Item it;
                 int g = 0;
                 bool ok = true;
@@ -528,7 +535,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t dv = d_st0 + st * STAGE16 + TILE16;   // 16 keys = 2048 bytes of V
+                        const uint64_t dv = d_st0 + st * KV16 + TILE16;   // 16 keys = 2048 bytes of V
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)   // P: 16 keys = 8 TMEM columns
                             mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, dv + 128 * kk, idesc_o,
@@ -543,36 +550,30 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     } else {
         setmaxnreg_inc<REG_HIGH>();
         // =============================================================== softmax
-        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 4) >> 2;          // keys 64*half .. +63 of each tile
-        const int ii = quarter * 32 + lane;        // this thread's query row
-        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        float *xm = reinterpret_cast<float *>(smem + S::XM);
-        int xk = 0;                                // exchanges done with the partner warp
-        // trade a per-row value with the partner warp (same rows, other key
-        // half); exchange k uses buffer k & 1 and phase k of the quadrant's barrier
-        auto exchange = [&](float v, float &other) {
-            xm[((xk & 1) * 2 + half) * BM + ii] = v;
-            mbar_arrive(bar(S::B_X + quarter));
-            const bool ok = wwait(S::B_X + quarter, xk & 1);
-            other = xm[((xk & 1) * 2 + (1 - half)) * BM + ii];
-            ++xk;
-            return ok;
-        };
-        // q+u and q+v of an item's row ii, scaled by log2(e)/sqrt(D) and
-        // rounded once to bf16, from the raw rows into the MMA operand buffers
-        // (warps 4-7; item number ni)
+        // warp w owns 16 query rows (TMEM lanes lb..lb+15, lb = 32*quarter +
+        // 16*rh) with the 16-lane TMEM shape: lanes 0-15 of the warp take keys
+        // 0-63 of each tile, lanes 16-31 keys 64-127 of the same rows, so a
+        // row's two halves meet in one warp (shuffles, no shared memory)
+        const int quarter = warp & 3, rh = (warp - 4) >> 2;
+        const int r16 = lane & 15, half = lane >> 4;
+        const int lb = quarter * 32 + rh * 16;     // the warp's first row (TMEM lane)
+        const int ii = lb + r16;                   // this thread's query row
+        const uint32_t tl = tmem + ((uint32_t)lb << 16);
+        // q+u and q+v of an item's row, scaled by log2(e)/sqrt(D) and rounded
+        // once to bf16, from the raw rows into the MMA operand buffers (warps
+        // 4-7, one row per thread: row 32*quarter + lane; item number ni)
         auto convert_q = [&](const Item &it, int ni) {
             if (!wwait(S::B_QRAW, ni & 1)) return false;
+            const int ic = quarter * 32 + lane;
             const float4 *uw4 = reinterpret_cast<const float4 *>(smem + S::UW);
-            const float keep = ii < it.rows_here ? 1.f : 0.f;   // rows past L: zero operands
+            const float keep = ic < it.rows_here ? 1.f : 0.f;   // rows past L: zero operands
             // every load first (the stores below could alias them as far as the
             // compiler knows), then the arithmetic and the stores
             uint4 raw[DP / 8];
             float4 u4[DP / 4], w4[DP / 4];
 #pragma unroll
             for (int d8 = 0; d8 < DP / 8; ++d8)
-                raw[d8] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * d8));
+                raw[d8] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ic, 8 * d8));
 #pragma unroll
             for (int d4 = 0; d4 < DP / 4; ++d4) {
                 u4[d4] = uw4[d4];
@@ -591,9 +592,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
                     c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
                 }
-                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
+                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ic, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
-                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ii, 8 * d8)) =
+                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ic, 8 * d8)) =
                     make_uint4(c4[0], c4[1], c4[2], c4[3]);
             }
             fence_proxy_async_smem();
@@ -602,33 +603,24 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             return true;
         };
 
-        const int shift = 31 - lane;
-        // this thread's 64 S columns and the 96-column band window its row
-        // needs (band column 127-ii+jj of chunks n, n+1: a warp-uniform start
-        // plus 31-lane), in one batch of TMEM loads; the buffers are free for
-        // the next tile's MMAs right after.  Chunk c of the item is in band
-        // slot (g0 + c) % 2, so tile g reads slots g % 2 and (g+1) % 2.
-        auto load_tile = [&](int g, float (&x)[64], float (&a)[96]) {
-            const int rel = 96 - 32 * quarter + HN * half;   // window start in chunks n, n+1
-            uint32_t c[3];
-#pragma unroll
-            for (int z = 0; z < 3; ++z) {
-                const int rz = rel + 32 * z;
-                c[z] = TM_BAND + BN * (uint32_t)((g + (rz >> 7)) & 1) + (rz & (BN - 1));
-            }
-            const uint32_t ts = tl + TM_S + HN * half;
-            tmem_ld_5x32(ts, ts + 32, tl + c[0], tl + c[1], tl + c[2], x, a);
+        // this thread's 64 S columns and the 80-column band window its row
+        // needs: band column 127-ii+jj of the tile's 256-row window, a
+        // warp-uniform start W0 (+64 for the key-half lanes 16-31) plus
+        // 15-r16; one batch of five loads, the buffers free right after
+        const int shift = 15 - r16;
+        const int W0 = 112 - lb;
+        auto load_tile = [&](float (&x)[64], float (&a)[80]) {
+            const uint32_t ts = tl + TM_S, tb = tl + TM_BAND + (uint32_t)W0;
+            tmem_ld_h_tile<HN>(ts, ts + 32, tb, tb + 32, tb + 64, x, a);
         };
         // the band aligned to this row and added to its 64 fp32 content
         // logits.  The shift runs on the band rounded to fp16 pairs (11-bit
-        // significand, saturated to the finite range): four select stages
-        // move whole registers (shift / 2) within a 48-register window, one
+        // significand, saturated to the finite range): three select stages
+        // move whole registers (shift / 2) within a 40-register window, one
         // byte permute moves half a register (shift & 1), then each fp16 is
         // added to its fp32 logit.
         const uint32_t odd_sel = (shift & 1) ? 0x5432u : 0x3210u;
         auto band_all = [&](uint32_t *w, float *xb) {
-#pragma unroll
-            for (int y = 0; y < 40; ++y) w[y] = (shift & 16) ? w[y + 8] : w[y];
 #pragma unroll
             for (int y = 0; y < 36; ++y) w[y] = (shift & 8) ? w[y + 4] : w[y];
 #pragma unroll
@@ -669,25 +661,25 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             unf2(acc[1], s2, s3);
             return (s0 + s1) + (s2 + s3);
         };
+        // the other half of this thread's row (lane ^ 16)
+        auto partner = [&](float v) { return __shfl_xor_sync(0xffffffffu, v, 16); };
 
-        constexpr int DH = DP / 2;                 // O columns this warp rescales and stores
-        const uint32_t to = tl + TM_O + DH * half;
-        // an item's output: O / l for this warp's half of the columns (after
-        // the item's last P.V; l is the sum of both key halves)
+        constexpr int DH = DP / 2;                 // O columns of each key-half lane
+        const uint32_t to = tl + TM_O;
+        // an item's output: O / l for this thread's half of the columns
         struct Done {
             long head_off;
             int i0, rows_here, bh, split;
             float m, l;
         };
         auto epilogue = [&](const Done &dn, int g_last) {
-            float l_other = 0.f;
-            if (!wwait(S::B_PV, g_last & 1) || !exchange(dn.l, l_other)) return false;
+            if (!wwait(S::B_PV, g_last & 1)) return false;
+            const float l = dn.l + partner(dn.l);
             tc_fence_after();
             float o[DH];
 #pragma unroll
-            for (int c = 0; c < DH / 8; ++c) tmem_ld8(to + 8 * c, o + 8 * c);
+            for (int c = 0; c < DH / 8; ++c) tmem_ld_h8<DH>(to + 8 * c, o + 8 * c);
             tc_fence_before();
-            const float l = dn.l + l_other;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int d0 = DH * half;
             const int i = dn.i0 + ii;
@@ -740,7 +732,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         bool ok = true;
         Item it;
         int j = next_busy(p, 0, it);
-        if (half == 0 && j >= 0) ok = convert_q(it, 0);
+        if (rh == 0 && j >= 0) ok = convert_q(it, 0);
         int g = 0, ni = 0;
         bool pending = false;                      // the previous item's output is still in O
         Done prev;
@@ -761,20 +753,20 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 // the item's last S MMAs have read q+u, q+v: the next item's
                 // operands go in now, so that its first MMAs overlap the rest
                 // of this item
-                if (n == it.N - 1 && half == 0 && jn >= 0 && !convert_q(nx, ni + 1)) {
+                if (n == it.N - 1 && rh == 0 && jn >= 0 && !convert_q(nx, ni + 1)) {
                     ok = false;
                     break;
                 }
-                // the mask matters only where this warp's rows meet the diagonal
-                const bool diag = j0 + HN - 1 > p.M + it.i0 + 32 * quarter;
+                // the mask matters only where the warp's rows meet the diagonal
+                const bool diag = (it.t0 + n) * BN + BN - 1 > p.M + it.i0 + lb;
                 const int lim = row_valid ? (p.M + i - j0) : (p.T - 1 - j0);
-                float x[64], a[96];
-                load_tile(g, x, a);
+                float x[64], a[80];
+                load_tile(x, a);
                 tc_fence_before();
                 mbar_arrive(bar(S::B_SF));
-                uint32_t hb[48];
+                uint32_t hb[40];
 #pragma unroll
-                for (int y = 0; y < 48; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
+                for (int y = 0; y < 40; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
                 band_all(hb, x);
                 if (diag) {
                     mask_block(x, 0, lim);
@@ -782,20 +774,18 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
                 // exponentials against the running reference max; rows without
                 // a finite reference yet take the row's max first.  The row's
-                // sum over all 128 keys is then checked (both warps of the pair
-                // see the same sum and take the same branch): past SUM_LIMIT the
-                // reference is raised to the row's max and the pass repeated.
-                float pk[32], psum, alpha = 1.f, other;
+                // sum over all 128 keys is then checked (the row's two lanes
+                // see the same sum and the whole warp takes one branch): past
+                // SUM_LIMIT the reference is raised to the row's max and the
+                // pass repeated.
+                float pk[32], psum, alpha = 1.f;
                 bool raise = false;
                 bool find_max = __any_sync(0xffffffffu, m_used == -INFINITY);
                 for (int pass = 0;; ++pass) {
                     if (find_max) {
-                        const float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                        if (!exchange(lmax, other)) {
-                            ok = false;
-                            break;
-                        }
-                        const float m_new = fmaxf(m_used, fmaxf(lmax, other));
+                        float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                        lmax = fmaxf(lmax, partner(lmax));
+                        const float m_new = fmaxf(m_used, lmax);
                         if (m_new > m_used) {
                             alpha *= ex2(m_used - m_new);      // 0 when m_used = -inf
                             m_used = m_new;
@@ -804,14 +794,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     }
                     const float mu = (m_used == -INFINITY) ? 0.f : m_used;
                     psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
-                    if (!exchange(psum, other)) {
-                        ok = false;
-                        break;
-                    }
-                    find_max = __any_sync(0xffffffffu, !(psum + other <= SUM_LIMIT));
+                    find_max = __any_sync(0xffffffffu, !(psum + partner(psum) <= SUM_LIMIT));
                     if (!find_max || pass > 0) break;
                 }
-                if (!ok) break;
                 l_run = l_run * alpha + psum;
                 if (n == 0) {
                     // the previous item's output leaves O before this item's
@@ -831,13 +816,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
                     for (int c = 0; c < DH / 8; ++c) {
                         float o[8];
-                        tmem_ld8(to + 8 * c, o);
+                        tmem_ld_h8<DH>(to + 8 * c, o);
 #pragma unroll
                         for (int y = 0; y < 8; ++y) o[y] *= alpha;
-                        tmem_st8(to + 8 * c, o);
+                        tmem_st_h8<DH>(to + 8 * c, o);
                     }
                 }
-                tmem_st32(tl + TM_P + 32 * half, *reinterpret_cast<float(*)[32]>(pk));
+                tmem_st_h32<HN / 2>(tl + TM_P, *reinterpret_cast<float(*)[32]>(pk));
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(S::B_P));

@@ -312,6 +312,83 @@ __device__ __forceinline__ void tmem_ld_3x32(uint32_t s0, uint32_t b0, uint32_t 
 #undef TXL_R8
 }
 
+// ---- the 16-lane shape (.16x32bx2): a warp reads or writes 16 TMEM lanes
+// (its lane base: the address's lane field); threads 0-15 take lanes
+// base..base+15 at the given columns, threads 16-31 the same lanes at the
+// columns + OFF.  Two threads per lane: each can own half of a row.
+
+// S: two 32-column loads; band window: 32 + 32 + 16 columns; one wait.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_h_tile(uint32_t s0, uint32_t s1, uint32_t b0, uint32_t b1, uint32_t b2,
+                                               float (&x)[64], float (&a)[80])
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(x);
+    uint32_t *q = reinterpret_cast<uint32_t *>(a);
+#define TXL_R8(p, o) "=r"(p[o]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3]), "=r"(p[o + 4]), \
+                     "=r"(p[o + 5]), "=r"(p[o + 6]), "=r"(p[o + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%144], %149;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%145], %149;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%146], %149;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%147], %149;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%128,%129,%130,%131,%132,%133,%134,%135,%136,%137,%138,%139,%140,%141,%142,%143}, [%148], %149;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TXL_R8(r, 0), TXL_R8(r, 8), TXL_R8(r, 16), TXL_R8(r, 24), TXL_R8(r, 32), TXL_R8(r, 40),
+          TXL_R8(r, 48), TXL_R8(r, 56), TXL_R8(q, 0), TXL_R8(q, 8), TXL_R8(q, 16), TXL_R8(q, 24),
+          TXL_R8(q, 32), TXL_R8(q, 40), TXL_R8(q, 48), TXL_R8(q, 56), TXL_R8(q, 64), TXL_R8(q, 72)
+        : "r"(s0), "r"(s1), "r"(b0), "r"(b1), "r"(b2), "n"(OFF)
+        : "memory");
+#undef TXL_R8
+}
+
+template <int OFF>
+__device__ __forceinline__ void tmem_st_h32(uint32_t taddr, const float (&v)[32])
+{
+    const uint32_t *r = reinterpret_cast<const uint32_t *>(v);
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %33, "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31]), "n"(OFF)
+        : "memory");
+}
+
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_h8(uint32_t taddr, float *v)
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr), "n"(OFF)
+        : "memory");
+}
+
+template <int OFF>
+__device__ __forceinline__ void tmem_st_h8(uint32_t taddr, const float *v)
+{
+    const uint32_t *r = reinterpret_cast<const uint32_t *>(v);
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %9, {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "n"(OFF)
+                 : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
