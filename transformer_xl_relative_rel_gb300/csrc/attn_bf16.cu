@@ -473,10 +473,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         } else if (warp == 1) {
             // =============================================================== S / band MMAs
             // per tile: S = (q+u) K^T (N = 128) and the tile's band window
-            // (q+v) [chunk n; chunk n+1]^T (two N = 128 MMAs per K step) into
-            // TMEM.  One thread waits and issues.
+            // (q+v) [chunk n; chunk n+1]^T (N = 256) into TMEM.  One thread
+            // waits and issues.
             if (lane == 0) {
                 const uint32_t idesc_n = idesc_bf16(BM, BN, 0, 0);
+                const uint32_t idesc_w = idesc_bf16(BM, 2 * BN, 0, 0);   // the band of two adjacent chunks
                 // descriptors built once; the 14-bit start-address field (address / 16)
                 // advances by 2 per 32-byte K step within a 128-byte swizzled row
                 const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
@@ -502,13 +503,22 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         if (!ok) break;
                         tc_fence_after();
                         const uint64_t dk = d_st0 + st * KV16, da = d_ch0 + sa * TILE16, db = d_ch0 + sb * TILE16;
+                        // S and band K steps alternate (two accumulation chains
+                        // in flight); when chunk n+1 sits in the slot after
+                        // chunk n the band is one N = 256 MMA per K step
+                        if (sb == sa + 1) {
 #pragma unroll
-                        for (int ks = 0; ks < DP / 16; ++ks)
-                            mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+                            for (int ks = 0; ks < DP / 16; ++ks) {
+                                mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+                                mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_w, ks > 0);
+                            }
+                        } else {
 #pragma unroll
-                        for (int ks = 0; ks < DP / 16; ++ks) {
-                            mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_n, ks > 0);
-                            mma_bf16_ss(tmem + TM_BAND + BN, d_qv + 2 * ks, db + 2 * ks, idesc_n, ks > 0);
+                            for (int ks = 0; ks < DP / 16; ++ks) {
+                                mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+                                mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_n, ks > 0);
+                                mma_bf16_ss(tmem + TM_BAND + BN, d_qv + 2 * ks, db + 2 * ks, idesc_n, ks > 0);
+                            }
                         }
                         mma_commit(bar(S::B_S));
                         mma_commit(bar(S::B_CHE + sa));                   // chunk n: read for the last time
