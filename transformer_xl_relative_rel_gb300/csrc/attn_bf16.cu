@@ -78,6 +78,7 @@ struct Params {
     int nqt, splits;
     int items;          // B*H*nqt*splits work items
     int kv_start;       // K, V rows form a ring: key j at row (kv_start + j) mod T
+    int ost;            // 1: output tiles written by TMA store (tensor map tm_o)
     float sl2;          // log2(e) / sqrt(D)
 };
 
@@ -92,15 +93,17 @@ struct Smem {
     static constexpr uint32_t QU = CH0 + NCH * TILE;        // q+u, q+v: 128 rows of 128 bytes
     static constexpr uint32_t QV = QU + BM * 128;
     static constexpr uint32_t QRAW = QV + BM * 128;         // raw q rows of the next item
-    static constexpr uint32_t UW = QRAW + BM * 128;         // its head's u and v biases (fp32, 2 x 64)
+    static constexpr uint32_t OST = QRAW + BM * 128;        // an item's output tile (bf16), for the TMA store
+    static constexpr uint32_t UW = OST + BM * 128;          // the next item's u and v biases (fp32, 2 x 64)
     static constexpr uint32_t BARS = UW + 2 * 64 * 4;
     // barrier slots (8 bytes each): q+u/q+v ready, raw q ready, raw q read;
     // per K/V stage full / empty; per chunk slot full / empty; S full, S
-    // free (loaded by the softmax), P full, P.V done
+    // free (loaded by the softmax), P full, P.V done; output tile written,
+    // output buffer free
     static constexpr int B_Q = 0, B_QRAW = 1, B_QRF = 2, B_FULL = 3, B_EMPTY = 3 + NSTAGE,
                          B_CHF = 3 + 2 * NSTAGE, B_CHE = B_CHF + NCH, B_S = B_CHE + NCH, B_SF = B_S + 1,
-                         B_P = B_SF + 1, B_PV = B_P + 1;
-    static_assert(B_PV < 32, "barrier slots");
+                         B_P = B_SF + 1, B_PV = B_P + 1, B_OST = B_PV + 1, B_OFR = B_OST + 1;
+    static_assert(B_OFR < 32, "barrier slots");
     static constexpr uint32_t MISC = BARS + 32 * 8;         // tmem holder, abort flag
     static constexpr uint32_t USED = MISC + 16;
     // + 1 KB to align the base to the 1024-byte swizzle atom; at least 120 KB
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(NT, 1)
 rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8,
-                     const Params p)
+                     const __grid_constant__ CUtensorMap tm_o, const Params p)
 {
     using S = Smem<DP>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -314,9 +317,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
     if (tid == 0) {
         *abort = 0;
-        mbar_init(bar(S::B_Q), 128);
+        mbar_init(bar(S::B_Q), 256);
         mbar_init(bar(S::B_QRAW), kTma ? 1 : 32);
-        mbar_init(bar(S::B_QRF), 128);
+        mbar_init(bar(S::B_QRF), 256);
         for (int x = 0; x < NSTAGE; ++x) {
             mbar_init(bar(S::B_FULL + x), kTma ? 1 : 64);
             mbar_init(bar(S::B_EMPTY + x), 1);
@@ -329,6 +332,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         mbar_init(bar(S::B_SF), 256);
         mbar_init(bar(S::B_P), 256);
         mbar_init(bar(S::B_PV), 1);
+        mbar_init(bar(S::B_OST), 256);
+        mbar_init(bar(S::B_OFR), 1);
         fence_mbar_init();
         if (kTma) {
             prefetch_tmap(&tm_k);
@@ -339,6 +344,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 prefetch_tmap(&tm_k8);
                 prefetch_tmap(&tm_v8);
             }
+            if (p.ost) prefetch_tmap(&tm_o);
         }
     }
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
@@ -570,31 +576,33 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int ii = lb + r16;                   // this thread's query row
         const uint32_t tl = tmem + ((uint32_t)lb << 16);
         // q+u and q+v of an item's row, scaled by log2(e)/sqrt(D) and rounded
-        // once to bf16, from the raw rows into the MMA operand buffers (warps
-        // 4-7, one row per thread: row 32*quarter + lane; item number ni)
+        // once to bf16, from the raw rows into the MMA operand buffers (every
+        // softmax thread: half of its own row, columns 8*DC*half ..; item
+        // number ni)
+        constexpr int DC = DP / 16;                // 8-column chunks per half row
         auto convert_q = [&](const Item &it, int ni) {
             if (!wwait(S::B_QRAW, ni & 1)) return false;
-            const int ic = quarter * 32 + lane;
             const float4 *uw4 = reinterpret_cast<const float4 *>(smem + S::UW);
-            const float keep = ic < it.rows_here ? 1.f : 0.f;   // rows past L: zero operands
+            const float keep = ii < it.rows_here ? 1.f : 0.f;   // rows past L: zero operands
             // every load first (the stores below could alias them as far as the
             // compiler knows), then the arithmetic and the stores
-            uint4 raw[DP / 8];
-            float4 u4[DP / 4], w4[DP / 4];
+            uint4 raw[DC];
+            float4 u4[2 * DC], w4[2 * DC];
 #pragma unroll
-            for (int d8 = 0; d8 < DP / 8; ++d8)
-                raw[d8] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ic, 8 * d8));
+            for (int c = 0; c < DC; ++c)
+                raw[c] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * (DC * half + c)));
 #pragma unroll
-            for (int d4 = 0; d4 < DP / 4; ++d4) {
-                u4[d4] = uw4[d4];
-                w4[d4] = uw4[16 + d4];
+            for (int d4 = 0; d4 < 2 * DC; ++d4) {
+                u4[d4] = uw4[2 * DC * half + d4];
+                w4[d4] = uw4[16 + 2 * DC * half + d4];
             }
             const float sk = p.sl2 * keep;
 #pragma unroll
-            for (int d8 = 0; d8 < DP / 8; ++d8) {
-                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw[d8]);
-                const float *uu = reinterpret_cast<const float *>(&u4[2 * d8]);
-                const float *ww = reinterpret_cast<const float *>(&w4[2 * d8]);
+            for (int c = 0; c < DC; ++c) {
+                const int d8 = DC * half + c;
+                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw[c]);
+                const float *uu = reinterpret_cast<const float *>(&u4[2 * c]);
+                const float *ww = reinterpret_cast<const float *>(&w4[2 * c]);
                 uint32_t a4[4], c4[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
@@ -602,9 +610,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
                     c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
                 }
-                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ic, 8 * d8)) =
+                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
-                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ic, 8 * d8)) =
+                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ii, 8 * d8)) =
                     make_uint4(c4[0], c4[1], c4[2], c4[3]);
             }
             fence_proxy_async_smem();
@@ -639,6 +647,22 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             for (int y = 0; y < 33; ++y) w[y] = (shift & 2) ? w[y + 1] : w[y];
 #pragma unroll
             for (int k = 0; k < 32; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(w[k], w[k + 1], odd_sel));
+        };
+        // the same for 32 keys from a 24-register piece of the window (keys
+        // 0-31: registers 0-23, keys 32-63: registers 16-39), so that the
+        // exponentials of one piece can overlap the shifts of the other
+        auto band_half = [&](const uint32_t *w0, float *xb) {
+            uint32_t w[24];
+#pragma unroll
+            for (int y = 0; y < 24; ++y) w[y] = w0[y];
+#pragma unroll
+            for (int y = 0; y < 20; ++y) w[y] = (shift & 8) ? w[y + 4] : w[y];
+#pragma unroll
+            for (int y = 0; y < 18; ++y) w[y] = (shift & 4) ? w[y + 2] : w[y];
+#pragma unroll
+            for (int y = 0; y < 17; ++y) w[y] = (shift & 2) ? w[y + 1] : w[y];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(w[k], w[k + 1], odd_sel));
         };
         // keys past the row's causal limit (j > M+i) get -inf
         auto mask_block = [&](float *xb, int first, int lim) {
@@ -682,6 +706,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             int i0, rows_here, bh, split;
             float m, l;
         };
+        int n_out = 0;                             // items stored through the output buffer
         auto epilogue = [&](const Done &dn, int g_last) {
             if (!wwait(S::B_PV, g_last & 1)) return false;
             const float l = dn.l + partner(dn.l);
@@ -693,6 +718,36 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int d0 = DH * half;
             const int i = dn.i0 + ii;
+            if (kTma && p.ost) {
+                // the 128 x 64 tile goes through shared memory (the tensor
+                // map's swizzled layout) and out by one TMA store; rows past L
+                // are not written.  The buffer is free once the previous
+                // item's store has read it.
+                const bool lead = warp == 4 && lane == 0;
+                if (lead) {
+                    bulk_wait_read();
+                    mbar_arrive(bar(S::B_OFR));
+                }
+                if (!wwait(S::B_OFR, n_out & 1)) return false;
+#pragma unroll
+                for (int c = 0; c < DH / 8; ++c) {
+                    uint4 pk4;
+                    pk4.x = pack_bf16(o[c * 8 + 0] * inv, o[c * 8 + 1] * inv);
+                    pk4.y = pack_bf16(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv);
+                    pk4.z = pack_bf16(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv);
+                    pk4.w = pack_bf16(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv);
+                    *reinterpret_cast<uint4 *>(smem + S::OST + sw128_offset(ii, d0 + 8 * c)) = pk4;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(S::B_OST));
+                if (lead) {
+                    if (!wait_or_abort(bar(S::B_OST), n_out & 1, abort)) return false;
+                    tma_store_3d(&tm_o, sbase + S::OST, 0, dn.i0, dn.bh);
+                    bulk_commit();
+                }
+                ++n_out;
+                return true;
+            }
             if (ii >= dn.rows_here) return true;
             if (p.splits == 1) {
                 __nv_bfloat16 *op = p.out + (long)i * qkv_row + dn.head_off + d0;
@@ -742,7 +797,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         bool ok = true;
         Item it;
         int j = next_busy(p, 0, it);
-        if (rh == 0 && j >= 0) ok = convert_q(it, 0);
+        if (j >= 0) ok = convert_q(it, 0);
         int g = 0, ni = 0;
         bool pending = false;                      // the previous item's output is still in O
         Done prev;
@@ -763,7 +818,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 // the item's last S MMAs have read q+u, q+v: the next item's
                 // operands go in now, so that its first MMAs overlap the rest
                 // of this item
-                if (n == it.N - 1 && rh == 0 && jn >= 0 && !convert_q(nx, ni + 1)) {
+                if (n == it.N - 1 && jn >= 0 && !convert_q(nx, ni + 1)) {
                     ok = false;
                     break;
                 }
@@ -777,35 +832,42 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 uint32_t hb[40];
 #pragma unroll
                 for (int y = 0; y < 40; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
-                band_all(hb, x);
-                if (diag) {
-                    mask_block(x, 0, lim);
-                    mask_block(x + 32, 32, lim);
-                }
-                // exponentials against the running reference max; rows without
-                // a finite reference yet take the row's max first.  The row's
-                // sum over all 128 keys is then checked (the row's two lanes
-                // see the same sum and the whole warp takes one branch): past
-                // SUM_LIMIT the reference is raised to the row's max and the
-                // pass repeated.
-                float pk[32], psum, alpha = 1.f;
-                bool raise = false;
-                bool find_max = __any_sync(0xffffffffu, m_used == -INFINITY);
-                for (int pass = 0;; ++pass) {
-                    if (find_max) {
-                        float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
-                        lmax = fmaxf(lmax, partner(lmax));
-                        const float m_new = fmaxf(m_used, lmax);
-                        if (m_new > m_used) {
-                            alpha *= ex2(m_used - m_new);      // 0 when m_used = -inf
-                            m_used = m_new;
-                            raise = true;
-                        }
-                    }
-                    const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-                    psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
+                // exponentials against the running reference max.  Off the
+                // diagonal, once the rows have a finite reference, the tile
+                // runs straight through: shift, add and exponentials of the
+                // two 32-key pieces.  The row's sum over all 128 keys is then
+                // checked (the row's two lanes see the same sum and the whole
+                // warp takes one branch): past SUM_LIMIT, and on the first
+                // tile of an item or a diagonal tile, the reference is first
+                // raised to the row's max.
+                float pk[32], psum = 0.f, alpha = 1.f;
+                bool raise = false, find_max;
+                if (!diag && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
+                    band_half(hb, x);
+                    const float s0 = expo(x, m_used, pk);
+                    band_half(hb + 16, x + 32);
+                    const float s1 = expo(x + 32, m_used, pk + 16);
+                    psum = s0 + s1;
                     find_max = __any_sync(0xffffffffu, !(psum + partner(psum) <= SUM_LIMIT));
-                    if (!find_max || pass > 0) break;
+                } else {
+                    band_all(hb, x);
+                    if (diag) {
+                        mask_block(x, 0, lim);
+                        mask_block(x + 32, 32, lim);
+                    }
+                    find_max = true;
+                }
+                if (find_max) {
+                    float lmax = fmaxf(rowmax32(x), rowmax32(x + 32));
+                    lmax = fmaxf(lmax, partner(lmax));
+                    const float m_new = fmaxf(m_used, lmax);
+                    if (m_new > m_used) {
+                        alpha = ex2(m_used - m_new);      // 0 when m_used = -inf
+                        m_used = m_new;
+                        raise = true;
+                    }
+                    const float mu = (m_used == -INFINITY) ? 0.f : m_used;   // a row masked so far
+                    psum = expo(x, mu, pk) + expo(x + 32, mu, pk + 16);
                 }
                 l_run = l_run * alpha + psum;
                 if (n == 0) {
@@ -852,6 +914,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             ++ni;
         }
         if (ok && pending) epilogue(prev, g - 1);
+        if (warp == 4 && lane == 0) bulk_wait_all();   // the output stores are done
     }
 
     tc_fence_before();
@@ -923,7 +986,7 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
 template <int DP, bool kTma>
 cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                      const CUtensorMap &mr, const CUtensorMap &mq, const CUtensorMap &mk8,
-                     const CUtensorMap &mv8, cudaStream_t s)
+                     const CUtensorMap &mv8, const CUtensorMap &mo, cudaStream_t s)
 {
     const uint32_t smem = Smem<DP>::TOTAL;
     auto kern = rel_attn_bf16_kernel<DP, kTma>;
@@ -931,7 +994,7 @@ cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM, each walks its share of the work items
     const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
-    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, mk8, mv8, p);
+    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, mk8, mv8, mo, p);
     return cudaGetLastError();
 }
 
@@ -1012,7 +1075,9 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
     p.kv_start = a.kv_start;
-    CUtensorMap mk, mv, mr, mq, mk8, mv8;
+    CUtensorMap mk, mv, mr, mq, mk8, mv8, mo;
+    memset(&mo, 0, sizeof(mo));
+    p.ost = 0;
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
     memset(&mr, 0, sizeof(mr));
@@ -1032,13 +1097,18 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
             !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM) ||
             !make_map(&mk8, a.k, p.T, rs, bhn, 8) || !make_map(&mv8, a.v, p.T, rs, bhn, 8))
             return cudaErrorInvalidValue;
+        // the output by TMA store when it is one pass (no key splits) and 16-byte aligned
+        if (splits == 1 && ((uintptr_t)a.out & 15) == 0) {
+            if (!make_map(&mo, a.out, a.L, rs, bhn, BM)) return cudaErrorInvalidValue;
+            p.ost = 1;
+        }
     }
     cudaError_t e;
     switch (DP) {
-    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<16, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
-    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<32, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
-    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<48, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
-    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, s); break;
+    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<16, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<32, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<48, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
     }
     if (e != cudaSuccess || splits == 1) return e;
     rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
