@@ -536,21 +536,39 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             __syncwarp();
         } else if (warp == 2) {
             // =============================================================== P.V MMAs
+            // This thread also writes the output tiles: the softmax threads
+            // stage an item's O / l in shared memory during the next item's
+            // first tile, before that tile's P, so the tile's P barrier shows
+            // the stage complete.  The buffer is handed back (B_OFR) once the
+            // store has read it; the CTA's last item signals on B_OST.
             if (lane == 0) {
                 const uint32_t idesc_o = idesc_bf16(BM, DP, 0, 1);   // V is MN-major (d contiguous)
                 const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
                 constexpr uint64_t KV16 = S::KV >> 4, TILE16 = S::TILE >> 4;
-                Item it;
+                const bool ost = kTma && p.ost;
+                if (ost) mbar_arrive(bar(S::B_OFR));   // the buffer starts free
+                bool in_flight = false;                // a store may still be reading the buffer
+                Item it, prev;
                 int g = 0;
-                bool ok = true;
+                bool ok = true, have_prev = false;
                 for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it)) {
                     for (int n = 0; n < it.N; ++n, ++g) {
                         const int st = g % NSTAGE;
+                        if (in_flight) {
+                            bulk_wait_read();
+                            mbar_arrive(bar(S::B_OFR));
+                            in_flight = false;
+                        }
                         if (!wait_or_abort(bar(S::B_P), g & 1, abort)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        if (ost && n == 0 && have_prev) {
+                            tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0, prev.bh);
+                            bulk_commit();
+                            in_flight = true;
+                        }
                         const uint64_t dv = d_st0 + st * KV16 + TILE16;   // 16 keys = 2048 bytes of V
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)   // P: 16 keys = 8 TMEM columns
@@ -559,7 +577,20 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         mma_commit(bar(S::B_PV));
                         mma_commit(bar(S::B_EMPTY + st));
                     }
+                    prev = it;
+                    have_prev = true;
                 }
+                if (ok && ost && have_prev) {
+                    if (in_flight) {
+                        bulk_wait_read();
+                        mbar_arrive(bar(S::B_OFR));
+                    }
+                    if (wait_or_abort(bar(S::B_OST), 0, abort)) {
+                        tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0, prev.bh);
+                        bulk_commit();
+                    }
+                }
+                bulk_wait_all();   // the output stores are done
             }
             __syncwarp();
         }
@@ -707,7 +738,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             float m, l;
         };
         int n_out = 0;                             // items stored through the output buffer
-        auto epilogue = [&](const Done &dn, int g_last) {
+        auto epilogue = [&](const Done &dn, int g_last, bool last) {
             if (!wwait(S::B_PV, g_last & 1)) return false;
             const float l = dn.l + partner(dn.l);
             tc_fence_after();
@@ -720,14 +751,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int i = dn.i0 + ii;
             if (kTma && p.ost) {
                 // the 128 x 64 tile goes through shared memory (the tensor
-                // map's swizzled layout) and out by one TMA store; rows past L
-                // are not written.  The buffer is free once the previous
-                // item's store has read it.
-                const bool lead = warp == 4 && lane == 0;
-                if (lead) {
-                    bulk_wait_read();
-                    mbar_arrive(bar(S::B_OFR));
-                }
+                // map's swizzled layout) and out by one TMA store, issued by
+                // the P.V thread; rows past L are not written.  The buffer is
+                // free once the previous item's store has read it.
                 if (!wwait(S::B_OFR, n_out & 1)) return false;
 #pragma unroll
                 for (int c = 0; c < DH / 8; ++c) {
@@ -739,12 +765,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     *reinterpret_cast<uint4 *>(smem + S::OST + sw128_offset(ii, d0 + 8 * c)) = pk4;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(bar(S::B_OST));
-                if (lead) {
-                    if (!wait_or_abort(bar(S::B_OST), n_out & 1, abort)) return false;
-                    tma_store_3d(&tm_o, sbase + S::OST, 0, dn.i0, dn.bh);
-                    bulk_commit();
-                }
+                if (last) mbar_arrive(bar(S::B_OST));   // no later P barrier shows it
                 ++n_out;
                 return true;
             }
@@ -873,7 +894,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 if (n == 0) {
                     // the previous item's output leaves O before this item's
                     // first P.V overwrites it; its last P.V has long finished
-                    if (pending && !epilogue(prev, g - 1)) {
+                    if (pending && !epilogue(prev, g - 1, false)) {
                         ok = false;
                         break;
                     }
@@ -913,8 +934,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             it = nx;
             ++ni;
         }
-        if (ok && pending) epilogue(prev, g - 1);
-        if (warp == 4 && lane == 0) bulk_wait_all();   // the output stores are done
+        if (ok && pending) epilogue(prev, g - 1, true);
     }
 
     tc_fence_before();
