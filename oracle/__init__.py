@@ -9,6 +9,8 @@ Contents
   * ``txl_oracle.c`` -- the float64 triple loop over (i, j, d) with direct
     ``r_{i-j}`` indexing (Transformer-XL, Section 3.3 procedure and Appendix B
     table order), built here with gcc into ``liboracle.so``.
+  * ``rel_attn_bwd`` (same C file) -- the gradients of one layer call for a
+    given output gradient, the chain rule written out per query row.
   * ``mem_update`` -- the memory rollover of Section 3.2 written as its plain
     definition in numpy: the new memory is the newest M rows of
     [old memory; current hidden states].
@@ -70,6 +72,11 @@ def _load() -> ctypes.CDLL:
             ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
             ctypes.POINTER(ctypes.c_int64), ctypes.c_long, _dp, ctypes.c_int]
         lib.txl_oracle_rel_attn_rows.restype = None
+        lib.txl_oracle_rel_attn_bwd.argtypes = [
+            _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+        lib.txl_oracle_rel_attn_bwd.restype = None
         lib.txl_oracle_max_threads.argtypes = []
         lib.txl_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -138,6 +145,33 @@ def rel_attn_rows(q, k, v, r, u, w, mem_len: int, rows, nthreads: int = 0):
         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.shape[0],
         _ptr(out), int(nthreads))
     return out
+
+
+def rel_attn_bwd(q, k, v, r, u, w, dout, mem_len: int, nthreads: int = 0):
+    """Gradients of ``rel_attn`` for the output gradient ``dout`` [L, B, H, D],
+    float64: the chain rule through the masked softmax and the four-term
+    score, written out per query row (Section 3.3 procedure; every input,
+    the memory rows of k and v included, gets its gradient).
+
+    Returns a dict with ``dq`` [L,B,H,D], ``dk``, ``dv`` [T,B,H,D], ``dr``
+    [T,H,D] (summed over the batch), ``du``, ``dw`` [H,D] (the u and v bias
+    gradients, summed over batch and query rows).
+    """
+    q, k, v, r, u, w, dout = (_f64(x) for x in (q, k, v, r, u, w, dout))
+    B, H, D, L, T = _shapes(q, k, v, r, u, w, mem_len)
+    if dout.shape != q.shape:
+        raise ValueError(f"dout must be {q.shape}, got {dout.shape}")
+    g = dict(dq=np.zeros((L, B, H, D)), dk=np.zeros((T, B, H, D)), dv=np.zeros((T, B, H, D)),
+             dr=np.zeros((T, H, D)), du=np.zeros((H, D)), dw=np.zeros((H, D)))
+    dr_part = np.zeros((B * H, T, D))
+    du_part = np.zeros((B * H, D))
+    dw_part = np.zeros((B * H, D))
+    _load().txl_oracle_rel_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u), _ptr(w), _ptr(dout),
+        B, H, D, L, mem_len,
+        _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dr"]), _ptr(g["du"]), _ptr(g["dw"]),
+        _ptr(dr_part), _ptr(du_part), _ptr(dw_part), int(nthreads))
+    return g
 
 
 def mem_update(ext_ctx, mem_len: int) -> np.ndarray:

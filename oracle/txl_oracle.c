@@ -146,6 +146,115 @@ void txl_oracle_rel_attn_rows(const double *q, const double *k, const double *v,
     }
 }
 
+/* Gradients of one layer call for a given output gradient dout (the
+ * backward of the function above, written out by the chain rule).  For one
+ * query row (b, h, i), with P_j the softmax weights and A_j the unscaled
+ * four-term score:
+ *   dP_j  = dout_i . v_j
+ *   dS_j  = P_j (dP_j - sum_l P_l dP_l)          (softmax, on the scaled score)
+ *   dA_j  = dS_j / sqrt(D)
+ *   dq_i += dA_j (k_j + r_{T-1-off})             (both bias-shifted queries)
+ *   dk_j += dA_j (q_i + u)      dv_j += P_j dout_i
+ *   dr_{T-1-off} += dA_j (q_i + v)               (summed over the batch)
+ *   du   += dA_j k_j            dw   += dA_j r_{T-1-off}
+ * with off = M+i-j the relative distance of the visible pair (j <= M+i).
+ * Every input gets its gradient, the memory rows of k and v included: the
+ * stop-gradient of Section 3.2 stops at the cached hidden states, not at the
+ * keys and values computed from them.  dr_part, du_part, dw_part are scratch
+ * of B*H*T*D, B*H*D, B*H*D doubles (one slice per (b, h), summed at the end
+ * so that the parallel loop shares no accumulator). */
+void txl_oracle_rel_attn_bwd(const double *q, const double *k, const double *v,
+                             const double *r, const double *u, const double *w,
+                             const double *dout, long B, long H, long D, long L,
+                             long M, double *dq, double *dk, double *dv, double *dr,
+                             double *du, double *dw, double *dr_part,
+                             double *du_part, double *dw_part, int nthreads)
+{
+    const long T = M + L;
+    const long nbh = B * H;
+    const double scale = 1.0 / sqrt((double)D);
+    for (long x = 0; x < L * B * H * D; ++x) dq[x] = 0.0;
+    for (long x = 0; x < T * B * H * D; ++x) dk[x] = dv[x] = 0.0;
+    for (long x = 0; x < nbh * T * D; ++x) dr_part[x] = 0.0;
+    for (long x = 0; x < nbh * D; ++x) du_part[x] = dw_part[x] = 0.0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (long bh = 0; bh < nbh; ++bh) {
+            const long b = bh / H, h = bh % H;
+            const double *uh = u + h * D, *wh = w + h * D;
+            double *drp = dr_part + bh * T * D, *dup = du_part + bh * D, *dwp = dw_part + bh * D;
+            for (long i = 0; i < L; ++i) {
+                const double *qi = q + ((i * B + b) * H + h) * D;
+                const double *gi = dout + ((i * B + b) * H + h) * D;
+                double *dqi = dq + ((i * B + b) * H + h) * D;
+                const long last = M + i;
+                double mx = -INFINITY;
+                for (long j = 0; j <= last; ++j) {
+                    const long off = M + i - j;
+                    const double *rr = r + ((T - 1 - off) * H + h) * D;
+                    const double *kj = k + ((j * B + b) * H + h) * D;
+                    double a = 0.0;
+                    for (long d = 0; d < D; ++d) a += (qi[d] + uh[d]) * kj[d] + (qi[d] + wh[d]) * rr[d];
+                    s[j] = a * scale;
+                    if (s[j] > mx) mx = s[j];
+                }
+                double z = 0.0;
+                for (long j = 0; j <= last; ++j) {
+                    s[j] = exp(s[j] - mx);
+                    z += s[j];
+                }
+                double delta = 0.0;
+                for (long j = 0; j <= last; ++j) {
+                    s[j] /= z; /* P_j */
+                    const double *vj = v + ((j * B + b) * H + h) * D;
+                    double g = 0.0;
+                    for (long d = 0; d < D; ++d) g += gi[d] * vj[d];
+                    dp[j] = g;
+                    delta += s[j] * g;
+                }
+                for (long j = 0; j <= last; ++j) {
+                    const long off = M + i - j;
+                    const long t = T - 1 - off;
+                    const double *rr = r + (t * H + h) * D;
+                    const double *kj = k + ((j * B + b) * H + h) * D;
+                    double *dkj = dk + ((j * B + b) * H + h) * D;
+                    double *dvj = dv + ((j * B + b) * H + h) * D;
+                    const double da = s[j] * (dp[j] - delta) * scale;
+                    for (long d = 0; d < D; ++d) {
+                        dqi[d] += da * (kj[d] + rr[d]);
+                        dkj[d] += da * (qi[d] + uh[d]);
+                        dvj[d] += s[j] * gi[d];
+                        drp[t * D + d] += da * (qi[d] + wh[d]);
+                        dup[d] += da * kj[d];
+                        dwp[d] += da * rr[d];
+                    }
+                }
+            }
+        }
+        free(s);
+        free(dp);
+    }
+    for (long x = 0; x < T * H * D; ++x) dr[x] = 0.0;
+    for (long x = 0; x < H * D; ++x) du[x] = dw[x] = 0.0;
+    for (long bh = 0; bh < nbh; ++bh) {
+        const long h = bh % H;
+        for (long t = 0; t < T; ++t)
+            for (long d = 0; d < D; ++d) dr[(t * H + h) * D + d] += dr_part[(bh * T + t) * D + d];
+        for (long d = 0; d < D; ++d) {
+            du[h * D + d] += du_part[bh * D + d];
+            dw[h * D + d] += dw_part[bh * D + d];
+        }
+    }
+}
+
 /* Number of threads OpenMP would use (1 when built without OpenMP). */
 int txl_oracle_max_threads(void)
 {
