@@ -156,6 +156,42 @@ txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int 
                          txl_dtype dtype, void *stream);
 
 /*
+ * txl_rel_attn_bwd -- gradients of one txl_rel_attn_fwd call for a given
+ * output gradient dout (the chain rule through the masked softmax and the
+ * four-term score of Section 3.3).  With P the softmax weights of query row
+ * i, dA_ij = P_ij (dout_i.v_j - sum_l P_il dout_i.v_l) / sqrt(d_head) for the
+ * visible keys j <= M+i and off = M+i-j:
+ *     dq_i = sum_j dA_ij (k_j + r[T-1-off])    dk_j = sum_i dA_ij (q_i + u)
+ *     dv_j = sum_i P_ij dout_i                 dr[T-1-off] += dA_ij (q_i + v)
+ *     du   = sum_{b,i,j} dA_ij k_j             dw = sum_{b,i,j} dA_ij r[T-1-off]
+ * (dr, du, dw summed over the batch).  Every input gets its gradient, the
+ * memory rows 0..M-1 of k and v included: Section 3.2's stop-gradient acts
+ * on the cached hidden states, while the keys and values projected from them
+ * still carry gradient to the projections.
+ *
+ * q, k, v, r, dout : device, dtype, layouts as txl_rel_attn_fwd (dout like q).
+ * u_bias, v_bias   : device float32 [heads][d_head] or NULL (zero bias).
+ * dq, dk, dv, dr   : device outputs, dtype, shaped like q, k, v, r.
+ * du, dw           : device float32 [heads][d_head] outputs, or NULL (not
+ *                    computed).  Outputs must not overlap each other, any
+ *                    input or the workspace.
+ * workspace        : device scratch of at least the bytes that
+ *                    txl_rel_attn_bwd_workspace reports, 256-byte aligned,
+ *                    owned by the caller (about 3 x 4 + 3 x dtype bytes per
+ *                    (b, h, i, j) score entry: the score, P, dP and dA of
+ *                    every head are materialised).
+ * Limits: d_head <= 128 (else TXL_ERR_UNSUPPORTED).  Asynchronous on stream.
+ * bf16: operands of the contractions in bf16 (q+u, q+v, P and dA rounded
+ * once), fp32 accumulation, fp32 softmax; fp32: fp32 throughout.
+ */
+txl_status txl_rel_attn_bwd_workspace(int batch, int mem_len, int seg_len, int heads, int d_head,
+                                      txl_dtype dtype, size_t *bytes);
+txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const void *r, const float *u_bias,
+                            const float *v_bias, const void *dout, int batch, int mem_len, int seg_len, int heads,
+                            int d_head, txl_dtype dtype, void *dq, void *dk, void *dv, void *dr, float *du,
+                            float *dw, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * txl_ring_append -- write n_rows new rows into a ring of ring_len rows at
  * rows (start + i) mod ring_len, i = 0 .. n_rows-1 (the oldest rows of the
  * ring, for a ring kept as above: start = the current kv_start, after which

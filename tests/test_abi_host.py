@@ -116,3 +116,61 @@ def test_ring_calls_reject_bad_arguments(lib):
     assert g(None, FAKE * 4, 10, 3, 8, 0, 1, None) == INVALID
     assert g(FAKE, FAKE * 4, 10, 3, 8, 0, 9, None) == UNSUPPORTED
     assert g(None, None, 10, 0, 8, 0, 1, None) == OK              # nothing to copy
+
+
+def _bwd_ws(B=2, M=8, L=8, H=2, D=16, dt=1):
+    n = ctypes.c_size_t(0)
+    st = abi.load_library().txl_rel_attn_bwd_workspace(B, M, L, H, D, dt, ctypes.byref(n))
+    return st, n.value
+
+
+def test_bwd_workspace_query(lib):
+    st, n = _bwd_ws()
+    assert st == OK
+    B, M, L, H, D = 2, 8, 8, 2, 16
+    # at least the score, P, dP and dA of every (b, h, i, j) (two fp32, three bf16)
+    assert n >= B * H * L * (M + L) * (2 * 4 + 3 * 2)
+    assert _bwd_ws(dt=0)[1] > n                      # fp32 operands take more
+    assert _bwd_ws(B=4)[1] > n
+    assert _bwd_ws(dt=7)[0] == UNSUPPORTED
+    assert _bwd_ws(D=129)[0] == UNSUPPORTED
+    assert _bwd_ws(B=0)[0] == INVALID
+    assert _bwd_ws(L=0)[0] == INVALID
+    assert _bwd_ws(M=-1)[0] == INVALID
+    assert abi.load_library().txl_rel_attn_bwd_workspace(2, 8, 8, 2, 16, 1, None) == INVALID
+
+
+def _bwd(**kw):
+    st, need = _bwd_ws()
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, r=FAKE * 4, u=FAKE * 5, w=FAKE * 6, dout=FAKE * 7,
+             B=2, M=8, L=8, H=2, D=16, dt=1, dq=FAKE * 8, dk=FAKE * 9, dv=FAKE * 10, dr=FAKE * 11,
+             du=FAKE * 12, dw=FAKE * 13, ws=FAKE * 14, nws=need, stream=None)
+    a.update(kw)
+    return abi.load_library().txl_rel_attn_bwd(
+        a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["dout"], a["B"], a["M"], a["L"], a["H"], a["D"],
+        a["dt"], a["dq"], a["dk"], a["dv"], a["dr"], a["du"], a["dw"], a["ws"], a["nws"], a["stream"])
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert _bwd(dt=7) == UNSUPPORTED
+    assert _bwd(D=129) == UNSUPPORTED
+    assert _bwd(B=0) == INVALID
+    assert _bwd(L=0) == INVALID
+    assert _bwd(M=-2) == INVALID
+    for name in ("q", "k", "v", "r", "dout", "dq", "dk", "dv", "dr", "ws"):
+        assert _bwd(**{name: None}) == INVALID, name
+    assert _bwd(nws=1024) == INVALID                  # workspace too small
+    assert _bwd(ws=FAKE * 14 + 16) == INVALID         # workspace not 256-byte aligned
+    assert _bwd(q=FAKE + 1) == INVALID                # misaligned bf16 operand
+    assert _bwd(du=FAKE * 12 + 2) == INVALID          # misaligned fp32 output
+    assert _bwd(dq=FAKE) == INVALID                   # dq overlaps q
+    assert _bwd(dv=FAKE * 9 + 64) == INVALID          # dv overlaps dk
+    assert _bwd(dr=FAKE * 14 + 4096) == INVALID       # dr inside the workspace
+
+
+def test_bwd_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the call would launch on the fake pointers")
+    assert _bwd() == CUDA
+    assert _bwd(u=None, w=None, du=None, dw=None) == CUDA

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libtxl.so")
-SOURCES = ["api.cu", "attn_f32.cu", "attn_bf16.cu", "rollover.cu", "noalloc.cu", "project.cu", "pack.cu"]
+SOURCES = ["api.cu", "attn_f32.cu", "attn_bf16.cu", "rollover.cu", "noalloc.cu", "project.cu", "pack.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table")
+           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace")
 
 
 class TxlError(RuntimeError):
@@ -63,6 +63,11 @@ def load_library() -> ctypes.CDLL:
     lib.txl_project_heads.restype = i
     lib.txl_rel_table.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     lib.txl_rel_table.restype = i
+    lib.txl_rel_attn_bwd_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.txl_rel_attn_bwd_workspace.restype = i
+    lib.txl_rel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                     vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.txl_rel_attn_bwd.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_mem_update.restype = i
     lib.txl_check.argtypes = [vp]
@@ -150,6 +155,53 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd")
     return out
+
+
+def rel_attn_bwd_workspace_bytes(batch: int, mem_len: int, seg_len: int, heads: int, d_head: int,
+                                 dtype_code: int) -> int:
+    """Workspace bytes txl_rel_attn_bwd needs for this shape."""
+    n = ctypes.c_size_t(0)
+    st = load_library().txl_rel_attn_bwd_workspace(batch, mem_len, seg_len, heads, d_head, dtype_code,
+                                                   ctypes.byref(n))
+    _raise(st, "txl_rel_attn_bwd_workspace")
+    return int(n.value)
+
+
+def rel_attn_bwd(q, k, v, r, u_bias, v_bias, dout, mem_len: int, workspace=None, grads=None,
+                 bias_grads: bool = True, stream=None):
+    """Gradients of ``rel_attn_fwd`` for the output gradient ``dout`` (shaped
+    like q).  Returns a dict ``dq, dk, dv, dr`` (shaped and typed like q, k,
+    v, r) and ``du, dw`` (float32 [H, D]; None when ``bias_grads`` is False).
+    ``workspace``: a CUDA uint8 tensor of at least
+    ``rel_attn_bwd_workspace_bytes`` bytes (allocated when None); ``grads``:
+    preallocated outputs with the same keys."""
+    import torch
+    L, B, H, D = q.shape
+    _check_attn(q, k, v, r, u_bias, v_bias, mem_len, q)
+    if tuple(dout.shape) != (L, B, H, D) or dout.dtype != q.dtype or not dout.is_cuda \
+            or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous CUDA tensor shaped and typed like q")
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dr=torch.empty_like(r))
+        if bias_grads:
+            grads["du"] = torch.empty((H, D), dtype=torch.float32, device=q.device)
+            grads["dw"] = torch.empty((H, D), dtype=torch.float32, device=q.device)
+    grads.setdefault("du", None)
+    grads.setdefault("dw", None)
+    nbytes = rel_attn_bwd_workspace_bytes(B, mem_len, L, H, D, _dtype_code(q))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace must hold {nbytes} bytes")
+    st = load_library().txl_rel_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias), _ptr(dout),
+        B, mem_len, L, H, D, _dtype_code(q),
+        _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dr"]),
+        _ptr(grads["du"]), _ptr(grads["dw"]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_bwd")
+    return grads
 
 
 def rel_attn_fwd_ring(q, k, v, r, u_bias, v_bias, mem_len: int, kv_start: int, out=None, stream=None):

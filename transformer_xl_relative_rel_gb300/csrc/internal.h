@@ -48,6 +48,9 @@ cudaError_t zero_bias(size_t count, const float **out);
 
 // releases the per-device cuBLAS handles of project.cu
 cudaError_t blas_shutdown();
+// the current device's cuBLAS handle (a cublasHandle_t) bound to stream s,
+// created on first use; NULL when cuBLAS cannot be initialised
+void *blas_on_stream(cudaStream_t s);
 
 // records `e` as the thread's last CUDA error (reported by txl_last_cuda_error)
 // and clears the runtime's error state; returns e

@@ -132,6 +132,13 @@ bool overlap_bytes(const void *a, size_t na, const void *b, size_t nb)
 
 }  // namespace
 
+void *blas_on_stream(cudaStream_t s)
+{
+    cublasHandle_t h = nullptr;
+    if (blas_handle(&h) != CUBLAS_STATUS_SUCCESS || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return nullptr;
+    return (void *)h;
+}
+
 cudaError_t blas_shutdown()
 {
     std::lock_guard<std::mutex> lock(g_blas_mu);
