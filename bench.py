@@ -492,6 +492,62 @@ def recompute_vs_reuse(args, local: int):
     return 0
 
 
+def backward(args, local: int):
+    """Time txl_rel_attn_bwd (the gradients of one layer call) at the
+    workload's per-call shape: unit-variance bf16 inputs and output gradient,
+    workspace and outputs allocated once, CUDA events over the timed calls
+    (per-call working set > L2).  Algorithmic work of the backward: 16*D
+    FLOPs per visible (query, key) pair -- the content and position scores
+    recomputed (2D + 2D), dP, dV, dK (2D each), dQ through the keys and
+    through the table (2D each), the table gradient (2D)."""
+    import transformer_xl_relative_rel_gb300 as txl
+    w = WORKLOADS[args.workload]
+    s = w.shape
+    B, H, D, L, M = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len
+    T = L + M
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    dev = torch.device("cuda", local)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+    q, k, v, r, dout = rnd(L, B, H, D), rnd(T, B, H, D), rnd(T, B, H, D), rnd(T, H, D), rnd(L, B, H, D)
+    u = torch.randn(H, D, generator=gen, device=dev)
+    wb = torch.randn(H, D, generator=gen, device=dev)
+    nbytes = txl.rel_attn_bwd_workspace_bytes(B, M, L, H, D, txl.TXL_BF16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    grads = txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws)
+    call = lambda: txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws, grads=grads)
+    for _ in range(args.warmup):
+        call()
+    txl.check()
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    txl.check()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    pairs = L * M + L * (L + 1) / 2
+    flops = 16.0 * D * B * H * pairs
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    print(json.dumps({
+        "metric": "rel-attn backward query-tokens/s and TFLOP/s (16*D flops per visible pair), 1 GB300",
+        "value": B * L / t, "unit": "query-tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_call": t * 1e3, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": w.name, "batch": B, "heads": H, "d_head": D,
+                                       "seg_len": L, "mem_len": M,
+                                       "l2": f"workspace {nbytes / 1e9:.2f} GB > 129 MB L2 (no flush)"},
+        "tflops": flops / t / 1e12, "frac_bf16_peak": flops / t / 1e12 / peak, "peak": peak,
+        "peak_source": src, "launches_per_call": 15,
+        "design": "materialised scores: cuBLAS batched GEMMs + row kernels (see profiles/)",
+        "clocks": clk}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,6 +564,8 @@ def main(argv=None):
     ap.add_argument("--batch-t9", type=int, default=22, help="batch for --recompute-vs-reuse")
     ap.add_argument("--pad", type=int, default=0,
                     help="store head vectors padded to this many elements (txl_rel_attn_fwd_padded)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time txl_rel_attn_bwd (gradients of one layer call) at the workload's shape")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
     args = ap.parse_args(argv)
@@ -530,6 +588,8 @@ def main(argv=None):
 
     if args.recompute_vs_reuse:
         return recompute_vs_reuse(args, local)
+    if args.backward:
+        return backward(args, local)
 
     w = WORKLOADS[args.workload]
     if args.layers or args.segments:

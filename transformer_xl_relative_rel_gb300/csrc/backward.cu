@@ -84,6 +84,45 @@ __global__ void bwd_table_rep_kernel(const T *__restrict__ r, T *__restrict__ rr
     }
 }
 
+// The same two copies in 16-byte chunks (8 bf16 or 4 fp32 elements) when D
+// is a multiple of the chunk: one index decomposition per chunk.
+template <typename T>
+__global__ void bwd_fold_vec_kernel(const T *__restrict__ q, const float *__restrict__ u,
+                                    const float *__restrict__ w, T *__restrict__ qu, T *__restrict__ qv, long nch,
+                                    int H, int D)
+{
+    constexpr int C = 16 / sizeof(T);
+    const int dc = D / C;
+    for (long x = (long)blockIdx.x * blockDim.x + threadIdx.x; x < nch; x += (long)gridDim.x * blockDim.x) {
+        const int d0 = (int)(x % dc) * C, h = (int)((x / dc) % H);
+        const uint4 raw = reinterpret_cast<const uint4 *>(q)[x];
+        const T *e = reinterpret_cast<const T *>(&raw);
+        uint4 a, b;
+        T *ea = reinterpret_cast<T *>(&a), *eb = reinterpret_cast<T *>(&b);
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const float qq = to_f(e[c]);
+            ea[c] = from_f<T>(qq + u[h * D + d0 + c]);
+            eb[c] = from_f<T>(qq + w[h * D + d0 + c]);
+        }
+        reinterpret_cast<uint4 *>(qu)[x] = a;
+        reinterpret_cast<uint4 *>(qv)[x] = b;
+    }
+}
+
+template <typename T>
+__global__ void bwd_table_rep_vec_kernel(const T *__restrict__ r, T *__restrict__ rrep, long nch, int H, int D,
+                                         int Tn)
+{
+    const int dc = D / (16 / (int)sizeof(T));
+    for (long x = (long)blockIdx.x * blockDim.x + threadIdx.x; x < nch; x += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(x % dc);
+        const long tr = x / dc;                        // (b*H + h)*T + t
+        const int t = (int)(tr % Tn), h = (int)((tr / Tn) % H);
+        reinterpret_cast<uint4 *>(rrep)[x] = reinterpret_cast<const uint4 *>(r)[((long)t * H + h) * dc + c];
+    }
+}
+
 // One warp per query row (b, h, i) (row = (b*H + h)*L + i): the score from
 // the content product s (in place) and the table product bt read at column
 // L-1-i+j, the masked softmax over keys 0..M+i, P written back to s (fp32,
@@ -141,6 +180,98 @@ __global__ void bwd_score_grad_kernel(const float *__restrict__ p, const float *
         dar[j] = from_f<T>(j <= last ? pr[j] * (gr[j] - delta) * scale : 0.f);
         const int jj = j - sh;   // the key whose pair has table column j
         dbr[j] = from_f<T>(jj >= 0 && jj <= last ? pr[jj] * (gr[jj] - delta) * scale : 0.f);
+    }
+}
+
+// The same two steps with one 256-thread block per row and the row held in
+// registers (NPT entries per thread, rows of up to 256*NPT keys): each input
+// is read once and each output written once.
+constexpr int RB = 256;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red)
+{
+    v = is_max ? warp_max(v) : warp_sum(v);
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();                       // red is reused across calls
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float x = lane < (RB >> 5) ? red[lane] : (is_max ? -INFINITY : 0.f);
+    return is_max ? warp_max(x) : warp_sum(x);
+}
+
+template <typename T, int NPT>
+__global__ void __launch_bounds__(RB) bwd_softmax_row_kernel(float *__restrict__ s, const float *__restrict__ bt,
+                                                             T *__restrict__ pb, int L, int M, int Tn, float scale)
+{
+    __shared__ float red[RB / 32];
+    const long row = blockIdx.x;
+    const int i = (int)(row % L), last = M + i, sh = L - 1 - i;
+    float *sr = s + row * Tn;
+    const float *br = bt + row * Tn;
+    float x[NPT];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        const int j = threadIdx.x + RB * m;
+        x[m] = j <= last ? (sr[j] + br[sh + j]) * scale : -INFINITY;
+        mx = fmaxf(mx, x[m]);
+    }
+    mx = block_reduce(mx, true, red);
+    float z = 0.f;
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        x[m] = expf(x[m] - mx);            // 0 for masked keys
+        z += x[m];
+    }
+    const float inv = 1.f / block_reduce(z, false, red);
+    T *pr = pb + row * Tn;
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        const int j = threadIdx.x + RB * m;
+        if (j < Tn) {
+            sr[j] = x[m] * inv;
+            pr[j] = from_f<T>(x[m] * inv);
+        }
+    }
+}
+
+template <typename T, int NPT>
+__global__ void __launch_bounds__(RB) bwd_score_grad_row_kernel(const float *__restrict__ p,
+                                                                const float *__restrict__ dp, T *__restrict__ da,
+                                                                T *__restrict__ db, int L, int M, int Tn,
+                                                                float scale)
+{
+    __shared__ float red[RB / 32];
+    __shared__ float row_da[RB * NPT];
+    const long row = blockIdx.x;
+    const int i = (int)(row % L), last = M + i, sh = L - 1 - i;
+    const float *pr = p + row * Tn, *gr = dp + row * Tn;
+    float pv[NPT], gv[NPT];
+    float delta = 0.f;
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        const int j = threadIdx.x + RB * m;
+        pv[m] = j <= last ? pr[j] : 0.f;
+        gv[m] = j <= last ? gr[j] : 0.f;
+        delta += pv[m] * gv[m];
+    }
+    delta = block_reduce(delta, false, red);
+    T *dar = da + row * Tn, *dbr = db + row * Tn;
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        const int j = threadIdx.x + RB * m;
+        const float a = pv[m] * (gv[m] - delta) * scale;   // 0 past the last key
+        if (j < Tn) {
+            row_da[j] = a;
+            dar[j] = from_f<T>(a);
+        }
+    }
+    __syncthreads();
+    // table frame: column c holds the pair of key c - (L-1-i)
+#pragma unroll
+    for (int m = 0; m < NPT; ++m) {
+        const int c = threadIdx.x + RB * m, jj = c - sh;
+        if (c < Tn) dbr[c] = from_f<T>(jj >= 0 ? row_da[jj] : 0.f);
     }
 }
 
@@ -260,10 +391,20 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
         e = cudaGetLastError();
         return e == cudaSuccess;
     };
-    bwd_fold_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq, H, D);
-    if (!chk()) goto cuda_fail;
-    bwd_table_rep_kernel<E><<<grid_for(BH * T * D, 256), 256, 0, s>>>((const E *)r, rrep, BH * T * D, H, D, (int)T);
-    if (!chk()) goto cuda_fail;
+    if (D % (16 / (int)sizeof(E)) == 0 && ((uintptr_t)q & 15) == 0 && ((uintptr_t)r & 15) == 0) {
+        const int C = 16 / (int)sizeof(E);
+        bwd_fold_vec_kernel<E><<<grid_for(nq / C, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / C, H, D);
+        if (!chk()) goto cuda_fail;
+        bwd_table_rep_vec_kernel<E><<<grid_for(BH * T * D / C, 256), 256, 0, s>>>((const E *)r, rrep,
+                                                                                BH * T * D / C, H, D, (int)T);
+        if (!chk()) goto cuda_fail;
+    } else {
+        bwd_fold_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq, H, D);
+        if (!chk()) goto cuda_fail;
+        bwd_table_rep_kernel<E><<<grid_for(BH * T * D, 256), 256, 0, s>>>((const E *)r, rrep, BH * T * D, H, D,
+                                                                         (int)T);
+        if (!chk()) goto cuda_fail;
+    }
     {
         const long long LT = (long long)L * T, TD = (long long)T * D;
         const int Ti = (int)T, nb = (int)BH;
@@ -271,13 +412,23 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
         if (gemm_rm(hd, false, true, L, Ti, D, qu, ld, D, k, ld, D, x1, T, LT, nb, ty, CUDA_R_32F) ||
             gemm_rm(hd, false, true, L, Ti, D, qv, ld, D, rrep, D, TD, x2, T, LT, nb, ty, CUDA_R_32F))
             return TXL_ERR_CUDA;
-        bwd_softmax_kernel<E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x1, x2, pb, rows, L, M, Ti, scale);
+        if (T <= RB * 6)
+            bwd_softmax_row_kernel<E, 6><<<(unsigned)rows, RB, 0, s>>>(x1, x2, pb, L, M, Ti, scale);
+        else if (T <= RB * 16)
+            bwd_softmax_row_kernel<E, 16><<<(unsigned)rows, RB, 0, s>>>(x1, x2, pb, L, M, Ti, scale);
+        else
+            bwd_softmax_kernel<E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x1, x2, pb, rows, L, M, Ti, scale);
         if (!chk()) goto cuda_fail;
         // dP, then the score gradient in both frames
         if (gemm_rm(hd, false, true, L, Ti, D, dout, ld, D, v, ld, D, x2, T, LT, nb, ty, CUDA_R_32F))
             return TXL_ERR_CUDA;
-        bwd_score_grad_kernel<E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x1, x2, dab, dbb, rows, L, M, Ti,
-                                                                            scale);
+        if (T <= RB * 6)
+            bwd_score_grad_row_kernel<E, 6><<<(unsigned)rows, RB, 0, s>>>(x1, x2, dab, dbb, L, M, Ti, scale);
+        else if (T <= RB * 16)
+            bwd_score_grad_row_kernel<E, 16><<<(unsigned)rows, RB, 0, s>>>(x1, x2, dab, dbb, L, M, Ti, scale);
+        else
+            bwd_score_grad_kernel<E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x1, x2, dab, dbb, rows, L, M,
+                                                                                Ti, scale);
         if (!chk()) goto cuda_fail;
         // dV = P^T dO, dK = dA^T qu, dQ = dA K + dB~ r, dr per (b, h) = dB~^T qv
         if (gemm_rm(hd, true, false, Ti, D, L, pb, T, LT, dout, ld, D, dv, ld, D, nb, ty, ty) ||
@@ -292,7 +443,12 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
     if (du || dw) {
         if (du && (e = cudaMemsetAsync(du, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
         if (dw && (e = cudaMemsetAsync(dw, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
-        bwd_bias_grad_kernel<<<dim3(64, (unsigned)H), 128, 0, s>>>(dqc, dqp, du, dw, (long)L * B, H, D);
+        // about 16 rows per block: enough blocks in flight to stream the two
+        // fp32 halves of dq at bandwidth
+        const long brows = (long)L * B;
+        const unsigned chunks = (unsigned)(brows / 16 < 1 ? 1 : (brows / 16 > 4096 ? 4096 : brows / 16));
+        bwd_bias_grad_kernel<<<dim3(chunks, (unsigned)H), D <= 64 ? 64 : 128, 0, s>>>(dqc, dqp, du, dw, brows, H,
+                                                                                     D);
         if (!chk()) goto cuda_fail;
     }
     bwd_table_grad_kernel<E><<<grid_for(T * H * D, 256), 256, 0, s>>>(drp, (E *)dr, B, H, D, (int)T);
