@@ -34,10 +34,11 @@ class Workload:
 
     def issued_flops_per_call(self, splits: int = 1) -> float:
         """FLOPs the bf16 kernel issues to the tensor cores for one call: per
-        128-key tile of a 128-row query tile, the content tile, one 128-row
-        band chunk and the P.V tile (each 2*128*128*DP, DP = D padded to 16),
-        plus band chunk 0 once per work item.  Tiles past a query tile's
-        causal limit are not issued."""
+        128-key tile of a 128-row query tile, the content tile (2*128*128*DP,
+        DP = D padded to 16), the tile's whole 256-column band window
+        (2*128*256*DP: rows need columns 127-i .. 254-i) and the P.V tile
+        (2*128*128*DP).  Tiles past a query tile's causal limit are not
+        issued; key splits only partition the tiles."""
         s = self.shape
         dp = (s.d_head + 15) // 16 * 16
         per = 2.0 * 128 * 128 * dp
@@ -46,7 +47,7 @@ class Workload:
         for qt in range(nqt):
             kend = min(s.klen, s.mem_len + min(s.seg_len, (qt + 1) * 128))
             ntile = (kend + 127) // 128
-            total += 3 * per * ntile + per * min(splits, ntile)
+            total += 4 * per * ntile
         return total * s.batch * s.heads
 
     def bytes_per_call(self) -> float:
