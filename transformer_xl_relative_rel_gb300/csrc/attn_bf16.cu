@@ -41,6 +41,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+#include <vector>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -989,7 +993,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
 // rows `row_stride` elements apart and groups (b*H+h or h) 64 elements apart;
 // the box {64, box_rows, 1} lands in shared memory as 128-byte rows with the
 // 128-byte swizzle (the layout the MMA descriptors expect).
-bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long groups, int box_rows)
+bool encode_map(CUtensorMap *m, const void *base, long rows, long row_stride, long groups, int box_rows)
 {
     auto enc = get_encode();
     if (!enc) return false;
@@ -1003,6 +1007,48 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
     return r == CUDA_SUCCESS;
 }
 
+// Encoded maps of recent calls (a map holds only the address and the shape,
+// so repeated calls on the same buffers reuse it: the encode is a driver call
+// that costs about as much as a short launch).
+struct MapEntry {
+    int dev;
+    const void *base;
+    long rows, row_stride, groups;
+    int box_rows;
+    CUtensorMap map;
+};
+constexpr int MAP_CACHE = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[MAP_CACHE];
+int g_map_count = 0, g_map_next = 0;
+
+bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long groups, int box_rows)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int x = 0; x < g_map_count; ++x) {
+        const MapEntry &e = g_maps[x];
+        if (e.dev == dev && e.base == base && e.rows == rows && e.row_stride == row_stride &&
+            e.groups == groups && e.box_rows == box_rows) {
+            *m = e.map;
+            return true;
+        }
+    }
+    if (!encode_map(m, base, rows, row_stride, groups, box_rows)) return false;
+    MapEntry &e = g_maps[g_map_next];
+    e.dev = dev;
+    e.base = base;
+    e.rows = rows;
+    e.row_stride = row_stride;
+    e.groups = groups;
+    e.box_rows = box_rows;
+    e.map = *m;
+    g_map_next = (g_map_next + 1) % MAP_CACHE;
+    if (g_map_count < MAP_CACHE) ++g_map_count;
+    return true;
+}
+
 template <int DP, bool kTma>
 cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                      const CUtensorMap &mr, const CUtensorMap &mq, const CUtensorMap &mk8,
@@ -1010,8 +1056,17 @@ cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &
 {
     const uint32_t smem = Smem<DP>::TOTAL;
     auto kern = rel_attn_bf16_kernel<DP, kTma>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the shared-memory opt-in, once per device for this variant
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(opted.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_relaxed);
+    }
     // persistent: one CTA per SM, each walks its share of the work items
     const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
     kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, mk8, mv8, mo, p);
@@ -1022,31 +1077,69 @@ int dpad(int D) { return (D + 15) / 16 * 16; }
 
 }  // namespace
 
+namespace {
+// The kernel's busiest CTA for a split count: the items of the static
+// schedule (heaviest query tiles first, CTA c of G taking items c, 2G-1-c,
+// 2G+c, ...) laid out exactly as the kernel does, in units of one key tile
+// (~1.6 us of one SM), with one tile of fill per item (its first tile's max
+// pass, the q conversion and the epilogue).
+double busiest_cta(const AttnArgs &a, int num_sms, int s)
+{
+    const int nqt = (a.L + BM - 1) / BM;
+    const long bh = (long)a.B * a.H;
+    const long items = bh * nqt * s;
+    const long G = items < num_sms ? items : num_sms;
+    std::vector<double> load((size_t)G, 0.0);
+    const long per_qt = bh * s;
+    for (long k = 0; k < items; ++k) {
+        const int qt = nqt - 1 - (int)(k / per_qt);
+        const int split = (int)((k % per_qt) % s);
+        const int i0 = qt * BM, rows = a.L - i0 < BM ? a.L - i0 : BM;
+        const long kend = (long)a.M + a.L < (long)a.M + i0 + rows ? (long)a.M + a.L : (long)a.M + i0 + rows;
+        const int ntile = (int)((kend + BN - 1) / BN);
+        const int n = (split + 1) * ntile / s - split * ntile / s;
+        if (n <= 0) continue;
+        const long j = k / G, c = (j & 1) ? G - 1 - k % G : k % G;
+        load[(size_t)c] += n + 1.0;
+    }
+    double mx = 0.0;
+    for (double x : load) mx = x > mx ? x : mx;
+    return mx;
+}
+
+struct SplitKey {
+    int B, H, L, M, D, sms, s;
+};
+std::mutex g_split_mu;
+SplitKey g_split_cache[64];
+int g_split_count = 0, g_split_next = 0;
+}  // namespace
+
 int bf16_num_splits(const AttnArgs &a, int num_sms)
 {
-    // cost model in units of one key tile (~1.2 us of one SM): the CTAs share
-    // the items' tiles (plus about half a tile of fill per item), the last
-    // item adds about half its length, and splitting pays for the fp32
+    {
+        std::lock_guard<std::mutex> lock(g_split_mu);
+        for (int x = 0; x < g_split_count; ++x) {
+            const SplitKey &k = g_split_cache[x];
+            if (k.B == a.B && k.H == a.H && k.L == a.L && k.M == a.M && k.D == a.D && k.sms == num_sms) return k.s;
+        }
+    }
+    // the busiest CTA (simulated schedule) plus, when split, the fp32
     // partials (written and read once, ~6 TB/s) and the combine launch
     const int nqt = (a.L + BM - 1) / BM;
     const long bh = (long)a.B * a.H;
-    const long T = (long)a.M + a.L;
-    long tiles = 0;
     int maxn = 1;
     for (int qt = 0; qt < nqt; ++qt) {
-        const long kend = T < a.M + (long)(qt + 1) * BM ? T : a.M + (long)(qt + 1) * BM;
+        const int i0 = qt * BM, rows = a.L - i0 < BM ? a.L - i0 : BM;
+        const long kend = (long)a.M + i0 + rows;
         const int nt = (int)((kend + BN - 1) / BN);
-        tiles += nt;
         maxn = nt > maxn ? nt : maxn;
     }
-    tiles *= bh;
-    const double tile_us = 1.2;
+    const double tile_us = 1.6;
     double best = 1e30;
     int best_s = 1;
     for (int s = 1; s <= 16 && s <= maxn; ++s) {
-        const long items = bh * nqt * s;
-        const long G = items < num_sms ? items : num_sms;
-        double cost = ((double)tiles + 0.5 * (double)items) / (double)G + 0.5 * (double)((maxn + s - 1) / s);
+        double cost = busiest_cta(a, num_sms, s);
         if (s > 1) {
             const double bytes = 2.0 * s * (double)bh * a.L * (dpad(a.D) + 1) * 4.0;
             cost += (bytes / 6.0e6 + 3.0) / tile_us;
@@ -1056,6 +1149,10 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
             best_s = s;
         }
     }
+    std::lock_guard<std::mutex> lock(g_split_mu);
+    g_split_cache[g_split_next] = SplitKey{a.B, a.H, a.L, a.M, a.D, num_sms, best_s};
+    g_split_next = (g_split_next + 1) % 64;
+    if (g_split_count < 64) ++g_split_count;
     return best_s;
 }
 
