@@ -152,3 +152,26 @@ def test_absent_biases_are_the_shaw_form(dtype, tol, D):
     got_u = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], None, dev["w"], mem_len=M).clone()
     same_u = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], zero, dev["w"], mem_len=M)
     assert torch.equal(got_u, same_u)
+
+
+# ------------------------------------------------ seeded random shape sweep
+def _random_shapes(seed, n, dmax):
+    g = np.random.Generator(np.random.PCG64(seed))
+    ds = [d for d in (1, 5, 8, 16, 24, 32, 40, 41, 48, 56, 64, 96, 128) if d <= dmax]
+    out = []
+    for _ in range(n):
+        out.append((int(g.integers(1, 4)), int(g.integers(1, 4)), int(g.choice(ds)),
+                    int(g.integers(1, 301)), int(g.choice([0, int(g.integers(1, 450))]))))
+    return out
+
+
+@pytest.mark.parametrize("B,H,D,L,M", _random_shapes(31, 16, 64))
+def test_bf16_random_shapes(B, H, D, L, M):
+    """Shapes drawn from one seed (any head size up to 64, ragged lengths,
+    with and without memory), element by element against the oracle."""
+    _check_full(B, H, D, L, M, torch.bfloat16, seed=3000 + B * 131 + H * 17 + D * 7 + L + M, tol=TOL_BF16)
+
+
+@pytest.mark.parametrize("B,H,D,L,M", _random_shapes(37, 6, 128))
+def test_f32_random_shapes(B, H, D, L, M):
+    _check_full(B, H, D, L, M, torch.float32, seed=4000 + B * 131 + H * 17 + D * 7 + L + M, tol=TOL_F32)

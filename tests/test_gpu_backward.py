@@ -112,3 +112,19 @@ def test_bwd_char_train_shape_one_head_slice():
         assert _rel_err(pick[n], ref[n]) <= TOL[torch.bfloat16], n
     colsum = got["dv"].sum(axis=0)
     assert _rel_err(colsum, dout_h.sum(axis=0)) <= TOL[torch.bfloat16]
+
+
+def _random_shapes(seed, n):
+    g = np.random.Generator(np.random.PCG64(seed))
+    return [(int(g.integers(1, 3)), int(g.integers(1, 3)), int(g.choice([8, 16, 41, 64])),
+             int(g.integers(1, 160)), int(g.choice([0, int(g.integers(1, 220))])),
+             [torch.float32, torch.bfloat16][int(g.integers(0, 2))]) for _ in range(n)]
+
+
+@pytest.mark.parametrize("B,H,D,L,M,dtype", _random_shapes(41, 6))
+def test_bwd_random_shapes(B, H, D, L, M, dtype):
+    got, host, dout = _run(B, H, D, L, M, dtype, seed=5000 + B * 13 + H * 7 + D + L + M)
+    ref = oracle.rel_attn_bwd(**host, dout=dout, mem_len=M)
+    for n in NAMES:
+        assert np.isfinite(got[n]).all(), n
+        assert _rel_err(got[n], ref[n]) <= TOL[dtype], n
