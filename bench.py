@@ -564,6 +564,8 @@ def main(argv=None):
     ap.add_argument("--batch-t9", type=int, default=22, help="batch for --recompute-vs-reuse")
     ap.add_argument("--pad", type=int, default=0,
                     help="store head vectors padded to this many elements (txl_rel_attn_fwd_padded)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the eager step only (no CUDA-graph replay of the step)")
     ap.add_argument("--backward", action="store_true",
                     help="time txl_rel_attn_bwd (gradients of one layer call) at the workload's shape")
     ap.add_argument("--ring", action="store_true",
@@ -619,6 +621,45 @@ def main(argv=None):
     clk = clocks.stop()
     txl.check()
     local_s = e0.elapsed_time(e1) / 1e3
+    eager_step_s = max_over_ranks(local_s, world) / args.steps
+    # The same step captured once in a CUDA graph and replayed: the kernels,
+    # their arguments and their order are those of the eager step; the
+    # per-call host work (binding checks, launch calls) leaves the timed
+    # region.  Falls back to the eager timing if the capture fails.
+    timing = {"mode": "eager", "eager_ms_per_step": eager_step_s * 1e3}
+    if not args.no_graph:
+        try:
+            gph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                chain.step(txl)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(gph):
+                chain.step(txl)
+            for _ in range(args.warmup):
+                gph.replay()
+            torch.cuda.synchronize()
+            txl.check()
+            clocks = ClockSampler(local)
+            clocks.start()
+            barrier(world)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(args.steps):
+                gph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            barrier(world)
+            clk = clocks.stop()
+            txl.check()
+            local_s = e0.elapsed_time(e1) / 1e3
+            timing["mode"] = "cuda_graph"
+            del gph
+        except Exception as ex:   # keep the eager numbers
+            torch.cuda.synchronize()
+            timing["graph_error"] = str(ex)[:160]
     tokens_per_step = s.batch * s.seg_len * w.segments
     value = aggregate_rate(tokens_per_step * args.steps, local_s, world)
     step_s = max_over_ranks(local_s, world) / args.steps
@@ -652,7 +693,7 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": config_of(w, world, chain.working_set_bytes, args.ring, args.pad),
             "tflops": tflops_step, "pct_bf16_peak": tflops_step / peaks["bf16_tflops"] * 100.0,
-            "roofline": roof, "clocks": clk, "gpu_launches": launches}
+            "roofline": roof, "clocks": clk, "gpu_launches": launches, "timing": timing}
 
     e2e_steps = args.e2e_steps or max(2, min(args.steps, 5))
     line["e2e"] = measure_e2e(w, chain, txl, e2e_steps, world)
