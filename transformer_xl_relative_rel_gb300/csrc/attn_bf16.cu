@@ -78,6 +78,14 @@ struct Params {
     __nv_bfloat16 *out;
     float *part_o;      // [splits][B*H][L][DP] when splits > 1
     float *part_lse;    // [splits][B*H][L]
+    float *lse;         // optional [B*H][L]: each row's log-sum-exp (log2 units of the scaled score)
+    // backward scores only: dO, delta = rowsum(dO * O), the outputs P, dA and
+    // dA in the table frame ([B*H][L][TP]), 1/sqrt(d_head)
+    const __nv_bfloat16 *dout;
+    const float *delta;
+    __nv_bfloat16 *p_out, *da_out, *db_out;
+    long TP;
+    float inv_sqrt_d;
     int B, H, D, L, M, T;
     int nqt, splits;
     int items;          // B*H*nqt*splits work items
@@ -753,6 +761,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int d0 = DH * half;
             const int i = dn.i0 + ii;
+            if (p.lse && p.splits == 1 && half == 0 && ii < dn.rows_here)
+                p.lse[(long)dn.bh * p.L + i] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
             if (kTma && p.ost) {
                 // the 128 x 64 tile goes through shared memory (the tensor
                 // map's swizzled layout) and out by one TMA store, issued by
@@ -949,11 +959,435 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
 }
 
+// ------------------------------------------------------------ backward scores
+// The score side of the backward (txl_rel_attn_bwd, bf16, D = 64): for each
+// 128-row block of one (b, h) and each 128-key tile, the tile's content and
+// band products (as in the forward) and dP = dO V^T on the tensor cores, then
+// per row P = 2^(s - lse) (the forward's log-sum-exp) and
+// dA = P (dP - delta) / sqrt(D) (delta = rowsum(dO * O)); P and dA are written
+// as bf16 [B*H][L][TP] matrices, and dA once more in the table's column
+// frame (row i moved right by L-1-i: column c holds the pair of key
+// c - (L-1-i)), the operands of the backward's plain contractions.
+constexpr int BW_NSTAGE = 2;      // K/V stages
+constexpr int BW_NCH = 3;         // table chunk slots
+constexpr uint32_t TM_DP = 384;   // dP of the tile, 128 columns
+
+struct BwdSmem {
+    static constexpr uint32_t TILE = BN * 128;
+    static constexpr uint32_t KV = 2 * TILE;
+    static constexpr uint32_t QT = BM * 128;
+    static constexpr uint32_t ST0 = 0;
+    static constexpr uint32_t CH0 = BW_NSTAGE * KV;
+    static constexpr uint32_t QU = CH0 + BW_NCH * TILE;
+    static constexpr uint32_t QV = QU + QT;
+    static constexpr uint32_t DO0 = QV + QT;                // two dO buffers (items alternate)
+    static constexpr uint32_t QRAW = DO0 + 2 * QT;
+    static constexpr uint32_t STG = QRAW + QT;              // per softmax warp: 16 rows of 256 bytes of dA
+    static constexpr uint32_t UW = STG + 8 * 16 * 256;
+    static constexpr uint32_t BARS = UW + 2 * 64 * 4;
+    // q+u/q+v ready; raw q (+ u, v, the item's dO) ready, raw q read; per
+    // K/V stage full / empty; per chunk slot full / empty; S, band, dP
+    // full; S, band, dP free (loaded by the softmax)
+    static constexpr int B_Q = 0, B_QRAW = 1, B_QRF = 2, B_FULL = 3, B_EMPTY = 3 + BW_NSTAGE,
+                         B_CHF = 3 + 2 * BW_NSTAGE, B_CHE = B_CHF + BW_NCH, B_S = B_CHE + BW_NCH,
+                         B_SF = B_S + 1;
+    static_assert(B_SF < 32, "barrier slots");
+    static constexpr uint32_t MISC = BARS + 32 * 8;
+    static constexpr uint32_t USED = MISC + 16;
+    static constexpr uint32_t TOTAL = USED + 1024;
+};
+
+__global__ void __launch_bounds__(NT, 1)
+rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_do, const Params p)
+{
+    using S = BwdSmem;
+    constexpr int DP = 64;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + S::BARS + 8u * (uint32_t)i; };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::MISC + 8);
+    auto wwait = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_or_abort(bar(i), parity, abort)) != 0;
+    };
+
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        *abort = 0;
+        mbar_init(bar(S::B_Q), 256);
+        mbar_init(bar(S::B_QRAW), 1);
+        mbar_init(bar(S::B_QRF), 256);
+        for (int x = 0; x < BW_NSTAGE; ++x) {
+            mbar_init(bar(S::B_FULL + x), 1);
+            mbar_init(bar(S::B_EMPTY + x), 1);
+        }
+        for (int x = 0; x < BW_NCH; ++x) {
+            mbar_init(bar(S::B_CHF + x), 1);
+            mbar_init(bar(S::B_CHE + x), 1);
+        }
+        mbar_init(bar(S::B_S), 1);
+        mbar_init(bar(S::B_SF), 256);
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_r);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_do);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp < 4) {
+        setmaxnreg_dec<REG_LOW>();
+        if (warp == 0) {
+            // =============================================================== producer
+            // an item's raw q rows, its head's biases and its dO rows (into
+            // the dO buffer of its parity)
+            auto load_q = [&](const Item &it, int ni) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_QRAW), 2 * S::QT + 2 * 64 * 4);
+                    tma_load_3d(sbase + S::QRAW, &tm_q, bar(S::B_QRAW), 0, it.i0, it.bh);
+                    tma_load_3d(sbase + S::DO0 + (uint32_t)(ni & 1) * S::QT, &tm_do, bar(S::B_QRAW), 0, it.i0,
+                                it.bh);
+                    bulk_load(sbase + S::UW, p.u + it.h * p.D, 64 * 4, bar(S::B_QRAW));
+                    bulk_load(sbase + S::UW + 256, p.w + it.h * p.D, 64 * 4, bar(S::B_QRAW));
+                }
+            };
+            auto load_chunk = [&](int cg, int row, int h) {
+                const int slot = cg % BW_NCH;
+                if (cg >= BW_NCH && !wwait(S::B_CHE + slot, ((cg / BW_NCH) - 1) & 1)) return false;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_CHF + slot), S::TILE);
+                    tma_load_3d(sbase + S::CH0 + slot * S::TILE, &tm_r, bar(S::B_CHF + slot), 0, row, h);
+                }
+                return true;
+            };
+            Item it;
+            int j = next_busy(p, 0, it);
+            if (j >= 0) load_q(it, 0);
+            int g = 0, cg = 0, ni = 0;
+            bool ok = true;
+            while (ok && j >= 0) {
+                if (!load_chunk(cg, it.kb0, it.h)) break;
+                ++cg;
+                for (int n = 0; n < it.N; ++n, ++g) {
+                    const int st = g % BW_NSTAGE;
+                    if (g >= BW_NSTAGE && !wwait(S::B_EMPTY + st, ((g / BW_NSTAGE) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int j0 = (it.t0 + n) * BN;
+                    const uint32_t dst = sbase + S::ST0 + st * S::KV;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(S::B_FULL + st), S::KV);
+                        tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, j0, it.bh);
+                        tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, j0, it.bh);
+                    }
+                    if (!load_chunk(cg, it.kb0 + (n + 1) * BN, it.h)) {
+                        ok = false;
+                        break;
+                    }
+                    ++cg;
+                }
+                if (!ok) break;
+                Item nx;
+                const int jn = next_busy(p, j + 1, nx);
+                if (jn >= 0) {
+                    if (!wwait(S::B_QRF, ni & 1)) break;
+                    load_q(nx, ni + 1);
+                }
+                j = jn;
+                it = nx;
+                ++ni;
+            }
+        } else if (warp == 1) {
+            // =============================================================== S, band, dP MMAs
+            if (lane == 0) {
+                const uint32_t idesc_n = idesc_bf16(BM, BN, 0, 0);
+                const uint32_t idesc_w = idesc_bf16(BM, 2 * BN, 0, 0);
+                const uint64_t d_qu = smem_desc_sw128(sbase + S::QU, 16, 1024);
+                const uint64_t d_qv = smem_desc_sw128(sbase + S::QV, 16, 1024);
+                const uint64_t d_do0 = smem_desc_sw128(sbase + S::DO0, 16, 1024);
+                const uint64_t d_st0 = smem_desc_sw128(sbase + S::ST0, 16, 1024);
+                const uint64_t d_ch0 = smem_desc_sw128(sbase + S::CH0, 16, 1024);
+                constexpr uint64_t KV16 = S::KV >> 4, TILE16 = S::TILE >> 4, QT16 = S::QT >> 4;
+                Item it;
+                int g = 0, cg = 0, ni = 0;
+                bool ok = true;
+                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it), ++ni) {
+                    if (!wait_or_abort(bar(S::B_Q), ni & 1, abort)) break;
+                    const uint64_t d_do = d_do0 + (uint64_t)(ni & 1) * QT16;
+                    const int c0 = cg;
+                    for (int n = 0; n < it.N; ++n, ++g) {
+                        const int st = g % BW_NSTAGE;
+                        const int ca = c0 + n, cb = ca + 1, sa = ca % BW_NCH, sb = cb % BW_NCH;
+                        if (g >= 1) ok = wait_or_abort(bar(S::B_SF), (g - 1) & 1, abort);
+                        ok = ok && wait_or_abort(bar(S::B_FULL + st), (g / BW_NSTAGE) & 1, abort) &&
+                             wait_or_abort(bar(S::B_CHF + sa), (ca / BW_NCH) & 1, abort) &&
+                             wait_or_abort(bar(S::B_CHF + sb), (cb / BW_NCH) & 1, abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t dk = d_st0 + st * KV16, dv = dk + TILE16;
+                        const uint64_t da = d_ch0 + sa * TILE16, db = d_ch0 + sb * TILE16;
+#pragma unroll
+                        for (int ks = 0; ks < DP / 16; ++ks) {
+                            mma_bf16_ss(tmem + TM_S, d_qu + 2 * ks, dk + 2 * ks, idesc_n, ks > 0);
+                            if (sb == sa + 1) {
+                                mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_w, ks > 0);
+                            } else {
+                                mma_bf16_ss(tmem + TM_BAND, d_qv + 2 * ks, da + 2 * ks, idesc_n, ks > 0);
+                                mma_bf16_ss(tmem + TM_BAND + BN, d_qv + 2 * ks, db + 2 * ks, idesc_n, ks > 0);
+                            }
+                            // dP = dO V^T: V rows are K-major for N = keys, like K
+                            mma_bf16_ss(tmem + TM_DP, d_do + 2 * ks, dv + 2 * ks, idesc_n, ks > 0);
+                        }
+                        mma_commit(bar(S::B_S));
+                        mma_commit(bar(S::B_EMPTY + st));
+                        mma_commit(bar(S::B_CHE + sa));
+                        if (n == it.N - 1) mma_commit(bar(S::B_CHE + sb));
+                    }
+                    cg = c0 + it.N + 1;
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+        setmaxnreg_inc<REG_HIGH>();
+        // =============================================================== scores
+        const int quarter = warp & 3, rh = (warp - 4) >> 2;
+        const int r16 = lane & 15, half = lane >> 4;
+        const int lb = quarter * 32 + rh * 16;
+        const int ii = lb + r16;
+        const uint32_t tl = tmem + ((uint32_t)lb << 16);
+        constexpr int DC = DP / 16;
+        auto convert_q = [&](const Item &it, int ni) {
+            if (!wwait(S::B_QRAW, ni & 1)) return false;
+            const float4 *uw4 = reinterpret_cast<const float4 *>(smem + S::UW);
+            const float keep = ii < it.rows_here ? 1.f : 0.f;
+            uint4 raw[DC];
+            float4 u4[2 * DC], w4[2 * DC];
+#pragma unroll
+            for (int c = 0; c < DC; ++c)
+                raw[c] = *reinterpret_cast<const uint4 *>(smem + S::QRAW + sw128_offset(ii, 8 * (DC * half + c)));
+#pragma unroll
+            for (int d4 = 0; d4 < 2 * DC; ++d4) {
+                u4[d4] = uw4[2 * DC * half + d4];
+                w4[d4] = uw4[16 + 2 * DC * half + d4];
+            }
+            const float sk = p.sl2 * keep;
+#pragma unroll
+            for (int c = 0; c < DC; ++c) {
+                const int d8 = DC * half + c;
+                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&raw[c]);
+                const float *uu = reinterpret_cast<const float *>(&u4[2 * c]);
+                const float *ww = reinterpret_cast<const float *>(&w4[2 * c]);
+                uint32_t a4[4], c4[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const float q0 = __bfloat162float(e[2 * z]), q1 = __bfloat162float(e[2 * z + 1]);
+                    a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
+                    c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
+                }
+                *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
+                    make_uint4(a4[0], a4[1], a4[2], a4[3]);
+                *reinterpret_cast<uint4 *>(smem + S::QV + sw128_offset(ii, 8 * d8)) =
+                    make_uint4(c4[0], c4[1], c4[2], c4[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(S::B_Q));
+            mbar_arrive(bar(S::B_QRF));
+            return true;
+        };
+        const int shift = 15 - r16;
+        const int W0 = 112 - lb;
+        const uint32_t odd_sel = (shift & 1) ? 0x5432u : 0x3210u;
+        auto band_all = [&](uint32_t *w, float *xb) {
+#pragma unroll
+            for (int y = 0; y < 36; ++y) w[y] = (shift & 8) ? w[y + 4] : w[y];
+#pragma unroll
+            for (int y = 0; y < 34; ++y) w[y] = (shift & 4) ? w[y + 2] : w[y];
+#pragma unroll
+            for (int y = 0; y < 33; ++y) w[y] = (shift & 2) ? w[y + 1] : w[y];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) add_f16x2_to(xb[2 * k], xb[2 * k + 1], __byte_perm(w[k], w[k + 1], odd_sel));
+        };
+        // dA of this warp's 16 rows staged for the table-frame copy: row r at
+        // 256 bytes, 16-byte chunk c at position c ^ (r & 7) (conflict-free
+        // both for the rows' chunk writes and the warp's column reads)
+        unsigned char *stg = smem + S::STG + (uint32_t)(warp - 4) * 16 * 256;
+        auto stg_off = [&](int r, int col) {   // byte offset of element col of row r
+            return r * 256 + ((((col >> 3) ^ (r & 7)) & 15) << 4) + ((col & 7) << 1);
+        };
+        const long rowpitch = p.TP;
+        bool ok = true;
+        Item it;
+        int j = next_busy(p, 0, it);
+        if (j >= 0) ok = convert_q(it, 0);
+        int g = 0, ni = 0;
+        while (ok && j >= 0) {
+            const int i = it.i0 + ii;
+            const bool row_valid = ii < it.rows_here;
+            Item nx;
+            const int jn = next_busy(p, j + 1, nx);
+            const long row = (long)it.bh * p.L + i;   // this thread's row of the [B*H][L] matrices
+            const float lse = row_valid ? p.lse[row] : 0.f;
+            const float delta = row_valid ? p.delta[row] : 0.f;
+            // keys past the item's last tile are masked for all its rows: P
+            // and dA there are zeros (the columns up to the row pitch); and
+            // the table frame of the rows before their first key (no key
+            // lands there) is zero.  Each warp clears its 16 rows with
+            // contiguous 16-byte stores.
+            {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                const long c_end = (long)(it.t0 + it.N) * BN;
+                for (int r = 0; r < 16; ++r) {
+                    const int ir = it.i0 + lb + r;
+                    if (ir >= p.L) break;
+                    const long rr = ((long)it.bh * p.L + ir) * rowpitch;
+                    for (long c = c_end + 8 * lane; c < rowpitch; c += 256) {
+                        *reinterpret_cast<uint4 *>(p.p_out + rr + c) = z;
+                        *reinterpret_cast<uint4 *>(p.da_out + rr + c) = z;
+                    }
+                    if (it.t0 == 0) {
+                        const int pre = p.L - 1 - ir;                // table columns before key 0
+                        for (int c = 8 * lane; c < pre; c += 256) {
+                            if (c + 8 <= pre)
+                                *reinterpret_cast<uint4 *>(p.db_out + rr + c) = z;
+                            else
+                                for (int e = c; e < pre; ++e) p.db_out[rr + e] = __float2bfloat16(0.f);
+                        }
+                    }
+                }
+            }
+            for (int n = 0; n < it.N; ++n, ++g) {
+                const int jt = (it.t0 + n) * BN;                 // the tile's first key
+                const int j0 = jt + HN * half;                    // first key of this thread's half
+                if (!wwait(S::B_S, g & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (n == it.N - 1 && jn >= 0 && !convert_q(nx, ni + 1)) {
+                    ok = false;
+                    break;
+                }
+                const bool diag = jt + BN - 1 > p.M + it.i0 + lb;
+                const int lim = row_valid ? (p.M + i - j0) : -1;   // rows past L: nothing visible
+                float x[64];
+                {
+                    float a[80];
+                    const uint32_t ts = tl + TM_S, tb = tl + TM_BAND + (uint32_t)W0;
+                    tmem_ld_h_tile<HN>(ts, ts + 32, tb, tb + 32, tb + 64, x, a);
+                    uint32_t hb[40];
+#pragma unroll
+                    for (int y = 0; y < 40; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
+                    band_all(hb, x);
+                }
+                if (diag) {
+#pragma unroll
+                    for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
+                }
+                // P from the forward's log-sum-exp (0 where masked)
+#pragma unroll
+                for (int y = 0; y < 64; ++y) x[y] = ex2(x[y] - lse);
+                float dp[64];
+                tmem_ld_h64<HN>(tl + TM_DP, tl + TM_DP + 32, dp);
+                tc_fence_before();
+                mbar_arrive(bar(S::B_SF));
+                uint32_t pp[32], aa[32];   // this row's P and dA, bf16 pairs
+#pragma unroll
+                for (int y = 0; y < 32; ++y) {
+                    const float a0 = x[2 * y] * (dp[2 * y] - delta) * p.inv_sqrt_d;
+                    const float a1 = x[2 * y + 1] * (dp[2 * y + 1] - delta) * p.inv_sqrt_d;
+                    pp[y] = pack_bf16(x[2 * y], x[2 * y + 1]);
+                    aa[y] = pack_bf16(a0, a1);
+                }
+                // P and dA go out through the warp's staging tile: a thread
+                // stages its row's 64 values, then two rows per store
+                // instruction leave as contiguous 256-byte runs
+                auto stage = [&](const uint32_t *v) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(stg + stg_off(r16, 64 * half + 8 * c)) =
+                            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                    __syncwarp();
+                };
+                auto write_rows = [&](__nv_bfloat16 *dstm) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = 2 * k + (lane >> 4), ch = lane & 15;
+                        const int ir = it.i0 + lb + r;
+                        if (ir < p.L)
+                            *reinterpret_cast<uint4 *>(dstm + ((long)it.bh * p.L + ir) * rowpitch + jt + 8 * ch) =
+                                *reinterpret_cast<const uint4 *>(stg + stg_off(r, 8 * ch));
+                    }
+                    __syncwarp();
+                };
+                auto elem = [&](int r, int col) {
+                    return *reinterpret_cast<const unsigned short *>(stg + stg_off(r, col));
+                };
+                stage(pp);
+                write_rows(p.p_out);
+                stage(aa);
+                write_rows(p.da_out);
+                // dA in the table frame from the same staged rows: row i's 128
+                // values start at column L-1-i+jt; written as 4-byte pairs
+                // (shifted by one element when that column is odd)
+                for (int r = 0; r < 16; ++r) {
+                    const int ir = it.i0 + lb + r;
+                    if (ir >= p.L) break;
+                    const long c0 = (long)(p.L - 1 - ir) + jt;
+                    __nv_bfloat16 *dst = p.db_out + ((long)it.bh * p.L + ir) * rowpitch + c0;
+                    const long room = rowpitch - c0;              // columns left in the row
+                    const int odd = (int)(c0 & 1);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int l = lane + 32 * k;              // pair l: elements 2l-odd, 2l+1-odd
+                        const int e0 = 2 * l - odd;
+                        if (e0 >= 0 && e0 + 1 < room) {
+                            const uint32_t lo = elem(r, e0), hi = elem(r, e0 + 1);
+                            *reinterpret_cast<uint32_t *>(dst + e0) = lo | (hi << 16);
+                        }
+                    }
+                    if (odd && lane == 0 && room > 0) {
+                        // the first element and the last one
+                        reinterpret_cast<unsigned short *>(dst)[0] = elem(r, 0);
+                        if (127 < room) reinterpret_cast<unsigned short *>(dst)[127] = elem(r, 127);
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            j = jn;
+            it = nx;
+            ++ni;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
 // Merge the key-split partials of one (b, h, i) row: weights 2^(lse_s - max).
 __global__ void __launch_bounds__(64)
 rel_attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
-                        __nv_bfloat16 *__restrict__ out, int splits, int B, int H, int L, int D,
-                        int DP)
+                        __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, int splits, int B, int H,
+                        int L, int D, int DP)
 {
     const int row = blockIdx.x;           // over B*H*L
     const int bh = row / L, i = row % L;
@@ -961,6 +1395,14 @@ rel_attn_combine_kernel(const float *__restrict__ part_o, const float *__restric
     const long BHL = (long)B * H * L;
     float mx = -INFINITY;
     for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[s * BHL + (long)bh * L + i]);
+    if (lse_out && threadIdx.x == 0) {
+        float w = 0.f;
+        for (int s = 0; s < splits; ++s) {
+            const float lse = part_lse[s * BHL + (long)bh * L + i];
+            w += (lse == -INFINITY) ? 0.f : exp2f(lse - mx);
+        }
+        lse_out[(long)bh * L + i] = w > 0.f ? mx + log2f(w) : -INFINITY;
+    }
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float acc = 0.f, wsum = 0.f;
         for (int s = 0; s < splits; ++s) {
@@ -1185,6 +1627,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.sl2 = LOG2E / sqrtf((float)(a.scale_d ? a.scale_d : a.D));
     p.part_o = nullptr;
     p.part_lse = nullptr;
+    p.lse = a.lse;
     if (splits > 1) {
         const size_t rows = (size_t)splits * a.B * a.H * a.L;
         p.part_o = (float *)scratch;
@@ -1229,7 +1672,59 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     if (e != cudaSuccess || splits == 1) return e;
     rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
-        p.part_o, p.part_lse, p.out, splits, a.B, a.H, a.L, a.D, DP);
+        p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, const float *delta,
+                              void *p_out, void *da_out, void *db_out, long TP, cudaStream_t s)
+{
+    if (a.D != 64) return cudaErrorNotSupported;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.q = (const __nv_bfloat16 *)a.q;
+    p.k = (const __nv_bfloat16 *)a.k;
+    p.v = (const __nv_bfloat16 *)a.v;
+    p.r = (const __nv_bfloat16 *)a.r;
+    p.u = a.u;
+    p.w = a.w;
+    p.B = a.B;
+    p.H = a.H;
+    p.D = a.D;
+    p.L = a.L;
+    p.M = a.M;
+    p.T = a.M + a.L;
+    p.nqt = (a.L + BM - 1) / BM;
+    p.splits = 1;
+    p.items = (int)((long)a.B * a.H * p.nqt);
+    p.sl2 = LOG2E / sqrtf((float)a.D);
+    p.lse = const_cast<float *>(lse);
+    p.dout = (const __nv_bfloat16 *)dout;
+    p.delta = delta;
+    p.p_out = (__nv_bfloat16 *)p_out;
+    p.da_out = (__nv_bfloat16 *)da_out;
+    p.db_out = (__nv_bfloat16 *)db_out;
+    p.TP = TP;
+    p.inv_sqrt_d = 1.f / sqrtf((float)a.D);
+    const long bhn = (long)a.B * a.H, rs = bhn * a.D;
+    CUtensorMap mk, mv, mr, mq, md;
+    if (!make_map(&mk, a.k, p.T, rs, bhn, BN) || !make_map(&mv, a.v, p.T, rs, bhn, BN) ||
+        !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM) ||
+        !make_map(&md, dout, a.L, rs, bhn, BM))
+        return cudaErrorInvalidValue;
+    const uint32_t smem = BwdSmem::TOTAL;
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(opted.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(rel_attn_bwd_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_relaxed);
+    }
+    const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
+    rel_attn_bwd_scores_kernel<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, md, p);
     return cudaGetLastError();
 }
 

@@ -316,6 +316,23 @@ __global__ void bwd_table_grad_kernel(const float *__restrict__ part, T *__restr
     }
 }
 
+// delta[(b*H + h)*L + i] = sum_d dO[i][b][h][d] * O[i][b][h][d] (one warp per
+// row, fp32)
+__global__ void bwd_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
+                                 float *__restrict__ delta, long nrows, int B, int H, int L, int D)
+{
+    const long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= nrows) return;
+    const int i = (int)(row % L);
+    const long bh = row / L;
+    const long base = ((long)i * B * H + bh) * D;   // [L][B][H][D]: (i*B + b)*H + h = i*B*H + bh
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) acc += __bfloat162float(dout[base + d]) * __bfloat162float(o[base + d]);
+    acc = warp_sum(acc);
+    if (lane == 0) delta[row] = acc;
+}
+
 // Row-major C (m x n, ldc) = op(A) . op(B) for `batch` problems at the given
 // element strides; ta: A is stored k x m (used transposed), tb: B is stored
 // n x k.  cuBLAS sees the column-major transpose C^T = op(B)^T op(A)^T.
@@ -352,6 +369,47 @@ Ws layout(long B, long H, long D, long L, long M, size_t es)
     w.dqc = o;  o += up256((size_t)L * B * H * D * 4);
     w.dqp = o;  o += up256((size_t)L * B * H * D * 4);
     w.drp = o;  o += up256((size_t)B * H * T * D * 4);
+    w.total = o;
+    return w;
+}
+
+// The fused path (bf16, D = 64): P, dA and dA in the table frame as bf16
+// [B*H][L][TP] (TP = M+L rounded up to 128) written by the tcgen05 scores
+// kernel, the forward's output and row log-sum-exp, delta, and the same
+// GEMM operands and partial sums as the materialised path.
+struct WsF {
+    size_t pb, da, db, qu, qv, rrep, dqc, dqp, drp, out, lse, delta, split, total;
+    long TP;
+    int splits;
+};
+
+WsF layout_fused(long B, long H, long D, long L, long M)
+{
+    const long T = M + L;
+    WsF w;
+    w.TP = (T + 127) / 128 * 128;
+    const size_t sq = (size_t)B * H * L * w.TP * 2;
+    size_t o = 0;
+    w.pb = o;    o += up256(sq);
+    w.da = o;    o += up256(sq);
+    w.db = o;    o += up256(sq);
+    w.qu = o;    o += up256((size_t)L * B * H * D * 2);
+    w.qv = o;    o += up256((size_t)L * B * H * D * 2);
+    w.rrep = o;  o += up256((size_t)B * H * T * D * 2);
+    w.dqc = o;   o += up256((size_t)L * B * H * D * 4);
+    w.dqp = o;   o += up256((size_t)L * B * H * D * 4);
+    w.drp = o;   o += up256((size_t)B * H * T * D * 4);
+    w.out = o;   o += up256((size_t)L * B * H * D * 2);
+    w.lse = o;   o += up256((size_t)B * H * L * 4);
+    w.delta = o; o += up256((size_t)B * H * L * 4);
+    AttnArgs a{};
+    a.B = (int)B;
+    a.H = (int)H;
+    a.D = (int)D;
+    a.L = (int)L;
+    a.M = (int)M;
+    w.splits = bf16_num_splits(a, device_sm_count());
+    w.split = o; o += up256(w.splits > 1 ? bf16_scratch_bytes(a, w.splits) : 0);
     w.total = o;
     return w;
 }
@@ -459,6 +517,90 @@ cuda_fail:
     return TXL_ERR_CUDA;
 }
 
+txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void *r, const float *u,
+                         const float *w, const void *dout, int B, int M, int L, int H, int D, void *dq, void *dk,
+                         void *dv, void *dr, float *du, float *dw, unsigned char *ws, const WsF &lay,
+                         cudaStream_t s)
+{
+    typedef __nv_bfloat16 E;
+    const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, ld = BH * D, TP = lay.TP;
+    E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv), *rrep = (E *)(ws + lay.rrep);
+    E *pb = (E *)(ws + lay.pb), *dab = (E *)(ws + lay.da), *dbb = (E *)(ws + lay.db), *outf = (E *)(ws + lay.out);
+    float *lse = (float *)(ws + lay.lse), *delta = (float *)(ws + lay.delta);
+    float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp), *drp = (float *)(ws + lay.drp);
+    cublasHandle_t hd = (cublasHandle_t)blas_on_stream(s);
+    if (!hd) return TXL_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    auto chk = [&]() {
+        e = cudaGetLastError();
+        return e == cudaSuccess;
+    };
+    // the forward (its output and row log-sum-exp), then delta = rowsum(dO * O)
+    AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.r = r;
+    a.u = u;
+    a.w = w;
+    a.out = outf;
+    a.B = B;
+    a.H = H;
+    a.D = D;
+    a.L = L;
+    a.M = M;
+    a.lse = lse;
+    if ((e = launch_attn_bf16(a, lay.splits, lay.splits > 1 ? ws + lay.split : nullptr, s)) != cudaSuccess)
+        goto cuda_fail;
+    bwd_delta_kernel<<<(unsigned)((BH * L + 7) / 8), 256, 0, s>>>((const E *)dout, outf, delta, BH * L, B, H, L, D);
+    if (!chk()) goto cuda_fail;
+    if ((e = launch_bwd_scores(a, dout, lse, delta, pb, dab, dbb, TP, s)) != cudaSuccess) goto cuda_fail;
+    // the GEMM operands q+u, q+v and the table per (b, h)
+    {
+        const int C = 8;
+        bwd_fold_vec_kernel<E><<<grid_for(nq / C, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / C, H, D);
+        if (!chk()) goto cuda_fail;
+        bwd_table_rep_vec_kernel<E><<<grid_for(BH * T * D / C, 256), 256, 0, s>>>((const E *)r, rrep, BH * T * D / C,
+                                                                                H, D, (int)T);
+        if (!chk()) goto cuda_fail;
+    }
+    {
+        const long long LTP = (long long)L * TP, TD = (long long)T * D;
+        const int Ti = (int)T, nb = (int)BH;
+        // dV = P^T dO, dK = dA^T qu, dQ = dA K + dB~ r, dr per (b, h) = dB~^T qv
+        if (gemm_rm(hd, true, false, Ti, D, L, pb, TP, LTP, dout, ld, D, dv, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
+            gemm_rm(hd, true, false, Ti, D, L, dab, TP, LTP, qu, ld, D, dk, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
+            gemm_rm(hd, false, false, L, D, Ti, dab, TP, LTP, k, ld, D, dqc, ld, D, nb, CUDA_R_16BF, CUDA_R_32F) ||
+            gemm_rm(hd, false, false, L, D, Ti, dbb, TP, LTP, rrep, D, TD, dqp, ld, D, nb, CUDA_R_16BF, CUDA_R_32F) ||
+            gemm_rm(hd, true, false, Ti, D, L, dbb, TP, LTP, qv, ld, D, drp, D, TD, nb, CUDA_R_16BF, CUDA_R_32F))
+            return TXL_ERR_CUDA;
+    }
+    bwd_sum_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>(dqc, dqp, (E *)dq, nq);
+    if (!chk()) goto cuda_fail;
+    if (du || dw) {
+        if (du && (e = cudaMemsetAsync(du, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
+        if (dw && (e = cudaMemsetAsync(dw, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
+        const long brows = (long)L * B;
+        const unsigned chunks = (unsigned)(brows / 16 < 1 ? 1 : (brows / 16 > 4096 ? 4096 : brows / 16));
+        bwd_bias_grad_kernel<<<dim3(chunks, (unsigned)H), 64, 0, s>>>(dqc, dqp, du, dw, brows, H, D);
+        if (!chk()) goto cuda_fail;
+    }
+    bwd_table_grad_kernel<E><<<grid_for(T * H * D, 256), 256, 0, s>>>(drp, (E *)dr, B, H, D, (int)T);
+    if (!chk()) goto cuda_fail;
+    return TXL_OK;
+cuda_fail:
+    note_cuda_error(e);
+    return TXL_ERR_CUDA;
+}
+
+bool fused_ok(int d_head, const void *const *ptrs, int n)
+{
+    if (d_head != 64) return false;
+    for (int x = 0; x < n; ++x)
+        if ((uintptr_t)ptrs[x] & 15) return false;
+    return true;
+}
+
 txl_status check_sizes(int batch, int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
@@ -484,7 +626,13 @@ txl_status txl_rel_attn_bwd_workspace(int batch, int mem_len, int seg_len, int h
     if (!bytes) return TXL_ERR_INVALID;
     const txl_status st = check_sizes(batch, mem_len, seg_len, heads, d_head, dtype);
     if (st != TXL_OK) return st;
-    *bytes = layout(batch, heads, d_head, seg_len, mem_len, dtype == TXL_F32 ? 4 : 2).total;
+    size_t n = layout(batch, heads, d_head, seg_len, mem_len, dtype == TXL_F32 ? 4 : 2).total;
+    if (dtype == TXL_BF16 && d_head == 64) {
+        // the fused path when the operands are 16-byte aligned (else the materialised one)
+        const size_t f = layout_fused(batch, heads, d_head, seg_len, mem_len).total;
+        n = f > n ? f : n;
+    }
+    *bytes = n;
     return TXL_OK;
 }
 
@@ -498,7 +646,12 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     if (!q || !k || !v || !r || !dout || !dq || !dk || !dv || !dr || !workspace) return TXL_ERR_INVALID;
     const size_t es = dtype == TXL_F32 ? 4 : 2;
     const Ws lay = layout(batch, heads, d_head, seg_len, mem_len, es);
-    if (workspace_bytes < lay.total || ((uintptr_t)workspace & 255)) return TXL_ERR_INVALID;
+    size_t need = lay.total;
+    if (dtype == TXL_BF16 && d_head == 64) {
+        const size_t f = layout_fused(batch, heads, d_head, seg_len, mem_len).total;
+        need = f > need ? f : need;
+    }
+    if (workspace_bytes < need || ((uintptr_t)workspace & 255)) return TXL_ERR_INVALID;
     const void *ins[] = {q, k, v, r, dout, dq, dk, dv, dr};
     for (const void *x : ins)
         if ((uintptr_t)x % es) return TXL_ERR_INVALID;
@@ -511,7 +664,7 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     const void *outs[] = {dq, dk, dv, dr, du, dw};
     const size_t osz[] = {nq, nk, nk, nr, nb, nb};
     const void *rd[] = {q, k, v, r, dout, u_bias, v_bias, workspace};
-    const size_t rsz[] = {nq, nk, nk, nr, nq, nb, nb, lay.total};
+    const size_t rsz[] = {nq, nk, nk, nr, nq, nb, nb, need};
     for (int a = 0; a < 6; ++a) {
         for (int b = 0; b < 8; ++b)
             if (overlaps(outs[a], osz[a], rd[b], rsz[b])) return TXL_ERR_INVALID;
@@ -519,7 +672,7 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
             if (overlaps(outs[a], osz[a], outs[b], osz[b])) return TXL_ERR_INVALID;
     }
     for (int b = 0; b < 7; ++b)
-        if (overlaps(workspace, lay.total, rd[b], rsz[b])) return TXL_ERR_INVALID;
+        if (overlaps(workspace, need, rd[b], rsz[b])) return TXL_ERR_INVALID;
     // absent biases: the zero vector (their gradients are still reported when asked)
     const float *uu = u_bias, *ww = v_bias;
     if (!uu || !ww) {
@@ -538,6 +691,10 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     if (dtype == TXL_F32)
         return run_bwd<float>(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr, du,
                               dw, wsb, lay, s, false);
+    const void *al[] = {q, k, v, r, dout, uu, ww};
+    if (fused_ok(d_head, al, 7))
+        return run_bwd_fused(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr, du, dw,
+                             wsb, layout_fused(batch, heads, d_head, seg_len, mem_len), s);
     return run_bwd<__nv_bfloat16>(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr,
                                   du, dw, wsb, lay, s, true);
 }

@@ -15,6 +15,7 @@ struct AttnArgs {
     int B, H, D, L, M;
     int kv_start = 0;             // K, V in a ring of M+L rows: key j at row (kv_start + j) mod (M+L)
     int scale_d = 0;              // d_head for the 1/sqrt(d_head) scale when D is a padded width (0: D)
+    float *lse = nullptr;         // bf16 path, optional [B*H][L]: row log-sum-exp, log2 units of the scaled score
 };
 
 // fp32 SIMT path (attn_f32.cu)
@@ -25,6 +26,12 @@ cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s);
 int bf16_num_splits(const AttnArgs &a, int num_sms);
 size_t bf16_scratch_bytes(const AttnArgs &a, int splits);
 cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaStream_t s);
+// The score side of the backward (bf16, D = 64, 16-byte aligned operands):
+// P, dA and dA in the table frame, each bf16 [B*H][L][TP] (TP >= M+L rounded
+// up to 128), from the forward's row log-sum-exp `lse` and delta =
+// rowsum(dO * O), both [B*H][L].
+cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, const float *delta,
+                              void *p_out, void *da_out, void *db_out, long TP, cudaStream_t s);
 // reads and clears the device error word written by bounded waits (syncs on s)
 cudaError_t read_and_clear_device_error(unsigned int *word, cudaStream_t s);
 

@@ -366,6 +366,29 @@ __device__ __forceinline__ void tmem_ld_h_tile(uint32_t s0, uint32_t s1, uint32_
 #undef TXL_R8
 }
 
+// 64 columns per thread: two 32-column loads (threads 16-31 at the address
+// + OFF); one wait
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_h64(uint32_t t0, uint32_t t1, float (&x)[64])
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(x);
+#define TXL_R8(p, o) "=r"(p[o]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3]), "=r"(p[o + 4]), \
+                     "=r"(p[o + 5]), "=r"(p[o + 6]), "=r"(p[o + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64], %66;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65], %66;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TXL_R8(r, 0), TXL_R8(r, 8), TXL_R8(r, 16), TXL_R8(r, 24), TXL_R8(r, 32), TXL_R8(r, 40),
+          TXL_R8(r, 48), TXL_R8(r, 56)
+        : "r"(t0), "r"(t1), "n"(OFF)
+        : "memory");
+#undef TXL_R8
+}
+
 template <int OFF>
 __device__ __forceinline__ void tmem_st_h32(uint32_t taddr, const float (&v)[32])
 {
