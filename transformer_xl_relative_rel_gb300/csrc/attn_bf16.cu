@@ -1324,46 +1324,57 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                     __syncwarp();
                 };
                 auto write_rows = [&](__nv_bfloat16 *dstm) {
+                    const int ch = lane & 15;
+                    __nv_bfloat16 *base = dstm + ((long)it.bh * p.L + it.i0 + lb + (lane >> 4)) * rowpitch + jt + 8 * ch;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int r = 2 * k + (lane >> 4), ch = lane & 15;
-                        const int ir = it.i0 + lb + r;
-                        if (ir < p.L)
-                            *reinterpret_cast<uint4 *>(dstm + ((long)it.bh * p.L + ir) * rowpitch + jt + 8 * ch) =
-                                *reinterpret_cast<const uint4 *>(stg + stg_off(r, 8 * ch));
+                        const int r = 2 * k + (lane >> 4);
+                        if (it.i0 + lb + r < p.L)
+                            *reinterpret_cast<uint4 *>(base + (long)(2 * k) * rowpitch) =
+                                *reinterpret_cast<const uint4 *>(stg + r * 256 + ((ch ^ (r & 7)) << 4));
                     }
                     __syncwarp();
-                };
-                auto elem = [&](int r, int col) {
-                    return *reinterpret_cast<const unsigned short *>(stg + stg_off(r, col));
                 };
                 stage(pp);
                 write_rows(p.p_out);
                 stage(aa);
                 write_rows(p.da_out);
                 // dA in the table frame from the same staged rows: row i's 128
-                // values start at column L-1-i+jt; written as 4-byte pairs
-                // (shifted by one element when that column is odd)
-                for (int r = 0; r < 16; ++r) {
-                    const int ir = it.i0 + lb + r;
-                    if (ir >= p.L) break;
-                    const long c0 = (long)(p.L - 1 - ir) + jt;
-                    __nv_bfloat16 *dst = p.db_out + ((long)it.bh * p.L + ir) * rowpitch + c0;
-                    const long room = rowpitch - c0;              // columns left in the row
-                    const int odd = (int)(c0 & 1);
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int l = lane + 32 * k;              // pair l: elements 2l-odd, 2l+1-odd
-                        const int e0 = 2 * l - odd;
-                        if (e0 >= 0 && e0 + 1 < room) {
-                            const uint32_t lo = elem(r, e0), hi = elem(r, e0 + 1);
-                            *reinterpret_cast<uint32_t *>(dst + e0) = lo | (hi << 16);
+                // values start at column L-1-i+jt.  Each lane takes staged
+                // words lane and lane+32 (keys 2w, 2w+1); when that column is
+                // odd the pairs are realigned with the neighbouring lane's
+                // word (one element across), the two end elements on their own.
+                {
+                    const int x0 = lane >> 2, y0 = (lane & 3) << 2;     // word lane: 16-byte chunk, offset
+                    const long rb0 = ((long)it.bh * p.L + it.i0 + lb) * rowpitch;
+                    for (int r = 0; r < 16; ++r) {
+                        const int ir = it.i0 + lb + r;
+                        if (ir >= p.L) break;
+                        const unsigned char *srow = stg + r * 256;
+                        const int sw = r & 7;
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(srow + ((x0 ^ sw) << 4) + y0);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(srow + (((x0 + 8) ^ sw) << 4) + y0);
+                        const long c0 = (long)(p.L - 1 - ir) + jt;
+                        const long room = rowpitch - c0;                   // columns left in the row
+                        __nv_bfloat16 *dst = p.db_out + rb0 + (long)r * rowpitch + c0;
+                        if ((c0 & 1) == 0) {
+                            if (2 * lane + 1 < room) *reinterpret_cast<uint32_t *>(dst + 2 * lane) = w0;
+                            if (2 * lane + 65 < room) *reinterpret_cast<uint32_t *>(dst + 2 * lane + 64) = w1;
+                        } else {
+                            // pair l = (element 2l-1, element 2l): high half of word l-1, low half of word l
+                            const uint32_t up0 = __shfl_up_sync(0xffffffffu, w0, 1);
+                            const uint32_t up1 = __shfl_up_sync(0xffffffffu, w1, 1);
+                            const uint32_t w0_31 = __shfl_sync(0xffffffffu, w0, 31);
+                            const uint32_t prev1 = lane == 0 ? w0_31 : up1;
+                            if (lane > 0 && 2 * lane < room)
+                                *reinterpret_cast<uint32_t *>(dst + 2 * lane - 1) = __byte_perm(up0, w0, 0x5432);
+                            if (2 * lane + 64 < room)
+                                *reinterpret_cast<uint32_t *>(dst + 2 * lane + 63) = __byte_perm(prev1, w1, 0x5432);
+                            if (lane == 0 && room > 0)
+                                reinterpret_cast<unsigned short *>(dst)[0] = (unsigned short)(w0 & 0xFFFFu);
+                            if (lane == 31 && 127 < room)
+                                reinterpret_cast<unsigned short *>(dst)[127] = (unsigned short)(w1 >> 16);
                         }
-                    }
-                    if (odd && lane == 0 && room > 0) {
-                        // the first element and the last one
-                        reinterpret_cast<unsigned short *>(dst)[0] = elem(r, 0);
-                        if (127 < room) reinterpret_cast<unsigned short *>(dst)[127] = elem(r, 127);
                     }
                 }
                 __syncwarp();
