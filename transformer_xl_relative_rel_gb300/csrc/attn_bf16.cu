@@ -79,10 +79,10 @@ struct Params {
     float *part_o;      // [splits][B*H][L][DP] when splits > 1
     float *part_lse;    // [splits][B*H][L]
     float *lse;         // optional [B*H][L]: each row's log-sum-exp (log2 units of the scaled score)
-    // backward scores only: dO, delta = rowsum(dO * O), the outputs P, dA and
-    // dA in the table frame ([B*H][L][TP]), 1/sqrt(d_head)
+    // backward scores only (the forward's output O comes in `out`): dO, the
+    // outputs P and dA ([B*H][L][TP]) and dA in the table frame
+    // ([H][L][B][TP]), 1/sqrt(d_head)
     const __nv_bfloat16 *dout;
-    const float *delta;
     __nv_bfloat16 *p_out, *da_out, *db_out;
     long TP;
     float inv_sqrt_d;
@@ -1242,7 +1242,31 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
             const int jn = next_busy(p, j + 1, nx);
             const long row = (long)it.bh * p.L + i;   // this thread's row of the [B*H][L] matrices
             const float lse = row_valid ? p.lse[row] : 0.f;
-            const float delta = row_valid ? p.delta[row] : 0.f;
+            // the table-frame matrix is head-major, [H][L][B][TP]: row (i, b) of
+            // head h, so that one GEMM per head contracts over (i, b)
+            auto db_row = [&](int ir) { return (((long)it.h * p.L + ir) * p.B + it.b) * rowpitch; };
+            // delta = rowsum(dO * O): this thread's half of the row, dO from
+            // the item's operand buffer (loaded with its q rows), O from the
+            // forward's output
+            float delta;
+            {
+                float acc = 0.f;
+                if (row_valid) {
+                    const unsigned char *dob = smem + S::DO0 + (uint32_t)(ni & 1) * S::QT;
+                    const uint4 *op = reinterpret_cast<const uint4 *>(
+                        p.out + ((long)i * p.B * p.H + it.bh) * DP + 32 * half);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 dv4 = *reinterpret_cast<const uint4 *>(dob + sw128_offset(ii, 32 * half + 8 * c));
+                        const uint4 ov4 = op[c];
+                        const __nv_bfloat16 *de = reinterpret_cast<const __nv_bfloat16 *>(&dv4);
+                        const __nv_bfloat16 *oe = reinterpret_cast<const __nv_bfloat16 *>(&ov4);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc += __bfloat162float(de[e]) * __bfloat162float(oe[e]);
+                    }
+                }
+                delta = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
+            }
             // keys past the item's last tile are masked for all its rows: P
             // and dA there are zeros (the columns up to the row pitch); and
             // the table frame of the rows before their first key (no key
@@ -1261,11 +1285,12 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                     }
                     if (it.t0 == 0) {
                         const int pre = p.L - 1 - ir;                // table columns before key 0
+                        const long dr0 = db_row(ir);
                         for (int c = 8 * lane; c < pre; c += 256) {
                             if (c + 8 <= pre)
-                                *reinterpret_cast<uint4 *>(p.db_out + rr + c) = z;
+                                *reinterpret_cast<uint4 *>(p.db_out + dr0 + c) = z;
                             else
-                                for (int e = c; e < pre; ++e) p.db_out[rr + e] = __float2bfloat16(0.f);
+                                for (int e = c; e < pre; ++e) p.db_out[dr0 + e] = __float2bfloat16(0.f);
                         }
                     }
                 }
@@ -1346,7 +1371,6 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 // word (one element across), the two end elements on their own.
                 {
                     const int x0 = lane >> 2, y0 = (lane & 3) << 2;     // word lane: 16-byte chunk, offset
-                    const long rb0 = ((long)it.bh * p.L + it.i0 + lb) * rowpitch;
                     for (int r = 0; r < 16; ++r) {
                         const int ir = it.i0 + lb + r;
                         if (ir >= p.L) break;
@@ -1356,7 +1380,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(srow + (((x0 + 8) ^ sw) << 4) + y0);
                         const long c0 = (long)(p.L - 1 - ir) + jt;
                         const long room = rowpitch - c0;                   // columns left in the row
-                        __nv_bfloat16 *dst = p.db_out + rb0 + (long)r * rowpitch + c0;
+                        __nv_bfloat16 *dst = p.db_out + db_row(ir) + c0;
                         if ((c0 & 1) == 0) {
                             if (2 * lane + 1 < room) *reinterpret_cast<uint32_t *>(dst + 2 * lane) = w0;
                             if (2 * lane + 65 < room) *reinterpret_cast<uint32_t *>(dst + 2 * lane + 64) = w1;
@@ -1687,8 +1711,8 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, const float *delta,
-                              void *p_out, void *da_out, void *db_out, long TP, cudaStream_t s)
+cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, void *p_out, void *da_out,
+                              void *db_out, long TP, cudaStream_t s)
 {
     if (a.D != 64) return cudaErrorNotSupported;
     Params p;
@@ -1711,7 +1735,7 @@ cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *
     p.sl2 = LOG2E / sqrtf((float)a.D);
     p.lse = const_cast<float *>(lse);
     p.dout = (const __nv_bfloat16 *)dout;
-    p.delta = delta;
+    p.out = (__nv_bfloat16 *)a.out;   // the forward's output O (read: delta = rowsum(dO * O))
     p.p_out = (__nv_bfloat16 *)p_out;
     p.da_out = (__nv_bfloat16 *)da_out;
     p.db_out = (__nv_bfloat16 *)db_out;

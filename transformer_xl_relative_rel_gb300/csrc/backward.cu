@@ -316,23 +316,6 @@ __global__ void bwd_table_grad_kernel(const float *__restrict__ part, T *__restr
     }
 }
 
-// delta[(b*H + h)*L + i] = sum_d dO[i][b][h][d] * O[i][b][h][d] (one warp per
-// row, fp32)
-__global__ void bwd_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
-                                 float *__restrict__ delta, long nrows, int B, int H, int L, int D)
-{
-    const long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= nrows) return;
-    const int i = (int)(row % L);
-    const long bh = row / L;
-    const long base = ((long)i * B * H + bh) * D;   // [L][B][H][D]: (i*B + b)*H + h = i*B*H + bh
-    float acc = 0.f;
-    for (int d = lane; d < D; d += 32) acc += __bfloat162float(dout[base + d]) * __bfloat162float(o[base + d]);
-    acc = warp_sum(acc);
-    if (lane == 0) delta[row] = acc;
-}
-
 // Row-major C (m x n, ldc) = op(A) . op(B) for `batch` problems at the given
 // element strides; ta: A is stored k x m (used transposed), tb: B is stored
 // n x k.  cuBLAS sees the column-major transpose C^T = op(B)^T op(A)^T.
@@ -378,7 +361,7 @@ Ws layout(long B, long H, long D, long L, long M, size_t es)
 // kernel, the forward's output and row log-sum-exp, delta, and the same
 // GEMM operands and partial sums as the materialised path.
 struct WsF {
-    size_t pb, da, db, qu, qv, rrep, dqc, dqp, drp, out, lse, delta, split, total;
+    size_t pb, da, db, qu, qv, dqc, dqp, out, lse, split, total;
     long TP;
     int splits;
 };
@@ -395,13 +378,10 @@ WsF layout_fused(long B, long H, long D, long L, long M)
     w.db = o;    o += up256(sq);
     w.qu = o;    o += up256((size_t)L * B * H * D * 2);
     w.qv = o;    o += up256((size_t)L * B * H * D * 2);
-    w.rrep = o;  o += up256((size_t)B * H * T * D * 2);
     w.dqc = o;   o += up256((size_t)L * B * H * D * 4);
     w.dqp = o;   o += up256((size_t)L * B * H * D * 4);
-    w.drp = o;   o += up256((size_t)B * H * T * D * 4);
     w.out = o;   o += up256((size_t)L * B * H * D * 2);
     w.lse = o;   o += up256((size_t)B * H * L * 4);
-    w.delta = o; o += up256((size_t)B * H * L * 4);
     AttnArgs a{};
     a.B = (int)B;
     a.H = (int)H;
@@ -524,10 +504,10 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
 {
     typedef __nv_bfloat16 E;
     const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, ld = BH * D, TP = lay.TP;
-    E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv), *rrep = (E *)(ws + lay.rrep);
+    E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv);
     E *pb = (E *)(ws + lay.pb), *dab = (E *)(ws + lay.da), *dbb = (E *)(ws + lay.db), *outf = (E *)(ws + lay.out);
-    float *lse = (float *)(ws + lay.lse), *delta = (float *)(ws + lay.delta);
-    float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp), *drp = (float *)(ws + lay.drp);
+    float *lse = (float *)(ws + lay.lse);
+    float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp);
     cublasHandle_t hd = (cublasHandle_t)blas_on_stream(s);
     if (!hd) return TXL_ERR_CUDA;
     cudaError_t e = cudaSuccess;
@@ -535,7 +515,7 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
         e = cudaGetLastError();
         return e == cudaSuccess;
     };
-    // the forward (its output and row log-sum-exp), then delta = rowsum(dO * O)
+    // the forward (its output and row log-sum-exp)
     AttnArgs a{};
     a.q = q;
     a.k = k;
@@ -552,27 +532,22 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
     a.lse = lse;
     if ((e = launch_attn_bf16(a, lay.splits, lay.splits > 1 ? ws + lay.split : nullptr, s)) != cudaSuccess)
         goto cuda_fail;
-    bwd_delta_kernel<<<(unsigned)((BH * L + 7) / 8), 256, 0, s>>>((const E *)dout, outf, delta, BH * L, B, H, L, D);
+    if ((e = launch_bwd_scores(a, dout, lse, pb, dab, dbb, TP, s)) != cudaSuccess) goto cuda_fail;
+    // the GEMM operands q+u, q+v
+    bwd_fold_vec_kernel<E><<<grid_for(nq / 8, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / 8, H, D);
     if (!chk()) goto cuda_fail;
-    if ((e = launch_bwd_scores(a, dout, lse, delta, pb, dab, dbb, TP, s)) != cudaSuccess) goto cuda_fail;
-    // the GEMM operands q+u, q+v and the table per (b, h)
     {
-        const int C = 8;
-        bwd_fold_vec_kernel<E><<<grid_for(nq / C, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / C, H, D);
-        if (!chk()) goto cuda_fail;
-        bwd_table_rep_vec_kernel<E><<<grid_for(BH * T * D / C, 256), 256, 0, s>>>((const E *)r, rrep, BH * T * D / C,
-                                                                                H, D, (int)T);
-        if (!chk()) goto cuda_fail;
-    }
-    {
-        const long long LTP = (long long)L * TP, TD = (long long)T * D;
-        const int Ti = (int)T, nb = (int)BH;
-        // dV = P^T dO, dK = dA^T qu, dQ = dA K + dB~ r, dr per (b, h) = dB~^T qv
+        const long long LTP = (long long)L * TP, LBTP = (long long)L * B * TP;
+        const int Ti = (int)T, nb = (int)BH, LB = L * B, HD = H * D;
+        // per (b, h): dV = P^T dO, dK = dA^T qu, dQ (content) = dA K; per head
+        // over the rows (i, b) of the head-major table-frame matrix dA~:
+        // dQ (position) = dA~ r_h and dr_h = dA~^T qv, both straight into
+        // their [.., H, D] layouts
         if (gemm_rm(hd, true, false, Ti, D, L, pb, TP, LTP, dout, ld, D, dv, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
             gemm_rm(hd, true, false, Ti, D, L, dab, TP, LTP, qu, ld, D, dk, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
             gemm_rm(hd, false, false, L, D, Ti, dab, TP, LTP, k, ld, D, dqc, ld, D, nb, CUDA_R_16BF, CUDA_R_32F) ||
-            gemm_rm(hd, false, false, L, D, Ti, dbb, TP, LTP, rrep, D, TD, dqp, ld, D, nb, CUDA_R_16BF, CUDA_R_32F) ||
-            gemm_rm(hd, true, false, Ti, D, L, dbb, TP, LTP, qv, ld, D, drp, D, TD, nb, CUDA_R_16BF, CUDA_R_32F))
+            gemm_rm(hd, false, false, LB, D, Ti, dbb, TP, LBTP, r, HD, D, dqp, HD, D, H, CUDA_R_16BF, CUDA_R_32F) ||
+            gemm_rm(hd, true, false, Ti, D, LB, dbb, TP, LBTP, qv, HD, D, dr, HD, D, H, CUDA_R_16BF, CUDA_R_16BF))
             return TXL_ERR_CUDA;
     }
     bwd_sum_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>(dqc, dqp, (E *)dq, nq);
@@ -585,8 +560,6 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
         bwd_bias_grad_kernel<<<dim3(chunks, (unsigned)H), 64, 0, s>>>(dqc, dqp, du, dw, brows, H, D);
         if (!chk()) goto cuda_fail;
     }
-    bwd_table_grad_kernel<E><<<grid_for(T * H * D, 256), 256, 0, s>>>(drp, (E *)dr, B, H, D, (int)T);
-    if (!chk()) goto cuda_fail;
     return TXL_OK;
 cuda_fail:
     note_cuda_error(e);

@@ -27,11 +27,11 @@ int bf16_num_splits(const AttnArgs &a, int num_sms);
 size_t bf16_scratch_bytes(const AttnArgs &a, int splits);
 cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaStream_t s);
 // The score side of the backward (bf16, D = 64, 16-byte aligned operands):
-// P, dA and dA in the table frame, each bf16 [B*H][L][TP] (TP >= M+L rounded
-// up to 128), from the forward's row log-sum-exp `lse` and delta =
-// rowsum(dO * O), both [B*H][L].
-cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, const float *delta,
-                              void *p_out, void *da_out, void *db_out, long TP, cudaStream_t s);
+// P and dA as bf16 [B*H][L][TP] and dA in the table frame as bf16
+// [H][L][B][TP] (TP = M+L rounded up to 128), from the forward's output
+// a.out and row log-sum-exp `lse` ([B*H][L]).
+cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, void *p_out, void *da_out,
+                              void *db_out, long TP, cudaStream_t s);
 // reads and clears the device error word written by bounded waits (syncs on s)
 cudaError_t read_and_clear_device_error(unsigned int *word, cudaStream_t s);
 
