@@ -499,7 +499,11 @@ def backward(args, local: int):
     (per-call working set > L2).  Algorithmic work of the backward: 16*D
     FLOPs per visible (query, key) pair -- the content and position scores
     recomputed (2D + 2D), dP, dV, dK (2D each), dQ through the keys and
-    through the table (2D each), the table gradient (2D)."""
+    through the table (2D each), the table gradient (2D).
+
+    Three timings: the backward that runs its own forward (the headline
+    value), the backward fed the forward's saved output and row log-sum-exp,
+    and a training layer's forward (with log-sum-exp) plus that backward."""
     import transformer_xl_relative_rel_gb300 as txl
     w = WORKLOADS[args.workload]
     s = w.shape
@@ -513,23 +517,39 @@ def backward(args, local: int):
     wb = torch.randn(H, D, generator=gen, device=dev)
     nbytes = txl.rel_attn_bwd_workspace_bytes(B, M, L, H, D, txl.TXL_BF16)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    fwd = lambda: txl.rel_attn_fwd(q, k, v, r, u, wb, mem_len=M, out=out, lse=lse)
+    fwd()
     grads = txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws)
-    call = lambda: txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws, grads=grads)
-    for _ in range(args.warmup):
-        call()
+    bwd = lambda: txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws, grads=grads)
+    bwd_saved = lambda: txl.rel_attn_bwd(q, k, v, r, u, wb, dout, mem_len=M, workspace=ws, grads=grads,
+                                         out=out, lse=lse)
+
+    def layer():
+        fwd()
+        bwd_saved()
+
+    def timed(call):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / args.steps
+
     txl.check()
     clocks = ClockSampler(local)
     clocks.start()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        call()
-    e1.record()
-    torch.cuda.synchronize()
+    t = timed(bwd)
+    t_saved = timed(bwd_saved)
+    t_layer = timed(layer)
     clk = clocks.stop()
     txl.check()
-    t = e0.elapsed_time(e1) / 1e3 / args.steps
     pairs = L * M + L * (L + 1) / 2
     flops = 16.0 * D * B * H * pairs
     peaks, src = load_peaks()
@@ -542,8 +562,12 @@ def backward(args, local: int):
                                        "seg_len": L, "mem_len": M,
                                        "l2": f"workspace {nbytes / 1e9:.2f} GB > 129 MB L2 (no flush)"},
         "tflops": flops / t / 1e12, "frac_bf16_peak": flops / t / 1e12 / peak, "peak": peak,
-        "peak_source": src, "launches_per_call": 15,
-        "design": "materialised scores: cuBLAS batched GEMMs + row kernels (see profiles/)",
+        "peak_source": src, "launches_per_call": 10,
+        "saved_forward": {"ms_per_call": t_saved * 1e3, "tflops": flops / t_saved / 1e12,
+                          "frac_bf16_peak": flops / t_saved / 1e12 / peak, "launches_per_call": 9},
+        "forward_plus_backward": {"ms_per_call": t_layer * 1e3,
+                                  "tflops": (flops + 6.0 * D * B * H * pairs) / t_layer / 1e12},
+        "design": "tcgen05 scores kernel (P, dA, table-frame dA in bf16) + cuBLAS GEMMs (see profiles/)",
         "clocks": clk}), flush=True)
     return 0
 

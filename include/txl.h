@@ -82,6 +82,26 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
                             txl_dtype dtype, void *out, void *stream);
 
 /*
+ * txl_rel_attn_fwd_lse -- txl_rel_attn_fwd that also stores, per query row,
+ * the natural log of the softmax denominator (the log-sum-exp of the row's
+ * visible scaled scores s_ij above):
+ *     lse[(b*heads + h)*seg_len + i] = log sum_{j <= M+i} exp(s_ij)
+ * so that P_ij = exp(s_ij - lse) recovers the weights without a second pass
+ * over the keys.  txl_rel_attn_bwd takes out and lse back to skip its own
+ * forward.
+ *
+ * lse : device float32 [batch][heads][seg_len], 4-byte aligned, must not
+ *       overlap out or any input; required (NULL => TXL_ERR_INVALID unless
+ *       there is nothing to do).
+ * Only TXL_BF16 (else TXL_ERR_UNSUPPORTED).  Everything else, including the
+ * result in out, as txl_rel_attn_fwd.
+ */
+txl_status txl_rel_attn_fwd_lse(const void *q, const void *k, const void *v, const void *r,
+                                const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                int seg_len, int heads, int d_head, txl_dtype dtype, void *out,
+                                float *lse, void *stream);
+
+/*
  * txl_mem_update -- the per-layer memory rollover (Transformer-XL,
  * Section 3.2: a cache of the last M hidden states, possibly spanning several
  * segments, reused as extended context by the next segment).
@@ -171,15 +191,24 @@ txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int 
  *
  * q, k, v, r, dout : device, dtype, layouts as txl_rel_attn_fwd (dout like q).
  * u_bias, v_bias   : device float32 [heads][d_head] or NULL (zero bias).
+ * out, lse         : the forward's output and row log-sum-exp as
+ *                    txl_rel_attn_fwd_lse wrote them for these inputs (out
+ *                    16-byte aligned, lse 4-byte aligned), or both NULL.
+ *                    Given, they spare the backward its own forward pass;
+ *                    the bf16 d_head = 64 path reads them, the others (which
+ *                    recompute the scores in full) ignore them.  Exactly one
+ *                    of them NULL => TXL_ERR_INVALID.
  * dq, dk, dv, dr   : device outputs, dtype, shaped like q, k, v, r.
  * du, dw           : device float32 [heads][d_head] outputs, or NULL (not
  *                    computed).  Outputs must not overlap each other, any
  *                    input or the workspace.
  * workspace        : device scratch of at least the bytes that
  *                    txl_rel_attn_bwd_workspace reports, 256-byte aligned,
- *                    owned by the caller (about 3 x 4 + 3 x dtype bytes per
- *                    (b, h, i, j) score entry: the score, P, dP and dA of
- *                    every head are materialised).
+ *                    owned by the caller.  bf16 with d_head = 64: P and dA
+ *                    as bf16 plus dA in the table's frame (about 3 x 2 bytes
+ *                    per (b, h, i, j) score entry); otherwise the score, P,
+ *                    dP and dA of every head (about 3 x 4 + 3 x dtype bytes
+ *                    per entry).
  * Limits: d_head <= 128 (else TXL_ERR_UNSUPPORTED).  Asynchronous on stream.
  * bf16: operands of the contractions in bf16 (q+u, q+v, P and dA rounded
  * once), fp32 accumulation, fp32 softmax; fp32: fp32 throughout.
@@ -187,9 +216,10 @@ txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int 
 txl_status txl_rel_attn_bwd_workspace(int batch, int mem_len, int seg_len, int heads, int d_head,
                                       txl_dtype dtype, size_t *bytes);
 txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const void *r, const float *u_bias,
-                            const float *v_bias, const void *dout, int batch, int mem_len, int seg_len, int heads,
-                            int d_head, txl_dtype dtype, void *dq, void *dk, void *dv, void *dr, float *du,
-                            float *dw, void *workspace, size_t workspace_bytes, void *stream);
+                            const float *v_bias, const void *dout, const void *out, const float *lse, int batch,
+                            int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype, void *dq, void *dk,
+                            void *dv, void *dr, float *du, float *dw, void *workspace, size_t workspace_bytes,
+                            void *stream);
 
 /*
  * txl_ring_append -- write n_rows new rows into a ring of ring_len rows at

@@ -65,7 +65,7 @@ def _load() -> ctypes.CDLL:
         lib.txl_oracle_rel_attn.argtypes = [
             _dp, _dp, _dp, _dp, _dp, _dp,
             ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
-            _dp, _dp, ctypes.c_int]
+            _dp, _dp, _dp, ctypes.c_int]
         lib.txl_oracle_rel_attn.restype = None
         lib.txl_oracle_rel_attn_rows.argtypes = [
             _dp, _dp, _dp, _dp, _dp, _dp,
@@ -109,21 +109,27 @@ def _shapes(q, k, v, r, u, w, mem_len):
 
 
 def rel_attn(q, k, v, r, u, w, mem_len: int, return_prob: bool = False,
-             nthreads: int = 0):
+             nthreads: int = 0, return_lse: bool = False):
     """Relative attention of one layer over [memory; segment], float64.
 
-    Returns ``out`` of shape [L, B, H, D] and, when ``return_prob``, the
-    attention weights ``P`` of shape [B, H, L, M+L] (exact zeros where masked).
+    Returns ``out`` of shape [L, B, H, D]; then, when ``return_prob``, the
+    attention weights ``P`` of shape [B, H, L, M+L] (exact zeros where
+    masked); then, when ``return_lse``, each row's log-sum-exp of its scaled
+    scores, [B, H, L].
     """
     q, k, v, r, u, w = (_f64(x) for x in (q, k, v, r, u, w))
     B, H, D, L, T = _shapes(q, k, v, r, u, w, mem_len)
     out = np.zeros((L, B, H, D), dtype=np.float64)
     prob = np.zeros((B, H, L, T), dtype=np.float64) if return_prob else None
+    lse = np.zeros((B, H, L), dtype=np.float64) if return_lse else None
+    null = ctypes.cast(None, _dp)
     _load().txl_oracle_rel_attn(
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u), _ptr(w),
         B, H, D, L, mem_len, _ptr(out),
-        _ptr(prob) if prob is not None else ctypes.cast(None, _dp), int(nthreads))
-    return (out, prob) if return_prob else out
+        _ptr(prob) if prob is not None else null, _ptr(lse) if lse is not None else null,
+        int(nthreads))
+    res = (out,) + ((prob,) if return_prob else ()) + ((lse,) if return_lse else ())
+    return res if len(res) > 1 else out
 
 
 def rel_attn_rows(q, k, v, r, u, w, mem_len: int, rows, nthreads: int = 0):

@@ -30,6 +30,8 @@
  *   r      : [T][H][D], row t holds W_kR R_{T-1-t}
  *   u, w   : [H][D]            (w is the paper's v bias)
  *   prob   : [B][H][L][T]      (optional, may be NULL)
+ *   lse    : [B][H][L]         (optional, may be NULL: each row's log of its
+ *                               softmax denominator)
  *
  * Status: parity pinned.  The pins (tests/test_oracle_pins.py) check this code
  * against the four-term expansion from hidden states, the Appendix B
@@ -45,11 +47,14 @@
 
 /* One query row (b, h, i): the masked, scaled softmax over keys 0..M+i of the
  * four-term score, then the weighted sum of the values.  s is scratch of T
- * doubles.  The exact definition: no blocking, no online rescaling. */
+ * doubles.  The exact definition: no blocking, no online rescaling.  When
+ * lse_out is not NULL it receives the natural log of the softmax denominator,
+ * log sum_j exp(s_j) over the visible keys. */
 static void one_row(const double *q, const double *k, const double *v,
                     const double *r, const double *u, const double *w,
                     long B, long H, long D, long L, long M, long b, long h,
-                    long i, double *s, double *out_row, double *prob_row)
+                    long i, double *s, double *out_row, double *prob_row,
+                    double *lse_out)
 {
     const long T = M + L;
     const double scale = 1.0 / sqrt((double)D);
@@ -76,6 +81,7 @@ static void one_row(const double *q, const double *k, const double *v,
         s[j] = exp(s[j] - mx);
         z += s[j];
     }
+    if (lse_out) *lse_out = mx + log(z);
     for (long j = 0; j <= last; ++j) s[j] /= z;
     for (long d = 0; d < D; ++d) {
         double o = 0.0;
@@ -91,7 +97,7 @@ static void one_row(const double *q, const double *k, const double *v,
 void txl_oracle_rel_attn(const double *q, const double *k, const double *v,
                          const double *r, const double *u, const double *w,
                          long B, long H, long D, long L, long M,
-                         double *out, double *prob, int nthreads)
+                         double *out, double *prob, double *lse, int nthreads)
 {
     const long T = M + L;
     const long nbh = B * H;
@@ -109,7 +115,8 @@ void txl_oracle_rel_attn(const double *q, const double *k, const double *v,
             const long b = bh / H, h = bh % H;
             for (long i = 0; i < L; ++i) {
                 double *prow = prob ? prob + ((b * H + h) * L + i) * T : NULL;
-                one_row(q, k, v, r, u, w, B, H, D, L, M, b, h, i, s, row, prow);
+                one_row(q, k, v, r, u, w, B, H, D, L, M, b, h, i, s, row, prow,
+                        lse ? lse + (b * H + h) * L + i : NULL);
                 double *o = out + ((i * B + b) * H + h) * D;
                 for (long d = 0; d < D; ++d) o[d] = row[d];
             }
@@ -140,7 +147,7 @@ void txl_oracle_rel_attn_rows(const double *q, const double *k, const double *v,
         for (long x = 0; x < n; ++x) {
             one_row(q, k, v, r, u, w, B, H, D, L, M, (long)rows[3 * x],
                     (long)rows[3 * x + 1], (long)rows[3 * x + 2], s,
-                    out_rows + x * D, NULL);
+                    out_rows + x * D, NULL, NULL);
         }
         free(s);
     }

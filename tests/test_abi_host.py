@@ -143,12 +143,13 @@ def test_bwd_workspace_query(lib):
 def _bwd(**kw):
     st, need = _bwd_ws()
     a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, r=FAKE * 4, u=FAKE * 5, w=FAKE * 6, dout=FAKE * 7,
-             B=2, M=8, L=8, H=2, D=16, dt=1, dq=FAKE * 8, dk=FAKE * 9, dv=FAKE * 10, dr=FAKE * 11,
-             du=FAKE * 12, dw=FAKE * 13, ws=FAKE * 14, nws=need, stream=None)
+             out=None, lse=None, B=2, M=8, L=8, H=2, D=16, dt=1, dq=FAKE * 8, dk=FAKE * 9, dv=FAKE * 10,
+             dr=FAKE * 11, du=FAKE * 12, dw=FAKE * 13, ws=FAKE * 14, nws=need, stream=None)
     a.update(kw)
     return abi.load_library().txl_rel_attn_bwd(
-        a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["dout"], a["B"], a["M"], a["L"], a["H"], a["D"],
-        a["dt"], a["dq"], a["dk"], a["dv"], a["dr"], a["du"], a["dw"], a["ws"], a["nws"], a["stream"])
+        a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["dout"], a["out"], a["lse"], a["B"], a["M"],
+        a["L"], a["H"], a["D"], a["dt"], a["dq"], a["dk"], a["dv"], a["dr"], a["du"], a["dw"], a["ws"],
+        a["nws"], a["stream"])
 
 
 def test_bwd_rejects_bad_arguments(lib):
@@ -166,6 +167,31 @@ def test_bwd_rejects_bad_arguments(lib):
     assert _bwd(dq=FAKE) == INVALID                   # dq overlaps q
     assert _bwd(dv=FAKE * 9 + 64) == INVALID          # dv overlaps dk
     assert _bwd(dr=FAKE * 14 + 4096) == INVALID       # dr inside the workspace
+    # the saved forward output and log-sum-exp come together
+    assert _bwd(out=FAKE * 15) == INVALID
+    assert _bwd(lse=FAKE * 16) == INVALID
+    assert _bwd(out=FAKE * 15 + 2, lse=FAKE * 16) == INVALID   # out not 16-byte aligned
+    assert _bwd(out=FAKE * 15, lse=FAKE * 16 + 2) == INVALID   # lse not 4-byte aligned
+    assert _bwd(out=FAKE * 15, lse=FAKE * 16, dq=FAKE * 15) == INVALID   # dq overlaps out
+    assert _bwd(out=FAKE * 15, lse=FAKE * 16, ws=FAKE * 16) == INVALID   # lse inside the workspace
+
+
+def _attn_lse(**kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, r=FAKE * 4, u=FAKE * 5, w=FAKE * 6, B=2, M=8, L=8, H=2,
+             D=16, dt=1, out=FAKE * 7, lse=FAKE * 8, stream=None)
+    a.update(kw)
+    return abi.load_library().txl_rel_attn_fwd_lse(
+        a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["B"], a["M"], a["L"], a["H"], a["D"], a["dt"],
+        a["out"], a["lse"], a["stream"])
+
+
+def test_attn_lse_rejects_bad_arguments(lib):
+    assert _attn_lse(lse=None) == INVALID
+    assert _attn_lse(dt=0) == UNSUPPORTED             # the log-sum-exp comes from the bf16 kernels
+    assert _attn_lse(lse=FAKE * 8 + 2) == INVALID     # misaligned
+    assert _attn_lse(lse=FAKE * 7 + 64) == INVALID    # inside out
+    assert _attn_lse(lse=FAKE * 2 + 16) == INVALID    # inside k
+    assert _attn_lse(B=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None, lse=None) == OK
 
 
 def test_bwd_without_gpu_reports_cuda_error(lib):
@@ -173,4 +199,6 @@ def test_bwd_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present: the call would launch on the fake pointers")
     assert _bwd() == CUDA
+    assert _bwd(out=FAKE * 15, lse=FAKE * 16) == CUDA
+    assert _attn_lse() == CUDA
     assert _bwd(u=None, w=None, du=None, dw=None) == CUDA

@@ -12,7 +12,10 @@ routine or to a closed form:
   angle-difference identities), which pins the sign of i-j and the table order;
 * the segment-recurrence identity (Section 3.2): the memory path equals the
   last L rows of the same attention over the whole concatenated context;
-* reductions to torch's scaled-dot-product attention and to a plain softmax.
+* reductions to torch's scaled-dot-product attention and to a plain softmax;
+* for the row log-sum-exp: a closed form (all scores zero: log of the count of
+  visible keys), torch's logsumexp on textbook attention, and exp(s - lse)
+  against the row's weights.
 
 A final test plants mistakes in copies of the oracle's C source and checks that
 these pins catch every one of them.
@@ -335,6 +338,68 @@ def test_rows_variant_matches_full(oracle_lib):
         assert np.array_equal(got[x], full[i, b, h])
 
 
+def _lse_textbook(q, k, L, M):
+    """torch log-sum-exp of the masked scaled dot products, float64."""
+    qt = torch.from_numpy(np.ascontiguousarray(q.transpose(1, 2, 0, 3)))
+    kt = torch.from_numpy(np.ascontiguousarray(k.transpose(1, 2, 0, 3)))
+    s = qt @ kt.transpose(-1, -2) / np.sqrt(q.shape[-1])
+    s = s.masked_fill(~torch.from_numpy(_visible(L, M)), float("-inf"))
+    return torch.logsumexp(s, dim=-1).numpy()
+
+
+def _lse_pins_pass(mod):
+    # no key and no table content: every visible score is 0, so row i's
+    # denominator is its count of visible keys, M + i + 1
+    B, H, D, L, M = 2, 2, 4, 5, 3
+    p, _ = _problem(B, H, D, L, M, seed=61)
+    p["k"][:] = 0.0
+    p["r"][:] = 0.0
+    _, lse = mod.rel_attn(**p, mem_len=M, return_lse=True)
+    if not np.allclose(lse, np.log(M + 1 + np.arange(L))[None, None], rtol=0, atol=1e-12):
+        return False
+    # no position term and no biases: the log-sum-exp of textbook attention
+    p, _ = _problem(B, H, D, L, M, seed=62)
+    p["q"] *= 3.0                                        # rows with a clear maximum
+    p["r"][:] = 0.0
+    p["u"][:] = 0.0
+    p["w"][:] = 0.0
+    _, lse = mod.rel_attn(**p, mem_len=M, return_lse=True)
+    return np.allclose(lse, _lse_textbook(p["q"], p["k"], L, M), rtol=0, atol=1e-12)
+
+
+def test_lse_pins(oracle_lib):
+    assert _lse_pins_pass(oracle)
+
+
+def test_lse_matches_its_probabilities(oracle_lib):
+    """P_ij = exp(s_ij - lse_i) on the full four-term score of a single query
+    row written out by hand."""
+    B, H, D, L, M = 2, 2, 5, 1, 9
+    p, _ = _problem(B, H, D, L, M, seed=63)
+    _, prob, lse = oracle.rel_attn(**p, mem_len=M, return_prob=True, return_lse=True)
+    T = M + L
+    for b in range(B):
+        for hd in range(H):
+            s = np.array([((p["q"][0, b, hd] + p["u"][hd]) @ p["k"][j, b, hd]
+                           + (p["q"][0, b, hd] + p["w"][hd]) @ p["r"][T - 1 - (M - j), hd])
+                          for j in range(T)]) / np.sqrt(D)
+            np.testing.assert_allclose(np.exp(s - lse[b, hd, 0]), prob[b, hd, 0], rtol=0, atol=TOL)
+
+
+LSE_MUTANTS = {
+    "lse_without_max": ("*lse_out = mx + log(z);", "*lse_out = log(z);"),
+    "lse_of_max_only": ("*lse_out = mx + log(z);", "*lse_out = mx;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LSE_MUTANTS))
+def test_lse_pins_catch_planted_mistake(tmp_path, name):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc missing")
+    mod = _build_mutant(tmp_path, name)
+    assert not _lse_pins_pass(mod), f"planted mistake {name!r} went unnoticed"
+
+
 # ---------------------------------------------------------------------------
 # 7. Memory rollover (Section 3.2): newest M rows of [memory; segment]
 # ---------------------------------------------------------------------------
@@ -374,7 +439,7 @@ MUTANTS = {
 
 def _build_mutant(tmp_path, name):
     src = open(os.path.join(os.path.dirname(oracle.__file__), "txl_oracle.c")).read()
-    old, new = MUTANTS[name]
+    old, new = {**MUTANTS, **LSE_MUTANTS}[name]
     assert old in src, f"mutation anchor for {name} no longer in the oracle source"
     mdir = tmp_path / name
     mdir.mkdir()

@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace")
+           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse")
 
 
 class TxlError(RuntimeError):
@@ -51,6 +51,8 @@ def load_library() -> ctypes.CDLL:
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.txl_rel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd.restype = i
+    lib.txl_rel_attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
+    lib.txl_rel_attn_fwd_lse.restype = i
     lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd_noalloc.restype = i
     lib.txl_rel_attn_fwd_ring.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
@@ -65,7 +67,7 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_table.restype = i
     lib.txl_rel_attn_bwd_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.txl_rel_attn_bwd_workspace.restype = i
-    lib.txl_rel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+    lib.txl_rel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                      vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.txl_rel_attn_bwd.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
@@ -139,21 +141,33 @@ def _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out):
     return out
 
 
-def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None):
+def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None, lse=None):
     """Relative attention of one layer (Transformer-XL Section 3.3).
 
     q: [L, B, H, D]; k, v: [M+L, B, H, D]; r: [M+L, H, D] (reversed table);
     u_bias, v_bias: [H, D] float32, or None to drop that bias term (both
     None: Shaw et al.'s form, terms (a) + (b) only); all CUDA, contiguous,
     same dtype (float32 or bfloat16) except the biases.  Returns ``out``
-    [L, B, H, D].
+    [L, B, H, D].  ``lse`` (bfloat16 inputs only): a contiguous float32 CUDA
+    tensor [B, H, L] that receives each query row's log-sum-exp of its
+    scaled scores (txl_rel_attn_fwd_lse), to hand to ``rel_attn_bwd``.
     """
+    import torch
     L, B, H, D = q.shape
     out = _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
-    st = load_library().txl_rel_attn_fwd(
+    if lse is None:
+        st = load_library().txl_rel_attn_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+            B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _stream_ptr(stream))
+        _raise(st, "txl_rel_attn_fwd")
+        return out
+    if tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32 or not lse.is_cuda \
+            or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 CUDA tensor [{B}, {H}, {L}]")
+    st = load_library().txl_rel_attn_fwd_lse(
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
-        B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _stream_ptr(stream))
-    _raise(st, "txl_rel_attn_fwd")
+        B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _ptr(lse), _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_lse")
     return out
 
 
@@ -168,13 +182,16 @@ def rel_attn_bwd_workspace_bytes(batch: int, mem_len: int, seg_len: int, heads: 
 
 
 def rel_attn_bwd(q, k, v, r, u_bias, v_bias, dout, mem_len: int, workspace=None, grads=None,
-                 bias_grads: bool = True, stream=None):
+                 bias_grads: bool = True, stream=None, out=None, lse=None):
     """Gradients of ``rel_attn_fwd`` for the output gradient ``dout`` (shaped
     like q).  Returns a dict ``dq, dk, dv, dr`` (shaped and typed like q, k,
     v, r) and ``du, dw`` (float32 [H, D]; None when ``bias_grads`` is False).
     ``workspace``: a CUDA uint8 tensor of at least
     ``rel_attn_bwd_workspace_bytes`` bytes (allocated when None); ``grads``:
-    preallocated outputs with the same keys."""
+    preallocated outputs with the same keys.  ``out``, ``lse``: the forward's
+    output and row log-sum-exp from ``rel_attn_fwd(..., lse=...)`` on the
+    same inputs (both or neither); given, the backward skips its own
+    forward."""
     import torch
     L, B, H, D = q.shape
     _check_attn(q, k, v, r, u_bias, v_bias, mem_len, q)
@@ -189,13 +206,22 @@ def rel_attn_bwd(q, k, v, r, u_bias, v_bias, dout, mem_len: int, workspace=None,
             grads["dw"] = torch.empty((H, D), dtype=torch.float32, device=q.device)
     grads.setdefault("du", None)
     grads.setdefault("dw", None)
+    if (out is None) != (lse is None):
+        raise ValueError("out and lse come together or not at all")
+    if out is not None:
+        if tuple(out.shape) != (L, B, H, D) or out.dtype != q.dtype or not out.is_cuda \
+                or not out.is_contiguous():
+            raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+        if tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32 or not lse.is_cuda \
+                or not lse.is_contiguous():
+            raise ValueError(f"lse must be a contiguous float32 CUDA tensor [{B}, {H}, {L}]")
     nbytes = rel_attn_bwd_workspace_bytes(B, mem_len, L, H, D, _dtype_code(q))
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     elif workspace.numel() * workspace.element_size() < nbytes:
         raise ValueError(f"workspace must hold {nbytes} bytes")
     st = load_library().txl_rel_attn_bwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias), _ptr(dout),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias), _ptr(dout), _ptr(out), _ptr(lse),
         B, mem_len, L, H, D, _dtype_code(q),
         _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dr"]),
         _ptr(grads["du"]), _ptr(grads["dw"]), _ptr(workspace),

@@ -130,7 +130,7 @@ extern "C" {
 static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
                                   const float *u_bias, const float *v_bias, int batch, int mem_len,
                                   int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
-                                  void *out, void *stream, int scale_d = 0)
+                                  void *out, void *stream, int scale_d = 0, float *lse = nullptr)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
@@ -156,6 +156,14 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
         overlaps(out, nq, r, nr) || overlaps(out, nq, u_bias, nb) || overlaps(out, nq, v_bias, nb))
         return TXL_ERR_INVALID;
     if ((seg_len + 31) / 32 > 65535) return TXL_ERR_UNSUPPORTED;
+    if (lse) {
+        // the row log-sum-exp comes from the bf16 kernels
+        if (dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+        const size_t nl = (size_t)batch * heads * seg_len * 4;
+        if (!aligned(lse, 4) || overlaps(lse, nl, out, nq) || overlaps(lse, nl, q, nq) || overlaps(lse, nl, k, nk) ||
+            overlaps(lse, nl, v, nk) || overlaps(lse, nl, r, nr))
+            return TXL_ERR_INVALID;
+    }
 
     // an absent bias drops its term (terms (a) + (b) only: Shaw et al.'s form)
     if (!u_bias || !v_bias) {
@@ -167,6 +175,7 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
         if (!v_bias) v_bias = z;
     }
     AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len, kv_start, scale_d};
+    a.lse = lse;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     if (dtype == TXL_F32) {
@@ -228,6 +237,15 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
 {
     return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0,
                            dtype, out, stream);
+}
+
+txl_status txl_rel_attn_fwd_lse(const void *q, const void *k, const void *v, const void *r,
+                                const float *u_bias, const float *v_bias, int batch, int mem_len, int seg_len,
+                                int heads, int d_head, txl_dtype dtype, void *out, float *lse, void *stream)
+{
+    if (!lse && batch > 0 && seg_len > 0 && heads > 0) return TXL_ERR_INVALID;
+    return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0, dtype, out,
+                           stream, 0, lse);
 }
 
 txl_status txl_rel_attn_fwd_padded(const void *q, const void *k, const void *v, const void *r,

@@ -70,6 +70,7 @@ constexpr uint32_t REG_LOW = 96, REG_HIGH = 200;     // per-thread registers aft
 static_assert(128 * REG_LOW + 256 * REG_HIGH <= 65536 / NT / 8 * 8 * NT, "register split exceeds the launch");
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait, then give up
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
 constexpr float SUM_LIMIT = 4096.0f;          // raise the exponent base once a row sum passes 2^12
 
 struct Params {
@@ -78,7 +79,7 @@ struct Params {
     __nv_bfloat16 *out;
     float *part_o;      // [splits][B*H][L][DP] when splits > 1
     float *part_lse;    // [splits][B*H][L]
-    float *lse;         // optional [B*H][L]: each row's log-sum-exp (log2 units of the scaled score)
+    float *lse;         // optional [B*H][L]: each row's log-sum-exp (natural log) of the scaled scores
     // backward scores only (the forward's output O comes in `out`): dO, the
     // outputs P and dA ([B*H][L][TP]) and dA in the table frame
     // ([H][L][B][TP]), 1/sqrt(d_head)
@@ -762,7 +763,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int d0 = DH * half;
             const int i = dn.i0 + ii;
             if (p.lse && p.splits == 1 && half == 0 && ii < dn.rows_here)
-                p.lse[(long)dn.bh * p.L + i] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
+                p.lse[(long)dn.bh * p.L + i] = l > 0.f ? (dn.m + log2f(l)) * LN2 : -INFINITY;
             if (kTma && p.ost) {
                 // the 128 x 64 tile goes through shared memory (the tensor
                 // map's swizzled layout) and out by one TMA store, issued by
@@ -1241,7 +1242,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
             Item nx;
             const int jn = next_busy(p, j + 1, nx);
             const long row = (long)it.bh * p.L + i;   // this thread's row of the [B*H][L] matrices
-            const float lse = row_valid ? p.lse[row] : 0.f;
+            const float lse = row_valid ? p.lse[row] * LOG2E : 0.f;   // log2 units of the scaled score
             // the table-frame matrix is head-major, [H][L][B][TP]: row (i, b) of
             // head h, so that one GEMM per head contracts over (i, b)
             auto db_row = [&](int ir) { return (((long)it.h * p.L + ir) * p.B + it.b) * rowpitch; };
@@ -1436,7 +1437,7 @@ rel_attn_combine_kernel(const float *__restrict__ part_o, const float *__restric
             const float lse = part_lse[s * BHL + (long)bh * L + i];
             w += (lse == -INFINITY) ? 0.f : exp2f(lse - mx);
         }
-        lse_out[(long)bh * L + i] = w > 0.f ? mx + log2f(w) : -INFINITY;
+        lse_out[(long)bh * L + i] = w > 0.f ? (mx + log2f(w)) * LN2 : -INFINITY;
     }
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float acc = 0.f, wsum = 0.f;

@@ -498,9 +498,9 @@ cuda_fail:
 }
 
 txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void *r, const float *u,
-                         const float *w, const void *dout, int B, int M, int L, int H, int D, void *dq, void *dk,
-                         void *dv, void *dr, float *du, float *dw, unsigned char *ws, const WsF &lay,
-                         cudaStream_t s)
+                         const float *w, const void *dout, const void *out_saved, const float *lse_saved, int B,
+                         int M, int L, int H, int D, void *dq, void *dk, void *dv, void *dr, float *du, float *dw,
+                         unsigned char *ws, const WsF &lay, cudaStream_t s)
 {
     typedef __nv_bfloat16 E;
     const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, ld = BH * D, TP = lay.TP;
@@ -515,7 +515,8 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
         e = cudaGetLastError();
         return e == cudaSuccess;
     };
-    // the forward (its output and row log-sum-exp)
+    // the forward's output and row log-sum-exp: the caller's saved ones, or
+    // the forward once more
     AttnArgs a{};
     a.q = q;
     a.k = k;
@@ -530,8 +531,13 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
     a.L = L;
     a.M = M;
     a.lse = lse;
-    if ((e = launch_attn_bf16(a, lay.splits, lay.splits > 1 ? ws + lay.split : nullptr, s)) != cudaSuccess)
+    if (out_saved && lse_saved) {
+        a.out = const_cast<void *>(out_saved);
+        a.lse = const_cast<float *>(lse_saved);
+        lse = a.lse;
+    } else if ((e = launch_attn_bf16(a, lay.splits, lay.splits > 1 ? ws + lay.split : nullptr, s)) != cudaSuccess) {
         goto cuda_fail;
+    }
     if ((e = launch_bwd_scores(a, dout, lse, pb, dab, dbb, TP, s)) != cudaSuccess) goto cuda_fail;
     // the GEMM operands q+u, q+v
     bwd_fold_vec_kernel<E><<<grid_for(nq / 8, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / 8, H, D);
@@ -610,9 +616,10 @@ txl_status txl_rel_attn_bwd_workspace(int batch, int mem_len, int seg_len, int h
 }
 
 txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const void *r, const float *u_bias,
-                            const float *v_bias, const void *dout, int batch, int mem_len, int seg_len, int heads,
-                            int d_head, txl_dtype dtype, void *dq, void *dk, void *dv, void *dr, float *du,
-                            float *dw, void *workspace, size_t workspace_bytes, void *stream)
+                            const float *v_bias, const void *dout, const void *out, const float *lse, int batch,
+                            int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype, void *dq, void *dk,
+                            void *dv, void *dr, float *du, float *dw, void *workspace, size_t workspace_bytes,
+                            void *stream)
 {
     const txl_status st = check_sizes(batch, mem_len, seg_len, heads, d_head, dtype);
     if (st != TXL_OK) return st;
@@ -628,6 +635,9 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     const void *ins[] = {q, k, v, r, dout, dq, dk, dv, dr};
     for (const void *x : ins)
         if ((uintptr_t)x % es) return TXL_ERR_INVALID;
+    // the forward's saved output and row log-sum-exp come together or not at all
+    if ((out == nullptr) != (lse == nullptr)) return TXL_ERR_INVALID;
+    if (out && (((uintptr_t)out & 15) || ((uintptr_t)lse & 3))) return TXL_ERR_INVALID;
     if (((uintptr_t)u_bias & 3) || ((uintptr_t)v_bias & 3) || ((uintptr_t)du & 3) || ((uintptr_t)dw & 3))
         return TXL_ERR_INVALID;
     const long T = (long)mem_len + seg_len;
@@ -636,16 +646,17 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     // outputs must not overlap the inputs, each other or the workspace
     const void *outs[] = {dq, dk, dv, dr, du, dw};
     const size_t osz[] = {nq, nk, nk, nr, nb, nb};
-    const void *rd[] = {q, k, v, r, dout, u_bias, v_bias, workspace};
-    const size_t rsz[] = {nq, nk, nk, nr, nq, nb, nb, need};
+    const size_t nl = (size_t)batch * heads * seg_len * 4;
+    const void *rd[] = {q, k, v, r, dout, u_bias, v_bias, workspace, out, lse};
+    const size_t rsz[] = {nq, nk, nk, nr, nq, nb, nb, need, nq, nl};
     for (int a = 0; a < 6; ++a) {
-        for (int b = 0; b < 8; ++b)
+        for (int b = 0; b < 10; ++b)
             if (overlaps(outs[a], osz[a], rd[b], rsz[b])) return TXL_ERR_INVALID;
         for (int b = a + 1; b < 6; ++b)
             if (overlaps(outs[a], osz[a], outs[b], osz[b])) return TXL_ERR_INVALID;
     }
-    for (int b = 0; b < 7; ++b)
-        if (overlaps(workspace, need, rd[b], rsz[b])) return TXL_ERR_INVALID;
+    for (int b = 0; b < 10; ++b)
+        if (b != 7 && overlaps(workspace, need, rd[b], rsz[b])) return TXL_ERR_INVALID;
     // absent biases: the zero vector (their gradients are still reported when asked)
     const float *uu = u_bias, *ww = v_bias;
     if (!uu || !ww) {
@@ -666,8 +677,8 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
                               dw, wsb, lay, s, false);
     const void *al[] = {q, k, v, r, dout, uu, ww};
     if (fused_ok(d_head, al, 7))
-        return run_bwd_fused(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr, du, dw,
-                             wsb, layout_fused(batch, heads, d_head, seg_len, mem_len), s);
+        return run_bwd_fused(q, k, v, r, uu, ww, dout, out, lse, batch, mem_len, seg_len, heads, d_head, dq, dk, dv,
+                             dr, du, dw, wsb, layout_fused(batch, heads, d_head, seg_len, mem_len), s);
     return run_bwd<__nv_bfloat16>(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr,
                                   du, dw, wsb, lay, s, true);
 }

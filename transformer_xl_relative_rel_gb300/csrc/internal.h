@@ -15,7 +15,7 @@ struct AttnArgs {
     int B, H, D, L, M;
     int kv_start = 0;             // K, V in a ring of M+L rows: key j at row (kv_start + j) mod (M+L)
     int scale_d = 0;              // d_head for the 1/sqrt(d_head) scale when D is a padded width (0: D)
-    float *lse = nullptr;         // bf16 path, optional [B*H][L]: row log-sum-exp, log2 units of the scaled score
+    float *lse = nullptr;         // bf16 path, optional [B*H][L]: row log-sum-exp (natural log) of the scaled scores
 };
 
 // fp32 SIMT path (attn_f32.cu)
