@@ -5,35 +5,35 @@
 //     out_i = softmax_j(s_ij) v_j,
 // with Q the reversed projected table of Appendix B (row t = W_kR R_{T-1-t}).
 //
-// One CTA owns 128 query rows of one (b, h) -- or one key-range split of them
-// -- and walks its keys in tiles of 128.  Twelve warps with fixed roles:
-//   warp 0     producer: TMA loads of K, V and one 128-row chunk of the table
-//              per tile into a three-stage shared-memory ring (128-byte rows,
-//              128-byte swizzle); for head sizes other than 64, coalesced
-//              thread loads (warp 0: K and the table, warp 3: V);
-//   warp 1     one thread issues, per tile, S = (q+u) K^T (N = 128) into the
-//              TMEM S buffer and the next band chunk (q+v) Q_chunk^T (N = 128)
-//              into a two-slot TMEM ring;
-//   warp 2     one thread issues O += P V with P read from TMEM;
-//   warps 4-11 softmax: the two warps of a TMEM lane quadrant share its 32
-//              query rows (one row per thread), warps 4-7 take keys 0-63 of
-//              the tile and warps 8-11 keys 64-127.  Each thread loads its S
-//              columns and the 96-column band window its row needs in one
-//              batch (the S buffer is free for the next tile's MMAs right
-//              after), aligns the band to the row (Appendix B's left shift of
-//              row i by L-1-i, a register barrel shift by 31-lane on fp16
-//              pairs), adds, masks j <= M+i, trades its partial row max with
-//              the partner warp through shared memory, and writes P (bf16) to
-//              TMEM for the P.V MMA.
-// Appendix B's table product is formed once per 128-row chunk: tile n uses
-// chunks n and n+1 of the band and computes chunk n+1 itself, so the position
-// term costs the same tensor work as the content term.  The S and band MMAs of
-// tile n+1 run while the softmax of tile n runs.  The running max used for the
-// exponentials is raised only when a row's max grows by more than 8 (log2
-// units); O in TMEM is rescaled only then.  The scale log2(e)/sqrt(D) is
-// folded into q+u and q+v before rounding.  Every mbarrier wait is bounded; on
-// expiry the CTA records an error word (read by txl_check) and every role
-// winds down.
+// Persistent: one CTA of twelve warps per SM walks work items (128 query
+// rows of one (b, h), or one key-range split of them) heaviest first, and
+// each item's keys in tiles of 128.  Roles:
+//   warp 0     producer: TMA loads of K, V into a three-stage shared-memory
+//              ring, of 128-row table chunks into a four-slot ring, and of
+//              the next item's raw q rows and biases (for head sizes other
+//              than 64: coalesced thread loads, warp 3 taking V);
+//   warp 1     one thread issues, per tile, S = (q+u) K^T (N = 128) and the
+//              tile's band window (q+v) [chunk n; chunk n+1]^T (256 columns)
+//              into TMEM, their K steps interleaved;
+//   warp 2     one thread issues O += P V with P read from TMEM, and the TMA
+//              store of each finished output tile;
+//   warps 4-11 softmax on the 16-lane TMEM shape: a warp owns 16 query rows;
+//              lanes 0-15 take keys 0-63 of the tile, lanes 16-31 keys
+//              64-127 of the same rows.  Each thread loads its 64 S columns
+//              and the 80 band columns its row needs in one batch (S and the
+//              band are then free for the next tile's MMAs), aligns the band
+//              to the row (Appendix B's left shift of row i by L-1-i: a
+//              barrel shift by 15 - (row mod 16) on fp16 pairs), adds it,
+//              masks j <= M+i on diagonal tiles, exponentiates against the
+//              row's running reference max and writes P (bf16) to TMEM.
+// TMEM (512 columns): S 128, band window 256, P 64, O 64.  The band window
+// costs twice the position term's pairs: a window of two 128-row chunks keeps
+// each 16-row group's 80 columns contiguous for the load's fixed half-split
+// offset.  The reference max is raised (and O in TMEM rescaled) on an item's
+// first tile, on diagonal tiles and when a row's sum passes 2^12.  The scale
+// log2(e)/sqrt(D) is folded into q+u and q+v before rounding.  Every mbarrier
+// wait is bounded; on expiry the CTA records an error word (read by
+// txl_check) and every role winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
