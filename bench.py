@@ -303,7 +303,12 @@ def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
     """The same step through the public API with the inputs in pinned host
     memory: every step copies each layer's q, k, v, r, biases and extended
     context host->device, runs the calls, and reads the last layer's output
-    back.  Timed with CUDA events around the whole step."""
+    back.  Timed with CUDA events around the whole step.
+
+    The copies run on a second stream, one layer ahead: a layer's copies wait
+    (event) until that layer's previous calls have finished with its device
+    buffers, and its calls wait (event) for its copies, so the host link
+    (the bound: every input crosses it) never waits for the kernels."""
     host = []
     for lay in chain.layers:
         host.append({key: lay[key].cpu().pin_memory() for key in ("q", "k", "v", "r", "u", "w")}
@@ -313,14 +318,26 @@ def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
     h2d = sum(t.numel() * t.element_size() for hl in host for t in hl.values()) * w.segments
     d2h = out_host.numel() * out_host.element_size()
 
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    nl = len(chain.layers)
+    copied = [torch.cuda.Event() for _ in range(nl)]   # a layer's inputs are on the device
+    used = [torch.cuda.Event() for _ in range(nl)]     # a layer's calls are done with its buffers
+
     def one():
+        side.wait_stream(main)      # nothing of a step starts before the step's start event
         for _seg in range(w.segments):
-            for lay, hl in zip(chain.layers, host):
-                for key in ("q", "k", "v", "r", "u", "w"):
-                    lay[key].copy_(hl[key], non_blocking=True)
-                lay["ext"][0].copy_(hl["ext"], non_blocking=True)
+            for n, (lay, hl) in enumerate(zip(chain.layers, host)):
+                side.wait_event(used[n])
+                with torch.cuda.stream(side):
+                    for key in ("q", "k", "v", "r", "u", "w"):
+                        lay[key].copy_(hl[key], non_blocking=True)
+                    lay["ext"][0].copy_(hl["ext"], non_blocking=True)
+                    copied[n].record(side)
+                main.wait_event(copied[n])
                 chain.attn(txl, lay)
                 chain.memory(txl, lay)
+                used[n].record(main)
         out_host.copy_(chain.layers[-1]["out"], non_blocking=True)
 
     one()
