@@ -275,31 +275,45 @@ __global__ void __launch_bounds__(RB) bwd_score_grad_row_kernel(const float *__r
     }
 }
 
-// dq = dQ_content + dQ_position in the output type
+// dq = dQ_content + dQ_position in the output type, and in the same pass the
+// bias gradients: du[h][d] += the column sum over rows (i, b) of the content
+// part, dw[h][d] likewise of the position part (du, dw zeroed before; either
+// may be NULL).  Grid (row chunks, column slabs of blockDim.x); a thread owns
+// one column of the [L*B][H*D] matrices and strides over the rows.
 template <typename T>
-__global__ void bwd_sum_kernel(const float *__restrict__ a, const float *__restrict__ b, T *__restrict__ out,
-                               long n)
+__global__ void bwd_sum_bias_kernel(const float *__restrict__ a, const float *__restrict__ b, T *__restrict__ out,
+                                    float *__restrict__ du, float *__restrict__ dw, long rows, int hd)
 {
-    for (long x = (long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
-        out[x] = from_f<T>(a[x] + b[x]);
+    const int c = blockIdx.y * blockDim.x + threadIdx.x;
+    if (c >= hd) return;
+    float su = 0.f, sw = 0.f;
+    for (long rr = blockIdx.x; rr < rows; rr += gridDim.x) {
+        const long x = rr * hd + c;
+        const float va = a[x], vb = b[x];
+        out[x] = from_f<T>(va + vb);
+        su += va;
+        sw += vb;
+    }
+    if (du) atomicAdd(du + c, su);
+    if (dw) atomicAdd(dw + c, sw);
 }
 
-// du[h] += sum over rows (i, b) of the content part of dq, dw[h] likewise of
-// the position part; grid (row chunks, H), one thread per d
-__global__ void bwd_bias_grad_kernel(const float *__restrict__ dqc, const float *__restrict__ dqp,
-                                     float *__restrict__ du, float *__restrict__ dw, long rows, int H, int D)
+// bwd_sum_bias_kernel with du, dw zeroed first: about eight blocks of 256
+// threads per SM over the column slabs, so that each thread streams a few
+// dozen rows (enough loads in flight) and each column takes few atomics
+template <typename T>
+cudaError_t launch_sum_bias(const float *dqc, const float *dqp, T *dq, float *du, float *dw, long rows, int hd,
+                            cudaStream_t s)
 {
-    const int h = blockIdx.y;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float su = 0.f, sw = 0.f;
-        for (long rr = blockIdx.x; rr < rows; rr += gridDim.x) {
-            const long o = (rr * H + h) * D + d;
-            su += dqc[o];
-            sw += dqp[o];
-        }
-        if (du) atomicAdd(du + h * D + d, su);
-        if (dw) atomicAdd(dw + h * D + d, sw);
-    }
+    cudaError_t e;
+    if (du && (e = cudaMemsetAsync(du, 0, (size_t)hd * 4, s)) != cudaSuccess) return e;
+    if (dw && (e = cudaMemsetAsync(dw, 0, (size_t)hd * 4, s)) != cudaSuccess) return e;
+    const int slabs = (hd + 255) / 256;
+    long chunks = 8L * device_sm_count() / slabs;
+    if (chunks > rows) chunks = rows;
+    if (chunks < 1) chunks = 1;
+    bwd_sum_bias_kernel<T><<<dim3((unsigned)chunks, (unsigned)slabs), 256, 0, s>>>(dqc, dqp, dq, du, dw, rows, hd);
+    return cudaGetLastError();
 }
 
 // dr[t][h][d] = sum_b part[(b*H + h)*T + t][d]
@@ -476,19 +490,7 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
             gemm_rm(hd, true, false, Ti, D, L, dbb, T, LT, qv, ld, D, drp, D, TD, nb, ty, CUDA_R_32F))
             return TXL_ERR_CUDA;
     }
-    bwd_sum_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>(dqc, dqp, (E *)dq, nq);
-    if (!chk()) goto cuda_fail;
-    if (du || dw) {
-        if (du && (e = cudaMemsetAsync(du, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
-        if (dw && (e = cudaMemsetAsync(dw, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
-        // about 16 rows per block: enough blocks in flight to stream the two
-        // fp32 halves of dq at bandwidth
-        const long brows = (long)L * B;
-        const unsigned chunks = (unsigned)(brows / 16 < 1 ? 1 : (brows / 16 > 4096 ? 4096 : brows / 16));
-        bwd_bias_grad_kernel<<<dim3(chunks, (unsigned)H), D <= 64 ? 64 : 128, 0, s>>>(dqc, dqp, du, dw, brows, H,
-                                                                                     D);
-        if (!chk()) goto cuda_fail;
-    }
+    if ((e = launch_sum_bias<E>(dqc, dqp, (E *)dq, du, dw, (long)L * B, H * D, s)) != cudaSuccess) goto cuda_fail;
     bwd_table_grad_kernel<E><<<grid_for(T * H * D, 256), 256, 0, s>>>(drp, (E *)dr, B, H, D, (int)T);
     if (!chk()) goto cuda_fail;
     return TXL_OK;
@@ -556,16 +558,8 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
             gemm_rm(hd, true, false, Ti, D, LB, dbb, TP, LBTP, qv, HD, D, dr, HD, D, H, CUDA_R_16BF, CUDA_R_16BF))
             return TXL_ERR_CUDA;
     }
-    bwd_sum_kernel<E><<<grid_for(nq, 256), 256, 0, s>>>(dqc, dqp, (E *)dq, nq);
-    if (!chk()) goto cuda_fail;
-    if (du || dw) {
-        if (du && (e = cudaMemsetAsync(du, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
-        if (dw && (e = cudaMemsetAsync(dw, 0, (size_t)H * D * 4, s)) != cudaSuccess) goto cuda_fail;
-        const long brows = (long)L * B;
-        const unsigned chunks = (unsigned)(brows / 16 < 1 ? 1 : (brows / 16 > 4096 ? 4096 : brows / 16));
-        bwd_bias_grad_kernel<<<dim3(chunks, (unsigned)H), 64, 0, s>>>(dqc, dqp, du, dw, brows, H, D);
-        if (!chk()) goto cuda_fail;
-    }
+    // dq and the bias gradients in one pass over the two fp32 halves of dq
+    if ((e = launch_sum_bias<E>(dqc, dqp, (E *)dq, du, dw, (long)L * B, H * D, s)) != cudaSuccess) goto cuda_fail;
     return TXL_OK;
 cuda_fail:
     note_cuda_error(e);
