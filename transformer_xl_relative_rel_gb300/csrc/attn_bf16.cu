@@ -186,6 +186,18 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 
 __device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_err_word, code); }
 
@@ -1324,20 +1336,36 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
 #pragma unroll
                     for (int y = 0; y < 64; ++y) x[y] = (y <= lim) ? x[y] : -INFINITY;
                 }
-                // P from the forward's log-sum-exp (0 where masked)
+                // P from the forward's log-sum-exp (0 where masked); the
+                // subtraction on element pairs
+                {
+                    const uint64_t lse2 = f2(lse, lse);
 #pragma unroll
-                for (int y = 0; y < 64; ++y) x[y] = ex2(x[y] - lse);
+                    for (int y = 0; y < 32; ++y) {
+                        float e0, e1;
+                        unf2(sub2(f2(x[2 * y], x[2 * y + 1]), lse2), e0, e1);
+                        x[2 * y] = ex2(e0);
+                        x[2 * y + 1] = ex2(e1);
+                    }
+                }
                 float dp[64];
                 tmem_ld_h64<HN>(tl + TM_DP, tl + TM_DP + 32, dp);
                 tc_fence_before();
                 mbar_arrive(bar(S::B_SF));
                 uint32_t pp[32], aa[32];   // this row's P and dA, bf16 pairs
+                {
+                    // dA = P (dP - delta) / sqrt(D) = P (dP c - delta c), c = 1/sqrt(D),
+                    // on element pairs
+                    const float c = p.inv_sqrt_d;
+                    const uint64_t c2 = f2(c, c), ndc2 = f2(-delta * c, -delta * c);
 #pragma unroll
-                for (int y = 0; y < 32; ++y) {
-                    const float a0 = x[2 * y] * (dp[2 * y] - delta) * p.inv_sqrt_d;
-                    const float a1 = x[2 * y + 1] * (dp[2 * y + 1] - delta) * p.inv_sqrt_d;
-                    pp[y] = pack_bf16(x[2 * y], x[2 * y + 1]);
-                    aa[y] = pack_bf16(a0, a1);
+                    for (int y = 0; y < 32; ++y) {
+                        const uint64_t x2 = f2(x[2 * y], x[2 * y + 1]);
+                        float a0, a1;
+                        unf2(mul2(x2, fma2(f2(dp[2 * y], dp[2 * y + 1]), c2, ndc2)), a0, a1);
+                        pp[y] = pack_bf16(x[2 * y], x[2 * y + 1]);
+                        aa[y] = pack_bf16(a0, a1);
+                    }
                 }
                 // P and dA go out through the warp's staging tile: a thread
                 // stages its row's 64 values, then two rows per store
