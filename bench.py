@@ -182,10 +182,12 @@ class Chain:
     u, v-bias, the attention output and two extended-context buffers
     [M+L, B, d_model] that trade places every segment."""
 
-    def __init__(self, w: Workload, device, ring: bool = False, pad: int = 0):
+    def __init__(self, w: Workload, device, ring: bool = False, pad: int = 0, fused: bool = False):
         s = w.shape
         self.w = w
         self.ring = ring
+        # attention and rollover of a layer in one call (txl_rel_attn_fwd_mem)
+        self.fused = fused and not ring and not (pad and pad != s.d_head)
         self.pad = pad if pad and pad != s.d_head else 0
         self.dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         B, H, D, L, M, T, dm = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len, s.klen, s.d_model
@@ -225,20 +227,34 @@ class Chain:
         torch.cuda.synchronize()
 
     def step(self, txl, attn_events=None):
-        M, L = self.w.shape.mem_len, self.w.shape.seg_len
-        T = M + L
         launches = 0
         for _seg in range(self.w.segments):
             for lay in self.layers:
-                if attn_events is not None:
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                self.attn(txl, lay)
-                if attn_events is not None:
-                    e1.record()
-                    attn_events.append((e0, e1))
-                launches += 1 + self.attn_extra_launches + self.memory(txl, lay)
+                launches += self.layer(txl, lay, attn_events)
         return launches
+
+    def layer(self, txl, lay, attn_events=None) -> int:
+        """One layer of one segment: the attention call and the memory
+        update, in one library call when the chain is fused (the events
+        then bracket both); returns the kernels launched."""
+        if attn_events is not None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        if self.fused:
+            M = self.w.shape.mem_len
+            txl.rel_attn_fwd_mem(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"], mem_len=M,
+                                 mem_next=lay["ext"][1], ext_ctx=lay["ext"][0], out=lay["out"])
+            lay["ext"].reverse()
+            mem_launches = 0 if self.rollover_in_attention else 1
+        else:
+            self.attn(txl, lay)
+            mem_launches = None
+        if attn_events is not None:
+            e1.record()
+            attn_events.append((e0, e1))
+        if mem_launches is None:
+            mem_launches = self.memory(txl, lay)
+        return 1 + self.attn_extra_launches + mem_launches
 
     def attn(self, txl, lay):
         """The layer's attention call in this chain's storage mode."""
@@ -279,6 +295,31 @@ class Chain:
         return tot
 
     attn_extra_launches = 0
+    rollover_in_attention = False
+
+
+def rollover_fuses(w: Workload, splits: int) -> bool:
+    """Mirror of the library's choice to do the rollover inside the
+    attention launch (for the launch count only): bf16, d_head 64, 16-byte
+    rows, and a CTA's share of the copy at 8 GB/s within half of its share
+    of the tiles at 1.6 us each."""
+    s = w.shape
+    if w.dtype != "bf16" or s.d_head != 64:
+        return False
+    row = s.batch * s.d_model * 2
+    nbytes = s.mem_len * row
+    if (s.seg_len * row) % 16 or nbytes % 16 or nbytes == 0:
+        return False
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    nqt = (s.seg_len + 127) // 128
+    items = s.batch * s.heads * nqt * splits
+    G = min(items, sms)
+    tiles = 0.0
+    for qt in range(nqt):
+        kend = s.mem_len + qt * 128 + min(128, s.seg_len - qt * 128)
+        tiles += (kend + 127) // 128 + splits
+    tiles *= s.batch * s.heads / G
+    return nbytes / G / 8e3 <= 0.5 * tiles * 1.6
 
 
 def splits_for(w: Workload) -> int:
@@ -335,8 +376,7 @@ def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
                     lay["ext"][0].copy_(hl["ext"], non_blocking=True)
                     copied[n].record(side)
                 main.wait_event(copied[n])
-                chain.attn(txl, lay)
-                chain.memory(txl, lay)
+                chain.layer(txl, lay)
                 used[n].record(main)
         out_host.copy_(chain.layers[-1]["out"], non_blocking=True)
 
@@ -396,11 +436,14 @@ def oracle_rate(w: Workload, budget_s: float, layer=None):
     return rows_per_s / (s.heads * w.layers), done, threads, spent
 
 
-def config_of(w: Workload, world: int, working_set: int = 0, ring: bool = False, pad: int = 0):
+def config_of(w: Workload, world: int, working_set: int = 0, ring: bool = False, pad: int = 0,
+              rollover: str = ""):
     s = w.shape
     c = {"workload": w.name, "batch": s.batch, "heads": s.heads, "d_head": s.d_head,
          "seg_len": s.seg_len, "mem_len": s.mem_len, "layers": w.layers, "segments": w.segments,
          "parallelism": f"replicas x{world} (batch-independent, no collective)"}
+    if rollover:
+        c["rollover"] = rollover
     if ring:
         c["memory"] = "ring (txl_rel_attn_fwd_ring + txl_ring_append of L rows)"
     if pad and pad != s.d_head:
@@ -609,6 +652,9 @@ def main(argv=None):
                     help="time the eager step only (no CUDA-graph replay of the step)")
     ap.add_argument("--backward", action="store_true",
                     help="time txl_rel_attn_bwd (gradients of one layer call) at the workload's shape")
+    ap.add_argument("--fused-rollover", action="store_true",
+                    help="attention and memory update of a layer in one call (txl_rel_attn_fwd_mem); the "
+                         "roofline's launch time then includes the rollover copy")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
     args = ap.parse_args(argv)
@@ -639,9 +685,11 @@ def main(argv=None):
         import dataclasses
         w = dataclasses.replace(w, layers=args.layers or w.layers, segments=args.segments or w.segments)
     s = w.shape
-    chain = Chain(w, torch.device("cuda", local), ring=args.ring, pad=args.pad)
+    chain = Chain(w, torch.device("cuda", local), ring=args.ring, pad=args.pad,
+                  fused=args.fused_rollover)
     splits = splits_for(w) if w.dtype == "bf16" else 1
     chain.attn_extra_launches = 1 if splits > 1 else 0
+    chain.rollover_in_attention = chain.fused and rollover_fuses(w, splits)
     for _ in range(args.warmup):
         chain.step(txl)
     txl.check()
@@ -732,7 +780,10 @@ def main(argv=None):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": config_of(w, world, chain.working_set_bytes, args.ring, args.pad),
+            "config": config_of(w, world, chain.working_set_bytes, args.ring, args.pad,
+                                "in the attention launch (txl_rel_attn_fwd_mem)" if chain.rollover_in_attention
+                                else ("own launch (txl_rel_attn_fwd_mem)" if chain.fused
+                                      else "own launch (txl_mem_update)")),
             "tflops": tflops_step, "pct_bf16_peak": tflops_step / peaks["bf16_tflops"] * 100.0,
             "roofline": roof, "clocks": clk, "gpu_launches": launches, "timing": timing}
 

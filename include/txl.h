@@ -118,6 +118,28 @@ txl_status txl_mem_update(void *mem_next, const void *ext_ctx, int batch, int me
                           int seg_len, int d_model, txl_dtype dtype, void *stream);
 
 /*
+ * txl_rel_attn_fwd_mem -- one layer's txl_rel_attn_fwd and txl_mem_update in
+ * one call (Section 3.3's attention and Section 3.2's cache update of the
+ * same layer, which do not depend on each other).  Where it pays, the
+ * attention launch does the rollover copy as well (bf16, d_head = 64, the
+ * tensor-memory path, 16-byte aligned ext_ctx + seg_len rows and mem_next,
+ * M*batch*d_model*2 a multiple of 16, and a copy small against the
+ * attention's own work); otherwise the rollover runs as its own launch right
+ * after, on the same stream.  Results are exactly those of the two calls.
+ *
+ * Arguments as txl_rel_attn_fwd, plus mem_next, ext_ctx and d_model as
+ * txl_mem_update (same batch, mem_len, seg_len and dtype).  mem_next must not
+ * overlap ext_ctx or any buffer of the attention; ext_ctx must not overlap
+ * out.  With nothing to attend (batch, seg_len or heads 0) only the rollover
+ * runs; with nothing to roll (mem_len or d_model 0) mem_next and ext_ctx are
+ * unused.  Same error behaviour as the two calls.
+ */
+txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, const void *r,
+                                const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                int seg_len, int heads, int d_head, txl_dtype dtype, void *out,
+                                void *mem_next, const void *ext_ctx, int d_model, void *stream);
+
+/*
  * txl_rel_attn_fwd_ring -- txl_rel_attn_fwd with k and v stored as a ring.
  * The extended context [memory; segment] of Section 3.2 slides forward by L
  * rows per segment; kept in a ring of M+L rows, a segment adds only its L new

@@ -78,6 +78,43 @@ def test_attn_empty_is_a_no_op(lib):
     assert _attn(H=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None) == OK
 
 
+def _attn_mem(**kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, r=FAKE * 4, u=FAKE * 5, w=FAKE * 6, B=2, M=8, L=8, H=2,
+             D=16, dt=1, out=FAKE * 7, mem_next=FAKE * 8, ext=FAKE * 9, dm=32, stream=None)
+    a.update(kw)
+    return abi.load_library().txl_rel_attn_fwd_mem(
+        a["q"], a["k"], a["v"], a["r"], a["u"], a["w"], a["B"], a["M"], a["L"], a["H"], a["D"], a["dt"],
+        a["out"], a["mem_next"], a["ext"], a["dm"], a["stream"])
+
+
+def test_attn_mem_rejects_bad_arguments(lib):
+    assert _attn_mem(dt=7) == UNSUPPORTED
+    assert _attn_mem(dm=-1) == INVALID
+    assert _attn_mem(mem_next=None) == INVALID
+    assert _attn_mem(ext=None) == INVALID
+    assert _attn_mem(mem_next=FAKE * 8 + 1) == INVALID          # misaligned
+    assert _attn_mem(mem_next=FAKE * 9 + 64) == INVALID         # mem_next overlaps ext_ctx
+    assert _attn_mem(mem_next=FAKE * 2 + 32) == INVALID         # mem_next overlaps k
+    assert _attn_mem(mem_next=FAKE * 7) == INVALID              # mem_next overlaps out
+    assert _attn_mem(ext=FAKE * 7 - 64) == INVALID              # ext_ctx overlaps out
+    assert _attn_mem(q=None) == INVALID                         # the attention's own checks
+    assert _attn_mem(D=65) == UNSUPPORTED
+    # nothing to do at all: OK without touching a pointer
+    assert _attn_mem(B=0, M=0, q=None, k=None, v=None, r=None, u=None, w=None, out=None, mem_next=None,
+                     ext=None) == OK
+    # nothing to roll: the attention alone (its pointers are still checked)
+    assert _attn_mem(M=0, mem_next=None, ext=None, q=None) == INVALID
+
+
+def test_attn_mem_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the call would launch on the fake pointers")
+    assert _attn_mem() == CUDA
+    assert _attn_mem(H=0) == CUDA             # no heads: the rollover alone still launches
+    assert _attn_mem(B=0) == OK               # no batch: nothing to attend and no rows to roll
+
+
 def test_mem_update_rejects_bad_arguments(lib):
     f = abi.mem_update_raw
     assert f(FAKE, FAKE * 4, 2, 4, 4, 8, 9, None) == UNSUPPORTED

@@ -46,3 +46,36 @@ def test_rollover_zero_memory_is_noop():
     txl.mem_update(nxt, ext, mem_len=0)
     torch.cuda.synchronize()
     assert (nxt == 0).all()
+
+
+@pytest.mark.parametrize("B,H,D,L,M,dm,dtype", [
+    (22, 8, 64, 768, 768, 512, torch.bfloat16),    # the training shape: the attention launch takes the copy
+    (22, 8, 64, 128, 3800, 512, torch.bfloat16),   # a copy too large to hide: its own launch
+    (2, 3, 64, 150, 130, 41, torch.bfloat16),      # rows not 16-byte aligned: its own launch
+    (2, 2, 41, 37, 50, 82, torch.bfloat16),        # padded head size
+    (2, 2, 24, 40, 30, 48, torch.float32),         # fp32 path
+])
+def test_attn_with_rollover_equals_the_two_calls(B, H, D, L, M, dm, dtype):
+    """txl_rel_attn_fwd_mem: the attention output bit-identical to
+    txl_rel_attn_fwd's, the new memory bit-identical to the oracle's
+    rollover, rows past M of mem_next untouched."""
+    import transformer_xl_relative_rel_gb300 as txl
+    from tests.helpers import device_layer, unit_shape
+    from transformer_xl_relative_rel_gb300 import inputs
+    T = M + L
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), 300 + L + dm)
+    dev, _ = device_layer(p, dtype)
+    g = torch.Generator().manual_seed(dm + M)
+    ext = torch.randn(T, B, dm, generator=g).to(dtype)
+    nxt = torch.full((T, B, dm), -7.0).to(dtype)
+    d_ext, d_nxt = ext.cuda(), nxt.cuda()
+    args = (dev["q"], dev["k"], dev["v"], dev["r"], dev["u"], dev["w"])
+    out = txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=d_nxt, ext_ctx=d_ext)
+    plain = txl.rel_attn_fwd(*args, mem_len=M)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+    ibits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    want = oracle.mem_update(ext.view(ibits).numpy(), M)
+    got = d_nxt.cpu()
+    assert np.array_equal(got.view(ibits).numpy()[:M], want)
+    assert torch.equal(got[M:], nxt[M:])

@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse")
+           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem")
 
 
 class TxlError(RuntimeError):
@@ -53,6 +53,8 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd.restype = i
     lib.txl_rel_attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
     lib.txl_rel_attn_fwd_lse.restype = i
+    lib.txl_rel_attn_fwd_mem.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, i, vp]
+    lib.txl_rel_attn_fwd_mem.restype = i
     lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd_noalloc.restype = i
     lib.txl_rel_attn_fwd_ring.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
@@ -168,6 +170,27 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
         B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _ptr(lse), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd_lse")
+    return out
+
+
+def rel_attn_fwd_mem(q, k, v, r, u_bias, v_bias, mem_len: int, mem_next, ext_ctx, out=None, stream=None):
+    """``rel_attn_fwd`` and ``mem_update`` of one layer in one call
+    (txl_rel_attn_fwd_mem): returns ``out``; ``mem_next`` receives the newest
+    ``mem_len`` rows of ``ext_ctx`` [M+L, B, d_model] (same dtype as q)."""
+    L, B, H, D = q.shape
+    out = _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
+    if ext_ctx.dim() != 3 or ext_ctx.shape[0] != mem_len + L or ext_ctx.shape[1] != B:
+        raise ValueError(f"ext_ctx must be [{mem_len + L}, {B}, d_model]")
+    dm = ext_ctx.shape[2]
+    for name, t in (("ext_ctx", ext_ctx), ("mem_next", mem_next)):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor typed like q")
+    if mem_next.numel() < mem_len * B * dm:
+        raise ValueError(f"mem_next must hold at least [{mem_len}, {B}, {dm}]")
+    st = load_library().txl_rel_attn_fwd_mem(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),
+        B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _ptr(mem_next), _ptr(ext_ctx), dm, _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_mem")
     return out
 
 

@@ -130,7 +130,8 @@ extern "C" {
 static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
                                   const float *u_bias, const float *v_bias, int batch, int mem_len,
                                   int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
-                                  void *out, void *stream, int scale_d = 0, float *lse = nullptr)
+                                  void *out, void *stream, int scale_d = 0, float *lse = nullptr,
+                                  const void *roll_src = nullptr, void *roll_dst = nullptr, size_t roll_bytes = 0)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
@@ -176,10 +177,14 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
     }
     AttnArgs a{q, k, v, r, u_bias, v_bias, out, batch, heads, d_head, seg_len, mem_len, kv_start, scale_d};
     a.lse = lse;
+    a.roll_src = roll_src;
+    a.roll_dst = roll_dst;
+    a.roll_bytes = roll_bytes;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     if (dtype == TXL_F32) {
         e = launch_attn_f32(a, s);
+        if (e == cudaSuccess && roll_bytes) e = launch_rollover(roll_dst, roll_src, roll_bytes, 4, s);
     } else if (a.D == 64) {
         const int splits = bf16_num_splits(a, device_sm_count());
         void *scratch = nullptr;
@@ -237,6 +242,48 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
 {
     return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0,
                            dtype, out, stream);
+}
+
+txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, const void *r,
+                                const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                int seg_len, int heads, int d_head, txl_dtype dtype, void *out,
+                                void *mem_next, const void *ext_ctx, int d_model, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1 || d_model < 0) return TXL_ERR_INVALID;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    // the rollover's part: as txl_mem_update
+    size_t nbytes = 0;
+    const void *src = nullptr;
+    if (batch > 0 && mem_len > 0 && d_model > 0) {
+        if (!mem_next || !ext_ctx) return TXL_ERR_INVALID;
+        if (!aligned(mem_next, esz) || !aligned(ext_ctx, esz)) return TXL_ERR_INVALID;
+        const size_t row = (size_t)batch * (size_t)d_model * esz;
+        if (row / esz / (size_t)batch != (size_t)d_model) return TXL_ERR_UNSUPPORTED;
+        const size_t T = (size_t)mem_len + (size_t)seg_len;
+        nbytes = (size_t)mem_len * row;
+        if (overlaps(mem_next, nbytes, ext_ctx, T * row)) return TXL_ERR_INVALID;
+        // and the attention's: mem_next overlaps none of its buffers, ext_ctx not its output
+        if (batch > 0 && seg_len > 0 && heads > 0) {
+            const size_t hrow = (size_t)batch * (size_t)heads * (size_t)d_head * esz;
+            const size_t nq = (size_t)seg_len * hrow, nk = T * hrow, nr = T * (size_t)heads * d_head * esz;
+            const size_t nb = (size_t)heads * d_head * 4;
+            if (overlaps(mem_next, nbytes, q, nq) || overlaps(mem_next, nbytes, k, nk) ||
+                overlaps(mem_next, nbytes, v, nk) || overlaps(mem_next, nbytes, r, nr) ||
+                overlaps(mem_next, nbytes, out, nq) || overlaps(mem_next, nbytes, u_bias, nb) ||
+                overlaps(mem_next, nbytes, v_bias, nb) || overlaps(ext_ctx, T * row, out, nq))
+                return TXL_ERR_INVALID;
+        }
+        src = (const unsigned char *)ext_ctx + (size_t)seg_len * row;
+    }
+    if (batch == 0 || seg_len == 0 || heads == 0) {
+        // no attention work: the rollover alone
+        if (!nbytes) return TXL_OK;
+        const cudaError_t e = launch_rollover(mem_next, src, nbytes, (int)esz, (cudaStream_t)stream);
+        return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+    }
+    return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0, dtype, out,
+                           stream, 0, nullptr, src, nbytes ? mem_next : nullptr, nbytes);
 }
 
 txl_status txl_rel_attn_fwd_lse(const void *q, const void *k, const void *v, const void *r,

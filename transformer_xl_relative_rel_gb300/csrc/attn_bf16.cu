@@ -93,6 +93,11 @@ struct Params {
     int kv_start;       // K, V rows form a ring: key j at row (kv_start + j) mod T
     int ost;            // 1: output tiles written by TMA store (tensor map tm_o)
     float sl2;          // log2(e) / sqrt(D)
+    // the memory rollover copied by warp 3 of every CTA (its slice of
+    // roll_n16 16-byte units), 0 units when not fused
+    const uint4 *roll_src;
+    uint4 *roll_dst;
+    long roll_n16;
 };
 
 // Every operand tile in shared memory uses 128-byte rows with the 128-byte
@@ -559,6 +564,26 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
             }
             __syncwarp();
+        } else if (kTma && warp == 3) {
+            // =============================================================== memory rollover
+            // Section 3.2's cache update of this layer, independent of the
+            // attention: the CTA's contiguous slice of the flat copy,
+            // sixteen 16-byte loads in flight per lane, streaming cache hints
+            // (the data is used once; the layer's K, V and table stay in L2)
+            if (p.roll_n16 > 0) {
+                const long G = gridDim.x, per = (p.roll_n16 + G - 1) / G;
+                const long beg = (long)blockIdx.x * per;
+                const long end = beg + per < p.roll_n16 ? beg + per : p.roll_n16;
+                long x = beg + lane;
+                for (; x + 15 * 32 < end; x += 16 * 32) {
+                    uint4 t[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) t[u] = __ldcs(p.roll_src + x + 32 * u);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) __stcs(p.roll_dst + x + 32 * u, t[u]);
+                }
+                for (; x < end; x += 32) __stcs(p.roll_dst + x, __ldcs(p.roll_src + x));
+            }
         } else if (warp == 2) {
             // =============================================================== P.V MMAs
             // This thread also writes the output tiles: the softmax threads
@@ -1668,6 +1693,29 @@ size_t bf16_scratch_bytes(const AttnArgs &a, int splits)
     return rows * (size_t)dpad(a.D) * 4 + rows * 4 + 256;
 }
 
+// Whether the forward launch also does the memory rollover (warp 3 of each
+// CTA, otherwise idle under TMA): the pointers and size must allow 16-byte
+// vectors, and a CTA's slice must take well under the attention's own time.
+// One warp with sixteen 16-byte loads in flight moves about ROLL_GBS GB/s; a
+// CTA's attention work is about TILE_US per 128 x 128 tile (its share of the
+// launch's tiles, the per-item overhead counted as one tile).
+bool roll_fuses(const AttnArgs &a, long items, int splits)
+{
+    constexpr double ROLL_GBS = 8.0, TILE_US = 1.6;
+    if (((uintptr_t)a.roll_src & 15) || ((uintptr_t)a.roll_dst & 15) || (a.roll_bytes & 15)) return false;
+    const long G = items < device_sm_count() ? items : device_sm_count();
+    if (G <= 0) return false;
+    const int nqt = (a.L + BM - 1) / BM;
+    double tiles = 0.0;
+    for (int qt = 0; qt < nqt; ++qt) {
+        const long kend = (long)a.M + (long)qt * BM + (a.L - qt * BM < BM ? a.L - qt * BM : BM);
+        tiles += (double)((kend + BN - 1) / BN) + splits;
+    }
+    tiles *= (double)a.B * a.H / (double)G;           // per CTA
+    const double copy_us = (double)a.roll_bytes / (double)G / (ROLL_GBS * 1e3);
+    return copy_us <= 0.5 * tiles * TILE_US;
+}
+
 cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaStream_t s)
 {
     const int DP = dpad(a.D);
@@ -1699,6 +1747,9 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
     p.kv_start = a.kv_start;
+    p.roll_src = nullptr;
+    p.roll_dst = nullptr;
+    p.roll_n16 = 0;
     CUtensorMap mk, mv, mr, mq, mk8, mv8, mo;
     memset(&mo, 0, sizeof(mo));
     p.ost = 0;
@@ -1726,6 +1777,11 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
             if (!make_map(&mo, a.out, a.L, rs, bhn, BM)) return cudaErrorInvalidValue;
             p.ost = 1;
         }
+        if (a.roll_bytes && roll_fuses(a, p.items, splits)) {
+            p.roll_src = (const uint4 *)a.roll_src;
+            p.roll_dst = (uint4 *)a.roll_dst;
+            p.roll_n16 = (long)(a.roll_bytes / 16);
+        }
     }
     cudaError_t e;
     switch (DP) {
@@ -1734,10 +1790,15 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<48, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
     default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
     }
-    if (e != cudaSuccess || splits == 1) return e;
-    rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
-        p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
-    return cudaGetLastError();
+    if (e == cudaSuccess && splits > 1) {
+        rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
+            p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
+        e = cudaGetLastError();
+    }
+    // a rollover the attention launch did not take: its own copy
+    if (e == cudaSuccess && a.roll_bytes && p.roll_n16 == 0)
+        e = launch_rollover(a.roll_dst, a.roll_src, a.roll_bytes, 2, s);
+    return e;
 }
 
 cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, void *p_out, void *da_out,

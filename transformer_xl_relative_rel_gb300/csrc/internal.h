@@ -16,6 +16,12 @@ struct AttnArgs {
     int kv_start = 0;             // K, V in a ring of M+L rows: key j at row (kv_start + j) mod (M+L)
     int scale_d = 0;              // d_head for the 1/sqrt(d_head) scale when D is a padded width (0: D)
     float *lse = nullptr;         // bf16 path, optional [B*H][L]: row log-sum-exp (natural log) of the scaled scores
+    // optional memory rollover done by the same launch where that pays
+    // (bf16 TMA path): roll_bytes bytes from roll_src to roll_dst; otherwise
+    // the launcher issues the separate rollover copy after the attention
+    const void *roll_src = nullptr;
+    void *roll_dst = nullptr;
+    size_t roll_bytes = 0;
 };
 
 // fp32 SIMT path (attn_f32.cu)
