@@ -322,23 +322,6 @@ def rollover_fuses(w: Workload, splits: int) -> bool:
     return nbytes / G / 8e3 <= 0.5 * tiles * 1.6
 
 
-def splits_for(w: Workload) -> int:
-    """Mirror of the library's split choice (for the launch count only)."""
-    s = w.shape
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    nqt = (s.seg_len + 127) // 128
-    ctas = s.batch * s.heads * nqt
-    ntile = (s.klen + 127) // 128
-    best, best_s = 1e30, 1
-    for sp in range(1, min(16, ntile) + 1):
-        waves = (ctas * sp + sms - 1) // sms
-        per = (ntile + sp - 1) // sp
-        cost = waves * per + (1.0 if sp > 1 else 0.0)
-        if cost < best - 1e-9:
-            best, best_s = cost, sp
-    return best_s
-
-
 # ------------------------------------------------------------- e2e measurement
 def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
     """The same step through the public API with the inputs in pinned host
@@ -687,8 +670,11 @@ def main(argv=None):
     s = w.shape
     chain = Chain(w, torch.device("cuda", local), ring=args.ring, pad=args.pad,
                   fused=args.fused_rollover)
-    splits = splits_for(w) if w.dtype == "bf16" else 1
-    chain.attn_extra_launches = 1 if splits > 1 else 0
+    # the library's own plan for this call shape: key splits and launches
+    splits, call_launches = txl.rel_attn_fwd_plan(s.batch, s.mem_len, s.seg_len, s.heads, s.d_head,
+                                                  txl.TXL_BF16 if w.dtype == "bf16" else txl.TXL_F32)
+    # (head vectors stored padded go straight to the kernel: no padding copies)
+    chain.attn_extra_launches = (1 if splits > 1 else 0) if chain.pad else call_launches - 1
     chain.rollover_in_attention = chain.fused and rollover_fuses(w, splits)
     for _ in range(args.warmup):
         chain.step(txl)

@@ -82,6 +82,21 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
                             txl_dtype dtype, void *out, void *stream);
 
 /*
+ * txl_rel_attn_fwd_plan -- how txl_rel_attn_fwd runs a call of this shape:
+ * the number of key-range splits (the keys of each query block divided over
+ * that many CTAs, merged by a combine launch) and the number of kernel
+ * launches it makes, for 16-byte aligned operands.  No GPU work; the split
+ * choice is the one the call itself makes on the current device (a cost
+ * model of the kernel's schedule, measured on GB300).
+ *
+ * splits, launches : host int outputs (NULL => TXL_ERR_INVALID).  A call with
+ * nothing to do reports 1 split and 0 launches.  Same dtype and d_head limits
+ * as txl_rel_attn_fwd.
+ */
+txl_status txl_rel_attn_fwd_plan(int batch, int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype,
+                                 int *splits, int *launches);
+
+/*
  * txl_rel_attn_fwd_lse -- txl_rel_attn_fwd that also stores, per query row,
  * the natural log of the softmax denominator (the log-sum-exp of the row's
  * visible scaled scores s_ij above):

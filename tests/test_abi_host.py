@@ -115,6 +115,24 @@ def test_attn_mem_without_gpu_reports_cuda_error(lib):
     assert _attn_mem(B=0) == OK               # no batch: nothing to attend and no rows to roll
 
 
+def test_attn_plan(lib):
+    import torch
+    # the training shape runs unsplit in one launch; a head size other than 64
+    # adds the padding copies; fp32 is one launch; nothing to do is no launch
+    if not torch.cuda.is_available():
+        assert txl.rel_attn_fwd_plan(22, 768, 768, 8, 64, txl.TXL_BF16) == (1, 1)
+        sp, nl = txl.rel_attn_fwd_plan(60, 150, 150, 10, 41, txl.TXL_BF16)
+        assert nl == 8 + (1 if sp > 1 else 0)
+    assert txl.rel_attn_fwd_plan(1, 16, 16, 2, 16, txl.TXL_F32) == (1, 1)
+    assert txl.rel_attn_fwd_plan(0, 16, 16, 2, 16, txl.TXL_BF16) == (1, 0)
+    n = ctypes.c_int(0)
+    f = lib.txl_rel_attn_fwd_plan
+    assert f(1, 16, 16, 2, 16, 7, ctypes.byref(n), ctypes.byref(n)) == UNSUPPORTED
+    assert f(1, 16, 16, 2, 16, 1, None, ctypes.byref(n)) == INVALID
+    assert f(1, -1, 16, 2, 16, 1, ctypes.byref(n), ctypes.byref(n)) == INVALID
+    assert f(1, 16, 16, 2, 65, 1, ctypes.byref(n), ctypes.byref(n)) == UNSUPPORTED
+
+
 def test_mem_update_rejects_bad_arguments(lib):
     f = abi.mem_update_raw
     assert f(FAKE, FAKE * 4, 2, 4, 4, 8, 9, None) == UNSUPPORTED

@@ -66,11 +66,18 @@ def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
 
 
 def test_noalloc_refuses_scratch_beyond_its_maximum(lib):
-    # B1 H8 D64 L4096 M16384 (eight heads, a long memory) splits its keys
-    # five ways: ~41 MiB of partials, more than the fixed 32 MiB.  Real
-    # buffers, so nothing could go wrong on the device even if the refusal
-    # failed.
-    B, H, D, L, M = 1, 8, 64, 4096, 16384
+    # A long memory over few heads splits its keys several ways; the first of
+    # these shapes whose split partials (as the library plans the call) need
+    # more than the fixed 32 MiB is called.  Real buffers, so nothing could go
+    # wrong on the device even if the refusal failed.
+    import transformer_xl_relative_rel_gb300 as txl
+    D = 64
+    for B, H, L, M in ((1, 5, 4096, 32768), (1, 8, 4096, 32768), (1, 6, 4096, 32768), (1, 4, 8192, 65536)):
+        splits, _ = txl.rel_attn_fwd_plan(B, M, L, H, D, txl.TXL_BF16)
+        if splits * B * H * L * (D + 1) * 4 + 256 > (32 << 20):
+            break
+    else:
+        pytest.fail("no candidate shape splits past the no-alloc scratch")
     T = L + M
     dev = {"q": torch.zeros(L, B, H, D, dtype=torch.bfloat16, device="cuda"),
            "k": torch.zeros(T, B, H, D, dtype=torch.bfloat16, device="cuda"),

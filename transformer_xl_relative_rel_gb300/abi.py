@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem")
+           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan")
 
 
 class TxlError(RuntimeError):
@@ -53,6 +53,9 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd.restype = i
     lib.txl_rel_attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
     lib.txl_rel_attn_fwd_lse.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.txl_rel_attn_fwd_plan.argtypes = [i, i, i, i, i, i, ip, ip]
+    lib.txl_rel_attn_fwd_plan.restype = i
     lib.txl_rel_attn_fwd_mem.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, i, vp]
     lib.txl_rel_attn_fwd_mem.restype = i
     lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
@@ -171,6 +174,16 @@ def rel_attn_fwd(q, k, v, r, u_bias, v_bias, mem_len: int, out=None, stream=None
         B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _ptr(lse), _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd_lse")
     return out
+
+
+def rel_attn_fwd_plan(batch: int, mem_len: int, seg_len: int, heads: int, d_head: int,
+                      dtype_code: int) -> tuple:
+    """(key splits, kernel launches) of a txl_rel_attn_fwd call of this shape."""
+    sp, nl = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().txl_rel_attn_fwd_plan(batch, mem_len, seg_len, heads, d_head, dtype_code,
+                                              ctypes.byref(sp), ctypes.byref(nl))
+    _raise(st, "txl_rel_attn_fwd_plan")
+    return int(sp.value), int(nl.value)
 
 
 def rel_attn_fwd_mem(q, k, v, r, u_bias, v_bias, mem_len: int, mem_next, ext_ctx, out=None, stream=None):

@@ -244,6 +244,35 @@ txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const v
                            dtype, out, stream);
 }
 
+txl_status txl_rel_attn_fwd_plan(int batch, int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype,
+                                 int *splits, int *launches)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (!splits || !launches) return TXL_ERR_INVALID;
+    if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
+    *splits = 1;
+    *launches = 0;
+    if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
+    if (d_head > 128 || (dtype == TXL_BF16 && d_head > 64)) return TXL_ERR_UNSUPPORTED;
+    if (dtype == TXL_F32) {
+        *launches = 1;
+        return TXL_OK;
+    }
+    AttnArgs a{};
+    a.B = batch;
+    a.H = heads;
+    a.D = 64;                                     // other head sizes run on 64-wide padded copies
+    a.L = seg_len;
+    a.M = mem_len;
+    a.scale_d = d_head;
+    const int s = bf16_num_splits(a, device_sm_count());
+    *splits = s;
+    // the attention kernel, the split combine, and for head sizes other than
+    // 64 the six padding copies and the output's copy back
+    *launches = 1 + (s > 1 ? 1 : 0) + (d_head != 64 ? 7 : 0);
+    return TXL_OK;
+}
+
 txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, const void *r,
                                 const float *u_bias, const float *v_bias, int batch, int mem_len,
                                 int seg_len, int heads, int d_head, txl_dtype dtype, void *out,

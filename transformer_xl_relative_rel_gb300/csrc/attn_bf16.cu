@@ -1472,36 +1472,52 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
     }
 }
 
-// Merge the key-split partials of one (b, h, i) row: weights 2^(lse_s - max).
-__global__ void __launch_bounds__(64)
+// Merge the key-split partials: one warp per output row (b, h, i), rows
+// numbered bh*L + i, eight rows per block.  Lane s holds split s's
+// log-sum-exp (splits <= 16), so the row's max and the weights
+// 2^(lse_s - max) come from warp reductions; lane l then combines columns
+// 2l, 2l+1 over the splits (coalesced 256-byte reads of each partial row).
+constexpr int COMBINE_ROWS = 8;
+
+__global__ void __launch_bounds__(32 * COMBINE_ROWS)
 rel_attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                         __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, int splits, int B, int H,
                         int L, int D, int DP)
 {
-    const int row = blockIdx.x;           // over B*H*L
-    const int bh = row / L, i = row % L;
-    const int b = bh / H, h = bh % H;
     const long BHL = (long)B * H * L;
-    float mx = -INFINITY;
-    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[s * BHL + (long)bh * L + i]);
-    if (lse_out && threadIdx.x == 0) {
-        float w = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float lse = part_lse[s * BHL + (long)bh * L + i];
-            w += (lse == -INFINITY) ? 0.f : exp2f(lse - mx);
+    const long row = (long)blockIdx.x * COMBINE_ROWS + (threadIdx.x >> 5);
+    if (row >= BHL) return;
+    const int lane = threadIdx.x & 31;
+    const int bh = (int)(row / L), i = (int)(row % L);
+    const int b = bh / H, h = bh % H;
+    const float ls = lane < splits ? part_lse[lane * BHL + row] : -INFINITY;
+    float mx = ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float wgt = ls == -INFINITY ? 0.f : exp2f(ls - mx);
+    float wsum = wgt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    if (lse_out && lane == 0) lse_out[row] = wsum > 0.f ? (mx + log2f(wsum)) * LN2 : -INFINITY;
+    const int d0 = 2 * lane;
+    const bool act = d0 < D;                  // this lane's columns exist
+    float a0 = 0.f, a1 = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+        const float w = __shfl_sync(0xffffffffu, wgt, sp);
+        if (act) {
+            const float2 v = *reinterpret_cast<const float2 *>(part_o + (sp * BHL + row) * DP + d0);
+            a0 += w * v.x;
+            a1 += w * v.y;
         }
-        lse_out[(long)bh * L + i] = w > 0.f ? (mx + log2f(w)) * LN2 : -INFINITY;
     }
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float acc = 0.f, wsum = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const long prow = s * BHL + (long)bh * L + i;
-            const float lse = part_lse[prow];
-            const float wgt = (lse == -INFINITY) ? 0.f : exp2f(lse - mx);
-            wsum += wgt;
-            acc += wgt * part_o[prow * DP + d];
-        }
-        out[(((long)i * B + b) * H + h) * D + d] = __float2bfloat16(acc / wsum);
+    if (!act) return;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *op = out + (((long)i * B + b) * H + h) * D + d0;
+    if (d0 + 1 < D && ((((long)i * B + b) * H + h) * D + d0) % 2 == 0) {
+        *reinterpret_cast<__nv_bfloat162 *>(op) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+    } else {
+        op[0] = __float2bfloat16(a0 * inv);
+        if (d0 + 1 < D) op[1] = __float2bfloat16(a1 * inv);
     }
 }
 
@@ -1655,8 +1671,10 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
             if (k.B == a.B && k.H == a.H && k.L == a.L && k.M == a.M && k.D == a.D && k.sms == num_sms) return k.s;
         }
     }
-    // the busiest CTA (simulated schedule) plus, when split, the fp32
-    // partials (written and read once, ~6 TB/s) and the combine launch
+    // the busiest CTA (simulated schedule) plus, when split, what a split
+    // was measured to cost on GB300: about 10 us (the combine launch and the
+    // split items' epilogues) and 0.7 us per MB of fp32 partials written and
+    // read back (char_eval and long-memory sweeps of 1-8 splits)
     const int nqt = (a.L + BM - 1) / BM;
     const long bh = (long)a.B * a.H;
     int maxn = 1;
@@ -1673,7 +1691,7 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
         double cost = busiest_cta(a, num_sms, s);
         if (s > 1) {
             const double bytes = 2.0 * s * (double)bh * a.L * (dpad(a.D) + 1) * 4.0;
-            cost += (bytes / 6.0e6 + 3.0) / tile_us;
+            cost += (10.0 + 0.7 * bytes / 1.0e6) / tile_us;
         }
         if (cost < best - 1e-9) {
             best = cost;
@@ -1791,7 +1809,8 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
     }
     if (e == cudaSuccess && splits > 1) {
-        rel_attn_combine_kernel<<<(unsigned)((long)a.B * a.H * a.L), 64, 0, s>>>(
+        const long rows = (long)a.B * a.H * a.L;
+        rel_attn_combine_kernel<<<(unsigned)((rows + COMBINE_ROWS - 1) / COMBINE_ROWS), 32 * COMBINE_ROWS, 0, s>>>(
             p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
         e = cudaGetLastError();
     }
