@@ -289,7 +289,7 @@ txl_status txl_ring_append(void *ring, const void *rows, int ring_len, int n_row
  *
  * Same arguments, layouts, results and error rules as txl_rel_attn_fwd, plus:
  *   - a call whose key split needs more than TXL_NOALLOC_SCRATCH_BYTES
- *     (splits * batch * heads * seg_len * (ceil16(d_head) + 1) * 4 + 256
+ *     (splits * batch * heads * seg_len * (2 * ceil16(d_head) + 4) + 256
  *     bytes) returns TXL_ERR_UNSUPPORTED before touching the GPU;
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call

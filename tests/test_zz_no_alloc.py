@@ -72,9 +72,10 @@ def test_noalloc_refuses_scratch_beyond_its_maximum(lib):
     # wrong on the device even if the refusal failed.
     import transformer_xl_relative_rel_gb300 as txl
     D = 64
-    for B, H, L, M in ((1, 5, 4096, 32768), (1, 8, 4096, 32768), (1, 6, 4096, 32768), (1, 4, 8192, 65536)):
+    for B, H, L, M in ((1, 4, 16384, 65536), (1, 8, 8192, 65536), (1, 16, 4096, 65536), (1, 5, 4096, 32768),
+                       (1, 16, 2048, 65536), (1, 12, 4096, 65536)):
         splits, _ = txl.rel_attn_fwd_plan(B, M, L, H, D, txl.TXL_BF16)
-        if splits * B * H * L * (D + 1) * 4 + 256 > (32 << 20):
+        if splits * B * H * L * (2 * D + 4) + 256 > (32 << 20):
             break
     else:
         pytest.fail("no candidate shape splits past the no-alloc scratch")

@@ -77,8 +77,12 @@ struct Params {
     const __nv_bfloat16 *q, *k, *v, *r;
     const float *u, *w;
     __nv_bfloat16 *out;
-    float *part_o;      // [splits][B*H][L][DP] when splits > 1
-    float *part_lse;    // [splits][B*H][L]
+    // key-split partials when splits > 1: each split's normalised output in
+    // bf16, laid out like the output over splits*B*H heads ([L][splits*B*H][DP],
+    // head index split*B*H + bh), and its row log-sum-exp in log2 units,
+    // [splits][B*H][L]
+    __nv_bfloat16 *part_o;
+    float *part_lse;
     float *lse;         // optional [B*H][L]: each row's log-sum-exp (natural log) of the scaled scores
     // backward scores only (the forward's output O comes in `out`): dO, the
     // outputs P and dA ([B*H][L][TP]) and dA in the table frame
@@ -615,7 +619,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         }
                         tc_fence_after();
                         if (ost && n == 0 && have_prev) {
-                            tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0, prev.bh);
+                            tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
+                                         p.splits > 1 ? prev.split * p.B * p.H + prev.bh : prev.bh);
                             bulk_commit();
                             in_flight = true;
                         }
@@ -636,7 +641,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         mbar_arrive(bar(S::B_OFR));
                     }
                     if (wait_or_abort(bar(S::B_OST), 0, abort)) {
-                        tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0, prev.bh);
+                        tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
+                                     p.splits > 1 ? prev.split * p.B * p.H + prev.bh : prev.bh);
                         bulk_commit();
                     }
                 }
@@ -801,11 +807,14 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int i = dn.i0 + ii;
             if (p.lse && p.splits == 1 && half == 0 && ii < dn.rows_here)
                 p.lse[(long)dn.bh * p.L + i] = l > 0.f ? (dn.m + log2f(l)) * LN2 : -INFINITY;
+            if (p.splits > 1 && half == 0 && ii < dn.rows_here)   // m is in log2 units of the scaled logits
+                p.part_lse[((long)dn.split * p.B * p.H + dn.bh) * p.L + i] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
             if (kTma && p.ost) {
-                // the 128 x 64 tile goes through shared memory (the tensor
-                // map's swizzled layout) and out by one TMA store, issued by
-                // the P.V thread; rows past L are not written.  The buffer is
-                // free once the previous item's store has read it.
+                // the 128 x 64 tile (the output, or this split's partial)
+                // goes through shared memory (the tensor map's swizzled
+                // layout) and out by one TMA store, issued by the P.V thread;
+                // rows past L are not written.  The buffer is free once the
+                // previous item's store has read it.
                 if (!wwait(S::B_OFR, n_out & 1)) return false;
 #pragma unroll
                 for (int c = 0; c < DH / 8; ++c) {
@@ -842,14 +851,18 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         if (d0 + d < p.D) op[d] = __float2bfloat16(o[d] * inv);
                 }
             } else {
-                const long prow = ((long)dn.split * p.B * p.H + dn.bh) * p.L + i;
-                float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * DP + d0);
+                // this split's partial row (bf16, 16-byte pieces: DH is a multiple of 8)
+                const long BH = (long)p.B * p.H;
+                __nv_bfloat16 *po = p.part_o + (((long)i * p.splits + dn.split) * BH + dn.bh) * DP + d0;
 #pragma unroll
-                for (int d4 = 0; d4 < DH / 4; ++d4)
-                    po[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
-                                         o[4 * d4 + 3] * inv);
-                // m is in log2 units of the scaled logits
-                if (half == 0) p.part_lse[prow] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
+                for (int d8 = 0; d8 < DH / 8; ++d8) {
+                    uint4 pk4;
+                    pk4.x = pack_bf16(o[d8 * 8 + 0] * inv, o[d8 * 8 + 1] * inv);
+                    pk4.y = pack_bf16(o[d8 * 8 + 2] * inv, o[d8 * 8 + 3] * inv);
+                    pk4.z = pack_bf16(o[d8 * 8 + 4] * inv, o[d8 * 8 + 5] * inv);
+                    pk4.w = pack_bf16(o[d8 * 8 + 6] * inv, o[d8 * 8 + 7] * inv);
+                    *reinterpret_cast<uint4 *>(po + d8 * 8) = pk4;
+                }
             }
             return true;
         };
@@ -860,9 +873,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 if (k < 0) break;
                 const Item e = make_item(p, k);
                 if (e.N <= 0 && half == 0 && ii < e.rows_here) {
-                    const long prow = ((long)e.split * p.B * p.H + e.bh) * p.L + e.i0 + ii;
-                    p.part_lse[prow] = -INFINITY;
-                    for (int d = 0; d < DP; ++d) p.part_o[prow * DP + d] = 0.f;
+                    const long BH = (long)p.B * p.H, ir = e.i0 + ii;
+                    p.part_lse[((long)e.split * BH + e.bh) * p.L + ir] = -INFINITY;
+                    __nv_bfloat16 *po = p.part_o + ((ir * p.splits + e.split) * BH + e.bh) * DP;
+                    for (int d = 0; d < DP; ++d) po[d] = __float2bfloat16(0.f);
                 }
             }
         };
@@ -1472,52 +1486,56 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
     }
 }
 
-// Merge the key-split partials: one warp per output row (b, h, i), rows
-// numbered bh*L + i, eight rows per block.  Lane s holds split s's
-// log-sum-exp (splits <= 16), so the row's max and the weights
-// 2^(lse_s - max) come from warp reductions; lane l then combines columns
-// 2l, 2l+1 over the splits (coalesced 256-byte reads of each partial row).
-constexpr int COMBINE_ROWS = 8;
-
-__global__ void __launch_bounds__(32 * COMBINE_ROWS)
-rel_attn_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+// Merge the key-split partials: one thread per output row (b, h, i) and
+// 8-column chunk, rows numbered bh*L + i.  The row's weights 2^(lse_s - max)
+// come from its splits' log-sum-exps (the same few words for the row's
+// threads); each split's chunk is one 16-byte load, several in flight.
+__global__ void __launch_bounds__(256)
+rel_attn_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float *__restrict__ part_lse,
                         __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, int splits, int B, int H,
                         int L, int D, int DP)
 {
-    const long BHL = (long)B * H * L;
-    const long row = (long)blockIdx.x * COMBINE_ROWS + (threadIdx.x >> 5);
-    if (row >= BHL) return;
-    const int lane = threadIdx.x & 31;
+    const int nch = DP / 8;
+    const long BH = (long)B * H, BHL = BH * L;
+    const long t = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= BHL * nch) return;
+    const long row = t / nch;
+    const int c = (int)(t % nch);
     const int bh = (int)(row / L), i = (int)(row % L);
     const int b = bh / H, h = bh % H;
-    const float ls = lane < splits ? part_lse[lane * BHL + row] : -INFINITY;
-    float mx = ls;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float wgt = ls == -INFINITY ? 0.f : exp2f(ls - mx);
-    float wsum = wgt;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    if (lse_out && lane == 0) lse_out[row] = wsum > 0.f ? (mx + log2f(wsum)) * LN2 : -INFINITY;
-    const int d0 = 2 * lane;
-    const bool act = d0 < D;                  // this lane's columns exist
-    float a0 = 0.f, a1 = 0.f;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < splits; ++sp) mx = fmaxf(mx, part_lse[sp * BHL + row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, wsum = 0.f;
+#pragma unroll 4
     for (int sp = 0; sp < splits; ++sp) {
-        const float w = __shfl_sync(0xffffffffu, wgt, sp);
-        if (act) {
-            const float2 v = *reinterpret_cast<const float2 *>(part_o + (sp * BHL + row) * DP + d0);
-            a0 += w * v.x;
-            a1 += w * v.y;
+        const float ls = part_lse[sp * BHL + row];
+        const float w = ls == -INFINITY ? 0.f : exp2f(ls - mx);
+        wsum += w;
+        const uint4 v = *reinterpret_cast<const uint4 *>(part_o + (((long)i * splits + sp) * BH + bh) * DP + 8 * c);
+        const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+            const float2 f = __bfloat1622float2(e[z]);
+            acc[2 * z] += w * f.x;
+            acc[2 * z + 1] += w * f.y;
         }
     }
-    if (!act) return;
+    if (lse_out && c == 0) lse_out[row] = wsum > 0.f ? (mx + log2f(wsum)) * LN2 : -INFINITY;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int d0 = 8 * c;
+    if (d0 >= D) return;
     __nv_bfloat16 *op = out + (((long)i * B + b) * H + h) * D + d0;
-    if (d0 + 1 < D && ((((long)i * B + b) * H + h) * D + d0) % 2 == 0) {
-        *reinterpret_cast<__nv_bfloat162 *>(op) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+    if (D % 8 == 0) {
+        uint4 pk4;
+        pk4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        pk4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        pk4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+        pk4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4 *>(op) = pk4;
     } else {
-        op[0] = __float2bfloat16(a0 * inv);
-        if (d0 + 1 < D) op[1] = __float2bfloat16(a1 * inv);
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+            if (d0 + z < D) op[z] = __float2bfloat16(acc[z] * inv);
     }
 }
 
@@ -1672,9 +1690,9 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
         }
     }
     // the busiest CTA (simulated schedule) plus, when split, what a split
-    // was measured to cost on GB300: about 10 us (the combine launch and the
-    // split items' epilogues) and 0.7 us per MB of fp32 partials written and
-    // read back (char_eval and long-memory sweeps of 1-8 splits)
+    // was measured to cost on GB300: about 3 us (the merge launch) and
+    // 1.25 us per MB of bf16 partials written and read back (fitted to the
+    // best of 1-12 forced splits on char_eval and long-memory shapes)
     const int nqt = (a.L + BM - 1) / BM;
     const long bh = (long)a.B * a.H;
     int maxn = 1;
@@ -1690,8 +1708,8 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
     for (int s = 1; s <= 16 && s <= maxn; ++s) {
         double cost = busiest_cta(a, num_sms, s);
         if (s > 1) {
-            const double bytes = 2.0 * s * (double)bh * a.L * (dpad(a.D) + 1) * 4.0;
-            cost += (10.0 + 0.7 * bytes / 1.0e6) / tile_us;
+            const double bytes = 2.0 * s * (double)bh * a.L * (2.0 * dpad(a.D) + 4.0);
+            cost += (3.0 + 1.25 * bytes / 1.0e6) / tile_us;
         }
         if (cost < best - 1e-9) {
             best = cost;
@@ -1708,7 +1726,7 @@ int bf16_num_splits(const AttnArgs &a, int num_sms)
 size_t bf16_scratch_bytes(const AttnArgs &a, int splits)
 {
     const size_t rows = (size_t)splits * a.B * a.H * a.L;
-    return rows * (size_t)dpad(a.D) * 4 + rows * 4 + 256;
+    return rows * (size_t)dpad(a.D) * 2 + rows * 4 + 256;
 }
 
 // Whether the forward launch also does the memory rollover (warp 3 of each
@@ -1760,8 +1778,8 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.lse = a.lse;
     if (splits > 1) {
         const size_t rows = (size_t)splits * a.B * a.H * a.L;
-        p.part_o = (float *)scratch;
-        p.part_lse = (float *)((char *)scratch + rows * DP * 4);
+        p.part_o = (__nv_bfloat16 *)scratch;
+        p.part_lse = (float *)((char *)scratch + rows * DP * 2);
     }
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
     p.kv_start = a.kv_start;
@@ -1790,9 +1808,13 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
             !make_map(&mr, a.r, p.T, (long)a.H * a.D, a.H, BN) || !make_map(&mq, a.q, a.L, rs, bhn, BM) ||
             !make_map(&mk8, a.k, p.T, rs, bhn, 8) || !make_map(&mv8, a.v, p.T, rs, bhn, 8))
             return cudaErrorInvalidValue;
-        // the output by TMA store when it is one pass (no key splits) and 16-byte aligned
+        // the output (or with key splits, the bf16 partials laid out like it
+        // over splits*B*H heads) by TMA store
         if (splits == 1 && ((uintptr_t)a.out & 15) == 0) {
             if (!make_map(&mo, a.out, a.L, rs, bhn, BM)) return cudaErrorInvalidValue;
+            p.ost = 1;
+        } else if (splits > 1) {
+            if (!make_map(&mo, p.part_o, a.L, (long)splits * rs, (long)splits * bhn, BM)) return cudaErrorInvalidValue;
             p.ost = 1;
         }
         if (a.roll_bytes && roll_fuses(a, p.items, splits)) {
@@ -1809,8 +1831,8 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
     }
     if (e == cudaSuccess && splits > 1) {
-        const long rows = (long)a.B * a.H * a.L;
-        rel_attn_combine_kernel<<<(unsigned)((rows + COMBINE_ROWS - 1) / COMBINE_ROWS), 32 * COMBINE_ROWS, 0, s>>>(
+        const long threads = (long)a.B * a.H * a.L * (DP / 8);
+        rel_attn_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
             p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
         e = cudaGetLastError();
     }
