@@ -216,12 +216,9 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
         void *rp = base + 2 * bq + 2 * bk;
         float *up_ = (float *)(base + 2 * bq + 2 * bk + br), *wp = (float *)(base + 2 * bq + 2 * bk + br + bb);
         void *sp = bs ? base + 2 * bq + 2 * bk + br + 2 * bb : nullptr;
-        e = launch_pad_heads(qp, a.q, nq, a.D, W, 2, s);
-        if (e == cudaSuccess) e = launch_pad_heads(kp, a.k, nk, a.D, W, 2, s);
-        if (e == cudaSuccess) e = launch_pad_heads(vp, a.v, nk, a.D, W, 2, s);
-        if (e == cudaSuccess) e = launch_pad_heads(rp, a.r, nr, a.D, W, 2, s);
-        if (e == cudaSuccess) e = launch_pad_heads(up_, a.u, heads, a.D, W, 4, s);
-        if (e == cudaSuccess) e = launch_pad_heads(wp, a.w, heads, a.D, W, 4, s);
+        const PadJob jobs[6] = {{qp, a.q, nq, a.D, 2}, {kp, a.k, nk, a.D, 2}, {vp, a.v, nk, a.D, 2},
+                                {rp, a.r, nr, a.D, 2}, {up_, a.u, heads, a.D, 4}, {wp, a.w, heads, a.D, 4}};
+        e = launch_pad_heads_many(jobs, 6, s);
         ap.q = qp;
         ap.k = kp;
         ap.v = vp;
@@ -268,8 +265,8 @@ txl_status txl_rel_attn_fwd_plan(int batch, int mem_len, int seg_len, int heads,
     const int s = bf16_num_splits(a, device_sm_count());
     *splits = s;
     // the attention kernel, the split combine, and for head sizes other than
-    // 64 the six padding copies and the output's copy back
-    *launches = 1 + (s > 1 ? 1 : 0) + (d_head != 64 ? 7 : 0);
+    // 64 the padding copies (one launch) and the output's copy back
+    *launches = 1 + (s > 1 ? 1 : 0) + (d_head != 64 ? 2 : 0);
     return TXL_OK;
 }
 

@@ -48,6 +48,15 @@ cudaError_t launch_rollover(void *dst, const void *src, size_t bytes, int elem_s
 // head vectors to / from a zero-padded width (pack.cu); elem_size 2 or 4
 cudaError_t launch_pad_heads(void *dst, const void *src, long nvec, int d, int dp, int elem_size,
                              cudaStream_t s);
+// several pad jobs (as launch_pad_heads, dp 64) in one launch
+constexpr int kMaxPadJobs = 6;
+struct PadJob {
+    void *dst;
+    const void *src;
+    long nvec;
+    int d, elem_size;
+};
+cudaError_t launch_pad_heads_many(const PadJob *jobs, int n, cudaStream_t s);
 cudaError_t launch_unpad_heads(void *dst, const void *src, long nvec, int d, int dp, int elem_size,
                                cudaStream_t s);
 
