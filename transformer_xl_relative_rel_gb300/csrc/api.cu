@@ -408,7 +408,7 @@ const char *txl_status_string(txl_status st)
 
 int txl_last_cuda_error(void) { return g_last_cuda_error; }
 
-int txl_version(void) { return 100; }
+int txl_version(void) { return 200; }   // 0.2.0: log-sum-exp, fused rollover, plan query; backward takes the saved forward
 
 void txl_shutdown(void)
 {
