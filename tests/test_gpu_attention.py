@@ -175,3 +175,25 @@ def test_bf16_random_shapes(B, H, D, L, M):
 @pytest.mark.parametrize("B,H,D,L,M", _random_shapes(37, 6, 128))
 def test_f32_random_shapes(B, H, D, L, M):
     _check_full(B, H, D, L, M, torch.float32, seed=4000 + B * 131 + H * 17 + D * 7 + L + M, tol=TOL_F32)
+
+
+# ----------------------------------------------------- near the call's limits
+@pytest.mark.parametrize("B,H,D,L,M,dtype", [
+    (1, 2, 64, 128, 65536, torch.bfloat16),    # a 64K memory: the most key splits (16)
+    (1, 64, 64, 256, 256, torch.bfloat16),     # many heads
+    (1, 2, 128, 100, 60, torch.float32),       # the largest head size (fp32 path)
+])
+def test_near_limits_sampled_rows(B, H, D, L, M, dtype):
+    import transformer_xl_relative_rel_gb300 as txl
+    s = inputs.LayerShape(batch=B, heads=H, d_head=D, seg_len=L, mem_len=M)
+    if dtype == torch.bfloat16:
+        assert txl.rel_attn_fwd_plan(B, M, L, H, D, txl.TXL_BF16)[0] >= 1
+    p = inputs.unit_layer(s, 1234 + H)
+    dev, host = device_layer(p, dtype)
+    out = run_library(dev, M)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    rows = inputs.sample_rows(s, 1234 + H, n_random=96, all_heads_of_b0=False)
+    ref = oracle_rows(host, M, rows)
+    err = np.abs(gather_rows(out, rows) - ref).max()
+    assert err <= (TOL_BF16 if dtype == torch.bfloat16 else TOL_F32), f"max abs err {err:.3e}"
