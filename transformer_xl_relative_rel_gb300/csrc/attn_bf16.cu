@@ -684,6 +684,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 w4[d4] = uw4[16 + 2 * DC * half + d4];
             }
             const float sk = p.sl2 * keep;
+            const uint64_t sk2 = f2(sk, sk);
 #pragma unroll
             for (int c = 0; c < DC; ++c) {
                 const int d8 = DC * half + c;
@@ -693,9 +694,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 uint32_t a4[4], c4[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    const float q0 = __bfloat162float(e[2 * z]), q1 = __bfloat162float(e[2 * z + 1]);
-                    a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
-                    c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
+                    // (q + u) s as q s + (u s), on element pairs
+                    const uint64_t q2 = f2(__bfloat162float(e[2 * z]), __bfloat162float(e[2 * z + 1]));
+                    float a0, a1, b0, b1;
+                    unf2(fma2(q2, sk2, mul2(f2(uu[2 * z], uu[2 * z + 1]), sk2)), a0, a1);
+                    unf2(fma2(q2, sk2, mul2(f2(ww[2 * z], ww[2 * z + 1]), sk2)), b0, b1);
+                    a4[z] = pack_bf16(a0, a1);
+                    c4[z] = pack_bf16(b0, b1);
                 }
                 *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
@@ -1238,6 +1243,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 w4[d4] = uw4[16 + 2 * DC * half + d4];
             }
             const float sk = p.sl2 * keep;
+            const uint64_t sk2 = f2(sk, sk);
 #pragma unroll
             for (int c = 0; c < DC; ++c) {
                 const int d8 = DC * half + c;
@@ -1247,9 +1253,13 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 uint32_t a4[4], c4[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    const float q0 = __bfloat162float(e[2 * z]), q1 = __bfloat162float(e[2 * z + 1]);
-                    a4[z] = pack_bf16((q0 + uu[2 * z]) * sk, (q1 + uu[2 * z + 1]) * sk);
-                    c4[z] = pack_bf16((q0 + ww[2 * z]) * sk, (q1 + ww[2 * z + 1]) * sk);
+                    // (q + u) s as q s + (u s), on element pairs
+                    const uint64_t q2 = f2(__bfloat162float(e[2 * z]), __bfloat162float(e[2 * z + 1]));
+                    float a0, a1, b0, b1;
+                    unf2(fma2(q2, sk2, mul2(f2(uu[2 * z], uu[2 * z + 1]), sk2)), a0, a1);
+                    unf2(fma2(q2, sk2, mul2(f2(ww[2 * z], ww[2 * z + 1]), sk2)), b0, b1);
+                    a4[z] = pack_bf16(a0, a1);
+                    c4[z] = pack_bf16(b0, b1);
                 }
                 *reinterpret_cast<uint4 *>(smem + S::QU + sw128_offset(ii, 8 * d8)) =
                     make_uint4(a4[0], a4[1], a4[2], a4[3]);
