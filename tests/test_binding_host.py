@@ -1,15 +1,18 @@
 """The Python binding's argument checks, on the host: wrong shapes, dtypes,
 devices and pairings are refused with an exception before the library is
 called (these checks are what stands between a caller's tensors and the raw
-pointers the C ABI receives).  CPU tensors stand in for device tensors where
-the check under test comes first; no compute call is made."""
+pointers the C ABI receives).  Host tensors stand in for device tensors: the
+shape and dtype checks come before the device check, and the device check
+itself is one of the refusals tested.  No compute call is made."""
 import pytest
 import torch
 
 import transformer_xl_relative_rel_gb300 as txl
+from transformer_xl_relative_rel_gb300 import abi
 
 L, B, H, D, M = 8, 2, 2, 16, 8
 T = L + M
+ON_DEVICE = "contiguous CUDA tensors"
 
 
 def _layer(dtype=torch.bfloat16):
@@ -18,67 +21,53 @@ def _layer(dtype=torch.bfloat16):
                 u=torch.zeros(H, D), w=torch.zeros(H, D))
 
 
-def _fwd(p, **kw):
-    return txl.rel_attn_fwd(p["q"], p["k"], p["v"], p["r"], p["u"], p["w"], mem_len=M, **kw)
-
-
-def test_attention_shapes_and_dtypes():
+def test_attention_shape_dtype_and_device_checks():
     p = _layer()
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd(p["q"], p["k"][:-1], p["v"], p["r"], p["u"], p["w"], mem_len=M)   # k one row short
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd(p["q"], p["k"], p["v"], p["r"][:, :1], p["u"], p["w"], mem_len=M)   # table heads
-    with pytest.raises(TypeError):
-        txl.rel_attn_fwd(p["q"], p["k"].float(), p["v"], p["r"], p["u"], p["w"], mem_len=M)   # mixed dtypes
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd(p["q"], p["k"], p["v"], p["r"], p["u"].double(), p["w"], mem_len=M)  # bias dtype
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd(p["q"], p["k"], p["v"], p["r"], p["u"][:1], p["w"], mem_len=M)       # bias shape
-    with pytest.raises(ValueError):
-        _fwd(p)                                   # host tensors: refused before any pointer is taken
-    from transformer_xl_relative_rel_gb300 import abi
-    with pytest.raises(TypeError):
-        abi._dtype_code(torch.zeros(1, dtype=torch.float16))   # no fp16 path
+    q, k, v, r, u, w = (p[n] for n in ("q", "k", "v", "r", "u", "w"))
+    with pytest.raises(ValueError, match="k must be"):
+        txl.rel_attn_fwd(q, k[:-1], v, r, u, w, mem_len=M)          # k one row short
+    with pytest.raises(ValueError, match="r must be"):
+        txl.rel_attn_fwd(q, k, v, r[:, :1], u, w, mem_len=M)         # table heads
+    with pytest.raises(ValueError, match="k must be"):
+        txl.rel_attn_fwd(q, k, v, r, u, w, mem_len=M + 1)            # memory length against k
+    with pytest.raises(TypeError, match="dtype"):
+        txl.rel_attn_fwd(q, k.float(), v, r, u, w, mem_len=M)        # mixed dtypes
+    with pytest.raises(ValueError, match="u_bias"):
+        txl.rel_attn_fwd(q, k, v, r, u.double(), w, mem_len=M)       # bias dtype
+    with pytest.raises(ValueError, match="v_bias"):
+        txl.rel_attn_fwd(q, k, v, r, u, w[:1], mem_len=M)            # bias shape
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.rel_attn_fwd(q, k, v, r, u, w, mem_len=M)                # host tensors
+    for fn, extra in ((txl.rel_attn_fwd_mem, dict(mem_next=torch.zeros(T, B, 32, dtype=torch.bfloat16),
+                                                  ext_ctx=torch.zeros(T, B, 32, dtype=torch.bfloat16))),
+                      (txl.rel_attn_bwd, dict(dout=torch.zeros(L, B, H, D, dtype=torch.bfloat16)))):
+        with pytest.raises(ValueError, match="k must be"):          # the attention's checks come first
+            fn(q, k[:-1], v, r, u, w, mem_len=M, **extra)
+        with pytest.raises(ValueError, match=ON_DEVICE):
+            fn(q, k, v, r, u, w, mem_len=M, **extra)
+    with pytest.raises(TypeError, match="unsupported dtype"):
+        abi._dtype_code(torch.zeros(1, dtype=torch.float16))         # no fp16 path
 
 
-def test_attention_output_and_lse_checks():
-    p = _layer()
-    with pytest.raises(ValueError):
-        _fwd(p, out=torch.zeros(L, B, H, D + 1, dtype=torch.bfloat16))
-    with pytest.raises(ValueError):
-        _fwd(p, out=torch.zeros(L, B, H, D, dtype=torch.float32))
-
-
-def test_backward_pairing_and_shapes():
-    p = _layer()
-    dout = torch.zeros(L, B, H, D, dtype=torch.bfloat16)
-    args = (p["q"], p["k"], p["v"], p["r"], p["u"], p["w"])
-    with pytest.raises(ValueError):
-        txl.rel_attn_bwd(*args, dout[:-1], mem_len=M)                 # dout shaped unlike q
-    with pytest.raises(ValueError):
-        txl.rel_attn_bwd(*args, dout, mem_len=M)                      # host tensors
-
-
-def test_fused_rollover_checks():
-    p = _layer()
+def test_rollover_checks():
     ext = torch.zeros(T, B, 32, dtype=torch.bfloat16)
-    nxt = torch.zeros(T, B, 32, dtype=torch.bfloat16)
-    args = (p["q"], p["k"], p["v"], p["r"], p["u"], p["w"])
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=nxt, ext_ctx=ext[:-1])     # context rows
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=nxt[:1], ext_ctx=ext)      # too small
-    with pytest.raises(ValueError):
-        txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=nxt, ext_ctx=ext)          # host tensors
-
-
-def test_rollover_and_ring_checks():
-    ext = torch.zeros(T, B, 32, dtype=torch.bfloat16)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="larger than the extended context"):
         txl.mem_update(torch.zeros(T, B, 32, dtype=torch.bfloat16), ext, mem_len=T + 1)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="mem_next must be"):
         txl.mem_update(torch.zeros(M, B, 31, dtype=torch.bfloat16), ext, mem_len=M)
-    with pytest.raises(TypeError):
+    with pytest.raises(ValueError, match="mem_next must be"):
+        txl.mem_update(torch.zeros(M - 1, B, 32, dtype=torch.bfloat16), ext, mem_len=M)
+    with pytest.raises(TypeError, match="dtypes differ"):
         txl.mem_update(torch.zeros(M, B, 32, dtype=torch.float32), ext, mem_len=M)
-    with pytest.raises(ValueError):
-        txl.mem_update(torch.zeros(M, B, 32, dtype=torch.bfloat16), ext, mem_len=M)   # host tensors
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.mem_update(torch.zeros(M, B, 32, dtype=torch.bfloat16), ext, mem_len=M)
+
+
+def test_plan_query_rejects_bad_shapes():
+    from transformer_xl_relative_rel_gb300 import _build
+    _build.build()                      # the query runs in the library (no GPU needed)
+    txl.load_library()
+    with pytest.raises(txl.TxlError, match="invalid"):
+        txl.rel_attn_fwd_plan(1, -1, 16, 2, 64, txl.TXL_BF16)
+    with pytest.raises(txl.TxlError, match="unsupported"):
+        txl.rel_attn_fwd_plan(1, 16, 16, 2, 65, txl.TXL_BF16)        # bf16 head size past 64
