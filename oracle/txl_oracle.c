@@ -19,7 +19,7 @@
  *   - Appendix B: the relative distance of a visible pair lies in 0..M+L-1 and
  *     the projected table is stored reversed, Q_k = W_kR R_{M+L-1-k}; the
  *     query at segment position i sees key j exactly when j <= M+i.
- * Readings where the pages leave a step open (all listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - the whole score A is scaled by 1/sqrt(d_head) before the softmax (the
  *     scaled softmax of the vanilla attention on the summary page);
  *   - heads are independent, u and v are per head, and the projected table r
