@@ -12,12 +12,23 @@
 // where dB~ is dA moved into the table's column frame (row i shifted right by
 // L-1-i: the inverse of the forward's left shift).
 //
-// This is the materialised form: the score, P, dP and dA of every (b, h) are
-// written to the caller's workspace as [L][T] matrices, the eight plain
-// contractions run as strided-batched cuBLAS GEMMs (bf16 operands and fp32
-// accumulation on the bf16 path; fp32 throughout on the fp32 path), and the
-// kernels below do the bias fold, the softmax, its gradient and both shifts,
-// and the batch / row reductions of dq, du, dv_bias and dr.
+// Two routes, chosen per call:
+//   - bf16, d_head 64, 16-byte aligned operands (run_bwd_fused): the
+//     forward's output O and row log-sum-exp (the caller's saved ones, or the
+//     forward kernel once more) feed the tcgen05 score kernel
+//     (rel_attn_bwd_scores_kernel in attn_bf16.cu), which recomputes S and
+//     the band per tile, forms dP = dO V^T in tensor memory and writes P, dA
+//     and dB~ as bf16 matrices (delta = rowsum(dO * O) made in the kernel);
+//     five strided-batched cuBLAS GEMMs give dV, dK, both halves of dQ and
+//     dr (dr summed over the batch by the contraction itself), and one pass
+//     adds the halves of dQ and forms du, dv_bias as its column sums;
+//   - otherwise (fp32, other head sizes: run_bwd) the materialised form: the
+//     score, P, dP and dA of every (b, h) are written to the caller's
+//     workspace as [L][T] matrices, the eight plain contractions run as
+//     strided-batched cuBLAS GEMMs (bf16 operands and fp32 accumulation on
+//     the bf16 path; fp32 throughout on the fp32 path), and the kernels below
+//     do the bias fold, the softmax, its gradient and both shifts, and the
+//     batch / row reductions of dq, du, dv_bias and dr.
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
