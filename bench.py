@@ -12,7 +12,8 @@ timed region; the per-step working set is far larger than L2.
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (weak scaling: independent sequences, no data-path collective); timing is the
-max over ranks.
+max over ranks.  ``--gpus N`` run without a launcher starts the N ranks
+itself (torch.distributed.run on 127.0.0.1).
 """
 from __future__ import annotations
 
@@ -54,13 +55,59 @@ def dist_env():
     return rank, world, local
 
 
-def init_dist(world: int):
+def init_dist(world: int, cpu: bool = False):
     if world <= 1:
         return None
     import torch.distributed as dist
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    backend = "nccl" if (torch.cuda.is_available() and not cpu) else "gloo"
     dist.init_process_group(backend=backend)
     return dist
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n: int, argv) -> int:
+    """``--gpus N`` without a launcher around it: start N ranks on this node
+    (torch.distributed.run, rendezvous on 127.0.0.1), one replica per GPU;
+    rank 0 prints the line.  Returns the launcher's exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__)] + list(argv)
+    env = dict(os.environ)
+    env.setdefault("OMP_NUM_THREADS", "1")
+    return subprocess.call(cmd, env=env)
+
+
+def dry_run(args, rank: int, world: int) -> int:
+    """The launcher and the cross-rank timing without a GPU: each rank times
+    a fixed amount of host work per step (no CUDA call), the step time is the
+    max over ranks (gloo), and rank 0 prints the line with ``n_gpus`` = the
+    world size and ``value`` = all ranks' units over that time."""
+    init_dist(world, cpu=True)
+    units = 1000.0
+    x = np.ones(1 << 16)
+    for _ in range(args.warmup):
+        x = np.sqrt(x + 1.0)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x = np.sqrt(x + 1.0)
+    local_s = time.perf_counter() - t0
+    barrier(world)
+    step_s = max_over_ranks(local_s, world) / args.steps
+    value = aggregate_rate(units * args.steps, local_s, world)
+    if rank == 0:
+        print(json.dumps({"metric": "dry run: host work per rank, no GPU", "value": value, "unit": "units/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": step_s * 1e3, "scaling": "weak", "dry_run": True}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
 
 
 def max_over_ranks(value: float, world: int) -> float:
@@ -640,9 +687,16 @@ def main(argv=None):
                          "roofline's launch time then includes the rollover copy")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="no GPU: exercise the rank launcher and the max-over-ranks timing on host work")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one replica per GPU: this process becomes the launcher of N ranks
+        return launch_ranks(args.gpus, sys.argv[1:] if argv is None else argv)
     rank, world, local = dist_env()
+    if args.dry_run:
+        return dry_run(args, rank, world)
     if args.impl == "reference":
         return run_reference(args, rank, world)
 

@@ -68,13 +68,19 @@ typedef enum {
  * Returns TXL_OK once the work is enqueued.  TXL_ERR_INVALID /
  * TXL_ERR_UNSUPPORTED before any launch; TXL_ERR_CUDA if a launch fails.
  * Long memories (few query tiles, many keys) split the keys across CTAs; the
- * partial results then live in a library-owned device scratch buffer that is
- * allocated on first need, grown when needed and released by txl_shutdown().
- * bf16 heads with d_head != 64 also use it: q, k, v, r and the biases are
- * copied into 64-wide zero-padded vectors there (rows the TMA unit can
- * read), and the output's d_head columns are copied back.  Calls that need
- * the scratch must not run concurrently on different streams, and the first
- * such call of a size must not be made during stream capture.
+ * partial results then live in a library-owned device scratch buffer.  bf16
+ * heads with d_head != 64 also use it: q, k, v, r and the biases are copied
+ * into 64-wide zero-padded vectors there (rows the TMA unit can read), and
+ * the output's d_head columns are copied back.  There is one such buffer per
+ * (device, stream handle): calls on different streams never share one and may
+ * run concurrently.  A buffer is allocated on first need and grown in stream
+ * order (cudaFreeAsync / cudaMallocAsync on that stream, no host-side wait),
+ * so the first call of a larger size on a stream must not be made during
+ * stream capture (it returns TXL_ERR_UNSUPPORTED there); later captured calls
+ * reuse the buffer.  Buffers are keyed by the stream handle's value: destroy a
+ * stream only after its calls have finished if a new stream may reuse the
+ * handle.  At most 256 (device, stream) pairs are served (then
+ * TXL_ERR_UNSUPPORTED); txl_shutdown() releases the current device's.
  */
 txl_status txl_rel_attn_fwd(const void *q, const void *k, const void *v, const void *r,
                             const float *u_bias, const float *v_bias,
@@ -291,9 +297,16 @@ txl_status txl_ring_append(void *ring, const void *rows, int ring_len, int n_row
  *   - a call whose key split needs more than TXL_NOALLOC_SCRATCH_BYTES
  *     (splits * batch * heads * seg_len * (2 * ceil16(d_head) + 4) + 256
  *     bytes) returns TXL_ERR_UNSUPPORTED before touching the GPU;
- *   - the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture;
+ *   - the first call on a device that splits its keys looks up the array's
+ *     device address (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture.  Under CUDA's default lazy
+ *     module loading the array is reserved on a device when the library's
+ *     device code is first loaded there, which can be as late as that lookup:
+ *     a caller that reserves the rest of device memory afterwards should make
+ *     one such call first (a long-memory shape, e.g. B 1, H 4, D 64,
+ *     L 128, M 1600);
+ *   - the cached address belongs to the device's primary context: a device
+ *     reset (cudaDeviceReset) while the library is loaded is not supported;
  *   - every call shares the one array, and each call writes every part of it
  *     that it reads back, so nothing carries over between calls; but calls
  *     whose kernels overlap on the GPU (different streams, or concurrent
@@ -324,8 +337,10 @@ int txl_last_cuda_error(void);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int txl_version(void);
 
-/* Free the library-owned scratch of the current device.  Safe to call more
- * than once; later calls re-allocate on demand. */
+/* Free the library-owned scratch buffers of the current device (every
+ * stream's).  Waits for the device to finish its work first (this is not a
+ * compute call).  Safe to call more than once; later calls re-allocate on
+ * demand. */
 void txl_shutdown(void);
 
 #ifdef __cplusplus

@@ -1,5 +1,8 @@
 """Shared helpers for the GPU parity tests: seeded inputs -> device tensors,
 the oracle on exactly the values the device saw, and error measures."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -51,3 +54,15 @@ def gather_rows(out, rows):
 
 def unit_shape(B, H, D, L, M):
     return inputs.LayerShape(B, H, D, L, M)
+
+
+def record_error(case, shape, err, tol):
+    """Append one parity result (the case, its shape, the max abs error and
+    the tolerance) to the JSON-lines file named by TXL_PARITY_LOG, if set, so
+    a run reports how much of each tolerance the kernels use."""
+    path = os.environ.get("TXL_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": case, "shape": [int(x) for x in shape], "max_abs_err": float(err),
+                            "tol": float(tol)}) + "\n")

@@ -71,3 +71,28 @@ def test_plan_query_rejects_bad_shapes():
         txl.rel_attn_fwd_plan(1, -1, 16, 2, 64, txl.TXL_BF16)
     with pytest.raises(txl.TxlError, match="unsupported"):
         txl.rel_attn_fwd_plan(1, 16, 16, 2, 65, txl.TXL_BF16)        # bf16 head size past 64
+
+
+def test_noalloc_binding_checks_like_the_default_entry():
+    # the no-alloc entry point refuses what rel_attn_fwd refuses, and also a
+    # missing output (it would have to allocate one)
+    p = _layer()
+    q, k, v, r, u, w = (p[n] for n in ("q", "k", "v", "r", "u", "w"))
+    out = torch.zeros_like(q)
+    with pytest.raises(ValueError, match="out must be given"):
+        txl.rel_attn_fwd_noalloc(q, k, v, r, u, w, mem_len=M, out=None)
+    with pytest.raises(ValueError, match="k must be"):
+        txl.rel_attn_fwd_noalloc(q, k[:-1], v, r, u, w, mem_len=M, out=out)
+    with pytest.raises(ValueError, match="k must be"):
+        txl.rel_attn_fwd_noalloc(q, k, v, r, u, w, mem_len=M + 1, out=out)
+    with pytest.raises(TypeError, match="dtype"):
+        txl.rel_attn_fwd_noalloc(q, k, v.float(), r, u, w, mem_len=M, out=out)
+    with pytest.raises(ValueError, match="u_bias"):
+        txl.rel_attn_fwd_noalloc(q, k, v, r, u[:, :1], w, mem_len=M, out=out)
+    with pytest.raises(ValueError, match="out must be"):
+        txl.rel_attn_fwd_noalloc(q, k, v, r, u, w, mem_len=M, out=out[:1])
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.rel_attn_fwd_noalloc(q, k, v, r, u, w, mem_len=M, out=out)
+    r_strided = torch.zeros(T, D, H, dtype=r.dtype).transpose(1, 2)     # right shape, not contiguous
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.rel_attn_fwd_noalloc(q, k, v, r_strided, u, w, mem_len=M, out=out)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from tests.helpers import (TOL_BF16, TOL_F32, device_layer, gather_rows, oracle_full,
-                           oracle_rows, run_library, unit_shape)
+                           oracle_rows, record_error, run_library, unit_shape)
 from transformer_xl_relative_rel_gb300 import inputs
 from transformer_xl_relative_rel_gb300.workloads import WORKLOADS
 
@@ -35,6 +35,7 @@ def _check_full(B, H, D, L, M, dtype, seed, tol):
     ref = oracle_full(host, M)
     got = out.double().cpu().numpy()
     err = np.abs(got - ref).max()
+    record_error("full_" + ("f32" if dtype == torch.float32 else "bf16"), (B, H, D, L, M), err, tol)
     assert np.isfinite(got).all()
     assert err <= tol, f"max abs err {err:.3e} > {tol} for B{B} H{H} D{D} L{L} M{M} {dtype}"
     return err
@@ -109,6 +110,7 @@ def test_bf16_full_size_unit_variance(name):
     ref = oracle_rows(host, s.mem_len, rows)
     got = gather_rows(out, rows)
     err = np.abs(got - ref).max()
+    record_error("full_size_unit_" + name, (s.batch, s.heads, s.d_head, s.seg_len, s.mem_len), err, TOL_BF16)
     assert err <= TOL_BF16, f"{name}: max abs err {err:.3e}"
     assert torch.isfinite(out.float()).all()
 
@@ -128,6 +130,7 @@ def test_bf16_recompute_vs_reuse_shapes(B, H, L, M):
     rows = inputs.sample_rows(s, 900 + L, n_random=128, all_heads_of_b0=False)
     ref = oracle_rows(host, M, rows)
     err = np.abs(gather_rows(out, rows) - ref).max()
+    record_error("recompute_vs_reuse", (B, H, 64, L, M), err, TOL_BF16)
     assert err <= TOL_BF16, f"max abs err {err:.3e}"
 
 
@@ -196,4 +199,5 @@ def test_near_limits_sampled_rows(B, H, D, L, M, dtype):
     rows = inputs.sample_rows(s, 1234 + H, n_random=96, all_heads_of_b0=False)
     ref = oracle_rows(host, M, rows)
     err = np.abs(gather_rows(out, rows) - ref).max()
+    record_error("near_limits", (B, H, D, L, M), err, TOL_BF16 if dtype == torch.bfloat16 else TOL_F32)
     assert err <= (TOL_BF16 if dtype == torch.bfloat16 else TOL_F32), f"max abs err {err:.3e}"

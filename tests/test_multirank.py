@@ -68,3 +68,25 @@ def test_two_ranks_gloo(tmp_path):
     full = oracle.rel_attn(p["q"], p["k"], p["v"], p["r"], p["u"], p["w"], mem_len=shape.mem_len)
     parts = np.concatenate([np.load(tmp_path / f"part{r}.npy") for r in range(world)], axis=1)
     assert np.array_equal(parts, full)
+
+
+def test_bench_launches_its_own_ranks():
+    """``bench.py --gpus 2`` started without a launcher starts two ranks
+    itself (torch.distributed.run on 127.0.0.1); the dry-run leg makes no
+    CUDA call, so the launcher, the gloo barrier and the max-over-ranks
+    timing run here on the CPU.  Rank 0 alone prints one line naming both."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run",
+                          "--steps", "5", "--warmup", "3"], capture_output=True, text=True, timeout=300,
+                         env=env, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = lines[0]
+    assert line["n_gpus"] == 2 and line["dry_run"] and line["steps"] == 5
+    # whole-job rate: both ranks' units over the slowest rank's time
+    assert abs(line["value"] - 2 * 1000.0 * 5 / (line["ms_per_step"] * 5 / 1e3)) <= 1e-6 * line["value"]

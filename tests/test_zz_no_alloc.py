@@ -48,6 +48,13 @@ def _call_default(lib, dev, out, mem_len):
 @pytest.mark.parametrize("B,H,D,L,M", [(1, 4, 64, 128, 1600),    # key split + combine
                                        (2, 2, 41, 130, 900)])    # split, no-TMA loads
 def test_noalloc_matches_default_on_two_calls(lib, B, H, D, L, M):
+    import transformer_xl_relative_rel_gb300 as txl
+    # both shapes must take the split path, or the fixed array goes unused.
+    # The plan query prices head sizes other than 64 at the padded width 64;
+    # this entry point runs D = 41 at its own width, whose split partials are
+    # smaller, which only makes a split cheaper against the unsplit call.
+    splits, _ = txl.rel_attn_fwd_plan(B, M, L, H, D, txl.TXL_BF16)
+    assert splits > 1, f"shape {(B, H, D, L, M)} does not split its keys ({splits})"
     for call in range(2):                       # the second call reuses the array
         p = inputs.unit_layer(unit_shape(B, H, D, L, M), 300 + call)
         dev, host = device_layer(p, torch.bfloat16)

@@ -136,13 +136,13 @@ def _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out):
     for name, t in (("u_bias", u_bias), ("v_bias", v_bias)):
         if t is not None and (tuple(t.shape) != (H, D) or t.dtype != torch.float32):
             raise ValueError(f"{name} must be float32 [{H}, {D}] or None")
-    for t in (q, k, v, r, u_bias, v_bias):
+    if out is not None and (tuple(out.shape) != (L, B, H, D) or out.dtype != q.dtype):
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    for t in (q, k, v, r, u_bias, v_bias, out):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("all tensors must be contiguous CUDA tensors")
     if out is None:
         out = torch.empty_like(q)
-    elif tuple(out.shape) != (L, B, H, D) or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped and typed like q")
     return out
 
 
@@ -347,8 +347,12 @@ def ring_append(ring, rows, start: int, stream=None):
 def rel_attn_fwd_noalloc(q, k, v, r, u_bias, v_bias, mem_len: int, out, stream=None):
     """The same call through txl_rel_attn_fwd_noalloc, for callers that may not
     allocate device memory: ``out`` must be given, and the library allocates
-    nothing (its split-key scratch is a fixed array in the library)."""
+    nothing (its split-key scratch is a fixed array in the library).  The
+    arguments are checked exactly as ``rel_attn_fwd`` checks them."""
+    if out is None:
+        raise ValueError("out must be given: this entry point allocates nothing")
     L, B, H, D = q.shape
+    _check_attn(q, k, v, r, u_bias, v_bias, mem_len, out)
     code = _dtype_code(q)
     st = load_library().txl_rel_attn_fwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(u_bias), _ptr(v_bias),

@@ -44,46 +44,63 @@ int device_sm_count()
     return cached[dev];
 }
 
-// Library-owned scratch for split-key partial results, one buffer per device.
+// Library-owned scratch for split-key partial results and padded head copies:
+// one buffer per (device, stream).  Calls on one stream run in order, so a
+// stream's buffer is never used by two kernels at once, and calls on
+// different streams never share one.  A buffer grows in stream order
+// (cudaFreeAsync of the old one, cudaMallocAsync of the new one, both on that
+// stream), so growing it waits for nothing on the host.
 namespace {
 struct Scratch {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
     void *ptr = nullptr;
     size_t bytes = 0;
 };
+constexpr int kMaxScratch = 256;   // (device, stream) pairs served until txl_shutdown
 std::mutex g_scratch_mu;
-Scratch g_scratch[64];
+Scratch g_scratch[kMaxScratch];
+int g_scratch_n = 0;
 
 txl_status get_scratch(size_t bytes, cudaStream_t stream, void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= 64) return TXL_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    Scratch &s = g_scratch[dev];
-    if (s.bytes < bytes) {
+    Scratch *s = nullptr;
+    for (int x = 0; x < g_scratch_n; ++x)
+        if (g_scratch[x].dev == dev && g_scratch[x].stream == stream) s = &g_scratch[x];
+    if (!s) {
+        if (g_scratch_n == kMaxScratch) return TXL_ERR_UNSUPPORTED;
+        s = &g_scratch[g_scratch_n++];
+        *s = Scratch{};
+        s->dev = dev;
+        s->stream = stream;
+    }
+    if (s->bytes < bytes) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         e = cudaStreamIsCapturing(stream, &cs);
         if (e != cudaSuccess) return cuda_fail(e);
         // growing the buffer allocates; a call made once outside capture first
         // sizes it, after which captured calls reuse it.
         if (cs != cudaStreamCaptureStatusNone) return TXL_ERR_UNSUPPORTED;
-        if (s.ptr) {
-            e = cudaDeviceSynchronize();   // earlier launches may still read it
+        if (s->ptr) {
+            // earlier calls on this stream may still read it: freed in stream order
+            e = cudaFreeAsync(s->ptr, stream);
+            s->ptr = nullptr;
+            s->bytes = 0;
             if (e != cudaSuccess) return cuda_fail(e);
-            cudaFree(s.ptr);
-            s.ptr = nullptr;
-            s.bytes = 0;
         }
-        size_t want = bytes + bytes / 4;
-        e = cudaMalloc(&s.ptr, want);
+        const size_t want = bytes + bytes / 4;
+        e = cudaMallocAsync(&s->ptr, want, stream);
         if (e != cudaSuccess) {
-            s.ptr = nullptr;
+            s->ptr = nullptr;
             return cuda_fail(e);
         }
-        s.bytes = want;
+        s->bytes = want;
     }
-    *out = s.ptr;
+    *out = s->ptr;
     return TXL_OK;
 }
 
@@ -413,15 +430,24 @@ int txl_version(void) { return 200; }   // 0.2.0: log-sum-exp, fused rollover, p
 void txl_shutdown(void)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    Scratch &s = g_scratch[dev];
-    if (s.ptr) {
-        cudaDeviceSynchronize();
-        cudaFree(s.ptr);
+    bool synced = false;
+    int kept = 0;
+    for (int x = 0; x < g_scratch_n; ++x) {
+        Scratch &s = g_scratch[x];
+        if (s.dev != dev) {
+            g_scratch[kept++] = s;
+            continue;
+        }
+        if (s.ptr) {
+            if (!synced) cudaDeviceSynchronize();   // every call that may read a buffer is done
+            synced = true;
+            cudaFree(s.ptr);
+        }
     }
-    s.ptr = nullptr;
-    s.bytes = 0;
+    g_scratch_n = kept;
+    cudaGetLastError();
     blas_shutdown();
 }
 
