@@ -14,6 +14,11 @@ Contents
   * ``mem_update`` -- the memory rollover of Section 3.2 written as its plain
     definition in numpy: the new memory is the newest M rows of
     [old memory; current hidden states].
+  * ``project_heads`` -- the projections of Section 3.3's procedure
+    (q = h W_q, k = h~ W_kE, v = h~ W_v) in float64, laid out per head.
+  * ``sinusoid`` / ``rel_table`` -- the relative encoding R (the sinusoid of
+    Vaswani et al. that Section 3.3 re-uses) and Appendix B's reversed
+    projected table Q_t = W_kR R_{T-1-t}, in float64.
 
 All functions take numpy arrays in the T-major layouts of the library:
 ``q, out: [L, B, H, D]``, ``k, v: [T, B, H, D]`` with ``T = M + L``,
@@ -191,3 +196,50 @@ def mem_update(ext_ctx, mem_len: int) -> np.ndarray:
     if mem_len == 0:
         return ext[:0].copy()
     return ext[ext.shape[0] - mem_len:].copy()
+
+
+def project_heads(x, w, heads: int, d_head: int, d_pad: Optional[int] = None) -> np.ndarray:
+    """One projection of Section 3.3's procedure, per head, in float64.
+
+    ``x`` [..., d_in] (hidden states, e.g. the extended context
+    [SG(memory); h] for k and v, the segment h for q) times ``w``
+    [d_in, heads*d_head]: element (..., h, d) is sum_c x[..., c] w[c, h*d_head + d].
+    The result is [..., heads, d_pad] with zeros in columns d_head..d_pad-1
+    (``d_pad`` defaults to ``d_head``).
+    """
+    x = _f64(x)
+    w = _f64(w)
+    d_pad = d_head if d_pad is None else d_pad
+    if w.shape != (x.shape[-1], heads * d_head):
+        raise ValueError(f"w must be [{x.shape[-1]}, {heads * d_head}], got {w.shape}")
+    if d_pad < d_head:
+        raise ValueError("d_pad < d_head")
+    y = np.matmul(x, w).reshape(x.shape[:-1] + (heads, d_head))
+    out = np.zeros(x.shape[:-1] + (heads, d_pad))
+    out[..., :d_head] = y
+    return out
+
+
+def sinusoid(n_pos: int, d_model: int) -> np.ndarray:
+    """The relative encoding R as a [n_pos, d_model] float64 table, row p for
+    distance p: frequencies w_c = 10000^(-2c/d_model) for column pairs
+    (2c, 2c+1), column 2c = sin(p w_c), column 2c+1 = cos(p w_c) (a last odd
+    column is a sine)."""
+    out = np.zeros((n_pos, d_model))
+    for c2 in range(0, d_model, 2):
+        freq = 10000.0 ** (-c2 / d_model)
+        ang = np.arange(n_pos, dtype=np.float64) * freq
+        out[:, c2] = np.sin(ang)
+        if c2 + 1 < d_model:
+            out[:, c2 + 1] = np.cos(ang)
+    return out
+
+
+def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: Optional[int] = None) -> np.ndarray:
+    """Appendix B's table in the library's row order, float64 [klen, heads, d_pad]:
+    row t holds W_kR R_{klen-1-t} (the projection of distance klen-1-t), split
+    into heads, zeros past d_head.  ``w_r`` is W_kR as [d_model, heads*d_head]."""
+    w_r = _f64(w_r)
+    R = sinusoid(klen, w_r.shape[0])
+    by_distance = project_heads(R, w_r, heads, d_head, d_pad)      # row p: distance p
+    return np.ascontiguousarray(by_distance[::-1])

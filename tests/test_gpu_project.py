@@ -1,6 +1,7 @@
 """Projections into the attention layout, the device-built relative table and
-attention on padded heads (CUDA, `-m gpu`).  References: float64 numpy on
-exactly the values the device read, the oracle for the attention."""
+attention on padded heads (CUDA, `-m gpu`).  References: the oracle's float64
+projections and table on exactly the values the device read, and its
+attention."""
 import numpy as np
 import pytest
 import torch
@@ -25,9 +26,9 @@ def test_project_heads(dtype, rtol, rows, d_in, heads, d_head, d_pad):
     x = torch.randn(rows, d_in, generator=g, device="cuda").to(dtype)
     w = (0.05 * torch.randn(d_in, heads * d_head, generator=g, device="cuda")).to(dtype)
     y = txl.project_heads(x, w, heads, d_head, d_pad)
-    ref = (x.double().cpu().numpy() @ w.double().cpu().numpy()).reshape(rows, heads, d_head)
+    ref = oracle.project_heads(x.double().cpu().numpy(), w.double().cpu().numpy(), heads, d_head, d_pad)
     got = y.double().cpu().numpy()
-    assert _rel_err(got[..., :d_head], ref) <= rtol
+    assert _rel_err(got[..., :d_head], ref[..., :d_head]) <= rtol
     assert (got[..., d_head:] == 0).all()
 
 
@@ -39,10 +40,9 @@ def test_rel_table(dtype, rtol, klen, d_model, heads, d_head, d_pad):
     g = torch.Generator(device="cuda").manual_seed(klen + d_model)
     w_r = (0.02 * torch.randn(d_model, heads * d_head, generator=g, device="cuda")).to(dtype)
     r = txl.rel_table(w_r, klen, heads, d_head, d_pad)
-    R = inputs.sinusoid(klen, d_model)[::-1]            # row t: distance klen-1-t (Appendix B)
-    ref = (R @ w_r.double().cpu().numpy()).reshape(klen, heads, d_head)
+    ref = oracle.rel_table(w_r.double().cpu().numpy(), klen, heads, d_head, d_pad)   # row t: distance klen-1-t
     got = r.double().cpu().numpy()
-    assert _rel_err(got[..., :d_head], ref) <= rtol
+    assert _rel_err(got[..., :d_head], ref[..., :d_head]) <= rtol
     assert (got[..., d_head:] == 0).all()
 
 

@@ -483,3 +483,140 @@ def test_pins_catch_planted_mistake(tmp_path, name):
     assert _pins_pass(oracle), "pins must pass on the real oracle"
     mod = _build_mutant(tmp_path, name)
     assert not _pins_pass(mod), f"planted mistake {name!r} went unnoticed"
+
+
+# ---------------------------------------------------------------------------
+# Projections and the relative table (Section 3.3 procedure, Appendix B)
+# ---------------------------------------------------------------------------
+def _pin_projections_end_to_end(project_heads, rel_table, sinusoid):
+    """q, k, v from the oracle's projections of [memory; segment] states and
+    Q from its table, through the oracle's attention, equal the four-term
+    expansion with W_kR R_{i-j} projected per pair (R by distance)."""
+    g = np.random.Generator(np.random.PCG64(77))
+    B, H, D, L, M = 2, 2, 3, 5, 4
+    T, dm = M + L, H * D
+    h_ext = g.standard_normal((T, B, dm))
+    Wq, Wk, Wv, Wr = (g.standard_normal((dm, dm)) * 0.5 for _ in range(4))
+    u, w = g.standard_normal((H, D)), g.standard_normal((H, D))
+    R = sinusoid(T, dm)
+    ref = _four_term_bruteforce(h_ext, Wq, Wk, Wv, Wr, R, u, w, B, H, D, L, M)
+    q = project_heads(h_ext[M:], Wq, H, D)
+    k = project_heads(h_ext, Wk, H, D)
+    v = project_heads(h_ext, Wv, H, D)
+    Q = rel_table(Wr, T, H, D)
+    got = oracle.rel_attn(q, k, v, Q, u, w, mem_len=M)
+    return np.abs(got - ref).max() <= TOL * max(1.0, np.abs(ref).max())
+
+
+def _pin_sinusoid(sinusoid):
+    """The sinusoid of Vaswani et al. by its stated properties, not its
+    formula: distance 0 encodes as [0, 1, 0, 1, ...]; each column pair is a
+    (sin, cos) of one angle; the angles per unit distance, read back with
+    atan2, form a geometric progression from 1 down to 1/10000 over the
+    pairs (wavelengths 2 pi .. 10000 * 2 pi); and the encoding of p + k is a
+    fixed rotation (depending on k only) of the encoding of p."""
+    dm, n = 16, 40
+    R = sinusoid(n, dm)
+    ok = R.shape == (n, dm)
+    ok &= np.array_equal(R[0], np.tile([0.0, 1.0], dm // 2))
+    ok &= np.abs(R[:, 0::2] ** 2 + R[:, 1::2] ** 2 - 1.0).max() < 1e-12
+    omega = np.arctan2(R[1, 0::2], R[1, 1::2])
+    ratio = 10000.0 ** (-2.0 / dm)
+    ok &= abs(omega[0] - 1.0) < 1e-12
+    ok &= np.abs(omega[1:] / omega[:-1] - ratio).max() < 1e-9
+    for kk in (1, 3, 17):
+        for c in range(dm // 2):
+            s, co = np.sin(kk * omega[c]), np.cos(kk * omega[c])
+            rot = np.array([[co, s], [-s, co]])          # [sin(a+b), cos(a+b)] from [sin a, cos a]
+            pair = R[:n - kk, 2 * c:2 * c + 2]
+            ok &= np.abs(pair @ rot.T - R[kk:, 2 * c:2 * c + 2]).max() < 1e-9
+    return bool(ok)
+
+
+def _pin_padding(project_heads, rel_table):
+    """Zero columns past d_head; the first d_head columns are the unpadded result."""
+    g = np.random.Generator(np.random.PCG64(5))
+    x, w = g.standard_normal((3, 4, 10)), g.standard_normal((10, 2 * 3))
+    a, b = project_heads(x, w, 2, 3), project_heads(x, w, 2, 3, 8)
+    t, tp = rel_table(w, 6, 2, 3), rel_table(w, 6, 2, 3, 8)
+    return (b.shape == (3, 4, 2, 8) and np.array_equal(b[..., 3:], np.zeros((3, 4, 2, 5)))
+            and np.array_equal(b[..., :3], a) and np.array_equal(tp[..., :3], t)
+            and not tp[..., 3:].any())
+
+
+def test_projection_and_table_pins():
+    assert _pin_projections_end_to_end(oracle.project_heads, oracle.rel_table, oracle.sinusoid)
+    assert _pin_sinusoid(oracle.sinusoid)
+    assert _pin_padding(oracle.project_heads, oracle.rel_table)
+
+
+def _mutant_project_transposed_heads(x, w, heads, d_head, d_pad=None):
+    # heads and head columns interleaved the wrong way round
+    y = np.matmul(np.asarray(x, float), np.asarray(w, float))
+    y = y.reshape(y.shape[:-1] + (d_head, heads)).swapaxes(-1, -2)
+    return oracle.project_heads(x, w, heads, d_head, d_pad) * 0 + np.pad(
+        y, [(0, 0)] * (y.ndim - 1) + [(0, (d_pad or d_head) - d_head)])
+
+
+def _mutant_table_not_reversed(w_r, klen, heads, d_head, d_pad=None):
+    return oracle.rel_table(w_r, klen, heads, d_head, d_pad)[::-1]
+
+
+def _mutant_table_off_by_one(w_r, klen, heads, d_head, d_pad=None):
+    R = oracle.sinusoid(klen + 1, np.asarray(w_r).shape[0])[1:]       # distances 1..klen
+    return oracle.project_heads(R, w_r, heads, d_head, d_pad)[::-1]
+
+
+def _mutant_sin_cos_swapped(n_pos, d_model):
+    R = oracle.sinusoid(n_pos, d_model)
+    out = R.copy()
+    out[:, 0::2], out[:, 1::2] = R[:, 1::2], R[:, 0::2]
+    return out
+
+
+def _mutant_frequency_exponent(n_pos, d_model):
+    out = np.zeros((n_pos, d_model))
+    for c2 in range(0, d_model, 2):
+        f = 10000.0 ** (-c2 / (2 * d_model))          # half the exponent
+        out[:, c2] = np.sin(np.arange(n_pos) * f)
+        out[:, c2 + 1] = np.cos(np.arange(n_pos) * f)
+    return out
+
+
+def _mutant_cos_frequency(n_pos, d_model):
+    out = oracle.sinusoid(n_pos, d_model)
+    for c2 in range(0, d_model, 2):                     # cos column uses the next pair's frequency
+        f = 10000.0 ** (-min(c2 + 2, d_model - 2) / d_model)
+        out[:, c2 + 1] = np.cos(np.arange(n_pos) * f)
+    return out
+
+
+def _mutant_padding_garbage(x, w, heads, d_head, d_pad=None):
+    y = oracle.project_heads(x, w, heads, d_head, d_pad)
+    if d_pad and d_pad > d_head:
+        y[..., d_head:] = 1.0
+    return y
+
+
+@pytest.mark.parametrize("name", ["project_heads_transposed", "table_not_reversed", "table_off_by_one",
+                                  "sin_cos_swapped", "frequency_exponent", "cos_frequency",
+                                  "padding_garbage"])
+def test_projection_pins_catch_planted_mistakes(name):
+    ph, rt, sn = oracle.project_heads, oracle.rel_table, oracle.sinusoid
+    if name == "project_heads_transposed":
+        ph = _mutant_project_transposed_heads
+    elif name == "table_not_reversed":
+        rt = _mutant_table_not_reversed
+    elif name == "table_off_by_one":
+        rt = _mutant_table_off_by_one
+    elif name == "sin_cos_swapped":
+        sn = _mutant_sin_cos_swapped
+    elif name == "frequency_exponent":
+        sn = _mutant_frequency_exponent
+    elif name == "cos_frequency":
+        sn = _mutant_cos_frequency
+    elif name == "padding_garbage":
+        ph = _mutant_padding_garbage
+    caught = (not _pin_projections_end_to_end(ph, rt, sn)) or (not _pin_sinusoid(sn)) or \
+        (not _pin_padding(ph, rt))
+    assert caught, f"planted mistake {name} passed every pin"
