@@ -196,24 +196,33 @@ txl_status txl_rel_attn_fwd_padded(const void *q, const void *k, const void *v, 
                                    void *out, void *stream);
 
 /*
- * txl_project_heads -- the projections of Section 3.3 (W_q, W_kE, W_v) into
- * the attention's layout: y[rows][heads][d_pad] = x[rows][d_in] .
- * W[d_in][heads*d_head], padding columns d_head..d_pad-1 set to zero.  With
+ * txl_project_heads -- the projections of Section 3.3's procedure
+ * (q = h W_q^T, k = h~ W_kE^T, v = h~ W_v^T) into the attention's layout:
+ *     y[rows][heads][d_pad] = x[rows][d_in] . W^T
+ * with W in the paper's layout, [heads*d_head][d_in] (row h*d_head + d is
+ * output column d of head h; also torch.nn.Linear's weight layout), and
+ * padding columns d_head..d_pad-1 of every head exactly zero.  With
  * x = a T-major [positions][batch][d_model] buffer (rows = positions*batch)
- * the result is the T-major [positions][batch][heads][d_pad] layout.  A plain
- * GEMM (cuBLAS, fp32 accumulation); x, w, out device, row-major, dtype
- * elements, out must not overlap x or w.  d_pad >= d_head >= 1.
+ * the result is the T-major [positions][batch][heads][d_pad] layout.
+ * bf16: the library's tcgen05 GEMM (fp32 accumulation, one rounding to
+ * bf16), for d_in even and x, w 4-byte aligned (TMA operand loads when d_in
+ * is a multiple of 8, x and w 16-byte aligned and d_pad divides 256; TMA
+ * output stores when out is 16-byte aligned and heads*d_pad*2 a multiple of
+ * 16); fp32 and other bf16 shapes: a CUDA-core kernel (fp32 accumulation).
+ * x, w, out device, row-major, dtype elements; out must not overlap x or w.
+ * d_pad >= d_head >= 1; d_in == 0 gives zeros.
  */
 txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, int d_in, int heads,
                              int d_head, int d_pad, txl_dtype dtype, void *stream);
 
 /*
  * txl_rel_table -- Appendix B's reversed projected table of one layer:
- * out[t][h][d] = sum_c R[klen-1-t][c] * W_kR[c][h*d_head + d] for t < klen,
+ * out[t][h][d] = sum_c R[klen-1-t][c] * W_kR[h*d_head + d][c] for t < klen,
  * R[p][2c] = sin(p * 10000^(-2c/d_model)), R[p][2c+1] = cos(the same angle)
  * (the sinusoid of the relative distance p, evaluated in fp32 on the device;
- * fp32 accumulation).  out [klen][heads][d_pad], padding zero; W_kR
- * [d_model][heads*d_head].  Batch- and segment-independent: once per layer.
+ * fp32 accumulation).  out [klen][heads][d_pad], padding zero; W_kR in the
+ * paper's layout [heads*d_head][d_model].  Batch- and segment-independent:
+ * once per layer.
  */
 txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int heads, int d_head, int d_pad,
                          txl_dtype dtype, void *stream);

@@ -202,19 +202,20 @@ def project_heads(x, w, heads: int, d_head: int, d_pad: Optional[int] = None) ->
     """One projection of Section 3.3's procedure, per head, in float64.
 
     ``x`` [..., d_in] (hidden states, e.g. the extended context
-    [SG(memory); h] for k and v, the segment h for q) times ``w``
-    [d_in, heads*d_head]: element (..., h, d) is sum_c x[..., c] w[c, h*d_head + d].
-    The result is [..., heads, d_pad] with zeros in columns d_head..d_pad-1
-    (``d_pad`` defaults to ``d_head``).
+    [SG(memory); h] for k and v, the segment h for q) times ``w``^T, with
+    ``w`` the paper's projection matrix [heads*d_head, d_in] (q = h W_q^T):
+    element (..., h, d) is sum_c x[..., c] w[h*d_head + d, c].  The result is
+    [..., heads, d_pad] with zeros in columns d_head..d_pad-1 (``d_pad``
+    defaults to ``d_head``).
     """
     x = _f64(x)
     w = _f64(w)
     d_pad = d_head if d_pad is None else d_pad
-    if w.shape != (x.shape[-1], heads * d_head):
-        raise ValueError(f"w must be [{x.shape[-1]}, {heads * d_head}], got {w.shape}")
+    if w.shape != (heads * d_head, x.shape[-1]):
+        raise ValueError(f"w must be [{heads * d_head}, {x.shape[-1]}], got {w.shape}")
     if d_pad < d_head:
         raise ValueError("d_pad < d_head")
-    y = np.matmul(x, w).reshape(x.shape[:-1] + (heads, d_head))
+    y = np.matmul(x, w.T).reshape(x.shape[:-1] + (heads, d_head))
     out = np.zeros(x.shape[:-1] + (heads, d_pad))
     out[..., :d_head] = y
     return out
@@ -238,8 +239,9 @@ def sinusoid(n_pos: int, d_model: int) -> np.ndarray:
 def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: Optional[int] = None) -> np.ndarray:
     """Appendix B's table in the library's row order, float64 [klen, heads, d_pad]:
     row t holds W_kR R_{klen-1-t} (the projection of distance klen-1-t), split
-    into heads, zeros past d_head.  ``w_r`` is W_kR as [d_model, heads*d_head]."""
+    into heads, zeros past d_head.  ``w_r`` is W_kR in the paper's layout,
+    [heads*d_head, d_model]."""
     w_r = _f64(w_r)
-    R = sinusoid(klen, w_r.shape[0])
+    R = sinusoid(klen, w_r.shape[1])
     by_distance = project_heads(R, w_r, heads, d_head, d_pad)      # row p: distance p
     return np.ascontiguousarray(by_distance[::-1])

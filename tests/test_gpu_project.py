@@ -17,6 +17,12 @@ def _rel_err(got, ref):
     return np.abs(got - ref).max() / max(1e-12, np.abs(ref).max())
 
 
+def _bf16_close(got, ref, d_in):
+    """bf16 output of an fp32-accumulated product: one bf16 unit in the last
+    place of the reference plus the fp32 accumulation error of d_in terms."""
+    return np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6 * np.sqrt(d_in) * (1 + np.abs(ref))
+
+
 @pytest.mark.parametrize("dtype,rtol", [(torch.float32, 1e-5), (torch.bfloat16, 1e-2)])
 @pytest.mark.parametrize("rows,d_in,heads,d_head,d_pad", [(300, 410, 10, 41, 64), (96, 64, 2, 32, 32),
                                                           (7, 24, 3, 5, 8)])
@@ -24,12 +30,68 @@ def test_project_heads(dtype, rtol, rows, d_in, heads, d_head, d_pad):
     import transformer_xl_relative_rel_gb300 as txl
     g = torch.Generator(device="cuda").manual_seed(rows + d_in)
     x = torch.randn(rows, d_in, generator=g, device="cuda").to(dtype)
-    w = (0.05 * torch.randn(d_in, heads * d_head, generator=g, device="cuda")).to(dtype)
+    w = (0.05 * torch.randn(heads * d_head, d_in, generator=g, device="cuda")).to(dtype)
     y = txl.project_heads(x, w, heads, d_head, d_pad)
     ref = oracle.project_heads(x.double().cpu().numpy(), w.double().cpu().numpy(), heads, d_head, d_pad)
     got = y.double().cpu().numpy()
     assert _rel_err(got[..., :d_head], ref[..., :d_head]) <= rtol
     assert (got[..., d_head:] == 0).all()
+
+
+# the tensor-core GEMM: several 128-row tiles with a ragged last one, K tails
+# (d_in not a multiple of 64), one and several 256-column tiles, padded heads,
+# TMA operand loads (d_in % 8 == 0) and the cp.async loaders (d_in % 8 != 0)
+@pytest.mark.parametrize("rows,d_in,heads,d_head,d_pad", [
+    (1000, 512, 8, 64, 64),       # char-LM head shape, two 256-column tiles
+    (777, 1024, 16, 64, 64),      # large-LM, four column tiles, ragged rows
+    (300, 410, 10, 41, 64),       # base-LM: cp.async loaders (row pitch 820 bytes), padded heads
+    (129, 96, 3, 32, 32),         # one 96-column tile, K tail
+    (50, 200, 5, 48, 48),         # 240 columns, 48-wide heads (TMA box of 5 heads)
+    (130, 66, 4, 20, 24),         # cp.async, heads padded 20 -> 24, output rows 192 bytes
+    (5, 16, 1, 16, 16),           # a single small tile
+])
+def test_project_heads_tensor_core(rows, d_in, heads, d_head, d_pad):
+    import transformer_xl_relative_rel_gb300 as txl
+    g = torch.Generator(device="cuda").manual_seed(7 * rows + d_in)
+    x = torch.randn(rows, d_in, generator=g, device="cuda").bfloat16()
+    w = (0.02 * torch.randn(heads * d_head, d_in, generator=g, device="cuda")).bfloat16()
+    y = torch.full((rows, heads, d_pad), float("nan"), dtype=torch.bfloat16, device="cuda")
+    txl.project_heads(x, w, heads, d_head, d_pad, out=y)
+    ref = oracle.project_heads(x.double().cpu().numpy(), w.double().cpu().numpy(), heads, d_head, d_pad)
+    got = y.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert _bf16_close(got, ref, d_in).all(), f"max abs err {np.abs(got - ref).max():.3e}"
+    assert (got[..., d_head:] == 0).all()
+    # the same product again (the pipeline's barriers restart cleanly)
+    y2 = txl.project_heads(x, w, heads, d_head, d_pad)
+    assert torch.equal(y, y2)
+
+
+def test_project_heads_padding_stays_zero_with_inf_inputs():
+    """Padding columns are written as zeros, not as products with zero
+    weights (an infinite input would make those NaN)."""
+    import transformer_xl_relative_rel_gb300 as txl
+    x = torch.randn(256, 128, device="cuda").bfloat16()
+    x[3, 5] = float("inf")
+    w = (0.02 * torch.randn(4 * 24, 128, device="cuda")).bfloat16()
+    y = txl.project_heads(x, w, 4, 24, 32)
+    assert (y[..., 24:] == 0).all()
+
+
+def test_project_heads_full_size_sampled_rows():
+    """char-LM evaluation's k projection: [M+L]*B = 86,416 rows of 512, as the
+    chain runs it; sampled rows against the oracle."""
+    import transformer_xl_relative_rel_gb300 as txl
+    T, B, dm, H, D = 3928, 22, 512, 8, 64
+    g = torch.Generator(device="cuda").manual_seed(3928)
+    x = torch.randn(T, B, dm, generator=g, device="cuda").bfloat16()
+    w = (0.02 * torch.randn(H * D, dm, generator=g, device="cuda")).bfloat16()
+    y = txl.project_heads(x, w, H, D, D)
+    sel = np.random.Generator(np.random.PCG64(1)).choice(T * B, 256, replace=False)
+    xs = x.reshape(T * B, dm)[torch.tensor(sel, device="cuda")].double().cpu().numpy()
+    ref = oracle.project_heads(xs, w.double().cpu().numpy(), H, D)
+    got = y.reshape(T * B, H, D)[torch.tensor(sel, device="cuda")].double().cpu().numpy()
+    assert _bf16_close(got, ref, dm).all(), f"max abs err {np.abs(got - ref).max():.3e}"
 
 
 @pytest.mark.parametrize("dtype,rtol", [(torch.float32, 2e-4), (torch.bfloat16, 1e-2)])
@@ -38,7 +100,7 @@ def test_project_heads(dtype, rtol, rows, d_in, heads, d_head, d_pad):
 def test_rel_table(dtype, rtol, klen, d_model, heads, d_head, d_pad):
     import transformer_xl_relative_rel_gb300 as txl
     g = torch.Generator(device="cuda").manual_seed(klen + d_model)
-    w_r = (0.02 * torch.randn(d_model, heads * d_head, generator=g, device="cuda")).to(dtype)
+    w_r = (0.02 * torch.randn(heads * d_head, d_model, generator=g, device="cuda")).to(dtype)
     r = txl.rel_table(w_r, klen, heads, d_head, d_pad)
     ref = oracle.rel_table(w_r.double().cpu().numpy(), klen, heads, d_head, d_pad)   # row t: distance klen-1-t
     got = r.double().cpu().numpy()

@@ -500,10 +500,11 @@ def _pin_projections_end_to_end(project_heads, rel_table, sinusoid):
     u, w = g.standard_normal((H, D)), g.standard_normal((H, D))
     R = sinusoid(T, dm)
     ref = _four_term_bruteforce(h_ext, Wq, Wk, Wv, Wr, R, u, w, B, H, D, L, M)
-    q = project_heads(h_ext[M:], Wq, H, D)
-    k = project_heads(h_ext, Wk, H, D)
-    v = project_heads(h_ext, Wv, H, D)
-    Q = rel_table(Wr, T, H, D)
+    # the paper's projection matrices are [out, in]: q = h W_q^T
+    q = project_heads(h_ext[M:], Wq.T, H, D)
+    k = project_heads(h_ext, Wk.T, H, D)
+    v = project_heads(h_ext, Wv.T, H, D)
+    Q = rel_table(Wr.T, T, H, D)
     got = oracle.rel_attn(q, k, v, Q, u, w, mem_len=M)
     return np.abs(got - ref).max() <= TOL * max(1.0, np.abs(ref).max())
 
@@ -536,7 +537,7 @@ def _pin_sinusoid(sinusoid):
 def _pin_padding(project_heads, rel_table):
     """Zero columns past d_head; the first d_head columns are the unpadded result."""
     g = np.random.Generator(np.random.PCG64(5))
-    x, w = g.standard_normal((3, 4, 10)), g.standard_normal((10, 2 * 3))
+    x, w = g.standard_normal((3, 4, 10)), g.standard_normal((2 * 3, 10))
     a, b = project_heads(x, w, 2, 3), project_heads(x, w, 2, 3, 8)
     t, tp = rel_table(w, 6, 2, 3), rel_table(w, 6, 2, 3, 8)
     return (b.shape == (3, 4, 2, 8) and np.array_equal(b[..., 3:], np.zeros((3, 4, 2, 5)))
@@ -552,7 +553,7 @@ def test_projection_and_table_pins():
 
 def _mutant_project_transposed_heads(x, w, heads, d_head, d_pad=None):
     # heads and head columns interleaved the wrong way round
-    y = np.matmul(np.asarray(x, float), np.asarray(w, float))
+    y = np.matmul(np.asarray(x, float), np.asarray(w, float).T)
     y = y.reshape(y.shape[:-1] + (d_head, heads)).swapaxes(-1, -2)
     return oracle.project_heads(x, w, heads, d_head, d_pad) * 0 + np.pad(
         y, [(0, 0)] * (y.ndim - 1) + [(0, (d_pad or d_head) - d_head)])
@@ -563,7 +564,7 @@ def _mutant_table_not_reversed(w_r, klen, heads, d_head, d_pad=None):
 
 
 def _mutant_table_off_by_one(w_r, klen, heads, d_head, d_pad=None):
-    R = oracle.sinusoid(klen + 1, np.asarray(w_r).shape[0])[1:]       # distances 1..klen
+    R = oracle.sinusoid(klen + 1, np.asarray(w_r).shape[1])[1:]       # distances 1..klen
     return oracle.project_heads(R, w_r, heads, d_head, d_pad)[::-1]
 
 

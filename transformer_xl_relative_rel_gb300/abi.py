@@ -291,18 +291,22 @@ def rel_attn_fwd_padded(q, k, v, r, u_bias, v_bias, mem_len: int, d_head: int, o
 
 
 def project_heads(x, w, heads: int, d_head: int, d_pad: int, out=None, stream=None):
-    """y[..., heads, d_pad] = x[..., d_in] @ w[d_in, heads*d_head], padding zero.
-    x: [*lead, d_in]; returns [*lead, heads, d_pad]."""
+    """y[..., heads, d_pad] = x[..., d_in] @ w.T with ``w`` the paper's
+    [heads*d_head, d_in] projection (torch.nn.Linear's weight layout);
+    padding columns d_head.. are zero.  x: [*lead, d_in]; returns
+    [*lead, heads, d_pad]."""
     import torch
     lead = tuple(x.shape[:-1])
     d_in = x.shape[-1]
     rows = 1
     for n in lead:
         rows *= n
-    if tuple(w.shape) != (d_in, heads * d_head) or w.dtype != x.dtype:
-        raise ValueError(f"w must be [{d_in}, {heads * d_head}] of x's dtype")
-    for t in (x, w):
-        if not t.is_cuda or not t.is_contiguous():
+    if tuple(w.shape) != (heads * d_head, d_in) or w.dtype != x.dtype:
+        raise ValueError(f"w must be [{heads * d_head}, {d_in}] of x's dtype")
+    if out is not None and (tuple(out.shape) != lead + (heads, d_pad) or out.dtype != x.dtype):
+        raise ValueError(f"out must be {list(lead + (heads, d_pad))} of x's dtype")
+    for t in (x, w, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
     if out is None:
         out = torch.empty(*lead, heads, d_pad, dtype=x.dtype, device=x.device)
@@ -313,12 +317,13 @@ def project_heads(x, w, heads: int, d_head: int, d_pad: int, out=None, stream=No
 
 
 def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: int, out=None, stream=None):
-    """Appendix B's reversed projected table [klen, heads, d_pad] from W_kR
-    [d_model, heads*d_head] and the sinusoid of the relative distance."""
+    """Appendix B's reversed projected table [klen, heads, d_pad] from W_kR in
+    the paper's layout [heads*d_head, d_model] and the sinusoid of the
+    relative distance."""
     import torch
-    d_model = w_r.shape[0]
-    if w_r.dim() != 2 or w_r.shape[1] != heads * d_head or not w_r.is_cuda or not w_r.is_contiguous():
-        raise ValueError(f"w_r must be a contiguous CUDA [d_model, {heads * d_head}] tensor")
+    if w_r.dim() != 2 or w_r.shape[0] != heads * d_head or not w_r.is_cuda or not w_r.is_contiguous():
+        raise ValueError(f"w_r must be a contiguous CUDA [{heads * d_head}, d_model] tensor")
+    d_model = w_r.shape[1]
     if out is None:
         out = torch.empty(klen, heads, d_pad, dtype=w_r.dtype, device=w_r.device)
     st = load_library().txl_rel_table(_ptr(w_r), _ptr(out), klen, d_model, heads, d_head, d_pad,

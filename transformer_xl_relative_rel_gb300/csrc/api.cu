@@ -405,10 +405,11 @@ txl_status txl_check(void *stream)
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned int word = 0;
+    unsigned int word = 0, gword = 0;
     e = read_and_clear_device_error(&word, s);
+    if (e == cudaSuccess) e = read_and_clear_gemm_error(&gword, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return word ? TXL_ERR_TIMEOUT : TXL_OK;
+    return (word | gword) ? TXL_ERR_TIMEOUT : TXL_OK;
 }
 
 const char *txl_status_string(txl_status st)

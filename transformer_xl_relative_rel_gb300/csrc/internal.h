@@ -68,6 +68,9 @@ int device_sm_count();
 // the lookup.
 cudaError_t zero_bias(size_t count, const float **out);
 
+// the projection kernel's error word (bounded waits that gave up), as above
+cudaError_t read_and_clear_gemm_error(unsigned int *word, cudaStream_t s);
+
 // releases the per-device cuBLAS handles of project.cu
 cudaError_t blas_shutdown();
 // the current device's cuBLAS handle (a cublasHandle_t) bound to stream s,

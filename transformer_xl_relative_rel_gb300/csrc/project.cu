@@ -1,30 +1,43 @@
 // project.cu -- the rest of a layer's attention inputs, written straight into
 // the layout the attention kernels read (Transformer-XL, Section 3.3):
 //
-//   txl_project_heads: y[rows][heads][d_pad] = x[rows][d_in] . W[d_in][heads*d_head]
-//     (the q / k / v projections W_q, W_kE, W_v of the extended context; with
-//     rows = positions x batch of a T-major [T][B][d_model] buffer the result
-//     is the T-major [T][B][H][d_pad] layout).  A plain GEMM: cuBLAS, one
-//     strided batch over the heads; the padding columns d_head..d_pad-1 are
-//     zeroed so that a padded head (d_pad a multiple of 8) can be read by TMA.
-//   txl_rel_table: r[t][h][d] = sum_c R[T-1-t][c] W_kR[c][h*d_head + d], the
+//   txl_project_heads: y[rows][heads][d_pad] = x[rows][d_in] . W^T with W the
+//     paper's [heads*d_head][d_in] projection (q = h W_q^T, k = h~ W_kE^T,
+//     v = h~ W_v^T); with rows = positions x batch of a T-major [T][B][d_model]
+//     buffer the result is the T-major [T][B][H][d_pad] layout, padding
+//     columns d_head..d_pad-1 exactly zero.  bf16: a persistent tcgen05 GEMM
+//     (128 x up to 256 output tiles, fp32 accumulation in TMEM, operands
+//     staged by TMA or, for rows TMA cannot address, by 4-byte cp.async, a
+//     double-buffered accumulator so that a tile's epilogue overlaps the
+//     next tile's MMAs, output by TMA store); fp32 and odd shapes: a tiled
+//     CUDA-core kernel.
+//   txl_rel_table: r[t][h][d] = sum_c R[T-1-t][c] W_kR[h*d_head + d][c], the
 //     reversed projected table of Appendix B, with R the sinusoid encoding of
 //     the relative distance (row p: sin / cos of p * 10000^(-2c/d_model)).
 //     Computed once per layer (it does not depend on the batch or on the
 //     segment); the sinusoid is evaluated in the kernel, fp32 accumulation.
 #include <cublas_v2.h>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
+#include "sm100.cuh"
 #include "txl.h"
 
 namespace txl {
+
+// bounded waits of the projection kernel that gave up (read by txl_check)
+__device__ unsigned int g_gemm_err;
+
 namespace {
+using namespace sm100;
 
 std::mutex g_blas_mu;
 cublasHandle_t g_blas[64] = {nullptr};
@@ -60,9 +73,475 @@ __device__ __forceinline__ float to_float<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-constexpr int TB_T = 32;     // table rows per block
+// =========================================================================
+// tcgen05 projection GEMM (bf16 in, fp32 accumulation, bf16 out)
+//
+// D[m][c] = sum_k x[m][k] W[row(c)][k] over output columns c of the padded
+// head layout: c = h*d_pad + d is W's row h*d_head + d when d < d_head, a
+// zero row otherwise.  Both operands are K-major (rows of 64 K-elements =
+// 128 bytes, the 128-byte swizzle), so the MMA is the plain A.B^T form.
+// Roles (eight warps, one CTA per SM, persistent over 128 x bn tiles):
+//   warp 0     TMA producer (one thread), or with warps 2 and 3 the
+//              cp.async loaders when TMA cannot address the rows;
+//   warp 1     one thread issues the MMAs (four K=16 steps per stage);
+//   warps 4-7  epilogue: TMEM -> registers -> bf16 -> swizzled staging ->
+//              TMA store (32 rows x 64 columns per warp and chunk).
+// TMEM: two 256-column accumulators (tile i's epilogue overlaps tile i+1).
+constexpr int GM = 128;           // output rows per tile (TMEM lanes)
+constexpr int GK = 64;            // K elements per stage (one swizzled row)
+constexpr int GST = 4;            // pipeline stages
+constexpr int GNT = 256;          // threads
+constexpr int GBN = 256;          // widest output tile
+constexpr int GLOADERS = 96;      // cp.async loader threads (warps 0, 2, 3)
+constexpr uint64_t GWAIT_NS = 2000000000ull;   // 2 s per wait, then give up
+
+struct GemmSmem {
+    static constexpr uint32_t ASZ = GM * 128;                 // one stage of x: 16 KB
+    static constexpr uint32_t BSZ = GBN * 128;                // one stage of W: up to 32 KB
+    static constexpr uint32_t A = 0;
+    static constexpr uint32_t B = A + GST * ASZ;
+    static constexpr uint32_t OST = B + GST * BSZ;            // 4 epilogue warps x 4 KB staging
+    static constexpr uint32_t BARS = OST + 4 * 4096;
+    static constexpr int FULL = 0, EMPTY = GST, AFULL = 2 * GST, AEMPTY = 2 * GST + 2, DONE = 2 * GST + 4,
+                         NBAR = 2 * GST + 5;
+    static constexpr uint32_t MISC = BARS + NBAR * 8;          // tmem holder, abort flag
+    static constexpr uint32_t TOTAL = MISC + 16 + 1024;        // + alignment of the base to 1024
+};
+
+struct GemmParams {
+    const __nv_bfloat16 *x, *w;
+    __nv_bfloat16 *out;
+    int rows, d_in, heads, d_head, d_pad, n_out;
+    int bn, tiles_n, tiles, ksteps;
+    int tma_out;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <bool kTmaIn>
+__global__ void __launch_bounds__(GNT, 1)
+project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_o, const GemmParams p)
+{
+    using S = GemmSmem;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + S::BARS + 8u * (uint32_t)i; };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::MISC + 8);
+    // bounded wait; gives up when another role has given up
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        const uint32_t b = bar(i);
+        if (mbar_try_wait(b, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            if (mbar_try_wait_sleep(b, parity, WAIT_SLEEP_NS)) return true;
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > GWAIT_NS) {
+                *abort = 1;
+                atomicOr(&g_gemm_err, 1u);
+                return false;
+            }
+        }
+    };
+
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        *abort = 0;
+        for (int s = 0; s < GST; ++s) {
+            mbar_init(bar(S::FULL + s), kTmaIn ? 1 : GLOADERS);
+            mbar_init(bar(S::EMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(S::AFULL + b), 1);
+            mbar_init(bar(S::AEMPTY + b), 128);
+        }
+        mbar_init(bar(S::DONE), 1);
+        fence_mbar_init();
+        if (kTmaIn) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_w);
+        }
+        if (p.tma_out) prefetch_tmap(&tm_o);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int G = gridDim.x;
+
+    if (warp == 1) {
+        // =================================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(GM, p.bn, 0, 0);
+            const uint64_t da0 = smem_desc_sw128(sbase + S::A, 16, 1024);
+            const uint64_t db0 = smem_desc_sw128(sbase + S::B, 16, 1024);
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += G, ++lt) {
+                const int buf = lt & 1;
+                // the accumulator was last read by the epilogue of tile lt-2
+                if (lt >= 2 && !wait(S::AEMPTY + buf, ((lt >> 1) - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)buf * 256u;
+                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                    const int s = it % GST;
+                    if (!wait(S::FULL + s, (it / GST) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = da0 + ((uint64_t)(s * S::ASZ) >> 4), db = db0 + ((uint64_t)(s * S::BSZ) >> 4);
+#pragma unroll
+                    for (int k = 0; k < GK / 16; ++k)   // 32 bytes of the swizzled row per K step
+                        mma_bf16_ss(acc, da + 2 * k, db + 2 * k, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(S::EMPTY + s));
+                }
+                if (ok) mma_commit(bar(S::AFULL + buf));
+            }
+            // every MMA issued here has completed before the CTA winds down
+            mma_commit(bar(S::DONE));
+            wait(S::DONE, 0);
+        }
+        __syncwarp();
+    } else if (warp == 0 || warp == 2 || warp == 3) {
+        // =================================================================== operands
+        if (kTmaIn) {
+            if (warp == 0 && lane == 0) {
+                const uint32_t bytes = (uint32_t)(GM * 128 + p.bn * 128);
+                int it = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
+                    const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+                    for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                        const int s = it % GST;
+                        if (it >= GST && !wait(S::EMPTY + s, ((it / GST) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(S::FULL + s), bytes);
+                        tma_load_2d(sbase + S::A + s * S::ASZ, &tm_x, bar(S::FULL + s), ks * GK, m0);
+                        // W viewed as [heads][d_head][d_in]: a box of bn / d_pad heads
+                        // of d_pad rows each; rows d_head.. of a head are zero-filled
+                        tma_load_3d(sbase + S::B + s * S::BSZ, &tm_w, bar(S::FULL + s), ks * GK, 0, n0 / p.d_pad);
+                    }
+                }
+            }
+        } else {
+            // 96 threads; thread li moves 4-byte word `lane` (elements 2*lane,
+            // 2*lane+1 of the stage's 64) of rows wi, wi+3, ... of both operands
+            const int wi = warp == 0 ? 0 : warp - 1;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
+                const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+                for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
+                    const int s = it % GST;
+                    if (it >= GST && !wait(S::EMPTY + s, ((it / GST) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_dst = sbase + S::A + s * S::ASZ, b_dst = sbase + S::B + s * S::BSZ;
+                    const int kw = ks * GK + 2 * lane;
+                    const bool kin = kw < p.d_in;      // d_in is even: the word is wholly in or out
+                    for (int r = wi; r < GM; r += 3) {
+                        const int grow = m0 + r;
+                        const bool v = kin && grow < p.rows;
+                        cp_async4(a_dst + sw128_offset(r, 2 * lane), p.x + (v ? (long)grow * p.d_in + kw : 0), v);
+                    }
+                    for (int r = wi; r < p.bn; r += 3) {
+                        const int col = n0 + r, h = col / p.d_pad, d = col - h * p.d_pad;
+                        const bool v = kin && h < p.heads && d < p.d_head;
+                        cp_async4(b_dst + sw128_offset(r, 2 * lane),
+                                  p.w + (v ? ((long)h * p.d_head + d) * p.d_in + kw : 0), v);
+                    }
+                    cp_async_commit();
+                    if (it > 0) {
+                        // the previous stage's copies have landed: hand it to the MMA
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(S::FULL + (it - 1) % GST));
+                    }
+                }
+            }
+            cp_async_wait<0>();
+            if (ok && it > 0) {
+                fence_proxy_async_smem();
+                mbar_arrive(bar(S::FULL + (it - 1) % GST));
+            }
+        }
+    } else {
+        // =================================================================== epilogue
+        const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31
+        unsigned char *stg = smem + S::OST + (uint32_t)(warp - 4) * 4096u;
+        const uint32_t stg_a = sbase + S::OST + (uint32_t)(warp - 4) * 4096u;
+        const int nch = (p.bn + 63) / 64;
+        int lt = 0;
+        for (int t = blockIdx.x; t < p.tiles; t += G, ++lt) {
+            const int buf = lt & 1;
+            const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+            if (!wait(S::AFULL + buf, (lt >> 1) & 1)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
+            for (int c = 0; c < nch; ++c) {
+                float v[64];
+                tmem_ld32(tacc + 64u * c, *reinterpret_cast<float(*)[32]>(v));
+                tmem_ld32(tacc + 64u * c + 32u, *reinterpret_cast<float(*)[32]>(v + 32));
+                if (c == nch - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(S::AEMPTY + buf));   // the accumulator is free for tile lt+2
+                }
+                const int col0 = n0 + 64 * c;
+                // padding columns come out exactly zero (whatever x holds)
+                int d = col0 % p.d_pad;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    if (d >= p.d_head) v[j] = 0.f;
+                    if (++d == p.d_pad) d = 0;
+                }
+                if (p.tma_out) {
+                    if (col0 >= p.n_out) continue;
+                    if (lane == 0) bulk_wait_read();   // the previous store has read the staging
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 pk;
+                        pk.x = pack2_bf16(v[8 * j + 0], v[8 * j + 1]);
+                        pk.y = pack2_bf16(v[8 * j + 2], v[8 * j + 3]);
+                        pk.z = pack2_bf16(v[8 * j + 4], v[8 * j + 5]);
+                        pk.w = pack2_bf16(v[8 * j + 6], v[8 * j + 7]);
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_o, stg_a, col0, m0 + 32 * q);   // rows / columns past the end are clipped
+                        bulk_commit();
+                    }
+                } else {
+                    const int row = m0 + 32 * q + lane;
+                    if (row < p.rows) {
+                        __nv_bfloat16 *o = p.out + (long)row * p.n_out;
+                        for (int j = 0; j < 64; ++j)
+                            if (col0 + j < p.n_out) o[col0 + j] = __float2bfloat16(v[j]);
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Encoded bf16 tensor maps with the 128-byte swizzle, cached by their
+// arguments (an encode is a driver call that costs about a short launch).
+struct GMap {
+    int dev, rank;
+    const void *base;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    CUtensorMap map;
+};
+constexpr int GMAPS = 48;
+std::mutex g_gmap_mu;
+GMap g_gmaps[GMAPS];
+int g_gmap_n = 0, g_gmap_next = 0;
+
+bool gmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+          const cuuint32_t *box)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_gmap_mu);
+    for (int i = 0; i < g_gmap_n; ++i) {
+        const GMap &e = g_gmaps[i];
+        bool same = e.dev == dev && e.rank == rank && e.base == base;
+        for (int d = 0; same && d < rank; ++d) same = e.dims[d] == dims[d] && e.box[d] == box[d];
+        for (int d = 0; same && d < rank - 1; ++d) same = e.strides[d] == strides[d];
+        if (same) {
+            *m = e.map;
+            return true;
+        }
+    }
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    GMap &e = g_gmaps[g_gmap_next];
+    e.dev = dev;
+    e.rank = rank;
+    e.base = base;
+    for (int d = 0; d < 3; ++d) {
+        e.dims[d] = d < rank ? dims[d] : 0;
+        e.box[d] = d < rank ? box[d] : 0;
+    }
+    for (int d = 0; d < 2; ++d) e.strides[d] = d < rank - 1 ? strides[d] : 0;
+    e.map = *m;
+    g_gmap_next = (g_gmap_next + 1) % GMAPS;
+    if (g_gmap_n < GMAPS) ++g_gmap_n;
+    return true;
+}
+
+bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
+
+template <bool kTmaIn>
+cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mo, const GemmParams &p,
+                          cudaStream_t s)
+{
+    auto kern = project_gemm_kernel<kTmaIn>;
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(opted.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GemmSmem::TOTAL);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_relaxed);
+    }
+    const int grid = p.tiles < device_sm_count() ? p.tiles : device_sm_count();
+    kern<<<(unsigned)grid, GNT, GemmSmem::TOTAL, s>>>(mx, mw, mo, p);
+    return cudaGetLastError();
+}
+
+// bf16 projection on the tensor cores: d_in even, x and w 4-byte aligned.
+cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int rows, int d_in, int heads, int d_head,
+                                int d_pad, cudaStream_t s)
+{
+    GemmParams p;
+    p.x = (const __nv_bfloat16 *)x;
+    p.w = (const __nv_bfloat16 *)w;
+    p.out = (__nv_bfloat16 *)out;
+    p.rows = rows;
+    p.d_in = d_in;
+    p.heads = heads;
+    p.d_head = d_head;
+    p.d_pad = d_pad;
+    p.n_out = heads * d_pad;
+    p.bn = p.n_out >= GBN ? GBN : (p.n_out + 15) / 16 * 16;
+    p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
+    const long tiles = (long)((rows + GM - 1) / GM) * p.tiles_n;
+    if (tiles > INT32_MAX) return cudaErrorNotSupported;
+    p.tiles = (int)tiles;
+    p.ksteps = (d_in + GK - 1) / GK;
+    // TMA addresses rows whose pitch is a multiple of 16 bytes; a W box holds
+    // whole heads of d_pad rows
+    const bool tma_in = d_in % 8 == 0 && al(x, 16) && al(w, 16) && p.bn % d_pad == 0 && d_pad <= 256;
+    p.tma_out = al(out, 16) && (p.n_out * 2) % 16 == 0;
+    CUtensorMap mx{}, mw{}, mo{};
+    if (tma_in) {
+        const cuuint64_t dx[2] = {(cuuint64_t)d_in, (cuuint64_t)rows}, sx[1] = {(cuuint64_t)d_in * 2};
+        const cuuint32_t bx[2] = {GK, GM};
+        const cuuint64_t dw[3] = {(cuuint64_t)d_in, (cuuint64_t)d_head, (cuuint64_t)heads};
+        const cuuint64_t sw[2] = {(cuuint64_t)d_in * 2, (cuuint64_t)d_head * d_in * 2};
+        const cuuint32_t bw[3] = {GK, (cuuint32_t)d_pad, (cuuint32_t)(p.bn / d_pad)};
+        if (!gmap(&mx, 2, x, dx, sx, bx) || !gmap(&mw, 3, w, dw, sw, bw)) return cudaErrorInvalidValue;
+    }
+    if (p.tma_out) {
+        const cuuint64_t dO[2] = {(cuuint64_t)p.n_out, (cuuint64_t)rows}, sO[1] = {(cuuint64_t)p.n_out * 2};
+        const cuuint32_t bO[2] = {64, 32};
+        if (!gmap(&mo, 2, out, dO, sO, bO)) return cudaErrorInvalidValue;
+    }
+    return tma_in ? launch_gemm_t<true>(mx, mw, mo, p, s) : launch_gemm_t<false>(mx, mw, mo, p, s);
+}
+
+// =========================================================================
+// CUDA-core kernels (fp32, and bf16 shapes the tensor path does not take)
+constexpr int TB_T = 32;     // rows per block
 constexpr int TB_N = 64;     // output columns per block
-constexpr int TB_K = 32;     // d_model slice staged per step
+constexpr int TB_K = 32;     // contraction slice staged per step
+
+// y[m][c] = sum_k x[m][k] W[row(c)][k] for a 32-row x 64-column block of the
+// padded output (c = h*d_pad + d, zero where d >= d_head)
+template <typename T>
+__global__ void __launch_bounds__(256)
+project_simt_kernel(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ out, int rows, int d_in,
+                    int heads, int d_head, int d_pad)
+{
+    __shared__ float xs[TB_T][TB_K + 1];
+    __shared__ float ws[TB_K][TB_N + 1];
+    const long m0 = (long)blockIdx.x * TB_T;
+    const int n0 = blockIdx.y * TB_N;
+    const int n_out = heads * d_pad;
+    const int tid = threadIdx.x;
+    const int tr = tid / 16, tc = tid % 16;    // rows tr, tr+16; columns tc + 16*c
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int k0 = 0; k0 < d_in; k0 += TB_K) {
+        for (int i = tid; i < TB_T * TB_K; i += 256) {
+            const long m = m0 + i / TB_K;
+            const int k = k0 + i % TB_K;
+            xs[i / TB_K][i % TB_K] = (m < rows && k < d_in) ? to_float(x[m * d_in + k]) : 0.f;
+        }
+        for (int i = tid; i < TB_K * TB_N; i += 256) {
+            const int kk = i / TB_N, c = n0 + i % TB_N, k = k0 + kk;
+            const int h = c / d_pad, d = c % d_pad;
+            ws[kk][i % TB_N] = (k < d_in && c < n_out && d < d_head) ? to_float(w[((long)h * d_head + d) * d_in + k])
+                                                                      : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < TB_K; ++kk) {
+            const float a0 = xs[tr][kk], a1 = xs[tr + 16][kk];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float b = ws[kk][tc + 16 * c];
+                acc[0][c] += a0 * b;
+                acc[1][c] += a1 * b;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const long m = m0 + tr + 16 * rr;
+        if (m >= rows) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int n = n0 + tc + 16 * c;
+            if (n >= n_out) continue;
+            out[m * n_out + n] = from_float<T>((n % d_pad) < d_head ? acc[rr][c] : 0.f);
+        }
+    }
+}
 
 // r[t][h][d] for a 32-row x 64-column block; the sinusoid rows of the block
 // are generated slice by slice in shared memory, W_kR slices are staged too.
@@ -92,7 +571,8 @@ rel_table_kernel(const T *__restrict__ w, T *__restrict__ out, int Tn, int d_mod
         }
         for (int x = tid; x < TB_K * TB_N; x += 256) {
             const int kk = x / TB_N, n = n0 + x % TB_N, c = k0 + kk;
-            ws[kk][x % TB_N] = (c < d_model && n < ncols) ? to_float(w[(long)c * ncols + n]) : 0.f;
+            // W_kR in the paper's layout: row n (an output column), d_model inputs
+            ws[kk][x % TB_N] = (c < d_model && n < ncols) ? to_float(w[(long)n * d_model + c]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -121,8 +601,6 @@ rel_table_kernel(const T *__restrict__ w, T *__restrict__ out, int Tn, int d_mod
     }
 }
 
-bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
-
 bool overlap_bytes(const void *a, size_t na, const void *b, size_t nb)
 {
     if (!a || !b || na == 0 || nb == 0) return false;
@@ -149,6 +627,20 @@ cudaError_t blas_shutdown()
     return cudaSuccess;
 }
 
+cudaError_t read_and_clear_gemm_error(unsigned int *word, cudaStream_t s)
+{
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_gemm_err, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_gemm_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
 }  // namespace txl
 
 using namespace txl;
@@ -170,28 +662,27 @@ txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, 
         overlap_bytes(out, nout, w, (size_t)d_in * heads * d_head * esz))
         return TXL_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
     if (d_in == 0) {   // empty contraction: zeros
-        cudaError_t e = cudaMemsetAsync(out, 0, nout, s);
-        return e == cudaSuccess ? TXL_OK : (note_cuda_error(e), TXL_ERR_CUDA);
+        e = cudaMemsetAsync(out, 0, nout, s);
+    } else if (dtype == TXL_BF16 && d_in % 2 == 0 && al(x, 4) && al(w, 4)) {
+        e = launch_project_gemm(x, w, out, rows, d_in, heads, d_head, d_pad, s);
+    } else {
+        const long n_out = (long)heads * d_pad;
+        dim3 grid((unsigned)((rows + TB_T - 1) / TB_T), (unsigned)((n_out + TB_N - 1) / TB_N));
+        if (grid.y > 65535) return TXL_ERR_UNSUPPORTED;
+        if (dtype == TXL_F32)
+            project_simt_kernel<float><<<grid, 256, 0, s>>>((const float *)x, (const float *)w, (float *)out, rows,
+                                                            d_in, heads, d_head, d_pad);
+        else
+            project_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)x,
+                                                                    (const __nv_bfloat16 *)w, (__nv_bfloat16 *)out,
+                                                                    rows, d_in, heads, d_head, d_pad);
+        e = cudaGetLastError();
     }
-    cublasHandle_t h = nullptr;
-    if (blas_handle(&h) != CUBLAS_STATUS_SUCCESS || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS)
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
         return TXL_ERR_CUDA;
-    // column-major view: per head, y_h^T [d_head x rows] = W_h^T [d_head x d_in] . x^T [d_in x rows]
-    const float one = 1.f, zero = 0.f;
-    const cudaDataType_t ty = dtype == TXL_F32 ? CUDA_R_32F : CUDA_R_16BF;
-    cublasStatus_t st = cublasGemmStridedBatchedEx(
-        h, CUBLAS_OP_N, CUBLAS_OP_N, d_head, rows, d_in, &one, w, ty, heads * d_head, (long long)d_head, x, ty,
-        d_in, 0LL, &zero, out, ty, heads * d_pad, (long long)d_pad, heads, CUBLAS_COMPUTE_32F,
-        CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return TXL_ERR_CUDA;
-    if (d_pad > d_head) {
-        cudaError_t e = cudaMemset2DAsync((unsigned char *)out + (size_t)d_head * esz, (size_t)d_pad * esz, 0,
-                                          (size_t)(d_pad - d_head) * esz, (size_t)rows * heads, s);
-        if (e != cudaSuccess) {
-            note_cuda_error(e);
-            return TXL_ERR_CUDA;
-        }
     }
     return TXL_OK;
 }
