@@ -1,10 +1,13 @@
 """Benchmark: Transformer-XL relative attention + memory rollover on GB300.
 
 One step = one pass of the hot path over one batch of the workload: every
-segment of the workload's chain, and in each segment every layer's relative
-attention call (txl_rel_attn_fwd) followed by its memory rollover
-(txl_mem_update).  Inputs are seeded and synthetic, resident in HBM before the
-timed region; the per-step working set is far larger than L2.
+segment of the workload's chain, and in each segment every layer's q, k, v
+projections of [memory; h] (txl_project_heads), its relative attention
+(txl_rel_attn_fwd) and its memory rollover (txl_mem_update), the rollover
+feeding the next segment's keys and values and each layer's output feeding
+the next layer (``--attn-only``: the attention and rollover alone on fixed
+per-layer inputs).  Inputs are seeded and synthetic, resident in HBM before
+the timed region; the per-step working set is far larger than L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the float64 CPU oracle
@@ -224,10 +227,17 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
-class Chain:
-    """Device buffers of one replica of a workload: per layer q, k, v, r,
-    u, v-bias, the attention output and two extended-context buffers
-    [M+L, B, d_model] that trade places every segment."""
+class AttnChain:
+    """``--attn-only``: every layer's attention on fixed q, k, v, r (drawn
+    once, outside the timed region) and the rollover of its extended
+    context, which no later attention reads.  Device buffers of one replica:
+    per layer q, k, v, r, u, v-bias, the attention output and two
+    extended-context buffers [M+L, B, d_model] that trade places every
+    segment."""
+
+    graph_steps = 1
+    step_desc = ("per segment, per layer: attention on fixed q, k, v (txl_rel_attn_fwd) and the rollover of "
+                 "the layer's extended context (no recurrence into k, v)")
 
     def __init__(self, w: Workload, device, ring: bool = False, pad: int = 0, fused: bool = False):
         s = w.shape
@@ -341,6 +351,223 @@ class Chain:
             tot += sum(x.numel() * x.element_size() for x in lay["ext"])
         return tot
 
+    def oracle_layer(self) -> dict:
+        lay = self.layers[0]
+        if not self.pad:
+            return lay
+        D = self.w.shape.d_head
+        return {k: lay[k][..., :D] for k in ("q", "k", "v", "r", "u", "w")}
+
+    def e2e(self, txl, steps: int, world: int) -> dict:
+        return measure_e2e(self.w, self, txl, steps, world)
+
+    attn_extra_launches = 0
+    rollover_in_attention = False
+
+
+class LayerChain:
+    """The recurrence of the pages, every step a library call.  Per segment
+    and layer n (Transformer-XL Sections 3.2-3.3): q = h W_q^T on the
+    segment's states, k = h~ W_kE^T and v = h~ W_v^T on the extended context
+    h~ = [memory; h] (txl_project_heads), the relative attention over h~,
+    and the rollover that keeps the newest M rows of h~ as the next
+    segment's memory (txl_mem_update), so each segment's keys and values
+    are projected from the memory the previous segment left.  Layer n+1's
+    segment states are layer n's attention output, written by the
+    attention straight into layer n+1's extended context (the output
+    projection, residual, LayerNorm and feed-forward between layers are not
+    on this path and are left out); layer 0's are the segment's input
+    states, copied in by the library (txl_ring_append of L rows).  Head
+    vectors other than 64 wide are stored padded to 64 (the layout the
+    projections write); their layers n >= 1 read fixed synthetic states,
+    because the padded output is not a d_model-wide row.  The relative
+    table of each layer depends on neither batch nor segment and is built
+    once (txl_rel_table), outside the timed region."""
+
+    def __init__(self, w: Workload, device, txl, ring: bool = False, fused: bool = False):
+        s = w.shape
+        self.w = w
+        self.txl = txl
+        B, H, D, L, M, T, dm = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len, s.klen, s.d_model
+        self.dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.dp = 64 if (D != 64 and w.dtype == "bf16") else D
+        if (ring or fused) and self.dp != D:
+            raise SystemExit("--ring / --fused-rollover need unpadded heads (d_head 64)")
+        self.ring, self.fused = ring, fused
+        dt, dp = self.dtype, self.dp
+        g = torch.Generator(device=device).manual_seed(w.seed)
+        # the segments' input states (layer 0), N(0, 1)
+        self.h0 = [torch.randn(L, B, dm, generator=g, device=device).to(dt) for _ in range(w.segments)]
+        self.layers = []
+        for _n in range(w.layers):
+            def wt():
+                return (0.02 * torch.randn(H * D, dm, generator=g, device=device)).to(dt).contiguous()
+            wq, wk, wv, wr = wt(), wt(), wt(), wt()
+            u = torch.zeros(H, dp, device=device)
+            wb = torch.zeros(H, dp, device=device)
+            u[:, :D] = 0.02 * torch.randn(H, D, generator=g, device=device)
+            wb[:, :D] = 0.02 * torch.randn(H, D, generator=g, device=device)
+            r = txl.rel_table(wr, T, H, D, dp)
+            # the first memory, and fixed segment states in rows M.. where no
+            # earlier layer writes them: N(0, 1)
+            ext0 = torch.randn(T, B, dm, generator=g, device=device).to(dt)
+            ext = [ext0] if ring else [ext0, ext0.clone()]
+            self.layers.append(dict(
+                wq=wq, wk=wk, wv=wv, r=r, u=u, w=wb, ext=ext, start=0, hin=None,
+                q=torch.empty(L, B, H, dp, dtype=dt, device=device),
+                k=torch.empty(T, B, H, dp, dtype=dt, device=device),
+                v=torch.empty(T, B, H, dp, dtype=dt, device=device),
+                out=torch.empty(L, B, H, dp, dtype=dt, device=device)))
+        self.cur = 0
+        torch.cuda.synchronize()
+
+    # every other step starts from the other buffer of each ping-pong pair
+    # when the segment count is odd: a graph then holds two steps
+    @property
+    def graph_steps(self) -> int:
+        return 1 if (self.ring or self.w.segments % 2 == 0) else 2
+
+    @property
+    def step_desc(self) -> str:
+        roll = ("ring append of the L new rows (txl_ring_append)" if self.ring else
+                "rollover in the attention call (txl_rel_attn_fwd_mem)" if self.fused else
+                "rollover of the extended context (txl_mem_update)")
+        return ("per segment: layer 0's input states copied in (txl_ring_append); per layer: q, k, v "
+                "projections of [memory; h] (txl_project_heads, tcgen05), attention, " + roll +
+                "; layer n's output is layer n+1's input")
+
+    def _ring_in(self, lay, rows) -> int:
+        """Append a segment's L states to a layer's ring (the oldest L rows)."""
+        s = self.w.shape
+        T = s.klen
+        pos = (lay["start"] + s.mem_len) % T
+        self.txl.ring_append(lay["ext"][0], rows, pos)
+        lay["hin"] = rows
+        return 2 if pos + s.seg_len > T else 1
+
+    def step(self, txl, attn_events=None) -> int:
+        launches = 0
+        for tau in range(self.w.segments):
+            launches += self.segment(txl, tau, attn_events)
+            if not self.ring:
+                self.cur ^= 1
+        return launches
+
+    def segment(self, txl, tau: int, attn_events=None) -> int:
+        s = self.w.shape
+        B, H, D, L, M, dm = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len, s.d_model
+        dp, cur, nl = self.dp, self.cur, len(self.layers)
+        launches = 0
+        first = self.layers[0]
+        if self.ring:
+            launches += self._ring_in(first, self.h0[tau])
+        else:
+            txl.ring_append(first["ext"][cur][M:], self.h0[tau], 0)     # a plain copy of L rows
+            launches += 1
+        for n, lay in enumerate(self.layers):
+            ext = lay["ext"][0 if self.ring else cur]
+            h = lay["hin"] if self.ring else ext[M:]
+            txl.project_heads(h, lay["wq"], H, D, dp, out=lay["q"])
+            txl.project_heads(ext, lay["wk"], H, D, dp, out=lay["k"])
+            txl.project_heads(ext, lay["wv"], H, D, dp, out=lay["v"])
+            launches += 3
+            nxt = self.layers[n + 1] if n + 1 < nl else None
+            out = lay["out"]
+            if nxt is not None and dp == D and not self.ring:
+                out = nxt["ext"][cur][M:].view(L, B, H, D)      # straight into the next layer's h~
+            if attn_events is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            args = (lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"])
+            if self.ring:
+                txl.rel_attn_fwd_ring(*args, mem_len=M, kv_start=lay["start"], out=out)
+            elif self.fused:
+                txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=lay["ext"][1 - cur], ext_ctx=ext, out=out)
+            elif dp != D:
+                txl.rel_attn_fwd_padded(*args, mem_len=M, d_head=D, out=out)
+            else:
+                txl.rel_attn_fwd(*args, mem_len=M, out=out)
+            if attn_events is not None:
+                e1.record()
+                attn_events.append((e0, e1))
+            launches += 1 + self.attn_extra_launches
+            if self.ring:
+                lay["start"] = (lay["start"] + L) % s.klen
+                if nxt is not None:
+                    launches += self._ring_in(nxt, out.view(L, B, dm))
+            elif self.fused:
+                launches += 0 if self.rollover_in_attention else 1
+            else:
+                txl.mem_update(lay["ext"][1 - cur], ext, mem_len=M)
+                launches += 1
+        return launches
+
+    @property
+    def working_set_bytes(self) -> int:
+        tot = sum(x.numel() * x.element_size() for x in self.h0)
+        for lay in self.layers:
+            for key in ("wq", "wk", "wv", "r", "q", "k", "v", "out"):
+                tot += lay[key].numel() * lay[key].element_size()
+            tot += sum(x.numel() * x.element_size() for x in lay["ext"])
+        return tot
+
+    def oracle_layer(self) -> dict:
+        """Layer 0's last attention inputs (first d_head columns), for the
+        CPU oracle's timing sample."""
+        D = self.w.shape.d_head
+        lay = self.layers[0]
+        return {k: lay[k][..., :D] for k in ("q", "k", "v", "r", "u", "w")}
+
+    def e2e(self, txl, steps: int, world: int) -> dict:
+        """The same step through the public API with each segment's input
+        states in pinned host memory: every step copies them host->device
+        (on a side stream, a segment ahead) and reads the last layer's
+        output of the last segment back; CUDA events around the steps."""
+        host = [x.cpu().pin_memory() for x in self.h0]
+        last = self.layers[-1]["out"]
+        out_host = torch.empty_like(last, device="cpu").pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host)
+        d2h = out_host.numel() * out_host.element_size()
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        S = self.w.segments
+        copied = [torch.cuda.Event() for _ in range(S)]
+        used = [torch.cuda.Event() for _ in range(S)]
+
+        def one():
+            side.wait_stream(main)
+            for tau in range(S):
+                side.wait_event(used[tau])
+                with torch.cuda.stream(side):
+                    self.h0[tau].copy_(host[tau], non_blocking=True)
+                    copied[tau].record(side)
+                main.wait_event(copied[tau])
+                self.segment(txl, tau)
+                used[tau].record(main)
+                if not self.ring:
+                    self.cur ^= 1
+            out_host.copy_(last, non_blocking=True)
+
+        one()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        sec = e0.elapsed_time(e1) / 1e3
+        tokens = self.w.shape.batch * self.w.shape.seg_len * S * steps
+        return {"value": aggregate_rate(tokens, sec, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+    def projection_flops_per_step(self) -> float:
+        s = self.w.shape
+        per_layer = 2.0 * s.batch * s.d_model * s.heads * s.d_head * (s.seg_len + 2 * s.klen)
+        return per_layer * self.w.layers * self.w.segments
+
     attn_extra_launches = 0
     rollover_in_attention = False
 
@@ -370,7 +597,7 @@ def rollover_fuses(w: Workload, splits: int) -> bool:
 
 
 # ------------------------------------------------------------- e2e measurement
-def measure_e2e(w: Workload, chain: Chain, txl, steps: int, world: int):
+def measure_e2e(w: Workload, chain: "AttnChain", txl, steps: int, world: int):
     """The same step through the public API with the inputs in pinned host
     memory: every step copies each layer's q, k, v, r, biases and extended
     context host->device, runs the calls, and reads the last layer's output
@@ -477,7 +704,7 @@ def config_of(w: Workload, world: int, working_set: int = 0, ring: bool = False,
     if ring:
         c["memory"] = "ring (txl_rel_attn_fwd_ring + txl_ring_append of L rows)"
     if pad and pad != s.d_head:
-        c["head_storage"] = f"padded to {pad} (txl_rel_attn_fwd_padded)"
+        c["head_storage"] = f"padded to {pad} (txl_project_heads writes it, txl_rel_attn_fwd_padded reads it)"
     if working_set:
         c["l2"] = f"per-step working set {working_set / 1e9:.2f} GB > 129 MB L2 (inputs larger than L2, no flush)"
     return c
@@ -687,6 +914,9 @@ def main(argv=None):
                          "roofline's launch time then includes the rollover copy")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="time attention + rollover on fixed per-layer q, k, v (no projections, no recurrence "
+                         "into k, v)")
     ap.add_argument("--dry-run", action="store_true",
                     help="no GPU: exercise the rank launcher and the max-over-ranks timing on host work")
     args = ap.parse_args(argv)
@@ -722,15 +952,20 @@ def main(argv=None):
         import dataclasses
         w = dataclasses.replace(w, layers=args.layers or w.layers, segments=args.segments or w.segments)
     s = w.shape
-    chain = Chain(w, torch.device("cuda", local), ring=args.ring, pad=args.pad,
-                  fused=args.fused_rollover)
+    dev = torch.device("cuda", local)
+    if args.attn_only:
+        chain = AttnChain(w, dev, ring=args.ring, pad=args.pad, fused=args.fused_rollover)
+        padded = bool(chain.pad)
+    else:
+        chain = LayerChain(w, dev, txl, ring=args.ring, fused=args.fused_rollover)
+        padded = chain.dp != s.d_head
     # the library's own plan for this call shape: key splits and launches
     splits, call_launches = txl.rel_attn_fwd_plan(s.batch, s.mem_len, s.seg_len, s.heads, s.d_head,
                                                   txl.TXL_BF16 if w.dtype == "bf16" else txl.TXL_F32)
     # (head vectors stored padded go straight to the kernel: no padding copies)
-    chain.attn_extra_launches = (1 if splits > 1 else 0) if chain.pad else call_launches - 1
+    chain.attn_extra_launches = (1 if splits > 1 else 0) if padded else call_launches - 1
     chain.rollover_in_attention = chain.fused and rollover_fuses(w, splits)
-    for _ in range(args.warmup):
+    for _ in range(args.warmup * chain.graph_steps):
         chain.step(txl)
     txl.check()
 
@@ -751,22 +986,37 @@ def main(argv=None):
     txl.check()
     local_s = e0.elapsed_time(e1) / 1e3
     eager_step_s = max_over_ranks(local_s, world) / args.steps
-    # The same step captured once in a CUDA graph and replayed: the kernels,
-    # their arguments and their order are those of the eager step; the
-    # per-call host work (binding checks, launch calls) leaves the timed
-    # region.  Falls back to the eager timing if the capture fails.
+    # The same step captured in a CUDA graph and replayed: the kernels, their
+    # arguments and their order are those of the eager step; the per-call
+    # host work (binding checks, launch calls) leaves the timed region.  A
+    # chain whose ping-pong buffers return to their start only every second
+    # step (odd segment count) is captured as two steps and replayed half as
+    # often, with one captured single step first when K is odd.  Falls back
+    # to the eager timing if the capture fails.
     timing = {"mode": "eager", "eager_ms_per_step": eager_step_s * 1e3}
-    if not args.no_graph:
+    if not args.no_graph and not args.ring:
         try:
-            gph = torch.cuda.CUDAGraph()
+            gs = chain.graph_steps
             side = torch.cuda.Stream()
             side.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(side):
-                chain.step(txl)
+                for _ in range(gs):
+                    chain.step(txl)
             torch.cuda.current_stream().wait_stream(side)
             torch.cuda.synchronize()
-            with torch.cuda.graph(gph):
-                chain.step(txl)
+            # captured on the stream that ran the warm-up step: the library's
+            # split scratch is kept per stream and was sized there
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=side):
+                for _ in range(gs):
+                    chain.step(txl)
+            g1 = None
+            if gs > 1 and args.steps % gs:
+                # one more step, replayed after the pairs: it leaves the buffers
+                # where this capture leaves the chain's host-side parity
+                g1 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g1, stream=side):
+                    chain.step(txl)
             for _ in range(args.warmup):
                 gph.replay()
             torch.cuda.synchronize()
@@ -776,8 +1026,10 @@ def main(argv=None):
             barrier(world)
             torch.cuda.synchronize()
             e0.record()
-            for _ in range(args.steps):
+            for _ in range(args.steps // gs):
                 gph.replay()
+            if g1 is not None:
+                g1.replay()
             e1.record()
             torch.cuda.synchronize()
             barrier(world)
@@ -785,7 +1037,7 @@ def main(argv=None):
             txl.check()
             local_s = e0.elapsed_time(e1) / 1e3
             timing["mode"] = "cuda_graph"
-            del gph
+            del gph, g1
         except Exception as ex:   # keep the eager numbers
             torch.cuda.synchronize()
             timing["graph_error"] = str(ex)[:160]
@@ -820,18 +1072,24 @@ def main(argv=None):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": config_of(w, world, chain.working_set_bytes, args.ring, args.pad,
+            "config": config_of(w, world, chain.working_set_bytes, args.ring,
+                                args.pad if args.attn_only else (chain.dp if chain.dp != s.d_head else 0),
                                 "in the attention launch (txl_rel_attn_fwd_mem)" if chain.rollover_in_attention
                                 else ("own launch (txl_rel_attn_fwd_mem)" if chain.fused
                                       else "own launch (txl_mem_update)")),
             "tflops": tflops_step, "pct_bf16_peak": tflops_step / peaks["bf16_tflops"] * 100.0,
             "roofline": roof, "clocks": clk, "gpu_launches": launches, "timing": timing}
+    line["config"]["step"] = chain.step_desc
+    if isinstance(chain, LayerChain):
+        pf = chain.projection_flops_per_step()
+        line["projection_tflops"] = pf / step_s / 1e12
+        line["step_tflops_with_projections"] = (flops_call * calls_per_step + pf) / step_s / 1e12
 
     e2e_steps = args.e2e_steps or max(2, min(args.steps, 5))
-    line["e2e"] = measure_e2e(w, chain, txl, e2e_steps, world)
+    line["e2e"] = chain.e2e(txl, e2e_steps, world)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows, threads, spent = oracle_rate(w, 12.0, layer=chain.layers[0])
+        rate, rows, threads, spent = oracle_rate(w, 12.0, layer=chain.oracle_layer())
         line["cpu_baseline"] = {
             "value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{rows} random (b,h,i) rows of layer 0's inputs ({spent:.1f} s of CPU); rate scaled "

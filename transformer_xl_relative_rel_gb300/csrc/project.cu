@@ -101,7 +101,8 @@ struct GemmSmem {
     static constexpr uint32_t A = 0;
     static constexpr uint32_t B = A + GST * ASZ;
     static constexpr uint32_t OST = B + GST * BSZ;            // 4 epilogue warps x 4 KB staging
-    static constexpr uint32_t BARS = OST + 4 * 4096;
+    static constexpr uint32_t BOFF = OST + 4 * 4096;          // W row offsets of a tile, per loader warp
+    static constexpr uint32_t BARS = BOFF + 3 * 128 * 4;
     static constexpr int FULL = 0, EMPTY = GST, AFULL = 2 * GST, AEMPTY = 2 * GST + 2, DONE = 2 * GST + 4,
                          NBAR = 2 * GST + 5;
     static constexpr uint32_t MISC = BARS + NBAR * 8;          // tmem holder, abort flag
@@ -244,13 +245,25 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
         } else {
-            // 96 threads; thread li moves 4-byte word `lane` (elements 2*lane,
-            // 2*lane+1 of the stage's 64) of rows wi, wi+3, ... of both operands
+            // 96 threads; warp wi (0..2) moves rows wi, wi+3, ... of both
+            // operands, lane l the 4-byte word l of each row's 64 elements.
+            // Per tile, each warp puts the element offsets of its W rows (-1:
+            // a zero row) in a table of its own, so the stages do no index
+            // division and the warps never wait on one another.
             const int wi = warp == 0 ? 0 : warp - 1;
+            int *boff = reinterpret_cast<int *>(smem + S::BOFF) + wi * 128;
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
                 const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+                __syncwarp();                          // the previous tile's stages have read the table
+                for (int j = lane; wi + 3 * j < p.bn; j += 32) {
+                    const int col = n0 + wi + 3 * j, h = col / p.d_pad, d = col - h * p.d_pad;
+                    boff[j] = (h < p.heads && d < p.d_head) ? (h * p.d_head + d) * p.d_in : -1;
+                }
+                __syncwarp();
+                const long a_row0 = (long)(m0 + wi) * p.d_in;
+                const long a_step = 3L * p.d_in;
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % GST;
                     if (it >= GST && !wait(S::EMPTY + s, ((it / GST) - 1) & 1)) {
@@ -260,16 +273,18 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const uint32_t a_dst = sbase + S::A + s * S::ASZ, b_dst = sbase + S::B + s * S::BSZ;
                     const int kw = ks * GK + 2 * lane;
                     const bool kin = kw < p.d_in;      // d_in is even: the word is wholly in or out
-                    for (int r = wi; r < GM; r += 3) {
-                        const int grow = m0 + r;
-                        const bool v = kin && grow < p.rows;
-                        cp_async4(a_dst + sw128_offset(r, 2 * lane), p.x + (v ? (long)grow * p.d_in + kw : 0), v);
+                    const uint32_t cw = (uint32_t)(lane & 3) * 4u;     // byte within the 16-byte chunk
+                    const uint32_t ch = (uint32_t)(lane >> 2);         // 16-byte chunk of the 128-byte row
+                    const __nv_bfloat16 *ap = p.x + a_row0 + kw;
+                    for (int r = wi; r < GM; r += 3, ap += a_step) {
+                        const bool v = kin && m0 + r < p.rows;
+                        cp_async4(a_dst + (uint32_t)r * 128u + ((ch ^ (uint32_t)(r & 7)) << 4) + cw, v ? ap : p.x, v);
                     }
-                    for (int r = wi; r < p.bn; r += 3) {
-                        const int col = n0 + r, h = col / p.d_pad, d = col - h * p.d_pad;
-                        const bool v = kin && h < p.heads && d < p.d_head;
-                        cp_async4(b_dst + sw128_offset(r, 2 * lane),
-                                  p.w + (v ? ((long)h * p.d_head + d) * p.d_in + kw : 0), v);
+                    for (int r = wi, j = 0; r < p.bn; r += 3, ++j) {
+                        const int o = boff[j];
+                        const bool v = kin && o >= 0;
+                        cp_async4(b_dst + (uint32_t)r * 128u + ((ch ^ (uint32_t)(r & 7)) << 4) + cw,
+                                  v ? p.w + o + kw : p.w, v);
                     }
                     cp_async_commit();
                     if (it > 0) {
@@ -665,7 +680,8 @@ txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, 
     cudaError_t e;
     if (d_in == 0) {   // empty contraction: zeros
         e = cudaMemsetAsync(out, 0, nout, s);
-    } else if (dtype == TXL_BF16 && d_in % 2 == 0 && al(x, 4) && al(w, 4)) {
+    } else if (dtype == TXL_BF16 && d_in % 2 == 0 && al(x, 4) && al(w, 4) &&
+               (long)heads * d_head * d_in <= INT32_MAX) {
         e = launch_project_gemm(x, w, out, rows, d_in, heads, d_head, d_pad, s);
     } else {
         const long n_out = (long)heads * d_pad;
