@@ -206,9 +206,9 @@ txl_status txl_rel_attn_fwd_padded(const void *q, const void *k, const void *v, 
  * the result is the T-major [positions][batch][heads][d_pad] layout.
  * bf16: the library's tcgen05 GEMM (fp32 accumulation, one rounding to
  * bf16), for d_in even and x, w 4-byte aligned (TMA operand loads when d_in
- * is a multiple of 8, x and w 16-byte aligned and d_pad divides 256; 16-byte
- * output stores when out is 16-byte aligned and heads*d_pad a multiple of 8);
- * fp32 and other bf16 shapes: a CUDA-core kernel (fp32 accumulation).
+ * is a multiple of 8, x and w 16-byte aligned and d_pad divides 256; TMA
+ * output stores when out is 16-byte aligned and heads*d_pad*2 a multiple of
+ * 16); fp32 and other bf16 shapes: a CUDA-core kernel (fp32 accumulation).
  * x, w, out device, row-major, dtype elements; out must not overlap x or w.
  * d_pad >= d_head >= 1; d_in == 0 gives zeros.
  */
@@ -335,6 +335,17 @@ txl_status txl_rel_attn_fwd_noalloc(const void *q, const void *k, const void *v,
  * TXL_OK.
  */
 txl_status txl_check(void *stream);
+
+/*
+ * txl_selftest_wait -- exercise the failure path of the kernels' bounded
+ * waits without any fault: a one-warp kernel waits on an mbarrier that
+ * nothing completes, through the same bounded wait the kernels use but
+ * limited to limit_us microseconds (1 .. 1,000,000; else TXL_ERR_INVALID).
+ * The wait runs out and records the device error word, so the next
+ * txl_check(stream) returns TXL_ERR_TIMEOUT (and clears it); the context
+ * stays usable.  No counterpart in the paper: a test hook of the library.
+ */
+txl_status txl_selftest_wait(unsigned int limit_us, void *stream);
 
 /* Static description of a status code; never NULL. */
 const char *txl_status_string(txl_status s);

@@ -257,3 +257,9 @@ def test_bwd_without_gpu_reports_cuda_error(lib):
     assert _bwd(out=FAKE * 15, lse=FAKE * 16) == CUDA
     assert _attn_lse() == CUDA
     assert _bwd(u=None, w=None, du=None, dw=None) == CUDA
+
+
+def test_selftest_wait_rejects_bad_limits(lib):
+    # the limit is checked on the host before anything is launched
+    assert lib.txl_selftest_wait(0, None) == INVALID
+    assert lib.txl_selftest_wait(1000001, None) == INVALID

@@ -72,11 +72,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
-        # cuBLAS (the plain projection GEMM of project.cu) from the toolkit's
-        # library directory, found at run time through the rpath
-        libdir = os.path.join(os.path.dirname(os.path.dirname(cc)), "lib64")
-        cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + \
-            ["-lcublas", "-Xlinker", "-rpath=" + libdir]
+        # every kernel is the library's own: no CUDA math library is linked
+        cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan")
+           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
 
 
 class TxlError(RuntimeError):
@@ -77,6 +77,8 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_bwd.restype = i
     lib.txl_mem_update.argtypes = [vp, vp, i, i, i, i, i, vp]
     lib.txl_mem_update.restype = i
+    lib.txl_selftest_wait.argtypes = [ctypes.c_uint, vp]
+    lib.txl_selftest_wait.restype = i
     lib.txl_check.argtypes = [vp]
     lib.txl_check.restype = i
     lib.txl_status_string.argtypes = [i]
@@ -400,6 +402,13 @@ def mem_update_raw(dst_ptr, src_ptr, batch, mem_len, seg_len, d_model, dtype_cod
                    stream_ptr) -> int:
     return load_library().txl_mem_update(dst_ptr, src_ptr, batch, mem_len, seg_len, d_model,
                                          dtype_code, stream_ptr)
+
+
+def selftest_wait(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self test (txl_selftest_wait): a wait that runs
+    out after ``limit_us`` microseconds; the next ``check`` raises
+    TXL_ERR_TIMEOUT."""
+    _raise(load_library().txl_selftest_wait(int(limit_us), _stream_ptr(stream)), "txl_selftest_wait")
 
 
 def check(stream=None) -> None:

@@ -400,16 +400,24 @@ txl_status txl_ring_append(void *ring, const void *rows, int ring_len, int n_row
     return e == cudaSuccess ? TXL_OK : cuda_fail(e);
 }
 
+txl_status txl_selftest_wait(unsigned int limit_us, void *stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return TXL_ERR_INVALID;
+    const cudaError_t e = launch_selftest_wait((uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
+    return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+}
+
 txl_status txl_check(void *stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned int word = 0, gword = 0;
+    unsigned int word = 0, gword = 0, bword = 0;
     e = read_and_clear_device_error(&word, s);
     if (e == cudaSuccess) e = read_and_clear_gemm_error(&gword, s);
+    if (e == cudaSuccess) e = read_and_clear_bwd_error(&bword, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (word | gword) ? TXL_ERR_TIMEOUT : TXL_OK;
+    return (word | gword | bword) ? TXL_ERR_TIMEOUT : TXL_OK;
 }
 
 const char *txl_status_string(txl_status st)
@@ -449,7 +457,6 @@ void txl_shutdown(void)
     }
     g_scratch_n = kept;
     cudaGetLastError();
-    blas_shutdown();
 }
 
 }  // extern "C"

@@ -211,14 +211,15 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
 __device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_err_word, code); }
 
 // A bounded wait that also gives up as soon as another role has given up.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort)
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              uint64_t limit_ns = WAIT_NS)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > WAIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             record_error(1u);
             return false;
@@ -1901,6 +1902,33 @@ cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *
     }
     const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
     rel_attn_bwd_scores_kernel<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, md, p);
+    return cudaGetLastError();
+}
+
+namespace {
+// The failure path of the bounded waits, on its own: one warp waits on an
+// mbarrier that nothing ever completes, through the same wait the kernels
+// use but with the caller's limit.  The wait runs out, records the device
+// error word exactly as a kernel's wait does, and the kernel returns; no
+// copy, MMA or tensor memory is in flight, so nothing is left to drain.
+__global__ void selftest_wait_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_or_abort(smem_u32(&bar), 0, &abort_flag, limit_ns);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s)
+{
+    selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
     return cudaGetLastError();
 }
 

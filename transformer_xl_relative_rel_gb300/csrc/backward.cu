@@ -29,16 +29,25 @@
 //     the bf16 path; fp32 throughout on the fp32 path), and the kernels below
 //     do the bias fold, the softmax, its gradient and both shifts, and the
 //     batch / row reductions of dq, du, dv_bias and dr.
-#include <cublas_v2.h>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "internal.h"
+#include "sm100.cuh"
 #include "txl.h"
 
 namespace txl {
+
+// bounded waits of the backward's contraction kernel that gave up (read by txl_check)
+__device__ unsigned int g_bwd_err;
+
 namespace {
 
 template <typename T>
@@ -342,16 +351,365 @@ __global__ void bwd_table_grad_kernel(const float *__restrict__ part, T *__restr
 }
 
 // Row-major C (m x n, ldc) = op(A) . op(B) for `batch` problems at the given
-// element strides; ta: A is stored k x m (used transposed), tb: B is stored
-// n x k.  cuBLAS sees the column-major transpose C^T = op(B)^T op(A)^T.
-cublasStatus_t gemm_rm(cublasHandle_t hd, bool ta, bool tb, int m, int n, int k, const void *A, long lda,
-                       long long sA, const void *Bm, long ldb, long long sB, void *C, long ldc, long long sC,
-                       int batch, cudaDataType_t tab, cudaDataType_t tc)
+// element strides (sA, sB, sC between problems); ta: A is stored k x m (used
+// transposed), tb: B is stored n x k.  A 64 x 64 block of C per CTA, K in
+// slices of 16 staged in shared memory, 4 x 4 outputs per thread, fp32
+// accumulation: the plain contractions of the materialised route (the fp32
+// parity path and head sizes the tensor-core route does not take).
+constexpr int SG_T = 64, SG_K = 16;
+
+template <typename E, typename C>
+__global__ void __launch_bounds__(256)
+simt_gemm_kernel(bool ta, bool tb, int m, int n, int k, const E *__restrict__ A, long lda, long long sA,
+                 const E *__restrict__ Bm, long ldb, long long sB, C *__restrict__ Cm, long ldc, long long sC)
 {
-    const float one = 1.f, zero = 0.f;
-    return cublasGemmStridedBatchedEx(hd, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, n, m, k,
-                                      &one, Bm, tab, (int)ldb, sB, A, tab, (int)lda, sA, &zero, C, tc, (int)ldc,
-                                      sC, batch, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    __shared__ float as[SG_K][SG_T + 1];
+    __shared__ float bs[SG_K][SG_T + 1];
+    const long z = blockIdx.z;
+    const E *a = A + z * sA;
+    const E *b = Bm + z * sB;
+    C *c = Cm + z * sC;
+    const int m0 = blockIdx.y * SG_T, n0 = blockIdx.x * SG_T;
+    const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < k; k0 += SG_K) {
+        for (int x = tid; x < SG_K * SG_T; x += 256) {
+            // both tiles staged as [kk][row or column], element (row, k) read
+            // along whichever index is contiguous in memory
+            const int kk = ta ? x / SG_T : x % SG_K, mm = ta ? x % SG_T : x / SG_K;
+            const int gm = m0 + mm, gk = k0 + kk;
+            as[kk][mm] = (gm < m && gk < k) ? to_f(ta ? a[(long)gk * lda + gm] : a[(long)gm * lda + gk]) : 0.f;
+            const int kb = tb ? x % SG_K : x / SG_T, nn = tb ? x / SG_K : x % SG_T;
+            const int gn = n0 + nn, gkb = k0 + kb;
+            bs[kb][nn] = (gn < n && gkb < k) ? to_f(tb ? b[(long)gn * ldb + gkb] : b[(long)gkb * ldb + gn]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < SG_K; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = as[kk][tr + 16 * i];
+                bv[i] = bs[kk][tc + 16 * i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + tr + 16 * i;
+        if (gm >= m) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tc + 16 * j;
+            if (gn < n) c[(long)gm * ldc + gn] = from_f<C>(acc[i][j]);
+        }
+    }
+}
+
+template <typename E, typename C>
+bool gemm_rm(cudaStream_t s, bool ta, bool tb, int m, int n, int k, const void *A, long lda, long long sA,
+             const void *Bm, long ldb, long long sB, void *Cm, long ldc, long long sC, int batch)
+{
+    const dim3 grid((unsigned)((n + SG_T - 1) / SG_T), (unsigned)((m + SG_T - 1) / SG_T), (unsigned)batch);
+    if (grid.y > 65535 || grid.z > 65535) return false;
+    simt_gemm_kernel<E, C><<<grid, 256, 0, s>>>(ta, tb, m, n, k, (const E *)A, lda, sA, (const E *)Bm, ldb, sB,
+                                                (C *)Cm, ldc, sC);
+    return cudaGetLastError() == cudaSuccess;
+}
+
+// =========================================================================
+// The fused route's contractions on the tensor cores (bf16 operands, fp32
+// accumulation in TMEM).  For each batch entry z and 128-row block of C:
+//     C[z][m][0..63] = sum_p sum_k A_p[z](m, k) B_p[z](k, 0..63)
+// over one or two operand pairs p (dQ's content and position halves could
+// share a pass; each runs as its own pair here so that the bias gradients
+// see them apart).  A is K-major (rows m of a matrix contiguous along k) or
+// MN-major (the matrix stored with m contiguous, i.e. A^T row-major: P, dA
+// and the table-frame dA used transposed); B is MN-major with 64 columns
+// (rows k of 64 contiguous elements: dO, q+u, K, the table, q+v).  Both
+// arrive by TMA with the 128-byte swizzle: a K-major A stage is 128 rows x
+// 64 k; an MN-major A stage is two 64-row blocks of 64 k-rows, 8 KB apart
+// (the descriptor's leading-dimension offset), a B stage is 64 k-rows.
+// Warp 0 loads, warp 1 issues the MMAs (four K=16 steps per 64-wide stage),
+// warps 4-7 take the accumulator (two 64-column buffers in TMEM) to global
+// memory, a lane per row.
+constexpr int BG_M = 128, BG_K = 64, BG_ST = 6, BG_NT = 256;
+constexpr uint64_t BG_WAIT_NS = 2000000000ull;
+
+struct BgSmem {
+    static constexpr uint32_t ASZ = BG_M * 128;        // 16 KB
+    static constexpr uint32_t BSZ = BG_K * 128;        // 8 KB
+    static constexpr uint32_t A = 0;
+    static constexpr uint32_t B = A + BG_ST * ASZ;
+    static constexpr uint32_t BARS = B + BG_ST * BSZ;
+    static constexpr int FULL = 0, EMPTY = BG_ST, AFULL = 2 * BG_ST, AEMPTY = 2 * BG_ST + 2,
+                         DONE = 2 * BG_ST + 4, NBAR = 2 * BG_ST + 5;
+    static constexpr uint32_t MISC = BARS + NBAR * 8;
+    static constexpr uint32_t TOTAL = MISC + 16 + 1024;
+};
+
+struct BgOperand {
+    int rank;         // 3: coordinates (c0, c1, z') ; 4: (c0, c1, z / H, z % H)
+    int zmod;         // rank 3: z' = z (0) or z % H (1)
+};
+
+struct BgParams {
+    BgOperand a[2], b[2];
+    int pairs, a_mn, ksteps[2];
+    int M, nz, H, mtiles, tiles;
+    void *out;
+    long ostride;     // elements between output rows; batch entry z starts at z * 64
+    int ofp32;        // output fp32 (else bf16)
+};
+
+__device__ __forceinline__ void bg_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bg_load(uint32_t dst, const CUtensorMap *m, uint32_t bar, const BgOperand &o, int c0,
+                                        int c1, int z, int H)
+{
+    if (o.rank == 4)
+        sm100::tma_load_4d(dst, m, bar, c0, c1, z / H, z % H);
+    else
+        sm100::tma_load_3d(dst, m, bar, c0, c1, o.zmod ? z % H : z);
+}
+
+__global__ void __launch_bounds__(BG_NT, 1)
+bwd_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
+                const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, const BgParams p)
+{
+    using namespace sm100;
+    using S = BgSmem;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + S::BARS + 8u * (uint32_t)i; };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::MISC + 8);
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        const uint32_t b = bar(i);
+        if (mbar_try_wait(b, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            if (mbar_try_wait_sleep(b, parity, WAIT_SLEEP_NS)) return true;
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > BG_WAIT_NS) {
+                *abort = 1;
+                atomicOr(&g_bwd_err, 1u);
+                return false;
+            }
+        }
+    };
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), 128);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        *abort = 0;
+        for (int x = 0; x < BG_ST; ++x) {
+            mbar_init(bar(S::FULL + x), 1);
+            mbar_init(bar(S::EMPTY + x), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(S::AFULL + x), 1);
+            mbar_init(bar(S::AEMPTY + x), 128);
+        }
+        mbar_init(bar(S::DONE), 1);
+        fence_mbar_init();
+        prefetch_tmap(&ta0);
+        prefetch_tmap(&tb0);
+        if (p.pairs > 1) {
+            prefetch_tmap(&ta1);
+            prefetch_tmap(&tb1);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int G = gridDim.x;
+
+    if (warp == 0) {
+        // =================================================================== TMA producer
+        if (lane == 0) {
+            const uint32_t bytes = S::ASZ + S::BSZ;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
+                const int z = t / p.mtiles, m0 = (t % p.mtiles) * BG_M;
+                for (int q = 0; ok && q < p.pairs; ++q) {
+                    const CUtensorMap *ma = q ? &ta1 : &ta0, *mb = q ? &tb1 : &tb0;
+                    for (int ks = 0; ks < p.ksteps[q]; ++ks, ++it) {
+                        const int s = it % BG_ST;
+                        if (it >= BG_ST && !wait(S::EMPTY + s, ((it / BG_ST) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t da = sbase + S::A + s * S::ASZ, db = sbase + S::B + s * S::BSZ;
+                        mbar_arrive_expect_tx(bar(S::FULL + s), bytes);
+                        if (p.a_mn) {
+                            // two 64-row blocks of the transposed matrix, 8 KB apart
+                            bg_load(da, ma, bar(S::FULL + s), p.a[q], m0, ks * BG_K, z, p.H);
+                            bg_load(da + 8192u, ma, bar(S::FULL + s), p.a[q], m0 + 64, ks * BG_K, z, p.H);
+                        } else {
+                            bg_load(da, ma, bar(S::FULL + s), p.a[q], ks * BG_K, m0, z, p.H);
+                        }
+                        bg_load(db, mb, bar(S::FULL + s), p.b[q], 0, ks * BG_K, z, p.H);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // =================================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(BG_M, 64, p.a_mn, 1);
+            // K-major A: K steps of 32 bytes along the row; MN-major A and B:
+            // K steps of 16 rows (2 KB), the A blocks 8 KB apart
+            const uint64_t da0 = p.a_mn ? smem_desc_sw128(sbase + S::A, 8192, 1024)
+                                        : smem_desc_sw128(sbase + S::A, 16, 1024);
+            const uint64_t db0 = smem_desc_sw128(sbase + S::B, 16, 1024);
+            const uint64_t astep = p.a_mn ? 128 : 2;
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += G, ++lt) {
+                const int buf = lt & 1;
+                if (lt >= 2 && !wait(S::AEMPTY + buf, ((lt >> 1) - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)buf * 64u;
+                bool first = true;
+                for (int q = 0; ok && q < p.pairs; ++q) {
+                    for (int ks = 0; ks < p.ksteps[q]; ++ks, ++it) {
+                        const int s = it % BG_ST;
+                        if (!wait(S::FULL + s, (it / BG_ST) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t da = da0 + ((uint64_t)(s * S::ASZ) >> 4);
+                        const uint64_t db = db0 + ((uint64_t)(s * S::BSZ) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < BG_K / 16; ++kk) {
+                            mma_bf16_ss(acc, da + astep * kk, db + 128 * kk, idesc, first ? 0u : 1u);
+                            first = false;
+                        }
+                        mma_commit(bar(S::EMPTY + s));
+                    }
+                }
+                if (ok) mma_commit(bar(S::AFULL + buf));
+            }
+            mma_commit(bar(S::DONE));
+            wait(S::DONE, 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // =================================================================== epilogue
+        const int q = warp & 3;
+        int lt = 0;
+        for (int t = blockIdx.x; t < p.tiles; t += G, ++lt) {
+            const int buf = lt & 1;
+            const int z = t / p.mtiles, m0 = (t % p.mtiles) * BG_M;
+            if (!wait(S::AFULL + buf, (lt >> 1) & 1)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 64u;
+            float v[64];
+            tmem_ld32(tacc, *reinterpret_cast<float(*)[32]>(v));
+            tmem_ld32(tacc + 32u, *reinterpret_cast<float(*)[32]>(v + 32));
+            tc_fence_before();
+            bg_arrive(bar(S::AEMPTY + buf));
+            const int row = m0 + 32 * q + lane;
+            if (row < p.M) {
+                const long off = (long)row * p.ostride + (long)z * 64;
+                if (p.ofp32) {
+                    float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + off);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else {
+                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + off);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 pk;
+                        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
+                        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+                        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+                        pk.x = *reinterpret_cast<uint32_t *>(&h0);
+                        pk.y = *reinterpret_cast<uint32_t *>(&h1);
+                        pk.z = *reinterpret_cast<uint32_t *>(&h2);
+                        pk.w = *reinterpret_cast<uint32_t *>(&h3);
+                        o[j] = pk;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 bg_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// A bf16 tensor map with the 128-byte swizzle: dims / byte strides (of dims
+// 1..rank-1) / box, innermost first.
+bool bg_map(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+            const cuuint32_t *box)
+{
+    auto enc = bg_encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_bwd_gemm(const CUtensorMap *ma, const CUtensorMap *mb, const BgParams &p0, cudaStream_t s)
+{
+    BgParams p = p0;
+    p.mtiles = (p.M + BG_M - 1) / BG_M;
+    const long tiles = (long)p.mtiles * p.nz;
+    if (tiles > INT32_MAX) return cudaErrorNotSupported;
+    p.tiles = (int)tiles;
+    if (p.tiles == 0) return cudaSuccess;
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(opted.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BgSmem::TOTAL);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_relaxed);
+    }
+    const int grid = p.tiles < device_sm_count() ? p.tiles : device_sm_count();
+    bwd_gemm_kernel<<<(unsigned)grid, BG_NT, BgSmem::TOTAL, s>>>(ma[0], mb[0], p.pairs > 1 ? ma[1] : ma[0],
+                                                                  p.pairs > 1 ? mb[1] : mb[0], p);
+    return cudaGetLastError();
 }
 
 struct Ws {
@@ -442,13 +800,11 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
     const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, rows = BH * L;
     const long ld = BH * D;                 // row pitch of the [pos][B][H][D] tensors
     const float scale = 1.f / sqrtf((float)D);
-    const cudaDataType_t ty = bf16 ? CUDA_R_16BF : CUDA_R_32F;
     E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv), *rrep = (E *)(ws + lay.rrep);
     E *pb = (E *)(ws + lay.pb), *dab = (E *)(ws + lay.da), *dbb = (E *)(ws + lay.db);
     float *x1 = (float *)(ws + lay.x1), *x2 = (float *)(ws + lay.x2);
     float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp), *drp = (float *)(ws + lay.drp);
-    cublasHandle_t hd = (cublasHandle_t)blas_on_stream(s);
-    if (!hd) return TXL_ERR_CUDA;
+    (void)bf16;
     cudaError_t e = cudaSuccess;
     auto chk = [&]() {
         e = cudaGetLastError();
@@ -472,8 +828,8 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
         const long long LT = (long long)L * T, TD = (long long)T * D;
         const int Ti = (int)T, nb = (int)BH;
         // content and table products, then the softmax
-        if (gemm_rm(hd, false, true, L, Ti, D, qu, ld, D, k, ld, D, x1, T, LT, nb, ty, CUDA_R_32F) ||
-            gemm_rm(hd, false, true, L, Ti, D, qv, ld, D, rrep, D, TD, x2, T, LT, nb, ty, CUDA_R_32F))
+        if (!gemm_rm<E, float>(s, false, true, L, Ti, D, qu, ld, D, k, ld, D, x1, T, LT, nb) ||
+            !gemm_rm<E, float>(s, false, true, L, Ti, D, qv, ld, D, rrep, D, TD, x2, T, LT, nb))
             return TXL_ERR_CUDA;
         if (T <= RB * 6)
             bwd_softmax_row_kernel<E, 6><<<(unsigned)rows, RB, 0, s>>>(x1, x2, pb, L, M, Ti, scale);
@@ -483,8 +839,7 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
             bwd_softmax_kernel<E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x1, x2, pb, rows, L, M, Ti, scale);
         if (!chk()) goto cuda_fail;
         // dP, then the score gradient in both frames
-        if (gemm_rm(hd, false, true, L, Ti, D, dout, ld, D, v, ld, D, x2, T, LT, nb, ty, CUDA_R_32F))
-            return TXL_ERR_CUDA;
+        if (!gemm_rm<E, float>(s, false, true, L, Ti, D, dout, ld, D, v, ld, D, x2, T, LT, nb)) return TXL_ERR_CUDA;
         if (T <= RB * 6)
             bwd_score_grad_row_kernel<E, 6><<<(unsigned)rows, RB, 0, s>>>(x1, x2, dab, dbb, L, M, Ti, scale);
         else if (T <= RB * 16)
@@ -494,11 +849,11 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
                                                                                 Ti, scale);
         if (!chk()) goto cuda_fail;
         // dV = P^T dO, dK = dA^T qu, dQ = dA K + dB~ r, dr per (b, h) = dB~^T qv
-        if (gemm_rm(hd, true, false, Ti, D, L, pb, T, LT, dout, ld, D, dv, ld, D, nb, ty, ty) ||
-            gemm_rm(hd, true, false, Ti, D, L, dab, T, LT, qu, ld, D, dk, ld, D, nb, ty, ty) ||
-            gemm_rm(hd, false, false, L, D, Ti, dab, T, LT, k, ld, D, dqc, ld, D, nb, ty, CUDA_R_32F) ||
-            gemm_rm(hd, false, false, L, D, Ti, dbb, T, LT, rrep, D, TD, dqp, ld, D, nb, ty, CUDA_R_32F) ||
-            gemm_rm(hd, true, false, Ti, D, L, dbb, T, LT, qv, ld, D, drp, D, TD, nb, ty, CUDA_R_32F))
+        if (!gemm_rm<E, E>(s, true, false, Ti, D, L, pb, T, LT, dout, ld, D, dv, ld, D, nb) ||
+            !gemm_rm<E, E>(s, true, false, Ti, D, L, dab, T, LT, qu, ld, D, dk, ld, D, nb) ||
+            !gemm_rm<E, float>(s, false, false, L, D, Ti, dab, T, LT, k, ld, D, dqc, ld, D, nb) ||
+            !gemm_rm<E, float>(s, false, false, L, D, Ti, dbb, T, LT, rrep, D, TD, dqp, ld, D, nb) ||
+            !gemm_rm<E, float>(s, true, false, Ti, D, L, dbb, T, LT, qv, ld, D, drp, D, TD, nb))
             return TXL_ERR_CUDA;
     }
     if ((e = launch_sum_bias<E>(dqc, dqp, (E *)dq, du, dw, (long)L * B, H * D, s)) != cudaSuccess) goto cuda_fail;
@@ -516,13 +871,11 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
                          unsigned char *ws, const WsF &lay, cudaStream_t s)
 {
     typedef __nv_bfloat16 E;
-    const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, ld = BH * D, TP = lay.TP;
+    const long T = (long)M + L, BH = (long)B * H, nq = (long)L * BH * D, TP = lay.TP;
     E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv);
     E *pb = (E *)(ws + lay.pb), *dab = (E *)(ws + lay.da), *dbb = (E *)(ws + lay.db), *outf = (E *)(ws + lay.out);
     float *lse = (float *)(ws + lay.lse);
     float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp);
-    cublasHandle_t hd = (cublasHandle_t)blas_on_stream(s);
-    if (!hd) return TXL_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     auto chk = [&]() {
         e = cudaGetLastError();
@@ -556,18 +909,55 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
     bwd_fold_vec_kernel<E><<<grid_for(nq / 8, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / 8, H, D);
     if (!chk()) goto cuda_fail;
     {
-        const long long LTP = (long long)L * TP, LBTP = (long long)L * B * TP;
-        const int Ti = (int)T, nb = (int)BH, LB = L * B, HD = H * D;
-        // per (b, h): dV = P^T dO, dK = dA^T qu, dQ (content) = dA K; per head
-        // over the rows (i, b) of the head-major table-frame matrix dA~:
-        // dQ (position) = dA~ r_h and dr_h = dA~^T qv, both straight into
-        // their [.., H, D] layouts
-        if (gemm_rm(hd, true, false, Ti, D, L, pb, TP, LTP, dout, ld, D, dv, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
-            gemm_rm(hd, true, false, Ti, D, L, dab, TP, LTP, qu, ld, D, dk, ld, D, nb, CUDA_R_16BF, CUDA_R_16BF) ||
-            gemm_rm(hd, false, false, L, D, Ti, dab, TP, LTP, k, ld, D, dqc, ld, D, nb, CUDA_R_16BF, CUDA_R_32F) ||
-            gemm_rm(hd, false, false, LB, D, Ti, dbb, TP, LBTP, r, HD, D, dqp, HD, D, H, CUDA_R_16BF, CUDA_R_32F) ||
-            gemm_rm(hd, true, false, Ti, D, LB, dbb, TP, LBTP, qv, HD, D, dr, HD, D, H, CUDA_R_16BF, CUDA_R_16BF))
+        // per (b, h): dV = P^T dO, dK = dA^T qu (rows j of the transposed
+        // [L][TP] matrices), dQ's content half dA K (rows i); per (b, h) rows
+        // i of the head-major table-frame dA~: dQ's position half dA~ r; per
+        // head, over the head's (i, b) rows of dA~: dr = dA~^T qv (the batch
+        // sum falls out of the contraction)
+        const cuuint64_t e2 = 2, tp2 = (cuuint64_t)TP * e2, row2 = (cuuint64_t)BH * 64 * e2;
+        CUtensorMap pmn, damn, dak, dbk, dbmn, mdo, mqu, mk, mr, mqv;
+        const cuuint64_t d_mat[3] = {(cuuint64_t)TP, (cuuint64_t)L, (cuuint64_t)BH};
+        const cuuint64_t s_mat[2] = {tp2, (cuuint64_t)L * tp2};
+        const cuuint32_t box_mn[3] = {64, 64, 1}, box_k[3] = {64, 128, 1};
+        const cuuint64_t d_db4[4] = {(cuuint64_t)TP, (cuuint64_t)L, (cuuint64_t)B, (cuuint64_t)H};
+        const cuuint64_t s_db4[3] = {(cuuint64_t)B * tp2, tp2, (cuuint64_t)L * B * tp2};
+        const cuuint32_t box_k4[4] = {64, 128, 1, 1};
+        const cuuint64_t d_db3[3] = {(cuuint64_t)TP, (cuuint64_t)L * B, (cuuint64_t)H};
+        const cuuint64_t s_db3[2] = {tp2, (cuuint64_t)L * B * tp2};
+        const cuuint64_t d_q[3] = {64, (cuuint64_t)L, (cuuint64_t)BH}, s_q[2] = {row2, 64 * e2};
+        const cuuint64_t d_k[3] = {64, (cuuint64_t)T, (cuuint64_t)BH};
+        const cuuint64_t d_r[3] = {64, (cuuint64_t)T, (cuuint64_t)H}, s_r[2] = {(cuuint64_t)H * 64 * e2, 64 * e2};
+        const cuuint64_t d_qv[3] = {64, (cuuint64_t)L * B, (cuuint64_t)H};
+        if (!bg_map(&pmn, 3, pb, d_mat, s_mat, box_mn) || !bg_map(&damn, 3, dab, d_mat, s_mat, box_mn) ||
+            !bg_map(&dak, 3, dab, d_mat, s_mat, box_k) || !bg_map(&dbk, 4, dbb, d_db4, s_db4, box_k4) ||
+            !bg_map(&dbmn, 3, dbb, d_db3, s_db3, box_mn) || !bg_map(&mdo, 3, dout, d_q, s_q, box_mn) ||
+            !bg_map(&mqu, 3, qu, d_q, s_q, box_mn) || !bg_map(&mk, 3, k, d_k, s_q, box_mn) ||
+            !bg_map(&mr, 3, r, d_r, s_r, box_mn) || !bg_map(&mqv, 3, qv, d_qv, s_r, box_mn))
             return TXL_ERR_CUDA;
+        const BgOperand o3{3, 0}, o3h{3, 1}, o4{4, 0};
+        auto run = [&](const CUtensorMap &a, const BgOperand &ao, const CUtensorMap &b, const BgOperand &bo, int a_mn,
+                       long K, int M, int nz, void *outp, long ostride, int ofp32) {
+            BgParams g{};
+            g.a[0] = ao;
+            g.b[0] = bo;
+            g.pairs = 1;
+            g.a_mn = a_mn;
+            g.ksteps[0] = (int)((K + BG_K - 1) / BG_K);
+            g.M = M;
+            g.nz = nz;
+            g.H = H;
+            g.out = outp;
+            g.ostride = ostride;
+            g.ofp32 = ofp32;
+            return launch_bwd_gemm(&a, &b, g, s);
+        };
+        const long ld64 = BH * 64;
+        if ((e = run(pmn, o3, mdo, o3, 1, L, (int)T, (int)BH, dv, ld64, 0)) != cudaSuccess ||
+            (e = run(damn, o3, mqu, o3, 1, L, (int)T, (int)BH, dk, ld64, 0)) != cudaSuccess ||
+            (e = run(dak, o3, mk, o3, 0, T, L, (int)BH, dqc, ld64, 1)) != cudaSuccess ||
+            (e = run(dbk, o4, mr, o3h, 0, T, L, (int)BH, dqp, ld64, 1)) != cudaSuccess ||
+            (e = run(dbmn, o3, mqv, o3, 1, (long)L * B, (int)T, H, dr, (long)H * 64, 0)) != cudaSuccess)
+            goto cuda_fail;
     }
     // dq and the bias gradients in one pass over the two fp32 halves of dq
     if ((e = launch_sum_bias<E>(dqc, dqp, (E *)dq, du, dw, (long)L * B, H * D, s)) != cudaSuccess) goto cuda_fail;
@@ -591,13 +981,28 @@ txl_status check_sizes(int batch, int mem_len, int seg_len, int heads, int d_hea
     if (batch < 1 || mem_len < 0 || seg_len < 1 || heads < 1 || d_head < 1) return TXL_ERR_INVALID;
     if (d_head > 128) return TXL_ERR_UNSUPPORTED;
     const long T = (long)mem_len + seg_len;
-    // cuBLAS dimensions, leading dimensions and batch counts are int
-    if (T > INT32_MAX || (long)batch * heads * d_head > INT32_MAX || (long)batch * heads > INT32_MAX)
+    // GEMM dimensions and leading dimensions are int; batch counts index a grid dimension
+    if (T > INT32_MAX || (long)batch * heads * d_head > INT32_MAX || (long)batch * heads > 65535)
         return TXL_ERR_UNSUPPORTED;
     return TXL_OK;
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_bwd_error(unsigned int *word, cudaStream_t s)
+{
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_bwd_err, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_bwd_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
 }  // namespace txl
 
 using namespace txl;

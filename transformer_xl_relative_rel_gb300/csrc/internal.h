@@ -38,6 +38,9 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
 // a.out and row log-sum-exp `lse` ([B*H][L]).
 cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, void *p_out, void *da_out,
                               void *db_out, long TP, cudaStream_t s);
+// one warp's bounded wait on an mbarrier nothing completes, limit_ns long;
+// records the device error word when it runs out (the failure path, tested)
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
 // reads and clears the device error word written by bounded waits (syncs on s)
 cudaError_t read_and_clear_device_error(unsigned int *word, cudaStream_t s);
 
@@ -68,14 +71,10 @@ int device_sm_count();
 // the lookup.
 cudaError_t zero_bias(size_t count, const float **out);
 
-// the projection kernel's error word (bounded waits that gave up), as above
+// the projection kernel's and the backward contraction kernel's error words
+// (bounded waits that gave up), as above
 cudaError_t read_and_clear_gemm_error(unsigned int *word, cudaStream_t s);
-
-// releases the per-device cuBLAS handles of project.cu
-cudaError_t blas_shutdown();
-// the current device's cuBLAS handle (a cublasHandle_t) bound to stream s,
-// created on first use; NULL when cuBLAS cannot be initialised
-void *blas_on_stream(cudaStream_t s);
+cudaError_t read_and_clear_bwd_error(unsigned int *word, cudaStream_t s);
 
 // records `e` as the thread's last CUDA error (reported by txl_last_cuda_error)
 // and clears the runtime's error state; returns e

@@ -9,14 +9,13 @@
 //     (128 x up to 256 output tiles, fp32 accumulation in TMEM, operands
 //     staged by TMA or, for rows TMA cannot address, by 4-byte cp.async, a
 //     double-buffered accumulator so that a tile's epilogue overlaps the
-//     next tile's MMAs, output by 16-byte stores); fp32 and odd shapes: a tiled
+//     next tile's MMAs, output by TMA store); fp32 and odd shapes: a tiled
 //     CUDA-core kernel.
 //   txl_rel_table: r[t][h][d] = sum_c R[T-1-t][c] W_kR[h*d_head + d][c], the
 //     reversed projected table of Appendix B, with R the sinusoid encoding of
 //     the relative distance (row p: sin / cos of p * 10000^(-2c/d_model)).
 //     Computed once per layer (it does not depend on the batch or on the
 //     segment); the sinusoid is evaluated in the kernel, fp32 accumulation.
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,26 +37,6 @@ __device__ unsigned int g_gemm_err;
 
 namespace {
 using namespace sm100;
-
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {nullptr};
-
-// one cuBLAS handle per device, created on first use (released by txl_shutdown)
-cublasStatus_t blas_handle(cublasHandle_t *out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CUBLAS_STATUS_NOT_INITIALIZED;
-    std::lock_guard<std::mutex> lock(g_blas_mu);
-    if (!g_blas[dev]) {
-        cublasStatus_t st = cublasCreate(&g_blas[dev]);
-        if (st != CUBLAS_STATUS_SUCCESS) {
-            g_blas[dev] = nullptr;
-            return st;
-        }
-    }
-    *out = g_blas[dev];
-    return CUBLAS_STATUS_SUCCESS;
-}
 
 template <typename T>
 __device__ __forceinline__ T from_float(float x);
@@ -84,8 +63,9 @@ __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { retu
 //   warp 0     TMA producer (one thread), or with warps 2 and 3 the
 //              cp.async loaders when TMA cannot address the rows;
 //   warp 1     one thread issues the MMAs (four K=16 steps per stage);
-//   warps 4-7  epilogue: TMEM -> registers -> bf16 -> 16-byte stores (a
-//              lane per row, 64 columns per chunk).
+//   warps 4-7  epilogue: TMEM -> registers -> bf16 -> swizzled staging (two
+//              buffers per warp) -> TMA store (32 rows x 64 columns per warp
+//              and chunk).
 // TMEM: two 256-column accumulators (tile i's epilogue overlaps tile i+1).
 constexpr int GM = 128;           // output rows per tile (TMEM lanes)
 constexpr int GK = 64;            // K elements per stage (one swizzled row)
@@ -100,7 +80,8 @@ struct GemmSmem {
     static constexpr uint32_t BSZ = GBN * 128;                // one stage of W: up to 32 KB
     static constexpr uint32_t A = 0;
     static constexpr uint32_t B = A + GST * ASZ;
-    static constexpr uint32_t BOFF = B + GST * BSZ;           // W row offsets of a tile, per loader warp
+    static constexpr uint32_t OST = B + GST * BSZ;            // 4 epilogue warps x 2 x 4 KB staging
+    static constexpr uint32_t BOFF = OST + 8 * 4096;          // W row offsets of a tile, per loader warp
     static constexpr uint32_t BARS = BOFF + 3 * 128 * 4;
     static constexpr int FULL = 0, EMPTY = GST, AFULL = 2 * GST, AEMPTY = 2 * GST + 2, DONE = 2 * GST + 4,
                          NBAR = 2 * GST + 5;
@@ -113,7 +94,7 @@ struct GemmParams {
     __nv_bfloat16 *out;
     int rows, d_in, heads, d_head, d_pad, n_out;
     int bn, tiles_n, tiles, ksteps;
-    int vec_out;        // out 16-byte aligned and n_out a multiple of 8: 16-byte stores
+    int tma_out;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -130,7 +111,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
 template <bool kTmaIn>
 __global__ void __launch_bounds__(GNT, 1)
 project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                    const GemmParams p)
+                    const __grid_constant__ CUtensorMap tm_o, const GemmParams p)
 {
     using S = GemmSmem;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -177,6 +158,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             prefetch_tmap(&tm_x);
             prefetch_tmap(&tm_w);
         }
+        if (p.tma_out) prefetch_tmap(&tm_o);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -302,8 +284,10 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     } else {
         // =================================================================== epilogue
         const int q = warp & 3;                      // TMEM lanes 32q .. 32q+31
+        unsigned char *stg0 = smem + S::OST + (uint32_t)(warp - 4) * 8192u;
+        const uint32_t stg0_a = sbase + S::OST + (uint32_t)(warp - 4) * 8192u;
         const int nch = (p.bn + 63) / 64;
-        int lt = 0;
+        int lt = 0, nst = 0;                         // tiles, chunks stored (two staging buffers)
         for (int t = blockIdx.x; t < p.tiles; t += G, ++lt) {
             const int buf = lt & 1;
             const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
@@ -326,24 +310,27 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     if (d >= p.d_head) v[j] = 0.f;
                     if (++d == p.d_pad) d = 0;
                 }
-                if (p.vec_out) {
-                    // 16-byte stores straight from registers: lane = row, eight
-                    // columns per store (the row's next store fills the rest of
-                    // the 32-byte sector)
-                    const int row = m0 + 32 * q + lane;
-                    if (row < p.rows) {
-                        __nv_bfloat16 *o = p.out + (long)row * p.n_out + col0;
+                if (p.tma_out) {
+                    if (col0 >= p.n_out) continue;
+                    unsigned char *stg = stg0 + (nst & 1) * 4096;
+                    const uint32_t stg_a = stg0_a + (uint32_t)(nst & 1) * 4096u;
+                    ++nst;
+                    if (lane == 0) bulk_wait_read_1();   // the store before last has read this buffer
+                    __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (col0 + 8 * j < p.n_out) {
-                                uint4 pk;
-                                pk.x = pack2_bf16(v[8 * j + 0], v[8 * j + 1]);
-                                pk.y = pack2_bf16(v[8 * j + 2], v[8 * j + 3]);
-                                pk.z = pack2_bf16(v[8 * j + 4], v[8 * j + 5]);
-                                pk.w = pack2_bf16(v[8 * j + 6], v[8 * j + 7]);
-                                *reinterpret_cast<uint4 *>(o + 8 * j) = pk;
-                            }
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 pk;
+                        pk.x = pack2_bf16(v[8 * j + 0], v[8 * j + 1]);
+                        pk.y = pack2_bf16(v[8 * j + 2], v[8 * j + 3]);
+                        pk.z = pack2_bf16(v[8 * j + 4], v[8 * j + 5]);
+                        pk.w = pack2_bf16(v[8 * j + 6], v[8 * j + 7]);
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_o, stg_a, col0, m0 + 32 * q);   // rows / columns past the end are clipped
+                        bulk_commit();
                     }
                 } else {
                     const int row = m0 + 32 * q + lane;
@@ -355,6 +342,8 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -433,7 +422,8 @@ bool gmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, co
 bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
 template <bool kTmaIn>
-cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const GemmParams &p, cudaStream_t s)
+cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mo, const GemmParams &p,
+                          cudaStream_t s)
 {
     auto kern = project_gemm_kernel<kTmaIn>;
     static std::atomic<uint64_t> opted{0};
@@ -447,7 +437,7 @@ cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const Ge
         opted.fetch_or(bit, std::memory_order_relaxed);
     }
     const int grid = p.tiles < device_sm_count() ? p.tiles : device_sm_count();
-    kern<<<(unsigned)grid, GNT, GemmSmem::TOTAL, s>>>(mx, mw, p);
+    kern<<<(unsigned)grid, GNT, GemmSmem::TOTAL, s>>>(mx, mw, mo, p);
     return cudaGetLastError();
 }
 
@@ -474,8 +464,8 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
     // TMA addresses rows whose pitch is a multiple of 16 bytes; a W box holds
     // whole heads of d_pad rows
     const bool tma_in = d_in % 8 == 0 && al(x, 16) && al(w, 16) && p.bn % d_pad == 0 && d_pad <= 256;
-    p.vec_out = al(out, 16) && p.n_out % 8 == 0;
-    CUtensorMap mx{}, mw{};
+    p.tma_out = al(out, 16) && (p.n_out * 2) % 16 == 0;
+    CUtensorMap mx{}, mw{}, mo{};
     if (tma_in) {
         const cuuint64_t dx[2] = {(cuuint64_t)d_in, (cuuint64_t)rows}, sx[1] = {(cuuint64_t)d_in * 2};
         const cuuint32_t bx[2] = {GK, GM};
@@ -484,7 +474,12 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
         const cuuint32_t bw[3] = {GK, (cuuint32_t)d_pad, (cuuint32_t)(p.bn / d_pad)};
         if (!gmap(&mx, 2, x, dx, sx, bx) || !gmap(&mw, 3, w, dw, sw, bw)) return cudaErrorInvalidValue;
     }
-    return tma_in ? launch_gemm_t<true>(mx, mw, p, s) : launch_gemm_t<false>(mx, mw, p, s);
+    if (p.tma_out) {
+        const cuuint64_t dO[2] = {(cuuint64_t)p.n_out, (cuuint64_t)rows}, sO[1] = {(cuuint64_t)p.n_out * 2};
+        const cuuint32_t bO[2] = {64, 32};
+        if (!gmap(&mo, 2, out, dO, sO, bO)) return cudaErrorInvalidValue;
+    }
+    return tma_in ? launch_gemm_t<true>(mx, mw, mo, p, s) : launch_gemm_t<false>(mx, mw, mo, p, s);
 }
 
 // =========================================================================
@@ -612,23 +607,6 @@ bool overlap_bytes(const void *a, size_t na, const void *b, size_t nb)
 }
 
 }  // namespace
-
-void *blas_on_stream(cudaStream_t s)
-{
-    cublasHandle_t h = nullptr;
-    if (blas_handle(&h) != CUBLAS_STATUS_SUCCESS || cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    return (void *)h;
-}
-
-cudaError_t blas_shutdown()
-{
-    std::lock_guard<std::mutex> lock(g_blas_mu);
-    for (auto &h : g_blas) {
-        if (h) cublasDestroy(h);
-        h = nullptr;
-    }
-    return cudaSuccess;
-}
 
 cudaError_t read_and_clear_gemm_error(unsigned int *word, cudaStream_t s)
 {
