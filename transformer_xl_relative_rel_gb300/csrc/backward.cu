@@ -465,6 +465,7 @@ struct BgParams {
     void *out;
     long ostride;     // elements between output rows; batch entry z starts at z * 64
     int ofp32;        // output fp32 (else bf16)
+    int oadd;         // fp32 reductions into out at column (z % H) * 64 (the batch sum of dr)
 };
 
 __device__ __forceinline__ void bg_arrive(uint32_t bar)
@@ -628,7 +629,16 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__
             tc_fence_before();
             bg_arrive(bar(S::AEMPTY + buf));
             const int row = m0 + 32 * q + lane;
-            if (row < p.M) {
+            if (row < p.M && p.oadd) {
+                // this batch entry's share of a sum over the batch: 16-byte
+                // fp32 reductions (the order of the adds is not fixed)
+                float *o = reinterpret_cast<float *>(p.out) + (long)row * p.ostride + (long)(z % p.H) * 64;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(o + 4 * j), "f"(v[4 * j]),
+                                 "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                                 : "memory");
+            } else if (row < p.M) {
                 const long off = (long)row * p.ostride + (long)z * 64;
                 if (p.ofp32) {
                     float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + off);
@@ -658,6 +668,19 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
+    }
+}
+
+// bf16 copy of an fp32 array, four elements per thread and step
+__global__ void bwd_round_kernel(const float *__restrict__ src, __nv_bfloat16 *__restrict__ dst, long n4)
+{
+    for (long x = (long)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (long)gridDim.x * blockDim.x) {
+        const float4 f = reinterpret_cast<const float4 *>(src)[x];
+        __nv_bfloat162 a = __floats2bfloat162_rn(f.x, f.y), b = __floats2bfloat162_rn(f.z, f.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a);
+        u.y = *reinterpret_cast<uint32_t *>(&b);
+        reinterpret_cast<uint2 *>(dst)[x] = u;
     }
 }
 
@@ -744,7 +767,7 @@ Ws layout(long B, long H, long D, long L, long M, size_t es)
 // kernel, the forward's output and row log-sum-exp, delta, and the same
 // GEMM operands and partial sums as the materialised path.
 struct WsF {
-    size_t pb, da, db, qu, qv, dqc, dqp, out, lse, split, total;
+    size_t pb, da, db, qu, qv, dqc, dqp, out, lse, split, dracc, total;
     long TP;
     int splits;
 };
@@ -773,6 +796,7 @@ WsF layout_fused(long B, long H, long D, long L, long M)
     a.M = (int)M;
     w.splits = bf16_num_splits(a, device_sm_count());
     w.split = o; o += up256(w.splits > 1 ? bf16_scratch_bytes(a, w.splits) : 0);
+    w.dracc = o; o += up256((size_t)T * H * D * 4);
     w.total = o;
     return w;
 }
@@ -875,7 +899,7 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
     E *qu = (E *)(ws + lay.qu), *qv = (E *)(ws + lay.qv);
     E *pb = (E *)(ws + lay.pb), *dab = (E *)(ws + lay.da), *dbb = (E *)(ws + lay.db), *outf = (E *)(ws + lay.out);
     float *lse = (float *)(ws + lay.lse);
-    float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp);
+    float *dqc = (float *)(ws + lay.dqc), *dqp = (float *)(ws + lay.dqp), *dracc = (float *)(ws + lay.dracc);
     cudaError_t e = cudaSuccess;
     auto chk = [&]() {
         e = cudaGetLastError();
@@ -922,21 +946,19 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
         const cuuint64_t d_db4[4] = {(cuuint64_t)TP, (cuuint64_t)L, (cuuint64_t)B, (cuuint64_t)H};
         const cuuint64_t s_db4[3] = {(cuuint64_t)B * tp2, tp2, (cuuint64_t)L * B * tp2};
         const cuuint32_t box_k4[4] = {64, 128, 1, 1};
-        const cuuint64_t d_db3[3] = {(cuuint64_t)TP, (cuuint64_t)L * B, (cuuint64_t)H};
-        const cuuint64_t s_db3[2] = {tp2, (cuuint64_t)L * B * tp2};
+        const cuuint32_t box_mn4[4] = {64, 64, 1, 1};
         const cuuint64_t d_q[3] = {64, (cuuint64_t)L, (cuuint64_t)BH}, s_q[2] = {row2, 64 * e2};
         const cuuint64_t d_k[3] = {64, (cuuint64_t)T, (cuuint64_t)BH};
         const cuuint64_t d_r[3] = {64, (cuuint64_t)T, (cuuint64_t)H}, s_r[2] = {(cuuint64_t)H * 64 * e2, 64 * e2};
-        const cuuint64_t d_qv[3] = {64, (cuuint64_t)L * B, (cuuint64_t)H};
         if (!bg_map(&pmn, 3, pb, d_mat, s_mat, box_mn) || !bg_map(&damn, 3, dab, d_mat, s_mat, box_mn) ||
             !bg_map(&dak, 3, dab, d_mat, s_mat, box_k) || !bg_map(&dbk, 4, dbb, d_db4, s_db4, box_k4) ||
-            !bg_map(&dbmn, 3, dbb, d_db3, s_db3, box_mn) || !bg_map(&mdo, 3, dout, d_q, s_q, box_mn) ||
+            !bg_map(&dbmn, 4, dbb, d_db4, s_db4, box_mn4) || !bg_map(&mdo, 3, dout, d_q, s_q, box_mn) ||
             !bg_map(&mqu, 3, qu, d_q, s_q, box_mn) || !bg_map(&mk, 3, k, d_k, s_q, box_mn) ||
-            !bg_map(&mr, 3, r, d_r, s_r, box_mn) || !bg_map(&mqv, 3, qv, d_qv, s_r, box_mn))
+            !bg_map(&mr, 3, r, d_r, s_r, box_mn) || !bg_map(&mqv, 3, qv, d_q, s_q, box_mn))
             return TXL_ERR_CUDA;
         const BgOperand o3{3, 0}, o3h{3, 1}, o4{4, 0};
         auto run = [&](const CUtensorMap &a, const BgOperand &ao, const CUtensorMap &b, const BgOperand &bo, int a_mn,
-                       long K, int M, int nz, void *outp, long ostride, int ofp32) {
+                       long K, int M, int nz, void *outp, long ostride, int ofp32, int oadd = 0) {
             BgParams g{};
             g.a[0] = ao;
             g.b[0] = bo;
@@ -949,6 +971,7 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
             g.out = outp;
             g.ostride = ostride;
             g.ofp32 = ofp32;
+            g.oadd = oadd;
             return launch_bwd_gemm(&a, &b, g, s);
         };
         const long ld64 = BH * 64;
@@ -956,8 +979,12 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
             (e = run(damn, o3, mqu, o3, 1, L, (int)T, (int)BH, dk, ld64, 0)) != cudaSuccess ||
             (e = run(dak, o3, mk, o3, 0, T, L, (int)BH, dqc, ld64, 1)) != cudaSuccess ||
             (e = run(dbk, o4, mr, o3h, 0, T, L, (int)BH, dqp, ld64, 1)) != cudaSuccess ||
-            (e = run(dbmn, o3, mqv, o3, 1, (long)L * B, (int)T, H, dr, (long)H * 64, 0)) != cudaSuccess)
+            (e = cudaMemsetAsync(dracc, 0, (size_t)T * H * 64 * 4, s)) != cudaSuccess ||
+            (e = run(dbmn, o4, mqv, o3, 1, L, (int)T, (int)BH, dracc, (long)H * 64, 1, 1)) != cudaSuccess)
             goto cuda_fail;
+        // dr (bf16) from its fp32 batch sum
+        bwd_round_kernel<<<grid_for(T * H * 64 / 4, 256), 256, 0, s>>>(dracc, (E *)dr, T * H * 64 / 4);
+        if (!chk()) goto cuda_fail;
     }
     // dq and the bias gradients in one pass over the two fp32 halves of dq
     if ((e = launch_sum_bias<E>(dqc, dqp, (E *)dq, du, dw, (long)L * B, H * D, s)) != cudaSuccess) goto cuda_fail;
@@ -1085,8 +1112,10 @@ txl_status txl_rel_attn_bwd(const void *q, const void *k, const void *v, const v
     if (dtype == TXL_F32)
         return run_bwd<float>(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr, du,
                               dw, wsb, lay, s, false);
-    const void *al[] = {q, k, v, r, dout, uu, ww};
-    if (fused_ok(d_head, al, 7))
+    // the tensor-core route reads its operands by TMA and writes dk, dv, dr
+    // with 16-byte stores: every one of them 16-byte aligned
+    const void *al[] = {q, k, v, r, dout, uu, ww, dk, dv, dr};
+    if (fused_ok(d_head, al, 10))
         return run_bwd_fused(q, k, v, r, uu, ww, dout, out, lse, batch, mem_len, seg_len, heads, d_head, dq, dk, dv,
                              dr, du, dw, wsb, layout_fused(batch, heads, d_head, seg_len, mem_len), s);
     return run_bwd<__nv_bfloat16>(q, k, v, r, uu, ww, dout, batch, mem_len, seg_len, heads, d_head, dq, dk, dv, dr,

@@ -69,15 +69,20 @@ __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { retu
 // TMEM: two 256-column accumulators (tile i's epilogue overlaps tile i+1).
 constexpr int GM = 128;           // output rows per tile (TMEM lanes)
 constexpr int GK = 64;            // K elements per stage (one swizzled row)
-constexpr int GST = 4;            // pipeline stages
 constexpr int GNT = 256;          // threads
-constexpr int GBN = 256;          // widest output tile
 constexpr int GLOADERS = 96;      // cp.async loader threads (warps 0, 2, 3)
 constexpr uint64_t GWAIT_NS = 2000000000ull;   // 2 s per wait, then give up
 
+// Two shapes of the kernel: TMA operands with 256-wide tiles and four
+// stages, one CTA per SM; cp.async operands (issue-bound loaders) with
+// 128-wide tiles and two stages, two CTAs per SM so that one CTA's loaders
+// run while the other's wait.
+template <int BN_, int ST_>
 struct GemmSmem {
+    static constexpr int GBN = BN_;                           // widest output tile
+    static constexpr int GST = ST_;                           // pipeline stages
     static constexpr uint32_t ASZ = GM * 128;                 // one stage of x: 16 KB
-    static constexpr uint32_t BSZ = GBN * 128;                // one stage of W: up to 32 KB
+    static constexpr uint32_t BSZ = GBN * 128;                // one stage of W
     static constexpr uint32_t A = 0;
     static constexpr uint32_t B = A + GST * ASZ;
     static constexpr uint32_t OST = B + GST * BSZ;            // 4 epilogue warps x 2 x 4 KB staging
@@ -88,6 +93,9 @@ struct GemmSmem {
     static constexpr uint32_t MISC = BARS + NBAR * 8;          // tmem holder, abort flag
     static constexpr uint32_t TOTAL = MISC + 16 + 1024;        // + alignment of the base to 1024
 };
+using SmemTma = GemmSmem<256, 4>;
+using SmemCpa = GemmSmem<128, 2>;
+static_assert(SmemTma::TOTAL <= 232448 && 2 * (SmemCpa::TOTAL + 1024) <= 233472, "shared memory");
 
 struct GemmParams {
     const __nv_bfloat16 *x, *w;
@@ -108,12 +116,12 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <bool kTmaIn>
-__global__ void __launch_bounds__(GNT, 1)
+template <bool kTmaIn, typename S, int kMinBlocks>
+__global__ void __launch_bounds__(GNT, kMinBlocks)
 project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_o, const GemmParams p)
 {
-    using S = GemmSmem;
+    constexpr int GST = S::GST, GBN = S::GBN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -139,7 +147,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     };
 
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), 512);
+        tmem_alloc(smem_u32(tmem_holder), 2 * GBN);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -180,7 +188,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 // the accumulator was last read by the epilogue of tile lt-2
                 if (lt >= 2 && !wait(S::AEMPTY + buf, ((lt >> 1) - 1) & 1)) break;
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)buf * 256u;
+                const uint32_t acc = tmem + (uint32_t)(buf * GBN);
                 for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                     const int s = it % GST;
                     if (!wait(S::FULL + s, (it / GST) & 1)) {
@@ -293,7 +301,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
             if (!wait(S::AFULL + buf, (lt >> 1) & 1)) break;
             tc_fence_after();
-            const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * 256u;
+            const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * GBN);
             for (int c = 0; c < nch; ++c) {
                 float v[64];
                 tmem_ld32(tacc + 64u * c, *reinterpret_cast<float(*)[32]>(v));
@@ -349,7 +357,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 2 * GBN);
     }
 }
 
@@ -421,23 +429,24 @@ bool gmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, co
 
 bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
-template <bool kTmaIn>
+template <bool kTmaIn, typename S, int kMinBlocks>
 cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mo, const GemmParams &p,
                           cudaStream_t s)
 {
-    auto kern = project_gemm_kernel<kTmaIn>;
+    auto kern = project_gemm_kernel<kTmaIn, S, kMinBlocks>;
     static std::atomic<uint64_t> opted{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(opted.load(std::memory_order_relaxed) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GemmSmem::TOTAL);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::TOTAL);
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_relaxed);
     }
-    const int grid = p.tiles < device_sm_count() ? p.tiles : device_sm_count();
-    kern<<<(unsigned)grid, GNT, GemmSmem::TOTAL, s>>>(mx, mw, mo, p);
+    const long slots = (long)kMinBlocks * device_sm_count();
+    const int grid = p.tiles < slots ? p.tiles : (int)slots;
+    kern<<<(unsigned)grid, GNT, S::TOTAL, s>>>(mx, mw, mo, p);
     return cudaGetLastError();
 }
 
@@ -455,15 +464,16 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
     p.d_head = d_head;
     p.d_pad = d_pad;
     p.n_out = heads * d_pad;
-    p.bn = p.n_out >= GBN ? GBN : (p.n_out + 15) / 16 * 16;
+    // TMA addresses rows whose pitch is a multiple of 16 bytes; a W box holds
+    // whole heads of d_pad rows
+    const int bn_max = d_in % 8 == 0 && al(x, 16) && al(w, 16) ? SmemTma::GBN : SmemCpa::GBN;
+    p.bn = p.n_out >= bn_max ? bn_max : (p.n_out + 15) / 16 * 16;
     p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
     const long tiles = (long)((rows + GM - 1) / GM) * p.tiles_n;
     if (tiles > INT32_MAX) return cudaErrorNotSupported;
     p.tiles = (int)tiles;
     p.ksteps = (d_in + GK - 1) / GK;
-    // TMA addresses rows whose pitch is a multiple of 16 bytes; a W box holds
-    // whole heads of d_pad rows
-    const bool tma_in = d_in % 8 == 0 && al(x, 16) && al(w, 16) && p.bn % d_pad == 0 && d_pad <= 256;
+    const bool tma_in = bn_max == SmemTma::GBN && p.bn % d_pad == 0 && d_pad <= 256;
     p.tma_out = al(out, 16) && (p.n_out * 2) % 16 == 0;
     CUtensorMap mx{}, mw{}, mo{};
     if (tma_in) {
@@ -479,7 +489,15 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
         const cuuint32_t bO[2] = {64, 32};
         if (!gmap(&mo, 2, out, dO, sO, bO)) return cudaErrorInvalidValue;
     }
-    return tma_in ? launch_gemm_t<true>(mx, mw, mo, p, s) : launch_gemm_t<false>(mx, mw, mo, p, s);
+    if (!tma_in && p.bn > SmemCpa::GBN) {   // TMA-able rows whose heads do not tile the box: 128-wide tiles
+        p.bn = SmemCpa::GBN;
+        p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
+        const long t2 = (long)((rows + GM - 1) / GM) * p.tiles_n;
+        if (t2 > INT32_MAX) return cudaErrorNotSupported;
+        p.tiles = (int)t2;
+    }
+    return tma_in ? launch_gemm_t<true, SmemTma, 1>(mx, mw, mo, p, s)
+                  : launch_gemm_t<false, SmemCpa, 2>(mx, mw, mo, p, s);
 }
 
 // =========================================================================
