@@ -19,13 +19,14 @@
 //     (rel_attn_bwd_scores_kernel in attn_bf16.cu), which recomputes S and
 //     the band per tile, forms dP = dO V^T in tensor memory and writes P, dA
 //     and dB~ as bf16 matrices (delta = rowsum(dO * O) made in the kernel);
-//     five strided-batched cuBLAS GEMMs give dV, dK, both halves of dQ and
-//     dr (dr summed over the batch by the contraction itself), and one pass
-//     adds the halves of dQ and forms du, dv_bias as its column sums;
+//     five launches of the tcgen05 contraction kernel below give dV, dK,
+//     both halves of dQ and dr (dr per (b, h), summed over the batch by fp32
+//     reductions), and one pass adds the halves of dQ and forms du, dv_bias
+//     as its column sums;
 //   - otherwise (fp32, other head sizes: run_bwd) the materialised form: the
 //     score, P, dP and dA of every (b, h) are written to the caller's
-//     workspace as [L][T] matrices, the eight plain contractions run as
-//     strided-batched cuBLAS GEMMs (bf16 operands and fp32 accumulation on
+//     workspace as [L][T] matrices, the eight plain contractions run on the
+//     batched CUDA-core GEMM below (bf16 operands and fp32 accumulation on
 //     the bf16 path; fp32 throughout on the fp32 path), and the kernels below
 //     do the bias fold, the softmax, its gradient and both shifts, and the
 //     batch / row reductions of dq, du, dv_bias and dr.
