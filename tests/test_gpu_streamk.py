@@ -1,0 +1,89 @@
+"""The stream-K schedule of the bf16 kernel (CUDA, `-m gpu`).
+
+With one query tile per (b, h) (L <= 128) and at least as many (b, h) as
+SMs, the key tiles of all items are cut into equal contiguous ranges, one per
+CTA: items inside a range are computed whole, items cut by a range boundary in
+two parts that a merge launch combines.  Every output row, whole or merged,
+must match the oracle element by element; the log-sum-exp output too.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests.helpers import TOL_BF16, device_layer, oracle_full, record_error, unit_shape
+from transformer_xl_relative_rel_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from transformer_xl_relative_rel_gb300 import _build, abi
+    _build.build()
+    abi.load_library()
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _shapes():
+    """(B, H, D, L, M): B*H at least the SM count and not a multiple of it,
+    so that range boundaries cut items; key tiles per item from 1 to 13."""
+    n = _sms()
+    return [(n + 8, 1, 64, 128, 300),        # 4 tiles per item, a few cut items
+            (n // 2 + 3, 2, 64, 100, 1500),  # 13 tiles per item, ragged query block
+            (n + 1, 1, 64, 1, 127),          # one tile per item: nothing to cut
+            (n + 5, 1, 64, 33, 530),         # ragged keys in the last tile
+            (2 * n - 7, 1, 41, 70, 400),     # head size 41: thread loads
+            (n + 20, 1, 64, 128, 0)]         # no memory
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_streamk_matches_oracle(idx):
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, D, L, M = _shapes()[idx]
+    splits, launches = txl.rel_attn_fwd_plan(B, M, L, H, D, txl.TXL_BF16)
+    assert splits == 2 and launches >= 2            # the schedule's two partial slots and the merge
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), 7000 + idx)
+    dev, host = device_layer(p, torch.bfloat16)
+    out = torch.full_like(dev["q"], float("nan"))
+    txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], dev["u"], dev["w"], mem_len=M, out=out)
+    txl.check()
+    ref = oracle_full(host, M)
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref).max()
+    record_error("streamk", (B, H, D, L, M), err, TOL_BF16)
+    assert np.isfinite(got).all() and err <= TOL_BF16, f"max abs err {err:.3e}"
+
+
+def test_streamk_lse_and_repeatable():
+    """The row log-sum-exp of whole and merged items, and the same bits on
+    a second call."""
+    import oracle
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, D, L, M = _sms() + 9, 1, 64, 96, 700
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), 7100)
+    dev, host = device_layer(p, torch.bfloat16)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    out = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], dev["u"], dev["w"], mem_len=M, lse=lse)
+    again = txl.rel_attn_fwd(dev["q"], dev["k"], dev["v"], dev["r"], dev["u"], dev["w"], mem_len=M)
+    assert torch.equal(out, again)
+    ref_out, ref_lse = oracle.rel_attn(host["q"], host["k"], host["v"], host["r"], host["u"], host["w"],
+                                       mem_len=M, return_lse=True)
+    assert np.abs(out.double().cpu().numpy() - ref_out).max() <= TOL_BF16
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 5e-2
+
+
+def test_streamk_ring():
+    """The schedule with keys and values stored as a ring."""
+    import transformer_xl_relative_rel_gb300 as txl
+    B, H, D, L, M, start = _sms() + 4, 1, 64, 128, 600, 200
+    p = inputs.unit_layer(unit_shape(B, H, D, L, M), 7200)
+    dev, host = device_layer(p, torch.bfloat16)
+    k_ring = torch.roll(dev["k"], shifts=start, dims=0).contiguous()
+    v_ring = torch.roll(dev["v"], shifts=start, dims=0).contiguous()
+    out = txl.rel_attn_fwd_ring(dev["q"], k_ring, v_ring, dev["r"], dev["u"], dev["w"], mem_len=M, kv_start=start)
+    assert np.abs(out.double().cpu().numpy() - oracle_full(host, M)).max() <= TOL_BF16

@@ -94,6 +94,7 @@ struct Params {
     int B, H, D, L, M, T;
     int nqt, splits;
     int items;          // B*H*nqt*splits work items
+    int streamk, sk_nt; // stream-K schedule (splits = 2 partial slots), key tiles per item
     int kv_start;       // K, V rows form a ring: key j at row (kv_start + j) mod T
     int ost;            // 1: output tiles written by TMA store (tensor map tm_o)
     float sl2;          // log2(e) / sqrt(D)
@@ -277,6 +278,7 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
 // sorted list, so that every CTA gets a similar total of key tiles).
 struct Item {
     int bh, b, h, i0, rows_here, split, t0, N, kb0;
+    int whole;          // the item's output is final (else a partial: key split or cut item)
     long head_off;
 };
 
@@ -300,7 +302,38 @@ __device__ __forceinline__ Item make_item(const Params &p, int k)
     // table row of (query i0+ii, key j0+jj) in tile n: kb0 + n*BN + 127 - ii + jj
     it.kb0 = p.L - BM - it.i0 + it.t0 * BN;
     it.head_off = ((long)it.b * p.H + it.h) * p.D;
+    it.whole = p.splits == 1;
     return it;
+}
+
+// Stream-K schedule (one query tile per (b, h), at least as many (b, h) as
+// CTAs): the B*H items' key tiles, numbered item by item, are cut into
+// gridDim.x equal contiguous ranges, one per CTA.  An item inside one range
+// is computed whole; an item cut by a range boundary (at most once, since a
+// range holds at least one item's tiles) is computed in two parts, part 0
+// from its first tile, part 1 to its last, each written as a partial and
+// merged afterwards.  The j-th part or item of this CTA, or -1 past the end.
+__device__ __forceinline__ int streamk_item(const Params &p, int j, Item &it)
+{
+    const long G = gridDim.x, c = blockIdx.x, nt = p.sk_nt;
+    const long tt = (long)p.B * p.H * nt;
+    const long s0 = c * tt / G, s1 = (c + 1) * tt / G;
+    const long k = s0 / nt + j;
+    if (s1 <= s0 || k * nt >= s1) return -1;
+    const long a = (s0 > k * nt ? s0 : k * nt) - k * nt;
+    const long e = (s1 < (k + 1) * nt ? s1 : (k + 1) * nt) - k * nt;
+    it.bh = (int)k;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    it.i0 = 0;
+    it.rows_here = min(BM, p.L);
+    it.t0 = (int)a;
+    it.N = (int)(e - a);
+    it.split = a == 0 ? 0 : 1;
+    it.whole = a == 0 && e == nt;
+    it.kb0 = p.L - BM + it.t0 * BN;
+    it.head_off = ((long)it.b * p.H + it.h) * p.D;
+    return j;
 }
 
 // the j-th item of this CTA, or -1 past the end
@@ -314,6 +347,7 @@ __device__ __forceinline__ int item_of(const Params &p, int j)
 // the first item at position >= j with at least one key tile (-1 if none)
 __device__ __forceinline__ int next_busy(const Params &p, int j, Item &it)
 {
+    if (p.streamk) return streamk_item(p, j, it);
     for (;; ++j) {
         const int k = item_of(p, j);
         if (k < 0) return -1;
@@ -619,9 +653,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                             break;
                         }
                         tc_fence_after();
-                        if (ost && n == 0 && have_prev) {
+                        // under the stream-K schedule only whole items go
+                        // through the staged tile (tm_o is then the output)
+                        if (ost && n == 0 && have_prev && (prev.whole || !p.streamk)) {
                             tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
-                                         p.splits > 1 ? prev.split * p.B * p.H + prev.bh : prev.bh);
+                                         (p.splits > 1 && !p.streamk) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                             bulk_commit();
                             in_flight = true;
                         }
@@ -636,14 +672,14 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     prev = it;
                     have_prev = true;
                 }
-                if (ok && ost && have_prev) {
+                if (ok && ost && have_prev && (prev.whole || !p.streamk)) {
                     if (in_flight) {
                         bulk_wait_read();
                         mbar_arrive(bar(S::B_OFR));
                     }
                     if (wait_or_abort(bar(S::B_OST), 0, abort)) {
                         tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
-                                     p.splits > 1 ? prev.split * p.B * p.H + prev.bh : prev.bh);
+                                     (p.splits > 1 && !p.streamk) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                         bulk_commit();
                     }
                 }
@@ -796,7 +832,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         // an item's output: O / l for this thread's half of the columns
         struct Done {
             long head_off;
-            int i0, rows_here, bh, split;
+            int i0, rows_here, bh, split, whole;
             float m, l;
         };
         int n_out = 0;                             // items stored through the output buffer
@@ -811,11 +847,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int d0 = DH * half;
             const int i = dn.i0 + ii;
-            if (p.lse && p.splits == 1 && half == 0 && ii < dn.rows_here)
+            if (p.lse && dn.whole && half == 0 && ii < dn.rows_here)
                 p.lse[(long)dn.bh * p.L + i] = l > 0.f ? (dn.m + log2f(l)) * LN2 : -INFINITY;
-            if (p.splits > 1 && half == 0 && ii < dn.rows_here)   // m is in log2 units of the scaled logits
+            if (!dn.whole && half == 0 && ii < dn.rows_here)   // m is in log2 units of the scaled logits
                 p.part_lse[((long)dn.split * p.B * p.H + dn.bh) * p.L + i] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
-            if (kTma && p.ost) {
+            if (kTma && p.ost && (dn.whole || !p.streamk)) {
                 // the 128 x 64 tile (the output, or this split's partial)
                 // goes through shared memory (the tensor map's swizzled
                 // layout) and out by one TMA store, issued by the P.V thread;
@@ -837,7 +873,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 return true;
             }
             if (ii >= dn.rows_here) return true;
-            if (p.splits == 1) {
+            if (dn.whole) {
                 __nv_bfloat16 *op = p.out + (long)i * qkv_row + dn.head_off + d0;
                 if ((p.D & 7) == 0) {
 #pragma unroll
@@ -874,6 +910,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         };
         // items without key tiles (empty key splits) only get neutral partials
         auto neutral = [&](int jfrom, int jto) {
+            if (p.streamk) return;                 // every part of the stream-K schedule has key tiles
             for (int q = jfrom; q < jto; ++q) {
                 const int k = item_of(p, q);
                 if (k < 0) break;
@@ -998,6 +1035,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             prev.rows_here = it.rows_here;
             prev.bh = it.bh;
             prev.split = it.split;
+            prev.whole = it.whole;
             prev.m = m_used;
             prev.l = l_run;
             pending = true;
@@ -1504,7 +1542,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
 __global__ void __launch_bounds__(256)
 rel_attn_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float *__restrict__ part_lse,
                         __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, int splits, int B, int H,
-                        int L, int D, int DP)
+                        int L, int D, int DP, int sk_nt, int sk_grid)
 {
     const int nch = DP / 8;
     const long BH = (long)B * H, BHL = BH * L;
@@ -1513,6 +1551,19 @@ rel_attn_combine_kernel(const __nv_bfloat16 *__restrict__ part_o, const float *_
     const long row = t / nch;
     const int c = (int)(t % nch);
     const int bh = (int)(row / L), i = (int)(row % L);
+    if (sk_grid > 0) {
+        // stream-K schedule: only items cut by a CTA's range boundary have
+        // parts to merge (the attention kernel wrote the others); the item
+        // is cut when its first and last key tiles fall in different ranges
+        const long tt = BH * sk_nt, G = sk_grid;
+        auto cta_of = [&](long x) {
+            long cc = x * G / tt;
+            while (cc + 1 < G && (cc + 1) * tt / G <= x) ++cc;
+            while (cc > 0 && cc * tt / G > x) --cc;
+            return cc;
+        };
+        if (cta_of((long)bh * sk_nt) == cta_of((long)(bh + 1) * sk_nt - 1)) return;
+    }
     const int b = bh / H, h = bh % H;
     float mx = -INFINITY;
     for (int sp = 0; sp < splits; ++sp) mx = fmaxf(mx, part_lse[sp * BHL + row]);
@@ -1691,8 +1742,19 @@ SplitKey g_split_cache[64];
 int g_split_count = 0, g_split_next = 0;
 }  // namespace
 
+// The stream-K schedule applies to one query tile per (b, h) (L <= 128)
+// with at least as many (b, h) as SMs, not a multiple of them: equal
+// contiguous ranges of key tiles per CTA then cut each item at most once.
+bool streamk_ok(const AttnArgs &a, int num_sms)
+{
+    const long bh = (long)a.B * a.H;
+    return a.L <= BM && bh >= num_sms && bh % num_sms != 0 && bh <= INT32_MAX;
+}
+
 int bf16_num_splits(const AttnArgs &a, int num_sms)
 {
+    // stream-K: two partial slots (the parts of cut items)
+    if (streamk_ok(a, num_sms)) return 2;
     {
         std::lock_guard<std::mutex> lock(g_split_mu);
         for (int x = 0; x < g_split_count; ++x) {
@@ -1793,6 +1855,11 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
         p.part_lse = (float *)((char *)scratch + rows * DP * 2);
     }
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
+    // the stream-K schedule where it applies: the two partial slots are then
+    // only the parts of items cut by a CTA's range
+    p.streamk = splits == 2 && streamk_ok(a, device_sm_count());
+    p.sk_nt = (a.M + a.L + BN - 1) / BN;
+    if (p.streamk) p.items = a.B * a.H;   // grid: one CTA per SM (B*H >= SMs)
     p.kv_start = a.kv_start;
     p.roll_src = nullptr;
     p.roll_dst = nullptr;
@@ -1821,10 +1888,10 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
             return cudaErrorInvalidValue;
         // the output (or with key splits, the bf16 partials laid out like it
         // over splits*B*H heads) by TMA store
-        if (splits == 1 && ((uintptr_t)a.out & 15) == 0) {
+        if ((splits == 1 || p.streamk) && ((uintptr_t)a.out & 15) == 0) {
             if (!make_map(&mo, a.out, a.L, rs, bhn, BM)) return cudaErrorInvalidValue;
             p.ost = 1;
-        } else if (splits > 1) {
+        } else if (splits > 1 && !p.streamk) {
             if (!make_map(&mo, p.part_o, a.L, (long)splits * rs, (long)splits * bhn, BM)) return cudaErrorInvalidValue;
             p.ost = 1;
         }
@@ -1843,8 +1910,9 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     if (e == cudaSuccess && splits > 1) {
         const long threads = (long)a.B * a.H * a.L * (DP / 8);
+        const int sk_grid = p.streamk ? (p.items < device_sm_count() ? p.items : device_sm_count()) : 0;
         rel_attn_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-            p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP);
+            p.part_o, p.part_lse, p.out, a.lse, splits, a.B, a.H, a.L, a.D, DP, p.sk_nt, sk_grid);
         e = cudaGetLastError();
     }
     // a rollover the attention launch did not take: its own copy
