@@ -1742,6 +1742,8 @@ SplitKey g_split_cache[64];
 int g_split_count = 0, g_split_next = 0;
 }  // namespace
 
+int bf16_uniform_splits(const AttnArgs &a, int num_sms);
+
 // The stream-K schedule applies to one query tile per (b, h) (L <= 128)
 // with at least as many (b, h) as SMs, not a multiple of them: equal
 // contiguous ranges of key tiles per CTA then cut each item at most once.
@@ -1753,8 +1755,17 @@ bool streamk_ok(const AttnArgs &a, int num_sms)
 
 int bf16_num_splits(const AttnArgs &a, int num_sms)
 {
-    // stream-K: two partial slots (the parts of cut items)
-    if (streamk_ok(a, num_sms)) return 2;
+    const int s = bf16_uniform_splits(a, num_sms);
+    // where the uniform model splits a shape the stream-K schedule can take,
+    // stream-K replaces the split (two partial slots: the parts of cut
+    // items): char_eval 93.3 -> 84.7 us.  Where it keeps a shape whole, so
+    // does this (long_mem_b16: 54.4 us whole, 77.4 us under stream-K, whose
+    // partials and merge cost what a two-way split costs there).
+    return (s > 1 && streamk_ok(a, num_sms)) ? 2 : s;
+}
+
+int bf16_uniform_splits(const AttnArgs &a, int num_sms)
+{
     {
         std::lock_guard<std::mutex> lock(g_split_mu);
         for (int x = 0; x < g_split_count; ++x) {
@@ -1857,7 +1868,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
     // the stream-K schedule where it applies: the two partial slots are then
     // only the parts of items cut by a CTA's range
-    p.streamk = splits == 2 && streamk_ok(a, device_sm_count());
+    p.streamk = splits == 2 && streamk_ok(a, device_sm_count()) && bf16_uniform_splits(a, device_sm_count()) > 1;
     p.sk_nt = (a.M + a.L + BN - 1) / BN;
     if (p.streamk) p.items = a.B * a.H;   // grid: one CTA per SM (B*H >= SMs)
     p.kv_start = a.kv_start;
