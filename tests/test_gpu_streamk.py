@@ -37,7 +37,7 @@ def _candidates():
     return [(n + 8, 1, 64, 128, 3000),       # a full query block
             (n + 8, 1, 64, 64, 3000),        # a ragged query block
             (n + 18, 1, 64, 33, 2600),       # ragged keys in the last tile
-            (n + 9, 1, 41, 100, 3000),       # head size 41: thread loads
+            (n + 9, 1, 56, 100, 3000),       # head size 56: thread loads
             (n + 9, 1, 64, 1, 3000),         # one query per item
             (n + 3, 1, 64, 128, 4000)]
 

@@ -345,9 +345,10 @@ __device__ __forceinline__ int item_of(const Params &p, int j)
 }
 
 // the first item at position >= j with at least one key tile (-1 if none)
+template <bool kSK>
 __device__ __forceinline__ int next_busy(const Params &p, int j, Item &it)
 {
-    if (p.streamk) return streamk_item(p, j, it);
+    if (kSK) return streamk_item(p, j, it);
     for (;; ++j) {
         const int k = item_of(p, j);
         if (k < 0) return -1;
@@ -356,7 +357,7 @@ __device__ __forceinline__ int next_busy(const Params &p, int j, Item &it)
     }
 }
 
-template <int DP, bool kTma>
+template <int DP, bool kTma, bool kSK>
 __global__ void __launch_bounds__(NT, 1)
 rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
@@ -475,7 +476,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 return true;
             };
             Item it;
-            int j = next_busy(p, 0, it);
+            int j = next_busy<kSK>(p, 0, it);
             if (j >= 0) load_q(it);
             int g = 0, cg = 0, ni = 0;               // key tiles, table chunks, items so far
             bool ok = true;
@@ -536,7 +537,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 if (!ok) break;
                 // the next item's q rows, once this item's have been converted
                 Item nx;
-                const int jn = next_busy(p, j + 1, nx);
+                const int jn = next_busy<kSK>(p, j + 1, nx);
                 if (jn >= 0) {
                     if (!wwait(S::B_QRF, ni & 1)) break;
                     load_q(nx);
@@ -563,7 +564,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 Item it;
                 int g = 0, cg = 0, ni = 0;
                 bool ok = true;
-                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it), ++ni) {
+                for (int j = next_busy<kSK>(p, 0, it); ok && j >= 0; j = next_busy<kSK>(p, j + 1, it), ++ni) {
                     if (!wait_or_abort(bar(S::B_Q), ni & 1, abort)) break;     // q+u, q+v of the item
                     const int c0 = cg;
                     for (int n = 0; n < it.N; ++n, ++g) {
@@ -640,7 +641,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 Item it, prev;
                 int g = 0;
                 bool ok = true, have_prev = false;
-                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it)) {
+                for (int j = next_busy<kSK>(p, 0, it); ok && j >= 0; j = next_busy<kSK>(p, j + 1, it)) {
                     for (int n = 0; n < it.N; ++n, ++g) {
                         const int st = g % NSTAGE;
                         if (in_flight) {
@@ -655,9 +656,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         tc_fence_after();
                         // under the stream-K schedule only whole items go
                         // through the staged tile (tm_o is then the output)
-                        if (ost && n == 0 && have_prev && (prev.whole || !p.streamk)) {
+                        if (ost && n == 0 && have_prev && (prev.whole || !kSK)) {
                             tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
-                                         (p.splits > 1 && !p.streamk) ? prev.split * p.B * p.H + prev.bh : prev.bh);
+                                         (p.splits > 1 && !kSK) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                             bulk_commit();
                             in_flight = true;
                         }
@@ -672,14 +673,14 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     prev = it;
                     have_prev = true;
                 }
-                if (ok && ost && have_prev && (prev.whole || !p.streamk)) {
+                if (ok && ost && have_prev && (prev.whole || !kSK)) {
                     if (in_flight) {
                         bulk_wait_read();
                         mbar_arrive(bar(S::B_OFR));
                     }
                     if (wait_or_abort(bar(S::B_OST), 0, abort)) {
                         tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
-                                     (p.splits > 1 && !p.streamk) ? prev.split * p.B * p.H + prev.bh : prev.bh);
+                                     (p.splits > 1 && !kSK) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                         bulk_commit();
                     }
                 }
@@ -851,7 +852,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 p.lse[(long)dn.bh * p.L + i] = l > 0.f ? (dn.m + log2f(l)) * LN2 : -INFINITY;
             if (!dn.whole && half == 0 && ii < dn.rows_here)   // m is in log2 units of the scaled logits
                 p.part_lse[((long)dn.split * p.B * p.H + dn.bh) * p.L + i] = l > 0.f ? dn.m + log2f(l) : -INFINITY;
-            if (kTma && p.ost && (dn.whole || !p.streamk)) {
+            if (kTma && p.ost && (dn.whole || !kSK)) {
                 // the 128 x 64 tile (the output, or this split's partial)
                 // goes through shared memory (the tensor map's swizzled
                 // layout) and out by one TMA store, issued by the P.V thread;
@@ -910,7 +911,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         };
         // items without key tiles (empty key splits) only get neutral partials
         auto neutral = [&](int jfrom, int jto) {
-            if (p.streamk) return;                 // every part of the stream-K schedule has key tiles
+            if (kSK) return;                 // every part of the stream-K schedule has key tiles
             for (int q = jfrom; q < jto; ++q) {
                 const int k = item_of(p, q);
                 if (k < 0) break;
@@ -926,7 +927,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
         bool ok = true;
         Item it;
-        int j = next_busy(p, 0, it);
+        int j = next_busy<kSK>(p, 0, it);
         if (j >= 0) ok = convert_q(it, 0);
         int g = 0, ni = 0;
         bool pending = false;                      // the previous item's output is still in O
@@ -936,7 +937,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int i = it.i0 + ii;
             const bool row_valid = ii < it.rows_here;
             Item nx;
-            const int jn = next_busy(p, j + 1, nx);
+            const int jn = next_busy<kSK>(p, j + 1, nx);
             float m_used = -INFINITY, l_run = 0.f;     // l_run: this thread's key half only
             for (int n = 0; n < it.N; ++n, ++g) {
                 const int j0 = (it.t0 + n) * BN + HN * half;     // first key of this thread's half
@@ -1170,7 +1171,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 return true;
             };
             Item it;
-            int j = next_busy(p, 0, it);
+            int j = next_busy<false>(p, 0, it);
             if (j >= 0) load_q(it, 0);
             int g = 0, cg = 0, ni = 0;
             bool ok = true;
@@ -1198,7 +1199,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 }
                 if (!ok) break;
                 Item nx;
-                const int jn = next_busy(p, j + 1, nx);
+                const int jn = next_busy<false>(p, j + 1, nx);
                 if (jn >= 0) {
                     if (!wwait(S::B_QRF, ni & 1)) break;
                     load_q(nx, ni + 1);
@@ -1221,7 +1222,7 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
                 Item it;
                 int g = 0, cg = 0, ni = 0;
                 bool ok = true;
-                for (int j = next_busy(p, 0, it); ok && j >= 0; j = next_busy(p, j + 1, it), ++ni) {
+                for (int j = next_busy<false>(p, 0, it); ok && j >= 0; j = next_busy<false>(p, j + 1, it), ++ni) {
                     if (!wait_or_abort(bar(S::B_Q), ni & 1, abort)) break;
                     const uint64_t d_do = d_do0 + (uint64_t)(ni & 1) * QT16;
                     const int c0 = cg;
@@ -1333,14 +1334,14 @@ rel_attn_bwd_scores_kernel(const __grid_constant__ CUtensorMap tm_k, const __gri
         const long rowpitch = p.TP;
         bool ok = true;
         Item it;
-        int j = next_busy(p, 0, it);
+        int j = next_busy<false>(p, 0, it);
         if (j >= 0) ok = convert_q(it, 0);
         int g = 0, ni = 0;
         while (ok && j >= 0) {
             const int i = it.i0 + ii;
             const bool row_valid = ii < it.rows_here;
             Item nx;
-            const int jn = next_busy(p, j + 1, nx);
+            const int jn = next_busy<false>(p, j + 1, nx);
             const long row = (long)it.bh * p.L + i;   // this thread's row of the [B*H][L] matrices
             const float lse = row_valid ? p.lse[row] * LOG2E : 0.f;   // log2 units of the scaled score
             // the table-frame matrix is head-major, [H][L][B][TP]: row (i, b) of
@@ -1676,13 +1677,13 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
     return true;
 }
 
-template <int DP, bool kTma>
+template <int DP, bool kTma, bool kSK>
 cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                      const CUtensorMap &mr, const CUtensorMap &mq, const CUtensorMap &mk8,
                      const CUtensorMap &mv8, const CUtensorMap &mo, cudaStream_t s)
 {
     const uint32_t smem = Smem<DP>::TOTAL;
-    auto kern = rel_attn_bf16_kernel<DP, kTma>;
+    auto kern = rel_attn_bf16_kernel<DP, kTma, kSK>;
     // the shared-memory opt-in, once per device for this variant
     static std::atomic<uint64_t> opted{0};
     int dev = 0;
@@ -1750,7 +1751,7 @@ int bf16_uniform_splits(const AttnArgs &a, int num_sms);
 bool streamk_ok(const AttnArgs &a, int num_sms)
 {
     const long bh = (long)a.B * a.H;
-    return a.L <= BM && bh >= num_sms && bh % num_sms != 0 && bh <= INT32_MAX;
+    return a.L <= BM && (a.D + 15) / 16 * 16 == 64 && bh >= num_sms && bh % num_sms != 0 && bh <= INT32_MAX;
 }
 
 int bf16_num_splits(const AttnArgs &a, int num_sms)
@@ -1914,10 +1915,17 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     cudaError_t e;
     switch (DP) {
-    case 16: e = tma ? launch_t<16, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<16, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
-    case 32: e = tma ? launch_t<32, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<32, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
-    case 48: e = tma ? launch_t<48, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<48, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
-    default: e = tma ? launch_t<64, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<64, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 16: e = tma ? launch_t<16, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<16, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 32: e = tma ? launch_t<32, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<32, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 48: e = tma ? launch_t<48, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<48, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    default:
+        if (p.streamk)
+            e = tma ? launch_t<64, true, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s)
+                    : launch_t<64, false, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s);
+        else
+            e = tma ? launch_t<64, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s)
+                    : launch_t<64, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s);
+        break;
     }
     if (e == cudaSuccess && splits > 1) {
         const long threads = (long)a.B * a.H * a.L * (DP / 8);
