@@ -30,7 +30,7 @@
 // costs twice the position term's pairs: a window of two 128-row chunks keeps
 // each 16-row group's 80 columns contiguous for the load's fixed half-split
 // offset.  The reference max is raised (and O in TMEM rescaled) on an item's
-// first tile, on diagonal tiles and when a row's sum passes 2^12.  The scale
+// first tile and when a row's sum passes 2^12.  The scale
 // log2(e)/sqrt(D) is folded into q+u and q+v before rounding.  Every mbarrier
 // wait is bounded; on expiry the CTA records an error word (read by
 // txl_check) and every role winds down.
@@ -963,20 +963,22 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 uint32_t hb[40];
 #pragma unroll
                 for (int y = 0; y < 40; ++y) hb[y] = pack_f16_sat(a[2 * y], a[2 * y + 1]);
-                // exponentials against the running reference max.  Off the
-                // diagonal, once the rows have a finite reference, the tile
-                // runs straight through: shift, add and exponentials of the
-                // two 32-key pieces.  The row's sum over all 128 keys is then
-                // checked (the row's two lanes see the same sum and the whole
-                // warp takes one branch): past SUM_LIMIT, and on the first
-                // tile of an item or a diagonal tile, the reference is first
-                // raised to the row's max.
+                // exponentials against the running reference max.  Once the
+                // rows have a finite reference the tile runs straight
+                // through: shift, add (on diagonal tiles the causal mask) and
+                // exponentials of the two 32-key pieces.  The row's sum over
+                // all 128 keys is then checked (the row's two lanes see the
+                // same sum and the whole warp takes one branch): past
+                // SUM_LIMIT, and on the first tile of an item, the reference
+                // is first raised to the row's max.
                 float pk[32], psum = 0.f, alpha = 1.f;
                 bool raise = false, find_max;
-                if (!diag && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
+                if (!__any_sync(0xffffffffu, m_used == -INFINITY)) {
                     band_half(hb, x);
+                    if (diag) mask_block(x, 0, lim);
                     const float s0 = expo(x, m_used, pk);
                     band_half(hb + 16, x + 32);
+                    if (diag) mask_block(x + 32, 32, lim);
                     const float s1 = expo(x + 32, m_used, pk + 16);
                     psum = s0 + s1;
                     find_max = __any_sync(0xffffffffu, !(psum + partner(psum) <= SUM_LIMIT));
