@@ -201,3 +201,47 @@ def test_near_limits_sampled_rows(B, H, D, L, M, dtype):
     err = np.abs(gather_rows(out, rows) - ref).max()
     record_error("near_limits", (B, H, D, L, M), err, TOL_BF16 if dtype == torch.bfloat16 else TOL_F32)
     assert err <= (TOL_BF16 if dtype == torch.bfloat16 else TOL_F32), f"max abs err {err:.3e}"
+
+
+# ------------------------------------------------------------------ diagonal tiles
+def _memory_below_segment(shape, seed):
+    """Inputs whose memory keys point away from every query (logits near -8
+    in the kernel's log2 units) and whose segment keys point along it (logits
+    near +4): each row meets its first large logits on its diagonal tile,
+    about 2^12 above the reference max its earlier tiles set.  The
+    dominant logits stay small, so the bf16 roundings of the inputs keep the
+    usual error scale."""
+    L, B, H, D, M = shape.seg_len, shape.batch, shape.heads, shape.d_head, shape.mem_len
+    T = M + L
+    g = inputs.rng(seed)
+    e = g.standard_normal((B, H, D)).astype(np.float32)
+    e /= np.linalg.norm(e, axis=-1, keepdims=True)
+    p = inputs.unit_layer(shape, seed)
+    p["q"] = (4.0 * e[None] + 0.1 * g.standard_normal((L, B, H, D))).astype(np.float32)
+    sign = np.where(np.arange(T) < M, -11.0, 5.5).astype(np.float32)[:, None, None, None]
+    p["k"] = (sign * e[None] + 0.1 * g.standard_normal((T, B, H, D))).astype(np.float32)
+    p["u"] = (0.1 * g.standard_normal((H, D))).astype(np.float32)
+    p["w"] = (0.1 * g.standard_normal((H, D))).astype(np.float32)
+    return p
+
+
+@pytest.mark.parametrize("B,H,D,L,M", [
+    (1, 2, 64, 128, 512),      # one query block, four memory tiles before its diagonal
+    (2, 1, 64, 100, 300),      # ragged query block and key tail
+    (1, 2, 64, 128, 2048),     # long memory: the planner splits the keys
+])
+def test_bf16_diagonal_raises_the_row_max(B, H, D, L, M):
+    """Diagonal tiles run the straight exponential path once a row has a
+    finite reference max; when their logits lie far above it the row-sum
+    check must raise the reference (and rescale the accumulated output)."""
+    shape = unit_shape(B, H, D, L, M)
+    p = _memory_below_segment(shape, 4242 + L + M)
+    dev, host = device_layer(p, torch.bfloat16)
+    out = run_library(dev, M)
+    torch.cuda.synchronize()
+    ref = oracle_full(host, M)
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref).max()
+    record_error("diag_raise_bf16", (B, H, D, L, M), err, TOL_BF16)
+    assert np.isfinite(got).all()
+    assert err <= TOL_BF16, f"max abs err {err:.3e} for B{B} H{H} D{D} L{L} M{M}"
