@@ -312,11 +312,13 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
                 const int col0 = n0 + 64 * c;
                 // padding columns come out exactly zero (whatever x holds)
-                int d = col0 % p.d_pad;
+                if (p.d_head != p.d_pad) {
+                    int d = col0 % p.d_pad;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    if (d >= p.d_head) v[j] = 0.f;
-                    if (++d == p.d_pad) d = 0;
+                    for (int j = 0; j < 64; ++j) {
+                        if (d >= p.d_head) v[j] = 0.f;
+                        if (++d == p.d_pad) d = 0;
+                    }
                 }
                 if (p.tma_out) {
                     if (col0 >= p.n_out) continue;
