@@ -2,7 +2,7 @@
 
 One step = one pass of the hot path over one batch of the workload: every
 segment of the workload's chain, and in each segment every layer's q, k, v
-projections of [memory; h] (txl_project_heads), its relative attention
+projections of [memory; h] (txl_project_qkv), its relative attention
 (txl_rel_attn_fwd) and its memory rollover (txl_mem_update), the rollover
 feeding the next segment's keys and values and each layer's output feeding
 the next layer (``--attn-only``: the attention and rollover alone on fixed
@@ -365,11 +365,28 @@ class AttnChain:
     rollover_in_attention = False
 
 
+def qkv_launches(w: Workload, dp: int, ring: bool) -> int:
+    """Launches of a layer's q, k, v projections under txl_project_qkv's
+    rule (include/txl.h): bf16 TMA-addressable operands put k and v in one
+    launch, q joins it when its first row (mem_len x batch) starts a
+    128-row block; the ring variant projects q on its own."""
+    s = w.shape
+    n_out = s.heads * dp
+    bn = 256 if n_out >= 256 else (n_out + 15) // 16 * 16
+    fused = (w.dtype == "bf16" and s.d_model % 8 == 0 and (n_out * 2) % 16 == 0 and dp <= 256
+             and bn % dp == 0)
+    if not fused:
+        return 3
+    if ring:
+        return 2
+    return 1 if (s.mem_len * s.batch) % 128 == 0 else 2
+
+
 class LayerChain:
     """The recurrence of the pages, every step a library call.  Per segment
     and layer n (Transformer-XL Sections 3.2-3.3): q = h W_q^T on the
     segment's states, k = h~ W_kE^T and v = h~ W_v^T on the extended context
-    h~ = [memory; h] (txl_project_heads), the relative attention over h~,
+    h~ = [memory; h] (txl_project_qkv), the relative attention over h~,
     and the rollover that keeps the newest M rows of h~ as the next
     segment's memory (txl_mem_update), so each segment's keys and values
     are projected from the memory the previous segment left.  Layer n+1's
@@ -419,6 +436,7 @@ class LayerChain:
                 v=torch.empty(T, B, H, dp, dtype=dt, device=device),
                 out=torch.empty(L, B, H, dp, dtype=dt, device=device)))
         self.cur = 0
+        self.proj_launches = qkv_launches(w, dp, ring)
         torch.cuda.synchronize()
 
     # every other step starts from the other buffer of each ping-pong pair
@@ -433,7 +451,8 @@ class LayerChain:
                 "rollover in the attention call (txl_rel_attn_fwd_mem)" if self.fused else
                 "rollover of the extended context (txl_mem_update)")
         return ("per segment: layer 0's input states copied in (txl_ring_append); per layer: q, k, v "
-                "projections of [memory; h] (txl_project_heads, tcgen05), attention, " + roll +
+                "projections of [memory; h] (txl_project_qkv, tcgen05: x read once for the three), "
+                "attention, " + roll +
                 "; layer n's output is layer n+1's input")
 
     def _ring_in(self, lay, rows) -> int:
@@ -466,11 +485,13 @@ class LayerChain:
             launches += 1
         for n, lay in enumerate(self.layers):
             ext = lay["ext"][0 if self.ring else cur]
-            h = lay["hin"] if self.ring else ext[M:]
-            txl.project_heads(h, lay["wq"], H, D, dp, out=lay["q"])
-            txl.project_heads(ext, lay["wk"], H, D, dp, out=lay["k"])
-            txl.project_heads(ext, lay["wv"], H, D, dp, out=lay["v"])
-            launches += 3
+            if self.ring:   # the segment's states are not the ring's last rows
+                txl.project_heads(lay["hin"], lay["wq"], H, D, dp, out=lay["q"])
+                txl.project_qkv(ext, None, lay["wk"], lay["wv"], H, D, dp, k=lay["k"], v=lay["v"])
+            else:
+                txl.project_qkv(ext, lay["wq"], lay["wk"], lay["wv"], H, D, dp, q_from=M,
+                                q=lay["q"], k=lay["k"], v=lay["v"])
+            launches += self.proj_launches
             nxt = self.layers[n + 1] if n + 1 < nl else None
             out = lay["out"]
             if nxt is not None and dp == D and not self.ring:

@@ -216,6 +216,27 @@ txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, 
                              int d_head, int d_pad, txl_dtype dtype, void *stream);
 
 /*
+ * txl_project_qkv -- a layer's three projections of Section 3.3's procedure
+ * from one extended context h~ = [memory; h] (x, [rows][d_in], rows =
+ * positions x batch of a T-major buffer):
+ *     k = x W_k^T and v = x W_v^T over all rows, and
+ *     q = x[q_row0 ..] W_q^T over the last rows - q_row0 rows (the segment's
+ *         own positions h: q_row0 = mem_len x batch),
+ * each as txl_project_heads writes it ([..][heads][d_pad], padding zero).
+ * w_q and q are both given or both NULL (then only k and v).  bf16 with
+ * d_in a multiple of 8, every pointer 16-byte aligned, heads*d_pad*2 a
+ * multiple of 16 and d_pad dividing 256: k and v come from one launch of
+ * the projection GEMM that reads x once, and q joins that launch when
+ * q_row0 is a multiple of 128 (else it is a launch of its own); other shapes
+ * are computed as by three txl_project_heads calls.
+ * Outputs must not overlap x, the weights or one another; 0 <= q_row0 <=
+ * rows.  Results equal the separate txl_project_heads calls bit for bit.
+ */
+txl_status txl_project_qkv(const void *x, int rows, int d_in, const void *w_q, const void *w_k, const void *w_v,
+                           void *q, void *k, void *v, int q_row0, int heads, int d_head, int d_pad, txl_dtype dtype,
+                           void *stream);
+
+/*
  * txl_rel_table -- Appendix B's reversed projected table of one layer:
  * out[t][h][d] = sum_c R[klen-1-t][c] * W_kR[h*d_head + d][c] for t < klen,
  * R[p][2c] = sin(p * 10000^(-2c/d_model)), R[p][2c+1] = cos(the same angle)

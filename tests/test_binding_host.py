@@ -96,3 +96,27 @@ def test_noalloc_binding_checks_like_the_default_entry():
     r_strided = torch.zeros(T, D, H, dtype=r.dtype).transpose(1, 2)     # right shape, not contiguous
     with pytest.raises(ValueError, match=ON_DEVICE):
         txl.rel_attn_fwd_noalloc(q, k, v, r_strided, u, w, mem_len=M, out=out)
+
+
+def test_project_qkv_checks():
+    d_in, heads, d_head, d_pad = 32, 2, 16, 16
+    x = torch.zeros(T, B, d_in, dtype=torch.bfloat16)
+    w = [torch.zeros(heads * d_head, d_in, dtype=torch.bfloat16) for _ in range(3)]
+    with pytest.raises(ValueError, match="q_from"):
+        txl.project_qkv(x, w[0], w[1], w[2], heads, d_head, d_pad, q_from=T + 1)
+    with pytest.raises(ValueError, match="w_k must be"):
+        txl.project_qkv(x, w[0], w[1][:, :-1], w[2], heads, d_head, d_pad, q_from=M)   # contraction length
+    with pytest.raises(ValueError, match="w_v is required"):
+        txl.project_qkv(x, w[0], w[1], None, heads, d_head, d_pad, q_from=M)
+    with pytest.raises(ValueError, match="w_q must be"):
+        txl.project_qkv(x, w[0].float(), w[1], w[2], heads, d_head, d_pad, q_from=M)  # weight dtype
+    with pytest.raises(ValueError, match="q is given without w_q"):
+        txl.project_qkv(x, None, w[1], w[2], heads, d_head, d_pad, q=torch.zeros(L, B, heads, d_pad))
+    with pytest.raises(ValueError, match="q must be"):                                # q spans L rows, not T
+        txl.project_qkv(x, w[0], w[1], w[2], heads, d_head, d_pad, q_from=M,
+                        q=torch.zeros(T, B, heads, d_pad, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="k must be"):                                # padded width
+        txl.project_qkv(x, w[0], w[1], w[2], heads, d_head, d_pad, q_from=M,
+                        k=torch.zeros(T, B, heads, d_pad + 8, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.project_qkv(x, w[0], w[1], w[2], heads, d_head, d_pad, q_from=M)          # host tensors

@@ -6,7 +6,7 @@ is [SG(memory); h], where the memory is the newest M hidden states that layer
 n saw in segment tau.  Section 3.3's procedure projects q from the segment's
 states and k, v from the whole extended context, builds the relative table
 from W_kR and the sinusoid, and attends.  Here every step of that per-layer
-procedure runs in the library (txl_project_heads, txl_rel_table, the
+procedure runs in the library (txl_project_qkv, txl_project_heads, txl_rel_table, the
 attention entry point, txl_mem_update or txl_ring_append); the glue between
 layers, h^n = LayerNorm(a^{n-1} W_o + h^{n-1}), runs in torch and is not
 checked.  Language-model initialisation: hidden states N(0, 1), weights and
@@ -149,9 +149,9 @@ def test_chain_matches_oracle_every_call(name):
             # extended context [SG(memory); h]: the memory rows came from the
             # previous segment's rollover of this layer
             ext[n][M:].copy_(h)
-            q = txl.project_heads(h, lay.wq, H, D, dp)
-            k = txl.project_heads(ext[n], lay.wk, H, D, dp)
-            v = txl.project_heads(ext[n], lay.wv, H, D, dp)
+            # q of the segment's rows M.., k and v of all rows: one call, as
+            # the benchmark's recurrence makes it
+            q, k, v = txl.project_qkv(ext[n], lay.wq, lay.wk, lay.wv, H, D, dp, q_from=M)
             a = attend(q, k, v, tables[n], lay)
             if seg > 0 and M > 0:
                 # keys and values of the rolled memory

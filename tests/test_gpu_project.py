@@ -67,6 +67,68 @@ def test_project_heads_tensor_core(rows, d_in, heads, d_head, d_pad):
     assert torch.equal(y, y2)
 
 
+# the layer's three projections from one extended context [M+L, B, d_in]:
+# the fused launch (x read once; q's rows start a 128-row block), k and v
+# fused with q on its own (q's first row inside a block), and shapes that
+# take one launch per product (cp.async rows, fp32); every case against the
+# oracle and bit for bit against three project_heads calls
+@pytest.mark.parametrize("dtype,T,B,M,d_in,heads,d_head,d_pad", [
+    (torch.bfloat16, 384, 2, 256, 512, 8, 64, 64),    # q from row 512: fused q, k, v
+    (torch.bfloat16, 200, 3, 72, 256, 4, 64, 64),     # q from row 216 (inside a block): k, v fused, q alone
+    (torch.bfloat16, 97, 3, 32, 512, 8, 64, 64),      # ragged last block (291 rows), q from row 96
+    (torch.bfloat16, 160, 2, 64, 1024, 16, 64, 64),   # four column tiles per product
+    (torch.bfloat16, 150, 2, 100, 410, 10, 41, 64),   # cp.async rows: three launches
+    (torch.bfloat16, 64, 2, 0, 128, 2, 48, 48),       # no memory: q over all rows
+    (torch.float32, 40, 2, 24, 64, 2, 16, 16),        # fp32: the CUDA-core kernel three times
+])
+def test_project_qkv(dtype, T, B, M, d_in, heads, d_head, d_pad):
+    import transformer_xl_relative_rel_gb300 as txl
+    g = torch.Generator(device="cuda").manual_seed(T * 31 + d_in)
+    x = torch.randn(T, B, d_in, generator=g, device="cuda").to(dtype)
+    ws = [(0.02 * torch.randn(heads * d_head, d_in, generator=g, device="cuda")).to(dtype) for _ in range(3)]
+    nan = float("nan")
+    q = torch.full((T - M, B, heads, d_pad), nan, dtype=dtype, device="cuda")
+    k = torch.full((T, B, heads, d_pad), nan, dtype=dtype, device="cuda")
+    v = torch.full((T, B, heads, d_pad), nan, dtype=dtype, device="cuda")
+    txl.project_qkv(x, ws[0], ws[1], ws[2], heads, d_head, d_pad, q_from=M, q=q, k=k, v=v)
+    xd = x.double().cpu().numpy().reshape(T * B, d_in)
+    for name, got, xr, w in (("q", q, xd[M * B:], ws[0]), ("k", k, xd, ws[1]), ("v", v, xd, ws[2])):
+        ref = oracle.project_heads(xr, w.double().cpu().numpy(), heads, d_head, d_pad)
+        gn = got.double().cpu().numpy().reshape(ref.shape)
+        assert np.isfinite(gn).all(), name
+        if dtype == torch.bfloat16:
+            assert _bf16_close(gn, ref, d_in).all(), f"{name}: max abs err {np.abs(gn - ref).max():.3e}"
+        else:
+            assert _rel_err(gn, ref) <= 1e-5, name
+        assert (gn[..., d_head:] == 0).all(), name
+    assert torch.equal(q, txl.project_heads(x[M:], ws[0], heads, d_head, d_pad))
+    assert torch.equal(k, txl.project_heads(x, ws[1], heads, d_head, d_pad))
+    assert torch.equal(v, txl.project_heads(x, ws[2], heads, d_head, d_pad))
+    # without q
+    q2, k2, v2 = txl.project_qkv(x, None, ws[1], ws[2], heads, d_head, d_pad)
+    assert q2 is None and torch.equal(k2, k) and torch.equal(v2, v)
+
+
+def test_project_qkv_full_size_sampled_rows():
+    """char-LM training's layer inputs as the recurrence runs them (T = 1536,
+    B = 22, q from the memory's end, row 16,896): one fused launch; sampled
+    rows of each product against the oracle."""
+    import transformer_xl_relative_rel_gb300 as txl
+    T, B, M, dm, H, D = 1536, 22, 768, 512, 8, 64
+    g = torch.Generator(device="cuda").manual_seed(1536)
+    x = torch.randn(T, B, dm, generator=g, device="cuda").bfloat16()
+    ws = [(0.02 * torch.randn(H * D, dm, generator=g, device="cuda")).bfloat16() for _ in range(3)]
+    q, k, v = txl.project_qkv(x, ws[0], ws[1], ws[2], H, D, D, q_from=M)
+    rng = np.random.Generator(np.random.PCG64(2))
+    xf = x.reshape(T * B, dm)
+    for got, lo, w in ((q, M * B, ws[0]), (k, 0, ws[1]), (v, 0, ws[2])):
+        sel = rng.choice(T * B - lo, 128, replace=False)
+        idx = torch.tensor(sel, device="cuda")
+        ref = oracle.project_heads(xf[lo:][idx].double().cpu().numpy(), w.double().cpu().numpy(), H, D)
+        gn = got.reshape(-1, H, D)[idx].double().cpu().numpy()
+        assert _bf16_close(gn, ref, dm).all(), f"max abs err {np.abs(gn - ref).max():.3e}"
+
+
 def test_project_heads_padding_stays_zero_with_inf_inputs():
     """Padding columns are written as zeros, not as products with zero
     weights (an infinite input would make those NaN)."""

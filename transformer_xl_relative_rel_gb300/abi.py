@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
+           "txl_project_qkv", "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
 
 
 class TxlError(RuntimeError):
@@ -68,6 +68,8 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd_padded.restype = i
     lib.txl_project_heads.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
     lib.txl_project_heads.restype = i
+    lib.txl_project_qkv.argtypes = [vp, i, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.txl_project_qkv.restype = i
     lib.txl_rel_table.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     lib.txl_rel_table.restype = i
     lib.txl_rel_attn_bwd_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
@@ -316,6 +318,48 @@ def project_heads(x, w, heads: int, d_head: int, d_pad: int, out=None, stream=No
                                           _dtype_code(x), _stream_ptr(stream))
     _raise(st, "txl_project_heads")
     return out
+
+
+def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: int = 0,
+                q=None, k=None, v=None, stream=None):
+    """A layer's q, k, v projections of one extended context: k = x @ w_k.T
+    and v = x @ w_v.T over all of x's leading positions, q = x[q_from:] @
+    w_q.T (the segment's own positions; ``w_q=None`` skips q).  x: [T, *rest,
+    d_in]; outputs [T or T - q_from, *rest, heads, d_pad], as project_heads
+    writes them.  Returns (q, k, v)."""
+    import torch
+    T = x.shape[0]
+    rest = tuple(x.shape[1:-1])
+    d_in = x.shape[-1]
+    per = 1
+    for n in rest:
+        per *= n
+    if not 0 <= q_from <= T:
+        raise ValueError(f"q_from must lie in [0, {T}]")
+    for name, w in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v)):
+        if w is None and name != "w_q":
+            raise ValueError(f"{name} is required")
+        if w is not None and (tuple(w.shape) != (heads * d_head, d_in) or w.dtype != x.dtype):
+            raise ValueError(f"{name} must be [{heads * d_head}, {d_in}] of x's dtype")
+    if w_q is None and q is not None:
+        raise ValueError("q is given without w_q")
+    shapes = {"q": (T - q_from,) + rest + (heads, d_pad), "k": (T,) + rest + (heads, d_pad),
+              "v": (T,) + rest + (heads, d_pad)}
+    outs = {"q": q, "k": k, "v": v}
+    for name, t in outs.items():
+        if t is not None and (tuple(t.shape) != shapes[name] or t.dtype != x.dtype):
+            raise ValueError(f"{name} must be {list(shapes[name])} of x's dtype")
+    for t in (x, w_q, w_k, w_v, q, k, v):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    for name in ("k", "v") + (("q",) if w_q is not None else ()):
+        if outs[name] is None:
+            outs[name] = torch.empty(*shapes[name], dtype=x.dtype, device=x.device)
+    st = load_library().txl_project_qkv(
+        _ptr(x), T * per, d_in, _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(outs["q"]), _ptr(outs["k"]),
+        _ptr(outs["v"]), q_from * per, heads, d_head, d_pad, _dtype_code(x), _stream_ptr(stream))
+    _raise(st, "txl_project_qkv")
+    return outs["q"], outs["k"], outs["v"]
 
 
 def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: int, out=None, stream=None):

@@ -22,6 +22,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <atomic>
 #include <mutex>
@@ -97,13 +98,47 @@ using SmemTma = GemmSmem<256, 4>;
 using SmemCpa = GemmSmem<128, 2>;
 static_assert(SmemTma::TOTAL <= 232448 && 2 * (SmemCpa::TOTAL + 1024) <= 233472, "shared memory");
 
+// Up to three products of the same x in one launch (q, k, v of a layer):
+// segment s multiplies x by its own W and writes its own output, over the
+// row blocks from seg_fb[s] on (seg_fb non-decreasing), output row = x row -
+// seg_row0[s].  One segment is the plain y = x W^T.
+constexpr int GSEG = 3;
 struct GemmParams {
     const __nv_bfloat16 *x, *w;
     __nv_bfloat16 *out;
     int rows, d_in, heads, d_head, d_pad, n_out;
-    int bn, tiles_n, tiles, ksteps;
+    int bn, tiles_n, tiles, ksteps;   // tiles_n: column tiles of one segment
     int tma_out;
+    int nseg, row_blocks;
+    int seg_fb[GSEG], seg_row0[GSEG];
 };
+struct GemmMaps {
+    CUtensorMap x, w[GSEG], o[GSEG];
+};
+
+// Tile t of the launch: the row blocks fall into bands [seg_fb[b],
+// seg_fb[b+1]) in which segments 0..b are active; within a row block the
+// tiles run over the active segments' column tiles, so neighbouring CTAs
+// read the same x rows.
+struct GTile {
+    int m0, seg, n0;
+};
+__host__ __device__ __forceinline__ GTile gemm_tile(const GemmParams &p, int t)
+{
+#pragma unroll
+    for (int b = 0; b < GSEG; ++b) {   // unrolled: the fields are indexed by constants
+        if (b >= p.nseg) break;
+        const int end = b + 1 < p.nseg ? p.seg_fb[b + 1 < GSEG ? b + 1 : b] : p.row_blocks;
+        const int per = (b + 1) * p.tiles_n;
+        const int cnt = (end - p.seg_fb[b]) * per;
+        if (t < cnt) {
+            const int r = t % per;
+            return {(p.seg_fb[b] + t / per) * GM, r / p.tiles_n, (r % p.tiles_n) * p.bn};
+        }
+        t -= cnt;
+    }
+    return {-1, 0, 0};
+}
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
@@ -118,8 +153,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
 
 template <bool kTmaIn, typename S, int kMinBlocks>
 __global__ void __launch_bounds__(GNT, kMinBlocks)
-project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                    const __grid_constant__ CUtensorMap tm_o, const GemmParams p)
+project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
 {
     constexpr int GST = S::GST, GBN = S::GBN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -163,10 +197,11 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         mbar_init(bar(S::DONE), 1);
         fence_mbar_init();
         if (kTmaIn) {
-            prefetch_tmap(&tm_x);
-            prefetch_tmap(&tm_w);
+            prefetch_tmap(&maps.x);
+            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.w[sg]);
         }
-        if (p.tma_out) prefetch_tmap(&tm_o);
+        if (p.tma_out)
+            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.o[sg]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -217,7 +252,9 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 int it = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
-                    const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+                    const GTile tt = gemm_tile(p, t);
+                    const int m0 = tt.m0, n0 = tt.n0;
+                    const CUtensorMap *mw = &maps.w[tt.seg];
                     for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                         const int s = it % GST;
                         if (it >= GST && !wait(S::EMPTY + s, ((it / GST) - 1) & 1)) {
@@ -225,10 +262,10 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                             break;
                         }
                         mbar_arrive_expect_tx(bar(S::FULL + s), bytes);
-                        tma_load_2d(sbase + S::A + s * S::ASZ, &tm_x, bar(S::FULL + s), ks * GK, m0);
+                        tma_load_2d(sbase + S::A + s * S::ASZ, &maps.x, bar(S::FULL + s), ks * GK, m0);
                         // W viewed as [heads][d_head][d_in]: a box of bn / d_pad heads
                         // of d_pad rows each; rows d_head.. of a head are zero-filled
-                        tma_load_3d(sbase + S::B + s * S::BSZ, &tm_w, bar(S::FULL + s), ks * GK, 0, n0 / p.d_pad);
+                        tma_load_3d(sbase + S::B + s * S::BSZ, mw, bar(S::FULL + s), ks * GK, 0, n0 / p.d_pad);
                     }
                 }
             }
@@ -243,7 +280,8 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
-                const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+                const GTile tt = gemm_tile(p, t);
+                const int m0 = tt.m0, n0 = tt.n0;
                 __syncwarp();                          // the previous tile's stages have read the table
                 for (int j = lane; wi + 3 * j < p.bn; j += 32) {
                     const int col = n0 + wi + 3 * j, h = col / p.d_pad, d = col - h * p.d_pad;
@@ -298,7 +336,11 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         int lt = 0, nst = 0;                         // tiles, chunks stored (two staging buffers)
         for (int t = blockIdx.x; t < p.tiles; t += G, ++lt) {
             const int buf = lt & 1;
-            const int m0 = (t / p.tiles_n) * GM, n0 = (t % p.tiles_n) * p.bn;
+            const GTile tt = gemm_tile(p, t);
+            const int m0 = tt.m0, n0 = tt.n0;
+            const CUtensorMap *mo = &maps.o[tt.seg];
+            const int orow = m0 - (tt.seg == 2 ? p.seg_row0[2] : tt.seg == 1 ? p.seg_row0[1] : p.seg_row0[0]) +
+                             32 * q;   // this warp's first output row
             if (!wait(S::AFULL + buf, (lt >> 1) & 1)) break;
             tc_fence_after();
             const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * GBN);
@@ -339,7 +381,7 @@ project_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tm_o, stg_a, col0, m0 + 32 * q);   // rows / columns past the end are clipped
+                        tma_store_2d(mo, stg_a, col0, orow);   // rows / columns past the end are clipped
                         bulk_commit();
                     }
                 } else {
@@ -432,8 +474,7 @@ bool gmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, co
 bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
 template <bool kTmaIn, typename S, int kMinBlocks>
-cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mo, const GemmParams &p,
-                          cudaStream_t s)
+cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmParams &p, cudaStream_t s)
 {
     auto kern = project_gemm_kernel<kTmaIn, S, kMinBlocks>;
     static std::atomic<uint64_t> opted{0};
@@ -448,8 +489,61 @@ cudaError_t launch_gemm_t(const CUtensorMap &mx, const CUtensorMap &mw, const CU
     }
     const long slots = (long)kMinBlocks * device_sm_count();
     const int grid = p.tiles < slots ? p.tiles : (int)slots;
-    kern<<<(unsigned)grid, GNT, S::TOTAL, s>>>(mx, mw, mo, p);
+    kern<<<(unsigned)grid, GNT, S::TOTAL, s>>>(maps, p);
     return cudaGetLastError();
+}
+
+// the shape fields of a launch and its single segment (y = x W^T, all rows)
+void gemm_shape(GemmParams &p, int rows, int d_in, int heads, int d_head, int d_pad, int bn)
+{
+    p.rows = rows;
+    p.d_in = d_in;
+    p.heads = heads;
+    p.d_head = d_head;
+    p.d_pad = d_pad;
+    p.n_out = heads * d_pad;
+    p.bn = p.n_out >= bn ? bn : (p.n_out + 15) / 16 * 16;
+    p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
+    p.ksteps = (d_in + GK - 1) / GK;
+    p.row_blocks = (rows + GM - 1) / GM;
+    p.nseg = 1;
+    for (int sg = 0; sg < GSEG; ++sg) p.seg_fb[sg] = p.seg_row0[sg] = 0;
+}
+
+// tiles of a launch: each band of row blocks times its active segments
+bool gemm_count_tiles(GemmParams &p)
+{
+    long tiles = 0;
+    for (int b = 0; b < p.nseg; ++b) {
+        const int end = b + 1 < p.nseg ? p.seg_fb[b + 1] : p.row_blocks;
+        tiles += (long)(end - p.seg_fb[b]) * (b + 1) * p.tiles_n;
+    }
+    if (tiles > INT32_MAX) return false;
+    p.tiles = (int)tiles;
+    return true;
+}
+
+// the tensor maps of one segment's W ([heads][d_head][d_in], a box of
+// bn / d_pad whole heads of d_pad rows, rows d_head.. zero-filled) and
+// output ([rows][n_out], 32-row x 64-column boxes)
+bool gemm_wmap(CUtensorMap *m, const void *w, const GemmParams &p)
+{
+    const cuuint64_t dw[3] = {(cuuint64_t)p.d_in, (cuuint64_t)p.d_head, (cuuint64_t)p.heads};
+    const cuuint64_t sw[2] = {(cuuint64_t)p.d_in * 2, (cuuint64_t)p.d_head * p.d_in * 2};
+    const cuuint32_t bw[3] = {GK, (cuuint32_t)p.d_pad, (cuuint32_t)(p.bn / p.d_pad)};
+    return gmap(m, 3, w, dw, sw, bw);
+}
+bool gemm_omap(CUtensorMap *m, void *out, int rows, const GemmParams &p)
+{
+    const cuuint64_t dO[2] = {(cuuint64_t)p.n_out, (cuuint64_t)rows}, sO[1] = {(cuuint64_t)p.n_out * 2};
+    const cuuint32_t bO[2] = {64, 32};
+    return gmap(m, 2, out, dO, sO, bO);
+}
+bool gemm_xmap(CUtensorMap *m, const void *x, const GemmParams &p)
+{
+    const cuuint64_t dx[2] = {(cuuint64_t)p.d_in, (cuuint64_t)p.rows}, sx[1] = {(cuuint64_t)p.d_in * 2};
+    const cuuint32_t bx[2] = {GK, GM};
+    return gmap(m, 2, x, dx, sx, bx);
 }
 
 // bf16 projection on the tensor cores: d_in even, x and w 4-byte aligned.
@@ -460,46 +554,71 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
     p.x = (const __nv_bfloat16 *)x;
     p.w = (const __nv_bfloat16 *)w;
     p.out = (__nv_bfloat16 *)out;
-    p.rows = rows;
-    p.d_in = d_in;
-    p.heads = heads;
-    p.d_head = d_head;
-    p.d_pad = d_pad;
-    p.n_out = heads * d_pad;
     // TMA addresses rows whose pitch is a multiple of 16 bytes; a W box holds
     // whole heads of d_pad rows
     const int bn_max = d_in % 8 == 0 && al(x, 16) && al(w, 16) ? SmemTma::GBN : SmemCpa::GBN;
-    p.bn = p.n_out >= bn_max ? bn_max : (p.n_out + 15) / 16 * 16;
-    p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
-    const long tiles = (long)((rows + GM - 1) / GM) * p.tiles_n;
-    if (tiles > INT32_MAX) return cudaErrorNotSupported;
-    p.tiles = (int)tiles;
-    p.ksteps = (d_in + GK - 1) / GK;
+    gemm_shape(p, rows, d_in, heads, d_head, d_pad, bn_max);
     const bool tma_in = bn_max == SmemTma::GBN && p.bn % d_pad == 0 && d_pad <= 256;
     p.tma_out = al(out, 16) && (p.n_out * 2) % 16 == 0;
-    CUtensorMap mx{}, mw{}, mo{};
-    if (tma_in) {
-        const cuuint64_t dx[2] = {(cuuint64_t)d_in, (cuuint64_t)rows}, sx[1] = {(cuuint64_t)d_in * 2};
-        const cuuint32_t bx[2] = {GK, GM};
-        const cuuint64_t dw[3] = {(cuuint64_t)d_in, (cuuint64_t)d_head, (cuuint64_t)heads};
-        const cuuint64_t sw[2] = {(cuuint64_t)d_in * 2, (cuuint64_t)d_head * d_in * 2};
-        const cuuint32_t bw[3] = {GK, (cuuint32_t)d_pad, (cuuint32_t)(p.bn / d_pad)};
-        if (!gmap(&mx, 2, x, dx, sx, bx) || !gmap(&mw, 3, w, dw, sw, bw)) return cudaErrorInvalidValue;
-    }
-    if (p.tma_out) {
-        const cuuint64_t dO[2] = {(cuuint64_t)p.n_out, (cuuint64_t)rows}, sO[1] = {(cuuint64_t)p.n_out * 2};
-        const cuuint32_t bO[2] = {64, 32};
-        if (!gmap(&mo, 2, out, dO, sO, bO)) return cudaErrorInvalidValue;
-    }
     if (!tma_in && p.bn > SmemCpa::GBN) {   // TMA-able rows whose heads do not tile the box: 128-wide tiles
         p.bn = SmemCpa::GBN;
         p.tiles_n = (p.n_out + p.bn - 1) / p.bn;
-        const long t2 = (long)((rows + GM - 1) / GM) * p.tiles_n;
-        if (t2 > INT32_MAX) return cudaErrorNotSupported;
-        p.tiles = (int)t2;
     }
-    return tma_in ? launch_gemm_t<true, SmemTma, 1>(mx, mw, mo, p, s)
-                  : launch_gemm_t<false, SmemCpa, 2>(mx, mw, mo, p, s);
+    if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
+    GemmMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (tma_in && (!gemm_xmap(&maps.x, x, p) || !gemm_wmap(&maps.w[0], w, p))) return cudaErrorInvalidValue;
+    if (p.tma_out && !gemm_omap(&maps.o[0], out, rows, p)) return cudaErrorInvalidValue;
+    return tma_in ? launch_gemm_t<true, SmemTma, 1>(maps, p, s) : launch_gemm_t<false, SmemCpa, 2>(maps, p, s);
+}
+
+// k = x W_k^T and v = x W_v^T over all rows and, when wq is given,
+// q = x[q_row0..] W_q^T.  When every operand is TMA-addressable, k and v
+// come from one launch that reads x once, and q joins it when its first row
+// starts a 128-row block (else q is a launch of its own); otherwise one
+// launch per product.
+cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq, const void *wk, const void *wv,
+                               void *q, void *k, void *v, int q_row0, int heads, int d_head, int d_pad,
+                               cudaStream_t s)
+{
+    const bool with_q = wq != nullptr && rows > q_row0;
+    const int n_out = heads * d_pad;
+    GemmParams p;
+    bool fused = d_in % 8 == 0 && al(x, 16) && al(wk, 16) && al(wv, 16) && al(k, 16) && al(v, 16) &&
+                 (n_out * 2) % 16 == 0 && d_pad <= 256;
+    if (fused) {
+        gemm_shape(p, rows, d_in, heads, d_head, d_pad, SmemTma::GBN);
+        fused = p.bn % d_pad == 0;
+    }
+    cudaError_t e = cudaSuccess;
+    bool q_done = false;
+    if (fused) {
+        const bool q_in = with_q && al(wq, 16) && al(q, 16) && q_row0 % GM == 0;
+        p.x = (const __nv_bfloat16 *)x;
+        p.w = (const __nv_bfloat16 *)wk;
+        p.out = (__nv_bfloat16 *)k;
+        p.tma_out = 1;
+        p.nseg = q_in ? 3 : 2;
+        p.seg_fb[2] = q_in ? q_row0 / GM : 0;
+        p.seg_row0[2] = q_in ? q_row0 : 0;
+        if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
+        GemmMaps maps;
+        memset(&maps, 0, sizeof(maps));
+        if (!gemm_xmap(&maps.x, x, p) || !gemm_wmap(&maps.w[0], wk, p) || !gemm_wmap(&maps.w[1], wv, p) ||
+            !gemm_omap(&maps.o[0], k, rows, p) || !gemm_omap(&maps.o[1], v, rows, p))
+            return cudaErrorInvalidValue;
+        if (q_in && (!gemm_wmap(&maps.w[2], wq, p) || !gemm_omap(&maps.o[2], q, rows - q_row0, p)))
+            return cudaErrorInvalidValue;
+        e = launch_gemm_t<true, SmemTma, 1>(maps, p, s);
+        q_done = q_in;
+    } else {
+        e = launch_project_gemm(x, wk, k, rows, d_in, heads, d_head, d_pad, s);
+        if (e == cudaSuccess) e = launch_project_gemm(x, wv, v, rows, d_in, heads, d_head, d_pad, s);
+    }
+    if (e == cudaSuccess && with_q && !q_done)
+        e = launch_project_gemm((const __nv_bfloat16 *)x + (size_t)q_row0 * d_in, wq, q, rows - q_row0, d_in, heads,
+                                d_head, d_pad, s);
+    return e;
 }
 
 // =========================================================================
@@ -687,6 +806,54 @@ txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, 
         return TXL_ERR_CUDA;
     }
     return TXL_OK;
+}
+
+txl_status txl_project_qkv(const void *x, int rows, int d_in, const void *w_q, const void *w_k, const void *w_v,
+                           void *q, void *k, void *v, int q_row0, int heads, int d_head, int d_pad, txl_dtype dtype,
+                           void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (rows < 0 || d_in < 0 || heads < 0 || d_head < 1 || d_pad < d_head) return TXL_ERR_INVALID;
+    if ((w_q == nullptr) != (q == nullptr)) return TXL_ERR_INVALID;
+    if (w_q && (q_row0 < 0 || q_row0 > rows)) return TXL_ERR_INVALID;
+    if (rows == 0 || heads == 0) return TXL_OK;
+    if (!x || !w_k || !w_v || !k || !v) return TXL_ERR_INVALID;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (!al(x, esz) || !al(w_k, esz) || !al(w_v, esz) || !al(k, esz) || !al(v, esz)) return TXL_ERR_INVALID;
+    if (w_q && (!al(w_q, esz) || !al(q, esz))) return TXL_ERR_INVALID;
+    if ((long)heads * d_pad > INT32_MAX || (long)heads * d_head > INT32_MAX) return TXL_ERR_UNSUPPORTED;
+    // every output apart from x, the weights and the other outputs
+    const size_t row_b = (size_t)heads * d_pad * esz, nw = (size_t)d_in * heads * d_head * esz;
+    const size_t nx = (size_t)rows * d_in * esz, nkv = (size_t)rows * row_b;
+    const size_t nq = w_q ? (size_t)(rows - q_row0) * row_b : 0;
+    const void *outs[3] = {k, v, q};
+    const size_t nout[3] = {nkv, nkv, nq};
+    const void *ins[4] = {x, w_k, w_v, w_q};
+    const size_t nin[4] = {nx, nw, nw, w_q ? nw : 0};
+    for (int o = 0; o < 3; ++o) {
+        if (nout[o] == 0) continue;
+        for (int i = 0; i < 4; ++i)
+            if (nin[i] && overlap_bytes(outs[o], nout[o], ins[i], nin[i])) return TXL_ERR_INVALID;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (nout[o2] && overlap_bytes(outs[o], nout[o], outs[o2], nout[o2])) return TXL_ERR_INVALID;
+    }
+    if (dtype == TXL_BF16 && d_in > 0 && d_in % 2 == 0 && al(x, 4) && al(w_k, 4) && al(w_v, 4) &&
+        (!w_q || al(w_q, 4)) && (long)heads * d_head * d_in <= INT32_MAX) {
+        const cudaError_t e = launch_project_qkv(x, rows, d_in, w_q, w_k, w_v, q, k, v, q_row0, heads, d_head,
+                                                 d_pad, (cudaStream_t)stream);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return TXL_ERR_CUDA;
+        }
+        return TXL_OK;
+    }
+    // the three products one by one
+    txl_status st = txl_project_heads(x, w_k, k, rows, d_in, heads, d_head, d_pad, dtype, stream);
+    if (st == TXL_OK) st = txl_project_heads(x, w_v, v, rows, d_in, heads, d_head, d_pad, dtype, stream);
+    if (st == TXL_OK && w_q && rows > q_row0)
+        st = txl_project_heads((const unsigned char *)x + (size_t)q_row0 * d_in * esz, w_q, q, rows - q_row0, d_in,
+                               heads, d_head, d_pad, dtype, stream);
+    return st;
 }
 
 txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int heads, int d_head, int d_pad,
