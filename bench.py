@@ -295,8 +295,7 @@ class AttnChain:
         update, in one library call when the chain is fused (the events
         then bracket both); returns the kernels launched."""
         if attn_events is not None:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+            attn_events.begin()
         if self.fused:
             M = self.w.shape.mem_len
             txl.rel_attn_fwd_mem(lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"], mem_len=M,
@@ -307,8 +306,7 @@ class AttnChain:
             self.attn(txl, lay)
             mem_launches = None
         if attn_events is not None:
-            e1.record()
-            attn_events.append((e0, e1))
+            attn_events.end()
         if mem_launches is None:
             mem_launches = self.memory(txl, lay)
         return 1 + self.attn_extra_launches + mem_launches
@@ -363,6 +361,81 @@ class AttnChain:
 
     attn_extra_launches = 0
     rollover_in_attention = False
+
+
+class EagerMarks:
+    """CUDA events around each attention call of an eagerly launched step."""
+
+    def __init__(self):
+        self.pairs = []
+
+    def begin(self):
+        self._e0 = torch.cuda.Event(enable_timing=True)
+        self._e0.record()
+
+    def end(self):
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record()
+        self.pairs.append((self._e0, e1))
+
+    def intervals_ms(self):
+        return [a.elapsed_time(b) for a, b in self.pairs]
+
+
+class GraphMarks:
+    """Event pairs around each attention call of a captured step, recorded by
+    the replayed graph itself: external event-record nodes through the
+    driver API (an event recorded by torch during a capture only orders
+    streams).  The times are then those of the graph-replayed step, with no
+    host work between the kernels; after the replays they hold the last one."""
+    RECORD_EXTERNAL = 1
+
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        cu = ctypes.CDLL("libcuda.so.1")
+        vp = ctypes.c_void_p
+        cu.cuEventCreate.argtypes = [ctypes.POINTER(vp), ctypes.c_uint]
+        cu.cuEventRecordWithFlags.argtypes = [vp, vp, ctypes.c_uint]
+        self._elapsed = getattr(cu, "cuEventElapsedTime_v2", None) or cu.cuEventElapsedTime
+        self._elapsed.argtypes = [ctypes.POINTER(ctypes.c_float), vp, vp]
+        self._destroy = getattr(cu, "cuEventDestroy_v2", None) or cu.cuEventDestroy
+        self._destroy.argtypes = [vp]
+        self.cu = cu
+        self.pairs = []
+
+    def _check(self, r, what):
+        if r != 0:
+            raise RuntimeError(f"{what}: CUresult {r}")
+
+    def _record(self):
+        c = self._c
+        ev = c.c_void_p()
+        self._check(self.cu.cuEventCreate(c.byref(ev), 0), "cuEventCreate")
+        stream = c.c_void_p(torch.cuda.current_stream().cuda_stream)
+        self._check(self.cu.cuEventRecordWithFlags(ev, stream, self.RECORD_EXTERNAL), "cuEventRecordWithFlags")
+        return ev
+
+    def begin(self):
+        self._e0 = self._record()
+
+    def end(self):
+        self.pairs.append((self._e0, self._record()))
+
+    def intervals_ms(self):
+        c = self._c
+        out = []
+        for a, b in self.pairs:
+            ms = c.c_float()
+            self._check(self._elapsed(c.byref(ms), a, b), "cuEventElapsedTime")
+            out.append(ms.value)
+        return out
+
+    def close(self):
+        for a, b in self.pairs:
+            self._destroy(a)
+            self._destroy(b)
+        self.pairs = []
 
 
 def qkv_launches(w: Workload, dp: int, ring: bool) -> int:
@@ -497,8 +570,7 @@ class LayerChain:
             if nxt is not None and dp == D and not self.ring:
                 out = nxt["ext"][cur][M:].view(L, B, H, D)      # straight into the next layer's h~
             if attn_events is not None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
+                attn_events.begin()
             args = (lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"])
             if self.ring:
                 txl.rel_attn_fwd_ring(*args, mem_len=M, kv_start=lay["start"], out=out)
@@ -509,8 +581,7 @@ class LayerChain:
             else:
                 txl.rel_attn_fwd(*args, mem_len=M, out=out)
             if attn_events is not None:
-                e1.record()
-                attn_events.append((e0, e1))
+                attn_events.end()
             launches += 1 + self.attn_extra_launches
             if self.ring:
                 lay["start"] = (lay["start"] + L) % s.klen
@@ -995,7 +1066,7 @@ def main(argv=None):
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    attn_events = []
+    attn_events = EagerMarks()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     launches = 0
@@ -1016,6 +1087,9 @@ def main(argv=None):
     # often, with one captured single step first when K is odd.  Falls back
     # to the eager timing if the capture fails.
     timing = {"mode": "eager", "eager_ms_per_step": eager_step_s * 1e3}
+    attn_ms = attn_events.intervals_ms()
+    attn_timing = "CUDA events around each attention call of the eagerly launched timed steps"
+    gmarks = None
     if not args.no_graph and not args.ring:
         try:
             gs = chain.graph_steps
@@ -1032,6 +1106,14 @@ def main(argv=None):
             with torch.cuda.graph(gph, stream=side):
                 for _ in range(gs):
                     chain.step(txl)
+            # the same step with an event pair around each attention call,
+            # replayed after the timed region (the event nodes cost the step
+            # about 5%, so the timed graph has none)
+            gmarks = GraphMarks()
+            gph_m = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph_m, stream=side):
+                for _ in range(gs):
+                    chain.step(txl, gmarks)
             g1 = None
             if gs > 1 and args.steps % gs:
                 # one more step, replayed after the pairs: it leaves the buffers
@@ -1059,14 +1141,23 @@ def main(argv=None):
             txl.check()
             local_s = e0.elapsed_time(e1) / 1e3
             timing["mode"] = "cuda_graph"
-            del gph, g1
+            for _ in range(2):
+                gph_m.replay()
+            torch.cuda.synchronize()
+            txl.check()
+            attn_ms = gmarks.intervals_ms()
+            attn_timing = ("event-record nodes around each attention call of the step's graph, replayed "
+                           "after the timed region (the last replay; eager-step events gave "
+                           f"{sum(attn_events.intervals_ms()) / len(attn_events.pairs) * 1e3:.1f} us)")
+            del gph, g1, gph_m
         except Exception as ex:   # keep the eager numbers
             torch.cuda.synchronize()
             timing["graph_error"] = str(ex)[:160]
     tokens_per_step = s.batch * s.seg_len * w.segments
     value = aggregate_rate(tokens_per_step * args.steps, local_s, world)
     step_s = max_over_ranks(local_s, world) / args.steps
-    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    if gmarks is not None:
+        gmarks.close()
     attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
 
     flops_call = w.flops_per_call()
@@ -1089,6 +1180,7 @@ def main(argv=None):
         roof["issued_to_algorithmic_flops"] = w.issued_flops_per_call(splits) / flops_call
     roof["kernel"] = "rel_attn_bf16_kernel" if w.dtype == "bf16" else "rel_attn_f32_kernel"
     roof["launch_avg_us"] = attn_avg_s * 1e6
+    roof["launch_timing"] = attn_timing
     roof["peak_source"] = f"{peak_kind} ({'MEASURED_PEAKS.json burst' if peak_kind == 'measured' else 'fallback'})"
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
