@@ -2,10 +2,10 @@
 
 One step = one pass of the hot path over one batch of the workload: every
 segment of the workload's chain, and in each segment every layer's q, k, v
-projections of [memory; h] (txl_project_qkv), its relative attention
-(txl_rel_attn_fwd) and its memory rollover (txl_mem_update), the rollover
-feeding the next segment's keys and values and each layer's output feeding
-the next layer (``--attn-only``: the attention and rollover alone on fixed
+projections of [memory; h] (txl_project_qkv), its relative attention and
+its memory rollover (one txl_rel_attn_fwd_mem call for 64-wide heads, else
+txl_rel_attn_fwd and txl_mem_update), the rollover feeding the next
+segment's keys and values and each layer's output feeding the next layer (``--attn-only``: the attention and rollover alone on fixed
 per-layer inputs).  Inputs are seeded and synthetic, resident in HBM before
 the timed region; the per-step working set is far larger than L2.
 
@@ -461,7 +461,8 @@ class LayerChain:
     segment's states, k = h~ W_kE^T and v = h~ W_v^T on the extended context
     h~ = [memory; h] (txl_project_qkv), the relative attention over h~,
     and the rollover that keeps the newest M rows of h~ as the next
-    segment's memory (txl_mem_update), so each segment's keys and values
+    segment's memory (inside the attention call, txl_rel_attn_fwd_mem, or
+    txl_mem_update), so each segment's keys and values
     are projected from the memory the previous segment left.  Layer n+1's
     segment states are layer n's attention output, written by the
     attention straight into layer n+1's extended context (the output
@@ -1003,8 +1004,12 @@ def main(argv=None):
     ap.add_argument("--backward", action="store_true",
                     help="time txl_rel_attn_bwd (gradients of one layer call) at the workload's shape")
     ap.add_argument("--fused-rollover", action="store_true",
-                    help="attention and memory update of a layer in one call (txl_rel_attn_fwd_mem); the "
-                         "roofline's launch time then includes the rollover copy")
+                    help="--attn-only: attention and memory update of a layer in one call "
+                         "(txl_rel_attn_fwd_mem; the recurrence step does this by default); the roofline's "
+                         "launch time then includes the rollover copy")
+    ap.add_argument("--separate-rollover", action="store_true",
+                    help="recurrence step: the memory update as its own call (txl_mem_update) instead of "
+                         "inside the attention call")
     ap.add_argument("--ring", action="store_true",
                     help="memory as a ring: each layer appends its L new rows instead of copying M")
     ap.add_argument("--attn-only", action="store_true",
@@ -1050,7 +1055,10 @@ def main(argv=None):
         chain = AttnChain(w, dev, ring=args.ring, pad=args.pad, fused=args.fused_rollover)
         padded = bool(chain.pad)
     else:
-        chain = LayerChain(w, dev, txl, ring=args.ring, fused=args.fused_rollover)
+        # the attention and the memory update of a layer in one call wherever
+        # the chain allows it (64-wide heads, a copied memory)
+        fused = not args.separate_rollover and not args.ring and (s.d_head == 64 or w.dtype != "bf16")
+        chain = LayerChain(w, dev, txl, ring=args.ring, fused=fused or args.fused_rollover)
         padded = chain.dp != s.d_head
     # the library's own plan for this call shape: key splits and launches
     splits, call_launches = txl.rel_attn_fwd_plan(s.batch, s.mem_len, s.seg_len, s.heads, s.d_head,

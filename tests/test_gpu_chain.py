@@ -7,7 +7,7 @@ n saw in segment tau.  Section 3.3's procedure projects q from the segment's
 states and k, v from the whole extended context, builds the relative table
 from W_kR and the sinusoid, and attends.  Here every step of that per-layer
 procedure runs in the library (txl_project_qkv, txl_project_heads, txl_rel_table, the
-attention entry point, txl_mem_update or txl_ring_append); the glue between
+attention entry point, txl_rel_attn_fwd_mem or txl_mem_update, txl_ring_append); the glue between
 layers, h^n = LayerNorm(a^{n-1} W_o + h^{n-1}), runs in torch and is not
 checked.  Language-model initialisation: hidden states N(0, 1), weights and
 biases N(0, 0.02^2).
@@ -152,14 +152,21 @@ def test_chain_matches_oracle_every_call(name):
             # q of the segment's rows M.., k and v of all rows: one call, as
             # the benchmark's recurrence makes it
             q, k, v = txl.project_qkv(ext[n], lay.wq, lay.wk, lay.wv, H, D, dp, q_from=M)
-            a = attend(q, k, v, tables[n], lay)
+            if dp == D:
+                # attention and the next segment's memory (newest M rows of
+                # [memory; h]) in one call, as the benchmark's recurrence runs it
+                a = txl.rel_attn_fwd_mem(q, k, v, tables[n], lay.u, lay.w, mem_len=M, mem_next=spare[n],
+                                         ext_ctx=ext[n])
+            else:
+                a = attend(q, k, v, tables[n], lay)
             if seg > 0 and M > 0:
                 # keys and values of the rolled memory
                 _check_projection(f"{name} k(mem)", ext[n][:M], lay.wk, k[:M], H, D, g)
                 _check_projection(f"{name} v(mem)", ext[n][:M], lay.wv, v[:M], H, D, g)
             worst = max(worst, _check_attention(f"chain_{name}", q, k, v, tables[n], lay.u, lay.w, a, D, M, g))
             # the memory for the next segment: newest M rows of [memory; h]
-            txl.mem_update(spare[n], ext[n], mem_len=M)
+            if dp != D:
+                txl.mem_update(spare[n], ext[n], mem_len=M)
             torch.cuda.synchronize()
             want = oracle.mem_update(ext[n].view(torch.int16).cpu().numpy(), M)
             assert np.array_equal(spare[n][:M].view(torch.int16).cpu().numpy(), want), f"{name}: rollover bits"
