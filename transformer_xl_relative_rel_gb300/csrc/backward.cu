@@ -438,8 +438,9 @@ bool gemm_rm(cudaStream_t s, bool ta, bool tb, int m, int n, int k, const void *
 // (the descriptor's leading-dimension offset), a B stage is 64 k-rows.
 // Warp 0 loads, warp 1 issues the MMAs (four K=16 steps per 64-wide stage),
 // warps 4-7 take the accumulator (two 64-column buffers in TMEM) to global
-// memory, a lane per row.
-constexpr int BG_M = 128, BG_K = 64, BG_ST = 6, BG_NT = 256;
+// memory, a lane per row.  Four 24 KB stages, so that two CTAs share an SM
+// (two independent load / MMA chains; 128 TMEM columns each).
+constexpr int BG_M = 128, BG_K = 64, BG_ST = 4, BG_NT = 256;
 constexpr uint64_t BG_WAIT_NS = 2000000000ull;
 
 struct BgSmem {
@@ -483,7 +484,7 @@ __device__ __forceinline__ void bg_load(uint32_t dst, const CUtensorMap *m, uint
         sm100::tma_load_3d(dst, m, bar, c0, c1, o.zmod ? z % H : z);
 }
 
-__global__ void __launch_bounds__(BG_NT, 1)
+__global__ void __launch_bounds__(BG_NT, 2)
 bwd_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
                 const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, const BgParams p)
 {
@@ -730,7 +731,7 @@ cudaError_t launch_bwd_gemm(const CUtensorMap *ma, const CUtensorMap *mb, const 
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_relaxed);
     }
-    const int grid = p.tiles < device_sm_count() ? p.tiles : device_sm_count();
+    const int grid = p.tiles < 2 * device_sm_count() ? p.tiles : 2 * device_sm_count();
     bwd_gemm_kernel<<<(unsigned)grid, BG_NT, BgSmem::TOTAL, s>>>(ma[0], mb[0], p.pairs > 1 ? ma[1] : ma[0],
                                                                   p.pairs > 1 ? mb[1] : mb[0], p);
     return cudaGetLastError();
