@@ -106,29 +106,66 @@ __global__ void bwd_table_rep_kernel(const T *__restrict__ r, T *__restrict__ rr
 }
 
 // The same two copies in 16-byte chunks (8 bf16 or 4 fp32 elements) when D
-// is a multiple of the chunk: one index decomposition per chunk.
-template <typename T>
+// is a multiple of the chunk.  A thread's chunk position within a row of
+// heads (H * D / C chunks) advances by the grid stride modulo that row, so
+// the loop needs one 32-bit division per chunk; with 16-byte aligned biases
+// their elements come as float4 loads.
+template <typename T, bool kB4>
 __global__ void bwd_fold_vec_kernel(const T *__restrict__ q, const float *__restrict__ u,
                                     const float *__restrict__ w, T *__restrict__ qu, T *__restrict__ qv, long nch,
                                     int H, int D)
 {
     constexpr int C = 16 / sizeof(T);
-    const int dc = D / C;
-    for (long x = (long)blockIdx.x * blockDim.x + threadIdx.x; x < nch; x += (long)gridDim.x * blockDim.x) {
-        const int d0 = (int)(x % dc) * C, h = (int)((x / dc) % H);
+    const unsigned dc = (unsigned)(D / C), hdc = (unsigned)H * dc;
+    const long x0 = (long)blockIdx.x * blockDim.x + threadIdx.x, stride = (long)gridDim.x * blockDim.x;
+    unsigned y = (unsigned)(x0 % hdc);
+    const unsigned ystep = (unsigned)(stride % hdc);
+    for (long x = x0; x < nch; x += stride) {
+        const unsigned h = y / dc;
+        const int hd = (int)(h * D + (y - h * dc) * C);   // bias element of this chunk's first column
         const uint4 raw = reinterpret_cast<const uint4 *>(q)[x];
         const T *e = reinterpret_cast<const T *>(&raw);
+        float ub[C], wb[C];
+        if (kB4) {
+#pragma unroll
+            for (int c = 0; c < C; c += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(u + hd + c);
+                const float4 b4 = *reinterpret_cast<const float4 *>(w + hd + c);
+                ub[c] = a4.x, ub[c + 1] = a4.y, ub[c + 2] = a4.z, ub[c + 3] = a4.w;
+                wb[c] = b4.x, wb[c + 1] = b4.y, wb[c + 2] = b4.z, wb[c + 3] = b4.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                ub[c] = u[hd + c];
+                wb[c] = w[hd + c];
+            }
+        }
         uint4 a, b;
         T *ea = reinterpret_cast<T *>(&a), *eb = reinterpret_cast<T *>(&b);
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             const float qq = to_f(e[c]);
-            ea[c] = from_f<T>(qq + u[h * D + d0 + c]);
-            eb[c] = from_f<T>(qq + w[h * D + d0 + c]);
+            ea[c] = from_f<T>(qq + ub[c]);
+            eb[c] = from_f<T>(qq + wb[c]);
         }
         reinterpret_cast<uint4 *>(qu)[x] = a;
         reinterpret_cast<uint4 *>(qv)[x] = b;
+        y += ystep;
+        if (y >= hdc) y -= hdc;
     }
+}
+
+// one launch of the chunked fold: float4 bias loads when both biases are
+// 16-byte aligned
+template <typename T>
+void launch_fold_vec(const T *q, const float *u, const float *w, T *qu, T *qv, long nch, int H, int D, unsigned grid,
+                     cudaStream_t s)
+{
+    if (((uintptr_t)u & 15) == 0 && ((uintptr_t)w & 15) == 0)
+        bwd_fold_vec_kernel<T, true><<<grid, 256, 0, s>>>(q, u, w, qu, qv, nch, H, D);
+    else
+        bwd_fold_vec_kernel<T, false><<<grid, 256, 0, s>>>(q, u, w, qu, qv, nch, H, D);
 }
 
 template <typename T>
@@ -838,7 +875,7 @@ txl_status run_bwd(const void *q, const void *k, const void *v, const void *r, c
     };
     if (D % (16 / (int)sizeof(E)) == 0 && ((uintptr_t)q & 15) == 0 && ((uintptr_t)r & 15) == 0) {
         const int C = 16 / (int)sizeof(E);
-        bwd_fold_vec_kernel<E><<<grid_for(nq / C, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / C, H, D);
+        launch_fold_vec<E>((const E *)q, u, w, qu, qv, nq / C, H, D, grid_for(nq / C, 256), s);
         if (!chk()) goto cuda_fail;
         bwd_table_rep_vec_kernel<E><<<grid_for(BH * T * D / C, 256), 256, 0, s>>>((const E *)r, rrep,
                                                                                 BH * T * D / C, H, D, (int)T);
@@ -932,7 +969,7 @@ txl_status run_bwd_fused(const void *q, const void *k, const void *v, const void
     }
     if ((e = launch_bwd_scores(a, dout, lse, pb, dab, dbb, TP, s)) != cudaSuccess) goto cuda_fail;
     // the GEMM operands q+u, q+v
-    bwd_fold_vec_kernel<E><<<grid_for(nq / 8, 256), 256, 0, s>>>((const E *)q, u, w, qu, qv, nq / 8, H, D);
+    launch_fold_vec<E>((const E *)q, u, w, qu, qv, nq / 8, H, D, grid_for(nq / 8, 256), s);
     if (!chk()) goto cuda_fail;
     {
         // per (b, h): dV = P^T dO, dK = dA^T qu (rows j of the transposed
