@@ -32,14 +32,19 @@ def _sms():
 def _candidates():
     """(B, H, D, L, M) with B*H at least the SM count and not a multiple of
     it, and memories long enough that the split model divides the keys (so
-    the stream-K schedule runs); key tiles per item from 24 to 32."""
+    the stream-K schedule runs; key tiles per item from 24 to 32), or B*H
+    just above the SM count."""
     n = _sms()
     return [(n + 8, 1, 64, 128, 3000),       # a full query block
             (n + 8, 1, 64, 64, 3000),        # a ragged query block
             (n + 18, 1, 64, 33, 2600),       # ragged keys in the last tile
             (n + 9, 1, 56, 100, 3000),       # head size 56: thread loads
             (n + 9, 1, 64, 1, 3000),         # one query per item
-            (n + 3, 1, 64, 128, 4000)]
+            (n + 3, 1, 64, 128, 4000),
+            # the long-memory evaluation shape with just over one (b, h) per
+            # SM: the model keeps its keys whole, but whole items would
+            # leave most CTAs idle in the second round, so stream-K runs
+            (-(-(n + 1) // 16), 16, 64, 128, 1600)]
 
 
 def _streamk(B, H, D, L, M):
@@ -52,7 +57,7 @@ def test_candidates_take_the_schedule():
     assert sum(_streamk(*c) for c in _candidates()) >= 4
 
 
-@pytest.mark.parametrize("idx", range(6))
+@pytest.mark.parametrize("idx", range(7))
 def test_streamk_matches_oracle(idx):
     import transformer_xl_relative_rel_gb300 as txl
     B, H, D, L, M = _candidates()[idx]

@@ -1756,15 +1756,24 @@ bool streamk_ok(const AttnArgs &a, int num_sms)
     return a.L <= BM && (a.D + 15) / 16 * 16 == 64 && bh >= num_sms && bh % num_sms != 0 && bh <= INT32_MAX;
 }
 
+// Whether a call the stream-K schedule can take runs under it: where the
+// uniform model splits the shape (stream-K replaces the split: char_eval
+// 93.3 -> 84.7 us), or where whole items would leave more than four fifths
+// of the CTAs idle in the last round (H 16, L 128, M 1600: batch 10, 160
+// items on 152 SMs, 48.6 us whole, 41.7 under stream-K; batch 12, 192
+// items, 50.0 / 50.3; batch 16, 50.2 / 63.0 -- graph-replayed calls).
+bool use_streamk(const AttnArgs &a, int num_sms)
+{
+    if (!streamk_ok(a, num_sms)) return false;
+    if (bf16_uniform_splits(a, num_sms) > 1) return true;
+    const long items = (long)a.B * a.H;                  // one query tile per (b, h)
+    const long idle = (items + num_sms - 1) / num_sms * num_sms - items;
+    return idle * 5 > (long)num_sms * 4;
+}
+
 int bf16_num_splits(const AttnArgs &a, int num_sms)
 {
-    const int s = bf16_uniform_splits(a, num_sms);
-    // where the uniform model splits a shape the stream-K schedule can take,
-    // stream-K replaces the split (two partial slots: the parts of cut
-    // items): char_eval 93.3 -> 84.7 us.  Where it keeps a shape whole, so
-    // does this (long_mem_b16: 54.4 us whole, 77.4 us under stream-K, whose
-    // partials and merge cost what a two-way split costs there).
-    return (s > 1 && streamk_ok(a, num_sms)) ? 2 : s;
+    return use_streamk(a, num_sms) ? 2 : bf16_uniform_splits(a, num_sms);
 }
 
 int bf16_uniform_splits(const AttnArgs &a, int num_sms)
@@ -1871,7 +1880,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.items = (int)((long)a.B * a.H * p.nqt * splits);
     // the stream-K schedule where it applies: the two partial slots are then
     // only the parts of items cut by a CTA's range
-    p.streamk = splits == 2 && streamk_ok(a, device_sm_count()) && bf16_uniform_splits(a, device_sm_count()) > 1;
+    p.streamk = splits == 2 && use_streamk(a, device_sm_count());
     p.sk_nt = (a.M + a.L + BN - 1) / BN;
     if (p.streamk) p.items = a.B * a.H;   // grid: one CTA per SM (B*H >= SMs)
     p.kv_start = a.kv_start;
