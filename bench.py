@@ -1184,6 +1184,10 @@ def main(argv=None):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
     roof["traffic"] = profiled_traffic(w.name)
+    if getattr(chain, "rollover_in_attention", False):
+        s_ = w.shape
+        roof["traffic_note"] = ("the launch also copies the layer's memory rollover "
+                                f"({2 * 2 * s_.mem_len * s_.batch * s_.d_model / 1e6:.1f} MB algorithmic)")
     if w.dtype == "bf16":
         roof["issued_to_algorithmic_flops"] = w.issued_flops_per_call(splits) / flops_call
     roof["kernel"] = "rel_attn_bf16_kernel" if w.dtype == "bf16" else "rel_attn_f32_kernel"
