@@ -524,10 +524,13 @@ class LayerChain:
         roll = ("ring append of the L new rows (txl_ring_append)" if self.ring else
                 "rollover in the attention call (txl_rel_attn_fwd_mem)" if self.fused else
                 "rollover of the extended context (txl_mem_update)")
+        order = ("" if self.ring else
+                 "; the (layer, segment) cells run as a wavefront over the diagonals layer + segment, "
+                 "each diagonal's projections then its attention calls")
         return ("per segment: layer 0's input states copied in (txl_ring_append); per layer: q, k, v "
                 "projections of [memory; h] (txl_project_qkv, tcgen05: x read once for the three), "
                 "attention, " + roll +
-                "; layer n's output is layer n+1's input")
+                "; layer n's output is layer n+1's input" + order)
 
     def _ring_in(self, lay, rows) -> int:
         """Append a segment's L states to a layer's ring (the oldest L rows)."""
@@ -538,13 +541,79 @@ class LayerChain:
         lay["hin"] = rows
         return 2 if pos + s.seg_len > T else 1
 
-    def step(self, txl, attn_events=None) -> int:
+    def step(self, txl, attn_events=None, inputs=None) -> int:
+        """One pass over the workload's segments.  With the memory copied
+        between ping-pong buffers the (layer, segment) cells run as a
+        wavefront: cell (n, tau) needs layer n-1's output of segment tau and
+        layer n's memory from segment tau-1, so the cells with the same
+        n + tau are independent; each such diagonal runs its projections,
+        then its attention calls back to back.  Every call gets exactly the
+        inputs of the segment-by-segment order.  ``inputs``: optional
+        (ready, used) CUDA events per segment around layer 0's input copy."""
+        if self.ring:
+            launches = 0
+            for tau in range(self.w.segments):
+                launches += self.segment(txl, tau, attn_events)
+            return launches
         launches = 0
-        for tau in range(self.w.segments):
-            launches += self.segment(txl, tau, attn_events)
-            if not self.ring:
-                self.cur ^= 1
+        cur0, nl, S = self.cur, len(self.layers), self.w.segments
+        for d in range(nl + S - 1):
+            cells = [(n, d - n) for n in range(nl) if 0 <= d - n < S]
+            for n, tau in cells:
+                par = (cur0 + tau) & 1
+                if n == 0:
+                    launches += self._input(txl, tau, par, inputs)
+                launches += self._project(txl, n, par)
+            for n, tau in cells:
+                launches += self._attend(txl, n, (cur0 + tau) & 1, attn_events)
+        self.cur = (cur0 + S) & 1
         return launches
+
+    def _input(self, txl, tau: int, par: int, inputs=None) -> int:
+        """Layer 0's segment states into its extended context (L rows)."""
+        M = self.w.shape.mem_len
+        if inputs is not None:
+            torch.cuda.current_stream().wait_event(inputs[0][tau])
+        txl.ring_append(self.layers[0]["ext"][par][M:], self.h0[tau], 0)     # a plain copy of L rows
+        if inputs is not None:
+            inputs[1][tau].record(torch.cuda.current_stream())
+        return 1
+
+    def _project(self, txl, n: int, par: int) -> int:
+        s = self.w.shape
+        lay = self.layers[n]
+        txl.project_qkv(lay["ext"][par], lay["wq"], lay["wk"], lay["wv"], s.heads, s.d_head, self.dp,
+                        q_from=s.mem_len, q=lay["q"], k=lay["k"], v=lay["v"])
+        return self.proj_launches
+
+    def _attend(self, txl, n: int, par: int, attn_events=None) -> int:
+        """Layer n's attention (its output straight into layer n+1's
+        extended context) and the rollover of its extended context into the
+        other buffer, the next segment's memory."""
+        s = self.w.shape
+        B, H, D, L, M = s.batch, s.heads, s.d_head, s.seg_len, s.mem_len
+        lay = self.layers[n]
+        ext = lay["ext"][par]
+        nxt = self.layers[n + 1] if n + 1 < len(self.layers) else None
+        out = lay["out"]
+        if nxt is not None and self.dp == D:
+            out = nxt["ext"][par][M:].view(L, B, H, D)
+        if attn_events is not None:
+            attn_events.begin()
+        args = (lay["q"], lay["k"], lay["v"], lay["r"], lay["u"], lay["w"])
+        if self.fused:
+            txl.rel_attn_fwd_mem(*args, mem_len=M, mem_next=lay["ext"][1 - par], ext_ctx=ext, out=out)
+        elif self.dp != D:
+            txl.rel_attn_fwd_padded(*args, mem_len=M, d_head=D, out=out)
+        else:
+            txl.rel_attn_fwd(*args, mem_len=M, out=out)
+        if attn_events is not None:
+            attn_events.end()
+        launches = 1 + self.attn_extra_launches
+        if self.fused:
+            return launches + (0 if self.rollover_in_attention else 1)
+        txl.mem_update(lay["ext"][1 - par], ext, mem_len=M)
+        return launches + 1
 
     def segment(self, txl, tau: int, attn_events=None) -> int:
         s = self.w.shape
@@ -629,16 +698,24 @@ class LayerChain:
 
         def one():
             side.wait_stream(main)
-            for tau in range(S):
-                side.wait_event(used[tau])
-                with torch.cuda.stream(side):
-                    self.h0[tau].copy_(host[tau], non_blocking=True)
-                    copied[tau].record(side)
-                main.wait_event(copied[tau])
-                self.segment(txl, tau)
-                used[tau].record(main)
-                if not self.ring:
-                    self.cur ^= 1
+            if self.ring:
+                for tau in range(S):
+                    side.wait_event(used[tau])
+                    with torch.cuda.stream(side):
+                        self.h0[tau].copy_(host[tau], non_blocking=True)
+                        copied[tau].record(side)
+                    main.wait_event(copied[tau])
+                    self.segment(txl, tau)
+                    used[tau].record(main)
+            else:
+                # every segment's copy is queued up front on the side
+                # stream; layer 0's input copy of segment tau waits for it
+                for tau in range(S):
+                    side.wait_event(used[tau])
+                    with torch.cuda.stream(side):
+                        self.h0[tau].copy_(host[tau], non_blocking=True)
+                        copied[tau].record(side)
+                self.step(txl, inputs=(copied, used))
             out_host.copy_(last, non_blocking=True)
 
         one()
