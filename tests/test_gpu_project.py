@@ -104,9 +104,11 @@ def test_project_qkv(dtype, T, B, M, d_in, heads, d_head, d_pad):
     assert torch.equal(q, txl.project_heads(x[M:], ws[0], heads, d_head, d_pad))
     assert torch.equal(k, txl.project_heads(x, ws[1], heads, d_head, d_pad))
     assert torch.equal(v, txl.project_heads(x, ws[2], heads, d_head, d_pad))
-    # without q
+    # without q, and with no q rows
     q2, k2, v2 = txl.project_qkv(x, None, ws[1], ws[2], heads, d_head, d_pad)
     assert q2 is None and torch.equal(k2, k) and torch.equal(v2, v)
+    q3, k3, v3 = txl.project_qkv(x, ws[0], ws[1], ws[2], heads, d_head, d_pad, q_from=T)
+    assert q3.shape[0] == 0 and torch.equal(k3, k) and torch.equal(v3, v)
 
 
 def test_project_qkv_full_size_sampled_rows():

@@ -355,9 +355,11 @@ def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: i
     for name in ("k", "v") + (("q",) if w_q is not None else ()):
         if outs[name] is None:
             outs[name] = torch.empty(*shapes[name], dtype=x.dtype, device=x.device)
+    # no q rows (q_from == T): the library is asked for k and v only
+    wq_arg = w_q if (w_q is not None and q_from < T) else None
     st = load_library().txl_project_qkv(
-        _ptr(x), T * per, d_in, _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(outs["q"]), _ptr(outs["k"]),
-        _ptr(outs["v"]), q_from * per, heads, d_head, d_pad, _dtype_code(x), _stream_ptr(stream))
+        _ptr(x), T * per, d_in, _ptr(wq_arg), _ptr(w_k), _ptr(w_v), _ptr(outs["q"]) if wq_arg is not None else None,
+        _ptr(outs["k"]), _ptr(outs["v"]), q_from * per, heads, d_head, d_pad, _dtype_code(x), _stream_ptr(stream))
     _raise(st, "txl_project_qkv")
     return outs["q"], outs["k"], outs["v"]
 
