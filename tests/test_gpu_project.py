@@ -79,6 +79,7 @@ def test_project_heads_tensor_core(rows, d_in, heads, d_head, d_pad):
     (torch.bfloat16, 160, 2, 64, 1024, 16, 64, 64),   # four column tiles per product
     (torch.bfloat16, 150, 2, 100, 410, 10, 41, 64),   # cp.async rows: three launches
     (torch.bfloat16, 64, 2, 0, 128, 2, 48, 48),       # no memory: q over all rows
+    (torch.bfloat16, 200, 1, 128, 64, 1, 16, 16),     # q fused: one partial row block, a 16-wide output
     (torch.float32, 40, 2, 24, 64, 2, 16, 16),        # fp32: the CUDA-core kernel three times
 ])
 def test_project_qkv(dtype, T, B, M, d_in, heads, d_head, d_pad):
