@@ -455,6 +455,16 @@ def qkv_launches(w: Workload, dp: int, ring: bool) -> int:
     return 1 if (s.mem_len * s.batch) % 128 == 0 else 2
 
 
+def qkv_cells_launches(w: Workload, dp: int, cells: int) -> int:
+    """Launches of txl_project_qkv_cells over ``cells`` layer calls: where a
+    call's q, k and v go in one launch, up to eight calls share a launch;
+    otherwise each call is projected as txl_project_qkv projects it."""
+    one = qkv_launches(w, dp, False)
+    if one == 1 and cells >= 2:
+        return (cells + 7) // 8
+    return cells * one
+
+
 class LayerChain:
     """The recurrence of the pages, every step a library call.  Per segment
     and layer n (Transformer-XL Sections 3.2-3.3): q = h W_q^T on the
@@ -526,7 +536,8 @@ class LayerChain:
                 "rollover of the extended context (txl_mem_update)")
         order = ("" if self.ring else
                  "; the (layer, segment) cells run as a wavefront over the diagonals layer + segment, "
-                 "each diagonal's projections then its attention calls")
+                 "each diagonal's projections (txl_project_qkv_cells, up to 8 cells a launch) then its "
+                 "attention calls")
         return ("per segment: layer 0's input states copied in (txl_ring_append); per layer: q, k, v "
                 "projections of [memory; h] (txl_project_qkv, tcgen05: x read once for the three), "
                 "attention, " + roll +
@@ -560,10 +571,9 @@ class LayerChain:
         for d in range(nl + S - 1):
             cells = [(n, d - n) for n in range(nl) if 0 <= d - n < S]
             for n, tau in cells:
-                par = (cur0 + tau) & 1
                 if n == 0:
-                    launches += self._input(txl, tau, par, inputs)
-                launches += self._project(txl, n, par)
+                    launches += self._input(txl, tau, (cur0 + tau) & 1, inputs)
+            launches += self._project_cells(txl, [(n, (cur0 + tau) & 1) for n, tau in cells])
             for n, tau in cells:
                 launches += self._attend(txl, n, (cur0 + tau) & 1, attn_events)
         self.cur = (cur0 + S) & 1
@@ -579,12 +589,17 @@ class LayerChain:
             inputs[1][tau].record(torch.cuda.current_stream())
         return 1
 
-    def _project(self, txl, n: int, par: int) -> int:
+    def _project_cells(self, txl, cells) -> int:
+        """The projections of a diagonal's (layer, buffer) cells in grouped
+        launches (txl_project_qkv_cells)."""
         s = self.w.shape
-        lay = self.layers[n]
-        txl.project_qkv(lay["ext"][par], lay["wq"], lay["wk"], lay["wv"], s.heads, s.d_head, self.dp,
-                        q_from=s.mem_len, q=lay["q"], k=lay["k"], v=lay["v"])
-        return self.proj_launches
+        lays = [self.layers[n] for n, _ in cells]
+        txl.project_qkv_cells([lay["ext"][par] for lay, (_, par) in zip(lays, cells)],
+                              [lay["wq"] for lay in lays], [lay["wk"] for lay in lays],
+                              [lay["wv"] for lay in lays], s.heads, s.d_head, self.dp, q_from=s.mem_len,
+                              qs=[lay["q"] for lay in lays], ks=[lay["k"] for lay in lays],
+                              vs=[lay["v"] for lay in lays])
+        return qkv_cells_launches(self.w, self.dp, len(cells))
 
     def _attend(self, txl, n: int, par: int, attn_events=None) -> int:
         """Layer n's attention (its output straight into layer n+1's

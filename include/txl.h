@@ -237,6 +237,22 @@ txl_status txl_project_qkv(const void *x, int rows, int d_in, const void *w_q, c
                            void *stream);
 
 /*
+ * txl_project_qkv_cells -- txl_project_qkv for several layer calls of one
+ * shape at once (cells c = 0 .. cells-1, e.g. the layer calls of a
+ * recurrence that do not depend on each other): cell c projects x[c] with
+ * w_q[c], w_k[c], w_v[c] into q[c], k[c], v[c] (rows, d_in, q_row0, heads,
+ * d_head, d_pad shared).  x, w_*, q, k, v are host arrays of `cells` device
+ * pointers (w_q and q both NULL, or both arrays with every entry set); no
+ * output may overlap any input or any other output of any cell.  Where
+ * txl_project_qkv would use one launch per cell, up to eight cells share a
+ * launch; results equal the per-cell calls bit for bit.
+ */
+txl_status txl_project_qkv_cells(int cells, const void *const *x, const void *const *w_q, const void *const *w_k,
+                                 const void *const *w_v, void *const *q, void *const *k, void *const *v, int rows,
+                                 int d_in, int q_row0, int heads, int d_head, int d_pad, txl_dtype dtype,
+                                 void *stream);
+
+/*
  * txl_rel_table -- Appendix B's reversed projected table of one layer:
  * out[t][h][d] = sum_c R[klen-1-t][c] * W_kR[h*d_head + d][c] for t < klen,
  * R[p][2c] = sin(p * 10000^(-2c/d_model)), R[p][2c+1] = cos(the same angle)

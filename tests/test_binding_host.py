@@ -120,3 +120,18 @@ def test_project_qkv_checks():
                         k=torch.zeros(T, B, heads, d_pad + 8, dtype=torch.bfloat16))
     with pytest.raises(ValueError, match=ON_DEVICE):
         txl.project_qkv(x, w[0], w[1], w[2], heads, d_head, d_pad, q_from=M)          # host tensors
+
+
+def test_project_qkv_cells_checks():
+    d_in, heads, d_head, d_pad = 32, 2, 16, 16
+    xs = [torch.zeros(T, B, d_in, dtype=torch.bfloat16) for _ in range(2)]
+    ws = [torch.zeros(heads * d_head, d_in, dtype=torch.bfloat16) for _ in range(2)]
+    with pytest.raises(ValueError, match="same length"):
+        txl.project_qkv_cells(xs, ws, ws[:1], ws, heads, d_head, d_pad, q_from=M)
+    with pytest.raises(ValueError, match="first cell's shape"):
+        txl.project_qkv_cells([xs[0], xs[1][:, :1]], ws, ws, ws, heads, d_head, d_pad, q_from=M)
+    with pytest.raises(ValueError, match="w_k must be"):                                # a cell's weight
+        txl.project_qkv_cells(xs, ws, [ws[0][:, :-1], ws[1]], ws, heads, d_head, d_pad, q_from=M)
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.project_qkv_cells(xs, ws, ws, ws, heads, d_head, d_pad, q_from=M)
+    assert txl.project_qkv_cells([], None, [], [], heads, d_head, d_pad) == ([], [], [])

@@ -221,3 +221,28 @@ def test_layer_from_hidden_states():
                                                                ("u", u), ("w", w))}
     ref = oracle.rel_attn(host["q"], host["k"], host["v"], host["r"], host["u"], host["w"], mem_len=M)
     assert np.abs(out[..., :D].double().cpu().numpy() - ref).max() <= TOL_BF16
+
+
+@pytest.mark.parametrize("cells,T,B,M,d_in,heads,with_q", [
+    (3, 384, 2, 256, 512, 8, True),      # one grouped launch, q fused
+    (10, 200, 3, 128, 256, 4, True),     # two launches (8 + 2 cells)
+    (4, 160, 2, 64, 1024, 16, False),    # k and v only
+    (3, 200, 3, 72, 256, 4, True),       # q's first row inside a block: each cell as project_qkv runs it
+])
+def test_project_qkv_cells_equals_per_cell(cells, T, B, M, d_in, heads, with_q):
+    """Several layer calls' projections in grouped launches: every output bit
+    for bit what project_qkv gives cell by cell (the oracle checks of
+    project_qkv above cover the values)."""
+    import transformer_xl_relative_rel_gb300 as txl
+    g = torch.Generator(device="cuda").manual_seed(cells * 101 + T)
+    xs = [torch.randn(T, B, d_in, generator=g, device="cuda").bfloat16() for _ in range(cells)]
+    mk = lambda: [(0.02 * torch.randn(heads * 64, d_in, generator=g, device="cuda")).bfloat16() for _ in range(cells)]
+    wqs, wks, wvs = (mk() if with_q else None), mk(), mk()
+    qs, ks, vs = txl.project_qkv_cells(xs, wqs, wks, wvs, heads, 64, 64, q_from=M)
+    for c in range(cells):
+        q1, k1, v1 = txl.project_qkv(xs[c], wqs[c] if with_q else None, wks[c], wvs[c], heads, 64, 64, q_from=M)
+        assert torch.equal(ks[c], k1) and torch.equal(vs[c], v1), c
+        if with_q:
+            assert torch.equal(qs[c], q1), c
+    if not with_q:
+        assert qs is None

@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_project_qkv", "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
+           "txl_project_qkv", "txl_project_qkv_cells", "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
 
 
 class TxlError(RuntimeError):
@@ -70,6 +70,9 @@ def load_library() -> ctypes.CDLL:
     lib.txl_project_heads.restype = i
     lib.txl_project_qkv.argtypes = [vp, i, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.txl_project_qkv.restype = i
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    lib.txl_project_qkv_cells.argtypes = [i, pp, pp, pp, pp, pp, pp, pp, i, i, i, i, i, i, i, vp]
+    lib.txl_project_qkv_cells.restype = i
     lib.txl_rel_table.argtypes = [vp, vp, i, i, i, i, i, i, vp]
     lib.txl_rel_table.restype = i
     lib.txl_rel_attn_bwd_workspace.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
@@ -320,13 +323,8 @@ def project_heads(x, w, heads: int, d_head: int, d_pad: int, out=None, stream=No
     return out
 
 
-def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: int = 0,
-                q=None, k=None, v=None, stream=None):
-    """A layer's q, k, v projections of one extended context: k = x @ w_k.T
-    and v = x @ w_v.T over all of x's leading positions, q = x[q_from:] @
-    w_q.T (the segment's own positions; ``w_q=None`` skips q).  x: [T, *rest,
-    d_in]; outputs [T or T - q_from, *rest, heads, d_pad], as project_heads
-    writes them.  Returns (q, k, v)."""
+def _qkv_prepare(x, w_q, w_k, w_v, heads, d_head, d_pad, q_from, q, k, v):
+    """project_qkv's argument checks; returns its (q, k, v) outputs, allocated where not given."""
     import torch
     T = x.shape[0]
     rest = tuple(x.shape[1:-1])
@@ -355,6 +353,23 @@ def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: i
     for name in ("k", "v") + (("q",) if w_q is not None else ()):
         if outs[name] is None:
             outs[name] = torch.empty(*shapes[name], dtype=x.dtype, device=x.device)
+    return outs["q"], outs["k"], outs["v"]
+
+
+def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: int = 0,
+                q=None, k=None, v=None, stream=None):
+    """A layer's q, k, v projections of one extended context: k = x @ w_k.T
+    and v = x @ w_v.T over all of x's leading positions, q = x[q_from:] @
+    w_q.T (the segment's own positions; ``w_q=None`` skips q).  x: [T, *rest,
+    d_in]; outputs [T or T - q_from, *rest, heads, d_pad], as project_heads
+    writes them.  Returns (q, k, v)."""
+    T = x.shape[0]
+    d_in = x.shape[-1]
+    per = 1
+    for n in x.shape[1:-1]:
+        per *= n
+    q, k, v = _qkv_prepare(x, w_q, w_k, w_v, heads, d_head, d_pad, q_from, q, k, v)
+    outs = {"q": q, "k": k, "v": v}
     # no q rows (q_from == T): the library is asked for k and v only
     wq_arg = w_q if (w_q is not None and q_from < T) else None
     st = load_library().txl_project_qkv(
@@ -362,6 +377,43 @@ def project_qkv(x, w_q, w_k, w_v, heads: int, d_head: int, d_pad: int, q_from: i
         _ptr(outs["k"]), _ptr(outs["v"]), q_from * per, heads, d_head, d_pad, _dtype_code(x), _stream_ptr(stream))
     _raise(st, "txl_project_qkv")
     return outs["q"], outs["k"], outs["v"]
+
+
+def project_qkv_cells(xs, wqs, wks, wvs, heads: int, d_head: int, d_pad: int, q_from: int = 0,
+                      qs=None, ks=None, vs=None, stream=None):
+    """project_qkv for several layer calls of one shape at once (lists of
+    equal length: the cells' extended contexts, their weights and, if given,
+    their outputs); ``wqs=None`` skips q.  Returns (qs, ks, vs) lists."""
+    n = len(xs)
+    if not (len(wks) == len(wvs) == n and (wqs is None or len(wqs) == n)):
+        raise ValueError("the cells' lists must have the same length")
+    if n == 0:
+        return [], [], []
+    T = xs[0].shape[0]
+    shape = tuple(xs[0].shape)
+    for x in xs:
+        if tuple(x.shape) != shape or x.dtype != xs[0].dtype:
+            raise ValueError("every cell's x must have the first cell's shape and dtype")
+    res = {"q": [], "k": [], "v": []}
+    for c in range(n):
+        # per cell, the single-cell binding's checks and allocations (no call)
+        q1, k1, v1 = _qkv_prepare(xs[c], None if wqs is None else wqs[c], wks[c], wvs[c], heads, d_head, d_pad,
+                                  q_from, None if qs is None else qs[c], None if ks is None else ks[c],
+                                  None if vs is None else vs[c])
+        res["q"].append(q1)
+        res["k"].append(k1)
+        res["v"].append(v1)
+    per = 1
+    for d in shape[1:-1]:
+        per *= d
+    with_q = wqs is not None and q_from < T
+    arr = lambda ts: (ctypes.c_void_p * n)(*[_ptr(t) for t in ts])
+    st = load_library().txl_project_qkv_cells(
+        n, arr(xs), arr(wqs) if with_q else None, arr(wks), arr(wvs), arr(res["q"]) if with_q else None,
+        arr(res["k"]), arr(res["v"]), T * per, shape[-1], q_from * per, heads, d_head, d_pad, _dtype_code(xs[0]),
+        _stream_ptr(stream))
+    _raise(st, "txl_project_qkv_cells")
+    return (res["q"] if wqs is not None else None), res["k"], res["v"]
 
 
 def rel_table(w_r, klen: int, heads: int, d_head: int, d_pad: int, out=None, stream=None):

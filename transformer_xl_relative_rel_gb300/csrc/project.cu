@@ -101,8 +101,12 @@ static_assert(SmemTma::TOTAL <= 232448 && 2 * (SmemCpa::TOTAL + 1024) <= 233472,
 // Up to three products of the same x in one launch (q, k, v of a layer):
 // segment s multiplies x by its own W and writes its own output, over the
 // row blocks from seg_fb[s] on (seg_fb non-decreasing), output row = x row -
-// seg_row0[s].  One segment is the plain y = x W^T.
+// seg_row0[s].  One segment is the plain y = x W^T.  A launch can also take
+// several such cells of one shape (the layer calls of one step that do not
+// depend on each other), each with its own x, weights and outputs: tile t
+// belongs to cell t / tiles_cell.
 constexpr int GSEG = 3;
+constexpr int GCELLS = 8;         // cells per launch of the grouped variant
 struct GemmParams {
     const __nv_bfloat16 *x, *w;
     __nv_bfloat16 *out;
@@ -111,20 +115,29 @@ struct GemmParams {
     int tma_out;
     int nseg, row_blocks;
     int seg_fb[GSEG], seg_row0[GSEG];
+    int tiles_cell, ncell;            // tiles of one cell, cells in the launch
 };
-struct GemmMaps {
-    CUtensorMap x, w[GSEG], o[GSEG];
+template <int NC>
+struct GemmMapsN {
+    CUtensorMap x[NC], w[NC][GSEG], o[NC][GSEG];
 };
+using GemmMaps = GemmMapsN<1>;
 
 // Tile t of the launch: the row blocks fall into bands [seg_fb[b],
 // seg_fb[b+1]) in which segments 0..b are active; within a row block the
 // tiles run over the active segments' column tiles, so neighbouring CTAs
 // read the same x rows.
 struct GTile {
-    int m0, seg, n0;
+    int m0, seg, n0, cell;
 };
+template <int NC>
 __host__ __device__ __forceinline__ GTile gemm_tile(const GemmParams &p, int t)
 {
+    int cell = 0;
+    if (NC > 1) {
+        cell = t / p.tiles_cell;
+        t -= cell * p.tiles_cell;
+    }
 #pragma unroll
     for (int b = 0; b < GSEG; ++b) {   // unrolled: the fields are indexed by constants
         if (b >= p.nseg) break;
@@ -133,11 +146,11 @@ __host__ __device__ __forceinline__ GTile gemm_tile(const GemmParams &p, int t)
         const int cnt = (end - p.seg_fb[b]) * per;
         if (t < cnt) {
             const int r = t % per;
-            return {(p.seg_fb[b] + t / per) * GM, r / p.tiles_n, (r % p.tiles_n) * p.bn};
+            return {(p.seg_fb[b] + t / per) * GM, r / p.tiles_n, (r % p.tiles_n) * p.bn, cell};
         }
         t -= cnt;
     }
-    return {-1, 0, 0};
+    return {-1, 0, 0, cell};
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -151,9 +164,9 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <bool kTmaIn, typename S, int kMinBlocks>
+template <bool kTmaIn, typename S, int kMinBlocks, int NC>
 __global__ void __launch_bounds__(GNT, kMinBlocks)
-project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
+project_gemm_kernel(const __grid_constant__ GemmMapsN<NC> maps, const GemmParams p)
 {
     constexpr int GST = S::GST, GBN = S::GBN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -197,11 +210,14 @@ project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
         mbar_init(bar(S::DONE), 1);
         fence_mbar_init();
         if (kTmaIn) {
-            prefetch_tmap(&maps.x);
-            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.w[sg]);
+            for (int c = 0; c < NC && c < p.ncell; ++c) {
+                prefetch_tmap(&maps.x[c]);
+                for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.w[c][sg]);
+            }
         }
         if (p.tma_out)
-            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.o[sg]);
+            for (int c = 0; c < NC && c < p.ncell; ++c)
+                for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.o[c][sg]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -252,9 +268,9 @@ project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
                 int it = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
-                    const GTile tt = gemm_tile(p, t);
+                    const GTile tt = gemm_tile<NC>(p, t);
                     const int m0 = tt.m0, n0 = tt.n0;
-                    const CUtensorMap *mw = &maps.w[tt.seg];
+                    const CUtensorMap *mw = &maps.w[tt.cell][tt.seg], *mx = &maps.x[tt.cell];
                     for (int ks = 0; ks < p.ksteps; ++ks, ++it) {
                         const int s = it % GST;
                         if (it >= GST && !wait(S::EMPTY + s, ((it / GST) - 1) & 1)) {
@@ -262,7 +278,7 @@ project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
                             break;
                         }
                         mbar_arrive_expect_tx(bar(S::FULL + s), bytes);
-                        tma_load_2d(sbase + S::A + s * S::ASZ, &maps.x, bar(S::FULL + s), ks * GK, m0);
+                        tma_load_2d(sbase + S::A + s * S::ASZ, mx, bar(S::FULL + s), ks * GK, m0);
                         // W viewed as [heads][d_head][d_in]: a box of bn / d_pad heads
                         // of d_pad rows each; rows d_head.. of a head are zero-filled
                         tma_load_3d(sbase + S::B + s * S::BSZ, mw, bar(S::FULL + s), ks * GK, 0, n0 / p.d_pad);
@@ -280,7 +296,7 @@ project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.tiles; t += G) {
-                const GTile tt = gemm_tile(p, t);
+                const GTile tt = gemm_tile<NC>(p, t);
                 const int m0 = tt.m0, n0 = tt.n0;
                 __syncwarp();                          // the previous tile's stages have read the table
                 for (int j = lane; wi + 3 * j < p.bn; j += 32) {
@@ -336,9 +352,9 @@ project_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p)
         int lt = 0, nst = 0;                         // tiles, chunks stored (two staging buffers)
         for (int t = blockIdx.x; t < p.tiles; t += G, ++lt) {
             const int buf = lt & 1;
-            const GTile tt = gemm_tile(p, t);
+            const GTile tt = gemm_tile<NC>(p, t);
             const int m0 = tt.m0, n0 = tt.n0;
-            const CUtensorMap *mo = &maps.o[tt.seg];
+            const CUtensorMap *mo = &maps.o[tt.cell][tt.seg];
             const int orow = m0 - (tt.seg == 2 ? p.seg_row0[2] : tt.seg == 1 ? p.seg_row0[1] : p.seg_row0[0]) +
                              32 * q;   // this warp's first output row
             if (!wait(S::AFULL + buf, (lt >> 1) & 1)) break;
@@ -473,10 +489,10 @@ bool gmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, co
 
 bool al(const void *p, uintptr_t n) { return ((uintptr_t)p & (n - 1)) == 0; }
 
-template <bool kTmaIn, typename S, int kMinBlocks>
-cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmParams &p, cudaStream_t s)
+template <bool kTmaIn, typename S, int kMinBlocks, int NC = 1>
+cudaError_t launch_gemm_t(const GemmMapsN<NC> &maps, const GemmParams &p, cudaStream_t s)
 {
-    auto kern = project_gemm_kernel<kTmaIn, S, kMinBlocks>;
+    auto kern = project_gemm_kernel<kTmaIn, S, kMinBlocks, NC>;
     static std::atomic<uint64_t> opted{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -520,6 +536,8 @@ bool gemm_count_tiles(GemmParams &p)
     }
     if (tiles > INT32_MAX) return false;
     p.tiles = (int)tiles;
+    p.tiles_cell = p.tiles;
+    p.ncell = 1;
     return true;
 }
 
@@ -567,8 +585,8 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
     if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
     GemmMaps maps;
     memset(&maps, 0, sizeof(maps));
-    if (tma_in && (!gemm_xmap(&maps.x, x, p) || !gemm_wmap(&maps.w[0], w, p))) return cudaErrorInvalidValue;
-    if (p.tma_out && !gemm_omap(&maps.o[0], out, rows, p)) return cudaErrorInvalidValue;
+    if (tma_in && (!gemm_xmap(&maps.x[0], x, p) || !gemm_wmap(&maps.w[0][0], w, p))) return cudaErrorInvalidValue;
+    if (p.tma_out && !gemm_omap(&maps.o[0][0], out, rows, p)) return cudaErrorInvalidValue;
     return tma_in ? launch_gemm_t<true, SmemTma, 1>(maps, p, s) : launch_gemm_t<false, SmemCpa, 2>(maps, p, s);
 }
 
@@ -604,10 +622,10 @@ cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq
         if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
         GemmMaps maps;
         memset(&maps, 0, sizeof(maps));
-        if (!gemm_xmap(&maps.x, x, p) || !gemm_wmap(&maps.w[0], wk, p) || !gemm_wmap(&maps.w[1], wv, p) ||
-            !gemm_omap(&maps.o[0], k, rows, p) || !gemm_omap(&maps.o[1], v, rows, p))
+        if (!gemm_xmap(&maps.x[0], x, p) || !gemm_wmap(&maps.w[0][0], wk, p) || !gemm_wmap(&maps.w[0][1], wv, p) ||
+            !gemm_omap(&maps.o[0][0], k, rows, p) || !gemm_omap(&maps.o[0][1], v, rows, p))
             return cudaErrorInvalidValue;
-        if (q_in && (!gemm_wmap(&maps.w[2], wq, p) || !gemm_omap(&maps.o[2], q, rows - q_row0, p)))
+        if (q_in && (!gemm_wmap(&maps.w[0][2], wq, p) || !gemm_omap(&maps.o[0][2], q, rows - q_row0, p)))
             return cudaErrorInvalidValue;
         e = launch_gemm_t<true, SmemTma, 1>(maps, p, s);
         q_done = q_in;
@@ -619,6 +637,67 @@ cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq
         e = launch_project_gemm((const __nv_bfloat16 *)x + (size_t)q_row0 * d_in, wq, q, rows - q_row0, d_in, heads,
                                 d_head, d_pad, s);
     return e;
+}
+
+// Several layer calls' q, k, v projections of one shape in one launch
+// (cells c = 0..n-1: k_c = x_c W_k,c^T, v_c = x_c W_v,c^T, q_c = x_c[q_row0..]
+// W_q,c^T), when every operand is TMA-addressable and q's first row starts a
+// 128-row block; otherwise each cell as launch_project_qkv runs it.  Up to
+// GCELLS cells per launch.
+cudaError_t launch_project_qkv_cells(int n, const void *const *x, const void *const *wq, const void *const *wk,
+                                     const void *const *wv, void *const *q, void *const *k, void *const *v,
+                                     int rows, int d_in, int q_row0, int heads, int d_head, int d_pad, cudaStream_t s)
+{
+    const bool with_q = wq != nullptr && rows > q_row0;
+    const int n_out = heads * d_pad;
+    bool ok = d_in % 8 == 0 && (n_out * 2) % 16 == 0 && d_pad <= 256 && (!with_q || q_row0 % GM == 0);
+    for (int c = 0; ok && c < n; ++c) {
+        ok = al(x[c], 16) && al(wk[c], 16) && al(wv[c], 16) && al(k[c], 16) && al(v[c], 16);
+        if (with_q) ok = ok && al(wq[c], 16) && al(q[c], 16);
+    }
+    GemmParams p;
+    if (ok) {
+        gemm_shape(p, rows, d_in, heads, d_head, d_pad, SmemTma::GBN);
+        ok = p.bn % d_pad == 0;
+    }
+    if (!ok || n < 2) {
+        for (int c = 0; c < n; ++c) {
+            const cudaError_t e = launch_project_qkv(x[c], rows, d_in, wq ? wq[c] : nullptr, wk[c], wv[c],
+                                                     q ? q[c] : nullptr, k[c], v[c], q_row0, heads, d_head, d_pad, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    p.tma_out = 1;
+    p.nseg = with_q ? 3 : 2;
+    p.seg_fb[2] = with_q ? q_row0 / GM : 0;
+    p.seg_row0[2] = with_q ? q_row0 : 0;
+    if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
+    const int per = p.tiles;
+    for (int c0 = 0; c0 < n; c0 += GCELLS) {
+        const int nc = n - c0 < GCELLS ? n - c0 : GCELLS;
+        if ((long)per * nc > INT32_MAX) return cudaErrorNotSupported;
+        p.x = (const __nv_bfloat16 *)x[c0];
+        p.w = (const __nv_bfloat16 *)wk[c0];
+        p.out = (__nv_bfloat16 *)k[c0];
+        p.tiles_cell = per;
+        p.tiles = per * nc;
+        p.ncell = nc;
+        GemmMapsN<GCELLS> maps;
+        memset(&maps, 0, sizeof(maps));
+        for (int c = 0; c < nc; ++c) {
+            const int g = c0 + c;
+            if (!gemm_xmap(&maps.x[c], x[g], p) || !gemm_wmap(&maps.w[c][0], wk[g], p) ||
+                !gemm_wmap(&maps.w[c][1], wv[g], p) || !gemm_omap(&maps.o[c][0], k[g], rows, p) ||
+                !gemm_omap(&maps.o[c][1], v[g], rows, p))
+                return cudaErrorInvalidValue;
+            if (with_q && (!gemm_wmap(&maps.w[c][2], wq[g], p) || !gemm_omap(&maps.o[c][2], q[g], rows - q_row0, p)))
+                return cudaErrorInvalidValue;
+        }
+        const cudaError_t e = launch_gemm_t<true, SmemTma, 1, GCELLS>(maps, p, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // =========================================================================
@@ -854,6 +933,68 @@ txl_status txl_project_qkv(const void *x, int rows, int d_in, const void *w_q, c
         st = txl_project_heads((const unsigned char *)x + (size_t)q_row0 * d_in * esz, w_q, q, rows - q_row0, d_in,
                                heads, d_head, d_pad, dtype, stream);
     return st;
+}
+
+txl_status txl_project_qkv_cells(int cells, const void *const *x, const void *const *w_q, const void *const *w_k,
+                                 const void *const *w_v, void *const *q, void *const *k, void *const *v, int rows,
+                                 int d_in, int q_row0, int heads, int d_head, int d_pad, txl_dtype dtype, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (cells < 0 || rows < 0 || d_in < 0 || heads < 0 || d_head < 1 || d_pad < d_head) return TXL_ERR_INVALID;
+    if ((w_q == nullptr) != (q == nullptr)) return TXL_ERR_INVALID;
+    if (w_q && (q_row0 < 0 || q_row0 > rows)) return TXL_ERR_INVALID;
+    if (cells == 0 || rows == 0 || heads == 0) return TXL_OK;
+    if (!x || !w_k || !w_v || !k || !v) return TXL_ERR_INVALID;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if ((long)heads * d_pad > INT32_MAX || (long)heads * d_head > INT32_MAX) return TXL_ERR_UNSUPPORTED;
+    const size_t row_b = (size_t)heads * d_pad * esz, nw = (size_t)d_in * heads * d_head * esz;
+    const size_t nx = (size_t)rows * d_in * esz, nkv = (size_t)rows * row_b;
+    const size_t nq = w_q ? (size_t)(rows - q_row0) * row_b : 0;
+    for (int c = 0; c < cells; ++c) {
+        if (!x[c] || !w_k[c] || !w_v[c] || !k[c] || !v[c]) return TXL_ERR_INVALID;
+        if (w_q && (!w_q[c] || !q[c])) return TXL_ERR_INVALID;
+        if (!al(x[c], esz) || !al(w_k[c], esz) || !al(w_v[c], esz) || !al(k[c], esz) || !al(v[c], esz))
+            return TXL_ERR_INVALID;
+        if (w_q && (!al(w_q[c], esz) || !al(q[c], esz))) return TXL_ERR_INVALID;
+    }
+    // every output apart from every input and every other output
+    for (int c = 0; c < cells; ++c) {
+        const void *outs[3] = {k[c], v[c], w_q ? q[c] : nullptr};
+        const size_t nout[3] = {nkv, nkv, nq};
+        for (int o = 0; o < 3; ++o) {
+            if (!outs[o] || nout[o] == 0) continue;
+            for (int c2 = 0; c2 < cells; ++c2) {
+                const void *ins[4] = {x[c2], w_k[c2], w_v[c2], w_q ? w_q[c2] : nullptr};
+                const size_t nin[4] = {nx, nw, nw, w_q ? nw : 0};
+                for (int i = 0; i < 4; ++i)
+                    if (ins[i] && nin[i] && overlap_bytes(outs[o], nout[o], ins[i], nin[i])) return TXL_ERR_INVALID;
+                const void *outs2[3] = {k[c2], v[c2], w_q ? q[c2] : nullptr};
+                for (int o2 = 0; o2 < 3; ++o2) {
+                    if ((c2 == c && o2 == o) || !outs2[o2] || nout[o2] == 0) continue;
+                    if (overlap_bytes(outs[o], nout[o], outs2[o2], nout[o2])) return TXL_ERR_INVALID;
+                }
+            }
+        }
+    }
+    bool grouped = dtype == TXL_BF16 && d_in > 0 && d_in % 2 == 0 && (long)heads * d_head * d_in <= INT32_MAX;
+    for (int c = 0; grouped && c < cells; ++c)
+        grouped = al(x[c], 4) && al(w_k[c], 4) && al(w_v[c], 4) && (!w_q || al(w_q[c], 4));
+    if (grouped) {
+        const cudaError_t e = launch_project_qkv_cells(cells, x, w_q, w_k, w_v, q, k, v, rows, d_in, q_row0, heads,
+                                                       d_head, d_pad, (cudaStream_t)stream);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return TXL_ERR_CUDA;
+        }
+        return TXL_OK;
+    }
+    for (int c = 0; c < cells; ++c) {
+        const txl_status st = txl_project_qkv(x[c], rows, d_in, w_q ? w_q[c] : nullptr, w_k[c], w_v[c],
+                                              w_q ? q[c] : nullptr, k[c], v[c], q_row0, heads, d_head, d_pad, dtype,
+                                              stream);
+        if (st != TXL_OK) return st;
+    }
+    return TXL_OK;
 }
 
 txl_status txl_rel_table(const void *w_r, void *out, int klen, int d_model, int heads, int d_head, int d_pad,
