@@ -161,6 +161,36 @@ txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, con
                                 void *mem_next, const void *ext_ctx, int d_model, void *stream);
 
 /*
+ * txl_rel_attn_fwd_mem_cells -- several independent txl_rel_attn_fwd_mem
+ * calls of one shape (e.g. the layer calls of one step of a layer-by-segment
+ * wavefront: different layers, different segments, none waiting for
+ * another's result).  Call c takes q[c], k[c], v[c], r[c], u_bias[c],
+ * v_bias[c], out[c], mem_next[c] and ext_ctx[c], each as
+ * txl_rel_attn_fwd_mem takes it; batch, mem_len, seg_len, heads, d_head,
+ * dtype and d_model are shared.  The results are exactly those of the calls
+ * one after another.  With bf16 and d_head = 64, unsplit calls with TMA-
+ * addressable operands share launches (up to 8 calls a launch, their work
+ * items in one persistent schedule, each call's rollover inside where it
+ * fuses); other shapes run call by call.
+ *
+ * cells           : number of calls, >= 0 (0: nothing).
+ * q .. ext_ctx    : host arrays of `cells` device pointers.  u_bias, v_bias
+ *                   may be NULL (no bias in any call) or hold NULL entries;
+ *                   mem_next and ext_ctx may be NULL when there is nothing to
+ *                   roll (batch, mem_len or d_model 0); the others are
+ *                   required when there is attention work.
+ * Errors: every call's txl_rel_attn_fwd_mem checks, plus TXL_ERR_INVALID
+ * when one call's out or mem_next overlaps any buffer of another call.
+ * Nothing is launched when an argument is rejected.
+ */
+txl_status txl_rel_attn_fwd_mem_cells(int cells, const void *const *q, const void *const *k,
+                                      const void *const *v, const void *const *r,
+                                      const float *const *u_bias, const float *const *v_bias, int batch,
+                                      int mem_len, int seg_len, int heads, int d_head, txl_dtype dtype,
+                                      void *const *out, void *const *mem_next, const void *const *ext_ctx,
+                                      int d_model, void *stream);
+
+/*
  * txl_rel_attn_fwd_ring -- txl_rel_attn_fwd with k and v stored as a ring.
  * The extended context [memory; segment] of Section 3.2 slides forward by L
  * rows per segment; kept in a ring of M+L rows, a segment adds only its L new

@@ -263,3 +263,33 @@ def test_selftest_wait_rejects_bad_limits(lib):
     # the limit is checked on the host before anything is launched
     assert lib.txl_selftest_wait(0, None) == INVALID
     assert lib.txl_selftest_wait(1000001, None) == INVALID
+
+
+def _attn_mem_cells(n=2, dt=1, B=2, M=8, L=8, H=2, D=16, dm=32, swap=None, cells=None):
+    """n calls of _attn_mem's shape, call c's buffers FAKE * (16 c + 1 ..)
+    (none overlapping); ``swap`` = (name, c, value) replaces one pointer."""
+    names = ("q", "k", "v", "r", "u", "w", "out", "mem_next", "ext")
+    ptrs = {nm: [FAKE * (16 * c + 1 + x) for c in range(n)] for x, nm in enumerate(names)}
+    if swap:
+        ptrs[swap[0]][swap[1]] = swap[2]
+    arr = lambda xs: (ctypes.c_void_p * n)(*xs)
+    return abi.load_library().txl_rel_attn_fwd_mem_cells(
+        n if cells is None else cells, *(arr(ptrs[nm]) for nm in names[:6]), B, M, L, H, D, dt,
+        arr(ptrs["out"]), arr(ptrs["mem_next"]), arr(ptrs["ext"]), dm, None)
+
+
+def test_attn_mem_cells_rejects_bad_arguments(lib):
+    assert _attn_mem_cells(dt=7) == UNSUPPORTED
+    assert _attn_mem_cells(cells=-1) == INVALID
+    assert _attn_mem_cells(cells=0) == OK                          # no calls: nothing looked at
+    assert _attn_mem_cells(dm=-1) == INVALID
+    assert _attn_mem_cells(D=65) == UNSUPPORTED                    # every call's own checks
+    assert _attn_mem_cells(swap=("q", 1, FAKE * 17 + 2)) == INVALID            # call 1 misaligned
+    assert _attn_mem_cells(swap=("mem_next", 1, FAKE * 8)) == INVALID          # call 1's mem_next is call 0's
+    assert _attn_mem_cells(swap=("out", 1, FAKE * 2 + 64)) == INVALID          # call 1 writes call 0's k
+    assert _attn_mem_cells(swap=("mem_next", 1, FAKE * 9 + 32)) == INVALID     # ... call 0's ext_ctx
+    # reads may be shared: both calls on one table and one q
+    assert _attn_mem_cells(swap=("r", 1, FAKE * 4)) == CUDA
+    assert _attn_mem_cells(swap=("q", 1, FAKE * 1)) == CUDA
+    # valid arguments reach the device (none here)
+    assert _attn_mem_cells(n=3) == CUDA

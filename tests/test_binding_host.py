@@ -135,3 +135,23 @@ def test_project_qkv_cells_checks():
     with pytest.raises(ValueError, match=ON_DEVICE):
         txl.project_qkv_cells(xs, ws, ws, ws, heads, d_head, d_pad, q_from=M)
     assert txl.project_qkv_cells([], None, [], [], heads, d_head, d_pad) == ([], [], [])
+
+
+def test_rel_attn_fwd_mem_cells_checks():
+    t = _layer()
+    ext = torch.zeros(T, B, 32, dtype=torch.bfloat16)
+    nxt = torch.zeros(T, B, 32, dtype=torch.bfloat16)
+    one = lambda key: [t[key], t[key]]
+    with pytest.raises(ValueError, match="same length"):
+        txl.rel_attn_fwd_mem_cells(one("q"), one("k"), one("v"), one("r"), one("u"), [t["w"]], M, [nxt, nxt],
+                                   [ext, ext])
+    with pytest.raises(ValueError, match="first call's shape"):
+        txl.rel_attn_fwd_mem_cells([t["q"], t["q"][:1]], one("k"), one("v"), one("r"), one("u"), one("w"), M,
+                                   [nxt, nxt], [ext, ext])
+    with pytest.raises(ValueError, match="ext_ctx must be"):
+        txl.rel_attn_fwd_mem_cells(one("q"), one("k"), one("v"), one("r"), one("u"), one("w"), M, [nxt, nxt],
+                                   [ext, ext[:, :1]])
+    with pytest.raises(ValueError, match=ON_DEVICE):
+        txl.rel_attn_fwd_mem_cells(one("q"), one("k"), one("v"), one("r"), one("u"), one("w"), M, [nxt, nxt],
+                                   [ext, ext])
+    assert txl.rel_attn_fwd_mem_cells([], [], [], [], None, None, M, [], []) == []

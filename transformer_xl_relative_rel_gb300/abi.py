@@ -26,7 +26,7 @@ _lib: Optional[ctypes.CDLL] = None
 EXPORTS = ("txl_rel_attn_fwd", "txl_mem_update", "txl_check", "txl_status_string",
            "txl_last_cuda_error", "txl_version", "txl_shutdown", "txl_rel_attn_fwd_noalloc",
            "txl_rel_attn_fwd_ring", "txl_ring_append", "txl_rel_attn_fwd_padded", "txl_project_heads",
-           "txl_project_qkv", "txl_project_qkv_cells", "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
+           "txl_project_qkv", "txl_project_qkv_cells", "txl_rel_table", "txl_rel_attn_bwd", "txl_rel_attn_bwd_workspace", "txl_rel_attn_fwd_lse", "txl_rel_attn_fwd_mem", "txl_rel_attn_fwd_mem_cells", "txl_rel_attn_fwd_plan", "txl_selftest_wait")
 
 
 class TxlError(RuntimeError):
@@ -58,6 +58,9 @@ def load_library() -> ctypes.CDLL:
     lib.txl_rel_attn_fwd_plan.restype = i
     lib.txl_rel_attn_fwd_mem.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, i, vp]
     lib.txl_rel_attn_fwd_mem.restype = i
+    pp = ctypes.POINTER(vp)
+    lib.txl_rel_attn_fwd_mem_cells.argtypes = [i, pp, pp, pp, pp, pp, pp, i, i, i, i, i, i, pp, pp, pp, i, vp]
+    lib.txl_rel_attn_fwd_mem_cells.restype = i
     lib.txl_rel_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.txl_rel_attn_fwd_noalloc.restype = i
     lib.txl_rel_attn_fwd_ring.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
@@ -212,6 +215,44 @@ def rel_attn_fwd_mem(q, k, v, r, u_bias, v_bias, mem_len: int, mem_next, ext_ctx
         B, mem_len, L, H, D, _dtype_code(q), _ptr(out), _ptr(mem_next), _ptr(ext_ctx), dm, _stream_ptr(stream))
     _raise(st, "txl_rel_attn_fwd_mem")
     return out
+
+
+def rel_attn_fwd_mem_cells(qs, ks, vs, rs, us, ws, mem_len: int, mem_nexts, ext_ctxs, outs=None, stream=None):
+    """Several independent ``rel_attn_fwd_mem`` calls of one shape
+    (txl_rel_attn_fwd_mem_cells): lists of equal length, call c taking
+    qs[c] .. ext_ctxs[c] (``us``/``ws`` may be None, or hold None entries).
+    Returns the list of outputs."""
+    n = len(qs)
+    lists = [ks, vs, rs, mem_nexts, ext_ctxs] + [x for x in (us, ws, outs) if x is not None]
+    if any(len(x) != n for x in lists):
+        raise ValueError("the calls' lists must have the same length")
+    if n == 0:
+        return []
+    L, B, H, D = qs[0].shape
+    dm = ext_ctxs[0].shape[2] if ext_ctxs[0].dim() == 3 else -1
+    for c in range(n):
+        if tuple(qs[c].shape) != (L, B, H, D) or qs[c].dtype != qs[0].dtype:
+            raise ValueError("every call's q must have the first call's shape and dtype")
+        if tuple(ext_ctxs[c].shape) != (mem_len + L, B, dm):
+            raise ValueError(f"ext_ctx must be [{mem_len + L}, {B}, {dm}] in every call")
+    res = []
+    for c in range(n):
+        u = None if us is None else us[c]
+        w = None if ws is None else ws[c]
+        out = _check_attn(qs[c], ks[c], vs[c], rs[c], u, w, mem_len, None if outs is None else outs[c])
+        ext, nxt = ext_ctxs[c], mem_nexts[c]
+        for name, t in (("ext_ctx", ext), ("mem_next", nxt)):
+            if t.dtype != qs[0].dtype or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor typed like q")
+        if nxt.numel() < mem_len * B * dm:
+            raise ValueError(f"mem_next must hold at least [{mem_len}, {B}, {dm}]")
+        res.append(out)
+    arr = lambda ts: (ctypes.c_void_p * n)(*[_ptr(t) for t in ts])
+    st = load_library().txl_rel_attn_fwd_mem_cells(
+        n, arr(qs), arr(ks), arr(vs), arr(rs), None if us is None else arr(us), None if ws is None else arr(ws),
+        B, mem_len, L, H, D, _dtype_code(qs[0]), arr(res), arr(mem_nexts), arr(ext_ctxs), dm, _stream_ptr(stream))
+    _raise(st, "txl_rel_attn_fwd_mem_cells")
+    return res
 
 
 def rel_attn_bwd_workspace_bytes(batch: int, mem_len: int, seg_len: int, heads: int, d_head: int,

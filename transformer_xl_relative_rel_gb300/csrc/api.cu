@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "internal.h"
 #include "txl.h"
@@ -144,11 +145,11 @@ using namespace txl;
 
 extern "C" {
 
-static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
-                                  const float *u_bias, const float *v_bias, int batch, int mem_len,
-                                  int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
-                                  void *out, void *stream, int scale_d = 0, float *lse = nullptr,
-                                  const void *roll_src = nullptr, void *roll_dst = nullptr, size_t roll_bytes = 0)
+// The argument checks of an attention call (no launch); TXL_OK also for an
+// empty call (batch, seg_len or heads 0), whose pointers are not looked at.
+static txl_status attn_checks(const void *q, const void *k, const void *v, const void *r, const float *u_bias,
+                              const float *v_bias, int batch, int mem_len, int seg_len, int heads, int d_head,
+                              int kv_start, txl_dtype dtype, const void *out, const float *lse)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1) return TXL_ERR_INVALID;
@@ -182,6 +183,20 @@ static txl_status rel_attn_common(const void *q, const void *k, const void *v, c
             overlaps(lse, nl, v, nk) || overlaps(lse, nl, r, nr))
             return TXL_ERR_INVALID;
     }
+    return TXL_OK;
+}
+
+static txl_status rel_attn_common(const void *q, const void *k, const void *v, const void *r,
+                                  const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                  int seg_len, int heads, int d_head, int kv_start, txl_dtype dtype,
+                                  void *out, void *stream, int scale_d = 0, float *lse = nullptr,
+                                  const void *roll_src = nullptr, void *roll_dst = nullptr, size_t roll_bytes = 0)
+{
+    const txl_status st = attn_checks(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, kv_start,
+                                      dtype, out, lse);
+    if (st != TXL_OK) return st;
+    if (batch == 0 || seg_len == 0 || heads == 0) return TXL_OK;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
 
     // an absent bias drops its term (terms (a) + (b) only: Shaw et al.'s form)
     if (!u_bias || !v_bias) {
@@ -287,38 +302,58 @@ txl_status txl_rel_attn_fwd_plan(int batch, int mem_len, int seg_len, int heads,
     return TXL_OK;
 }
 
-txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, const void *r,
-                                const float *u_bias, const float *v_bias, int batch, int mem_len,
-                                int seg_len, int heads, int d_head, txl_dtype dtype, void *out,
-                                void *mem_next, const void *ext_ctx, int d_model, void *stream)
+}  // extern "C"
+
+// The rollover half of a txl_rel_attn_fwd_mem call: its checks, and the
+// copy's source and size (0 bytes: nothing to roll).
+static txl_status mem_checks(const void *q, const void *k, const void *v, const void *r, const float *u_bias,
+                             const float *v_bias, int batch, int mem_len, int seg_len, int heads, int d_head,
+                             txl_dtype dtype, const void *out, const void *mem_next, const void *ext_ctx,
+                             int d_model, const void **src, size_t *nbytes)
 {
     if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
     if (batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1 || d_model < 0) return TXL_ERR_INVALID;
     const size_t esz = dtype == TXL_F32 ? 4 : 2;
-    // the rollover's part: as txl_mem_update
-    size_t nbytes = 0;
-    const void *src = nullptr;
+    *src = nullptr;
+    *nbytes = 0;
     if (batch > 0 && mem_len > 0 && d_model > 0) {
         if (!mem_next || !ext_ctx) return TXL_ERR_INVALID;
         if (!aligned(mem_next, esz) || !aligned(ext_ctx, esz)) return TXL_ERR_INVALID;
         const size_t row = (size_t)batch * (size_t)d_model * esz;
         if (row / esz / (size_t)batch != (size_t)d_model) return TXL_ERR_UNSUPPORTED;
         const size_t T = (size_t)mem_len + (size_t)seg_len;
-        nbytes = (size_t)mem_len * row;
-        if (overlaps(mem_next, nbytes, ext_ctx, T * row)) return TXL_ERR_INVALID;
+        const size_t n = (size_t)mem_len * row;
+        if (overlaps(mem_next, n, ext_ctx, T * row)) return TXL_ERR_INVALID;
         // and the attention's: mem_next overlaps none of its buffers, ext_ctx not its output
-        if (batch > 0 && seg_len > 0 && heads > 0) {
+        if (seg_len > 0 && heads > 0) {
             const size_t hrow = (size_t)batch * (size_t)heads * (size_t)d_head * esz;
             const size_t nq = (size_t)seg_len * hrow, nk = T * hrow, nr = T * (size_t)heads * d_head * esz;
             const size_t nb = (size_t)heads * d_head * 4;
-            if (overlaps(mem_next, nbytes, q, nq) || overlaps(mem_next, nbytes, k, nk) ||
-                overlaps(mem_next, nbytes, v, nk) || overlaps(mem_next, nbytes, r, nr) ||
-                overlaps(mem_next, nbytes, out, nq) || overlaps(mem_next, nbytes, u_bias, nb) ||
-                overlaps(mem_next, nbytes, v_bias, nb) || overlaps(ext_ctx, T * row, out, nq))
+            if (overlaps(mem_next, n, q, nq) || overlaps(mem_next, n, k, nk) || overlaps(mem_next, n, v, nk) ||
+                overlaps(mem_next, n, r, nr) || overlaps(mem_next, n, out, nq) ||
+                overlaps(mem_next, n, u_bias, nb) || overlaps(mem_next, n, v_bias, nb) ||
+                overlaps(ext_ctx, T * row, out, nq))
                 return TXL_ERR_INVALID;
         }
-        src = (const unsigned char *)ext_ctx + (size_t)seg_len * row;
+        *src = (const unsigned char *)ext_ctx + (size_t)seg_len * row;
+        *nbytes = n;
     }
+    return TXL_OK;
+}
+
+extern "C" {
+
+txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, const void *r,
+                                const float *u_bias, const float *v_bias, int batch, int mem_len,
+                                int seg_len, int heads, int d_head, txl_dtype dtype, void *out,
+                                void *mem_next, const void *ext_ctx, int d_model, void *stream)
+{
+    const void *src = nullptr;
+    size_t nbytes = 0;
+    const txl_status st = mem_checks(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, dtype,
+                                     out, mem_next, ext_ctx, d_model, &src, &nbytes);
+    if (st != TXL_OK) return st;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
     if (batch == 0 || seg_len == 0 || heads == 0) {
         // no attention work: the rollover alone
         if (!nbytes) return TXL_OK;
@@ -327,6 +362,88 @@ txl_status txl_rel_attn_fwd_mem(const void *q, const void *k, const void *v, con
     }
     return rel_attn_common(q, k, v, r, u_bias, v_bias, batch, mem_len, seg_len, heads, d_head, 0, dtype, out,
                            stream, 0, nullptr, src, nbytes ? mem_next : nullptr, nbytes);
+}
+
+txl_status txl_rel_attn_fwd_mem_cells(int cells, const void *const *q, const void *const *k, const void *const *v,
+                                      const void *const *r, const float *const *u_bias,
+                                      const float *const *v_bias, int batch, int mem_len, int seg_len, int heads,
+                                      int d_head, txl_dtype dtype, void *const *out, void *const *mem_next,
+                                      const void *const *ext_ctx, int d_model, void *stream)
+{
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    if (cells < 0 || batch < 0 || mem_len < 0 || seg_len < 0 || heads < 0 || d_head < 1 || d_model < 0)
+        return TXL_ERR_INVALID;
+    if (cells == 0) return TXL_OK;
+    const bool attend = batch > 0 && seg_len > 0 && heads > 0, roll = batch > 0 && mem_len > 0 && d_model > 0;
+    if ((attend && (!q || !k || !v || !r || !out)) || (roll && (!mem_next || !ext_ctx))) return TXL_ERR_INVALID;
+    auto at = [](const void *const *a, int c) { return a ? a[c] : nullptr; };
+    auto atf = [](const float *const *a, int c) { return a ? a[c] : nullptr; };
+    auto atw = [](void *const *a, int c) { return a ? a[c] : nullptr; };
+    // every call as txl_rel_attn_fwd_mem checks it
+    size_t nbytes = 0;
+    for (int c = 0; c < cells; ++c) {
+        const void *src = nullptr;
+        txl_status st = mem_checks(at(q, c), at(k, c), at(v, c), at(r, c), atf(u_bias, c), atf(v_bias, c), batch,
+                                   mem_len, seg_len, heads, d_head, dtype, at(out, c), at(mem_next, c),
+                                   at(ext_ctx, c), d_model, &src, &nbytes);
+        if (st == TXL_OK)
+            st = attn_checks(at(q, c), at(k, c), at(v, c), at(r, c), atf(u_bias, c), atf(v_bias, c), batch, mem_len,
+                             seg_len, heads, d_head, 0, dtype, at(out, c), nullptr);
+        if (st != TXL_OK) return st;
+    }
+    // the calls are independent: what one writes (out, mem_next) meets
+    // nothing another reads or writes
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    const size_t T = (size_t)mem_len + (size_t)seg_len;
+    const size_t hrow = (size_t)batch * (size_t)heads * (size_t)d_head * esz;
+    const size_t nq = attend ? (size_t)seg_len * hrow : 0, nk = attend ? T * hrow : 0;
+    const size_t nr = attend ? T * (size_t)heads * d_head * esz : 0, nb = attend ? (size_t)heads * d_head * 4 : 0;
+    const size_t next = roll ? T * (size_t)batch * (size_t)d_model * esz : 0;
+    for (int c = 0; c < cells; ++c) {
+        const void *wr[2] = {at(out, c), at(mem_next, c)};
+        const size_t nw[2] = {nq, nbytes};
+        for (int d = 0; d < cells; ++d) {
+            if (d == c) continue;
+            const void *bufs[9] = {at(q, d), at(k, d), at(v, d), at(r, d), atf(u_bias, d), atf(v_bias, d),
+                                   at(out, d), at(mem_next, d), at(ext_ctx, d)};
+            const size_t nbuf[9] = {nq, nk, nk, nr, nb, nb, nq, nbytes, next};
+            for (int x = 0; x < 2; ++x)
+                for (int y = 0; y < 9; ++y)
+                    if (overlaps(wr[x], nw[x], bufs[y], nbuf[y])) return TXL_ERR_INVALID;
+        }
+    }
+    // bf16 with 64-wide heads: the calls share launches
+    if (attend && dtype == TXL_BF16 && d_head == 64 && cells >= 2) {
+        const float *z = nullptr;
+        bool zero_ok = true;
+        for (int c = 0; c < cells && zero_ok; ++c)
+            if (!atf(u_bias, c) || !atf(v_bias, c)) zero_ok = zero_bias((size_t)heads * d_head, &z) == cudaSuccess;
+        if (zero_ok) {
+            AttnArgs *args = new (std::nothrow) AttnArgs[cells];
+            if (!args) return TXL_ERR_UNSUPPORTED;
+            const size_t row = roll ? (size_t)batch * (size_t)d_model * esz : 0;
+            for (int c = 0; c < cells; ++c) {
+                AttnArgs &a = args[c];
+                a = AttnArgs{q[c], k[c], v[c], r[c], atf(u_bias, c) ? u_bias[c] : z, atf(v_bias, c) ? v_bias[c] : z,
+                             out[c], batch, heads, d_head, seg_len, mem_len, 0, 0};
+                if (nbytes) {
+                    a.roll_src = (const unsigned char *)ext_ctx[c] + (size_t)seg_len * row;
+                    a.roll_dst = mem_next[c];
+                    a.roll_bytes = nbytes;
+                }
+            }
+            const cudaError_t e = launch_attn_bf16_cells(cells, args, (cudaStream_t)stream);
+            delete[] args;
+            if (e != cudaErrorNotSupported) return e == cudaSuccess ? TXL_OK : cuda_fail(e);
+        }
+    }
+    for (int c = 0; c < cells; ++c) {
+        const txl_status st = txl_rel_attn_fwd_mem(at(q, c), at(k, c), at(v, c), at(r, c), atf(u_bias, c),
+                                                   atf(v_bias, c), batch, mem_len, seg_len, heads, d_head, dtype,
+                                                   atw(out, c), atw(mem_next, c), at(ext_ctx, c), d_model, stream);
+        if (st != TXL_OK) return st;
+    }
+    return TXL_OK;
 }
 
 txl_status txl_rel_attn_fwd_lse(const void *q, const void *k, const void *v, const void *r,

@@ -96,13 +96,28 @@ struct Params {
     int items;          // B*H*nqt*splits work items
     int streamk, sk_nt; // stream-K schedule (splits = 2 partial slots), key tiles per item
     int kv_start;       // K, V rows form a ring: key j at row (kv_start + j) mod T
-    int ost;            // 1: output tiles written by TMA store (tensor map tm_o)
+    int ost;            // 1: output tiles written by TMA store (the output's tensor map)
     float sl2;          // log2(e) / sqrt(D)
     // the memory rollover copied by warp 3 of every CTA (its slice of
     // roll_n16 16-byte units), 0 units when not fused
     const uint4 *roll_src;
     uint4 *roll_dst;
     long roll_n16;
+    // several calls of one shape in one launch (kernel instantiations with
+    // NC > 1): ncell calls, each with its own tensor maps, biases and
+    // rollover (roll_n16 units each); the fields above are the first call's
+    int ncell;
+    const float *cell_u[ATTN_CELLS], *cell_w[ATTN_CELLS];
+    const uint4 *cell_roll_src[ATTN_CELLS];
+    uint4 *cell_roll_dst[ATTN_CELLS];
+};
+
+// The tensor maps of a launch: per call K, V, the table, q and the output
+// (NC calls), and the 8-row K, V boxes of a ring (one call only).
+template <int NC>
+struct AttnMaps {
+    CUtensorMap k[NC], v[NC], r[NC], q[NC], o[NC];
+    CUtensorMap k8, v8;
 };
 
 // Every operand tile in shared memory uses 128-byte rows with the 128-byte
@@ -274,10 +289,11 @@ __device__ __forceinline__ void warp_load_rows(unsigned char *dst, int nrows, co
 
 // One work item: 128 query rows of one (b, h) and one key-range split of
 // them.  Items are numbered heaviest first (query tiles from the last one
-// down); CTA c of G takes items c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the
-// sorted list, so that every CTA gets a similar total of key tiles).
+// down; see make_item for launches of several calls); CTA c of G takes items
+// c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the sorted list, so that every
+// CTA gets a similar total of key tiles).
 struct Item {
-    int bh, b, h, i0, rows_here, split, t0, N, kb0;
+    int cell, bh, b, h, i0, rows_here, split, t0, N, kb0;
     int whole;          // the item's output is final (else a partial: key split or cut item)
     long head_off;
 };
@@ -285,9 +301,20 @@ struct Item {
 __device__ __forceinline__ Item make_item(const Params &p, int k)
 {
     Item it;
-    const int per_qt = p.B * p.H * p.splits;
-    const int qt = p.nqt - 1 - k / per_qt;
-    const int rem = k % per_qt;
+    // The calls of a multi-call launch follow one another.  Inside a call the
+    // query tiles go heaviest first in the last call and in every second call
+    // before it, lightest first in the others, so that light items meet
+    // light ones at the calls' boundaries and the CTAs' totals stay even;
+    // a head's query tiles stay one level (B*H items) apart, so its keys and
+    // values are still in L2 when the next one reads them.
+    const int per_level = p.B * p.H * p.splits;           // one query tile level of one call
+    const int nc = p.ncell > 1 ? p.ncell : 1;
+    const int per_call = per_level * p.nqt;
+    it.cell = k / per_call;
+    const int kk = k % per_call;
+    const bool heavy_first = ((nc - 1 - it.cell) & 1) == 0;
+    const int qt = heavy_first ? p.nqt - 1 - kk / per_level : kk / per_level;
+    const int rem = kk % per_level;
     it.bh = rem / p.splits;
     it.split = rem % p.splits;
     it.b = it.bh / p.H;
@@ -320,6 +347,7 @@ __device__ __forceinline__ int streamk_item(const Params &p, int j, Item &it)
     const long s0 = c * tt / G, s1 = (c + 1) * tt / G;
     const long k = s0 / nt + j;
     if (s1 <= s0 || k * nt >= s1) return -1;
+    it.cell = 0;
     const long a = (s0 > k * nt ? s0 : k * nt) - k * nt;
     const long e = (s1 < (k + 1) * nt ? s1 : (k + 1) * nt) - k * nt;
     it.bh = (int)k;
@@ -357,12 +385,16 @@ __device__ __forceinline__ int next_busy(const Params &p, int j, Item &it)
     }
 }
 
-template <int DP, bool kTma, bool kSK>
+// the call an item belongs to (always the first in one-call launches)
+template <int NC>
+__device__ __forceinline__ int cell_of(const Item &it)
+{
+    return NC == 1 ? 0 : it.cell;
+}
+
+template <int DP, bool kTma, bool kSK, int NC>
 __global__ void __launch_bounds__(NT, 1)
-rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8,
-                     const __grid_constant__ CUtensorMap tm_o, const Params p)
+rel_attn_bf16_kernel(const __grid_constant__ AttnMaps<NC> tm, const Params p)
 {
     using S = Smem<DP>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -406,15 +438,17 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         mbar_init(bar(S::B_OFR), 1);
         fence_mbar_init();
         if (kTma) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            prefetch_tmap(&tm_r);
-            prefetch_tmap(&tm_q);
-            if (p.kv_start) {
-                prefetch_tmap(&tm_k8);
-                prefetch_tmap(&tm_v8);
+            for (int c = 0; c < (NC == 1 ? 1 : p.ncell); ++c) {
+                prefetch_tmap(&tm.k[c]);
+                prefetch_tmap(&tm.v[c]);
+                prefetch_tmap(&tm.r[c]);
+                prefetch_tmap(&tm.q[c]);
+                if (p.ost) prefetch_tmap(&tm.o[c]);
             }
-            if (p.ost) prefetch_tmap(&tm_o);
+            if (p.kv_start) {
+                prefetch_tmap(&tm.k8);
+                prefetch_tmap(&tm.v8);
+            }
         }
     }
     // the padding of D up to a multiple of 16 (the MMA K step) must be zero in
@@ -440,10 +474,12 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             auto load_q = [&](const Item &it) {
                 if (kTma) {
                     if (lane == 0) {
+                        const int c = cell_of<NC>(it);
+                        const float *u = NC == 1 ? p.u : p.cell_u[c], *w = NC == 1 ? p.w : p.cell_w[c];
                         mbar_arrive_expect_tx(bar(S::B_QRAW), S::TILE + 2 * 64 * 4);
-                        tma_load_3d(sbase + S::QRAW, &tm_q, bar(S::B_QRAW), 0, it.i0, it.bh);
-                        bulk_load(sbase + S::UW, p.u + it.h * p.D, 64 * 4, bar(S::B_QRAW));
-                        bulk_load(sbase + S::UW + 256, p.w + it.h * p.D, 64 * 4, bar(S::B_QRAW));
+                        tma_load_3d(sbase + S::QRAW, &tm.q[c], bar(S::B_QRAW), 0, it.i0, it.bh);
+                        bulk_load(sbase + S::UW, u + it.h * p.D, 64 * 4, bar(S::B_QRAW));
+                        bulk_load(sbase + S::UW + 256, w + it.h * p.D, 64 * 4, bar(S::B_QRAW));
                     }
                 } else if (warp == 0) {
                     warp_load_rows(smem + S::QRAW, BM, p.q, it.head_off + (long)it.i0 * qkv_row, qkv_row, 0,
@@ -459,13 +495,13 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             };
             // table chunk number cg (global count) into ring slot cg % NCH,
             // once the S MMAs of its previous occupant are done (warp 0)
-            auto load_chunk = [&](int cg, int row, int h) {
+            auto load_chunk = [&](int cg, int row, int h, int c) {
                 const int slot = cg % NCH;
                 if (cg >= NCH && !wwait(S::B_CHE + slot, ((cg / NCH) - 1) & 1)) return false;
                 if (kTma) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(bar(S::B_CHF + slot), S::TILE);
-                        tma_load_3d(sbase + S::CH0 + slot * S::TILE, &tm_r, bar(S::B_CHF + slot), 0, row, h);
+                        tma_load_3d(sbase + S::CH0 + slot * S::TILE, &tm.r[c], bar(S::B_CHF + slot), 0, row, h);
                     }
                 } else {
                     warp_load_rows(smem + S::CH0 + slot * S::TILE, BN, p.r, (long)h * p.D, (long)p.H * p.D, row,
@@ -482,7 +518,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             bool ok = true;
             while (ok && j >= 0) {
                 // chunk 0 of the item (its tile n reads chunks n and n+1)
-                if (warp == 0 && !load_chunk(cg, it.kb0, it.h)) break;
+                if (warp == 0 && !load_chunk(cg, it.kb0, it.h, cell_of<NC>(it))) break;
                 ++cg;
                 for (int n = 0; n < it.N; ++n, ++g) {
                     const int st = g % NSTAGE;
@@ -502,8 +538,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                             if (p.kv_start == 0 || s0 + BN <= p.T) {
                                 // one box; in the plain layout rows past the last key
                                 // are zero-filled
-                                tma_load_3d(dst, &tm_k, bar(S::B_FULL + st), 0, s0, it.bh);
-                                tma_load_3d(dst + S::TILE, &tm_v, bar(S::B_FULL + st), 0, s0, it.bh);
+                                tma_load_3d(dst, &tm.k[cell_of<NC>(it)], bar(S::B_FULL + st), 0, s0, it.bh);
+                                tma_load_3d(dst + S::TILE, &tm.v[cell_of<NC>(it)], bar(S::B_FULL + st), 0, s0, it.bh);
                             } else {
                                 // the tile crosses the ring's end: sixteen 8-row boxes
                                 // (one swizzle atom each, 1 KB apart in the stage), each
@@ -511,8 +547,8 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                                 // other ring rows (finite, masked)
                                 for (int m = 0; m < BN / 8; ++m) {
                                     const int sr = (s0 + 8 * m) % p.T;   // T may be below 128
-                                    tma_load_3d(dst + 1024u * m, &tm_k8, bar(S::B_FULL + st), 0, sr, it.bh);
-                                    tma_load_3d(dst + S::TILE + 1024u * m, &tm_v8, bar(S::B_FULL + st), 0, sr,
+                                    tma_load_3d(dst + 1024u * m, &tm.k8, bar(S::B_FULL + st), 0, sr, it.bh);
+                                    tma_load_3d(dst + S::TILE + 1024u * m, &tm.v8, bar(S::B_FULL + st), 0, sr,
                                                 it.bh);
                                 }
                             }
@@ -528,7 +564,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         mbar_arrive(bar(S::B_FULL + st));
                     }
                     // table chunk n+1
-                    if (warp == 0 && !load_chunk(cg, it.kb0 + (n + 1) * BN, it.h)) {
+                    if (warp == 0 && !load_chunk(cg, it.kb0 + (n + 1) * BN, it.h, cell_of<NC>(it))) {
                         ok = false;
                         break;
                     }
@@ -610,7 +646,10 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             // attention: the CTA's contiguous slice of the flat copy,
             // sixteen 16-byte loads in flight per lane, streaming cache hints
             // (the data is used once; the layer's K, V and table stay in L2)
-            if (p.roll_n16 > 0) {
+            // (each call's copy of a multi-call launch in turn)
+            for (int c = 0; p.roll_n16 > 0 && c < (NC == 1 ? 1 : p.ncell); ++c) {
+                const uint4 *src = NC == 1 ? p.roll_src : p.cell_roll_src[c];
+                uint4 *dst = NC == 1 ? p.roll_dst : p.cell_roll_dst[c];
                 const long G = gridDim.x, per = (p.roll_n16 + G - 1) / G;
                 const long beg = (long)blockIdx.x * per;
                 const long end = beg + per < p.roll_n16 ? beg + per : p.roll_n16;
@@ -618,11 +657,11 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 for (; x + 15 * 32 < end; x += 16 * 32) {
                     uint4 t[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) t[u] = __ldcs(p.roll_src + x + 32 * u);
+                    for (int u = 0; u < 16; ++u) t[u] = __ldcs(src + x + 32 * u);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) __stcs(p.roll_dst + x + 32 * u, t[u]);
+                    for (int u = 0; u < 16; ++u) __stcs(dst + x + 32 * u, t[u]);
                 }
-                for (; x < end; x += 32) __stcs(p.roll_dst + x, __ldcs(p.roll_src + x));
+                for (; x < end; x += 32) __stcs(dst + x, __ldcs(src + x));
             }
         } else if (warp == 2) {
             // =============================================================== P.V MMAs
@@ -655,9 +694,9 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         }
                         tc_fence_after();
                         // under the stream-K schedule only whole items go
-                        // through the staged tile (tm_o is then the output)
+                        // through the staged tile (the output map is then the output)
                         if (ost && n == 0 && have_prev && (prev.whole || !kSK)) {
-                            tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
+                            tma_store_3d(&tm.o[cell_of<NC>(prev)], sbase + S::OST, 0, prev.i0,
                                          (p.splits > 1 && !kSK) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                             bulk_commit();
                             in_flight = true;
@@ -679,7 +718,7 @@ rel_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         mbar_arrive(bar(S::B_OFR));
                     }
                     if (wait_or_abort(bar(S::B_OST), 0, abort)) {
-                        tma_store_3d(&tm_o, sbase + S::OST, 0, prev.i0,
+                        tma_store_3d(&tm.o[cell_of<NC>(prev)], sbase + S::OST, 0, prev.i0,
                                      (p.splits > 1 && !kSK) ? prev.split * p.B * p.H + prev.bh : prev.bh);
                         bulk_commit();
                     }
@@ -1639,34 +1678,36 @@ bool encode_map(CUtensorMap *m, const void *base, long rows, long row_stride, lo
 
 // Encoded maps of recent calls (a map holds only the address and the shape,
 // so repeated calls on the same buffers reuse it: the encode is a driver call
-// that costs about as much as a short launch).
+// that costs about as much as a short launch).  A direct-mapped table: a
+// key's slot is its hash; a new key takes the slot over.
 struct MapEntry {
+    bool used;
     int dev;
     const void *base;
     long rows, row_stride, groups;
     int box_rows;
     CUtensorMap map;
 };
-constexpr int MAP_CACHE = 64;
+constexpr int MAP_CACHE = 1024;
 std::mutex g_map_mu;
 MapEntry g_maps[MAP_CACHE];
-int g_map_count = 0, g_map_next = 0;
 
 bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long groups, int box_rows)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    uint64_t h = (uint64_t)(uintptr_t)base;
+    for (uint64_t x : {(uint64_t)dev, (uint64_t)rows, (uint64_t)row_stride, (uint64_t)groups, (uint64_t)box_rows})
+        h = (h ^ x) * 0x100000001b3ull;
+    MapEntry &e = g_maps[(h ^ (h >> 29)) % MAP_CACHE];
     std::lock_guard<std::mutex> lock(g_map_mu);
-    for (int x = 0; x < g_map_count; ++x) {
-        const MapEntry &e = g_maps[x];
-        if (e.dev == dev && e.base == base && e.rows == rows && e.row_stride == row_stride &&
-            e.groups == groups && e.box_rows == box_rows) {
-            *m = e.map;
-            return true;
-        }
+    if (e.used && e.dev == dev && e.base == base && e.rows == rows && e.row_stride == row_stride &&
+        e.groups == groups && e.box_rows == box_rows) {
+        *m = e.map;
+        return true;
     }
     if (!encode_map(m, base, rows, row_stride, groups, box_rows)) return false;
-    MapEntry &e = g_maps[g_map_next];
+    e.used = true;
     e.dev = dev;
     e.base = base;
     e.rows = rows;
@@ -1674,18 +1715,14 @@ bool make_map(CUtensorMap *m, const void *base, long rows, long row_stride, long
     e.groups = groups;
     e.box_rows = box_rows;
     e.map = *m;
-    g_map_next = (g_map_next + 1) % MAP_CACHE;
-    if (g_map_count < MAP_CACHE) ++g_map_count;
     return true;
 }
 
-template <int DP, bool kTma, bool kSK>
-cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                     const CUtensorMap &mr, const CUtensorMap &mq, const CUtensorMap &mk8,
-                     const CUtensorMap &mv8, const CUtensorMap &mo, cudaStream_t s)
+template <int DP, bool kTma, bool kSK, int NC = 1>
+cudaError_t launch_t(const Params &p, const AttnMaps<NC> &tm, cudaStream_t s)
 {
     const uint32_t smem = Smem<DP>::TOTAL;
-    auto kern = rel_attn_bf16_kernel<DP, kTma, kSK>;
+    auto kern = rel_attn_bf16_kernel<DP, kTma, kSK, NC>;
     // the shared-memory opt-in, once per device for this variant
     static std::atomic<uint64_t> opted{0};
     int dev = 0;
@@ -1699,7 +1736,7 @@ cudaError_t launch_t(const Params &p, const CUtensorMap &mk, const CUtensorMap &
     }
     // persistent: one CTA per SM, each walks its share of the work items
     const int grid = p.items < device_sm_count() ? p.items : device_sm_count();
-    kern<<<(unsigned)grid, NT, smem, s>>>(mk, mv, mr, mq, mk8, mv8, mo, p);
+    kern<<<(unsigned)grid, NT, smem, s>>>(tm, p);
     return cudaGetLastError();
 }
 
@@ -1853,6 +1890,7 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     const int DP = dpad(a.D);
     if (DP > 64) return cudaErrorNotSupported;
     Params p;
+    memset(&p, 0, sizeof(p));
     p.q = (const __nv_bfloat16 *)a.q;
     p.k = (const __nv_bfloat16 *)a.k;
     p.v = (const __nv_bfloat16 *)a.v;
@@ -1887,15 +1925,12 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     p.roll_src = nullptr;
     p.roll_dst = nullptr;
     p.roll_n16 = 0;
-    CUtensorMap mk, mv, mr, mq, mk8, mv8, mo;
-    memset(&mo, 0, sizeof(mo));
+    p.ncell = 1;
+    AttnMaps<1> tm;
+    memset(&tm, 0, sizeof(tm));
+    CUtensorMap &mk = tm.k[0], &mv = tm.v[0], &mr = tm.r[0], &mq = tm.q[0], &mo = tm.o[0], &mk8 = tm.k8,
+                &mv8 = tm.v8;
     p.ost = 0;
-    memset(&mk, 0, sizeof(mk));
-    memset(&mv, 0, sizeof(mv));
-    memset(&mr, 0, sizeof(mr));
-    memset(&mq, 0, sizeof(mq));
-    memset(&mk8, 0, sizeof(mk8));
-    memset(&mv8, 0, sizeof(mv8));
     // TMA for D = 64 (128-byte rows); the biases then come by bulk copy,
     // which wants them 16-byte aligned.  A K/V ring whose start or length is
     // not a multiple of 8 rows is read by the thread loader (the 8-row boxes
@@ -1926,16 +1961,14 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     }
     cudaError_t e;
     switch (DP) {
-    case 16: e = tma ? launch_t<16, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<16, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
-    case 32: e = tma ? launch_t<32, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<32, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
-    case 48: e = tma ? launch_t<48, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s) : launch_t<48, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s); break;
+    case 16: e = tma ? launch_t<16, true, false>(p, tm, s) : launch_t<16, false, false>(p, tm, s); break;
+    case 32: e = tma ? launch_t<32, true, false>(p, tm, s) : launch_t<32, false, false>(p, tm, s); break;
+    case 48: e = tma ? launch_t<48, true, false>(p, tm, s) : launch_t<48, false, false>(p, tm, s); break;
     default:
         if (p.streamk)
-            e = tma ? launch_t<64, true, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s)
-                    : launch_t<64, false, true>(p, mk, mv, mr, mq, mk8, mv8, mo, s);
+            e = tma ? launch_t<64, true, true>(p, tm, s) : launch_t<64, false, true>(p, tm, s);
         else
-            e = tma ? launch_t<64, true, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s)
-                    : launch_t<64, false, false>(p, mk, mv, mr, mq, mk8, mv8, mo, s);
+            e = tma ? launch_t<64, true, false>(p, tm, s) : launch_t<64, false, false>(p, tm, s);
         break;
     }
     if (e == cudaSuccess && splits > 1) {
@@ -1949,6 +1982,91 @@ cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaS
     if (e == cudaSuccess && a.roll_bytes && p.roll_n16 == 0)
         e = launch_rollover(a.roll_dst, a.roll_src, a.roll_bytes, 2, s);
     return e;
+}
+
+cudaError_t launch_attn_bf16_cells(int n, const AttnArgs *a, cudaStream_t s)
+{
+    if (n < 2) return cudaErrorNotSupported;
+    const AttnArgs &a0 = a[0];
+    const int sms = device_sm_count();
+    const int nqt = (a0.L + BM - 1) / BM;
+    const long per_call = (long)a0.B * a0.H * nqt;
+    auto al16 = [](const void *x) { return ((uintptr_t)x & 15) == 0; };
+    // every call: the shape of the first, unsplit, TMA operands and output
+    if (a0.D != 64 || a0.kv_start != 0 || a0.L < 1 || a0.B < 1 || a0.H < 1 || bf16_num_splits(a0, sms) != 1 ||
+        per_call * ATTN_CELLS > INT32_MAX)
+        return cudaErrorNotSupported;
+    bool roll_in = a0.roll_bytes > 0 && roll_fuses(a0, per_call, 1);
+    for (int c = 0; c < n; ++c) {
+        const AttnArgs &x = a[c];
+        if (x.B != a0.B || x.H != a0.H || x.D != a0.D || x.L != a0.L || x.M != a0.M || x.kv_start != 0 ||
+            x.scale_d != a0.scale_d || x.lse || x.roll_bytes != a0.roll_bytes || !al16(x.u) || !al16(x.w) ||
+            !al16(x.out))
+            return cudaErrorNotSupported;
+        if (x.roll_bytes && (!al16(x.roll_src) || !al16(x.roll_dst))) roll_in = false;
+    }
+    const int T = a0.M + a0.L;
+    const long bhn = (long)a0.B * a0.H, rs = bhn * a0.D;
+    for (int c0 = 0; c0 < n; c0 += ATTN_CELLS) {
+        const int nc = n - c0 < ATTN_CELLS ? n - c0 : ATTN_CELLS;
+        cudaError_t e;
+        if (nc == 1) {
+            AttnArgs x = a[c0];
+            e = launch_attn_bf16(x, 1, nullptr, s);    // its rollover as that call decides
+            if (e != cudaSuccess) return e;
+            continue;
+        }
+        Params p;
+        memset(&p, 0, sizeof(p));
+        p.q = (const __nv_bfloat16 *)a[c0].q;
+        p.k = (const __nv_bfloat16 *)a[c0].k;
+        p.v = (const __nv_bfloat16 *)a[c0].v;
+        p.r = (const __nv_bfloat16 *)a[c0].r;
+        p.u = a[c0].u;
+        p.w = a[c0].w;
+        p.out = (__nv_bfloat16 *)a[c0].out;
+        p.B = a0.B;
+        p.H = a0.H;
+        p.D = a0.D;
+        p.L = a0.L;
+        p.M = a0.M;
+        p.T = T;
+        p.nqt = nqt;
+        p.splits = 1;
+        p.sl2 = LOG2E / sqrtf((float)(a0.scale_d ? a0.scale_d : a0.D));
+        p.sk_nt = (T + BN - 1) / BN;
+        p.ncell = nc;
+        p.items = (int)(per_call * nc);
+        p.ost = 1;
+        AttnMaps<ATTN_CELLS> tm;
+        memset(&tm, 0, sizeof(tm));
+        for (int c = 0; c < nc; ++c) {
+            const AttnArgs &x = a[c0 + c];
+            if (!make_map(&tm.k[c], x.k, T, rs, bhn, BN) || !make_map(&tm.v[c], x.v, T, rs, bhn, BN) ||
+                !make_map(&tm.r[c], x.r, T, (long)a0.H * a0.D, a0.H, BN) ||
+                !make_map(&tm.q[c], x.q, a0.L, rs, bhn, BM) || !make_map(&tm.o[c], x.out, a0.L, rs, bhn, BM))
+                return cudaErrorInvalidValue;
+            p.cell_u[c] = x.u;
+            p.cell_w[c] = x.w;
+            if (roll_in) {
+                p.cell_roll_src[c] = (const uint4 *)x.roll_src;
+                p.cell_roll_dst[c] = (uint4 *)x.roll_dst;
+            }
+        }
+        if (roll_in) {
+            p.roll_src = p.cell_roll_src[0];
+            p.roll_dst = p.cell_roll_dst[0];
+            p.roll_n16 = (long)(a0.roll_bytes / 16);
+        }
+        e = launch_t<64, true, false, ATTN_CELLS>(p, tm, s);
+        if (e != cudaSuccess) return e;
+        // rollovers the launch did not take: their own copies
+        for (int c = 0; a0.roll_bytes && !roll_in && c < nc; ++c) {
+            e = launch_rollover(a[c0 + c].roll_dst, a[c0 + c].roll_src, a0.roll_bytes, 2, s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *lse, void *p_out, void *da_out,
@@ -1971,6 +2089,7 @@ cudaError_t launch_bwd_scores(const AttnArgs &a, const void *dout, const float *
     p.T = a.M + a.L;
     p.nqt = (a.L + BM - 1) / BM;
     p.splits = 1;
+    p.ncell = 1;
     p.items = (int)((long)a.B * a.H * p.nqt);
     p.sl2 = LOG2E / sqrtf((float)a.D);
     p.lse = const_cast<float *>(lse);

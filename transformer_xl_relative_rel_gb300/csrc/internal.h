@@ -32,6 +32,14 @@ cudaError_t launch_attn_f32(const AttnArgs &a, cudaStream_t s);
 int bf16_num_splits(const AttnArgs &a, int num_sms);
 size_t bf16_scratch_bytes(const AttnArgs &a, int splits);
 cudaError_t launch_attn_bf16(const AttnArgs &a, int splits, void *scratch, cudaStream_t s);
+// Calls of one shape (bf16, D = 64, K and V not a ring, no row log-sum-exp)
+// that each run unsplit with their output by TMA store: up to ATTN_CELLS of
+// them per launch, items of all calls in one persistent schedule, each call's
+// rollover (if any) in the same launch where it fuses, else after it.
+// Returns cudaErrorNotSupported, having launched nothing, for calls that do
+// not meet that (the caller then runs them one by one).
+constexpr int ATTN_CELLS = 8;
+cudaError_t launch_attn_bf16_cells(int n, const AttnArgs *a, cudaStream_t s);
 // The score side of the backward (bf16, D = 64, 16-byte aligned operands):
 // P and dA as bf16 [B*H][L][TP] and dA in the table frame as bf16
 // [H][L][B][TP] (TP = M+L rounded up to 128), from the forward's output
