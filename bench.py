@@ -151,15 +151,16 @@ def kernel_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source and this workload."""
+    """DRAM bytes of one layer call of the attention kernel (a launch's bytes
+    over the calls it carries) from the committed ncu summary, if it was
+    taken on the current kernel source and this workload."""
     try:
         text = open(PROFILE_TRAFFIC).read()
     except OSError:
         return None
     m_src = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]{16})", text)
     m_wl = re.search(r"workload:\s*(\S+)", text)
-    m_b = re.search(r"dram bytes per launch \(read\+write\):\s*([0-9.eE+]+)", text)
+    m_b = re.search(r"dram bytes per (?:launch|call) \(read\+write\):\s*([0-9.eE+]+)", text)
     if not (m_src and m_wl and m_b):
         return None
     if m_src.group(1) != kernel_hash() or m_wl.group(1) != workload:
