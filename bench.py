@@ -445,9 +445,8 @@ class GraphMarks:
 
 def qkv_launches(w: Workload, dp: int, ring: bool) -> int:
     """Launches of a layer's q, k, v projections under txl_project_qkv's
-    rule (include/txl.h): bf16 TMA-addressable operands put k and v in one
-    launch, q joins it when its first row (mem_len x batch) starts a
-    128-row block; the ring variant projects q on its own."""
+    rule (include/txl.h): bf16 TMA-addressable operands put the three in one
+    launch; the ring variant projects q on its own."""
     s = w.shape
     n_out = s.heads * dp
     bn = 256 if n_out >= 256 else (n_out + 15) // 16 * 16
@@ -455,9 +454,7 @@ def qkv_launches(w: Workload, dp: int, ring: bool) -> int:
              and bn % dp == 0)
     if not fused:
         return 3
-    if ring:
-        return 2
-    return 1 if (s.mem_len * s.batch) % 128 == 0 else 2
+    return 2 if ring else 1
 
 
 def qkv_cells_launches(w: Workload, dp: int, cells: int) -> int:

@@ -255,10 +255,11 @@ txl_status txl_project_heads(const void *x, const void *w, void *out, int rows, 
  * each as txl_project_heads writes it ([..][heads][d_pad], padding zero).
  * w_q and q are both given or both NULL (then only k and v).  bf16 with
  * d_in a multiple of 8, every pointer 16-byte aligned, heads*d_pad*2 a
- * multiple of 16 and d_pad dividing 256: k and v come from one launch of
- * the projection GEMM that reads x once, and q joins that launch when
- * q_row0 is a multiple of 128 (else it is a launch of its own); other shapes
- * are computed as by three txl_project_heads calls.
+ * multiple of 16 and d_pad dividing 256: the three come from one launch of
+ * the projection GEMM that reads x once for k and v (and for q too when
+ * q_row0 is a multiple of 128; otherwise q's rows are a band of their own in
+ * the same launch); other shapes are computed as by three txl_project_heads
+ * calls.
  * Outputs must not overlap x, the weights or one another; 0 <= q_row0 <=
  * rows.  Results equal the separate txl_project_heads calls bit for bit.
  */

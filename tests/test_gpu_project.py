@@ -68,13 +68,15 @@ def test_project_heads_tensor_core(rows, d_in, heads, d_head, d_pad):
 
 
 # the layer's three projections from one extended context [M+L, B, d_in]:
-# the fused launch (x read once; q's rows start a 128-row block), k and v
-# fused with q on its own (q's first row inside a block), and shapes that
-# take one launch per product (cp.async rows, fp32); every case against the
-# oracle and bit for bit against three project_heads calls
+# the fused launch (x read once; q's rows start a 128-row block), the fused
+# launch with q's rows as a band of their own (q's first row inside a
+# block), and shapes that take one launch per product (cp.async rows, fp32);
+# every case against the oracle and bit for bit against three project_heads
+# calls
 @pytest.mark.parametrize("dtype,T,B,M,d_in,heads,d_head,d_pad", [
     (torch.bfloat16, 384, 2, 256, 512, 8, 64, 64),    # q from row 512: fused q, k, v
-    (torch.bfloat16, 200, 3, 72, 256, 4, 64, 64),     # q from row 216 (inside a block): k, v fused, q alone
+    (torch.bfloat16, 200, 3, 72, 256, 4, 64, 64),     # q from row 216 (inside a block): q's own band
+    (torch.bfloat16, 150, 3, 50, 256, 16, 64, 64),    # q's own band from row 150, four column tiles
     (torch.bfloat16, 97, 3, 32, 512, 8, 64, 64),      # ragged last block (291 rows), q from row 96
     (torch.bfloat16, 160, 2, 64, 1024, 16, 64, 64),   # four column tiles per product
     (torch.bfloat16, 150, 2, 100, 410, 10, 41, 64),   # cp.async rows: three launches
@@ -227,7 +229,7 @@ def test_layer_from_hidden_states():
     (3, 384, 2, 256, 512, 8, True),      # one grouped launch, q fused
     (10, 200, 3, 128, 256, 4, True),     # two launches (8 + 2 cells)
     (4, 160, 2, 64, 1024, 16, False),    # k and v only
-    (3, 200, 3, 72, 256, 4, True),       # q's first row inside a block: each cell as project_qkv runs it
+    (3, 200, 3, 72, 256, 4, True),       # q's first row inside a block: q's own band in each cell
 ])
 def test_project_qkv_cells_equals_per_cell(cells, T, B, M, d_in, heads, with_q):
     """Several layer calls' projections in grouped launches: every output bit

@@ -101,7 +101,10 @@ static_assert(SmemTma::TOTAL <= 232448 && 2 * (SmemCpa::TOTAL + 1024) <= 233472,
 // Up to three products of the same x in one launch (q, k, v of a layer):
 // segment s multiplies x by its own W and writes its own output, over the
 // row blocks from seg_fb[s] on (seg_fb non-decreasing), output row = x row -
-// seg_row0[s].  One segment is the plain y = x W^T.  A launch can also take
+// seg_row0[s].  One segment is the plain y = x W^T.  When q's first row
+// (seg_row0[2]) does not start a row block, q is not a nested segment but
+// a band of its own after the others: qa_blocks 128-row blocks from x row
+// seg_row0[2] on (nseg is then 2).  A launch can also take
 // several such cells of one shape (the layer calls of one step that do not
 // depend on each other), each with its own x, weights and outputs: tile t
 // belongs to cell t / tiles_cell.
@@ -115,6 +118,7 @@ struct GemmParams {
     int tma_out;
     int nseg, row_blocks;
     int seg_fb[GSEG], seg_row0[GSEG];
+    int qa_blocks;                    // row blocks of q's own band (0: none)
     int tiles_cell, ncell;            // tiles of one cell, cells in the launch
 };
 template <int NC>
@@ -150,6 +154,8 @@ __host__ __device__ __forceinline__ GTile gemm_tile(const GemmParams &p, int t)
         }
         t -= cnt;
     }
+    if (t < p.qa_blocks * p.tiles_n)   // q's own band, its blocks from its first row
+        return {p.seg_row0[2] + (t / p.tiles_n) * GM, 2, (t % p.tiles_n) * p.bn, cell};
     return {-1, 0, 0, cell};
 }
 
@@ -212,12 +218,12 @@ project_gemm_kernel(const __grid_constant__ GemmMapsN<NC> maps, const GemmParams
         if (kTmaIn) {
             for (int c = 0; c < NC && c < p.ncell; ++c) {
                 prefetch_tmap(&maps.x[c]);
-                for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.w[c][sg]);
+                for (int sg = 0; sg < (p.qa_blocks ? 3 : p.nseg); ++sg) prefetch_tmap(&maps.w[c][sg]);
             }
         }
         if (p.tma_out)
             for (int c = 0; c < NC && c < p.ncell; ++c)
-                for (int sg = 0; sg < p.nseg; ++sg) prefetch_tmap(&maps.o[c][sg]);
+                for (int sg = 0; sg < (p.qa_blocks ? 3 : p.nseg); ++sg) prefetch_tmap(&maps.o[c][sg]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -523,7 +529,23 @@ void gemm_shape(GemmParams &p, int rows, int d_in, int heads, int d_head, int d_
     p.ksteps = (d_in + GK - 1) / GK;
     p.row_blocks = (rows + GM - 1) / GM;
     p.nseg = 1;
+    p.qa_blocks = 0;
     for (int sg = 0; sg < GSEG; ++sg) p.seg_fb[sg] = p.seg_row0[sg] = 0;
+}
+
+// q in the launch of k and v: a nested segment when its first row starts a
+// row block (the three products then share x's row blocks), else a band of
+// its own after k and v
+void gemm_add_q(GemmParams &p, int q_row0)
+{
+    p.seg_row0[2] = q_row0;
+    if (q_row0 % GM == 0) {
+        p.nseg = 3;
+        p.seg_fb[2] = q_row0 / GM;
+    } else {
+        p.nseg = 2;
+        p.qa_blocks = (p.rows - q_row0 + GM - 1) / GM;
+    }
 }
 
 // tiles of a launch: each band of row blocks times its active segments
@@ -534,6 +556,7 @@ bool gemm_count_tiles(GemmParams &p)
         const int end = b + 1 < p.nseg ? p.seg_fb[b + 1] : p.row_blocks;
         tiles += (long)(end - p.seg_fb[b]) * (b + 1) * p.tiles_n;
     }
+    tiles += (long)p.qa_blocks * p.tiles_n;
     if (tiles > INT32_MAX) return false;
     p.tiles = (int)tiles;
     p.tiles_cell = p.tiles;
@@ -591,10 +614,10 @@ cudaError_t launch_project_gemm(const void *x, const void *w, void *out, int row
 }
 
 // k = x W_k^T and v = x W_v^T over all rows and, when wq is given,
-// q = x[q_row0..] W_q^T.  When every operand is TMA-addressable, k and v
-// come from one launch that reads x once, and q joins it when its first row
-// starts a 128-row block (else q is a launch of its own); otherwise one
-// launch per product.
+// q = x[q_row0..] W_q^T.  When every operand is TMA-addressable, the three
+// come from one launch (q as a nested segment that shares x's row blocks
+// when its first row starts a 128-row block, else as a band of its own);
+// otherwise one launch per product.
 cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq, const void *wk, const void *wv,
                                void *q, void *k, void *v, int q_row0, int heads, int d_head, int d_pad,
                                cudaStream_t s)
@@ -611,14 +634,13 @@ cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq
     cudaError_t e = cudaSuccess;
     bool q_done = false;
     if (fused) {
-        const bool q_in = with_q && al(wq, 16) && al(q, 16) && q_row0 % GM == 0;
+        const bool q_in = with_q && al(wq, 16) && al(q, 16);
         p.x = (const __nv_bfloat16 *)x;
         p.w = (const __nv_bfloat16 *)wk;
         p.out = (__nv_bfloat16 *)k;
         p.tma_out = 1;
-        p.nseg = q_in ? 3 : 2;
-        p.seg_fb[2] = q_in ? q_row0 / GM : 0;
-        p.seg_row0[2] = q_in ? q_row0 : 0;
+        p.nseg = 2;
+        if (q_in) gemm_add_q(p, q_row0);
         if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
         GemmMaps maps;
         memset(&maps, 0, sizeof(maps));
@@ -641,16 +663,15 @@ cudaError_t launch_project_qkv(const void *x, int rows, int d_in, const void *wq
 
 // Several layer calls' q, k, v projections of one shape in one launch
 // (cells c = 0..n-1: k_c = x_c W_k,c^T, v_c = x_c W_v,c^T, q_c = x_c[q_row0..]
-// W_q,c^T), when every operand is TMA-addressable and q's first row starts a
-// 128-row block; otherwise each cell as launch_project_qkv runs it.  Up to
-// GCELLS cells per launch.
+// W_q,c^T), when every operand is TMA-addressable; otherwise each cell as
+// launch_project_qkv runs it.  Up to GCELLS cells per launch.
 cudaError_t launch_project_qkv_cells(int n, const void *const *x, const void *const *wq, const void *const *wk,
                                      const void *const *wv, void *const *q, void *const *k, void *const *v,
                                      int rows, int d_in, int q_row0, int heads, int d_head, int d_pad, cudaStream_t s)
 {
     const bool with_q = wq != nullptr && rows > q_row0;
     const int n_out = heads * d_pad;
-    bool ok = d_in % 8 == 0 && (n_out * 2) % 16 == 0 && d_pad <= 256 && (!with_q || q_row0 % GM == 0);
+    bool ok = d_in % 8 == 0 && (n_out * 2) % 16 == 0 && d_pad <= 256;
     for (int c = 0; ok && c < n; ++c) {
         ok = al(x[c], 16) && al(wk[c], 16) && al(wv[c], 16) && al(k[c], 16) && al(v[c], 16);
         if (with_q) ok = ok && al(wq[c], 16) && al(q[c], 16);
@@ -669,9 +690,8 @@ cudaError_t launch_project_qkv_cells(int n, const void *const *x, const void *co
         return cudaSuccess;
     }
     p.tma_out = 1;
-    p.nseg = with_q ? 3 : 2;
-    p.seg_fb[2] = with_q ? q_row0 / GM : 0;
-    p.seg_row0[2] = with_q ? q_row0 : 0;
+    p.nseg = 2;
+    if (with_q) gemm_add_q(p, q_row0);
     if (!gemm_count_tiles(p)) return cudaErrorNotSupported;
     const int per = p.tiles;
     for (int c0 = 0; c0 < n; c0 += GCELLS) {
